@@ -1,0 +1,193 @@
+/*
+ * qmv_oracle.c -- CPU fp64 oracle for the block-quantised weight x activation
+ * product of single-stream decode.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * CPU-baseline leg of the benchmark may load this code.  The CUDA library never
+ * links, includes or calls it, and it shares no code, header or table with the
+ * CUDA path.
+ *
+ * What it computes (the plain definition, no blocking, fusion or reordering):
+ *
+ *     y[m][n] = sum_k  x[m][k] * w[n][k]             (fp64)
+ *     S[m][n] = sum_k |x[m][k] * w[n][k]|            (fp64, for the tolerance)
+ *
+ * "a CPU double-precision reference of the same quantized weights"
+ *   -- volta-kernel-bakeoff, "Making it fair" (correct before fast).
+ * "Single-stream decode is a stack of GEMVs (one activation row x each weight
+ *  matrix)" -- H100-KERNEL-5X-ROADMAP, "Why the decode gap is bandwidth".
+ *
+ * Weight formats (GGUF; "Q4_0", "group_size 32" -- sm8x-bench, Q4_0 summary
+ * and "Our kernel does what llama.cpp does"; Q8_0 -- H100-KERNEL-5X-ROADMAP,
+ * "The measured baseline"):
+ *   Q4_0 block, 18 bytes, 32 weights:  bytes 0..1 = fp16 scale d (little
+ *     endian), bytes 2..17 = qs[0..15].  Element j<16 is the low nibble of
+ *     qs[j], element j>=16 is the high nibble of qs[j-16]; w = (c - 8) * d.
+ *   Q8_0 block, 34 bytes, 32 weights:  bytes 0..1 = fp16 d, bytes 2..33 =
+ *     int8 codes q[0..31]; w = q * d.
+ *   A row of W holds K/32 consecutive blocks; rows are dense (no padding).
+ *   x is fp16 (IEEE binary16 bit patterns), row-major [M][K].
+ *
+ * Parity pins: see tests/test_oracle.py (hand-computed fixtures under
+ * tests/golden/, closed forms, invariants, exhaustive fp16 decode against
+ * numpy, integer special cases against numpy matmul, planted mutations).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_FMT_Q4_0 0
+#define ORACLE_FMT_Q8_0 1
+
+/* IEEE 754 binary16 -> double, written out from the format's definition:
+ * 1 sign bit, 5 exponent bits (bias 15), 10 mantissa bits; exponent 0 is
+ * zero/subnormal (mantissa * 2^-24), exponent 31 is inf/NaN. */
+double oracle_half_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int expo = (h >> 10) & 0x1f;
+    int mant = h & 0x3ff;
+    double v;
+    if (expo == 0) {
+        v = ldexp((double)mant, -24);
+    } else if (expo == 31) {
+        v = (mant == 0) ? INFINITY : NAN;
+    } else {
+        v = ldexp((double)(1024 + mant), expo - 25);
+    }
+    return sign ? -v : v;
+}
+
+int64_t oracle_block_bytes(int fmt)
+{
+    if (fmt == ORACLE_FMT_Q4_0) return 18;
+    if (fmt == ORACLE_FMT_Q8_0) return 34;
+    return -1;
+}
+
+/* Dequantise one Q4_0 block of 32 weights into w[0..31]. */
+static void dequant_block_q4_0(const uint8_t *blk, double *w)
+{
+    uint16_t dbits = (uint16_t)(blk[0] | (blk[1] << 8));
+    double d = oracle_half_to_double(dbits);
+    const uint8_t *qs = blk + 2;
+    for (int j = 0; j < 16; ++j) {
+        int lo = qs[j] & 0x0f;
+        int hi = qs[j] >> 4;
+        w[j] = (double)(lo - 8) * d;
+        w[j + 16] = (double)(hi - 8) * d;
+    }
+}
+
+/* Dequantise one Q8_0 block of 32 weights into w[0..31]. */
+static void dequant_block_q8_0(const uint8_t *blk, double *w)
+{
+    uint16_t dbits = (uint16_t)(blk[0] | (blk[1] << 8));
+    double d = oracle_half_to_double(dbits);
+    const int8_t *q = (const int8_t *)(blk + 2);
+    for (int j = 0; j < 32; ++j) {
+        w[j] = (double)q[j] * d;
+    }
+}
+
+/* Dequantise row n of W (K weights) into w[0..K-1]. */
+int oracle_dequant_row(int fmt, const uint8_t *W, int64_t n, int64_t K, double *w)
+{
+    int64_t bb = oracle_block_bytes(fmt);
+    if (bb < 0 || K % 32 != 0) return -1;
+    int64_t nblk = K / 32;
+    const uint8_t *row = W + n * nblk * bb;
+    for (int64_t b = 0; b < nblk; ++b) {
+        if (fmt == ORACLE_FMT_Q4_0)
+            dequant_block_q4_0(row + b * bb, w + 32 * b);
+        else
+            dequant_block_q8_0(row + b * bb, w + 32 * b);
+    }
+    return 0;
+}
+
+/* y and S for the rows listed in rows[0..nrows-1] (all rows when rows is NULL,
+ * then nrows = N).  Outputs are [M][nrows] row-major. */
+int oracle_qmv_rows(int fmt, const uint8_t *W, const uint16_t *x,
+                    int64_t N, int64_t K, int64_t M,
+                    const int64_t *rows, int64_t nrows,
+                    double *y, double *S, int nthreads)
+{
+    if (oracle_block_bytes(fmt) < 0 || K % 32 != 0 || N < 0 || M < 0) return -1;
+    if (rows == NULL) nrows = N;
+    double *xd = (double *)malloc(sizeof(double) * (size_t)(M * K > 0 ? M * K : 1));
+    if (!xd) return -2;
+    for (int64_t i = 0; i < M * K; ++i) xd[i] = oracle_half_to_double(x[i]);
+    int failed = 0;
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for schedule(dynamic, 4) num_threads(nthreads) reduction(| : failed)
+#endif
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t n = rows ? rows[r] : r;
+        double *w = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+        if (!w || n < 0 || n >= N) { failed = 1; free(w); continue; }
+        oracle_dequant_row(fmt, W, n, K, w);
+        for (int64_t m = 0; m < M; ++m) {
+            double acc = 0.0, sabs = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double p = xd[m * K + k] * w[k];
+                acc += p;
+                sabs += fabs(p);
+            }
+            y[m * nrows + r] = acc;
+            S[m * nrows + r] = sabs;
+        }
+        free(w);
+    }
+    free(xd);
+    (void)nthreads;
+    return failed ? -3 : 0;
+}
+
+/* Full product: y[M][N], S[M][N]. */
+int oracle_qmv(int fmt, const uint8_t *W, const uint16_t *x,
+               int64_t N, int64_t K, int64_t M, double *y, double *S, int nthreads)
+{
+    return oracle_qmv_rows(fmt, W, x, N, K, M, NULL, N, y, S, nthreads);
+}
+
+/* Several experts, one token each, in one call ("moe_*: the MoE case: 8-10
+ * experts, one token each, in one launch" -- volta-kernel-bakeoff, "What's in
+ * the race"; "each expert with its own weights and token, so a wrong expert
+ * index fails too" -- "Making it fair").
+ * Slot s uses expert e = idx[s] of a pool of n_experts experts stored back to
+ * back (expert e starts e * N * (K/32) blocks in), token x[s][0..K-1], and
+ * writes y[s][0..N-1], S[s][0..N-1].  An index outside [0, n_experts) is an
+ * error (returns -4, outputs of that slot untouched). */
+int oracle_moe(int fmt, const uint8_t *W_pool, const int32_t *idx, int64_t n_experts,
+               const uint16_t *x, int64_t N, int64_t K, int64_t n_slots,
+               double *y, double *S, int nthreads)
+{
+    int64_t bb = oracle_block_bytes(fmt);
+    if (bb < 0 || K % 32 != 0) return -1;
+    int64_t expert_bytes = N * (K / 32) * bb;
+    int rc = 0;
+    for (int64_t s = 0; s < n_slots; ++s) {
+        int32_t e = idx[s];
+        if (e < 0 || e >= n_experts) { rc = -4; continue; }
+        int r = oracle_qmv(fmt, W_pool + (int64_t)e * expert_bytes, x + s * K,
+                           N, K, 1, y + s * N, S + s * N, nthreads);
+        if (r != 0) return r;
+    }
+    return rc;
+}
+
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,221 @@
+"""Pins for the CPU oracle (no GPU).
+
+Each pin ties the oracle to something other than itself: hand-computed closed
+forms (tests/golden), an exhaustive comparison of its fp16 decoder with numpy,
+integer special cases that reduce to a plain numpy matmul, exact invariants,
+and the sabotage check of volta-kernel-bakeoff ("Making it fair").
+"""
+import numpy as np
+import pytest
+
+from tests import helpers as H
+from weight_quantized_decode_gb300 import synth
+
+
+# -- fp16 decoding -------------------------------------------------------------
+
+def test_half_decode_exhaustive(orc):
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([orc.half_to_double(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+# -- hand-computed cases -----------------------------------------------------
+
+@pytest.mark.parametrize("case", H.load_cases("oracle_cases.txt"), ids=lambda c: c["name"])
+def test_golden_cases(orc, case):
+    y, S = orc.qmv(H.FMT[case["fmt"]], case["W"], case["xarr"], case["N"], case["K"])
+    for (m, n), v in case["y"].items():
+        assert y[m, n] == v, (case["name"], m, n, y[m, n], v)
+    for (m, n), v in case["S"].items():
+        assert S[m, n] == v, (case["name"], m, n, S[m, n], v)
+
+
+def test_golden_moe(orc):
+    (case,) = H.load_cases("moe_cases.txt")
+    E, idx = case["moe"]
+    y, S = orc.moe(H.FMT[case["fmt"]], case["W"], idx, E, case["xarr"], case["N"], case["K"])
+    for (s, n), v in case["y"].items():
+        assert y[s, n] == v
+
+
+def test_moe_rejects_bad_index(orc):
+    (case,) = H.load_cases("moe_cases.txt")
+    E, _ = case["moe"]
+    with pytest.raises(ValueError):
+        orc.moe(0, case["W"], [0, 3, 1], E, case["xarr"], case["N"], case["K"])
+    with pytest.raises(ValueError):
+        orc.moe(0, case["W"], [0, -1, 1], E, case["xarr"], case["N"], case["K"])
+
+
+# -- integer special cases: the product reduces to an integer matmul ----------
+
+@pytest.mark.parametrize("K", [32, 96, 256])
+def test_q4_0_integer_case_matches_numpy(orc, K):
+    rng = np.random.default_rng(7 + K)
+    N, M = 5, 3
+    codes = rng.integers(0, 16, size=(N, K))
+    d_bits = np.full((N, K // 32), 0x3C00, dtype=np.uint16)          # d = 1
+    W = H.encode_q4_0(codes, d_bits)
+    x = rng.integers(-50, 51, size=(M, K)).astype(np.float16)         # exact small ints
+    y, S = orc.qmv(0, W, x, N, K)
+    Wi = (codes - 8).astype(np.float64)
+    xf = x.astype(np.float64)
+    assert np.array_equal(y, xf @ Wi.T)
+    assert np.array_equal(S, np.abs(xf) @ np.abs(Wi).T)
+
+
+@pytest.mark.parametrize("K", [32, 128])
+def test_q8_0_integer_case_matches_numpy(orc, K):
+    rng = np.random.default_rng(11 + K)
+    N, M = 4, 2
+    codes = rng.integers(-128, 128, size=(N, K))
+    d_bits = np.full((N, K // 32), 0x3C00, dtype=np.uint16)
+    W = H.encode_q8_0(codes, d_bits)
+    x = rng.integers(-50, 51, size=(M, K)).astype(np.float16)
+    y, _ = orc.qmv(1, W, x, N, K)
+    assert np.array_equal(y, x.astype(np.float64) @ codes.astype(np.float64).T)
+
+
+def test_power_of_two_scales_per_block(orc):
+    """d = 2^e per block (exact): y equals the integer matmul with the scale
+    folded into the integer matrix column-block by column-block."""
+    rng = np.random.default_rng(3)
+    N, K, M = 3, 128, 2
+    codes = rng.integers(0, 16, size=(N, K))
+    e = rng.integers(-3, 4, size=(N, K // 32))
+    d_bits = (0x3C00 + (e << 10)).astype(np.uint16)                    # 2^e
+    W = H.encode_q4_0(codes, d_bits)
+    x = rng.integers(-20, 21, size=(M, K)).astype(np.float16)
+    y, _ = orc.qmv(0, W, x, N, K)
+    scale = np.repeat(2.0 ** e, 32, axis=1)
+    assert np.array_equal(y, x.astype(np.float64) @ ((codes - 8) * scale).T)
+
+
+# -- invariants ------------------------------------------------------------------
+
+def _rand(fmt, N, K, M, seed):
+    W = synth.weights(fmt, N, K, seed)
+    x = synth.activations(M, K, seed)
+    return W, x
+
+
+def test_all_code8_gives_zero(orc):
+    W, x = _rand("q4_0", 7, 512, 2, 1)
+    v = W.reshape(7, -1, 18)
+    v[:, :, 2:] = 0x88
+    y, _ = orc.qmv(0, W, x, 7, 512)
+    assert np.all(y == 0.0)
+
+
+def test_doubling_scales_doubles_y(orc):
+    for fmt in ("q4_0", "q8_0"):
+        bb = H.BLOCK_BYTES[fmt]
+        W, x = _rand(fmt, 6, 256, 2, 2)
+        W2 = W.copy().reshape(6, -1, bb)
+        d = W2[:, :, 0:2].copy().view(np.uint16)
+        W2[:, :, 0:2] = (d + 0x0400).view(np.uint8)                      # exponent + 1
+        y, _ = orc.qmv(H.FMT[fmt], W, x, 6, 256)
+        y2, _ = orc.qmv(H.FMT[fmt], W2.reshape(6, -1), x, 6, 256)
+        assert np.array_equal(y2, 2.0 * y)
+
+
+def test_linear_in_x(orc):
+    rng = np.random.default_rng(5)
+    W, _ = _rand("q4_0", 9, 512, 1, 3)
+    x1 = rng.integers(-100, 100, size=(1, 512)).astype(np.float16)
+    x2 = rng.integers(-100, 100, size=(1, 512)).astype(np.float16)
+    y1, _ = orc.qmv(0, W, x1, 9, 512)
+    y2, _ = orc.qmv(0, W, x2, 9, 512)
+    y12, S = orc.qmv(0, W, (x1.astype(np.float32) + x2).astype(np.float16), 9, 512)
+    assert np.max(np.abs(y12 - (y1 + y2)) / (S + 1e-30)) < 1e-12
+
+
+def test_q4_to_q8_reencoding_identical(orc):
+    N, K = 5, 256
+    W4, x = _rand("q4_0", N, K, 2, 4)
+    v = W4.reshape(N, K // 32, 18)
+    lo = (v[:, :, 2:] & 0x0F).astype(np.int16) - 8
+    hi = (v[:, :, 2:] >> 4).astype(np.int16) - 8
+    codes = np.concatenate([lo, hi], axis=2).reshape(N, K)
+    d_bits = v[:, :, 0:2].copy().view(np.uint16).reshape(N, K // 32)
+    W8 = H.encode_q8_0(codes, d_bits)
+    y4, S4 = orc.qmv(0, W4, x, N, K)
+    y8, S8 = orc.qmv(1, W8, x, N, K)
+    assert np.array_equal(y4, y8) and np.array_equal(S4, S8)
+
+
+def test_block_permutation_invariance(orc):
+    N, K, M = 4, 512, 2
+    for fmt in ("q4_0", "q8_0"):
+        bb = H.BLOCK_BYTES[fmt]
+        W, x = _rand(fmt, N, K, M, 6)
+        perm = np.random.default_rng(8).permutation(K // 32)
+        Wp = W.reshape(N, K // 32, bb)[:, perm].reshape(N, -1)
+        xp = x.reshape(M, K // 32, 32)[:, perm].reshape(M, K)
+        y, S = orc.qmv(H.FMT[fmt], W, x, N, K)
+        yp, _ = orc.qmv(H.FMT[fmt], Wp, xp, N, K)
+        assert np.max(np.abs(y - yp) / S) < 1e-13
+
+
+def test_tokens_and_rows_are_independent(orc):
+    N, K, M = 11, 256, 4
+    W, x = _rand("q8_0", N, K, M, 9)
+    y, S = orc.qmv(1, W, x, N, K)
+    for m in range(M):
+        ym, Sm = orc.qmv(1, W, x[m:m + 1], N, K)
+        assert np.array_equal(ym[0], y[m]) and np.array_equal(Sm[0], S[m])
+    rows = [10, 0, 3, 3]
+    yr, Sr = orc.qmv_rows(1, W, x, N, K, rows)
+    assert np.array_equal(yr, y[:, rows]) and np.array_equal(Sr, S[:, rows])
+
+
+def test_moe_identity_routing_equals_separate_gemvs(orc):
+    E, N, K = 4, 6, 256
+    pool = synth.q4_0_weights(E * N, K, 12)
+    x = synth.activations(E, K, 12)
+    y, _ = orc.moe(0, pool, np.arange(E), E, x, N, K)
+    for e in range(E):
+        ye, _ = orc.qmv(0, pool[e * N:(e + 1) * N], x[e:e + 1], N, K)
+        assert np.array_equal(ye[0], y[e])
+
+
+def test_empty_shapes(orc):
+    y, S = orc.qmv(0, np.zeros(0, np.uint8), np.zeros((2, 0), np.float16), 3, 0)
+    assert y.shape == (2, 3) and np.all(y == 0) and np.all(S == 0)
+    y, S = orc.qmv(0, np.zeros(0, np.uint8), np.zeros((1, 64), np.float16), 0, 64)
+    assert y.shape == (1, 0)
+
+
+# -- sabotage: corrupting the packed bytes must fail every check ----------------
+
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
+def test_sabotage_fails_the_check(orc, fmt):
+    """A check is the max error over a product's outputs.  Sabotage moves each
+    weight by +-8d (Q4_0) or more (Q8_0): the expected normalised error is
+    ~2.5/sqrt(K) = 0.055 at K=2048, so the check fails by a wide margin and
+    almost every single output fails on its own too."""
+    N, K, M = 64, 2048, 2
+    W, x = _rand(fmt, N, K, M, 13)
+    y, S = orc.qmv(H.FMT[fmt], W, x, N, K)
+    ys, _ = orc.qmv(H.FMT[fmt], H.sabotage(W, fmt), x, N, K)
+    err = np.abs(ys - y) / (S + 1e-6)
+    assert err.max() > 20 * H.TOL
+    assert (err > H.TOL).mean() > 0.9
+
+
+def test_sabotage_fails_golden(orc):
+    for case in H.load_cases("oracle_cases.txt"):
+        y, _ = orc.qmv(H.FMT[case["fmt"]], H.sabotage(case["W"], case["fmt"]),
+                       case["xarr"], case["N"], case["K"])
+        assert any(y[m, n] != v for (m, n), v in case["y"].items()), case["name"]
+
+
+def test_tolerance_helper():
+    assert H.normalised_error([1.0], [1.0], [1.0]) == 0.0
+    assert H.normalised_error([1.003], [1.0], [1.0]) > H.TOL
+    assert H.normalised_error([np.nan], [1.0], [1.0]) == np.inf
