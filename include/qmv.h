@@ -1,0 +1,162 @@
+/*
+ * qmv.h -- C ABI of the block-quantised weight x activation product used by
+ * single-stream LLM decode, for one NVIDIA GB300 (sm_103a).
+ *
+ * The operation, for every call below (the "stack of GEMVs, one activation row
+ * x each weight matrix" of H100-KERNEL-5X-ROADMAP, "Why the decode gap is
+ * bandwidth, not arithmetic"):
+ *
+ *     y[m][n] = sum_k x[m][k] * w[n][k],   0 <= m < M, 0 <= n < N, 0 <= k < K
+ *
+ * where w is the dequantised weight matrix W[N x K].
+ *
+ * Weight layout (GGUF; "Q4_0", "group_size 32" -- sm8x-bench, Q4_0 summary and
+ * "Our kernel does what llama.cpp does"; Q8_0 -- H100-KERNEL-5X-ROADMAP, "The
+ * measured baseline"):
+ *   - W is row-major: row n is K/32 consecutive blocks, rows are dense
+ *     (row stride = (K/32) * block bytes, no padding).
+ *   - Q4_0 block = 18 bytes: fp16 scale d (little endian) then 16 bytes qs;
+ *     element j < 16 is the low nibble of qs[j], element j >= 16 the high
+ *     nibble of qs[j-16]; w = (c - 8) * d.
+ *   - Q8_0 block = 34 bytes: fp16 scale d then 32 int8 codes q; w = q * d.
+ * Activations x: fp16, row-major [M][K].  Output y: fp32, row-major [M][N],
+ * overwritten (never accumulated into).  Accumulation is fp32.
+ *
+ * Accuracy contract: per output, |y - y_exact| <= 2e-3 * (sum_k |x w| + 1e-6),
+ * with y_exact the fp64 dequantise-then-dot (volta-kernel-bakeoff, "Making it
+ * fair": CPU double-precision reference; "A few tokens at once": checked like
+ * cuBLAS fp16, 2e-3, large and tiny activations planted).  Activations must be
+ * finite fp16.
+ *
+ * Conventions common to every entry point:
+ *   - All array pointers are DEVICE pointers on the current CUDA device, owned
+ *     by the caller; the library never allocates, frees or retains them.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous: they enqueue work on `stream` and return; the host never
+ *     blocks (except qmv_device_status, which synchronises `stream`).
+ *   - Argument errors are reported before anything is enqueued.  Errors found
+ *     on the device (an expert index out of range) are recorded in a device
+ *     status word read by qmv_device_status(); the kernel never traps.
+ *   - N == 0 or M == 0: nothing to do, QMV_OK, nothing enqueued.
+ *     K == 0: y is filled with zeros (an empty sum).
+ *   - The library is thread-safe for concurrent calls on different streams.
+ *   - Weights are read-only inputs.  By default the decode kernels use
+ *     programmatic dependent launch: a call may begin streaming W while the
+ *     previous kernel on `stream` is still finishing, and reads x / writes y
+ *     only after that kernel has completed.  If the kernel that runs right
+ *     before a call on the same stream WRITES W, call qmv_set_pdl(0) first.
+ */
+#ifndef QMV_H
+#define QMV_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QMV_API __attribute__((visibility("default")))
+#else
+#define QMV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ABI-compatible with cudaStream_t (struct CUstream_st *). */
+typedef struct CUstream_st *qmv_stream_t;
+
+typedef enum {
+    QMV_OK = 0,
+    QMV_ERR_NULL = 1,      /* a required pointer is NULL                        */
+    QMV_ERR_ALIGN = 2,     /* W not 16-byte aligned, x not 2-byte, y not 4-byte */
+    QMV_ERR_SHAPE = 3,     /* N, K, M or a count out of range, K % 32 != 0      */
+    QMV_ERR_LAUNCH = 4,    /* the CUDA launch failed (cudaGetLastError)         */
+    QMV_ERR_DEVICE = 5,    /* a device-side error was recorded                  */
+    QMV_ERR_CUDA = 6       /* another CUDA runtime call failed                  */
+} qmv_status;
+
+/* Device status word bits (qmv_device_status). */
+#define QMV_DEV_BAD_EXPERT  0x1   /* an expert index was outside [0, n_experts) */
+#define QMV_DEV_TIMEOUT     0x2   /* a bounded wait in a kernel gave up          */
+
+/*
+ * Q4_0 decode GEMV.  "fused_q4 ...: one warp per output row, unpacks in
+ * registers, fp32 sums; v2 = fp16 bit trick (0x6400 | n is the half 1024 + n)"
+ * (volta-kernel-bakeoff, "What's in the race"); "multiple output rows per warp
+ * for memory-level parallelism + a per-shape launch config" (sm8x-bench,
+ * summary).
+ *   W : Q4_0 bytes [N][K/32*18], 16-byte aligned.
+ *   x : fp16 [M][K], 2-byte aligned.        y : fp32 [M][N], 4-byte aligned.
+ *   N >= 0, K >= 0 with K % 32 == 0, 0 <= M <= 8.
+ * K % 256 == 0 (16-byte aligned rows) takes the streaming kernel; other K take
+ * a slower generic kernel with the same results contract.
+ */
+QMV_API qmv_status qmv_q4_0(const void *W, const void *x, float *y,
+                    int64_t N, int64_t K, int64_t M, qmv_stream_t stream);
+
+/*
+ * Q8_0 decode GEMV, same contract as qmv_q4_0 with 34-byte Q8_0 blocks
+ * ("fused_q8: ours, int8 weights" -- volta-kernel-bakeoff, "What's in the
+ * race"; k_q8_gemm -- H100-KERNEL-5X-ROADMAP, "Lever 1").
+ *   W : Q8_0 bytes [N][K/32*34], 16-byte aligned.  0 <= M <= 8.
+ */
+QMV_API qmv_status qmv_q8_0(const void *W, const void *x, float *y,
+                    int64_t N, int64_t K, int64_t M, qmv_stream_t stream);
+
+/*
+ * Several experts, one token each, in ONE launch ("moe_*: the MoE case: 8-10
+ * experts, one token each, in one launch" -- volta-kernel-bakeoff, "What's in
+ * the race"; "each expert with its own weights and token, so a wrong expert
+ * index fails too" -- "Making it fair").
+ *   W_pool     : n_experts Q4_0 experts of N x K each, back to back
+ *                (expert e starts at byte e * N * (K/32) * 18), 16-byte aligned.
+ *   expert_idx : DEVICE int32 [M]; slot s uses expert expert_idx[s].
+ *                Duplicates are allowed.
+ *   x          : fp16 [M][K] (row s = token of slot s).
+ *   y          : fp32 [M][N] (row s = output of slot s).
+ *   1 <= n_experts, 0 <= M <= 64.
+ * An index outside [0, n_experts) sets QMV_DEV_BAD_EXPERT in the device status
+ * word and fills that slot's row of y with NaN; other slots are unaffected.
+ * Row s of y is bit-identical to qmv_q4_0 on expert expert_idx[s] with token
+ * x[s] (same inner loop and reduction order).
+ */
+QMV_API qmv_status qmv_moe(const void *W_pool, const int32_t *expert_idx, int64_t n_experts,
+                   const void *x, float *y, int64_t N, int64_t K, int64_t M,
+                   qmv_stream_t stream);
+
+/*
+ * Q4_0 prefill GEMM for many tokens (M >= 1, intended for M >= 64): "tensor
+ * cores for prompts: unpack a tile to shared memory" (tc_q4 --
+ * volta-kernel-bakeoff, "What's in the race"; "unpack quantized weights inside
+ * a tensor-core multiply" -- "What we'd do next", item 3).  On sm_103a: packed
+ * W tiles staged by bulk copies, dequantised to 16-bit in shared memory, fed to
+ * tcgen05.mma with fp32 accumulators in tensor memory.
+ *   W : Q4_0 bytes [N][K/32*18], 16-byte aligned; requires K % 256 == 0 and
+ *       N % 128 == 0 for the tensor-core kernel (other shapes take the
+ *       generic kernel).
+ *   x : fp16 [M][K], 16-byte aligned.  y : fp32 [M][N].  M >= 0.
+ */
+QMV_API qmv_status qmm_q4_0_prefill(const void *W, const void *x, float *y,
+                            int64_t N, int64_t K, int64_t M, qmv_stream_t stream);
+
+/*
+ * Reads and clears the device status word (QMV_DEV_* bits) of the current
+ * device.  Synchronises `stream` first.  *out receives the bits.
+ * Returns QMV_ERR_NULL for out == NULL, QMV_ERR_CUDA on a runtime error.
+ */
+QMV_API qmv_status qmv_device_status(qmv_stream_t stream, int32_t *out);
+
+/* Programmatic dependent launch for the decode kernels: 1 = on (default),
+ * 0 = off (plain stream order).  Process-wide; affects later calls. */
+QMV_API void qmv_set_pdl(int enable);
+
+/* Static description of a status code. */
+QMV_API const char *qmv_status_str(qmv_status s);
+
+/* Library version, e.g. "qmv 0.1.0 sm_103a". */
+QMV_API const char *qmv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMV_H */

@@ -1,0 +1,87 @@
+"""The C-ABI library loads on a machine without a GPU, exports every symbol
+that include/*.h declares, and rejects bad arguments on the host before any
+CUDA call (no compute calls are made here)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import weight_quantized_decode_gb300 as q
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        txt = open(h).read()
+        names += re.findall(r"^QMV_API\s+[\w\s\*]+?\b(\w+)\s*\(", txt, flags=re.M)
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(q.LIB_PATH):
+        from weight_quantized_decode_gb300 import build
+        build.build()
+    return q.lib()
+
+
+def test_header_declares_the_boundary():
+    names = set(_declared())
+    for n in ("qmv_q4_0", "qmv_q8_0", "qmv_moe", "qmm_q4_0_prefill", "qmv_device_status"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(q.LIB_PATH)
+    missing = [n for n in _declared() if not hasattr(raw, n)]
+    assert not missing, missing
+
+
+def test_version_and_status_strings(lib):
+    assert "sm_103a" in q.qmv_version()
+    assert q.qmv_status_str(0) == "ok"
+    assert q.qmv_status_str(3) == "shape out of range"
+
+
+FAKE = 1 << 20      # a 16-byte-aligned non-null address; never dereferenced here
+
+
+@pytest.mark.parametrize("fn", ["qmv_q4_0", "qmv_q8_0", "qmm_q4_0_prefill"])
+def test_host_validation(lib, fn):
+    f = getattr(lib, fn)
+    assert f(None, FAKE, FAKE, 8, 256, 1, None) == 1          # NULL W
+    assert f(FAKE, None, FAKE, 8, 256, 1, None) == 1          # NULL x
+    assert f(FAKE, FAKE, None, 8, 256, 1, None) == 1          # NULL y
+    assert f(FAKE + 8, FAKE, FAKE, 8, 256, 1, None) == 2      # W not 16-byte aligned
+    assert f(FAKE, FAKE + 1, FAKE, 8, 256, 1, None) == 2      # x not 2-byte aligned
+    assert f(FAKE, FAKE, FAKE + 2, 8, 256, 1, None) == 2      # y not 4-byte aligned
+    assert f(FAKE, FAKE, FAKE, 8, 250, 1, None) == 3          # K % 32 != 0
+    assert f(FAKE, FAKE, FAKE, -1, 256, 1, None) == 3
+    assert f(FAKE, FAKE, FAKE, 8, -32, 1, None) == 3
+    assert f(FAKE, FAKE, FAKE, 8, 256, -1, None) == 3
+    assert f(None, None, None, 0, 256, 1, None) == 0          # empty: nothing to do
+    assert f(None, None, None, 8, 256, 0, None) == 0
+    if fn != "qmm_q4_0_prefill":
+        assert f(FAKE, FAKE, FAKE, 8, 256, 9, None) == 3      # decode takes M <= 8
+
+
+def test_host_validation_moe(lib):
+    f = lib.qmv_moe
+    assert f(FAKE, None, 4, FAKE, FAKE, 8, 256, 2, None) == 1     # NULL index array
+    assert f(FAKE, FAKE, 0, FAKE, FAKE, 8, 256, 2, None) == 3     # no experts
+    assert f(FAKE, FAKE + 2, 4, FAKE, FAKE, 8, 256, 2, None) == 2  # index array misaligned
+    assert f(FAKE, FAKE, 4, FAKE, FAKE, 8, 256, 65, None) == 3    # too many slots
+    assert f(FAKE, FAKE, 4, FAKE, FAKE, 8, 200, 2, None) == 3     # K % 32
+    assert f(None, None, 4, None, None, 8, 256, 0, None) == 0
+
+
+def test_no_cpu_path():
+    torch = pytest.importorskip("torch")
+    W = torch.zeros((4, 144), dtype=torch.uint8)
+    x = torch.zeros((1, 256), dtype=torch.float16)
+    with pytest.raises(TypeError):
+        q.qmv_q4_0(W, x)

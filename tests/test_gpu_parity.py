@@ -1,0 +1,272 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU fp64 oracle.
+
+Bar: max |y - y_ref| / (S + 1e-6) <= 2e-3 per output, S = sum_k |x w|
+(volta-kernel-bakeoff, "Making it fair" and "A few tokens at once").  Expert
+routing is checked bit for bit.  Inputs are seeded synthetic GGUF bytes shaped
+like the pages' workloads (weight_quantized_decode_gb300.synth).
+"""
+import numpy as np
+import pytest
+
+from tests import helpers as H
+from weight_quantized_decode_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import weight_quantized_decode_gb300 as q
+    q.lib()
+    yield q
+    torch.cuda.synchronize()
+
+
+@pytest.fixture(autouse=True)
+def clean_status(cuda_lib):
+    cuda_lib.qmv_device_status()
+    yield
+    # No test may leave a device-side error behind unless it expects one.
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def gpu_call(fmt, W, x):
+    import weight_quantized_decode_gb300 as q
+    fn = q.qmv_q4_0 if fmt == "q4_0" else q.qmv_q8_0
+    y = fn(dev(W), dev(x))
+    torch.cuda.synchronize()
+    return y.cpu().numpy().astype(np.float64)
+
+
+def check(fmt, W, x, N, K, orc, rows=None):
+    y = gpu_call(fmt, W, x)
+    if rows is None:
+        y_ref, S = orc.qmv(H.FMT[fmt], W, x, N, K, nthreads=8)
+        err = H.normalised_error(y, y_ref, S)
+    else:
+        y_ref, S = orc.qmv_rows(H.FMT[fmt], W, x, N, K, rows, nthreads=8)
+        err = H.normalised_error(y[:, rows], y_ref, S)
+    assert err <= H.TOL, (fmt, N, K, x.shape[0], err)
+    return y
+
+
+# -- decode GEMV: tiles, ragged tails, token counts -----------------------------------
+
+SHAPES = [(1, 256), (7, 512), (33, 768), (1000, 2048), (333, 4096), (4133, 1024), (64, 14336), (130, 2560),
+          (77, 6144)]
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("N,K", SHAPES)
+def test_decode_m1(orc, fmt, N, K):
+    W = synth.weights(fmt, N, K, seed=N * 7 + K)
+    x = synth.activations(1, K, seed=N + K)
+    check(fmt, W, x, N, K, orc)
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("M", [2, 3, 4, 5, 6, 7, 8])
+def test_decode_tokens(orc, fmt, M):
+    N, K = 515, 2560
+    W = synth.weights(fmt, N, K, seed=M)
+    x = synth.activations(M, K, seed=100 + M)
+    check(fmt, W, x, N, K, orc)
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("plant", ["large", "tiny"])
+@pytest.mark.parametrize("M", [1, 8])
+def test_planted_activations(orc, fmt, plant, M):
+    N, K = 300, 4096
+    W = synth.weights(fmt, N, K, seed=5)
+    x = synth.activations(M, K, seed=9, plant=plant)
+    y = check(fmt, W, x, N, K, orc)
+    assert np.all(np.isfinite(y))
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("K", [32, 96, 640, 1056])
+def test_generic_kernel_k_not_multiple_of_256(orc, fmt, K):
+    N, M = 45, 3
+    W = synth.weights(fmt, N, K, seed=K)
+    x = synth.activations(M, K, seed=K + 1)
+    check(fmt, W, x, N, K, orc)
+
+
+def test_all_code8_gives_exact_zero():
+    N, K = 257, 4096
+    W = synth.q4_0_weights(N, K, 3)
+    W.reshape(N, -1, 18)[:, :, 2:] = 0x88
+    x = synth.activations(4, K, 3)
+    assert np.all(gpu_call("q4_0", W, x) == 0.0)
+
+
+def test_empty_and_degenerate(cuda_lib):
+    q = cuda_lib
+    x = torch.zeros((2, 0), dtype=torch.float16, device="cuda")
+    W = torch.zeros((5, 0), dtype=torch.uint8, device="cuda")
+    y = torch.full((2, 5), 7.0, device="cuda")
+    q.qmv_q4_0(W, x, y)                      # K == 0: an empty sum
+    torch.cuda.synchronize()
+    assert torch.all(y == 0)
+    xN = torch.zeros((1, 256), dtype=torch.float16, device="cuda")
+    y0 = q.qmv_q4_0(torch.zeros((0, 144), dtype=torch.uint8, device="cuda"), xN)   # N == 0
+    assert y0.shape == (1, 0)
+
+
+def test_deterministic_and_pdl_independent(cuda_lib):
+    q = cuda_lib
+    N, K = 2048, 4096
+    W = dev(synth.q4_0_weights(N, K, 21))
+    x = dev(synth.activations(3, K, 22))
+    a = q.qmv_q4_0(W, x).clone()
+    b = q.qmv_q4_0(W, x).clone()
+    q.qmv_set_pdl(False)
+    try:
+        c = q.qmv_q4_0(W, x).clone()
+    finally:
+        q.qmv_set_pdl(True)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b) and torch.equal(a, c)
+
+
+def test_back_to_back_calls_keep_dependencies(cuda_lib, orc):
+    """With programmatic dependent launch a call may start streaming W early;
+    its x must still be the value written by the kernel before it."""
+    q = cuda_lib
+    N, K = 4096, 4096
+    W1 = synth.q4_0_weights(K, K, 31)
+    W2 = synth.q4_0_weights(N, K, 32)
+    x0 = synth.activations(1, K, 33)
+    Wd1, Wd2, xd = dev(W1), dev(W2), dev(x0)
+    h = torch.empty((1, K), dtype=torch.float32, device="cuda")
+    q.qmv_q4_0(Wd1, xd, h)                          # h = x0 @ W1^T  (K outputs)
+    hx = h.to(torch.float16)                          # a torch kernel between the two calls
+    y = q.qmv_q4_0(Wd2, hx)                          # consumes h
+    torch.cuda.synchronize()
+    y_ref, S = orc.qmv(0, W2, hx.cpu().numpy(), N, K, nthreads=8)
+    assert H.normalised_error(y.cpu().numpy(), y_ref, S) <= H.TOL
+
+
+# -- full-size configurations (sampled outputs) ----------------------------------------
+
+def _sample_rows(N, k=96, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = set(rng.choice(N, size=min(k, N), replace=False).tolist())
+    rows |= {0, N - 1, N // 2}
+    return sorted(rows)
+
+
+FULL_Q4 = [(6144, 2048), (4096, 4096), (6144, 4096), (4096, 14336), (14336, 4096), (28672, 4096),
+           (128256, 4096)]
+
+
+@pytest.mark.parametrize("N,K", FULL_Q4)
+def test_full_size_q4_0_m1(orc, N, K):
+    W = synth.q4_0_weights(N, K, synth.seed_for(f"q4_0_{N}x{K}"))
+    x = synth.activations(1, K, synth.seed_for(f"x_{K}"))
+    check("q4_0", W, x, N, K, orc, rows=_sample_rows(N))
+
+
+@pytest.mark.parametrize("N,K", [(12288, 2560), (2560, 6144), (8192, 2048)])
+@pytest.mark.parametrize("M", [1, 2, 4, 8])
+def test_full_size_q8_0(orc, N, K, M):
+    W = synth.q8_0_weights(N, K, synth.seed_for(f"q8_0_{N}x{K}"))
+    x = synth.activations(M, K, synth.seed_for(f"x_{K}_{M}"))
+    check("q8_0", W, x, N, K, orc, rows=_sample_rows(N))
+
+
+# -- multi-expert decode --------------------------------------------------------------
+
+@pytest.mark.parametrize("E,slots,N,K", [(128, 10, 640, 2560), (128, 8, 512, 2048), (5, 5, 64, 512),
+                                         (3, 7, 33, 256)])
+def test_moe_matches_oracle_and_single_calls(cuda_lib, orc, E, slots, N, K):
+    q = cuda_lib
+    pool = synth.q4_0_weights(E * N, K, 40 + E)
+    idx = synth.expert_indices(1, min(slots, E), E, 41)[0]
+    if slots > E:      # more slots than experts: duplicates
+        idx = np.resize(idx, slots).astype(np.int32)
+    x = synth.activations(slots, K, 42)
+    pd, xd = dev(pool), dev(x)
+    y = q.qmv_moe(pd, dev(idx), E, xd, N)
+    torch.cuda.synchronize()
+    yn = y.cpu().numpy().astype(np.float64)
+    y_ref, S = orc.moe(0, pool, idx, E, x, N, K, nthreads=8)
+    assert H.normalised_error(yn, y_ref, S) <= H.TOL
+    rb = (K // 32) * 18
+    for s in range(slots):
+        e = int(idx[s])
+        ys = q.qmv_q4_0(pd.view(E * N, rb)[e * N:(e + 1) * N], xd[s:s + 1])
+        torch.cuda.synchronize()
+        assert torch.equal(ys[0], y[s]), f"slot {s} is not bit-identical to the single call"
+        # every other expert fails this slot's check (a wrong index fails)
+        if s == 0:
+            for other in range(min(E, 6)):
+                if other == e:
+                    continue
+                yo, So = orc.qmv(0, pool[other * N:(other + 1) * N], x[s:s + 1], N, K)
+                assert H.normalised_error(yn[s:s + 1], yo, So) > H.TOL
+    assert q.qmv_device_status() == 0
+
+
+def test_moe_bad_index_sets_status_and_nans(cuda_lib):
+    q = cuda_lib
+    E, N, K = 4, 96, 512
+    pool = dev(synth.q4_0_weights(E * N, K, 50))
+    x = dev(synth.activations(3, K, 51))
+    idx = dev(np.array([1, 9, 2], dtype=np.int32))
+    y = q.qmv_moe(pool, idx, E, x, N)
+    st = q.qmv_device_status()
+    assert st & q.QMV_DEV_BAD_EXPERT
+    assert torch.all(torch.isnan(y[1]))
+    assert torch.all(torch.isfinite(y[0])) and torch.all(torch.isfinite(y[2]))
+    ok = q.qmv_moe(pool, dev(np.array([1, 3, 2], dtype=np.int32)), E, x, N)
+    assert torch.equal(ok[0], y[0]) and torch.equal(ok[2], y[2])
+    assert q.qmv_device_status() == 0
+
+
+# -- sabotage: corrupted packed bytes must fail every check ----------------------------
+
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
+def test_sabotage_fails(orc, fmt):
+    N, K = 512, 2048
+    W = synth.weights(fmt, N, K, 60)
+    x = synth.activations(2, K, 61)
+    y_bad = gpu_call(fmt, H.sabotage(W, fmt), x)
+    y_ref, S = orc.qmv(H.FMT[fmt], W, x, N, K, nthreads=8)
+    assert H.normalised_error(y_bad, y_ref, S) > 20 * H.TOL
+    # control: the kernel is consistent with the oracle on the corrupted bytes
+    y_ref_bad, S_bad = orc.qmv(H.FMT[fmt], H.sabotage(W, fmt), x, N, K, nthreads=8)
+    assert H.normalised_error(y_bad, y_ref_bad, S_bad) <= H.TOL
+
+
+# -- prefill ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("N,K,M", [(256, 512, 64), (384, 1024, 100), (128, 256, 1), (1024, 2560, 512),
+                                   (200, 512, 70), (128, 2048, 257)])
+def test_prefill(cuda_lib, orc, N, K, M):
+    q = cuda_lib
+    W = synth.q4_0_weights(N, K, N + K + M)
+    x = synth.activations(M, K, M)
+    y = q.qmm_q4_0_prefill(dev(W), dev(x))
+    torch.cuda.synchronize()
+    y_ref, S = orc.qmv(0, W, x, N, K, nthreads=8)
+    assert H.normalised_error(y.cpu().numpy(), y_ref, S) <= H.TOL
+
+
+@pytest.mark.parametrize("N,K,M", [(12288, 2560, 64), (8192, 2048, 512)])
+def test_prefill_full_size_sampled(cuda_lib, orc, N, K, M):
+    q = cuda_lib
+    W = synth.q4_0_weights(N, K, synth.seed_for(f"prefill_{N}x{K}"))
+    x = synth.activations(M, K, synth.seed_for(f"prefill_x_{M}"))
+    y = q.qmm_q4_0_prefill(dev(W), dev(x)).cpu().numpy()
+    rows = _sample_rows(N, k=48)
+    y_ref, S = orc.qmv_rows(0, W, x, N, K, rows, nthreads=8)
+    assert H.normalised_error(y[:, rows], y_ref, S) <= H.TOL

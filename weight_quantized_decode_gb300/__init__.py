@@ -1,1 +1,200 @@
-"""placeholder"""
+"""weight_quantized_decode_gb300 -- block-quantised (GGUF Q4_0 / Q8_0) weight x
+activation products for single-stream decode on one GB300 (sm_103a).
+
+A thin ctypes binding over the C ABI in ``include/qmv.h`` (``libqmv.so``,
+built in-tree by ``build.py``).  It only marshals arguments: every step of the
+computation runs in the library's CUDA kernels.  There is no CPU path; calls
+raise if the library is missing or a tensor is not on a CUDA device.
+
+Functions (same names as the C ABI):
+    qmv_q4_0(W, x, y=None, stream=None)          -> y fp32 [M, N]
+    qmv_q8_0(W, x, y=None, stream=None)          -> y fp32 [M, N]
+    qmv_moe(W_pool, expert_idx, n_experts, x, N, y=None, stream=None)
+    qmm_q4_0_prefill(W, x, y=None, stream=None)  -> y fp32 [M, N]
+    qmv_device_status(stream=None)               -> int (QMV_DEV_* bits, cleared)
+    qmv_set_pdl(enable), qmv_status_str(code), qmv_version()
+Raw-pointer forms (``*_ptr``) take integers and are what the benchmark times.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libqmv.so")
+
+QMV_OK = 0
+QMV_DEV_BAD_EXPERT = 0x1
+QMV_DEV_TIMEOUT = 0x2
+Q4_0_BLOCK_BYTES = 18
+Q8_0_BLOCK_BYTES = 34
+
+_lock = threading.Lock()
+_lib = None
+
+
+class QmvError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__(f"{fn} failed: {qmv_status_str(code)} ({code})")
+        self.code = code
+
+
+def lib():
+    """Load ``libqmv.so`` (raises loudly if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: run weight_quantized_decode_gb300/build.py "
+                               "(there is no CPU fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i64 = ctypes.c_void_p, ctypes.c_int64
+        for name in ("qmv_q4_0", "qmv_q8_0", "qmm_q4_0_prefill"):
+            f = getattr(L, name)
+            f.restype = ctypes.c_int
+            f.argtypes = [vp, vp, vp, i64, i64, i64, vp]
+        L.qmv_moe.restype = ctypes.c_int
+        L.qmv_moe.argtypes = [vp, vp, i64, vp, vp, i64, i64, i64, vp]
+        L.qmv_device_status.restype = ctypes.c_int
+        L.qmv_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
+        L.qmv_set_pdl.restype = None
+        L.qmv_set_pdl.argtypes = [ctypes.c_int]
+        L.qmv_status_str.restype = ctypes.c_char_p
+        L.qmv_status_str.argtypes = [ctypes.c_int]
+        L.qmv_version.restype = ctypes.c_char_p
+        L.qmv_version.argtypes = []
+        _lib = L
+        return L
+
+
+def qmv_status_str(code: int) -> str:
+    return lib().qmv_status_str(int(code)).decode()
+
+
+def qmv_version() -> str:
+    return lib().qmv_version().decode()
+
+
+def qmv_set_pdl(enable: bool) -> None:
+    lib().qmv_set_pdl(1 if enable else 0)
+
+
+# -- raw-pointer entry points ------------------------------------------------------
+
+def _check(fn, code):
+    if code != QMV_OK:
+        raise QmvError(fn, code)
+
+
+def qmv_q4_0_ptr(W: int, x: int, y: int, N: int, K: int, M: int, stream: int = 0) -> None:
+    _check("qmv_q4_0", lib().qmv_q4_0(W, x, y, N, K, M, stream))
+
+
+def qmv_q8_0_ptr(W: int, x: int, y: int, N: int, K: int, M: int, stream: int = 0) -> None:
+    _check("qmv_q8_0", lib().qmv_q8_0(W, x, y, N, K, M, stream))
+
+
+def qmv_moe_ptr(W_pool: int, idx: int, n_experts: int, x: int, y: int, N: int, K: int, M: int,
+                stream: int = 0) -> None:
+    _check("qmv_moe", lib().qmv_moe(W_pool, idx, n_experts, x, y, N, K, M, stream))
+
+
+def qmm_q4_0_prefill_ptr(W: int, x: int, y: int, N: int, K: int, M: int, stream: int = 0) -> None:
+    _check("qmm_q4_0_prefill", lib().qmm_q4_0_prefill(W, x, y, N, K, M, stream))
+
+
+# -- torch-tensor entry points ---------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _prep(W, x, y, block_bytes, fn):
+    torch = _torch()
+    if not (W.is_cuda and x.is_cuda):
+        raise TypeError(f"{fn}: W and x must be CUDA tensors (no CPU path)")
+    if W.dtype != torch.uint8:
+        raise TypeError(f"{fn}: W must be uint8 GGUF bytes")
+    if x.dtype != torch.float16:
+        raise TypeError(f"{fn}: x must be float16")
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    if not (W.is_contiguous() and x.is_contiguous()):
+        raise ValueError(f"{fn}: W and x must be contiguous")
+    M, K = x.shape
+    if K % 32:
+        raise ValueError(f"{fn}: K={K} is not a multiple of 32")
+    row_bytes = (K // 32) * block_bytes
+    if row_bytes == 0:
+        N = W.shape[0] if W.dim() >= 1 else 0
+    else:
+        if W.numel() % row_bytes:
+            raise ValueError(f"{fn}: W size {W.numel()} is not a whole number of rows of {row_bytes} bytes")
+        N = W.numel() // row_bytes
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    elif not (y.is_cuda and y.dtype == torch.float32 and y.is_contiguous() and y.numel() == M * N):
+        raise ValueError(f"{fn}: y must be a contiguous CUDA float32 tensor of {M}x{N}")
+    return W, x, y, N, K, M
+
+
+def qmv_q4_0(W, x, y=None, stream=None):
+    """y[M, N] = x[M, K] @ dequant(W)^T for Q4_0 weights ``W`` (uint8, N rows)."""
+    W, x, y, N, K, M = _prep(W, x, y, Q4_0_BLOCK_BYTES, "qmv_q4_0")
+    qmv_q4_0_ptr(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, _stream_handle(stream))
+    return y
+
+
+def qmv_q8_0(W, x, y=None, stream=None):
+    """y[M, N] = x[M, K] @ dequant(W)^T for Q8_0 weights."""
+    W, x, y, N, K, M = _prep(W, x, y, Q8_0_BLOCK_BYTES, "qmv_q8_0")
+    qmv_q8_0_ptr(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, _stream_handle(stream))
+    return y
+
+
+def qmm_q4_0_prefill(W, x, y=None, stream=None):
+    """Many-token (prefill) form of qmv_q4_0 on the tensor cores."""
+    W, x, y, N, K, M = _prep(W, x, y, Q4_0_BLOCK_BYTES, "qmm_q4_0_prefill")
+    qmm_q4_0_prefill_ptr(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, _stream_handle(stream))
+    return y
+
+
+def qmv_moe(W_pool, expert_idx, n_experts, x, N, y=None, stream=None):
+    """Slot s: y[s] = x[s] @ dequant(expert expert_idx[s])^T, all slots in one launch."""
+    torch = _torch()
+    if not (W_pool.is_cuda and x.is_cuda and expert_idx.is_cuda):
+        raise TypeError("qmv_moe: W_pool, expert_idx and x must be CUDA tensors (no CPU path)")
+    if expert_idx.dtype != torch.int32 or not expert_idx.is_contiguous():
+        raise TypeError("qmv_moe: expert_idx must be a contiguous int32 CUDA tensor")
+    if W_pool.dtype != torch.uint8 or x.dtype != torch.float16:
+        raise TypeError("qmv_moe: W_pool must be uint8, x float16")
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    M, K = x.shape
+    if expert_idx.numel() != M:
+        raise ValueError("qmv_moe: one expert index per token")
+    need = n_experts * N * (K // 32) * Q4_0_BLOCK_BYTES
+    if W_pool.numel() < need:
+        raise ValueError(f"qmv_moe: W_pool holds {W_pool.numel()} bytes, needs {need}")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    qmv_moe_ptr(W_pool.data_ptr(), expert_idx.data_ptr(), int(n_experts), x.data_ptr(), y.data_ptr(),
+                int(N), int(K), int(M), _stream_handle(stream))
+    return y
+
+
+def qmv_device_status(stream=None) -> int:
+    """Read and clear the device status word (synchronises the stream)."""
+    out = ctypes.c_int32(0)
+    _check("qmv_device_status", lib().qmv_device_status(_stream_handle(stream), ctypes.byref(out)))
+    return int(out.value)

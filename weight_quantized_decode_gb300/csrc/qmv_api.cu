@@ -1,0 +1,320 @@
+// qmv_api.cu -- the C ABI (include/qmv.h): argument validation, the per-shape
+// launch configuration, the device status word, and the generic kernel's
+// instantiations.
+#include <atomic>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/qmv.h"
+#include "qmv_gemv.cuh"
+#include "qmv_launch.h"
+#include "qmv_prefill.h"
+
+namespace qmv {
+
+// One status word per device; kernels receive its address.
+__device__ int g_device_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int *> g_status_ptr[kMaxDevices];
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<int> g_smem_optin[kMaxDevices];
+std::atomic<int> g_pdl{1};
+
+cudaError_t current_device(int *dev)
+{
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return e;
+    if (*dev < 0 || *dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    return cudaSuccess;
+}
+
+cudaError_t device_info(int dev, int **status, int *sms, int *smem_optin)
+{
+    int *sp = g_status_ptr[dev].load(std::memory_order_acquire);
+    if (!sp) {
+        void *addr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&addr, g_device_status);
+        if (e != cudaSuccess) return e;
+        int v = 0;
+        e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        g_sm_count[dev].store(v, std::memory_order_relaxed);
+        e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess) return e;
+        g_smem_optin[dev].store(v, std::memory_order_relaxed);
+        sp = static_cast<int *>(addr);
+        g_status_ptr[dev].store(sp, std::memory_order_release);
+    }
+    *status = sp;
+    *sms = g_sm_count[dev].load(std::memory_order_relaxed);
+    *smem_optin = g_smem_optin[dev].load(std::memory_order_relaxed);
+    return cudaSuccess;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int lanes_per_row(int U, int M)
+{
+    // Largest power of two dividing the number of 256-weight units of a row,
+    // capped so that the G distinct activation units a warp reads at once stay
+    // cheap for several tokens.
+    const int cap = (M <= 2) ? 16 : 8;
+    int G = 1;
+    while (G * 2 <= cap && U % (G * 2) == 0) G *= 2;
+    return G;
+}
+
+struct Plan {
+    bool streaming;
+    int grid, warps;
+    size_t smem;
+};
+
+// Choose the launch of the streaming kernel (or fall back to the generic one).
+Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
+{
+    Plan pl{false, 0, 8, 0};
+    if (p.K % 256 != 0 || p.K == 0) return pl;
+    const int64_t U = p.K / 256;
+    if (U > (1 << 20)) return pl;
+    p.U = static_cast<int>(U);
+    p.G = lanes_per_row(p.U, M);
+    p.SP = 1;
+    const int RG = 32 / p.G;
+    const int64_t groups = (p.rows_total + RG - 1) / RG;
+    int grid = static_cast<int>(groups < sms ? groups : sms);
+    if (grid < 1) grid = 1;
+    const int64_t rows_per_cta = (p.rows_total + grid - 1) / grid;
+    int64_t pmax = (rows_per_cta + p.N - 1) / p.N + 1;
+    if (pmax > p.n_problems) pmax = p.n_problems;
+    p.max_local_problems = static_cast<int>(pmax);
+    const int unit_bytes = fmt == kQ4_0 ? 144 : 272;
+    const size_t xbytes = static_cast<size_t>(pmax) * M * p.U * kXUnitBytes;
+    const size_t budget = static_cast<size_t>(smem_optin) - 1024;
+    if (xbytes + 8 * 1024 > budget) return pl;
+    for (int warps : {8, 4}) {
+        const size_t per_stage = static_cast<size_t>(warps) * (32 * p.SP * unit_bytes + 8);
+        int S = static_cast<int>((budget - xbytes) / per_stage);
+        if (S > 6) S = 6;
+        if (S >= 2) {
+            p.S = S;
+            pl.streaming = true;
+            pl.grid = grid;
+            pl.warps = warps;
+            pl.smem = gemv_smem_bytes(fmt, M, static_cast<int>(pmax), p.U, warps, S, p.SP);
+            return pl;
+        }
+    }
+    return pl;
+}
+
+qmv_status run_gemv(int fmt, const void *W, const int32_t *idx, int64_t n_experts, const void *x, float *y,
+                    int64_t N, int64_t K, int64_t M, int n_problems, cudaStream_t stream)
+{
+    int dev = 0;
+    if (current_device(&dev) != cudaSuccess) return QMV_ERR_CUDA;
+    int *status = nullptr;
+    int sms = 0, optin = 0;
+    if (device_info(dev, &status, &sms, &optin) != cudaSuccess) return QMV_ERR_CUDA;
+
+    GemvParams p = {};
+    p.W = static_cast<const uint8_t *>(W);
+    p.x = static_cast<const __half *>(x);
+    p.y = y;
+    p.expert_idx = idx;
+    p.N = N;
+    p.K = K;
+    p.n_experts = n_experts;
+    p.row_bytes = (K / 32) * (fmt == kQ4_0 ? 18 : 34);
+    p.n_problems = n_problems;
+    p.max_local_problems = n_problems;
+    p.rows_total = N * n_problems;
+    p.status = status;
+    const int Mk = static_cast<int>(M);
+    const bool pdl = g_pdl.load(std::memory_order_relaxed) != 0;
+
+    cudaError_t e;
+    Plan pl = plan_gemv(fmt, p, Mk, sms, optin);
+    if (pl.streaming) {
+        e = (fmt == kQ4_0) ? launch_gemv_stream_q4_0(Mk, p, pl.grid, pl.warps, pl.smem, stream, pdl)
+                           : launch_gemv_stream_q8_0(Mk, p, pl.grid, pl.warps, pl.smem, stream, pdl);
+    } else {
+        const int64_t warps_needed = p.rows_total;
+        int64_t grid = (warps_needed + 7) / 8;
+        if (grid > 32LL * sms) grid = 32LL * sms;
+        if (grid < 1) grid = 1;
+        e = launch_gemv_generic(fmt, p, Mk, static_cast<int>(grid), stream, pdl);
+    }
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return QMV_ERR_LAUNCH;
+    }
+    return QMV_OK;
+}
+
+qmv_status check_common(const void *W, const void *x, float *y, int64_t N, int64_t K, int64_t M, int64_t max_m)
+{
+    if (N < 0 || K < 0 || M < 0 || M > max_m) return QMV_ERR_SHAPE;
+    if (K % 32 != 0) return QMV_ERR_SHAPE;
+    if (N > (int64_t(1) << 40) || K > (int64_t(1) << 31)) return QMV_ERR_SHAPE;
+    if (N == 0 || M == 0) return QMV_OK;
+    if (!y) return QMV_ERR_NULL;
+    if (K > 0 && (!W || !x)) return QMV_ERR_NULL;
+    if (W && !aligned(W, 16)) return QMV_ERR_ALIGN;
+    if (x && !aligned(x, 2)) return QMV_ERR_ALIGN;
+    if (!aligned(y, 4)) return QMV_ERR_ALIGN;
+    return QMV_OK;
+}
+
+}  // namespace
+
+cudaError_t ensure_smem_optin(const void *func, size_t smem)
+{
+    if (smem <= 48 * 1024) return cudaSuccess;
+    // Setting the attribute is cheap but not free; do it for the maximum once
+    // per (kernel, device) pair and remember it.
+    static std::mutex mu;
+    static const void *seen_func[256];
+    static int seen_dev[256];
+    static int nseen = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < nseen; ++i)
+        if (seen_func[i] == func && seen_dev[i] == dev) return cudaSuccess;
+    int optin = 0;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    if (e != cudaSuccess) return e;
+    if (nseen < 256) {
+        seen_func[nseen] = func;
+        seen_dev[nseen] = dev;
+        ++nseen;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_gemv_generic(int fmt, const GemvParams &p, int M, int grid, cudaStream_t s, bool pdl)
+{
+    if (fmt == kQ4_0) return launch_ex(gemv_generic_kernel<kQ4_0>, dim3(grid), dim3(256), 0, s, pdl, p, M);
+    return launch_ex(gemv_generic_kernel<kQ8_0>, dim3(grid), dim3(256), 0, s, pdl, p, M);
+}
+
+}  // namespace qmv
+
+using namespace qmv;
+
+extern "C" {
+
+qmv_status qmv_q4_0(const void *W, const void *x, float *y, int64_t N, int64_t K, int64_t M, qmv_stream_t stream)
+{
+    qmv_status st = check_common(W, x, y, N, K, M, 8);
+    if (st != QMV_OK || N == 0 || M == 0) return st;
+    return run_gemv(kQ4_0, W, nullptr, 1, x, y, N, K, M, 1, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qmv_status qmv_q8_0(const void *W, const void *x, float *y, int64_t N, int64_t K, int64_t M, qmv_stream_t stream)
+{
+    qmv_status st = check_common(W, x, y, N, K, M, 8);
+    if (st != QMV_OK || N == 0 || M == 0) return st;
+    return run_gemv(kQ8_0, W, nullptr, 1, x, y, N, K, M, 1, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qmv_status qmv_moe(const void *W_pool, const int32_t *expert_idx, int64_t n_experts, const void *x, float *y,
+                   int64_t N, int64_t K, int64_t M, qmv_stream_t stream)
+{
+    qmv_status st = check_common(W_pool, x, y, N, K, M, 64);
+    if (st != QMV_OK) return st;
+    if (n_experts < 1) return QMV_ERR_SHAPE;
+    if (N == 0 || M == 0) return QMV_OK;
+    if (!expert_idx) return QMV_ERR_NULL;
+    if (!aligned(expert_idx, 4)) return QMV_ERR_ALIGN;
+    if (n_experts > (int64_t(1) << 31)) return QMV_ERR_SHAPE;
+    // Each token is one problem of one row-set: M slots with 1 token each.
+    return run_gemv(kQ4_0, W_pool, expert_idx, n_experts, x, y, N, K, 1, static_cast<int>(M),
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+qmv_status qmm_q4_0_prefill(const void *W, const void *x, float *y, int64_t N, int64_t K, int64_t M,
+                            qmv_stream_t stream)
+{
+    qmv_status st = check_common(W, x, y, N, K, M, int64_t(1) << 24);
+    if (st != QMV_OK || N == 0 || M == 0) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (x && !aligned(x, 16)) return QMV_ERR_ALIGN;
+    int dev = 0;
+    if (current_device(&dev) != cudaSuccess) return QMV_ERR_CUDA;
+    int *status = nullptr;
+    int sms = 0, optin = 0;
+    if (device_info(dev, &status, &sms, &optin) != cudaSuccess) return QMV_ERR_CUDA;
+    if (prefill_supported(N, K, M)) {
+        cudaError_t e = launch_prefill(W, x, y, N, K, M, sms, status, s);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return QMV_ERR_LAUNCH;
+        }
+        return QMV_OK;
+    }
+    // Other shapes: the generic kernel, eight tokens at a time per warp pass.
+    GemvParams p = {};
+    p.W = static_cast<const uint8_t *>(W);
+    p.x = static_cast<const __half *>(x);
+    p.y = y;
+    p.N = N;
+    p.K = K;
+    p.n_experts = 1;
+    p.row_bytes = (K / 32) * 18;
+    p.n_problems = 1;
+    p.max_local_problems = 1;
+    p.rows_total = N;
+    p.status = status;
+    int64_t grid = (N + 7) / 8;
+    if (grid > 32LL * sms) grid = 32LL * sms;
+    if (grid < 1) grid = 1;
+    cudaError_t e = launch_gemv_generic(kQ4_0, p, static_cast<int>(M), static_cast<int>(grid), s,
+                                        g_pdl.load() != 0);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return QMV_ERR_LAUNCH;
+    }
+    return QMV_OK;
+}
+
+qmv_status qmv_device_status(qmv_stream_t stream, int32_t *out)
+{
+    if (!out) return QMV_ERR_NULL;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return QMV_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return QMV_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return QMV_ERR_CUDA;
+    *out = v;
+    return QMV_OK;
+}
+
+void qmv_set_pdl(int enable) { g_pdl.store(enable ? 1 : 0); }
+
+const char *qmv_status_str(qmv_status s)
+{
+    switch (s) {
+    case QMV_OK: return "ok";
+    case QMV_ERR_NULL: return "null pointer";
+    case QMV_ERR_ALIGN: return "misaligned pointer";
+    case QMV_ERR_SHAPE: return "shape out of range";
+    case QMV_ERR_LAUNCH: return "kernel launch failed";
+    case QMV_ERR_DEVICE: return "device-side error";
+    case QMV_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown status";
+    }
+}
+
+const char *qmv_version(void) { return "qmv 0.1.0 sm_103a"; }
+
+}  // extern "C"

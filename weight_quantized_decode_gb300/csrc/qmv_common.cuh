@@ -1,0 +1,204 @@
+// qmv_common.cuh -- device-side building blocks shared by the decode and
+// prefill kernels: inline-PTX wrappers for mbarriers, bulk (TMA) copies,
+// programmatic dependent launch, and the fp16 magic-number unpack of GGUF
+// Q4_0 / Q8_0 codes.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace qmv {
+
+// Device status bits (mirrors QMV_DEV_* in include/qmv.h).
+constexpr int kDevBadExpert = 0x1;
+constexpr int kDevTimeout = 0x2;
+
+// A bounded wait gives up after this many nanoseconds of global time.
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---- mbarrier ---------------------------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void mbar_init_fence()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of `bar`, giving up after kWaitLimitNs.  Called by a
+// single thread.  Returns false (and records kDevTimeout) on give-up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int *status)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (status) atomicOr(status, kDevTimeout);
+            return false;
+        }
+    }
+}
+
+// Warp-collective bounded wait: every lane of the warp calls it; the result is
+// warp-uniform.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, int *status)
+{
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(bar, parity, status);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (ok) {
+        // The phase has completed; every lane observes it before touching data.
+        while (!mbar_try_wait(bar, parity)) {
+        }
+    }
+    return ok;
+}
+
+// ---- bulk copies (TMA, non-tensor) --------------------------------------------
+
+// Global -> shared bulk copy that signals `bar` with complete_tx.  dst, src and
+// bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// ---- programmatic dependent launch ---------------------------------------------
+
+__device__ __forceinline__ void pdl_wait_prior_grid()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_allow_next_grid()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---- integer helpers ------------------------------------------------------------
+
+// (a & b) | c in one LOP3.
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ __half2 as_h2(uint32_t u)
+{
+    return *reinterpret_cast<__half2 *>(&u);
+}
+
+__device__ __forceinline__ float half_lo_to_float(uint32_t u)
+{
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(u & 0xffffu)));
+}
+
+__device__ __forceinline__ float half_hi_to_float(uint32_t u)
+{
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(u >> 16)));
+}
+
+// ---- fp16 magic-number unpack -----------------------------------------------------
+//
+// The half with bit pattern 0x6400 | n is exactly 1024 + n for 0 <= n < 1024
+// ("v2 = fp16 bit trick (0x6400 | n is the half 1024 + n)" -- volta-kernel-
+// bakeoff, "What's in the race").  One LOP3 places two nibbles (or, after a
+// PRMT, two bytes) into the mantissas of a half2; one HFMA2 then removes the
+// 1024 offset and the code bias and applies a power-of-two pre-scale, exactly.
+//
+// The weights come out pre-scaled (Q4_0: (c - 8) / 32, Q8_0: q / 512) so that
+// fp16 partial sums of large activations cannot overflow ("weights are
+// unpacked as (code - 8) / 32 ... so no fp16 activation can overflow a partial
+// sum" -- volta-kernel-bakeoff, "A few tokens at once").  The fp32 block sums
+// are multiplied back by 32 (or 512) at the end.
+constexpr float kQ4Prescale = 32.0f;
+constexpr float kQ8Prescale = 512.0f;
+
+// Q4_0: one 32-bit word of qs holding bytes (b0, b1, b2, b3) -> four half2
+// weights:  w[0] = (lo b0, lo b2)   w[1] = (lo b1, lo b3)
+//           w[2] = (hi b0, hi b2)   w[3] = (hi b1, hi b3)
+// Low nibbles of qs[i] are element i of the block, high nibbles element i+16.
+__device__ __forceinline__ void unpack_q4_word(uint32_t v, __half2 (&w)[4])
+{
+    const uint32_t magic = 0x64006400u;
+    const uint32_t v8 = v >> 8;
+    const uint32_t l02 = and_or(v, 0x000F000Fu, magic);   // 1024 + n
+    const uint32_t l13 = and_or(v8, 0x000F000Fu, magic);
+    const uint32_t h02 = and_or(v, 0x00F000F0u, magic);   // 1024 + 16 n
+    const uint32_t h13 = and_or(v8, 0x00F000F0u, magic);
+    // (1024 + n) / 32 - 1032 / 32 = (n - 8) / 32
+    const __half2 s_lo = __halves2half2(__ushort_as_half(0x2800), __ushort_as_half(0x2800));  // 2^-5
+    const __half2 b_lo = __halves2half2(__ushort_as_half(0xD008), __ushort_as_half(0xD008));  // -32.25
+    // (1024 + 16 n) / 512 - 2.25 = (n - 8) / 32
+    const __half2 s_hi = __halves2half2(__ushort_as_half(0x1800), __ushort_as_half(0x1800));  // 2^-9
+    const __half2 b_hi = __halves2half2(__ushort_as_half(0xC080), __ushort_as_half(0xC080));  // -2.25
+    w[0] = __hfma2(as_h2(l02), s_lo, b_lo);
+    w[1] = __hfma2(as_h2(l13), s_lo, b_lo);
+    w[2] = __hfma2(as_h2(h02), s_hi, b_hi);
+    w[3] = __hfma2(as_h2(h13), s_hi, b_hi);
+}
+
+// Q8_0: one 32-bit word holding int8 codes (q0, q1, q2, q3) -> two half2
+// weights w[0] = (q0, q2) / 512, w[1] = (q1, q3) / 512.  Biasing each byte by
+// +128 (XOR 0x80) makes it an unsigned mantissa: 0x6400 | (q + 128) = 1152 + q.
+__device__ __forceinline__ void unpack_q8_word(uint32_t v, __half2 (&w)[2])
+{
+    const uint32_t u = v ^ 0x80808080u;
+    const uint32_t h02 = __byte_perm(u, 0x64646464u, 0x4240);   // (0x64|b0, 0x64|b2)
+    const uint32_t h13 = __byte_perm(u, 0x64646464u, 0x4341);   // (0x64|b1, 0x64|b3)
+    // (1152 + q) / 512 - 2.25 = q / 512
+    const __half2 s = __halves2half2(__ushort_as_half(0x1800), __ushort_as_half(0x1800));  // 2^-9
+    const __half2 b = __halves2half2(__ushort_as_half(0xC080), __ushort_as_half(0xC080));  // -2.25
+    w[0] = __hfma2(as_h2(h02), s, b);
+    w[1] = __hfma2(as_h2(h13), s, b);
+}
+
+}  // namespace qmv

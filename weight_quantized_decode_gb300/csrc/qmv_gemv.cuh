@@ -1,0 +1,482 @@
+// qmv_gemv.cuh -- the streaming decode GEMV for GGUF Q4_0 / Q8_0 on sm_103a,
+// and the one-launch multi-expert variant built on the same inner loop.
+//
+// Design (GB300-first; the pages' V100/RTX-3090 kernels are prior art):
+//   * Unit of work: 8 consecutive blocks of one row = 256 weights
+//     (144 bytes Q4_0, 272 bytes Q8_0; both are whole multiples of 16 bytes,
+//     so a unit is a run of aligned 128-bit words when K % 256 == 0).
+//   * Each warp is its own streaming engine: it owns a ring of S shared-memory
+//     stages and fills them with bulk (TMA) copies, one per row chunk, that
+//     signal an mbarrier on arrival.  A stage holds RG = 32/G rows x SP*G units.
+//   * Lane (r, q) of the warp (r = lane / G, q = lane % G) reads unit q (+G...)
+//     of row r from the stage with 128-bit shared loads (a 144-/272-byte lane
+//     stride is bank-conflict-free), unpacks nibbles/bytes with the fp16
+//     0x6400|n trick, and accumulates half2 products per block, scaled to fp32
+//     per block ("v2 = fp16 bit trick", "v2w = a whole 32-value group per lane
+//     step" -- volta-kernel-bakeoff, "What's in the race").
+//   * G lanes per row, RG rows per warp ("multiple output rows per warp for
+//     memory-level parallelism + a per-shape launch config" -- sm8x-bench,
+//     summary); the G partial sums of a row are combined with warp shuffles
+//     ("one warp (32 threads) per output row, __shfl_down_sync" --
+//     SovereignKernel diary, Phase 3).
+//   * Activations live in shared memory for the whole call, permuted once per
+//     CTA into the pair order the unpack produces and padded so that the G
+//     distinct units a warp reads at once fall in distinct banks.  For M > 1
+//     one unpacked weight register serves all M tokens ("lets one activation
+//     load serve several rows" -- volta-kernel-bakeoff, "A few tokens").
+//   * Rows are split across CTAs in balanced contiguous ranges; within a CTA
+//     the row groups are dealt to warps round-robin.
+//   * Programmatic dependent launch: the first S stages of W are requested
+//     before griddepcontrol.wait; x is read and y written only after it.
+#pragma once
+
+#include "qmv_common.cuh"
+
+namespace qmv {
+
+enum Fmt : int { kQ4_0 = 0, kQ8_0 = 1 };
+
+template <int FMT>
+struct FmtTraits;
+
+template <>
+struct FmtTraits<kQ4_0> {
+    static constexpr int kBlockBytes = 18;
+    static constexpr int kUnitBytes = 144;    // 8 blocks
+    static constexpr int kUnitWords = 36;
+    static constexpr float kPrescale = kQ4Prescale;
+};
+
+template <>
+struct FmtTraits<kQ8_0> {
+    static constexpr int kBlockBytes = 34;
+    static constexpr int kUnitBytes = 272;
+    static constexpr int kUnitWords = 68;
+    static constexpr float kPrescale = kQ8Prescale;
+};
+
+constexpr int kUnitWeights = 256;
+constexpr int kXUnitBytes = 528;   // 512 bytes of permuted activations + 16 bytes pad
+
+struct GemvParams {
+    const uint8_t *W;            // weights; for the multi-expert call, the expert pool
+    const __half *x;             // [n_problems * M][K]
+    float *y;                    // [n_problems * M][N]
+    const int32_t *expert_idx;   // multi-expert call only (else nullptr)
+    int64_t N;                   // rows per problem
+    int64_t K;
+    int64_t n_experts;
+    int64_t row_bytes;           // (K/32) * block bytes
+    int64_t rows_total;          // n_problems * N
+    int n_problems;              // 1 for a plain GEMV, slots for the multi-expert call
+    int max_local_problems;      // most problems one CTA's row range can touch
+    int U;                       // units per row = K / 256
+    int G;                       // lanes per row (power of two, 1..32)
+    int SP;                      // passes per stage (odd)
+    int S;                       // stages in each warp's ring
+    int *status;                 // device status word
+};
+
+// Shared-memory bytes the kernel needs for a configuration.
+__host__ __device__ inline size_t gemv_smem_bytes(int fmt, int M, int n_problems, int U, int warps, int S, int SP)
+{
+    const size_t unit_bytes = fmt == kQ4_0 ? 144 : 272;
+    const size_t xbytes = static_cast<size_t>(n_problems) * M * U * kXUnitBytes;
+    const size_t ring = static_cast<size_t>(warps) * S * 32 * SP * unit_bytes;
+    const size_t bars = static_cast<size_t>(warps) * S * 8;
+    return xbytes + ring + bars;
+}
+
+// Position, inside a block, of the code whose weight lands in permuted slot
+// `slot` (0..31) of the activation layout.  Even blocks of a unit start 2
+// bytes into a 32-bit word, so their first word is re-formed with a PRMT as
+// qs bytes (0, 1, 14, 15) [Q4_0] or (0, 1, 30, 31) [Q8_0].
+template <int FMT>
+__device__ __forceinline__ int x_perm_source(int block_parity, int slot)
+{
+    if (FMT == kQ4_0) {
+        const int word = slot >> 3, s8 = slot & 7;
+        const int pair = s8 >> 1, second = s8 & 1;
+        const int bp = (pair & 1) + 2 * second;             // byte within the word
+        int qi;
+        if (block_parity) qi = 4 * word + bp;
+        else if (word == 0) qi = (bp < 2) ? bp : 12 + bp;   // 0, 1, 14, 15
+        else qi = 4 * word - 2 + bp;
+        return qi + ((pair >= 2) ? 16 : 0);
+    } else {
+        const int word = slot >> 2, s4 = slot & 3;
+        const int pair = s4 >> 1, second = s4 & 1;
+        const int bp = pair + 2 * second;
+        if (block_parity) return 4 * word + bp;
+        if (word == 0) return (bp < 2) ? bp : 28 + bp;       // 0, 1, 30, 31
+        return 4 * word - 2 + bp;
+    }
+}
+
+// ---- per-unit dot products ------------------------------------------------------
+
+// acc[m] += sum over the 8 blocks of one unit of d_b * (partial_b / prescale).
+// wsrc: the unit's bytes in shared memory; xsrc: the unit's permuted
+// activations for token 0; xstride: bytes between tokens.
+template <int M>
+__device__ __forceinline__ void dot_unit_q4_0(const uint8_t *wsrc, const uint8_t *xsrc, int xstride,
+                                              float (&acc)[M])
+{
+    uint32_t w[36];
+#pragma unroll
+    for (int c = 0; c < 9; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(wsrc + 16 * c);
+        w[4 * c + 0] = v.x;
+        w[4 * c + 1] = v.y;
+        w[4 * c + 2] = v.z;
+        w[4 * c + 3] = v.w;
+    }
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+        const int h = b >> 1;
+        uint32_t q[4];
+        uint32_t dsrc;
+        if ((b & 1) == 0) {
+            dsrc = w[9 * h] & 0xffffu;
+            q[0] = __byte_perm(w[9 * h], w[9 * h + 4], 0x5432);
+            q[1] = w[9 * h + 1];
+            q[2] = w[9 * h + 2];
+            q[3] = w[9 * h + 3];
+        } else {
+            dsrc = w[9 * h + 4] >> 16;
+            q[0] = w[9 * h + 5];
+            q[1] = w[9 * h + 6];
+            q[2] = w[9 * h + 7];
+            q[3] = w[9 * h + 8];
+        }
+        const float d = half_lo_to_float(dsrc);
+        __half2 hacc[M];
+#pragma unroll
+        for (int m = 0; m < M; ++m) hacc[m] = __float2half2_rn(0.0f);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            __half2 wv[4];
+            unpack_q4_word(q[j], wv);
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                const uint4 xv = *reinterpret_cast<const uint4 *>(xsrc + m * xstride + b * 64 + j * 16);
+                hacc[m] = __hfma2(wv[0], as_h2(xv.x), hacc[m]);
+                hacc[m] = __hfma2(wv[1], as_h2(xv.y), hacc[m]);
+                hacc[m] = __hfma2(wv[2], as_h2(xv.z), hacc[m]);
+                hacc[m] = __hfma2(wv[3], as_h2(xv.w), hacc[m]);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            const float2 f = __half22float2(hacc[m]);
+            acc[m] = fmaf(d, f.x + f.y, acc[m]);
+        }
+    }
+}
+
+template <int M>
+__device__ __forceinline__ void dot_unit_q8_0(const uint8_t *wsrc, const uint8_t *xsrc, int xstride,
+                                              float (&acc)[M])
+{
+    uint32_t w[68];
+#pragma unroll
+    for (int c = 0; c < 17; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(wsrc + 16 * c);
+        w[4 * c + 0] = v.x;
+        w[4 * c + 1] = v.y;
+        w[4 * c + 2] = v.z;
+        w[4 * c + 3] = v.w;
+    }
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+        const int h = b >> 1;
+        uint32_t q[8];
+        uint32_t dsrc;
+        if ((b & 1) == 0) {
+            dsrc = w[17 * h] & 0xffffu;
+            q[0] = __byte_perm(w[17 * h], w[17 * h + 8], 0x5432);
+#pragma unroll
+            for (int j = 1; j < 8; ++j) q[j] = w[17 * h + j];
+        } else {
+            dsrc = w[17 * h + 8] >> 16;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) q[j] = w[17 * h + 9 + j];
+        }
+        const float d = half_lo_to_float(dsrc);
+        __half2 hacc[M];
+#pragma unroll
+        for (int m = 0; m < M; ++m) hacc[m] = __float2half2_rn(0.0f);
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+            __half2 wa[2], wb[2];
+            unpack_q8_word(q[j], wa);
+            unpack_q8_word(q[j + 1], wb);
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                const uint4 xv = *reinterpret_cast<const uint4 *>(xsrc + m * xstride + b * 64 + j * 8);
+                hacc[m] = __hfma2(wa[0], as_h2(xv.x), hacc[m]);
+                hacc[m] = __hfma2(wa[1], as_h2(xv.y), hacc[m]);
+                hacc[m] = __hfma2(wb[0], as_h2(xv.z), hacc[m]);
+                hacc[m] = __hfma2(wb[1], as_h2(xv.w), hacc[m]);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            const float2 f = __half22float2(hacc[m]);
+            acc[m] = fmaf(d, f.x + f.y, acc[m]);
+        }
+    }
+}
+
+// ---- the streaming kernel ----------------------------------------------------------
+
+template <int FMT, int M>
+__global__ void __launch_bounds__(256, 1) gemv_stream_kernel(const GemvParams p)
+{
+    using T = FmtTraits<FMT>;
+    extern __shared__ __align__(128) uint8_t smem[];
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int warps = blockDim.x >> 5;
+    const int U = p.U, G = p.G, SP = p.SP, S = p.S;
+    const int RG = 32 / G;
+
+    // Shared-memory carve-up: activations, then per-warp rings, then barriers.
+    const size_t xbytes = static_cast<size_t>(p.max_local_problems) * M * U * kXUnitBytes;
+    const int slot_bytes = 32 * SP * T::kUnitBytes;
+    uint8_t *xs = smem;
+    uint8_t *ring = smem + xbytes + static_cast<size_t>(warp) * S * slot_bytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + xbytes + static_cast<size_t>(warps) * S * slot_bytes) +
+                     warp * S;
+
+    // This CTA's contiguous range of (problem, row) pairs.
+    const int64_t R = p.rows_total;
+    const int64_t row0 = (R * blockIdx.x) / gridDim.x;
+    const int64_t row1 = (R * (blockIdx.x + 1)) / gridDim.x;
+    const int64_t nrows = row1 - row0;
+    // Problems (tokens of the plain GEMV, or expert slots) this CTA touches.
+    const int64_t prob_lo = nrows > 0 ? row0 / p.N : 0;
+    const int64_t prob_hi = nrows > 0 ? (row1 - 1) / p.N : -1;
+    const int64_t ngroups = (nrows + RG - 1) / RG;
+    const int64_t my_groups = (ngroups > warp) ? (ngroups - warp + warps - 1) / warps : 0;
+    const int units_per_stage = SP * G;
+    const int T_stages = (U + units_per_stage - 1) / units_per_stage;
+    const int64_t total = my_groups * T_stages;
+
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+        mbar_init_fence();
+    }
+    __syncwarp();
+
+    int64_t issued = 0;     // stages whose copies have been requested
+    int64_t consumed = 0;   // stages waited for successfully
+
+    // Lane `r` (< RG) requests row r of the group's chunk for stage i.
+    auto issue = [&](int64_t i) {
+        ++issued;
+        const int slot = static_cast<int>(i % S);
+        const int64_t g = warp + (i / T_stages) * warps;
+        const int t = static_cast<int>(i % T_stages);
+        const int u0 = t * units_per_stage;
+        const int u1 = min(U, u0 + units_per_stage);
+        const uint32_t chunk = static_cast<uint32_t>(u1 - u0) * T::kUnitBytes;
+        uint32_t my_bytes = 0;
+        const uint8_t *src = nullptr;
+        if (lane < RG) {
+            const int64_t lr = g * RG + lane;
+            if (lr < nrows) {
+                const int64_t row = row0 + lr;
+                const int64_t prob = row / p.N;
+                const int64_t n = row - prob * p.N;
+                int64_t e = 0;
+                bool ok = true;
+                if (p.expert_idx) {
+                    e = p.expert_idx[prob];
+                    ok = (e >= 0 && e < p.n_experts);
+                }
+                if (ok) {
+                    src = p.W + (e * p.N + n) * p.row_bytes + static_cast<int64_t>(u0) * T::kUnitBytes;
+                    my_bytes = chunk;
+                }
+            }
+        }
+        const uint32_t total_bytes = __reduce_add_sync(0xffffffffu, my_bytes);
+        if (lane == 0) mbar_arrive_expect_tx(&bars[slot], total_bytes);
+        __syncwarp();
+        if (my_bytes) bulk_g2s(ring + static_cast<size_t>(slot) * slot_bytes + lane * (units_per_stage * T::kUnitBytes),
+                               src, my_bytes, &bars[slot]);
+    };
+
+    // Request the first stages before waiting for the previous kernel: W is
+    // never written by it.
+    const int64_t prefetch = total < S ? total : S;
+    // The expert indices may be produced by the previous kernel: only a plain
+    // GEMV prefetches before the dependency wait.
+    if (!p.expert_idx) {
+        for (int64_t i = 0; i < prefetch; ++i) issue(i);
+    }
+
+    pdl_wait_prior_grid();
+
+    if (p.expert_idx) {
+        for (int64_t i = 0; i < prefetch; ++i) issue(i);
+    }
+
+    // Stage the activations: permuted pair order, 528-byte padded units.
+    {
+        const int64_t nhalf = (prob_hi - prob_lo + 1) * M * U * 256;
+        for (int64_t d = threadIdx.x; d < nhalf; d += blockDim.x) {
+            const int64_t tok = d / (static_cast<int64_t>(U) * 256);   // local token index
+            const int rem = static_cast<int>(d - tok * U * 256);
+            const int blk = rem >> 5;      // block within the row of K
+            const int slot = rem & 31;
+            const int src_in_blk = x_perm_source<FMT>(blk & 1, slot);
+            const __half v = p.x[(prob_lo * M + tok) * p.K + blk * 32 + src_in_blk];
+            const size_t off = (static_cast<size_t>(tok) * U + (blk >> 3)) * kXUnitBytes + (blk & 7) * 64 + slot * 2;
+            *reinterpret_cast<__half *>(xs + off) = v;
+        }
+    }
+    __syncthreads();
+    pdl_allow_next_grid();
+
+    const int r = lane / G;
+    const int q = lane % G;
+    const int xstride = U * kXUnitBytes;     // bytes between tokens of a problem
+    float acc[M];
+#pragma unroll
+    for (int m = 0; m < M; ++m) acc[m] = 0.0f;
+
+    bool alive = true;
+    int64_t lr = 0, row = 0, prob = 0;
+    bool row_ok = false;
+
+    for (int64_t i = 0; i < total; ++i) {
+        const int slot = static_cast<int>(i % S);
+        const uint32_t parity = static_cast<uint32_t>((i / S) & 1);
+        const int64_t g = warp + (i / T_stages) * warps;
+        const int t = static_cast<int>(i % T_stages);
+        if (t == 0) {
+            lr = g * RG + r;
+            row_ok = lr < nrows;
+            row = row0 + lr;
+            prob = row_ok ? row / p.N : 0;
+            if (row_ok && p.expert_idx) {
+                const int64_t e = p.expert_idx[prob];
+                row_ok = (e >= 0 && e < p.n_experts);
+            }
+        }
+        if (!mbar_wait_warp(&bars[slot], parity, p.status)) {
+            alive = false;
+            break;
+        }
+        consumed = i + 1;
+        const uint8_t *stage = ring + static_cast<size_t>(slot) * slot_bytes + r * (units_per_stage * T::kUnitBytes);
+        const int u0 = t * units_per_stage;
+        if (row_ok) {
+            const uint8_t *xrow = xs + static_cast<size_t>(prob - prob_lo) * M * xstride;
+            for (int pass = 0; pass < SP; ++pass) {
+                const int ul = pass * G + q;          // unit within the stage
+                const int u = u0 + ul;
+                if (u < U) {
+                    if (FMT == kQ4_0)
+                        dot_unit_q4_0<M>(stage + ul * T::kUnitBytes, xrow + static_cast<size_t>(u) * kXUnitBytes,
+                                         xstride, acc);
+                    else
+                        dot_unit_q8_0<M>(stage + ul * T::kUnitBytes, xrow + static_cast<size_t>(u) * kXUnitBytes,
+                                         xstride, acc);
+                }
+            }
+        }
+        __syncwarp();
+        if (i + S < total) issue(i + S);
+
+        if (t == T_stages - 1) {
+            // Combine the G partial sums of each row.
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                for (int off = G >> 1; off > 0; off >>= 1)
+                    acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], off);
+            }
+            if (q == 0 && lr < nrows) {
+                const int64_t n = row - prob * p.N;
+                const bool bad = !row_ok;
+                if (bad) atomicOr(p.status, kDevBadExpert);
+#pragma unroll
+                for (int m = 0; m < M; ++m)
+                    p.y[(prob * M + m) * p.N + n] = bad ? __int_as_float(0x7fc00000) : acc[m] * T::kPrescale;
+            }
+#pragma unroll
+            for (int m = 0; m < M; ++m) acc[m] = 0.0f;
+        }
+    }
+
+    if (!alive) {
+        // A wait gave up: let every copy this warp issued land before the CTA
+        // (and its shared memory) goes away, each wait again bounded.
+        // Each slot holds at most one outstanding stage.
+        if (lane == 0) {
+            for (int64_t j = consumed; j < issued; ++j)
+                mbar_wait_bounded(&bars[j % S], static_cast<uint32_t>((j / S) & 1), nullptr);
+        }
+        __syncwarp();
+    }
+}
+
+// ---- the generic kernel (any K % 32 == 0, any M, activations from global) ----------
+
+template <int FMT>
+__global__ void __launch_bounds__(256) gemv_generic_kernel(const GemvParams p, int M)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int bb = FmtTraits<FMT>::kBlockBytes;
+    const int64_t nblk = p.K / 32;
+    pdl_wait_prior_grid();
+    for (int64_t row = gw; row < p.rows_total; row += nw) {
+        const int64_t prob = row / p.N;
+        const int64_t n = row - prob * p.N;
+        int64_t e = 0;
+        bool ok = true;
+        if (p.expert_idx) {
+            e = p.expert_idx[prob];
+            ok = (e >= 0 && e < p.n_experts);
+        }
+        for (int m0 = 0; m0 < M; m0 += 8) {
+            float acc[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+            if (ok) {
+                const uint8_t *wr = p.W + (e * p.N + n) * p.row_bytes;
+                for (int64_t b = lane; b < nblk; b += 32) {
+                    const uint8_t *blk = wr + b * bb;
+                    const float d = __half2float(__ushort_as_half(
+                        static_cast<unsigned short>(blk[0] | (blk[1] << 8))));
+                    for (int j = 0; j < 32; ++j) {
+                        int c;
+                        if (FMT == kQ4_0) c = (j < 16 ? (blk[2 + j] & 0xF) : (blk[2 + j - 16] >> 4)) - 8;
+                        else c = static_cast<int8_t>(blk[2 + j]);
+                        const float wv = static_cast<float>(c) * d;
+#pragma unroll
+                        for (int mm = 0; mm < 8; ++mm) {
+                            if (m0 + mm < M)
+                                acc[mm] = fmaf(wv, __half2float(p.x[(prob * M + m0 + mm) * p.K + b * 32 + j]), acc[mm]);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int mm = 0; mm < 8; ++mm)
+                for (int off = 16; off > 0; off >>= 1) acc[mm] += __shfl_xor_sync(0xffffffffu, acc[mm], off);
+            if (lane == 0) {
+                if (!ok) atomicOr(p.status, kDevBadExpert);
+                for (int mm = 0; mm < 8 && m0 + mm < M; ++mm)
+                    p.y[(prob * M + m0 + mm) * p.N + n] = ok ? acc[mm] : __int_as_float(0x7fc00000);
+            }
+        }
+    }
+}
+
+}  // namespace qmv

@@ -1,0 +1,42 @@
+// qmv_launch.h -- host-side launch hooks shared by the translation units of
+// the library (internal; the public interface is include/qmv.h).
+#pragma once
+
+#include <cstddef>
+#include <cuda_runtime.h>
+
+namespace qmv {
+
+struct GemvParams;
+
+// Streaming decode kernel for one format and token count M (1..8).
+cudaError_t launch_gemv_stream_q4_0(int M, const GemvParams &p, int grid, int warps, size_t smem,
+                                    cudaStream_t s, bool pdl);
+cudaError_t launch_gemv_stream_q8_0(int M, const GemvParams &p, int grid, int warps, size_t smem,
+                                    cudaStream_t s, bool pdl);
+// Generic kernel (any K % 32 == 0, activations read from global memory).
+cudaError_t launch_gemv_generic(int fmt, const GemvParams &p, int M, int grid, cudaStream_t s, bool pdl);
+
+// Opt a kernel into more than 48 KB of dynamic shared memory on the current
+// device (once per device).
+cudaError_t ensure_smem_optin(const void *func, size_t smem);
+
+// Launch `kernel` with optional programmatic dependent launch.
+template <typename Kernel, typename... Args>
+cudaError_t launch_ex(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                      Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+}  // namespace qmv
