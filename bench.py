@@ -261,6 +261,17 @@ def run_ours(args, dist, rank, local, world):
     # ---- per-shape us/call (graph of R back-to-back calls cycling copies) -------
     sweep = []
     pk = peaks()
+    def event_time_us(g, reps=1):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for _ in range(reps):
+                g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3
+
     for c in calls:
         R = max(64, 2 * c["copies"])
 
@@ -269,36 +280,22 @@ def run_ours(args, dist, rank, local, world):
                 W = c["W"][s % c["copies"]]
                 fn_ptr(W.data_ptr(), c["x"].data_ptr(), c["y"].data_ptr(), c["N"], c["K"], c["M"], sh)
 
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(g, stream=stream):
-                one_shape(0, R)
-        g.replay()
-        torch.cuda.synchronize()
-        best = None
-        for _ in range(5):
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            g.replay()
-            b.record(stream)
-            torch.cuda.synchronize()
-            t = a.elapsed_time(b) * 1e3 / R
-            best = t if best is None else min(best, t)
-        # and one isolated call (launch + ramp + drain), median of 20
-        iso = []
-        for i in range(20):
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            torch.cuda.synchronize()
-            a.record(stream)
-            one_shape(i, 1)
-            b.record(stream)
-            torch.cuda.synchronize()
-            iso.append(a.elapsed_time(b) * 1e3)
+        def cap(count):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                with torch.cuda.graph(g, stream=stream):
+                    one_shape(0, count)
+            return g
+
+        g = cap(R)
+        g1 = cap(1)
+        event_time_us(g)
+        best = min(event_time_us(g) / R for _ in range(5))
+        # one call on its own (graph launch + ramp + drain), median of 20
+        iso = statistics.median(event_time_us(g1) for _ in range(20))
         gbs = c["bytes"] / (best * 1e-6) / 1e9
         sweep.append({"N": c["N"], "K": c["K"], "M": c["M"], "copies": c["copies"],
-                      "us_per_call": round(best, 3), "us_isolated_call": round(statistics.median(iso), 3),
+                      "us_per_call": round(best, 3), "us_isolated_call": round(iso, 3),
                       "GBps": round(gbs, 1), "frac_of_measured_hbm": round(gbs / pk["hbm_gbs"], 4),
                       "frac_of_8TBps_spec": round(gbs / SPEC_HBM_GBS, 4)})
 
@@ -472,6 +469,30 @@ def run_reference(args, rank, world):
 
 
 # ---------------------------------------------------------------------------------
+def ncu_case(spec):
+    """A handful of eager calls of one shape over rotated copies larger than L2
+    (a small, bounded program for an Nsight Compute capture)."""
+    import torch
+    import weight_quantized_decode_gb300 as q
+    fmt, shape, M = spec.split(":")
+    N, K = (int(v) for v in shape.split("x"))
+    M = int(M)
+    dev = torch.device("cuda", 0)
+    bb = 18 if fmt == "q4_0" else 34
+    wbytes = N * (K // 32) * bb
+    copies = max(2, math.ceil(2.5 * 128e6 / wbytes))
+    base = torch.from_numpy(synth.weights(fmt, N, K, synth.seed_for(f"{fmt}_{N}x{K}"))).to(dev)
+    W = base.unsqueeze(0).repeat(copies, 1, 1)
+    x = torch.from_numpy(synth.activations(M, K, 1)).to(dev)
+    y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    fn = {"q4_0": q.qmv_q4_0_ptr, "q8_0": q.qmv_q8_0_ptr}[fmt]
+    s = torch.cuda.current_stream().cuda_stream
+    for i in range(8):
+        fn(W[i % copies].data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, s)
+    torch.cuda.synchronize()
+    print(f"ncu case {spec}: {copies} copies, 8 calls, ok")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -482,7 +503,12 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ncu-case", default=None,
+                    help="FMT:NxK:M -- only run a few eager calls of one shape (for Nsight Compute captures)")
     args = ap.parse_args()
+    if args.ncu_case:
+        ncu_case(args.ncu_case)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 

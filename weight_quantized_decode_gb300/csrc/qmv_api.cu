@@ -80,6 +80,7 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
 {
     Plan pl{false, 0, 8, 0};
     if (p.K % 256 != 0 || p.K == 0) return pl;
+    if (reinterpret_cast<uintptr_t>(p.x) % 16 != 0) return pl;   // staged with 16-byte loads
     const int64_t U = p.K / 256;
     if (U > (1 << 20)) return pl;
     p.U = static_cast<int>(U);

@@ -87,29 +87,39 @@ __host__ __device__ inline size_t gemv_smem_bytes(int fmt, int M, int n_problems
     return xbytes + ring + bars;
 }
 
-// Position, inside a block, of the code whose weight lands in permuted slot
-// `slot` (0..31) of the activation layout.  Even blocks of a unit start 2
-// bytes into a 32-bit word, so their first word is re-formed with a PRMT as
-// qs bytes (0, 1, 14, 15) [Q4_0] or (0, 1, 30, 31) [Q8_0].
+// Permuted activation layout.  Within a block, the activation of element e
+// (0..31) is stored at slot x_perm_slot(parity, e) (0..31), so that each
+// 16-byte group of slots lines up with the half2 pairs one unpacked 32-bit word
+// of codes produces.  Even blocks of a unit start 2 bytes into a 32-bit word,
+// so their first word is re-formed with a PRMT as qs bytes (0, 1, 14, 15)
+// [Q4_0] or (0, 1, 30, 31) [Q8_0]; the other words are aligned.
 template <int FMT>
-__device__ __forceinline__ int x_perm_source(int block_parity, int slot)
+__host__ __device__ __forceinline__ int x_perm_slot(int block_parity, int e)
 {
     if (FMT == kQ4_0) {
-        const int word = slot >> 3, s8 = slot & 7;
-        const int pair = s8 >> 1, second = s8 & 1;
-        const int bp = (pair & 1) + 2 * second;             // byte within the word
-        int qi;
-        if (block_parity) qi = 4 * word + bp;
-        else if (word == 0) qi = (bp < 2) ? bp : 12 + bp;   // 0, 1, 14, 15
-        else qi = 4 * word - 2 + bp;
-        return qi + ((pair >= 2) ? 16 : 0);
+        const int hi = e >= 16 ? 1 : 0;
+        const int qi = e - 16 * hi;             // qs byte index 0..15
+        int word, bp;
+        if (block_parity) { word = qi >> 2; bp = qi & 3; }
+        else if (qi < 2) { word = 0; bp = qi; }
+        else if (qi >= 14) { word = 0; bp = qi - 12; }
+        else { word = (qi + 2) >> 2; bp = (qi + 2) & 3; }
+        // unpack_q4_word pairs: 0 = (lo b0, lo b2), 1 = (lo b1, lo b3),
+        //                       2 = (hi b0, hi b2), 3 = (hi b1, hi b3)
+        const int pair = (bp & 1) + 2 * hi;
+        const int second = bp >> 1;
+        return word * 8 + pair * 2 + second;
     } else {
-        const int word = slot >> 2, s4 = slot & 3;
-        const int pair = s4 >> 1, second = s4 & 1;
-        const int bp = pair + 2 * second;
-        if (block_parity) return 4 * word + bp;
-        if (word == 0) return (bp < 2) ? bp : 28 + bp;       // 0, 1, 30, 31
-        return 4 * word - 2 + bp;
+        const int qi = e;
+        int word, bp;
+        if (block_parity) { word = qi >> 2; bp = qi & 3; }
+        else if (qi < 2) { word = 0; bp = qi; }
+        else if (qi >= 30) { word = 0; bp = qi - 28; }
+        else { word = (qi + 2) >> 2; bp = (qi + 2) & 3; }
+        // unpack_q8_word pairs: 0 = (b0, b2), 1 = (b1, b3)
+        const int pair = bp & 1;
+        const int second = bp >> 1;
+        return word * 4 + pair * 2 + second;
     }
 }
 
@@ -324,18 +334,25 @@ __global__ void __launch_bounds__(256, 1) gemv_stream_kernel(const GemvParams p)
         for (int64_t i = 0; i < prefetch; ++i) issue(i);
     }
 
-    // Stage the activations: permuted pair order, 528-byte padded units.
+    // Stage the activations: permuted pair order, 528-byte padded units.  Each
+    // thread moves 8 consecutive activations (one 16-byte load) per step.
     {
-        const int64_t nhalf = (prob_hi - prob_lo + 1) * M * U * 256;
-        for (int64_t d = threadIdx.x; d < nhalf; d += blockDim.x) {
-            const int64_t tok = d / (static_cast<int64_t>(U) * 256);   // local token index
-            const int rem = static_cast<int>(d - tok * U * 256);
-            const int blk = rem >> 5;      // block within the row of K
-            const int slot = rem & 31;
-            const int src_in_blk = x_perm_source<FMT>(blk & 1, slot);
-            const __half v = p.x[(prob_lo * M + tok) * p.K + blk * 32 + src_in_blk];
-            const size_t off = (static_cast<size_t>(tok) * U + (blk >> 3)) * kXUnitBytes + (blk & 7) * 64 + slot * 2;
-            *reinterpret_cast<__half *>(xs + off) = v;
+        const int64_t per_tok = static_cast<int64_t>(U) * 32;        // 16-byte groups per token
+        const int64_t nvec = (prob_hi - prob_lo + 1) * M * per_tok;
+        const uint4 *xsrc = reinterpret_cast<const uint4 *>(p.x + prob_lo * M * p.K);
+        for (int64_t v = threadIdx.x; v < nvec; v += blockDim.x) {
+            const int64_t tok = v / per_tok;
+            const int g = static_cast<int>(v - tok * per_tok);     // group within the token row
+            const uint4 val = xsrc[tok * (p.K / 8) + g];
+            const int blk = g >> 2;                                  // block within the row
+            const int e0 = (g & 3) * 8;                              // first element in the block
+            uint8_t *dst = xs + (static_cast<size_t>(tok) * U + (blk >> 3)) * kXUnitBytes + (blk & 7) * 64;
+            const uint32_t wv[4] = {val.x, val.y, val.z, val.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const unsigned short h = static_cast<unsigned short>(wv[i >> 1] >> (16 * (i & 1)));
+                *reinterpret_cast<unsigned short *>(dst + 2 * x_perm_slot<FMT>(blk & 1, e0 + i)) = h;
+            }
         }
     }
     __syncthreads();
