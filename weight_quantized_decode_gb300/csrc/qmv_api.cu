@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "../../include/qmv.h"
@@ -75,20 +76,58 @@ struct Plan {
     size_t smem;
 };
 
+// Launch-shape overrides for tuning sweeps: QMV_GEMV_TUNE="warps=16,stages=3,
+// G=8,SP=1,ctas=2" (any subset; 0 or absent = the built-in rule).
+struct Tune {
+    int warps = 0, stages = 0, G = 0, SP = 0, ctas = 0;
+};
+
+const Tune &tune_overrides()
+{
+    static Tune t;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        const char *env = std::getenv("QMV_GEMV_TUNE");
+        if (!env) return;
+        const char *c = env;
+        while (*c) {
+            char key[16] = {0};
+            int k = 0;
+            while (*c && *c != '=' && k < 15) key[k++] = *c++;
+            if (*c != '=') break;
+            ++c;
+            const int v = std::atoi(c);
+            while (*c && *c != ',') ++c;
+            if (*c == ',') ++c;
+            if (!std::strcmp(key, "warps")) t.warps = v;
+            else if (!std::strcmp(key, "stages")) t.stages = v;
+            else if (!std::strcmp(key, "G")) t.G = v;
+            else if (!std::strcmp(key, "SP")) t.SP = v;
+            else if (!std::strcmp(key, "ctas")) t.ctas = v;
+        }
+    });
+    return t;
+}
+
 // Choose the launch of the streaming kernel (or fall back to the generic one).
 Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
 {
     Plan pl{false, 0, 8, 0};
     if (p.K % 256 != 0 || p.K == 0) return pl;
     if (reinterpret_cast<uintptr_t>(p.x) % 16 != 0) return pl;   // staged with 16-byte loads
+    if (p.rows_total >= (int64_t(1) << 31)) return pl;             // 32-bit row indices
     const int64_t U = p.K / 256;
     if (U > (1 << 20)) return pl;
+    const Tune &tu = tune_overrides();
     p.U = static_cast<int>(U);
     p.G = lanes_per_row(p.U, M);
-    p.SP = 1;
+    if (tu.G == 1 || tu.G == 2 || tu.G == 4 || tu.G == 8 || tu.G == 16 || tu.G == 32) p.G = tu.G;
+    p.SP = (tu.SP >= 1 && tu.SP <= 7 && (tu.SP & 1)) ? tu.SP : 1;
     const int RG = 32 / p.G;
+    const int ctas_per_sm = (tu.ctas >= 1 && tu.ctas <= 4) ? tu.ctas : 1;
     const int64_t groups = (p.rows_total + RG - 1) / RG;
-    int grid = static_cast<int>(groups < sms ? groups : sms);
+    const int64_t max_grid = static_cast<int64_t>(sms) * ctas_per_sm;
+    int grid = static_cast<int>(groups < max_grid ? groups : max_grid);
     if (grid < 1) grid = 1;
     const int64_t rows_per_cta = (p.rows_total + grid - 1) / grid;
     int64_t pmax = (rows_per_cta + p.N - 1) / p.N + 1;
@@ -96,12 +135,21 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
     p.max_local_problems = static_cast<int>(pmax);
     const int unit_bytes = fmt == kQ4_0 ? 144 : 272;
     const size_t xbytes = static_cast<size_t>(pmax) * M * p.U * kXUnitBytes;
-    const size_t budget = static_cast<size_t>(smem_optin) - 1024;
+    const size_t budget = static_cast<size_t>(smem_optin) / ctas_per_sm - 1024;
     if (xbytes + 8 * 1024 > budget) return pl;
-    for (int warps : {8, 4}) {
+    const int max_warps = (M <= 2) ? 16 : 8;
+    int warp_choices[2] = {8, 4};
+    int nchoices = 2;
+    if (tu.warps >= 1 && tu.warps <= max_warps) {
+        warp_choices[0] = tu.warps;
+        nchoices = 1;
+    }
+    for (int wi = 0; wi < nchoices; ++wi) {
+        const int warps = warp_choices[wi];
         const size_t per_stage = static_cast<size_t>(warps) * (32 * p.SP * unit_bytes + 8);
         int S = static_cast<int>((budget - xbytes) / per_stage);
         if (S > 6) S = 6;
+        if (tu.stages >= 2 && tu.stages < S) S = tu.stages;
         if (S >= 2) {
             p.S = S;
             pl.streaming = true;

@@ -160,9 +160,14 @@ __device__ __forceinline__ void dot_unit_q4_0(const uint8_t *wsrc, const uint8_t
             q[3] = w[9 * h + 8];
         }
         const float d = half_lo_to_float(dsrc);
-        __half2 hacc[M];
+        // Two independent half2 chains per token (words 0-1 and 2-3), joined
+        // in fp32: shorter dependency chains, each half sums 8 products.
+        __half2 ha[M], hb[M];
 #pragma unroll
-        for (int m = 0; m < M; ++m) hacc[m] = __float2half2_rn(0.0f);
+        for (int m = 0; m < M; ++m) {
+            ha[m] = __float2half2_rn(0.0f);
+            hb[m] = __float2half2_rn(0.0f);
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             __half2 wv[4];
@@ -170,16 +175,18 @@ __device__ __forceinline__ void dot_unit_q4_0(const uint8_t *wsrc, const uint8_t
 #pragma unroll
             for (int m = 0; m < M; ++m) {
                 const uint4 xv = *reinterpret_cast<const uint4 *>(xsrc + m * xstride + b * 64 + j * 16);
-                hacc[m] = __hfma2(wv[0], as_h2(xv.x), hacc[m]);
-                hacc[m] = __hfma2(wv[1], as_h2(xv.y), hacc[m]);
-                hacc[m] = __hfma2(wv[2], as_h2(xv.z), hacc[m]);
-                hacc[m] = __hfma2(wv[3], as_h2(xv.w), hacc[m]);
+                __half2 &h = (j < 2) ? ha[m] : hb[m];
+                h = __hfma2(wv[0], as_h2(xv.x), h);
+                h = __hfma2(wv[1], as_h2(xv.y), h);
+                h = __hfma2(wv[2], as_h2(xv.z), h);
+                h = __hfma2(wv[3], as_h2(xv.w), h);
             }
         }
 #pragma unroll
         for (int m = 0; m < M; ++m) {
-            const float2 f = __half22float2(hacc[m]);
-            acc[m] = fmaf(d, f.x + f.y, acc[m]);
+            const float2 fa = __half22float2(ha[m]);
+            const float2 fb = __half22float2(hb[m]);
+            acc[m] = fmaf(d, (fa.x + fa.y) + (fb.x + fb.y), acc[m]);
         }
     }
 }
@@ -213,9 +220,12 @@ __device__ __forceinline__ void dot_unit_q8_0(const uint8_t *wsrc, const uint8_t
             for (int j = 0; j < 8; ++j) q[j] = w[17 * h + 9 + j];
         }
         const float d = half_lo_to_float(dsrc);
-        __half2 hacc[M];
+        __half2 ha[M], hb[M];
 #pragma unroll
-        for (int m = 0; m < M; ++m) hacc[m] = __float2half2_rn(0.0f);
+        for (int m = 0; m < M; ++m) {
+            ha[m] = __float2half2_rn(0.0f);
+            hb[m] = __float2half2_rn(0.0f);
+        }
 #pragma unroll
         for (int j = 0; j < 8; j += 2) {
             __half2 wa[2], wb[2];
@@ -224,24 +234,26 @@ __device__ __forceinline__ void dot_unit_q8_0(const uint8_t *wsrc, const uint8_t
 #pragma unroll
             for (int m = 0; m < M; ++m) {
                 const uint4 xv = *reinterpret_cast<const uint4 *>(xsrc + m * xstride + b * 64 + j * 8);
-                hacc[m] = __hfma2(wa[0], as_h2(xv.x), hacc[m]);
-                hacc[m] = __hfma2(wa[1], as_h2(xv.y), hacc[m]);
-                hacc[m] = __hfma2(wb[0], as_h2(xv.z), hacc[m]);
-                hacc[m] = __hfma2(wb[1], as_h2(xv.w), hacc[m]);
+                __half2 &h = (j < 4) ? ha[m] : hb[m];
+                h = __hfma2(wa[0], as_h2(xv.x), h);
+                h = __hfma2(wa[1], as_h2(xv.y), h);
+                h = __hfma2(wb[0], as_h2(xv.z), h);
+                h = __hfma2(wb[1], as_h2(xv.w), h);
             }
         }
 #pragma unroll
         for (int m = 0; m < M; ++m) {
-            const float2 f = __half22float2(hacc[m]);
-            acc[m] = fmaf(d, f.x + f.y, acc[m]);
+            const float2 fa = __half22float2(ha[m]);
+            const float2 fb = __half22float2(hb[m]);
+            acc[m] = fmaf(d, (fa.x + fa.y) + (fb.x + fb.y), acc[m]);
         }
     }
 }
 
 // ---- the streaming kernel ----------------------------------------------------------
 
-template <int FMT, int M>
-__global__ void __launch_bounds__(256, 1) gemv_stream_kernel(const GemvParams p)
+template <int FMT, int M, int MAXT>
+__global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p)
 {
     using T = FmtTraits<FMT>;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -251,6 +263,8 @@ __global__ void __launch_bounds__(256, 1) gemv_stream_kernel(const GemvParams p)
     const int warps = blockDim.x >> 5;
     const int U = p.U, G = p.G, SP = p.SP, S = p.S;
     const int RG = 32 / G;
+    // Row indices fit in 32 bits (checked on the host).
+    const uint32_t N = static_cast<uint32_t>(p.N);
 
     // Shared-memory carve-up: activations, then per-warp rings, then barriers.
     const size_t xbytes = static_cast<size_t>(p.max_local_problems) * M * U * kXUnitBytes;
@@ -261,18 +275,19 @@ __global__ void __launch_bounds__(256, 1) gemv_stream_kernel(const GemvParams p)
                      warp * S;
 
     // This CTA's contiguous range of (problem, row) pairs.
-    const int64_t R = p.rows_total;
-    const int64_t row0 = (R * blockIdx.x) / gridDim.x;
-    const int64_t row1 = (R * (blockIdx.x + 1)) / gridDim.x;
-    const int64_t nrows = row1 - row0;
+    const uint32_t R = static_cast<uint32_t>(p.rows_total);
+    const uint32_t row0 = static_cast<uint32_t>((static_cast<uint64_t>(R) * blockIdx.x) / gridDim.x);
+    const uint32_t row1 = static_cast<uint32_t>((static_cast<uint64_t>(R) * (blockIdx.x + 1)) / gridDim.x);
+    const int nrows = static_cast<int>(row1 - row0);
     // Problems (tokens of the plain GEMV, or expert slots) this CTA touches.
-    const int64_t prob_lo = nrows > 0 ? row0 / p.N : 0;
-    const int64_t prob_hi = nrows > 0 ? (row1 - 1) / p.N : -1;
-    const int64_t ngroups = (nrows + RG - 1) / RG;
-    const int64_t my_groups = (ngroups > warp) ? (ngroups - warp + warps - 1) / warps : 0;
+    const int prob_lo = nrows > 0 ? static_cast<int>(row0 / N) : 0;
+    const int prob_hi = nrows > 0 ? static_cast<int>((row1 - 1) / N) : -1;
+    const int ngroups = (nrows + RG - 1) / RG;
+    const int my_groups = (ngroups > warp) ? (ngroups - warp + warps - 1) / warps : 0;
     const int units_per_stage = SP * G;
     const int T_stages = (U + units_per_stage - 1) / units_per_stage;
-    const int64_t total = my_groups * T_stages;
+    const int total = my_groups * T_stages;
+    const uint32_t lane_chunk_bytes = static_cast<uint32_t>(units_per_stage) * T::kUnitBytes;
 
     if (lane == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
@@ -280,72 +295,75 @@ __global__ void __launch_bounds__(256, 1) gemv_stream_kernel(const GemvParams p)
     }
     __syncwarp();
 
-    int64_t issued = 0;     // stages whose copies have been requested
-    int64_t consumed = 0;   // stages waited for successfully
+    // ---- copy issue: stages are requested strictly in order ----------------------
+    int issued = 0;          // stages requested
+    int is_slot = 0;         // slot of the next stage to request
+    int is_t = 0;            // its stage index within the row group
+    int is_g = warp;         // its row group (CTA-local)
+    // Lane r < RG requests row r of the group; cached per group.
+    const uint8_t *is_row = nullptr;
 
-    // Lane `r` (< RG) requests row r of the group's chunk for stage i.
-    auto issue = [&](int64_t i) {
-        ++issued;
-        const int slot = static_cast<int>(i % S);
-        const int64_t g = warp + (i / T_stages) * warps;
-        const int t = static_cast<int>(i % T_stages);
-        const int u0 = t * units_per_stage;
-        const int u1 = min(U, u0 + units_per_stage);
-        const uint32_t chunk = static_cast<uint32_t>(u1 - u0) * T::kUnitBytes;
-        uint32_t my_bytes = 0;
-        const uint8_t *src = nullptr;
-        if (lane < RG) {
-            const int64_t lr = g * RG + lane;
-            if (lr < nrows) {
-                const int64_t row = row0 + lr;
-                const int64_t prob = row / p.N;
-                const int64_t n = row - prob * p.N;
+    auto issue_next = [&]() {
+        if (is_t == 0) {
+            is_row = nullptr;
+            const int lr = is_g * RG + lane;
+            if (lane < RG && lr < nrows) {
+                const uint32_t row = row0 + lr;
+                uint32_t prob = 0, n = row;
+                if (p.n_problems > 1) {
+                    prob = row / N;
+                    n = row - prob * N;
+                }
                 int64_t e = 0;
                 bool ok = true;
                 if (p.expert_idx) {
                     e = p.expert_idx[prob];
                     ok = (e >= 0 && e < p.n_experts);
                 }
-                if (ok) {
-                    src = p.W + (e * p.N + n) * p.row_bytes + static_cast<int64_t>(u0) * T::kUnitBytes;
-                    my_bytes = chunk;
-                }
+                if (ok) is_row = p.W + (e * p.N + n) * p.row_bytes;
             }
         }
+        const int u0 = is_t * units_per_stage;
+        const int u1 = min(U, u0 + units_per_stage);
+        const uint32_t my_bytes = is_row ? static_cast<uint32_t>(u1 - u0) * T::kUnitBytes : 0u;
         const uint32_t total_bytes = __reduce_add_sync(0xffffffffu, my_bytes);
-        if (lane == 0) mbar_arrive_expect_tx(&bars[slot], total_bytes);
+        if (lane == 0) mbar_arrive_expect_tx(&bars[is_slot], total_bytes);
         __syncwarp();
-        if (my_bytes) bulk_g2s(ring + static_cast<size_t>(slot) * slot_bytes + lane * (units_per_stage * T::kUnitBytes),
-                               src, my_bytes, &bars[slot]);
+        if (my_bytes)
+            bulk_g2s(ring + static_cast<size_t>(is_slot) * slot_bytes + lane * lane_chunk_bytes,
+                     is_row + static_cast<size_t>(u0) * T::kUnitBytes, my_bytes, &bars[is_slot]);
+        ++issued;
+        if (++is_slot == S) is_slot = 0;
+        if (++is_t == T_stages) {
+            is_t = 0;
+            is_g += warps;
+        }
     };
 
-    // Request the first stages before waiting for the previous kernel: W is
-    // never written by it.
-    const int64_t prefetch = total < S ? total : S;
-    // The expert indices may be produced by the previous kernel: only a plain
-    // GEMV prefetches before the dependency wait.
-    if (!p.expert_idx) {
-        for (int64_t i = 0; i < prefetch; ++i) issue(i);
-    }
+    // Request the first stages before waiting for the previous kernel (W is
+    // never written by it).  The expert indices may be, so the multi-expert
+    // call waits first.
+    const int prefetch = total < S ? total : S;
+    if (!p.expert_idx)
+        for (int i = 0; i < prefetch; ++i) issue_next();
 
     pdl_wait_prior_grid();
 
-    if (p.expert_idx) {
-        for (int64_t i = 0; i < prefetch; ++i) issue(i);
-    }
+    if (p.expert_idx)
+        for (int i = 0; i < prefetch; ++i) issue_next();
 
     // Stage the activations: permuted pair order, 528-byte padded units.  Each
     // thread moves 8 consecutive activations (one 16-byte load) per step.
     {
-        const int64_t per_tok = static_cast<int64_t>(U) * 32;        // 16-byte groups per token
-        const int64_t nvec = (prob_hi - prob_lo + 1) * M * per_tok;
-        const uint4 *xsrc = reinterpret_cast<const uint4 *>(p.x + prob_lo * M * p.K);
-        for (int64_t v = threadIdx.x; v < nvec; v += blockDim.x) {
-            const int64_t tok = v / per_tok;
-            const int g = static_cast<int>(v - tok * per_tok);     // group within the token row
-            const uint4 val = xsrc[tok * (p.K / 8) + g];
-            const int blk = g >> 2;                                  // block within the row
-            const int e0 = (g & 3) * 8;                              // first element in the block
+        const int per_tok = U * 32;        // 16-byte groups per token
+        const int nvec = (prob_hi - prob_lo + 1) * M * per_tok;
+        const uint4 *xsrc = reinterpret_cast<const uint4 *>(p.x + static_cast<int64_t>(prob_lo) * M * p.K);
+        for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+            const int tok = v / per_tok;
+            const int g = v - tok * per_tok;                          // group within the token row
+            const uint4 val = xsrc[static_cast<int64_t>(tok) * (p.K / 8) + g];
+            const int blk = g >> 2;                                    // block within the row
+            const int e0 = (g & 3) * 8;                                // first element in the block
             uint8_t *dst = xs + (static_cast<size_t>(tok) * U + (blk >> 3)) * kXUnitBytes + (blk & 7) * 64;
             const uint32_t wv[4] = {val.x, val.y, val.z, val.w};
 #pragma unroll
@@ -359,57 +377,65 @@ __global__ void __launch_bounds__(256, 1) gemv_stream_kernel(const GemvParams p)
     pdl_allow_next_grid();
 
     const int r = lane / G;
-    const int q = lane % G;
+    const int q = lane - r * G;
     const int xstride = U * kXUnitBytes;     // bytes between tokens of a problem
     float acc[M];
 #pragma unroll
     for (int m = 0; m < M; ++m) acc[m] = 0.0f;
 
     bool alive = true;
-    int64_t lr = 0, row = 0, prob = 0;
+    int consumed = 0;
+    int slot = 0;
+    uint32_t phase = 0;
+    int t = 0;
+    int g = warp;
+    int lr = 0;
+    uint32_t row = 0, prob = 0;
     bool row_ok = false;
+    const uint8_t *xrow = xs;
 
-    for (int64_t i = 0; i < total; ++i) {
-        const int slot = static_cast<int>(i % S);
-        const uint32_t parity = static_cast<uint32_t>((i / S) & 1);
-        const int64_t g = warp + (i / T_stages) * warps;
-        const int t = static_cast<int>(i % T_stages);
+    for (int i = 0; i < total; ++i) {
         if (t == 0) {
             lr = g * RG + r;
             row_ok = lr < nrows;
             row = row0 + lr;
-            prob = row_ok ? row / p.N : 0;
+            prob = 0;
+            if (row_ok && p.n_problems > 1) prob = row / N;
             if (row_ok && p.expert_idx) {
                 const int64_t e = p.expert_idx[prob];
                 row_ok = (e >= 0 && e < p.n_experts);
             }
+            xrow = xs + static_cast<size_t>(prob - prob_lo) * M * xstride;
         }
-        if (!mbar_wait_warp(&bars[slot], parity, p.status)) {
+        if (!mbar_wait_warp(&bars[slot], phase, p.status)) {
             alive = false;
             break;
         }
         consumed = i + 1;
-        const uint8_t *stage = ring + static_cast<size_t>(slot) * slot_bytes + r * (units_per_stage * T::kUnitBytes);
+        const uint8_t *stage = ring + static_cast<size_t>(slot) * slot_bytes + r * lane_chunk_bytes;
         const int u0 = t * units_per_stage;
         if (row_ok) {
-            const uint8_t *xrow = xs + static_cast<size_t>(prob - prob_lo) * M * xstride;
             for (int pass = 0; pass < SP; ++pass) {
                 const int ul = pass * G + q;          // unit within the stage
                 const int u = u0 + ul;
                 if (u < U) {
                     if (FMT == kQ4_0)
-                        dot_unit_q4_0<M>(stage + ul * T::kUnitBytes, xrow + static_cast<size_t>(u) * kXUnitBytes,
-                                         xstride, acc);
+                        dot_unit_q4_0<M>(stage + ul * T::kUnitBytes, xrow + u * kXUnitBytes, xstride, acc);
                     else
-                        dot_unit_q8_0<M>(stage + ul * T::kUnitBytes, xrow + static_cast<size_t>(u) * kXUnitBytes,
-                                         xstride, acc);
+                        dot_unit_q8_0<M>(stage + ul * T::kUnitBytes, xrow + u * kXUnitBytes, xstride, acc);
                 }
             }
         }
         __syncwarp();
-        if (i + S < total) issue(i + S);
+        if (issued < total) issue_next();
 
-        if (t == T_stages - 1) {
+        if (++slot == S) {
+            slot = 0;
+            phase ^= 1u;
+        }
+        if (++t == T_stages) {
+            t = 0;
+            g += warps;
             // Combine the G partial sums of each row.
 #pragma unroll
             for (int m = 0; m < M; ++m) {
@@ -417,12 +443,13 @@ __global__ void __launch_bounds__(256, 1) gemv_stream_kernel(const GemvParams p)
                     acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], off);
             }
             if (q == 0 && lr < nrows) {
-                const int64_t n = row - prob * p.N;
+                const uint32_t n = row - prob * N;
                 const bool bad = !row_ok;
                 if (bad) atomicOr(p.status, kDevBadExpert);
 #pragma unroll
                 for (int m = 0; m < M; ++m)
-                    p.y[(prob * M + m) * p.N + n] = bad ? __int_as_float(0x7fc00000) : acc[m] * T::kPrescale;
+                    p.y[(static_cast<int64_t>(prob) * M + m) * p.N + n] =
+                        bad ? __int_as_float(0x7fc00000) : acc[m] * T::kPrescale;
             }
 #pragma unroll
             for (int m = 0; m < M; ++m) acc[m] = 0.0f;
@@ -430,11 +457,11 @@ __global__ void __launch_bounds__(256, 1) gemv_stream_kernel(const GemvParams p)
     }
 
     if (!alive) {
-        // A wait gave up: let every copy this warp issued land before the CTA
-        // (and its shared memory) goes away, each wait again bounded.
+        // A wait gave up: let every copy this warp requested land before the
+        // CTA (and its shared memory) goes away; each wait is bounded again.
         // Each slot holds at most one outstanding stage.
         if (lane == 0) {
-            for (int64_t j = consumed; j < issued; ++j)
+            for (int j = consumed; j < issued; ++j)
                 mbar_wait_bounded(&bars[j % S], static_cast<uint32_t>((j / S) & 1), nullptr);
         }
         __syncwarp();

@@ -4,13 +4,25 @@
 
 namespace qmv {
 
-template <int M>
-static cudaError_t launch_one(const GemvParams &p, int grid, int warps, size_t smem, cudaStream_t s, bool pdl)
+template <int M, int MAXT>
+static cudaError_t launch_t(const GemvParams &p, int grid, int warps, size_t smem, cudaStream_t s, bool pdl)
 {
-    auto kernel = gemv_stream_kernel<kQ4_0, M>;
+    auto kernel = gemv_stream_kernel<kQ4_0, M, MAXT>;
     cudaError_t e = ensure_smem_optin(reinterpret_cast<const void *>(kernel), smem);
     if (e != cudaSuccess) return e;
     return launch_ex(kernel, dim3(grid), dim3(warps * 32), smem, s, pdl, p);
+}
+
+// Up to 8 warps per CTA for every token count; up to 16 (at most 128
+// registers a thread) for one or two tokens.
+template <int M>
+static cudaError_t launch_one(const GemvParams &p, int grid, int warps, size_t smem, cudaStream_t s, bool pdl)
+{
+    if (warps <= 8) return launch_t<M, 256>(p, grid, warps, smem, s, pdl);
+    if constexpr (M <= 2) {
+        if (warps <= 16) return launch_t<M, 512>(p, grid, warps, smem, s, pdl);
+    }
+    return cudaErrorInvalidConfiguration;
 }
 
 cudaError_t launch_gemv_stream_q4_0(int M, const GemvParams &p, int grid, int warps, size_t smem, cudaStream_t s,

@@ -1,14 +1,470 @@
-// qmv_prefill.cu -- Q4_0 prefill GEMM on the 5th-generation tensor cores.
+// qmv_prefill.cu -- Q4_0 prefill GEMM on the 5th-generation tensor cores
+// (tcgen05.mma with fp32 accumulators in tensor memory), sm_103a.
+//
+//   y[m][n] = sum_k x[m][k] * w[n][k]     (many tokens m; W in GGUF Q4_0)
+//
+// Prior art on the pages: "tc_q4: ours, tensor cores for prompts: unpack a tile
+// to shared memory, WMMA 16x16x16" (volta-kernel-bakeoff, "What's in the
+// race"), and the Marlin-style plan of "What we'd do next" item 3 ("unpack
+// quantized weights inside a tensor-core multiply").  The GB300 form:
+//
+//   * One CTA computes a 128-row (weights) x TN-column (tokens) tile of y^T in
+//     tensor memory: weights are the MMA's M side (128 lanes), tokens its N
+//     side (TN <= 256 columns of fp32).
+//   * Warp 4 (producer) streams packed 128-row x 256-K Q4_0 tiles (144 bytes
+//     per row) and 64-K activation tiles with TMA tensor copies into
+//     shared-memory rings; the activation tiles land in the 128-byte-swizzled
+//     K-major layout the tensor core reads.
+//   * Warps 0-3 (one thread per weight row) dequantise a packed row into fp16
+//     with the 0x6400|n bit trick, w = (c - 8) * d, and write 64-K slices of
+//     the A operand in the same swizzled layout.
+//   * Warp 5 allocates tensor memory and one thread issues tcgen05.mma
+//     (kind::f16, 128 x TN x 16) four times per 64-K slice; tcgen05.commit
+//     releases the slice's buffers and finally signals the epilogue.
+//   * Warps 0-3 read the accumulator with tcgen05.ld (32 lanes x 32 columns
+//     per instruction) and store y with coalesced fp32 stores.
+// Operands are fp16: the activations arrive as fp16 and the dequantised
+// weight (c - 8) * d is rounded once to fp16.  Every wait is bounded.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "qmv_common.cuh"
+#include "qmv_launch.h"
 #include "qmv_prefill.h"
 
 namespace qmv {
 
-bool prefill_supported(int64_t, int64_t, int64_t) { return false; }
+namespace {
 
-cudaError_t launch_prefill(const void *, const void *, float *, int64_t, int64_t, int64_t, int, int *,
-                           cudaStream_t)
+constexpr int kBM = 128;                 // weight rows per tile (MMA M)
+constexpr int kKB = 64;                  // K per MMA slice (one 128-byte swizzle atom of fp16)
+constexpr int kKChunk = 256;             // K per packed weight tile (8 Q4_0 blocks = 144 bytes per row)
+constexpr int kPackedRowBytes = 144;
+constexpr int kPackedTileBytes = kBM * kPackedRowBytes;    // 18432
+constexpr int kATileBytes = kBM * kKB * 2;                 // 16384
+constexpr int kThreads = 192;
+
+struct PrefillParams {
+    float *y;
+    int *status;
+    int64_t N, K, M;
+    int TN;            // token columns per tile (multiple of 32, <= 256)
+    int SA;            // stages of (A, B) slices
+    uint32_t tmem_cols;
+};
+
+// ---- tcgen05 / TMA wrappers -------------------------------------------------------
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar)
 {
-    return cudaErrorNotSupported;
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (the canonical layout a TMA SWIZZLE_128B box produces).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFF);
+    d |= static_cast<uint64_t>(1) << 16;                 // leading byte offset (unused for this layout)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;         // stride byte offset: 8 rows x 128 bytes
+    d |= static_cast<uint64_t>(1) << 46;                 // descriptor version for sm_100 family
+    d |= static_cast<uint64_t>(2) << 61;                 // SWIZZLE_128B
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B (K-major), fp32 accumulator,
+// M = 128, N = tn.
+__host__ __device__ __forceinline__ uint32_t f16_idesc(int tn)
+{
+    return (1u << 4)                                   // D format: f32
+           | (0u << 7) | (0u << 10)                    // A, B format: f16
+           | (static_cast<uint32_t>(tn >> 3) << 17)    // N / 8
+           | (static_cast<uint32_t>(kBM >> 4) << 24);  // M / 16
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        bool accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate ? 1 : 0)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&v)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+          "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Bounded wait that also gives up when another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *status)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicOr(status, kDevTimeout);
+            return false;
+        }
+    }
+}
+
+// Dequantise one 32-weight Q4_0 block (scale bits `dbits`, codes in 4 aligned
+// words q[0..3] = qs[0..15]) into 32 fp16 weights in natural K order:
+// out[0..3] = elements 0..7, out[4..7] = 8..15, out[8..11] = 16..23,
+// out[12..15] = 24..31 (each entry a half2 of consecutive elements).
+__device__ __forceinline__ void dequant_block_f16(uint32_t dbits, const uint32_t (&q)[4], uint32_t (&out)[16])
+{
+    const __half d = __ushort_as_half(static_cast<unsigned short>(dbits));
+    const __half2 d2 = __halves2half2(d, d);
+    const uint32_t magic = 0x64006400u;
+    const __half2 c1032 = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));  // 1032
+    const __half2 s16 = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));    // 1/16
+    const __half2 m72 = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));    // -72
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t t01 = __byte_perm(q[i], 0u, 0x4140);   // (b0, b1) in the low bytes of two halves
+        const uint32_t t23 = __byte_perm(q[i], 0u, 0x4342);   // (b2, b3)
+        const __half2 lo01 = __hsub2(as_h2(and_or(t01, 0x000F000Fu, magic)), c1032);      // c - 8, exact
+        const __half2 lo23 = __hsub2(as_h2(and_or(t23, 0x000F000Fu, magic)), c1032);
+        const __half2 hi01 = __hfma2(as_h2(and_or(t01, 0x00F000F0u, magic)), s16, m72);   // c - 8, exact
+        const __half2 hi23 = __hfma2(as_h2(and_or(t23, 0x00F000F0u, magic)), s16, m72);
+        const __half2 a = __hmul2(lo01, d2), b = __hmul2(lo23, d2);
+        const __half2 c = __hmul2(hi01, d2), e = __hmul2(hi23, d2);
+        // word i holds qs[4i..4i+3]: elements 4i..4i+3 (low) and 16+4i..16+4i+3 (high)
+        out[2 * i] = *reinterpret_cast<const uint32_t *>(&a);
+        out[2 * i + 1] = *reinterpret_cast<const uint32_t *>(&b);
+        out[8 + 2 * i] = *reinterpret_cast<const uint32_t *>(&c);
+        out[8 + 2 * i + 1] = *reinterpret_cast<const uint32_t *>(&e);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
+                   const PrefillParams p)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1024-byte alignment of the operand tiles (required by the 128-byte swizzle).
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    const int SA = p.SA, TN = p.TN;
+    const int b_tile_bytes = TN * kKB * 2;
+    uint8_t *a_tiles = smem;
+    uint8_t *b_tiles = a_tiles + SA * kATileBytes;
+    uint8_t *w_tiles = b_tiles + SA * b_tile_bytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(w_tiles + 2 * kPackedTileBytes);
+    uint64_t *wfull = bars;            // [2]
+    uint64_t *wempty = bars + 2;       // [2]
+    uint64_t *bfull = bars + 4;        // [SA]
+    uint64_t *afull = bfull + SA;      // [SA]
+    uint64_t *abempty = afull + SA;    // [SA]
+    uint64_t *accfull = abempty + SA;  // [1]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accfull + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kBM;
+    const int64_t m0 = static_cast<int64_t>(blockIdx.y) * TN;
+    const int nK = static_cast<int>(p.K / kKB);            // 64-K slices
+    const int nC = static_cast<int>(p.K / kKChunk);        // packed 256-K tiles
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&wfull[i], 1);
+            mbar_init(&wempty[i], 4);
+        }
+        for (int s = 0; s < SA; ++s) {
+            mbar_init(&bfull[s], 1);
+            mbar_init(&afull[s], 4);
+            mbar_init(&abempty[s], 1);
+        }
+        mbar_init(accfull, 1);
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    if (warp == 5) tmem_alloc(tmem_slot, p.tmem_cols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 4) {
+        // ---------------- producer: TMA tensor copies ----------------
+        if (lane == 0) {
+            pdl_wait_prior_grid();
+            int issued_w = 0, issued_b = 0;
+            bool ok = true;
+            auto load_w = [&](int c) {
+                const int slot = c & 1;
+                if (!wait_or_abort(&wempty[slot], ((c >> 1) & 1) ^ 1, abort_flag, p.status)) return false;
+                mbar_arrive_expect_tx(&wfull[slot], kPackedTileBytes);
+                tma_load_2d(w_tiles + slot * kPackedTileBytes, &wmap, c * kPackedRowBytes, static_cast<int>(n0),
+                            &wfull[slot]);
+                ++issued_w;
+                return true;
+            };
+            if (nC > 0) ok = load_w(0);
+            if (ok && nC > 1) ok = load_w(1);
+            for (int j = 0; ok && j < nK; ++j) {
+                const int s = j % SA;
+                if (!wait_or_abort(&abempty[s], ((j / SA) & 1) ^ 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&bfull[s], b_tile_bytes);
+                tma_load_2d(b_tiles + s * b_tile_bytes, &xmap, j * kKB, static_cast<int>(m0), &bfull[s]);
+                ++issued_b;
+                // Two packed tiles ahead: chunk j/4 + 2 reuses the slot of chunk
+                // j/4, whose rows the dequantising warps read at its start.
+                if (j % 4 == 3 && j / 4 + 2 < nC) ok = load_w(j / 4 + 2);
+            }
+            if (!ok) {
+                // Let the copies already requested land before the CTA exits.
+                for (int c = 0; c < issued_w; ++c)
+                    mbar_wait_bounded(&wfull[c & 1], (c >> 1) & 1, nullptr);
+                for (int j = (issued_b > SA ? issued_b - SA : 0); j < issued_b; ++j)
+                    mbar_wait_bounded(&bfull[j % SA], (j / SA) & 1, nullptr);
+            }
+        }
+    } else if (warp == 5) {
+        // ---------------- MMA issue: one thread ----------------
+        if (lane == 0) {
+            const uint32_t idesc = f16_idesc(TN);
+            bool ok = true;
+            int committed = 0;
+            for (int j = 0; j < nK; ++j) {
+                const int s = j % SA;
+                const uint32_t par = (j / SA) & 1;
+                if (!wait_or_abort(&afull[s], par, abort_flag, p.status) ||
+                    !wait_or_abort(&bfull[s], par, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(a_tiles + s * kATileBytes);
+                const uint32_t b0 = smem_u32(b_tiles + s * b_tile_bytes);
+#pragma unroll
+                for (int kk = 0; kk < kKB / 16; ++kk)
+                    mma_f16(tmem_base, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc, (j | kk) != 0);
+                mma_commit(&abempty[s]);
+                ++committed;
+            }
+            mma_commit(accfull);
+            if (!ok && committed > 0) mbar_wait_bounded(accfull, 0, nullptr);
+        }
+    } else {
+        // ---------------- warps 0-3: dequantise, then the epilogue ----------------
+        const int r = threadIdx.x;                // weight row within the tile
+        bool ok = true;
+        for (int c = 0; ok && c < nC; ++c) {
+            const int slot = c & 1;
+            if (lane == 0) ok = wait_or_abort(&wfull[slot], (c >> 1) & 1, abort_flag, p.status);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) break;
+            while (!mbar_try_wait(&wfull[slot], (c >> 1) & 1)) {
+            }
+            uint32_t w[36];
+            const uint8_t *src = w_tiles + slot * kPackedTileBytes + r * kPackedRowBytes;
+#pragma unroll
+            for (int i = 0; i < 9; ++i) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(src + 16 * i);
+                w[4 * i] = v.x;
+                w[4 * i + 1] = v.y;
+                w[4 * i + 2] = v.z;
+                w[4 * i + 3] = v.w;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&wempty[slot]);
+#pragma unroll
+            for (int sub = 0; sub < 4; ++sub) {
+                const int j = c * 4 + sub;
+                const int s = j % SA;
+                if (lane == 0) ok = wait_or_abort(&abempty[s], ((j / SA) & 1) ^ 1, abort_flag, p.status);
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (!ok) break;
+                while (!mbar_try_wait(&abempty[s], ((j / SA) & 1) ^ 1)) {
+                }
+                // blocks 2*sub (even: starts 2 bytes into word 9*sub) and 2*sub+1
+                const int h = 9 * sub;
+                uint32_t qe[4], qo[4], fe[16], fo[16];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    qe[i] = __byte_perm(w[h + i], w[h + i + 1], 0x5432);
+                    qo[i] = w[h + 5 + i];
+                }
+                dequant_block_f16(w[h] & 0xffffu, qe, fe);
+                dequant_block_f16(w[h + 4] >> 16, qo, fo);
+                uint8_t *arow = a_tiles + s * kATileBytes + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    const uint32_t *f = (ch < 4) ? &fe[4 * ch] : &fo[4 * (ch - 4)];
+                    *reinterpret_cast<uint4 *>(arow + ((ch ^ (r & 7)) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&afull[s]);
+            }
+        }
+        // epilogue
+        if (lane == 0) ok = ok && wait_or_abort(accfull, 0, abort_flag, p.status);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (ok) {
+            while (!mbar_try_wait(accfull, 0)) {
+            }
+            tc_fence_after();
+            const int64_t row = n0 + 32 * warp + lane;
+            for (int c0 = 0; c0 < TN; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld_32cols(tmem_base + (static_cast<uint32_t>(32 * warp) << 16) + c0, v);
+                if (row < p.N) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int64_t m = m0 + c0 + i;
+                        if (m < p.M) p.y[m * p.N + row] = __uint_as_float(v[i]);
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, p.tmem_cols);
+    }
+}
+
+// ---- host side -------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+int pick_tn(int64_t M)
+{
+    if (M >= 256) return 256;
+    int tn = static_cast<int>((M + 31) / 32) * 32;
+    return tn < 32 ? 32 : tn;
+}
+
+}  // namespace
+
+bool prefill_supported(int64_t N, int64_t K, int64_t M)
+{
+    return K % kKChunk == 0 && K > 0 && N > 0 && M > 0 && N < (int64_t(1) << 31) && M < (int64_t(1) << 31) &&
+           K < (int64_t(1) << 30) && encode_fn() != nullptr;
+}
+
+cudaError_t launch_prefill(const void *W, const void *x, float *y, int64_t N, int64_t K, int64_t M, int /*sms*/,
+                           int *status, cudaStream_t s)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const int64_t row_bytes = (K / 32) * 18;
+    CUtensorMap wmap, xmap;
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(N)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+        const cuuint32_t box[2] = {kPackedRowBytes, kBM};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(W), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    const int TN = pick_tn(M);
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K * 2)};
+        const cuuint32_t box[2] = {kKB, static_cast<cuuint32_t>(TN)};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(x), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    PrefillParams p = {};
+    p.y = y;
+    p.status = status;
+    p.N = N;
+    p.K = K;
+    p.M = M;
+    p.TN = TN;
+    const int b_tile = TN * kKB * 2;
+    const size_t fixed = 1024 /*alignment slack*/ + 2 * kPackedTileBytes + 256 /*barriers etc.*/;
+    int SA = static_cast<int>((200 * 1024 - fixed) / (kATileBytes + b_tile));
+    if (SA > 4) SA = 4;
+    if (SA < 2) SA = 2;
+    p.SA = SA;
+    uint32_t cols = 32;
+    while (cols < static_cast<uint32_t>(TN)) cols <<= 1;
+    p.tmem_cols = cols;
+    const size_t smem = fixed + static_cast<size_t>(SA) * (kATileBytes + b_tile);
+    cudaError_t e = ensure_smem_optin(reinterpret_cast<const void *>(prefill_kernel), smem);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(static_cast<unsigned>((N + kBM - 1) / kBM), static_cast<unsigned>((M + TN - 1) / TN));
+    return launch_ex(prefill_kernel, grid, dim3(kThreads), smem, s, false, wmap, xmap, p);
 }
 
 }  // namespace qmv
