@@ -77,9 +77,12 @@ struct Plan {
 };
 
 // Launch-shape overrides for tuning sweeps: QMV_GEMV_TUNE="warps=16,stages=3,
-// G=8,SP=1,ctas=2" (any subset; 0 or absent = the built-in rule).
+// G=8,SP=1,ctas=2,share=2" (any subset; 0 or absent = the built-in rule).
+// ctas = CTAs per SM in the grid; share = the fraction 1/share of an SM's
+// shared memory one CTA may use (share=2 leaves room for the next call's CTA
+// to become resident early under programmatic dependent launch).
 struct Tune {
-    int warps = 0, stages = 0, G = 0, SP = 0, ctas = 0;
+    int warps = 0, stages = 0, G = 0, SP = 0, ctas = 0, share = 0;
 };
 
 const Tune &tune_overrides()
@@ -104,6 +107,7 @@ const Tune &tune_overrides()
             else if (!std::strcmp(key, "G")) t.G = v;
             else if (!std::strcmp(key, "SP")) t.SP = v;
             else if (!std::strcmp(key, "ctas")) t.ctas = v;
+            else if (!std::strcmp(key, "share")) t.share = v;
         }
     });
     return t;
@@ -122,7 +126,9 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
     p.U = static_cast<int>(U);
     p.G = lanes_per_row(p.U, M);
     if (tu.G == 1 || tu.G == 2 || tu.G == 4 || tu.G == 8 || tu.G == 16 || tu.G == 32) p.G = tu.G;
-    p.SP = (tu.SP >= 1 && tu.SP <= 7 && (tu.SP & 1)) ? tu.SP : 1;
+    // Passes per stage: odd for G < 8 keeps the lanes of a quarter warp in
+    // distinct banks; any value works for G >= 8.
+    p.SP = (tu.SP >= 1 && tu.SP <= 8 && ((tu.SP & 1) || p.G >= 8)) ? tu.SP : 1;
     const int RG = 32 / p.G;
     const int ctas_per_sm = (tu.ctas >= 1 && tu.ctas <= 4) ? tu.ctas : 1;
     const int64_t groups = (p.rows_total + RG - 1) / RG;
@@ -135,7 +141,8 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
     p.max_local_problems = static_cast<int>(pmax);
     const int unit_bytes = fmt == kQ4_0 ? 144 : 272;
     const size_t xbytes = static_cast<size_t>(pmax) * M * p.U * kXUnitBytes;
-    const size_t budget = static_cast<size_t>(smem_optin) / ctas_per_sm - 1024;
+    const int share = (tu.share >= 1 && tu.share <= 4) ? tu.share : 1;
+    const size_t budget = static_cast<size_t>(smem_optin) / (ctas_per_sm > share ? ctas_per_sm : share) - 1024;
     if (xbytes + 8 * 1024 > budget) return pl;
     const int max_warps = (M <= 2) ? 16 : 8;
     int warp_choices[2] = {8, 4};

@@ -125,6 +125,26 @@ __host__ __device__ __forceinline__ int x_perm_slot(int block_parity, int e)
 
 // ---- per-unit dot products ------------------------------------------------------
 
+// acc += d * (a.lo + a.hi + b.lo + b.hi), with fp16 inputs, exact products and
+// fp32 accumulation (mixed-precision fma.rn.f32.f16); d is the block's fp16
+// scale in the low 16 bits of `dbits`.
+__device__ __forceinline__ void acc_block(float &acc, uint32_t dbits, __half2 a, __half2 b)
+{
+    const uint32_t ua = *reinterpret_cast<uint32_t *>(&a);
+    const uint32_t ub = *reinterpret_cast<uint32_t *>(&b);
+    const unsigned short dh = static_cast<unsigned short>(dbits);
+    asm("{\n\t.reg .b16 d, a0, a1, b0, b1;\n\t"
+        "mov.b16 d, %1;\n\t"
+        "mov.b32 {a0, a1}, %2;\n\t"
+        "mov.b32 {b0, b1}, %3;\n\t"
+        "fma.rn.f32.f16 %0, a0, d, %0;\n\t"
+        "fma.rn.f32.f16 %0, a1, d, %0;\n\t"
+        "fma.rn.f32.f16 %0, b0, d, %0;\n\t"
+        "fma.rn.f32.f16 %0, b1, d, %0;\n\t}"
+        : "+f"(acc)
+        : "h"(dh), "r"(ua), "r"(ub));
+}
+
 // acc[m] += sum over the 8 blocks of one unit of d_b * (partial_b / prescale).
 // wsrc: the unit's bytes in shared memory; xsrc: the unit's permuted
 // activations for token 0; xstride: bytes between tokens.
@@ -159,7 +179,6 @@ __device__ __forceinline__ void dot_unit_q4_0(const uint8_t *wsrc, const uint8_t
             q[2] = w[9 * h + 7];
             q[3] = w[9 * h + 8];
         }
-        const float d = half_lo_to_float(dsrc);
         // Two independent half2 chains per token (words 0-1 and 2-3), joined
         // in fp32: shorter dependency chains, each half sums 8 products.
         __half2 ha[M], hb[M];
@@ -183,11 +202,7 @@ __device__ __forceinline__ void dot_unit_q4_0(const uint8_t *wsrc, const uint8_t
             }
         }
 #pragma unroll
-        for (int m = 0; m < M; ++m) {
-            const float2 fa = __half22float2(ha[m]);
-            const float2 fb = __half22float2(hb[m]);
-            acc[m] = fmaf(d, (fa.x + fa.y) + (fb.x + fb.y), acc[m]);
-        }
+        for (int m = 0; m < M; ++m) acc_block(acc[m], dsrc, ha[m], hb[m]);
     }
 }
 
@@ -219,7 +234,6 @@ __device__ __forceinline__ void dot_unit_q8_0(const uint8_t *wsrc, const uint8_t
 #pragma unroll
             for (int j = 0; j < 8; ++j) q[j] = w[17 * h + 9 + j];
         }
-        const float d = half_lo_to_float(dsrc);
         __half2 ha[M], hb[M];
 #pragma unroll
         for (int m = 0; m < M; ++m) {
@@ -242,11 +256,7 @@ __device__ __forceinline__ void dot_unit_q8_0(const uint8_t *wsrc, const uint8_t
             }
         }
 #pragma unroll
-        for (int m = 0; m < M; ++m) {
-            const float2 fa = __half22float2(ha[m]);
-            const float2 fb = __half22float2(hb[m]);
-            acc[m] = fmaf(d, (fa.x + fa.y) + (fb.x + fb.y), acc[m]);
-        }
+        for (int m = 0; m < M; ++m) acc_block(acc[m], dsrc, ha[m], hb[m]);
     }
 }
 

@@ -77,6 +77,7 @@ def main():
     ap.add_argument("--G", default="0")
     ap.add_argument("--SP", default="1")
     ap.add_argument("--ctas", default="1")
+    ap.add_argument("--share", default="1")
     ap.add_argument("--child", action="store_true")
     ap.add_argument("--out", default=None)
     args = ap.parse_args()
@@ -86,10 +87,10 @@ def main():
         child(args.fmt, shapes, Ms, args.reps)
         return
     grid = itertools.product(*[[int(v) for v in getattr(args, k).split(",")]
-                               for k in ("warps", "stages", "G", "SP", "ctas")])
+                               for k in ("warps", "stages", "G", "SP", "ctas", "share")])
     results = []
-    for warps, stages, G, SP, ctas in grid:
-        cfg = f"warps={warps},stages={stages},G={G},SP={SP},ctas={ctas}"
+    for warps, stages, G, SP, ctas, share in grid:
+        cfg = f"warps={warps},stages={stages},G={G},SP={SP},ctas={ctas},share={share}"
         env = dict(os.environ, QMV_GEMV_TUNE=cfg)
         r = subprocess.run([sys.executable, "-m", "weight_quantized_decode_gb300.tune", "--child",
                             "--fmt", args.fmt, "--shapes", args.shapes, "--M", args.M, "--reps", str(args.reps)],
