@@ -161,6 +161,9 @@ __device__ __forceinline__ void dot_unit_q4_0(const uint8_t *wsrc, const uint8_t
         w[4 * c + 2] = v.z;
         w[4 * c + 3] = v.w;
     }
+    float part[2][M];
+#pragma unroll
+    for (int m = 0; m < M; ++m) part[0][m] = part[1][m] = 0.0f;
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
         const int h = b >> 1;
@@ -202,8 +205,10 @@ __device__ __forceinline__ void dot_unit_q4_0(const uint8_t *wsrc, const uint8_t
             }
         }
 #pragma unroll
-        for (int m = 0; m < M; ++m) acc_block(acc[m], dsrc, ha[m], hb[m]);
+        for (int m = 0; m < M; ++m) acc_block(part[b & 1][m], dsrc, ha[m], hb[m]);
     }
+#pragma unroll
+    for (int m = 0; m < M; ++m) acc[m] += part[0][m] + part[1][m];
 }
 
 template <int M>
@@ -219,6 +224,9 @@ __device__ __forceinline__ void dot_unit_q8_0(const uint8_t *wsrc, const uint8_t
         w[4 * c + 2] = v.z;
         w[4 * c + 3] = v.w;
     }
+    float part[2][M];
+#pragma unroll
+    for (int m = 0; m < M; ++m) part[0][m] = part[1][m] = 0.0f;
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
         const int h = b >> 1;
@@ -256,13 +264,26 @@ __device__ __forceinline__ void dot_unit_q8_0(const uint8_t *wsrc, const uint8_t
             }
         }
 #pragma unroll
-        for (int m = 0; m < M; ++m) acc_block(acc[m], dsrc, ha[m], hb[m]);
+        for (int m = 0; m < M; ++m) acc_block(part[b & 1][m], dsrc, ha[m], hb[m]);
     }
+#pragma unroll
+    for (int m = 0; m < M; ++m) acc[m] += part[0][m] + part[1][m];
 }
 
 // ---- the streaming kernel ----------------------------------------------------------
 
-template <int FMT, int M, int MAXT>
+// Warp-collective wait for phase `parity` of `bar`: one vote when the stage
+// has landed (the common case), a bounded wait otherwise.
+__device__ __forceinline__ bool stage_wait(uint64_t *bar, uint32_t parity, int *status)
+{
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    return mbar_wait_warp(bar, parity, status);
+}
+
+// MOE = the one-launch multi-expert form: problem p is expert slot p with its
+// own token, weights from expert_idx[p] of the pool.  Otherwise one problem
+// of M tokens.
+template <int FMT, int M, int MAXT, bool MOE>
 __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p)
 {
     using T = FmtTraits<FMT>;
@@ -289,15 +310,16 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
     const uint32_t row0 = static_cast<uint32_t>((static_cast<uint64_t>(R) * blockIdx.x) / gridDim.x);
     const uint32_t row1 = static_cast<uint32_t>((static_cast<uint64_t>(R) * (blockIdx.x + 1)) / gridDim.x);
     const int nrows = static_cast<int>(row1 - row0);
-    // Problems (tokens of the plain GEMV, or expert slots) this CTA touches.
-    const int prob_lo = nrows > 0 ? static_cast<int>(row0 / N) : 0;
-    const int prob_hi = nrows > 0 ? static_cast<int>((row1 - 1) / N) : -1;
+    // Problems (expert slots) this CTA touches; always 0..0 for the plain GEMV.
+    const int prob_lo = (MOE && nrows > 0) ? static_cast<int>(row0 / N) : 0;
+    const int prob_hi = MOE ? (nrows > 0 ? static_cast<int>((row1 - 1) / N) : -1) : 0;
     const int ngroups = (nrows + RG - 1) / RG;
     const int my_groups = (ngroups > warp) ? (ngroups - warp + warps - 1) / warps : 0;
     const int units_per_stage = SP * G;
     const int T_stages = (U + units_per_stage - 1) / units_per_stage;
     const int total = my_groups * T_stages;
     const uint32_t lane_chunk_bytes = static_cast<uint32_t>(units_per_stage) * T::kUnitBytes;
+    const uint8_t *cta_rows = p.W + static_cast<int64_t>(row0) * p.row_bytes;   // plain GEMV only
 
     if (lane == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
@@ -310,27 +332,22 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
     int is_slot = 0;         // slot of the next stage to request
     int is_t = 0;            // its stage index within the row group
     int is_g = warp;         // its row group (CTA-local)
-    // Lane r < RG requests row r of the group; cached per group.
-    const uint8_t *is_row = nullptr;
+    const uint8_t *is_row = nullptr;   // row of lane r < RG in the current group (null: none)
 
     auto issue_next = [&]() {
         if (is_t == 0) {
             is_row = nullptr;
             const int lr = is_g * RG + lane;
             if (lane < RG && lr < nrows) {
-                const uint32_t row = row0 + lr;
-                uint32_t prob = 0, n = row;
-                if (p.n_problems > 1) {
-                    prob = row / N;
-                    n = row - prob * N;
+                if (MOE) {
+                    const uint32_t row = row0 + lr;
+                    const uint32_t prob = row / N;
+                    const uint32_t n = row - prob * N;
+                    const int64_t e = p.expert_idx[prob];
+                    if (e >= 0 && e < p.n_experts) is_row = p.W + (e * p.N + n) * p.row_bytes;
+                } else {
+                    is_row = cta_rows + static_cast<int64_t>(lr) * p.row_bytes;
                 }
-                int64_t e = 0;
-                bool ok = true;
-                if (p.expert_idx) {
-                    e = p.expert_idx[prob];
-                    ok = (e >= 0 && e < p.n_experts);
-                }
-                if (ok) is_row = p.W + (e * p.N + n) * p.row_bytes;
             }
         }
         const int u0 = is_t * units_per_stage;
@@ -350,36 +367,56 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
         }
     };
 
-    // Request the first stages before waiting for the previous kernel (W is
+    // Request the first stage before waiting for the previous kernel (W is
     // never written by it).  The expert indices may be, so the multi-expert
-    // call waits first.
+    // call waits first.  The remaining prefetch is requested after this
+    // thread's activation loads: the activations are on the critical path and
+    // must not queue behind megabytes of weight traffic.
     const int prefetch = total < S ? total : S;
-    if (!p.expert_idx)
-        for (int i = 0; i < prefetch; ++i) issue_next();
+    const int early = MOE ? 0 : (prefetch < 1 ? prefetch : 1);
+    for (int i = 0; i < early; ++i) issue_next();
 
     pdl_wait_prior_grid();
 
-    if (p.expert_idx)
-        for (int i = 0; i < prefetch; ++i) issue_next();
-
     // Stage the activations: permuted pair order, 528-byte padded units.  Each
-    // thread moves 8 consecutive activations (one 16-byte load) per step.
+    // thread moves 8 consecutive activations (one 16-byte load) per vector;
+    // up to four loads are in flight before their stores.
     {
         const int per_tok = U * 32;        // 16-byte groups per token
         const int nvec = (prob_hi - prob_lo + 1) * M * per_tok;
         const uint4 *xsrc = reinterpret_cast<const uint4 *>(p.x + static_cast<int64_t>(prob_lo) * M * p.K);
-        for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
-            const int tok = v / per_tok;
-            const int g = v - tok * per_tok;                          // group within the token row
-            const uint4 val = xsrc[static_cast<int64_t>(tok) * (p.K / 8) + g];
-            const int blk = g >> 2;                                    // block within the row
-            const int e0 = (g & 3) * 8;                                // first element in the block
-            uint8_t *dst = xs + (static_cast<size_t>(tok) * U + (blk >> 3)) * kXUnitBytes + (blk & 7) * 64;
-            const uint32_t wv[4] = {val.x, val.y, val.z, val.w};
+        const int kvec = static_cast<int>(p.K / 8);
+        bool first = true;
+        for (int v0 = threadIdx.x; v0 < nvec || first; v0 += 4 * blockDim.x) {
+            uint4 val[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const unsigned short h = static_cast<unsigned short>(wv[i >> 1] >> (16 * (i & 1)));
-                *reinterpret_cast<unsigned short *>(dst + 2 * x_perm_slot<FMT>(blk & 1, e0 + i)) = h;
+            for (int b = 0; b < 4; ++b) {
+                const int v = v0 + b * blockDim.x;
+                if (v < nvec) {
+                    const int tok = v / per_tok;
+                    val[b] = xsrc[static_cast<int64_t>(tok) * kvec + (v - tok * per_tok)];
+                }
+            }
+            if (first) {
+                first = false;
+                for (int i = early; i < prefetch; ++i) issue_next();
+            }
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const int v = v0 + b * blockDim.x;
+                if (v < nvec) {
+                    const int tok = v / per_tok;
+                    const int g = v - tok * per_tok;                       // group within the token row
+                    const int blk = g >> 2;                                 // block within the row
+                    const int e0 = (g & 3) * 8;                             // first element in the block
+                    uint8_t *dst = xs + (static_cast<size_t>(tok) * U + (blk >> 3)) * kXUnitBytes + (blk & 7) * 64;
+                    const uint32_t wv[4] = {val[b].x, val[b].y, val[b].z, val[b].w};
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const unsigned short h = static_cast<unsigned short>(wv[i >> 1] >> (16 * (i & 1)));
+                        *reinterpret_cast<unsigned short *>(dst + 2 * x_perm_slot<FMT>(blk & 1, e0 + i)) = h;
+                    }
+                }
             }
         }
     }
@@ -400,39 +437,39 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
     int t = 0;
     int g = warp;
     int lr = 0;
-    uint32_t row = 0, prob = 0;
+    uint32_t prob = 0;
     bool row_ok = false;
     const uint8_t *xrow = xs;
+    const uint8_t *lane_stage = ring + r * lane_chunk_bytes;
 
     for (int i = 0; i < total; ++i) {
         if (t == 0) {
             lr = g * RG + r;
             row_ok = lr < nrows;
-            row = row0 + lr;
-            prob = 0;
-            if (row_ok && p.n_problems > 1) prob = row / N;
-            if (row_ok && p.expert_idx) {
-                const int64_t e = p.expert_idx[prob];
-                row_ok = (e >= 0 && e < p.n_experts);
+            if (MOE) {
+                prob = row_ok ? (row0 + lr) / N : static_cast<uint32_t>(prob_lo);
+                if (row_ok) {
+                    const int64_t e = p.expert_idx[prob];
+                    row_ok = (e >= 0 && e < p.n_experts);
+                }
+                xrow = xs + static_cast<size_t>(prob - prob_lo) * M * xstride;
             }
-            xrow = xs + static_cast<size_t>(prob - prob_lo) * M * xstride;
         }
-        if (!mbar_wait_warp(&bars[slot], phase, p.status)) {
+        if (!stage_wait(&bars[slot], phase, p.status)) {
             alive = false;
             break;
         }
         consumed = i + 1;
-        const uint8_t *stage = ring + static_cast<size_t>(slot) * slot_bytes + r * lane_chunk_bytes;
-        const int u0 = t * units_per_stage;
+        const uint8_t *stage = lane_stage + static_cast<size_t>(slot) * slot_bytes;
         if (row_ok) {
+            const int u0 = t * units_per_stage + q;
             for (int pass = 0; pass < SP; ++pass) {
-                const int ul = pass * G + q;          // unit within the stage
-                const int u = u0 + ul;
+                const int u = u0 + pass * G;
                 if (u < U) {
                     if (FMT == kQ4_0)
-                        dot_unit_q4_0<M>(stage + ul * T::kUnitBytes, xrow + u * kXUnitBytes, xstride, acc);
+                        dot_unit_q4_0<M>(stage + (pass * G + q) * T::kUnitBytes, xrow + u * kXUnitBytes, xstride, acc);
                     else
-                        dot_unit_q8_0<M>(stage + ul * T::kUnitBytes, xrow + u * kXUnitBytes, xstride, acc);
+                        dot_unit_q8_0<M>(stage + (pass * G + q) * T::kUnitBytes, xrow + u * kXUnitBytes, xstride, acc);
                 }
             }
         }
@@ -453,13 +490,16 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
                     acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], off);
             }
             if (q == 0 && lr < nrows) {
-                const uint32_t n = row - prob * N;
-                const bool bad = !row_ok;
-                if (bad) atomicOr(p.status, kDevBadExpert);
+                const uint32_t row = row0 + lr;
+                if (MOE) {
+                    const uint32_t n = row - prob * N;
+                    if (!row_ok) atomicOr(p.status, kDevBadExpert);
+                    p.y[static_cast<int64_t>(prob) * p.N + n] =
+                        row_ok ? acc[0] * T::kPrescale : __int_as_float(0x7fc00000);
+                } else {
 #pragma unroll
-                for (int m = 0; m < M; ++m)
-                    p.y[(static_cast<int64_t>(prob) * M + m) * p.N + n] =
-                        bad ? __int_as_float(0x7fc00000) : acc[m] * T::kPrescale;
+                    for (int m = 0; m < M; ++m) p.y[static_cast<int64_t>(m) * p.N + row] = acc[m] * T::kPrescale;
+                }
             }
 #pragma unroll
             for (int m = 0; m < M; ++m) acc[m] = 0.0f;

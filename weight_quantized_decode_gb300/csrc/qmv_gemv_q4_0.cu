@@ -4,10 +4,10 @@
 
 namespace qmv {
 
-template <int M, int MAXT>
+template <int M, int MAXT, bool MOE>
 static cudaError_t launch_t(const GemvParams &p, int grid, int warps, size_t smem, cudaStream_t s, bool pdl)
 {
-    auto kernel = gemv_stream_kernel<kQ4_0, M, MAXT>;
+    auto kernel = gemv_stream_kernel<kQ4_0, M, MAXT, MOE>;
     cudaError_t e = ensure_smem_optin(reinterpret_cast<const void *>(kernel), smem);
     if (e != cudaSuccess) return e;
     return launch_ex(kernel, dim3(grid), dim3(warps * 32), smem, s, pdl, p);
@@ -18,9 +18,16 @@ static cudaError_t launch_t(const GemvParams &p, int grid, int warps, size_t sme
 template <int M>
 static cudaError_t launch_one(const GemvParams &p, int grid, int warps, size_t smem, cudaStream_t s, bool pdl)
 {
-    if (warps <= 8) return launch_t<M, 256>(p, grid, warps, smem, s, pdl);
+    if (p.expert_idx) {
+        if constexpr (M == 1) {
+            if (warps <= 8) return launch_t<1, 256, true>(p, grid, warps, smem, s, pdl);
+            if (warps <= 16) return launch_t<1, 512, true>(p, grid, warps, smem, s, pdl);
+        }
+        return cudaErrorInvalidConfiguration;
+    }
+    if (warps <= 8) return launch_t<M, 256, false>(p, grid, warps, smem, s, pdl);
     if constexpr (M <= 2) {
-        if (warps <= 16) return launch_t<M, 512>(p, grid, warps, smem, s, pdl);
+        if (warps <= 16) return launch_t<M, 512, false>(p, grid, warps, smem, s, pdl);
     }
     return cudaErrorInvalidConfiguration;
 }
