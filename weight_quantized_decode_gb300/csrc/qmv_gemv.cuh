@@ -333,6 +333,7 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
     int is_t = 0;            // its stage index within the row group
     int is_g = warp;         // its row group (CTA-local)
     const uint8_t *is_row = nullptr;   // row of lane r < RG in the current group (null: none)
+    const uint64_t l2_policy = l2_evict_first_policy();   // weights stream through L2 once
 
     auto issue_next = [&]() {
         if (is_t == 0) {
@@ -357,8 +358,8 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
         if (lane == 0) mbar_arrive_expect_tx(&bars[is_slot], total_bytes);
         __syncwarp();
         if (my_bytes)
-            bulk_g2s(ring + static_cast<size_t>(is_slot) * slot_bytes + lane * lane_chunk_bytes,
-                     is_row + static_cast<size_t>(u0) * T::kUnitBytes, my_bytes, &bars[is_slot]);
+            bulk_g2s_hint(ring + static_cast<size_t>(is_slot) * slot_bytes + lane * lane_chunk_bytes,
+                          is_row + static_cast<size_t>(u0) * T::kUnitBytes, my_bytes, &bars[is_slot], l2_policy);
         ++issued;
         if (++is_slot == S) is_slot = 0;
         if (++is_t == T_stages) {
@@ -379,42 +380,64 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
     pdl_wait_prior_grid();
 
     // Stage the activations: permuted pair order, 528-byte padded units.  Each
-    // thread moves 8 consecutive activations (one 16-byte load) per vector;
-    // up to four loads are in flight before their stores.
+    // thread builds whole 16-byte chunks of the permuted layout from four
+    // 4-byte loads (pairs of consecutive activations) and four PRMTs.
     {
-        const int per_tok = U * 32;        // 16-byte groups per token
-        const int nvec = (prob_hi - prob_lo + 1) * M * per_tok;
-        const uint4 *xsrc = reinterpret_cast<const uint4 *>(p.x + static_cast<int64_t>(prob_lo) * M * p.K);
-        const int kvec = static_cast<int>(p.K / 8);
+        const int ntok = (prob_hi - prob_lo + 1) * M;
+        const int chunks = static_cast<int>(p.K / 8);          // 16-byte chunks per token (4 per block)
+        const int per_thread = (chunks + blockDim.x - 1) / blockDim.x;
         bool first = true;
-        for (int v0 = threadIdx.x; v0 < nvec || first; v0 += 4 * blockDim.x) {
-            uint4 val[4];
+        for (int tok = 0; tok < ntok || first; ++tok) {
+            const bool tok_ok = tok < ntok;
+            const uint32_t *xt = reinterpret_cast<const uint32_t *>(p.x + (static_cast<int64_t>(prob_lo) * M + tok) * p.K);
+            uint8_t *xd = xs + static_cast<size_t>(tok) * U * kXUnitBytes;
+            for (int j0 = 0; j0 < per_thread || first; j0 += 2) {
+                uint32_t a[2][4];
+                int cidx[2];
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const int v = v0 + b * blockDim.x;
-                if (v < nvec) {
-                    const int tok = v / per_tok;
-                    val[b] = xsrc[static_cast<int64_t>(tok) * kvec + (v - tok * per_tok)];
+                for (int b = 0; b < 2; ++b) {
+                    const int c = threadIdx.x + (j0 + b) * blockDim.x;
+                    cidx[b] = (tok_ok && j0 + b < per_thread && c < chunks) ? c : -1;
+                    if (cidx[b] >= 0) {
+                        const int blk = c >> 2, sub = c & 3;
+                        int i0, i2, i4, i6;    // first element of each loaded pair (in half units)
+                        if (FMT == kQ4_0) {
+                            // word `sub` of the block: bytes b0,b1 from (i0, i0+1), b2,b3 from (i2, i2+1);
+                            // low nibbles are elements i, high nibbles i + 16.
+                            if (blk & 1) { i0 = 4 * sub; i2 = 4 * sub + 2; }
+                            else if (sub == 0) { i0 = 0; i2 = 14; }
+                            else { i0 = 4 * sub - 2; i2 = 4 * sub; }
+                            i4 = i0 + 16;
+                            i6 = i2 + 16;
+                        } else {
+                            // words 2*sub and 2*sub+1 of the block (Q8_0: four codes per word)
+                            const int w0 = 2 * sub, w1 = 2 * sub + 1;
+                            if (blk & 1) { i0 = 4 * w0; i2 = 4 * w0 + 2; }
+                            else if (w0 == 0) { i0 = 0; i2 = 30; }
+                            else { i0 = 4 * w0 - 2; i2 = 4 * w0; }
+                            if (blk & 1) { i4 = 4 * w1; i6 = 4 * w1 + 2; }
+                            else { i4 = 4 * w1 - 2; i6 = 4 * w1; }
+                        }
+                        const uint32_t *xb = xt + blk * 16;     // 32 halves = 16 words per block
+                        a[b][0] = __ldg(xb + (i0 >> 1));
+                        a[b][1] = __ldg(xb + (i2 >> 1));
+                        a[b][2] = __ldg(xb + (i4 >> 1));
+                        a[b][3] = __ldg(xb + (i6 >> 1));
+                    }
                 }
-            }
-            if (first) {
-                first = false;
-                for (int i = early; i < prefetch; ++i) issue_next();
-            }
+                if (first) {
+                    first = false;
+                    for (int i = early; i < prefetch; ++i) issue_next();
+                }
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const int v = v0 + b * blockDim.x;
-                if (v < nvec) {
-                    const int tok = v / per_tok;
-                    const int g = v - tok * per_tok;                       // group within the token row
-                    const int blk = g >> 2;                                 // block within the row
-                    const int e0 = (g & 3) * 8;                             // first element in the block
-                    uint8_t *dst = xs + (static_cast<size_t>(tok) * U + (blk >> 3)) * kXUnitBytes + (blk & 7) * 64;
-                    const uint32_t wv[4] = {val[b].x, val[b].y, val[b].z, val[b].w};
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const unsigned short h = static_cast<unsigned short>(wv[i >> 1] >> (16 * (i & 1)));
-                        *reinterpret_cast<unsigned short *>(dst + 2 * x_perm_slot<FMT>(blk & 1, e0 + i)) = h;
+                for (int b = 0; b < 2; ++b) {
+                    if (cidx[b] >= 0) {
+                        const int c = cidx[b];
+                        const int blk = c >> 2, sub = c & 3;
+                        // pairs (first of each, first of each) and (second, second)
+                        const uint4 v = make_uint4(__byte_perm(a[b][0], a[b][1], 0x5410), __byte_perm(a[b][0], a[b][1], 0x7632),
+                                                   __byte_perm(a[b][2], a[b][3], 0x5410), __byte_perm(a[b][2], a[b][3], 0x7632));
+                        *reinterpret_cast<uint4 *>(xd + (blk >> 3) * kXUnitBytes + (blk & 7) * 64 + sub * 16) = v;
                     }
                 }
             }
