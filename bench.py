@@ -44,12 +44,30 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
 WORKLOADS = {
-    # name: (fmt, [(N, K)], [M values])
-    "q4_0_m1_sweep": ("q4_0", [(4096, 4096), (6144, 4096), (4096, 14336), (14336, 4096), (28672, 4096),
-                               (128256, 4096)], [1]),
-    "q4_0_mlp_up": ("q4_0", [(6144, 2048)], [1]),
-    "q8_0": ("q8_0", [(12288, 2560), (2560, 6144), (8192, 2048)], [1, 2, 4, 8]),
+    # The configuration the headline metric is quoted on: Q4_0, one token,
+    # Llama-3-8B-style tables (sm8x-bench summary table).
+    "q4_0_m1_sweep": {"kind": "gemv", "fmt": "q4_0", "M": [1],
+                      "shapes": [(4096, 4096), (6144, 4096), (4096, 14336), (14336, 4096), (28672, 4096),
+                                 (128256, 4096)]},
+    # Qwen3-1.7B MLP up (volta-kernel-bakeoff, "What's in the race").
+    "q4_0_mlp_up": {"kind": "gemv", "fmt": "q4_0", "M": [1], "shapes": [(6144, 2048)]},
+    # Q8_0 attention / output tables at a few tokens.
+    "q8_0": {"kind": "gemv", "fmt": "q8_0", "M": [1, 2, 4, 8],
+             "shapes": [(12288, 2560), (2560, 6144), (8192, 2048)]},
+    # Experts in one launch: (pool size, slots, N, K).
+    "moe": {"kind": "moe", "fmt": "q4_0", "configs": [(128, 10, 640, 2560), (128, 8, 512, 2048)]},
+    # Prompt (prefill) on the tensor cores.
+    "prefill": {"kind": "prefill", "fmt": "q4_0", "M": [64, 512], "shapes": [(12288, 2560), (8192, 2048)]},
 }
+
+
+def metric_name(workload):
+    wl = WORKLOADS[workload]
+    if wl["kind"] == "prefill":
+        return "Q4_0 prefill GEMM TFLOP/s (fp16 tensor cores; us/call per table in 'sweep')"
+    if wl["kind"] == "moe":
+        return "Q4_0 multi-expert GEMV (one launch) HBM GB/s (algorithmic bytes; us/call per config in 'sweep')"
+    return f"{wl['fmt'].upper()} GEMV HBM GB/s (algorithmic bytes; us/call per table in 'sweep')"
 
 
 # ---------------------------------------------------------------------------------
@@ -163,47 +181,78 @@ def run_ours(args, dist, rank, local, world):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     q.lib()
-    fmt, shapes, Ms = WORKLOADS[args.workload]
+    wl = WORKLOADS[args.workload]
+    kind, fmt = wl["kind"], wl["fmt"]
     prop = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(prop, "L2_cache_size", 128 * 1024 * 1024) or 128 * 1024 * 1024)
+    bb = 18 if fmt == "q4_0" else 34
 
-    # ---- inputs: rotated weight copies per shape, activations, outputs ----------
-    # Copies per shape: a power of two >= 4 x L2 / table bytes, so every shape's
-    # rotation divides the longest one and a single CUDA graph of `period`
-    # steps replays the exact call sequence.
-    calls = []   # one entry per (shape, M): the call made once per step
-    for (N, K) in shapes:
-        wbytes = N * (K // 32) * (18 if fmt == "q4_0" else 34)
+    def rotated_copies(rows, K, seed_name):
+        """A power of two of weight copies, >= 4x L2 in total, each with distinct
+        bytes (codes XOR a per-copy constant; scales as generated)."""
+        wbytes = rows * (K // 32) * bb
         copies = 1 << max(1, math.ceil(math.log2(max(2.0, 4.0 * l2 / wbytes))))
-        base = synth.weights(fmt, N, K, synth.seed_for(f"{fmt}_{N}x{K}"))
-        bb = 18 if fmt == "q4_0" else 34
-        Wd = torch.empty((copies, N, base.shape[1]), dtype=torch.uint8, device=dev)
+        base = synth.weights(fmt, rows, K, synth.seed_for(seed_name))
+        Wd = torch.empty((copies, rows, base.shape[1]), dtype=torch.uint8, device=dev)
         Wd[0].copy_(torch.from_numpy(base))
         for c in range(1, copies):
-            # Distinct bytes per copy: XOR the code bytes with a per-copy
-            # constant (any byte is a valid code); scales stay as generated.
             Wd[c].copy_(Wd[0])
-            codes = Wd[c].view(N, K // 32, bb)[:, :, 2:]
-            codes.bitwise_xor_(c & 0xFF)
-        for M in Ms:
-            x = synth.activations(M, K, synth.seed_for(f"x_{K}_{M}"))
-            xd = torch.from_numpy(x).to(dev)
-            yd = torch.empty((M, N), dtype=torch.float32, device=dev)
-            calls.append({"N": N, "K": K, "M": M, "W": Wd, "copies": copies, "x": xd, "y": yd,
-                          "x_host": torch.from_numpy(x).pin_memory(),
-                          "y_host": torch.empty((M, N), dtype=torch.float32).pin_memory(),
-                          "bytes": algo_bytes(fmt, N, K, M)})
-    fn_ptr = q.qmv_q4_0_ptr if fmt == "q4_0" else q.qmv_q8_0_ptr
+            Wd[c].view(rows, K // 32, bb)[:, :, 2:].bitwise_xor_(c & 0xFF)
+        return Wd, copies
+
+    # ---- inputs: one entry per call made once per step ----------------------------
+    # Copies per table are powers of two, so every table's rotation divides the
+    # longest one and a single CUDA graph of `period` steps replays the exact
+    # call sequence.
+    calls = []
     stream = torch.cuda.Stream(dev)
     sh = int(stream.cuda_stream)
-    period = max(c["copies"] for c in calls)
+    if kind in ("gemv", "prefill"):
+        fn_ptr = {"gemv": q.qmv_q4_0_ptr if fmt == "q4_0" else q.qmv_q8_0_ptr,
+                  "prefill": q.qmm_q4_0_prefill_ptr}[kind]
+        for (N, K) in wl["shapes"]:
+            Wd, copies = rotated_copies(N, K, f"{fmt}_{N}x{K}")
+            for M in wl["M"]:
+                x = synth.activations(M, K, synth.seed_for(f"x_{K}_{M}"))
+                c = {"name": f"{N}x{K}/M{M}", "N": N, "K": K, "M": M, "W": Wd, "copies": copies,
+                     "x": torch.from_numpy(x).to(dev), "y": torch.empty((M, N), dtype=torch.float32, device=dev),
+                     "x_host": torch.from_numpy(x).pin_memory(),
+                     "y_host": torch.empty((M, N), dtype=torch.float32).pin_memory(),
+                     "bytes": algo_bytes(fmt, N, K, M), "flops": 2 * M * N * K}
+
+                def call(s, c=c):
+                    W = c["W"][s % c["copies"]]
+                    fn_ptr(W.data_ptr(), c["x"].data_ptr(), c["y"].data_ptr(), c["N"], c["K"], c["M"], sh)
+                c["call"] = call
+                calls.append(c)
+    else:  # moe: a pool of experts, distinct indices drawn per step
+        for (E, slots, N, K) in wl["configs"]:
+            Wd, copies = rotated_copies(E * N, K, f"moe_{E}x{N}x{K}")
+            period_idx = 64
+            idx = synth.expert_indices(period_idx, slots, E, synth.seed_for(f"moe_idx_{E}_{slots}"))
+            x = synth.activations(slots, K, synth.seed_for(f"moe_x_{K}_{slots}"))
+            c = {"name": f"{slots}x({N}x{K}) of {E}", "N": N, "K": K, "M": slots, "E": E, "W": Wd,
+                 "copies": copies, "idx": torch.from_numpy(idx).to(dev), "idx_period": period_idx,
+                 "x": torch.from_numpy(x).to(dev), "y": torch.empty((slots, N), dtype=torch.float32, device=dev),
+                 "x_host": torch.from_numpy(x).pin_memory(),
+                 "y_host": torch.empty((slots, N), dtype=torch.float32).pin_memory(),
+                 "bytes": slots * algo_bytes(fmt, N, K, 1) + 4 * slots, "flops": 2 * slots * N * K}
+
+            def call(s, c=c):
+                W = c["W"][s % c["copies"]]
+                ix = c["idx"][s % c["idx_period"]]
+                q.qmv_moe_ptr(W.data_ptr(), ix.data_ptr(), c["E"], c["x"].data_ptr(), c["y"].data_ptr(),
+                              c["N"], c["K"], c["M"], sh)
+            c["call"] = call
+            calls.append(c)
+    period = max(max(c["copies"] for c in calls), max(c.get("idx_period", 1) for c in calls))
 
     def enqueue_step(s):
         for c in calls:
-            W = c["W"][s % c["copies"]]
-            fn_ptr(W.data_ptr(), c["x"].data_ptr(), c["y"].data_ptr(), c["N"], c["K"], c["M"], sh)
+            c["call"](s)
 
     step_bytes = sum(c["bytes"] for c in calls)
+    step_flops = sum(c["flops"] for c in calls)
     launches_per_step = len(calls)
 
     # one eager pass (module loading, shared-memory opt-in) before any capture
@@ -275,16 +324,12 @@ def run_ours(args, dist, rank, local, world):
     for c in calls:
         R = max(64, 2 * c["copies"])
 
-        def one_shape(first, count, c=c):
-            for s in range(first, first + count):
-                W = c["W"][s % c["copies"]]
-                fn_ptr(W.data_ptr(), c["x"].data_ptr(), c["y"].data_ptr(), c["N"], c["K"], c["M"], sh)
-
-        def cap(count):
+        def cap(count, c=c):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.stream(stream):
                 with torch.cuda.graph(g, stream=stream):
-                    one_shape(0, count)
+                    for s_ in range(count):
+                        c["call"](s_)
             return g
 
         g = cap(R)
@@ -294,10 +339,15 @@ def run_ours(args, dist, rank, local, world):
         # one call on its own (graph launch + ramp + drain), median of 20
         iso = statistics.median(event_time_us(g1) for _ in range(20))
         gbs = c["bytes"] / (best * 1e-6) / 1e9
-        sweep.append({"N": c["N"], "K": c["K"], "M": c["M"], "copies": c["copies"],
-                      "us_per_call": round(best, 3), "us_isolated_call": round(iso, 3),
-                      "GBps": round(gbs, 1), "frac_of_measured_hbm": round(gbs / pk["hbm_gbs"], 4),
-                      "frac_of_8TBps_spec": round(gbs / SPEC_HBM_GBS, 4)})
+        row = {"call": c["name"], "copies": c["copies"], "us_per_call": round(best, 3),
+               "us_isolated_call": round(iso, 3), "GBps": round(gbs, 1),
+               "frac_of_measured_hbm": round(gbs / pk["hbm_gbs"], 4),
+               "frac_of_8TBps_spec": round(gbs / SPEC_HBM_GBS, 4)}
+        if kind == "prefill":
+            tf = c["flops"] / (best * 1e-6) / 1e12
+            row["TFLOPs"] = round(tf, 1)
+            row["frac_of_measured_tensor"] = round(tf / pk["bf16_tflops"], 4)
+        sweep.append(row)
 
     clock_info = clocks.stop()
 
@@ -307,8 +357,7 @@ def run_ours(args, dist, rank, local, world):
         def e2e_step(s):
             for c in calls:
                 c["x"].copy_(c["x_host"], non_blocking=True)
-                W = c["W"][s % c["copies"]]
-                fn_ptr(W.data_ptr(), c["x"].data_ptr(), c["y"].data_ptr(), c["N"], c["K"], c["M"], sh)
+                c["call"](s)
                 c["y_host"].copy_(c["y"], non_blocking=True)
 
         with torch.cuda.stream(stream):
@@ -325,9 +374,10 @@ def run_ours(args, dist, rank, local, world):
             stream.synchronize()
             wall = time.perf_counter() - t0
         e2e_ms = max(a.elapsed_time(b), wall * 1e3)
-        h2d = sum(2 * c["M"] * c["K"] for c in calls)
-        d2h = sum(4 * c["M"] * c["N"] for c in calls)
-        e2e = {"value": step_bytes * args.steps / (e2e_ms * 1e-3) / 1e9 * world, "unit": "GB/s",
+        h2d = sum(c["x_host"].numel() * 2 for c in calls)
+        d2h = sum(c["y_host"].numel() * 4 for c in calls)
+        e2e_val = (step_flops / 1e12 if kind == "prefill" else step_bytes / 1e9) * args.steps / (e2e_ms * 1e-3)
+        e2e = {"value": round(e2e_val * world, 3), "unit": "TFLOP/s" if kind == "prefill" else "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "note": "weights resident in HBM (model state); per step each call's x is copied from pinned "
                        "host memory and its y read back; host-launched calls through the C ABI"}
@@ -337,32 +387,42 @@ def run_ours(args, dist, rank, local, world):
         t = torch.tensor([ms], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
-    value = step_bytes * args.steps * world / (ms * 1e-3) / 1e9
+    gbs_total = step_bytes * args.steps * world / (ms * 1e-3) / 1e9
+    tflops_total = step_flops * args.steps * world / (ms * 1e-3) / 1e12
 
     out = None
     if rank == 0:
-        kname = "gemv_stream_kernel"
-        tr = traffic_record(f"{fmt}:{shapes[-1][0]}x{shapes[-1][1]}")
-        roof = {"bound": "hbm", "achieved": round(value / world, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": round(value / world / pk["hbm_gbs"], 4),
-                "traffic": (tr or {}).get("bytes_per_launch"),
-                "peak_source": f"{pk['source']} (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)",
-                "kernel": kname,
-                "achieved_basis": "algorithmic bytes of all launches in the timed region / CUDA-event time on "
-                                  "the launching stream"}
+        if kind == "prefill":
+            value, unit = tflops_total, "TFLOP/s"
+            roof = {"bound": "tensor", "achieved": round(tflops_total / world, 1), "peak": pk["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": round(tflops_total / world / pk["bf16_tflops"], 4),
+                    "peak_source": f"{pk['source']} (MEASURED_PEAKS.json bf16_tflops burst; fp16 has the same "
+                                   f"nominal dense rate)",
+                    "hbm_frac": round(gbs_total / world / pk["hbm_gbs"], 4), "kernel": "prefill_kernel"}
+        else:
+            value, unit = gbs_total, "GB/s"
+            roof = {"bound": "hbm", "achieved": round(gbs_total / world, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(gbs_total / world / pk["hbm_gbs"], 4),
+                    "peak_source": f"{pk['source']} (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)",
+                    "kernel": "gemv_stream_kernel"}
+        tr = traffic_record(args.workload)
+        roof["traffic"] = (tr or {}).get("bytes_per_launch")
+        if tr:
+            roof["traffic_launch"] = tr.get("launch")
+        roof["achieved_basis"] = ("algorithmic work of all launches in the timed region / CUDA-event time on the "
+                                  "launching stream (per-launch figures in 'sweep')")
+        cfg = {"workload": args.workload, "format": fmt, "calls_per_step": [c["name"] for c in calls],
+               "values": "Q4_0 codes uniform 0..15, d~U[0.005,0.02]; Q8_0 codes U[-127,127], d~U[0.001,0.01]; "
+                         "x fp16 N(0,1); seeded",
+               "l2": "inputs larger than L2: each table cycles >= 4x L2 bytes of weight copies",
+               "timing": "CUDA graphs of back-to-back calls (programmatic dependent launch for the decode "
+                         "kernels), CUDA events on the launching stream",
+               "parallelism": f"replica x{world} (independent problems per GPU)"}
         out = {
-            "metric": f"{fmt.upper()} GEMV HBM GB/s (algorithmic bytes; us/call per shape in 'sweep')",
-            "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "metric": metric_name(args.workload), "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-            "config": {"workload": args.workload, "format": fmt,
-                       "shapes": [f"{N}x{K}" for (N, K) in shapes], "M": Ms,
-                       "values": "Q4_0 codes uniform 0..15, d~U[0.005,0.02]; Q8_0 codes U[-127,127], "
-                                 "d~U[0.001,0.01]; x fp16 N(0,1); seeded",
-                       "l2": "inputs larger than L2: each shape cycles >= 4x L2 bytes of weight copies",
-                       "timing": "CUDA graphs of back-to-back calls (programmatic dependent launch), "
-                                 "CUDA events on the launching stream",
-                       "parallelism": f"replica x{world} (independent problems per GPU)"},
+            "config": cfg,
             "sweep": sweep,
             "roofline": roof,
             "clocks": clock_info,
@@ -374,37 +434,63 @@ def run_ours(args, dist, rank, local, world):
 
 
 # ---------------------------------------------------------------------------------
-def oracle_sample(fmt, shapes, Ms, budget_s):
-    """Time the CPU oracle (as it stands) on a bounded row sample of the workload."""
+def oracle_tasks(workload):
+    """The workload's tables as oracle jobs: run(frac) evaluates an evenly
+    spaced `frac` of each table's rows and returns (bytes, flops) of that work."""
     from oracle import oracle as O
     orc = O.default()
     threads = os.cpu_count() or 1
+    wl = WORKLOADS[workload]
+    fmt = wl["fmt"]
     fid = 0 if fmt == "q4_0" else 1
-    data = []
-    for (N, K) in shapes:
-        W = synth.weights(fmt, N, K, synth.seed_for(f"{fmt}_{N}x{K}"))
-        for M in Ms:
-            x = synth.activations(M, K, synth.seed_for(f"x_{K}_{M}"))
-            data.append((W, x, N, K, M))
-    # calibrate: 1 % of each table's rows
-    done_bytes, t_total = 0, 0.0
-    frac = 0.01
+    bb = 18 if fmt == "q4_0" else 34
+    jobs = []
+    if wl["kind"] in ("gemv", "prefill"):
+        for (N, K) in wl["shapes"]:
+            W = synth.weights(fmt, N, K, synth.seed_for(f"{fmt}_{N}x{K}"))
+            for M in wl["M"]:
+                x = synth.activations(M, K, synth.seed_for(f"x_{K}_{M}"))
+                jobs.append((W, x, N, K, M))
+    else:
+        for (E, slots, N, K) in wl["configs"]:
+            pool = synth.weights(fmt, E * N, K, synth.seed_for(f"moe_{E}x{N}x{K}"))
+            idx = synth.expert_indices(1, slots, E, synth.seed_for(f"moe_idx_{E}_{slots}"))[0]
+            x = synth.activations(slots, K, synth.seed_for(f"moe_x_{K}_{slots}"))
+            for sl in range(slots):
+                e = int(idx[sl])
+                jobs.append((pool[e * N:(e + 1) * N], x[sl:sl + 1], N, K, 1))
+
+    def run(frac):
+        b = f = 0
+        for (W, x, N, K, M) in jobs:
+            rows = np.linspace(0, N - 1, max(1, int(N * frac))).astype(np.int64)
+            orc.qmv_rows(fid, W, x, N, K, rows, nthreads=threads)
+            b += rows.size * (K // 32) * bb + 2 * M * K + 4 * M * rows.size
+            f += 2 * M * rows.size * K
+        return b, f
+    return run, threads, wl["kind"]
+
+
+def oracle_sample(workload, budget_s):
+    """Time the CPU oracle (as it stands) on a bounded row sample of the workload."""
+    run, threads, kind = oracle_tasks(workload)
+    done_b = done_f = 0
+    t_total = 0.0
+    frac = 0.001
     while True:
         t0 = time.perf_counter()
-        b = 0
-        for (W, x, N, K, M) in data:
-            nrows = max(1, int(N * frac))
-            rows = np.linspace(0, N - 1, nrows).astype(np.int64)
-            orc.qmv_rows(fid, W, x, N, K, rows, nthreads=threads)
-            b += nrows * (K // 32) * (18 if fmt == "q4_0" else 34) + 2 * M * K + 4 * M * nrows
+        b, f = run(frac)
         dt = time.perf_counter() - t0
-        done_bytes += b
+        done_b += b
+        done_f += f
         t_total += dt
         if t_total >= budget_s or frac >= 1.0:
             break
         frac = min(1.0, frac * max(1.5, min(8.0, budget_s / max(dt, 1e-3) / 4)))
-    return {"value": round(done_bytes / t_total / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"row samples (growing to {frac:.0%} of rows) of every table of the workload, "
+    val = done_f / t_total / 1e12 if kind == "prefill" else done_b / t_total / 1e9
+    return {"value": round(val, 5), "unit": "TFLOP/s" if kind == "prefill" else "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"evenly spaced row samples (up to {frac:.2%} of the rows) of every table of the workload, "
                       f"{t_total:.1f} s of fp64 oracle work, OpenMP over rows"}
 
 
@@ -412,83 +498,72 @@ def run_reference(args, rank, world):
     """The oracle arm: the CPU fp64 oracle timed on this host's cores."""
     if rank != 0:
         return None
-    fmt, shapes, Ms = WORKLOADS[args.workload]
-    from oracle import oracle as O
-    orc = O.default()
-    threads = os.cpu_count() or 1
-    fid = 0 if fmt == "q4_0" else 1
-    data = []
-    for (N, K) in shapes:
-        W = synth.weights(fmt, N, K, synth.seed_for(f"{fmt}_{N}x{K}"))
-        for M in Ms:
-            x = synth.activations(M, K, synth.seed_for(f"x_{K}_{M}"))
-            data.append((W, x, N, K, M))
+    run, threads, kind = oracle_tasks(args.workload)
     # Per step: the same fixed row sample of every table, sized so that the
     # whole run stays within about two minutes.
     per_step_budget = min(1.0, 120.0 / max(1, args.steps + args.warmup))
-    frac = 0.002
+    frac = 0.0005
     while True:
         t0 = time.perf_counter()
-        for (W, x, N, K, M) in data:
-            rows = np.linspace(0, N - 1, max(1, int(N * frac))).astype(np.int64)
-            orc.qmv_rows(fid, W, x, N, K, rows, nthreads=threads)
+        run(frac)
         dt = time.perf_counter() - t0
         if dt >= per_step_budget / 2 or frac >= 1.0:
             break
         frac = min(1.0, frac * 2)
-    samples = [(W, x, N, K, M, np.linspace(0, N - 1, max(1, int(N * frac))).astype(np.int64))
-               for (W, x, N, K, M) in data]
-    bb = 18 if fmt == "q4_0" else 34
-    step_bytes = sum(r.size * (K // 32) * bb + 2 * M * K + 4 * M * r.size for (_, _, _, K, M, r) in samples)
-
-    def step():
-        for (W, x, N, K, M, rows) in samples:
-            orc.qmv_rows(fid, W, x, N, K, rows, nthreads=threads)
-
     for _ in range(args.warmup):
-        step()
+        run(frac)
     t0 = time.perf_counter()
+    b = f = 0
     for _ in range(args.steps):
-        step()
+        bb_, ff_ = run(frac)
+        b += bb_
+        f += ff_
     dt = time.perf_counter() - t0
-    value = step_bytes * args.steps / dt / 1e9
-    sample = (f"{frac:.2%} of the rows of every table per step (evenly spaced), fp64 oracle, "
-              f"OpenMP over rows")
+    value = f / dt / 1e12 if kind == "prefill" else b / dt / 1e9
+    unit = "TFLOP/s" if kind == "prefill" else "GB/s"
+    wl = WORKLOADS[args.workload]
+    sample = f"{frac:.3%} of the rows of every table per step (evenly spaced), fp64 oracle, OpenMP over rows"
     return {
-        "metric": f"{fmt.upper()} GEMV HBM GB/s (algorithmic bytes; us/call per shape in 'sweep')",
-        "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "format": fmt, "shapes": [f"{N}x{K}" for (N, K) in shapes],
-                   "M": Ms},
+        "metric": metric_name(args.workload), "value": round(value, 5), "unit": unit, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "format": wl["fmt"]},
         "impl": "reference",
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 5), "unit": unit, "cores": threads, "kind": "oracle",
                          "sample": sample},
-        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "e2e": {"value": round(value, 5), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
 
 # ---------------------------------------------------------------------------------
 def ncu_case(spec):
-    """A handful of eager calls of one shape over rotated copies larger than L2
-    (a small, bounded program for an Nsight Compute capture)."""
+    """A handful of eager calls of one table over rotated copies larger than L2
+    (a small, bounded program for an Nsight Compute capture).
+    spec: q4_0:NxK:M | q8_0:NxK:M | prefill:NxK:M | moe:NxK:SLOTS (pool of 128)."""
     import torch
     import weight_quantized_decode_gb300 as q
-    fmt, shape, M = spec.split(":")
+    kind, shape, M = spec.split(":")
     N, K = (int(v) for v in shape.split("x"))
     M = int(M)
     dev = torch.device("cuda", 0)
+    fmt = "q8_0" if kind == "q8_0" else "q4_0"
     bb = 18 if fmt == "q4_0" else 34
-    wbytes = N * (K // 32) * bb
+    rows = 128 * N if kind == "moe" else N
+    wbytes = rows * (K // 32) * bb
     copies = max(2, math.ceil(2.5 * 128e6 / wbytes))
-    base = torch.from_numpy(synth.weights(fmt, N, K, synth.seed_for(f"{fmt}_{N}x{K}"))).to(dev)
+    base = torch.from_numpy(synth.weights(fmt, rows, K, synth.seed_for(f"{fmt}_{rows}x{K}"))).to(dev)
     W = base.unsqueeze(0).repeat(copies, 1, 1)
     x = torch.from_numpy(synth.activations(M, K, 1)).to(dev)
     y = torch.empty((M, N), dtype=torch.float32, device=dev)
-    fn = {"q4_0": q.qmv_q4_0_ptr, "q8_0": q.qmv_q8_0_ptr}[fmt]
     s = torch.cuda.current_stream().cuda_stream
+    idx = torch.from_numpy(synth.expert_indices(8, M, 128, 3)).to(dev) if kind == "moe" else None
     for i in range(8):
-        fn(W[i % copies].data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, s)
+        Wi = W[i % copies].data_ptr()
+        if kind == "moe":
+            q.qmv_moe_ptr(Wi, idx[i].data_ptr(), 128, x.data_ptr(), y.data_ptr(), N, K, M, s)
+        else:
+            fn = {"q4_0": q.qmv_q4_0_ptr, "q8_0": q.qmv_q8_0_ptr, "prefill": q.qmm_q4_0_prefill_ptr}[kind]
+            fn(Wi, x.data_ptr(), y.data_ptr(), N, K, M, s)
     torch.cuda.synchronize()
     print(f"ncu case {spec}: {copies} copies, 8 calls, ok")
 
@@ -524,8 +599,7 @@ def main():
     out, _, _ = run_ours(args, dist, rank, local, world)
     if rank == 0:
         if not args.no_cpu_baseline:
-            fmt, shapes, Ms = WORKLOADS[args.workload]
-            out["cpu_baseline"] = oracle_sample(fmt, shapes, Ms, args.cpu_budget)
+            out["cpu_baseline"] = oracle_sample(args.workload, args.cpu_budget)
         else:
             out["cpu_baseline"] = None
         print(json.dumps(out), flush=True)

@@ -12,6 +12,7 @@
 #include "qmv_gemv.cuh"
 #include "qmv_launch.h"
 #include "qmv_prefill.h"
+#include "qmv_tune_table.h"
 
 namespace qmv {
 
@@ -113,24 +114,67 @@ const Tune &tune_overrides()
     return t;
 }
 
+const TuneEntry *tune_lookup(int fmt, int64_t N, int64_t K, int M)
+{
+    for (const TuneEntry &e : kTuneTable)
+        if (e.fmt == fmt && e.M == M && e.N == N && e.K == K) return &e;
+    return nullptr;
+}
+
 // Choose the launch of the streaming kernel (or fall back to the generic one).
+// Order of precedence: QMV_GEMV_TUNE overrides (sweeps), the measured table
+// (qmv_tune_table.h), then a rule by weight bytes per SM.  Lanes-per-row (G)
+// fixes the summation order, so it depends only on (format, N, K, M) -- the
+// multi-expert call looks up its per-expert shape and matches a single call
+// bit for bit.
 Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
 {
     Plan pl{false, 0, 8, 0};
     if (p.K % 256 != 0 || p.K == 0) return pl;
-    if (reinterpret_cast<uintptr_t>(p.x) % 16 != 0) return pl;   // staged with 16-byte loads
+    if (reinterpret_cast<uintptr_t>(p.x) % 16 != 0) return pl;   // staged with 4-byte loads of 16-byte-aligned rows
     if (p.rows_total >= (int64_t(1) << 31)) return pl;             // 32-bit row indices
     const int64_t U = p.K / 256;
     if (U > (1 << 20)) return pl;
-    const Tune &tu = tune_overrides();
     p.U = static_cast<int>(U);
-    p.G = lanes_per_row(p.U, M);
-    if (tu.G == 1 || tu.G == 2 || tu.G == 4 || tu.G == 8 || tu.G == 16 || tu.G == 32) p.G = tu.G;
+    const int unit_bytes = fmt == kQ4_0 ? 144 : 272;
+    const Tune &tu = tune_overrides();
+    const TuneEntry *te = tune_lookup(fmt, p.N, p.K, M);
+
+    // defaults by rule
+    const int64_t wbytes_per_sm = p.N * (p.K / 256) * unit_bytes / (sms > 0 ? sms : 1);
+    const bool big = wbytes_per_sm > 128 * 1024 && M <= 2;
+    int G = lanes_per_row(p.U, M);
+    int warps = big ? 12 : 8;
+    int stages = 2;
+    int SP = 1;
+    int share = 1;
+    if (big && p.U % 8 == 0) {
+        G = 8;
+        if (p.U % 16 == 0) SP = 2;
+    }
+    if (te) {
+        if (te->G) G = te->G;
+        warps = te->warps;
+        stages = te->stages;
+        SP = te->SP;
+        share = te->share;
+    }
+    if (tu.G == 1 || tu.G == 2 || tu.G == 4 || tu.G == 8 || tu.G == 16 || tu.G == 32) G = tu.G;
+    if (tu.warps >= 1) warps = tu.warps;
+    if (tu.stages >= 1) stages = tu.stages;
+    if (tu.SP >= 1) SP = tu.SP;
+    if (tu.share >= 1) share = tu.share;
+    const int ctas_per_sm = (tu.ctas >= 1 && tu.ctas <= 4) ? tu.ctas : 1;
+
+    p.G = G;
     // Passes per stage: odd for G < 8 keeps the lanes of a quarter warp in
     // distinct banks; any value works for G >= 8.
-    p.SP = (tu.SP >= 1 && tu.SP <= 8 && ((tu.SP & 1) || p.G >= 8)) ? tu.SP : 1;
+    p.SP = (SP >= 1 && SP <= 8 && ((SP & 1) || p.G >= 8)) ? SP : 1;
+    if (share < 1 || share > 4) share = 1;
+    const int max_warps = (M <= 2) ? 16 : 8;
+    if (warps < 1 || warps > max_warps) warps = 8;
+
     const int RG = 32 / p.G;
-    const int ctas_per_sm = (tu.ctas >= 1 && tu.ctas <= 4) ? tu.ctas : 1;
     const int64_t groups = (p.rows_total + RG - 1) / RG;
     const int64_t max_grid = static_cast<int64_t>(sms) * ctas_per_sm;
     int grid = static_cast<int>(groups < max_grid ? groups : max_grid);
@@ -139,24 +183,14 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
     int64_t pmax = (rows_per_cta + p.N - 1) / p.N + 1;
     if (pmax > p.n_problems) pmax = p.n_problems;
     p.max_local_problems = static_cast<int>(pmax);
-    const int unit_bytes = fmt == kQ4_0 ? 144 : 272;
     const size_t xbytes = static_cast<size_t>(pmax) * M * p.U * kXUnitBytes;
-    const int share = (tu.share >= 1 && tu.share <= 4) ? tu.share : 1;
     const size_t budget = static_cast<size_t>(smem_optin) / (ctas_per_sm > share ? ctas_per_sm : share) - 1024;
     if (xbytes + 8 * 1024 > budget) return pl;
-    const int max_warps = (M <= 2) ? 16 : 8;
-    int warp_choices[2] = {8, 4};
-    int nchoices = 2;
-    if (tu.warps >= 1 && tu.warps <= max_warps) {
-        warp_choices[0] = tu.warps;
-        nchoices = 1;
-    }
-    for (int wi = 0; wi < nchoices; ++wi) {
-        const int warps = warp_choices[wi];
+    // Fit the ring: fewer stages, then fewer passes, then fewer warps.
+    for (int attempt = 0; attempt < 8; ++attempt) {
         const size_t per_stage = static_cast<size_t>(warps) * (32 * p.SP * unit_bytes + 8);
         int S = static_cast<int>((budget - xbytes) / per_stage);
-        if (S > 6) S = 6;
-        if (tu.stages >= 2 && tu.stages < S) S = tu.stages;
+        if (S > stages) S = stages;
         if (S >= 2) {
             p.S = S;
             pl.streaming = true;
@@ -165,6 +199,9 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
             pl.smem = gemv_smem_bytes(fmt, M, static_cast<int>(pmax), p.U, warps, S, p.SP);
             return pl;
         }
+        if (p.SP > 1) p.SP = 1;
+        else if (warps > 4) warps -= 4;
+        else break;
     }
     return pl;
 }
