@@ -62,12 +62,17 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int lanes_per_row(int U, int M)
 {
-    // Largest power of two dividing the number of 256-weight units of a row,
-    // capped so that the G distinct activation units a warp reads at once stay
-    // cheap for several tokens.
+    // G lanes share a row, each taking every G-th 256-weight unit.  Prefer a G
+    // that divides the row (no idle lanes); for rows of 8 or more units that no
+    // power of two of at least 8 divides (e.g. K = 2560: 10 units) take 8 and
+    // accept a partly idle last stage -- short rows otherwise leave most warps
+    // without work.  Capped for several tokens so the G distinct activation
+    // units a warp reads at once stay cheap.
     const int cap = (M <= 2) ? 16 : 8;
     int G = 1;
     while (G * 2 <= cap && U % (G * 2) == 0) G *= 2;
+    if (G < 8 && U >= 8) G = 8;
+    while (G > 1 && G > U) G >>= 1;
     return G;
 }
 

@@ -11,18 +11,20 @@
 //   * One CTA computes a 128-row (weights) x TN-column (tokens) tile of y^T in
 //     tensor memory: weights are the MMA's M side (128 lanes), tokens its N
 //     side (TN <= 256 columns of fp32).
-//   * Warp 4 (producer) streams packed 128-row x 256-K Q4_0 tiles (144 bytes
-//     per row) and 64-K activation tiles with TMA tensor copies into
-//     shared-memory rings; the activation tiles land in the 128-byte-swizzled
-//     K-major layout the tensor core reads.
-//   * Warps 0-3 (one thread per weight row) dequantise a packed row into fp16
-//     with the 0x6400|n bit trick, w = (c - 8) * d, and write 64-K slices of
-//     the A operand in the same swizzled layout.
-//   * Warp 5 allocates tensor memory and one thread issues tcgen05.mma
+//   * Warp 8 streams packed 128-row x 256-K Q4_0 tiles (144 bytes per row)
+//     and warp 10 streams 64-K activation tiles, both with TMA tensor copies,
+//     into their own shared-memory rings (deep enough to cover DRAM / L2
+//     latency); the activation tiles land in the 128-byte-swizzled K-major
+//     layout the tensor core reads.
+//   * Warps 0-7 (two threads per weight row, one block each) dequantise into
+//     fp16 with the 0x6400|n bit trick, w = (c - 8) * d, and write 64-K
+//     slices of the A operand in the same swizzled layout.
+//   * Warp 9 allocates tensor memory and one thread issues tcgen05.mma
 //     (kind::f16, 128 x TN x 16) four times per 64-K slice; tcgen05.commit
-//     releases the slice's buffers and finally signals the epilogue.
-//   * Warps 0-3 read the accumulator with tcgen05.ld (32 lanes x 32 columns
-//     per instruction) and store y with coalesced fp32 stores.
+//     releases the slice's A and B buffers and finally signals the epilogue.
+//   * Warps 0-7 read the accumulator with tcgen05.ld (32 lanes x 32 columns
+//     per instruction; warps w and w+4 share a lane quarter and split the
+//     columns) and store y with coalesced fp32 stores.
 // Operands are fp16: the activations arrive as fp16 and the dequantised
 // weight (c - 8) * d is rounded once to fp16.  Every wait is bounded.
 #include <cuda.h>
@@ -46,14 +48,17 @@ constexpr int kKChunk = 256;             // K per packed weight tile (8 Q4_0 blo
 constexpr int kPackedRowBytes = 144;
 constexpr int kPackedTileBytes = kBM * kPackedRowBytes;    // 18432
 constexpr int kATileBytes = kBM * kKB * 2;                 // 16384
-constexpr int kThreads = 192;
+constexpr int kThreads = 352;            // 8 dequant/epilogue warps, W producer, MMA, x producer
+constexpr int kDeqThreads = 256;
 
 struct PrefillParams {
     float *y;
     int *status;
     int64_t N, K, M;
     int TN;            // token columns per tile (multiple of 32, <= 256)
-    int SA;            // stages of (A, B) slices
+    int NW;            // packed-weight ring slots (256-K tiles)
+    int NA;            // dequantised-weight ring slots (64-K slices)
+    int NB;            // activation ring slots (64-K slices)
     uint32_t tmem_cols;
 };
 
@@ -191,18 +196,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 1024-byte alignment of the operand tiles (required by the 128-byte swizzle).
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-    const int SA = p.SA, TN = p.TN;
+    const int NW = p.NW, NA = p.NA, NB = p.NB, TN = p.TN;
     const int b_tile_bytes = TN * kKB * 2;
     uint8_t *a_tiles = smem;
-    uint8_t *b_tiles = a_tiles + SA * kATileBytes;
-    uint8_t *w_tiles = b_tiles + SA * b_tile_bytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(w_tiles + 2 * kPackedTileBytes);
-    uint64_t *wfull = bars;            // [2]
-    uint64_t *wempty = bars + 2;       // [2]
-    uint64_t *bfull = bars + 4;        // [SA]
-    uint64_t *afull = bfull + SA;      // [SA]
-    uint64_t *abempty = afull + SA;    // [SA]
-    uint64_t *accfull = abempty + SA;  // [1]
+    uint8_t *b_tiles = a_tiles + NA * kATileBytes;
+    uint8_t *w_tiles = b_tiles + NB * b_tile_bytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(w_tiles + NW * kPackedTileBytes);
+    uint64_t *wfull = bars;             // [NW]
+    uint64_t *wempty = wfull + NW;      // [NW]
+    uint64_t *afull = wempty + NW;      // [NA]
+    uint64_t *aempty = afull + NA;      // [NA]
+    uint64_t *bfull = aempty + NA;      // [NB]
+    uint64_t *bempty = bfull + NB;      // [NB]
+    uint64_t *accfull = bempty + NB;    // [1]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accfull + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -212,101 +218,110 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t m0 = static_cast<int64_t>(blockIdx.y) * TN;
     const int nK = static_cast<int>(p.K / kKB);            // 64-K slices
     const int nC = static_cast<int>(p.K / kKChunk);        // packed 256-K tiles
+    constexpr int kDeqWarps = kDeqThreads / 32;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NW; ++i) {
             mbar_init(&wfull[i], 1);
-            mbar_init(&wempty[i], 4);
+            mbar_init(&wempty[i], kDeqWarps);
         }
-        for (int s = 0; s < SA; ++s) {
-            mbar_init(&bfull[s], 1);
-            mbar_init(&afull[s], 4);
-            mbar_init(&abempty[s], 1);
+        for (int i = 0; i < NA; ++i) {
+            mbar_init(&afull[i], kDeqWarps);
+            mbar_init(&aempty[i], 1);
+        }
+        for (int i = 0; i < NB; ++i) {
+            mbar_init(&bfull[i], 1);
+            mbar_init(&bempty[i], 1);
         }
         mbar_init(accfull, 1);
         *abort_flag = 0;
         mbar_init_fence();
     }
-    if (warp == 5) tmem_alloc(tmem_slot, p.tmem_cols);
+    if (warp == 9) tmem_alloc(tmem_slot, p.tmem_cols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == 4) {
-        // ---------------- producer: TMA tensor copies ----------------
+    if (warp == 8) {
+        // ---------------- packed weights: TMA tensor copies, NW deep ----------------
         if (lane == 0) {
             pdl_wait_prior_grid();
-            int issued_w = 0, issued_b = 0;
+            int issued = 0;
             bool ok = true;
-            auto load_w = [&](int c) {
-                const int slot = c & 1;
-                if (!wait_or_abort(&wempty[slot], ((c >> 1) & 1) ^ 1, abort_flag, p.status)) return false;
+            for (int c = 0; c < nC; ++c) {
+                const int slot = c % NW;
+                if (!wait_or_abort(&wempty[slot], ((c / NW) & 1) ^ 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
                 mbar_arrive_expect_tx(&wfull[slot], kPackedTileBytes);
                 tma_load_2d(w_tiles + slot * kPackedTileBytes, &wmap, c * kPackedRowBytes, static_cast<int>(n0),
                             &wfull[slot]);
-                ++issued_w;
-                return true;
-            };
-            if (nC > 0) ok = load_w(0);
-            if (ok && nC > 1) ok = load_w(1);
-            for (int j = 0; ok && j < nK; ++j) {
-                const int s = j % SA;
-                if (!wait_or_abort(&abempty[s], ((j / SA) & 1) ^ 1, abort_flag, p.status)) {
+                ++issued;
+            }
+            if (!ok)   // let the copies already requested land before the CTA exits
+                for (int c = (issued > NW ? issued - NW : 0); c < issued; ++c)
+                    mbar_wait_bounded(&wfull[c % NW], (c / NW) & 1, nullptr);
+        }
+    } else if (warp == 10) {
+        // ---------------- activations: TMA tensor copies, NB deep ----------------
+        if (lane == 0) {
+            pdl_wait_prior_grid();
+            int issued = 0;
+            bool ok = true;
+            for (int j = 0; j < nK; ++j) {
+                const int s = j % NB;
+                if (!wait_or_abort(&bempty[s], ((j / NB) & 1) ^ 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 mbar_arrive_expect_tx(&bfull[s], b_tile_bytes);
                 tma_load_2d(b_tiles + s * b_tile_bytes, &xmap, j * kKB, static_cast<int>(m0), &bfull[s]);
-                ++issued_b;
-                // Two packed tiles ahead: chunk j/4 + 2 reuses the slot of chunk
-                // j/4, whose rows the dequantising warps read at its start.
-                if (j % 4 == 3 && j / 4 + 2 < nC) ok = load_w(j / 4 + 2);
+                ++issued;
             }
-            if (!ok) {
-                // Let the copies already requested land before the CTA exits.
-                for (int c = 0; c < issued_w; ++c)
-                    mbar_wait_bounded(&wfull[c & 1], (c >> 1) & 1, nullptr);
-                for (int j = (issued_b > SA ? issued_b - SA : 0); j < issued_b; ++j)
-                    mbar_wait_bounded(&bfull[j % SA], (j / SA) & 1, nullptr);
-            }
+            if (!ok)
+                for (int j = (issued > NB ? issued - NB : 0); j < issued; ++j)
+                    mbar_wait_bounded(&bfull[j % NB], (j / NB) & 1, nullptr);
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ---------------- MMA issue: one thread ----------------
         if (lane == 0) {
             const uint32_t idesc = f16_idesc(TN);
-            bool ok = true;
             int committed = 0;
+            bool ok = true;
             for (int j = 0; j < nK; ++j) {
-                const int s = j % SA;
-                const uint32_t par = (j / SA) & 1;
-                if (!wait_or_abort(&afull[s], par, abort_flag, p.status) ||
-                    !wait_or_abort(&bfull[s], par, abort_flag, p.status)) {
+                const int sa = j % NA, sb = j % NB;
+                if (!wait_or_abort(&afull[sa], (j / NA) & 1, abort_flag, p.status) ||
+                    !wait_or_abort(&bfull[sb], (j / NB) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a0 = smem_u32(a_tiles + s * kATileBytes);
-                const uint32_t b0 = smem_u32(b_tiles + s * b_tile_bytes);
+                const uint32_t a0 = smem_u32(a_tiles + sa * kATileBytes);
+                const uint32_t b0 = smem_u32(b_tiles + sb * b_tile_bytes);
 #pragma unroll
                 for (int kk = 0; kk < kKB / 16; ++kk)
                     mma_f16(tmem_base, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc, (j | kk) != 0);
-                mma_commit(&abempty[s]);
+                mma_commit(&aempty[sa]);
+                mma_commit(&bempty[sb]);
                 ++committed;
             }
             mma_commit(accfull);
             if (!ok && committed > 0) mbar_wait_bounded(accfull, 0, nullptr);
         }
     } else {
-        // ---------------- warps 0-3: dequantise, then the epilogue ----------------
-        const int r = threadIdx.x;                // weight row within the tile
+        // ---------------- warps 0-7: dequantise, then the epilogue ----------------
+        const int r = threadIdx.x & (kBM - 1);     // weight row within the tile
+        const int hsel = threadIdx.x >> 7;         // 0: even blocks of a slice, 1: odd blocks
         bool ok = true;
         for (int c = 0; ok && c < nC; ++c) {
-            const int slot = c & 1;
-            if (lane == 0) ok = wait_or_abort(&wfull[slot], (c >> 1) & 1, abort_flag, p.status);
+            const int slot = c % NW;
+            const uint32_t wpar = (c / NW) & 1;
+            if (lane == 0) ok = wait_or_abort(&wfull[slot], wpar, abort_flag, p.status);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok) break;
-            while (!mbar_try_wait(&wfull[slot], (c >> 1) & 1)) {
+            while (!mbar_try_wait(&wfull[slot], wpar)) {
             }
             uint32_t w[36];
             const uint8_t *src = w_tiles + slot * kPackedTileBytes + r * kPackedRowBytes;
@@ -323,44 +338,51 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int sub = 0; sub < 4; ++sub) {
                 const int j = c * 4 + sub;
-                const int s = j % SA;
-                if (lane == 0) ok = wait_or_abort(&abempty[s], ((j / SA) & 1) ^ 1, abort_flag, p.status);
+                const int sa = j % NA;
+                const uint32_t apar = ((j / NA) & 1) ^ 1;
+                if (lane == 0) ok = wait_or_abort(&aempty[sa], apar, abort_flag, p.status);
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) break;
-                while (!mbar_try_wait(&abempty[s], ((j / SA) & 1) ^ 1)) {
+                while (!mbar_try_wait(&aempty[sa], apar)) {
                 }
-                // blocks 2*sub (even: starts 2 bytes into word 9*sub) and 2*sub+1
+                // block 2*sub + hsel: even blocks start 2 bytes into word 9*sub
                 const int h = 9 * sub;
-                uint32_t qe[4], qo[4], fe[16], fo[16];
+                uint32_t q[4], f[16], dbits;
+                if (hsel == 0) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    qe[i] = __byte_perm(w[h + i], w[h + i + 1], 0x5432);
-                    qo[i] = w[h + 5 + i];
+                    for (int i = 0; i < 4; ++i) q[i] = __byte_perm(w[h + i], w[h + i + 1], 0x5432);
+                    dbits = w[h] & 0xffffu;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) q[i] = w[h + 5 + i];
+                    dbits = w[h + 4] >> 16;
                 }
-                dequant_block_f16(w[h] & 0xffffu, qe, fe);
-                dequant_block_f16(w[h + 4] >> 16, qo, fo);
-                uint8_t *arow = a_tiles + s * kATileBytes + (r >> 3) * 1024 + (r & 7) * 128;
+                dequant_block_f16(dbits, q, f);
+                uint8_t *arow = a_tiles + sa * kATileBytes + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const uint32_t *f = (ch < 4) ? &fe[4 * ch] : &fo[4 * (ch - 4)];
-                    *reinterpret_cast<uint4 *>(arow + ((ch ^ (r & 7)) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
+                for (int ch = 0; ch < 4; ++ch) {
+                    const int cc = 4 * hsel + ch;    // 16-byte chunk within the 128-byte row
+                    *reinterpret_cast<uint4 *>(arow + ((cc ^ (r & 7)) << 4)) =
+                        make_uint4(f[4 * ch], f[4 * ch + 1], f[4 * ch + 2], f[4 * ch + 3]);
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&afull[s]);
+                if (lane == 0) mbar_arrive(&afull[sa]);
             }
         }
-        // epilogue
+        // epilogue: warp w reads lane quarter (w & 3) and half (w >> 2) of the columns
         if (lane == 0) ok = ok && wait_or_abort(accfull, 0, abort_flag, p.status);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (ok) {
             while (!mbar_try_wait(accfull, 0)) {
             }
             tc_fence_after();
-            const int64_t row = n0 + 32 * warp + lane;
-            for (int c0 = 0; c0 < TN; c0 += 32) {
+            const int quarter = warp & 3;
+            const int64_t row = n0 + 32 * quarter + lane;
+            const int half_cols = TN / 2;
+            for (int c0 = (warp >> 2) * half_cols; c0 < (warp >> 2) * half_cols + half_cols; c0 += 32) {
                 uint32_t v[32];
-                tmem_ld_32cols(tmem_base + (static_cast<uint32_t>(32 * warp) << 16) + c0, v);
+                tmem_ld_32cols(tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) + c0, v);
                 if (row < p.N) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
@@ -374,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem_base, p.tmem_cols);
     }
@@ -403,9 +425,11 @@ EncodeTiledFn encode_fn()
 
 int pick_tn(int64_t M)
 {
+    // Multiples of 64 so that each of the two epilogue warps per lane quarter
+    // reads whole 32-column chunks.
     if (M >= 256) return 256;
-    int tn = static_cast<int>((M + 31) / 32) * 32;
-    return tn < 32 ? 32 : tn;
+    int tn = static_cast<int>((M + 63) / 64) * 64;
+    return tn < 64 ? 64 : tn;
 }
 
 }  // namespace
@@ -452,15 +476,29 @@ cudaError_t launch_prefill(const void *W, const void *x, float *y, int64_t N, in
     p.M = M;
     p.TN = TN;
     const int b_tile = TN * kKB * 2;
-    const size_t fixed = 1024 /*alignment slack*/ + 2 * kPackedTileBytes + 256 /*barriers etc.*/;
-    int SA = static_cast<int>((200 * 1024 - fixed) / (kATileBytes + b_tile));
-    if (SA > 4) SA = 4;
-    if (SA < 2) SA = 2;
-    p.SA = SA;
+    // Ring depths: the packed-weight ring must cover DRAM latency, the
+    // activation ring L2 latency, at the MMA rate of this tile width.
+    int NW = 4, NA = 3, NB = 3;
+    if (TN <= 64) {
+        NW = 6;
+        NB = 8;
+    } else if (TN <= 128) {
+        NW = 4;
+        NB = 6;
+    }
+    // alignment slack + barriers (2*(NW+NA+NB)+1 <= 41 of 8 bytes) + TMEM slot + flag
+    const size_t fixed = 1024 + 512;
+    auto total = [&] { return fixed + static_cast<size_t>(NW) * kPackedTileBytes + static_cast<size_t>(NA) * kATileBytes +
+                              static_cast<size_t>(NB) * b_tile; };
+    while (total() > 225 * 1024 && NB > 2) --NB;
+    while (total() > 225 * 1024 && NW > 2) --NW;
+    p.NW = NW;
+    p.NA = NA;
+    p.NB = NB;
     uint32_t cols = 32;
     while (cols < static_cast<uint32_t>(TN)) cols <<= 1;
     p.tmem_cols = cols;
-    const size_t smem = fixed + static_cast<size_t>(SA) * (kATileBytes + b_tile);
+    const size_t smem = total();
     cudaError_t e = ensure_smem_optin(reinterpret_cast<const void *>(prefill_kernel), smem);
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>((N + kBM - 1) / kBM), static_cast<unsigned>((M + TN - 1) / TN));
