@@ -67,6 +67,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// try_wait that lets the hardware suspend the thread (up to `hint_ns`) until
+// the phase completes, instead of returning at once: a waiting thread then
+// takes no issue slots from the warps doing the work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+constexpr uint32_t kSuspendHintNs = 20000;
+
 // Wait for phase `parity` of `bar`, giving up after kWaitLimitNs.  Called by a
 // single thread.  Returns false (and records kDevTimeout) on give-up.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int *status)
@@ -74,7 +92,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_timer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, kSuspendHintNs)) return true;
         if (global_timer_ns() - t0 > kWaitLimitNs) {
             if (status) atomicOr(status, kDevTimeout);
             return false;
@@ -91,7 +109,7 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, i
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     if (ok) {
         // The phase has completed; every lane observes it before touching data.
-        while (!mbar_try_wait(bar, parity)) {
+        while (!mbar_try_wait_sleep(bar, parity, kSuspendHintNs)) {
         }
     }
     return ok;

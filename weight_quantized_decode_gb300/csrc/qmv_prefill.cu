@@ -148,7 +148,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_timer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, kSuspendHintNs)) return true;
         if (*abort_flag) return false;
         if (global_timer_ns() - t0 > kWaitLimitNs) {
             *abort_flag = 1;
@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) ok = wait_or_abort(&wfull[slot], wpar, abort_flag, p.status);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok) break;
-            while (!mbar_try_wait(&wfull[slot], wpar)) {
+            while (!mbar_try_wait_sleep(&wfull[slot], wpar, kSuspendHintNs)) {
             }
             uint32_t w[36];
             const uint8_t *src = w_tiles + slot * kPackedTileBytes + r * kPackedRowBytes;
@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) ok = wait_or_abort(&aempty[sa], apar, abort_flag, p.status);
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) break;
-                while (!mbar_try_wait(&aempty[sa], apar)) {
+                while (!mbar_try_wait_sleep(&aempty[sa], apar, kSuspendHintNs)) {
                 }
                 // block 2*sub + hsel: even blocks start 2 bytes into word 9*sub
                 const int h = 9 * sub;
@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) ok = ok && wait_or_abort(accfull, 0, abort_flag, p.status);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (ok) {
-            while (!mbar_try_wait(accfull, 0)) {
+            while (!mbar_try_wait_sleep(accfull, 0, kSuspendHintNs)) {
             }
             tc_fence_after();
             const int quarter = warp & 3;
