@@ -247,11 +247,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- packed weights: TMA tensor copies, NW deep ----------------
         if (lane == 0) {
             pdl_wait_prior_grid();
-            int issued = 0;
+            // Loop state is kept incremental (no division): this thread's
+            // instruction latency is on the pipeline's critical path.
+            int issued = 0, slot = 0;
+            uint32_t phase = 1;            // an empty slot starts "released"
             bool ok = true;
             for (int c = 0; c < nC; ++c) {
-                const int slot = c % NW;
-                if (!wait_or_abort(&wempty[slot], ((c / NW) & 1) ^ 1, abort_flag, p.status)) {
+                if (!wait_or_abort(&wempty[slot], phase, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
@@ -259,6 +261,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_2d(w_tiles + slot * kPackedTileBytes, &wmap, c * kPackedRowBytes, static_cast<int>(n0),
                             &wfull[slot]);
                 ++issued;
+                if (++slot == NW) {
+                    slot = 0;
+                    phase ^= 1u;
+                }
             }
             if (!ok)   // let the copies already requested land before the CTA exits
                 for (int c = (issued > NW ? issued - NW : 0); c < issued; ++c)
@@ -268,17 +274,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- activations: TMA tensor copies, NB deep ----------------
         if (lane == 0) {
             pdl_wait_prior_grid();
-            int issued = 0;
+            int issued = 0, s = 0;
+            uint32_t phase = 1;
             bool ok = true;
             for (int j = 0; j < nK; ++j) {
-                const int s = j % NB;
-                if (!wait_or_abort(&bempty[s], ((j / NB) & 1) ^ 1, abort_flag, p.status)) {
+                if (!wait_or_abort(&bempty[s], phase, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 mbar_arrive_expect_tx(&bfull[s], b_tile_bytes);
                 tma_load_2d(b_tiles + s * b_tile_bytes, &xmap, j * kKB, static_cast<int>(m0), &bfull[s]);
                 ++issued;
+                if (++s == NB) {
+                    s = 0;
+                    phase ^= 1u;
+                }
             }
             if (!ok)
                 for (int j = (issued > NB ? issued - NB : 0); j < issued; ++j)
@@ -288,24 +298,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- MMA issue: one thread ----------------
         if (lane == 0) {
             const uint32_t idesc = f16_idesc(TN);
-            int committed = 0;
+            // Descriptors of slot 0; a slot (or a 16-wide K step: 32 bytes = 2
+            // in the 16-byte address field) is a plain addition.
+            const uint64_t a_desc0 = sw128_desc(smem_u32(a_tiles));
+            const uint64_t b_desc0 = sw128_desc(smem_u32(b_tiles));
+            const uint64_t a_step = kATileBytes >> 4, b_step = static_cast<uint64_t>(b_tile_bytes) >> 4;
+            int committed = 0, sa = 0, sb = 0;
+            uint32_t pa = 0, pb = 0;
+            uint64_t a_desc = a_desc0, b_desc = b_desc0;
             bool ok = true;
             for (int j = 0; j < nK; ++j) {
-                const int sa = j % NA, sb = j % NB;
-                if (!wait_or_abort(&afull[sa], (j / NA) & 1, abort_flag, p.status) ||
-                    !wait_or_abort(&bfull[sb], (j / NB) & 1, abort_flag, p.status)) {
+                if (!wait_or_abort(&afull[sa], pa, abort_flag, p.status) ||
+                    !wait_or_abort(&bfull[sb], pb, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a0 = smem_u32(a_tiles + sa * kATileBytes);
-                const uint32_t b0 = smem_u32(b_tiles + sb * b_tile_bytes);
-#pragma unroll
-                for (int kk = 0; kk < kKB / 16; ++kk)
-                    mma_f16(tmem_base, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc, (j | kk) != 0);
+                mma_f16(tmem_base, a_desc, b_desc, idesc, j != 0);
+                mma_f16(tmem_base, a_desc + 2, b_desc + 2, idesc, true);
+                mma_f16(tmem_base, a_desc + 4, b_desc + 4, idesc, true);
+                mma_f16(tmem_base, a_desc + 6, b_desc + 6, idesc, true);
                 mma_commit(&aempty[sa]);
                 mma_commit(&bempty[sb]);
                 ++committed;
+                if (++sa == NA) {
+                    sa = 0;
+                    pa ^= 1u;
+                    a_desc = a_desc0;
+                } else {
+                    a_desc += a_step;
+                }
+                if (++sb == NB) {
+                    sb = 0;
+                    pb ^= 1u;
+                    b_desc = b_desc0;
+                } else {
+                    b_desc += b_step;
+                }
             }
             mma_commit(accfull);
             if (!ok && committed > 0) mbar_wait_bounded(accfull, 0, nullptr);
@@ -315,9 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = threadIdx.x & (kBM - 1);     // weight row within the tile
         const int hsel = threadIdx.x >> 7;         // 0: even blocks of a slice, 1: odd blocks
         bool ok = true;
+        int slot = 0, sa = 0;
+        uint32_t wpar = 0, apar = 1;
         for (int c = 0; ok && c < nC; ++c) {
-            const int slot = c % NW;
-            const uint32_t wpar = (c / NW) & 1;
             if (lane == 0) ok = wait_or_abort(&wfull[slot], wpar, abort_flag, p.status);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok) break;
@@ -335,11 +364,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&wempty[slot]);
+            if (++slot == NW) {
+                slot = 0;
+                wpar ^= 1u;
+            }
 #pragma unroll
             for (int sub = 0; sub < 4; ++sub) {
-                const int j = c * 4 + sub;
-                const int sa = j % NA;
-                const uint32_t apar = ((j / NA) & 1) ^ 1;
                 if (lane == 0) ok = wait_or_abort(&aempty[sa], apar, abort_flag, p.status);
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) break;
@@ -368,6 +398,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&afull[sa]);
+                if (++sa == NA) {
+                    sa = 0;
+                    apar ^= 1u;
+                }
             }
         }
         // epilogue: warp w reads lane quarter (w & 3) and half (w >> 2) of the columns
