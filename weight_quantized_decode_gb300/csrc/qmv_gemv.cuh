@@ -84,7 +84,8 @@ __host__ __device__ inline size_t gemv_smem_bytes(int fmt, int M, int n_problems
     const size_t xbytes = static_cast<size_t>(n_problems) * M * U * kXUnitBytes;
     const size_t ring = static_cast<size_t>(warps) * S * 32 * SP * unit_bytes;
     const size_t bars = static_cast<size_t>(warps) * S * 8;
-    return xbytes + ring + bars;
+    const size_t idx = (static_cast<size_t>(n_problems) * 4 + 15) / 16 * 16;   // expert indices (multi-expert call)
+    return xbytes + ring + bars + idx;
 }
 
 // Permuted activation layout.  Within a block, the activation of element e
@@ -302,8 +303,9 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
     const int slot_bytes = 32 * SP * T::kUnitBytes;
     uint8_t *xs = smem;
     uint8_t *ring = smem + xbytes + static_cast<size_t>(warp) * S * slot_bytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + xbytes + static_cast<size_t>(warps) * S * slot_bytes) +
-                     warp * S;
+    uint64_t *bars_all = reinterpret_cast<uint64_t *>(smem + xbytes + static_cast<size_t>(warps) * S * slot_bytes);
+    uint64_t *bars = bars_all + warp * S;
+    int32_t *sidx = reinterpret_cast<int32_t *>(bars_all + warps * S);   // this CTA's expert indices
 
     // This CTA's contiguous range of (problem, row) pairs.
     const uint32_t R = static_cast<uint32_t>(p.rows_total);
@@ -344,7 +346,7 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
                     const uint32_t row = row0 + lr;
                     const uint32_t prob = row / N;
                     const uint32_t n = row - prob * N;
-                    const int64_t e = p.expert_idx[prob];
+                    const int64_t e = sidx[prob - prob_lo];
                     if (e >= 0 && e < p.n_experts) is_row = p.W + (e * p.N + n) * p.row_bytes;
                 } else {
                     is_row = cta_rows + static_cast<int64_t>(lr) * p.row_bytes;
@@ -378,6 +380,12 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
     for (int i = 0; i < early; ++i) issue_next();
 
     pdl_wait_prior_grid();
+
+    if (MOE) {
+        // The CTA's expert indices, once, before any copy needs them.
+        for (int i = threadIdx.x; i <= prob_hi - prob_lo; i += blockDim.x) sidx[i] = p.expert_idx[prob_lo + i];
+        __syncthreads();
+    }
 
     // Stage the activations: permuted pair order, 528-byte padded units.  Each
     // thread builds whole 16-byte chunks of the permuted layout from four
@@ -472,7 +480,7 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
             if (MOE) {
                 prob = row_ok ? (row0 + lr) / N : static_cast<uint32_t>(prob_lo);
                 if (row_ok) {
-                    const int64_t e = p.expert_idx[prob];
+                    const int64_t e = sidx[prob - prob_lo];
                     row_ok = (e >= 0 && e < p.n_experts);
                 }
                 xrow = xs + static_cast<size_t>(prob - prob_lo) * M * xstride;

@@ -57,8 +57,7 @@ struct PrefillParams {
     int64_t N, K, M;
     int TN;            // token columns per tile (multiple of 32, <= 256)
     int NW;            // packed-weight ring slots (256-K tiles)
-    int NA;            // dequantised-weight ring slots (64-K slices)
-    int NB;            // activation ring slots (64-K slices)
+    int NS;            // slice ring slots: one dequantised-weight and one activation tile each
     uint32_t tmem_cols;
 };
 
@@ -119,6 +118,26 @@ __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
         ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate ? 1 : 0)
+        : "memory");
+}
+
+// Four K=16 steps over one 64-K slice: descriptors advance by 32 bytes (2 in
+// the 16-byte address field) per step.  `first` clears the accumulator.
+__device__ __forceinline__ void mma_f16_slice(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              bool first)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        ".reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+        "setp.eq.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 q, 0, 0;\n\t"
+        "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"
+        "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, q;\n\t}"
+        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(first ? 1 : 0)
         : "memory");
 }
 
@@ -196,19 +215,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 1024-byte alignment of the operand tiles (required by the 128-byte swizzle).
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-    const int NW = p.NW, NA = p.NA, NB = p.NB, TN = p.TN;
+    const int NW = p.NW, NS = p.NS, TN = p.TN;
     const int b_tile_bytes = TN * kKB * 2;
     uint8_t *a_tiles = smem;
-    uint8_t *b_tiles = a_tiles + NA * kATileBytes;
-    uint8_t *w_tiles = b_tiles + NB * b_tile_bytes;
+    uint8_t *b_tiles = a_tiles + NS * kATileBytes;
+    uint8_t *w_tiles = b_tiles + NS * b_tile_bytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(w_tiles + NW * kPackedTileBytes);
     uint64_t *wfull = bars;             // [NW]
     uint64_t *wempty = wfull + NW;      // [NW]
-    uint64_t *afull = wempty + NW;      // [NA]
-    uint64_t *aempty = afull + NA;      // [NA]
-    uint64_t *bfull = aempty + NA;      // [NB]
-    uint64_t *bempty = bfull + NB;      // [NB]
-    uint64_t *accfull = bempty + NB;    // [1]
+    uint64_t *afull = wempty + NW;      // [NS] dequantised slice written
+    uint64_t *bfull = afull + NS;       // [NS] activation slice landed
+    uint64_t *sempty = bfull + NS;      // [NS] the slice's MMAs are done: both tiles free
+    uint64_t *accfull = sempty + NS;    // [1]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accfull + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -225,13 +243,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&wfull[i], 1);
             mbar_init(&wempty[i], kDeqWarps);
         }
-        for (int i = 0; i < NA; ++i) {
+        for (int i = 0; i < NS; ++i) {
             mbar_init(&afull[i], kDeqWarps);
-            mbar_init(&aempty[i], 1);
-        }
-        for (int i = 0; i < NB; ++i) {
             mbar_init(&bfull[i], 1);
-            mbar_init(&bempty[i], 1);
+            mbar_init(&sempty[i], 1);
         }
         mbar_init(accfull, 1);
         *abort_flag = 0;
@@ -278,21 +293,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 1;
             bool ok = true;
             for (int j = 0; j < nK; ++j) {
-                if (!wait_or_abort(&bempty[s], phase, abort_flag, p.status)) {
+                if (!wait_or_abort(&sempty[s], phase, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 mbar_arrive_expect_tx(&bfull[s], b_tile_bytes);
                 tma_load_2d(b_tiles + s * b_tile_bytes, &xmap, j * kKB, static_cast<int>(m0), &bfull[s]);
                 ++issued;
-                if (++s == NB) {
+                if (++s == NS) {
                     s = 0;
                     phase ^= 1u;
                 }
             }
             if (!ok)
-                for (int j = (issued > NB ? issued - NB : 0); j < issued; ++j)
-                    mbar_wait_bounded(&bfull[j % NB], (j / NB) & 1, nullptr);
+                for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j)
+                    mbar_wait_bounded(&bfull[j % NS], (j / NS) & 1, nullptr);
         }
     } else if (warp == 9) {
         // ---------------- MMA issue: one thread ----------------
@@ -303,36 +318,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t a_desc0 = sw128_desc(smem_u32(a_tiles));
             const uint64_t b_desc0 = sw128_desc(smem_u32(b_tiles));
             const uint64_t a_step = kATileBytes >> 4, b_step = static_cast<uint64_t>(b_tile_bytes) >> 4;
-            int committed = 0, sa = 0, sb = 0;
-            uint32_t pa = 0, pb = 0;
+            int committed = 0, s = 0;
+            uint32_t ph = 0;
             uint64_t a_desc = a_desc0, b_desc = b_desc0;
             bool ok = true;
             for (int j = 0; j < nK; ++j) {
-                if (!wait_or_abort(&afull[sa], pa, abort_flag, p.status) ||
-                    !wait_or_abort(&bfull[sb], pb, abort_flag, p.status)) {
+                if (!wait_or_abort(&bfull[s], ph, abort_flag, p.status) ||
+                    !wait_or_abort(&afull[s], ph, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                mma_f16(tmem_base, a_desc, b_desc, idesc, j != 0);
-                mma_f16(tmem_base, a_desc + 2, b_desc + 2, idesc, true);
-                mma_f16(tmem_base, a_desc + 4, b_desc + 4, idesc, true);
-                mma_f16(tmem_base, a_desc + 6, b_desc + 6, idesc, true);
-                mma_commit(&aempty[sa]);
-                mma_commit(&bempty[sb]);
+                mma_f16_slice(tmem_base, a_desc, b_desc, idesc, j == 0);
+                mma_commit(&sempty[s]);
                 ++committed;
-                if (++sa == NA) {
-                    sa = 0;
-                    pa ^= 1u;
+                if (++s == NS) {
+                    s = 0;
+                    ph ^= 1u;
                     a_desc = a_desc0;
-                } else {
-                    a_desc += a_step;
-                }
-                if (++sb == NB) {
-                    sb = 0;
-                    pb ^= 1u;
                     b_desc = b_desc0;
                 } else {
+                    a_desc += a_step;
                     b_desc += b_step;
                 }
             }
@@ -370,10 +376,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 #pragma unroll
             for (int sub = 0; sub < 4; ++sub) {
-                if (lane == 0) ok = wait_or_abort(&aempty[sa], apar, abort_flag, p.status);
+                if (lane == 0) ok = wait_or_abort(&sempty[sa], apar, abort_flag, p.status);
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) break;
-                while (!mbar_try_wait_sleep(&aempty[sa], apar, kSuspendHintNs)) {
+                while (!mbar_try_wait_sleep(&sempty[sa], apar, kSuspendHintNs)) {
                 }
                 // block 2*sub + hsel: even blocks start 2 bytes into word 9*sub
                 const int h = 9 * sub;
@@ -398,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&afull[sa]);
-                if (++sa == NA) {
+                if (++sa == NS) {
                     sa = 0;
                     apar ^= 1u;
                 }
@@ -512,23 +518,22 @@ cudaError_t launch_prefill(const void *W, const void *x, float *y, int64_t N, in
     const int b_tile = TN * kKB * 2;
     // Ring depths: the packed-weight ring must cover DRAM latency, the
     // activation ring L2 latency, at the MMA rate of this tile width.
-    int NW = 4, NA = 3, NB = 3;
+    int NW = 4, NS = 3;
     if (TN <= 64) {
-        NW = 6;
-        NB = 8;
-    } else if (TN <= 128) {
         NW = 4;
-        NB = 6;
+        NS = 6;
+    } else if (TN <= 128) {
+        NW = 3;
+        NS = 5;
     }
-    // alignment slack + barriers (2*(NW+NA+NB)+1 <= 41 of 8 bytes) + TMEM slot + flag
+    // alignment slack + barriers (2*NW + 3*NS + 1 of 8 bytes) + TMEM slot + flag
     const size_t fixed = 1024 + 512;
-    auto total = [&] { return fixed + static_cast<size_t>(NW) * kPackedTileBytes + static_cast<size_t>(NA) * kATileBytes +
-                              static_cast<size_t>(NB) * b_tile; };
-    while (total() > 225 * 1024 && NB > 2) --NB;
+    auto total = [&] { return fixed + static_cast<size_t>(NW) * kPackedTileBytes +
+                              static_cast<size_t>(NS) * (kATileBytes + b_tile); };
+    while (total() > 225 * 1024 && NS > 2) --NS;
     while (total() > 225 * 1024 && NW > 2) --NW;
     p.NW = NW;
-    p.NA = NA;
-    p.NB = NB;
+    p.NS = NS;
     uint32_t cols = 32;
     while (cols < static_cast<uint32_t>(TN)) cols <<= 1;
     p.tmem_cols = cols;
