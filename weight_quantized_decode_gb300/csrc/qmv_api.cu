@@ -71,7 +71,9 @@ int lanes_per_row(int U, int M)
     const int cap = (M <= 2) ? 16 : 8;
     int G = 1;
     while (G * 2 <= cap && U % (G * 2) == 0) G *= 2;
-    if (G < 8 && U >= 8) G = 8;
+    // For several tokens the kernel is bound by arithmetic, and idle lanes cost
+    // more than the lost parallelism.
+    if (G < 8 && U >= 8 && M <= 2) G = 8;
     while (G > 1 && G > U) G >>= 1;
     return G;
 }
@@ -156,6 +158,14 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
     if (big && p.U % 8 == 0) {
         G = 8;
         if (p.U % 16 == 0) SP = 2;
+    }
+    if (p.n_problems > 1) {
+        // The multi-expert call cannot request weights before the previous
+        // kernel (which may have written the expert indices) completes, so it
+        // keeps more warps and stages in flight from the start (measured on
+        // 10 x 640x2560 and 8 x 512x2048 expert calls).
+        warps = 12;
+        stages = 3;
     }
     if (te) {
         if (te->G) G = te->G;
