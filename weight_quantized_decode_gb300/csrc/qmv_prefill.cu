@@ -11,20 +11,25 @@
 //   * One CTA computes a 128-row (weights) x TN-column (tokens) tile of y^T in
 //     tensor memory: weights are the MMA's M side (128 lanes), tokens its N
 //     side (TN <= 256 columns of fp32).
-//   * Warp 8 streams packed 128-row x 256-K Q4_0 tiles (144 bytes per row)
-//     and warp 10 streams 64-K activation tiles, both with TMA tensor copies,
+//   * Roles by warp: a warp runs on scheduler (warp id mod 4).  Scheduler 1
+//     hosts only the MMA-issuing warp and the two copy producers, which sleep
+//     in mbarrier waits, so the single MMA-issuing thread is not starved of
+//     issue slots by the dequantising warps on schedulers 0, 2 and 3.
+//   * Warp 5 streams packed 128-row x 256-K Q4_0 tiles (144 bytes per row)
+//     and warp 9 streams 64-K activation tiles, both with TMA tensor copies,
 //     into their own shared-memory rings (deep enough to cover DRAM / L2
 //     latency); the activation tiles land in the 128-byte-swizzled K-major
 //     layout the tensor core reads.
-//   * Warps 0-7 (two threads per weight row, one block each) dequantise into
-//     fp16 with the 0x6400|n bit trick, w = (c - 8) * d, and write 64-K
-//     slices of the A operand in the same swizzled layout.
-//   * Warp 9 allocates tensor memory and one thread issues tcgen05.mma
+//   * Warps 0, 2, 3, 4, 6, 7, 8, 10 (two threads per weight row, one block
+//     each) dequantise into fp16 with the 0x6400|n bit trick,
+//     w = (c - 8) * d, and write 64-K slices of the A operand in the same
+//     swizzled layout.
+//   * Warp 1 allocates tensor memory and one thread issues tcgen05.mma
 //     (kind::f16, 128 x TN x 16) four times per 64-K slice; tcgen05.commit
 //     releases the slice's A and B buffers and finally signals the epilogue.
-//   * Warps 0-7 read the accumulator with tcgen05.ld (32 lanes x 32 columns
-//     per instruction; warps w and w+4 share a lane quarter and split the
-//     columns) and store y with coalesced fp32 stores.
+//   * All warps read the accumulator with tcgen05.ld (32 lanes x 32 columns
+//     per instruction; warp w reads lane quarter w mod 4, the warps of a
+//     quarter split the columns) and store y with coalesced fp32 stores.
 // Operands are fp16: the activations arrive as fp16 and the dequantised
 // weight (c - 8) * d is rounded once to fp16.  Every wait is bounded.
 #include <cuda.h>
@@ -48,7 +53,8 @@ constexpr int kKChunk = 256;             // K per packed weight tile (8 Q4_0 blo
 constexpr int kPackedRowBytes = 144;
 constexpr int kPackedTileBytes = kBM * kPackedRowBytes;    // 18432
 constexpr int kATileBytes = kBM * kKB * 2;                 // 16384
-constexpr int kThreads = 352;            // 8 dequant/epilogue warps, W producer, MMA, x producer
+constexpr int kThreads = 352;            // 11 warps: 8 dequantising, MMA issue, 2 copy producers
+constexpr int kMmaWarp = 1, kWProducerWarp = 5, kXProducerWarp = 9;
 constexpr int kDeqThreads = 256;
 
 struct PrefillParams {
@@ -252,13 +258,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         mbar_init_fence();
     }
-    if (warp == 9) tmem_alloc(tmem_slot, p.tmem_cols);
+    if (warp == kMmaWarp) tmem_alloc(tmem_slot, p.tmem_cols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == 8) {
+    bool ok = true;
+    if (warp == kWProducerWarp) {
         // ---------------- packed weights: TMA tensor copies, NW deep ----------------
         if (lane == 0) {
             pdl_wait_prior_grid();
@@ -266,7 +273,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             // instruction latency is on the pipeline's critical path.
             int issued = 0, slot = 0;
             uint32_t phase = 1;            // an empty slot starts "released"
-            bool ok = true;
             for (int c = 0; c < nC; ++c) {
                 if (!wait_or_abort(&wempty[slot], phase, abort_flag, p.status)) {
                     ok = false;
@@ -285,13 +291,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = (issued > NW ? issued - NW : 0); c < issued; ++c)
                     mbar_wait_bounded(&wfull[c % NW], (c / NW) & 1, nullptr);
         }
-    } else if (warp == 10) {
-        // ---------------- activations: TMA tensor copies, NB deep ----------------
+    } else if (warp == kXProducerWarp) {
+        // ---------------- activations: TMA tensor copies, one per slice slot ----------------
         if (lane == 0) {
             pdl_wait_prior_grid();
             int issued = 0, s = 0;
             uint32_t phase = 1;
-            bool ok = true;
             for (int j = 0; j < nK; ++j) {
                 if (!wait_or_abort(&sempty[s], phase, abort_flag, p.status)) {
                     ok = false;
@@ -309,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j)
                     mbar_wait_bounded(&bfull[j % NS], (j / NS) & 1, nullptr);
         }
-    } else if (warp == 9) {
+    } else if (warp == kMmaWarp) {
         // ---------------- MMA issue: one thread ----------------
         if (lane == 0) {
             const uint32_t idesc = f16_idesc(TN);
@@ -321,7 +326,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             int committed = 0, s = 0;
             uint32_t ph = 0;
             uint64_t a_desc = a_desc0, b_desc = b_desc0;
-            bool ok = true;
             for (int j = 0; j < nK; ++j) {
                 if (!wait_or_abort(&bfull[s], ph, abort_flag, p.status) ||
                     !wait_or_abort(&afull[s], ph, abort_flag, p.status)) {
@@ -346,10 +350,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok && committed > 0) mbar_wait_bounded(accfull, 0, nullptr);
         }
     } else {
-        // ---------------- warps 0-7: dequantise, then the epilogue ----------------
-        const int r = threadIdx.x & (kBM - 1);     // weight row within the tile
-        const int hsel = threadIdx.x >> 7;         // 0: even blocks of a slice, 1: odd blocks
-        bool ok = true;
+        // ---------------- dequantising warps ----------------
+        // warps 0, 2, 3, 4, 6, 7, 8, 10 -> dequantiser index 0..7
+        const int dw = warp - (warp >= 1) - (warp >= 5) - (warp >= 9);
+        const int dt = dw * 32 + lane;
+        const int r = dt & (kBM - 1);              // weight row within the tile
+        const int hsel = dt >> 7;                  // 0: even blocks of a slice, 1: odd blocks
         int slot = 0, sa = 0;
         uint32_t wpar = 0, apar = 1;
         for (int c = 0; ok && c < nC; ++c) {
@@ -410,25 +416,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        // epilogue: warp w reads lane quarter (w & 3) and half (w >> 2) of the columns
-        if (lane == 0) ok = ok && wait_or_abort(accfull, 0, abort_flag, p.status);
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (ok) {
-            while (!mbar_try_wait_sleep(accfull, 0, kSuspendHintNs)) {
-            }
-            tc_fence_after();
-            const int quarter = warp & 3;
-            const int64_t row = n0 + 32 * quarter + lane;
-            const int half_cols = TN / 2;
-            for (int c0 = (warp >> 2) * half_cols; c0 < (warp >> 2) * half_cols + half_cols; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld_32cols(tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) + c0, v);
-                if (row < p.N) {
+    }
+
+    // ---------------- epilogue: every warp ----------------
+    // Warp w reads TMEM lane quarter w mod 4; the warps of a quarter take its
+    // 32-column chunks round-robin.  A role that gave up skips it.
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (lane == 0) ok = ok && wait_or_abort(accfull, 0, abort_flag, p.status);
+    ok = __shfl_sync(0xffffffffu, (ok && !*abort_flag) ? 1 : 0, 0) != 0;
+    if (ok) {
+        while (!mbar_try_wait_sleep(accfull, 0, kSuspendHintNs)) {
+        }
+        tc_fence_after();
+        const int quarter = warp & 3;
+        const int nq = (kThreads / 32 - quarter + 3) / 4;   // warps in this quarter
+        const int rank = warp >> 2;
+        const int64_t row = n0 + 32 * quarter + lane;
+        for (int c0 = 32 * rank; c0 < TN; c0 += 32 * nq) {
+            uint32_t v[32];
+            tmem_ld_32cols(tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) + c0, v);
+            if (row < p.N) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int64_t m = m0 + c0 + i;
-                        if (m < p.M) p.y[m * p.N + row] = __uint_as_float(v[i]);
-                    }
+                for (int i = 0; i < 32; ++i) {
+                    const int64_t m = m0 + c0 + i;
+                    if (m < p.M) p.y[m * p.N + row] = __uint_as_float(v[i]);
                 }
             }
         }
@@ -436,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem_base, p.tmem_cols);
     }
