@@ -332,7 +332,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                tc_fence_after();
+                // The operands arrive through the async proxy (TMA writes, and
+                // dequantised writes published with fence.proxy.async before the
+                // arrive): the barrier wait is enough, no tcgen05 fence per slice.
                 mma_f16_slice(tmem_base, a_desc, b_desc, idesc, j == 0);
                 mma_commit(&sempty[s]);
                 ++committed;
