@@ -40,11 +40,12 @@
  *   - N == 0 or M == 0: nothing to do, QMV_OK, nothing enqueued.
  *     K == 0: y is filled with zeros (an empty sum).
  *   - The library is thread-safe for concurrent calls on different streams.
- *   - Weights are read-only inputs.  By default the decode kernels use
- *     programmatic dependent launch: a call may begin streaming W while the
- *     previous kernel on `stream` is still finishing, and reads x / writes y
- *     only after that kernel has completed.  If the kernel that runs right
- *     before a call on the same stream WRITES W, call qmv_set_pdl(0) first.
+ *   - Weights are read-only inputs.  By default the decode and prefill kernels
+ *     use programmatic dependent launch: a call may begin streaming (and, for
+ *     prefill, dequantising) W while the previous kernel on `stream` is still
+ *     finishing, and reads x / writes y only after that kernel has completed.
+ *     If the kernel that runs right before a call on the same stream WRITES W,
+ *     call qmv_set_pdl(0) first.
  */
 #ifndef QMV_H
 #define QMV_H
@@ -130,9 +131,9 @@ QMV_API qmv_status qmv_moe(const void *W_pool, const int32_t *expert_idx, int64_
  * a tensor-core multiply" -- "What we'd do next", item 3).  On sm_103a: packed
  * W tiles staged by bulk copies, dequantised to 16-bit in shared memory, fed to
  * tcgen05.mma with fp32 accumulators in tensor memory.
- *   W : Q4_0 bytes [N][K/32*18], 16-byte aligned; requires K % 256 == 0 and
- *       N % 128 == 0 for the tensor-core kernel (other shapes take the
- *       generic kernel).
+ *   W : Q4_0 bytes [N][K/32*18], 16-byte aligned.  The tensor-core kernel
+ *       takes K % 256 == 0 (any N: a ragged last 128-row tile is masked);
+ *       other K take the generic kernel.
  *   x : fp16 [M][K], 16-byte aligned.  y : fp32 [M][N].  M >= 0.
  */
 QMV_API qmv_status qmm_q4_0_prefill(const void *W, const void *x, float *y,
@@ -145,8 +146,8 @@ QMV_API qmv_status qmm_q4_0_prefill(const void *W, const void *x, float *y,
  */
 QMV_API qmv_status qmv_device_status(qmv_stream_t stream, int32_t *out);
 
-/* Programmatic dependent launch for the decode kernels: 1 = on (default),
- * 0 = off (plain stream order).  Process-wide; affects later calls. */
+/* Programmatic dependent launch for the decode and prefill kernels: 1 = on
+ * (default), 0 = off (plain stream order).  Process-wide; affects later calls. */
 QMV_API void qmv_set_pdl(int enable);
 
 /* Static description of a status code. */

@@ -155,6 +155,27 @@ def test_back_to_back_calls_keep_dependencies(cuda_lib, orc):
     assert H.normalised_error(y.cpu().numpy(), y_ref, S) <= H.TOL
 
 
+def test_prefill_back_to_back_keeps_dependencies(cuda_lib, orc):
+    """The prefill kernel also starts streaming and dequantising W before the
+    kernel ahead of it finishes; the activations it multiplies must still be
+    the ones that kernel wrote."""
+    q = cuda_lib
+    M, K, N = 96, 1024, 384
+    W1 = synth.q4_0_weights(K, K, 34)
+    W2 = synth.q4_0_weights(N, K, 35)
+    x0 = synth.activations(M, K, 36)
+    Wd1, Wd2 = dev(W1), dev(W2)
+    h = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    q.qmm_q4_0_prefill(Wd1, dev(x0), h)              # h = x0 @ W1^T
+    hx = (h * 0.25).to(torch.float16)                 # a torch kernel between the calls
+    y = q.qmm_q4_0_prefill(Wd2, hx)                   # consumes hx
+    y2 = q.qmm_q4_0_prefill(Wd2, hx)                  # straight after another prefill
+    torch.cuda.synchronize()
+    y_ref, S = orc.qmv(0, W2, hx.cpu().numpy(), N, K, nthreads=8)
+    assert H.normalised_error(y.cpu().numpy(), y_ref, S) <= H.TOL
+    assert torch.equal(y, y2)
+
+
 # -- full-size configurations (sampled outputs) ----------------------------------------
 
 def _sample_rows(N, k=96, seed=0):
@@ -230,6 +251,51 @@ def test_moe_bad_index_sets_status_and_nans(cuda_lib):
     ok = q.qmv_moe(pool, dev(np.array([1, 3, 2], dtype=np.int32)), E, x, N)
     assert torch.equal(ok[0], y[0]) and torch.equal(ok[2], y[2])
     assert q.qmv_device_status() == 0
+
+
+# -- launch shapes forced through the tuning override ----------------------------------
+
+OVERRIDES = {
+    # Launch shapes the measured table and the rule do not pick: lanes per row
+    # from 1 to 32, odd passes per stage, deep rings, two CTAs per SM; the
+    # multi-expert form must still equal the single calls bit for bit.
+    "G=4,SP=3": ["gemv:q4_0:77:6144:1", "gemv:q8_0:130:2560:2", "moe:q4_0:64:2560:5"],
+    "G=32,warps=4": ["gemv:q4_0:40:8192:1", "gemv:q8_0:130:2560:4", "moe:q4_0:96:4096:6"],
+    "G=1,SP=5,stages=3": ["gemv:q4_0:16:14336:1", "gemv:q4_0:33:2048:3", "moe:q4_0:20:2048:3"],
+    "warps=16,stages=4,G=2": ["gemv:q4_0:100:4096:2", "gemv:q8_0:9:3072:1"],
+    "ctas=2,share=2": ["gemv:q4_0:1000:4096:1", "gemv:q8_0:600:2048:1", "moe:q4_0:33:1024:7"],
+}
+
+
+@pytest.mark.parametrize("tune", list(OVERRIDES))
+def test_launch_overrides(orc, tmp_path, tune):
+    import os
+    import subprocess
+    import sys
+    out = tmp_path / "y.npz"
+    env = dict(os.environ, QMV_GEMV_TUNE=tune)
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-m", "tests._launch_override_child", str(out)] + OVERRIDES[tune],
+                       env=env, cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    res = np.load(out)
+    assert int(res["status"][0]) == 0
+    for case in OVERRIDES[tune]:
+        kind, fmt, n, k, m = case.split(":")
+        N, K, M = int(n), int(k), int(m)
+        y = res[case].astype(np.float64)
+        if kind == "gemv":
+            W = synth.weights(fmt, N, K, synth.seed_for(f"ovr_{fmt}_{N}x{K}"))
+            x = synth.activations(M, K, synth.seed_for(f"ovr_x_{K}_{M}"))
+            y_ref, S = orc.qmv(H.FMT[fmt], W, x, N, K, nthreads=8)
+        else:
+            E = 2 * M
+            pool = synth.q4_0_weights(E * N, K, synth.seed_for(f"ovr_pool_{N}x{K}"))
+            x = synth.activations(M, K, synth.seed_for(f"ovr_moe_x_{K}"))
+            y_ref, S = orc.moe(0, pool, res[case + ":idx"], E, x, N, K, nthreads=8)
+            assert np.array_equal(res[case], res[case + ":single"]), (tune, case, "not bit-identical")
+        err = H.normalised_error(y, y_ref, S)
+        assert err <= H.TOL, (tune, case, err)
 
 
 # -- sabotage: corrupted packed bytes must fail every check ----------------------------

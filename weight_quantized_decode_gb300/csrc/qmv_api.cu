@@ -363,7 +363,7 @@ qmv_status qmm_q4_0_prefill(const void *W, const void *x, float *y, int64_t N, i
     int sms = 0, optin = 0;
     if (device_info(dev, &status, &sms, &optin) != cudaSuccess) return QMV_ERR_CUDA;
     if (prefill_supported(N, K, M)) {
-        cudaError_t e = launch_prefill(W, x, y, N, K, M, sms, status, s);
+        cudaError_t e = launch_prefill(W, x, y, N, K, M, sms, status, s, g_pdl.load(std::memory_order_relaxed) != 0);
         if (e != cudaSuccess) {
             (void)cudaGetLastError();
             return QMV_ERR_LAUNCH;

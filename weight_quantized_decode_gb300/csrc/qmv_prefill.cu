@@ -263,12 +263,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // The next kernel of the stream may be scheduled now (its CTAs start on
+    // free SMs and stream their own weights); it reads what this kernel
+    // writes only after its own griddepcontrol.wait.
+    pdl_allow_next_grid();
 
     bool ok = true;
     if (warp == kWProducerWarp) {
         // ---------------- packed weights: TMA tensor copies, NW deep ----------------
         if (lane == 0) {
-            pdl_wait_prior_grid();
+            // W is never written by the kernel before this one (a documented
+            // condition of the call), so its copies do not wait for it.
             // Loop state is kept incremental (no division): this thread's
             // instruction latency is on the pipeline's critical path.
             int issued = 0, slot = 0;
@@ -494,7 +499,7 @@ bool prefill_supported(int64_t N, int64_t K, int64_t M)
 }
 
 cudaError_t launch_prefill(const void *W, const void *x, float *y, int64_t N, int64_t K, int64_t M, int /*sms*/,
-                           int *status, cudaStream_t s)
+                           int *status, cudaStream_t s, bool pdl)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
@@ -554,7 +559,7 @@ cudaError_t launch_prefill(const void *W, const void *x, float *y, int64_t N, in
     cudaError_t e = ensure_smem_optin(reinterpret_cast<const void *>(prefill_kernel), smem);
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>((N + kBM - 1) / kBM), static_cast<unsigned>((M + TN - 1) / TN));
-    return launch_ex(prefill_kernel, grid, dim3(kThreads), smem, s, false, wmap, xmap, p);
+    return launch_ex(prefill_kernel, grid, dim3(kThreads), smem, s, pdl, wmap, xmap, p);
 }
 
 }  // namespace qmv

@@ -10,6 +10,6 @@ namespace qmv {
 bool prefill_supported(int64_t N, int64_t K, int64_t M);
 
 cudaError_t launch_prefill(const void *W, const void *x, float *y, int64_t N, int64_t K, int64_t M, int sms,
-                           int *status, cudaStream_t s);
+                           int *status, cudaStream_t s, bool pdl);
 
 }  // namespace qmv
