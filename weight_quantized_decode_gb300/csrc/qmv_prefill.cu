@@ -25,8 +25,10 @@
 //     w = (c - 8) * d, and write 64-K slices of the A operand in the same
 //     swizzled layout.
 //   * Warp 1 allocates tensor memory and one thread issues tcgen05.mma
-//     (kind::f16, 128 x TN x 16) four times per 64-K slice; tcgen05.commit
-//     releases the slice's A and B buffers and finally signals the epilogue.
+//     (kind::f16, 128 x TN x 16) four times per 64-K atom; a ring slot holds
+//     one atom (TN = 256) or two (TN <= 128: eight MMAs per barrier round);
+//     tcgen05.commit releases the slot's A and B buffers and finally signals
+//     the epilogue.
 //   * All warps read the accumulator with tcgen05.ld (32 lanes x 32 columns
 //     per instruction; warp w reads lane quarter w mod 4, the warps of a
 //     quarter split the columns) and store y with coalesced fp32 stores.
@@ -63,7 +65,8 @@ struct PrefillParams {
     int64_t N, K, M;
     int TN;            // token columns per tile (multiple of 32, <= 256)
     int NW;            // packed-weight ring slots (256-K tiles)
-    int NS;            // slice ring slots: one dequantised-weight and one activation tile each
+    int NS;            // slot ring depth: each slot holds KSUB dequantised-weight and activation atoms
+    int KSUB;          // 64-K atoms per slot (1 or 2): MMAs per barrier round = 4 * KSUB
     uint32_t tmem_cols;
 };
 
@@ -221,11 +224,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 1024-byte alignment of the operand tiles (required by the 128-byte swizzle).
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-    const int NW = p.NW, NS = p.NS, TN = p.TN;
-    const int b_tile_bytes = TN * kKB * 2;
+    const int NW = p.NW, NS = p.NS, TN = p.TN, KSUB = p.KSUB;
+    const int b_atom_bytes = TN * kKB * 2;                  // one 64-K activation atom
+    const int a_slot_bytes = KSUB * kATileBytes;
+    const int b_slot_bytes = KSUB * b_atom_bytes;
     uint8_t *a_tiles = smem;
-    uint8_t *b_tiles = a_tiles + NS * kATileBytes;
-    uint8_t *w_tiles = b_tiles + NS * b_tile_bytes;
+    uint8_t *b_tiles = a_tiles + NS * a_slot_bytes;
+    uint8_t *w_tiles = b_tiles + NS * b_slot_bytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(w_tiles + NW * kPackedTileBytes);
     uint64_t *wfull = bars;             // [NW]
     uint64_t *wempty = wfull + NW;      // [NW]
@@ -240,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kBM;
     const int64_t m0 = static_cast<int64_t>(blockIdx.y) * TN;
-    const int nK = static_cast<int>(p.K / kKB);            // 64-K slices
+    const int nK = static_cast<int>(p.K / (kKB * KSUB));   // slots of KSUB x 64 K
     const int nC = static_cast<int>(p.K / kKChunk);        // packed 256-K tiles
     constexpr int kDeqWarps = kDeqThreads / 32;
 
@@ -307,8 +312,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(&bfull[s], b_tile_bytes);
-                tma_load_2d(b_tiles + s * b_tile_bytes, &xmap, j * kKB, static_cast<int>(m0), &bfull[s]);
+                mbar_arrive_expect_tx(&bfull[s], b_slot_bytes);
+                for (int a = 0; a < KSUB; ++a)
+                    tma_load_2d(b_tiles + s * b_slot_bytes + a * b_atom_bytes, &xmap, (j * KSUB + a) * kKB,
+                                static_cast<int>(m0), &bfull[s]);
                 ++issued;
                 if (++s == NS) {
                     s = 0;
@@ -327,7 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // in the 16-byte address field) is a plain addition.
             const uint64_t a_desc0 = sw128_desc(smem_u32(a_tiles));
             const uint64_t b_desc0 = sw128_desc(smem_u32(b_tiles));
-            const uint64_t a_step = kATileBytes >> 4, b_step = static_cast<uint64_t>(b_tile_bytes) >> 4;
+            const uint64_t a_step = static_cast<uint64_t>(a_slot_bytes) >> 4;
+            const uint64_t b_step = static_cast<uint64_t>(b_slot_bytes) >> 4;
             int committed = 0, s = 0;
             uint32_t ph = 0;
             uint64_t a_desc = a_desc0, b_desc = b_desc0;
@@ -341,6 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // dequantised writes published with fence.proxy.async before the
                 // arrive): the barrier wait is enough, no tcgen05 fence per slice.
                 mma_f16_slice(tmem_base, a_desc, b_desc, idesc, j == 0);
+                if (KSUB == 2)
+                    mma_f16_slice(tmem_base, a_desc + (kATileBytes >> 4),
+                                  b_desc + (static_cast<uint64_t>(b_atom_bytes) >> 4), idesc, false);
                 mma_commit(&sempty[s]);
                 ++committed;
                 if (++s == NS) {
@@ -389,10 +400,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 #pragma unroll
             for (int sub = 0; sub < 4; ++sub) {
-                if (lane == 0) ok = wait_or_abort(&sempty[sa], apar, abort_flag, p.status);
-                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                if (!ok) break;
-                while (!mbar_try_wait_sleep(&sempty[sa], apar, kSuspendHintNs)) {
+                const int atom = sub & (KSUB - 1);      // atom within the slot
+                if (atom == 0) {
+                    if (lane == 0) ok = wait_or_abort(&sempty[sa], apar, abort_flag, p.status);
+                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                    if (!ok) break;
+                    while (!mbar_try_wait_sleep(&sempty[sa], apar, kSuspendHintNs)) {
+                    }
                 }
                 // block 2*sub + hsel: even blocks start 2 bytes into word 9*sub
                 const int h = 9 * sub;
@@ -407,19 +421,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dbits = w[h + 4] >> 16;
                 }
                 dequant_block_f16(dbits, q, f);
-                uint8_t *arow = a_tiles + sa * kATileBytes + (r >> 3) * 1024 + (r & 7) * 128;
+                uint8_t *arow = a_tiles + sa * a_slot_bytes + atom * kATileBytes + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
                     const int cc = 4 * hsel + ch;    // 16-byte chunk within the 128-byte row
                     *reinterpret_cast<uint4 *>(arow + ((cc ^ (r & 7)) << 4)) =
                         make_uint4(f[4 * ch], f[4 * ch + 1], f[4 * ch + 2], f[4 * ch + 3]);
                 }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&afull[sa]);
-                if (++sa == NS) {
-                    sa = 0;
-                    apar ^= 1u;
+                if (atom == KSUB - 1) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&afull[sa]);
+                    if (++sa == NS) {
+                        sa = 0;
+                        apar ^= 1u;
+                    }
                 }
             }
         }
@@ -533,25 +549,31 @@ cudaError_t launch_prefill(const void *W, const void *x, float *y, int64_t N, in
     p.K = K;
     p.M = M;
     p.TN = TN;
-    const int b_tile = TN * kKB * 2;
+    // Up to 128 token columns a slot holds two 64-K atoms: eight MMAs per
+    // barrier round and per commit (the issuing thread's fixed cost per round
+    // is then paid half as often); a 256-column slot would not fit twice.
+    const int KSUB = TN <= 128 ? 2 : 1;
+    const int b_tile = KSUB * TN * kKB * 2;
+    const int a_tile = KSUB * kATileBytes;
     // Ring depths: the packed-weight ring must cover DRAM latency, the
     // activation ring L2 latency, at the MMA rate of this tile width.
     int NW = 4, NS = 3;
     if (TN <= 64) {
         NW = 4;
-        NS = 6;
+        NS = 3;
     } else if (TN <= 128) {
-        NW = 3;
-        NS = 5;
+        NW = 4;
+        NS = 2;
     }
     // alignment slack + barriers (2*NW + 3*NS + 1 of 8 bytes) + TMEM slot + flag
     const size_t fixed = 1024 + 512;
     auto total = [&] { return fixed + static_cast<size_t>(NW) * kPackedTileBytes +
-                              static_cast<size_t>(NS) * (kATileBytes + b_tile); };
+                              static_cast<size_t>(NS) * (a_tile + b_tile); };
     while (total() > 225 * 1024 && NS > 2) --NS;
     while (total() > 225 * 1024 && NW > 2) --NW;
     p.NW = NW;
     p.NS = NS;
+    p.KSUB = KSUB;
     uint32_t cols = 32;
     while (cols < static_cast<uint32_t>(TN)) cols <<= 1;
     p.tmem_cols = cols;
