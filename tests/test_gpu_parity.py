@@ -315,8 +315,11 @@ def test_sabotage_fails(orc, fmt):
 
 # -- prefill ---------------------------------------------------------------------------
 
+# (9856, 256, 300) and (12000, 512, 512): on a 152-SM GPU 256-token tiles would
+# need two waves, so one CTA takes 512 tokens in two accumulators (ragged
+# second half, ragged last row tile).
 @pytest.mark.parametrize("N,K,M", [(256, 512, 64), (384, 1024, 100), (128, 256, 1), (1024, 2560, 512),
-                                   (200, 512, 70), (128, 2048, 257)])
+                                   (200, 512, 70), (128, 2048, 257), (9856, 256, 300), (12000, 512, 512)])
 def test_prefill(cuda_lib, orc, N, K, M):
     q = cuda_lib
     W = synth.q4_0_weights(N, K, N + K + M)
@@ -327,7 +330,7 @@ def test_prefill(cuda_lib, orc, N, K, M):
     assert H.normalised_error(y.cpu().numpy(), y_ref, S) <= H.TOL
 
 
-@pytest.mark.parametrize("N,K,M", [(12288, 2560, 64), (8192, 2048, 512)])
+@pytest.mark.parametrize("N,K,M", [(12288, 2560, 64), (12288, 2560, 512), (8192, 2048, 64), (8192, 2048, 512)])
 def test_prefill_full_size_sampled(cuda_lib, orc, N, K, M):
     q = cuda_lib
     W = synth.q4_0_weights(N, K, synth.seed_for(f"prefill_{N}x{K}"))

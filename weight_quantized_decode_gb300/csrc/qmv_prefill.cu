@@ -10,7 +10,8 @@
 //
 //   * One CTA computes a 128-row (weights) x TN-column (tokens) tile of y^T in
 //     tensor memory: weights are the MMA's M side (128 lanes), tokens its N
-//     side (TN <= 256 columns of fp32).
+//     side (TN <= 256 columns of fp32; when 256-token tiles would need a
+//     second wave of CTAs, TN = 512 in two 256-column accumulators).
 //   * Roles by warp: a warp runs on scheduler (warp id mod 4).  Scheduler 1
 //     hosts only the MMA-issuing warp and the two copy producers, which sleep
 //     in mbarrier waits, so the single MMA-issuing thread is not starved of
@@ -63,7 +64,8 @@ struct PrefillParams {
     float *y;
     int *status;
     int64_t N, K, M;
-    int TN;            // token columns per tile (multiple of 32, <= 256)
+    int TN;            // token columns per tile (multiple of 64, <= 512)
+    int NH;            // accumulators per tile: TN / NH <= 256 columns each (the MMA's N)
     int NW;            // packed-weight ring slots (256-K tiles)
     int NS;            // slot ring depth: each slot holds KSUB dequantised-weight and activation atoms
     int KSUB;          // 64-K atoms per slot (1 or 2): MMAs per barrier round = 4 * KSUB
@@ -224,8 +226,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 1024-byte alignment of the operand tiles (required by the 128-byte swizzle).
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-    const int NW = p.NW, NS = p.NS, TN = p.TN, KSUB = p.KSUB;
-    const int b_atom_bytes = TN * kKB * 2;                  // one 64-K activation atom
+    const int NW = p.NW, NS = p.NS, TN = p.TN, KSUB = p.KSUB, NH = p.NH;
+    const int TNH = TN / NH;                                // MMA N: token columns per accumulator
+    const int b_atom_bytes = TN * kKB * 2;                  // one 64-K activation atom (all NH halves)
+    const int b_half_bytes = TNH * kKB * 2;
     const int a_slot_bytes = KSUB * kATileBytes;
     const int b_slot_bytes = KSUB * b_atom_bytes;
     uint8_t *a_tiles = smem;
@@ -314,8 +318,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mbar_arrive_expect_tx(&bfull[s], b_slot_bytes);
                 for (int a = 0; a < KSUB; ++a)
-                    tma_load_2d(b_tiles + s * b_slot_bytes + a * b_atom_bytes, &xmap, (j * KSUB + a) * kKB,
-                                static_cast<int>(m0), &bfull[s]);
+                    for (int h = 0; h < NH; ++h)
+                        tma_load_2d(b_tiles + s * b_slot_bytes + a * b_atom_bytes + h * b_half_bytes, &xmap,
+                                    (j * KSUB + a) * kKB, static_cast<int>(m0) + h * TNH, &bfull[s]);
                 ++issued;
                 if (++s == NS) {
                     s = 0;
@@ -329,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issue: one thread ----------------
         if (lane == 0) {
-            const uint32_t idesc = f16_idesc(TN);
+            const uint32_t idesc = f16_idesc(TNH);
             // Descriptors of slot 0; a slot (or a 16-wide K step: 32 bytes = 2
             // in the 16-byte address field) is a plain addition.
             const uint64_t a_desc0 = sw128_desc(smem_u32(a_tiles));
@@ -348,10 +353,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // The operands arrive through the async proxy (TMA writes, and
                 // dequantised writes published with fence.proxy.async before the
                 // arrive): the barrier wait is enough, no tcgen05 fence per slice.
-                mma_f16_slice(tmem_base, a_desc, b_desc, idesc, j == 0);
-                if (KSUB == 2)
-                    mma_f16_slice(tmem_base, a_desc + (kATileBytes >> 4),
-                                  b_desc + (static_cast<uint64_t>(b_atom_bytes) >> 4), idesc, false);
+                if (NH == 1) {
+                    mma_f16_slice(tmem_base, a_desc, b_desc, idesc, j == 0);
+                    if (KSUB == 2)
+                        mma_f16_slice(tmem_base, a_desc + (kATileBytes >> 4),
+                                      b_desc + (static_cast<uint64_t>(b_atom_bytes) >> 4), idesc, false);
+                } else {
+                    // Accumulator h (TMEM columns h * TNH ..) takes token half h;
+                    // 512-token tiles hold one atom per slot.
+                    for (int h = 0; h < NH; ++h)
+                        mma_f16_slice(tmem_base + h * TNH, a_desc,
+                                      b_desc + (static_cast<uint64_t>(h * b_half_bytes) >> 4), idesc, j == 0);
+                }
                 mma_commit(&sempty[s]);
                 ++committed;
                 if (++s == NS) {
@@ -514,7 +527,7 @@ bool prefill_supported(int64_t N, int64_t K, int64_t M)
            K < (int64_t(1) << 30) && encode_fn() != nullptr;
 }
 
-cudaError_t launch_prefill(const void *W, const void *x, float *y, int64_t N, int64_t K, int64_t M, int /*sms*/,
+cudaError_t launch_prefill(const void *W, const void *x, float *y, int64_t N, int64_t K, int64_t M, int sms,
                            int *status, cudaStream_t s, bool pdl)
 {
     EncodeTiledFn enc = encode_fn();
@@ -531,11 +544,20 @@ cudaError_t launch_prefill(const void *W, const void *x, float *y, int64_t N, in
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    const int TN = pick_tn(M);
+    int TN = pick_tn(M);
+    int NH = 1;
+    // When 256-token tiles would need a second wave of CTAs, one CTA takes
+    // 512 tokens in two accumulators (512 TMEM columns): one wave, and each
+    // weight tile is dequantised once for all of them.
+    const int64_t row_tiles = (N + kBM - 1) / kBM;
+    if (TN == 256 && row_tiles * ((M + 255) / 256) > sms && row_tiles * ((M + 511) / 512) <= sms) {
+        TN = 512;
+        NH = 2;
+    }
     {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K * 2)};
-        const cuuint32_t box[2] = {kKB, static_cast<cuuint32_t>(TN)};
+        const cuuint32_t box[2] = {kKB, static_cast<cuuint32_t>(TN / NH)};
         const cuuint32_t estr[2] = {1, 1};
         if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(x), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -549,6 +571,7 @@ cudaError_t launch_prefill(const void *W, const void *x, float *y, int64_t N, in
     p.K = K;
     p.M = M;
     p.TN = TN;
+    p.NH = NH;
     // Up to 128 token columns a slot holds two 64-K atoms: eight MMAs per
     // barrier round and per commit (the issuing thread's fixed cost per round
     // is then paid half as often); a 256-column slot would not fit twice.
@@ -558,7 +581,10 @@ cudaError_t launch_prefill(const void *W, const void *x, float *y, int64_t N, in
     // Ring depths: the packed-weight ring must cover DRAM latency, the
     // activation ring L2 latency, at the MMA rate of this tile width.
     int NW = 4, NS = 3;
-    if (TN <= 64) {
+    if (TN > 256) {
+        NW = 3;
+        NS = 2;
+    } else if (TN <= 64) {
         NW = 4;
         NS = 3;
     } else if (TN <= 128) {
