@@ -298,6 +298,28 @@ def test_launch_overrides(orc, tmp_path, tune):
         assert err <= H.TOL, (tune, case, err)
 
 
+def test_prefill_in_graph_on_a_new_stream(cuda_lib, orc):
+    """A prefill call captured into a CUDA graph on a fresh stream (tensor maps
+    are built on the host at capture time) replays correctly, twice."""
+    q = cuda_lib
+    N, K, M = 512, 2048, 64
+    W = synth.q4_0_weights(N, K, 61)
+    x = synth.activations(M, K, 62)
+    Wd, xd = dev(W), dev(x)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            q.qmm_q4_0_prefill(Wd, xd, y, stream=s)
+    for _ in range(2):
+        y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        y_ref, S = orc.qmv(0, W, x, N, K, nthreads=8)
+        assert H.normalised_error(y.cpu().numpy(), y_ref, S) <= H.TOL
+
+
 # -- sabotage: corrupted packed bytes must fail every check ----------------------------
 
 @pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
