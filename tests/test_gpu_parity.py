@@ -257,13 +257,18 @@ def test_moe_bad_index_sets_status_and_nans(cuda_lib):
 
 OVERRIDES = {
     # Launch shapes the measured table and the rule do not pick: lanes per row
-    # from 1 to 32, odd passes per stage, deep rings, two CTAs per SM; the
-    # multi-expert form must still equal the single calls bit for bit.
+    # from 1 to 32 (also ones that do not divide 32), odd passes per stage, deep
+    # rings, two CTAs per SM; the multi-expert form must still equal the single
+    # calls bit for bit.
     "G=4,SP=3": ["gemv:q4_0:77:6144:1", "gemv:q8_0:130:2560:2", "moe:q4_0:64:2560:5"],
     "G=32,warps=4": ["gemv:q4_0:40:8192:1", "gemv:q8_0:130:2560:4", "moe:q4_0:96:4096:6"],
     "G=1,SP=5,stages=3": ["gemv:q4_0:16:14336:1", "gemv:q4_0:33:2048:3", "moe:q4_0:20:2048:3"],
     "warps=16,stages=4,G=2": ["gemv:q4_0:100:4096:2", "gemv:q8_0:9:3072:1"],
     "ctas=2,share=2": ["gemv:q4_0:1000:4096:1", "gemv:q8_0:600:2048:1", "moe:q4_0:33:1024:7"],
+    # lanes per row that do not divide 32 (idle lanes, lane-order reduction)
+    "G=10": ["gemv:q4_0:130:2560:1", "gemv:q8_0:77:2560:2", "moe:q4_0:64:2560:5"],
+    "G=3,SP=3": ["gemv:q4_0:41:2304:1", "gemv:q8_0:50:1536:4", "moe:q4_0:20:2304:3"],
+    "G=12,warps=16": ["gemv:q4_0:90:3072:2", "gemv:q8_0:33:6144:1"],
 }
 
 

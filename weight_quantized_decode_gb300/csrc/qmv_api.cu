@@ -174,7 +174,7 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
         SP = te->SP;
         share = te->share;
     }
-    if (tu.G == 1 || tu.G == 2 || tu.G == 4 || tu.G == 8 || tu.G == 16 || tu.G == 32) G = tu.G;
+    if (tu.G >= 1 && tu.G <= 32) G = tu.G;
     if (tu.warps >= 1) warps = tu.warps;
     if (tu.stages >= 1) stages = tu.stages;
     if (tu.SP >= 1) SP = tu.SP;

@@ -14,11 +14,14 @@
 //     0x6400|n trick, and accumulates half2 products per block, scaled to fp32
 //     per block ("v2 = fp16 bit trick", "v2w = a whole 32-value group per lane
 //     step" -- volta-kernel-bakeoff, "What's in the race").
-//   * G lanes per row, RG rows per warp ("multiple output rows per warp for
-//     memory-level parallelism + a per-shape launch config" -- sm8x-bench,
+//   * G lanes per row, RG = 32/G rows per warp ("multiple output rows per warp
+//     for memory-level parallelism + a per-shape launch config" -- sm8x-bench,
 //     summary); the G partial sums of a row are combined with warp shuffles
 //     ("one warp (32 threads) per output row, __shfl_down_sync" --
-//     SovereignKernel diary, Phase 3).
+//     SovereignKernel diary, Phase 3): xor butterflies when G is a power of
+//     two; a G that does not divide 32 (a tuning choice, e.g. G = 10 for rows
+//     of 10 units) leaves lanes RG*G.. idle and sums the G partials in lane
+//     order.
 //   * Activations live in shared memory for the whole call, permuted once per
 //     CTA into the pair order the unpack produces and padded so that the G
 //     distinct units a warp reads at once fall in distinct banks.  For M > 1
@@ -71,7 +74,7 @@ struct GemvParams {
     int n_problems;              // 1 for a plain GEMV, slots for the multi-expert call
     int max_local_problems;      // most problems one CTA's row range can touch
     int U;                       // units per row = K / 256
-    int G;                       // lanes per row (power of two, 1..32)
+    int G;                       // lanes per row (1..32; RG = 32 / G rows per warp)
     int SP;                      // passes per stage (odd)
     int S;                       // stages in each warp's ring
     int *status;                 // device status word
@@ -456,6 +459,8 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
 
     const int r = lane / G;
     const int q = lane - r * G;
+    const bool lane_on = r < RG;             // G that does not divide 32 leaves lanes RG*G.. idle
+    const bool g_pow2 = (G & (G - 1)) == 0;
     const int xstride = U * kXUnitBytes;     // bytes between tokens of a problem
     float acc[M];
 #pragma unroll
@@ -476,7 +481,7 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
     for (int i = 0; i < total; ++i) {
         if (t == 0) {
             lr = g * RG + r;
-            row_ok = lr < nrows;
+            row_ok = lane_on && lr < nrows;
             if (MOE) {
                 prob = row_ok ? (row0 + lr) / N : static_cast<uint32_t>(prob_lo);
                 if (row_ok) {
@@ -515,12 +520,24 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
             t = 0;
             g += warps;
             // Combine the G partial sums of each row.
+            if (g_pow2) {
 #pragma unroll
-            for (int m = 0; m < M; ++m) {
-                for (int off = G >> 1; off > 0; off >>= 1)
-                    acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], off);
+                for (int m = 0; m < M; ++m) {
+                    for (int off = G >> 1; off > 0; off >>= 1)
+                        acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], off);
+                }
+            } else {
+                // G lanes per row, G not a power of two: the row's first lane
+                // adds the G partial sums in lane order.
+                const int src0 = (lane_on ? r : 0) * G;
+#pragma unroll
+                for (int m = 0; m < M; ++m) {
+                    float sum = 0.0f;
+                    for (int j = 0; j < G; ++j) sum += __shfl_sync(0xffffffffu, acc[m], src0 + j);
+                    acc[m] = sum;
+                }
             }
-            if (q == 0 && lr < nrows) {
+            if (q == 0 && lane_on && lr < nrows) {
                 const uint32_t row = row0 + lr;
                 if (MOE) {
                     const uint32_t n = row - prob * N;
