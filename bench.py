@@ -174,6 +174,22 @@ def dist_setup(args):
     return None, rank, local, world
 
 
+def cross_rank_max_ms(dist, ms, device):
+    """The slowest rank's duration of a timed region (every rank calls this)."""
+    if not dist:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_step, steps, world, ms):
+    """Units per second of the whole job: every rank processes units_per_step
+    per step (weak scaling), over the slowest rank's time."""
+    return units_per_step * steps * world / (ms * 1e-3)
+
+
 def run_ours(args, dist, rank, local, world):
     import torch
     import weight_quantized_decode_gb300 as q
@@ -364,6 +380,8 @@ def run_ours(args, dist, rank, local, world):
             for s in range(args.warmup):
                 e2e_step(s)
             torch.cuda.synchronize()
+            if dist:
+                dist.barrier()
             t0 = time.perf_counter()
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
@@ -373,22 +391,19 @@ def run_ours(args, dist, rank, local, world):
             b.record(stream)
             stream.synchronize()
             wall = time.perf_counter() - t0
-        e2e_ms = max(a.elapsed_time(b), wall * 1e3)
+        e2e_ms = cross_rank_max_ms(dist, max(a.elapsed_time(b), wall * 1e3), dev)
         h2d = sum(c["x_host"].numel() * 2 for c in calls)
         d2h = sum(c["y_host"].numel() * 4 for c in calls)
-        e2e_val = (step_flops / 1e12 if kind == "prefill" else step_bytes / 1e9) * args.steps / (e2e_ms * 1e-3)
-        e2e = {"value": round(e2e_val * world, 3), "unit": "TFLOP/s" if kind == "prefill" else "GB/s",
+        e2e_val = whole_job_rate(step_flops / 1e12 if kind == "prefill" else step_bytes / 1e9, args.steps, world, e2e_ms)
+        e2e = {"value": round(e2e_val, 3), "unit": "TFLOP/s" if kind == "prefill" else "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "note": "weights resident in HBM (model state); per step each call's x is copied from pinned "
                        "host memory and its y read back; host-launched calls through the C ABI"}
 
     # ---- cross-rank timing -----------------------------------------------------
-    if dist:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    gbs_total = step_bytes * args.steps * world / (ms * 1e-3) / 1e9
-    tflops_total = step_flops * args.steps * world / (ms * 1e-3) / 1e12
+    ms = cross_rank_max_ms(dist, ms, dev)
+    gbs_total = whole_job_rate(step_bytes, args.steps, world, ms) / 1e9
+    tflops_total = whole_job_rate(step_flops, args.steps, world, ms) / 1e12
 
     out = None
     if rank == 0:
