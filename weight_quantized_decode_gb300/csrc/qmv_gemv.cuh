@@ -392,64 +392,73 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
 
     // Stage the activations: permuted pair order, 528-byte padded units.  Each
     // thread builds whole 16-byte chunks of the permuted layout from four
-    // 4-byte loads (pairs of consecutive activations) and four PRMTs.
+    // 4-byte loads (pairs of consecutive activations) and four PRMTs.  The
+    // (token, chunk) items of all the CTA's tokens are dealt out together, up
+    // to kStageItems per thread per round with all their loads in flight, so
+    // several tokens cost few L2 round trips (one token of a plain call keeps
+    // two items per round: fewer registers live ahead of the main loop).
     {
+        constexpr bool kOneToken = (M == 1 && !MOE);
+        constexpr int kStageItems = kOneToken ? 2 : 4;
         const int ntok = (prob_hi - prob_lo + 1) * M;
         const int chunks = static_cast<int>(p.K / 8);          // 16-byte chunks per token (4 per block)
-        const int per_thread = (chunks + blockDim.x - 1) / blockDim.x;
+        const int items = ntok * chunks;
         bool first = true;
-        for (int tok = 0; tok < ntok || first; ++tok) {
-            const bool tok_ok = tok < ntok;
-            const uint32_t *xt = reinterpret_cast<const uint32_t *>(p.x + (static_cast<int64_t>(prob_lo) * M + tok) * p.K);
-            uint8_t *xd = xs + static_cast<size_t>(tok) * U * kXUnitBytes;
-            for (int j0 = 0; j0 < per_thread || first; j0 += 2) {
-                uint32_t a[2][4];
-                int cidx[2];
+        for (int it0 = 0; it0 < items || first; it0 += kStageItems * blockDim.x) {
+            uint32_t a[kStageItems][4];
+            int cidx[kStageItems], tidx[kStageItems];
 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    const int c = threadIdx.x + (j0 + b) * blockDim.x;
-                    cidx[b] = (tok_ok && j0 + b < per_thread && c < chunks) ? c : -1;
-                    if (cidx[b] >= 0) {
-                        const int blk = c >> 2, sub = c & 3;
-                        int i0, i2, i4, i6;    // first element of each loaded pair (in half units)
-                        if (FMT == kQ4_0) {
-                            // word `sub` of the block: bytes b0,b1 from (i0, i0+1), b2,b3 from (i2, i2+1);
-                            // low nibbles are elements i, high nibbles i + 16.
-                            if (blk & 1) { i0 = 4 * sub; i2 = 4 * sub + 2; }
-                            else if (sub == 0) { i0 = 0; i2 = 14; }
-                            else { i0 = 4 * sub - 2; i2 = 4 * sub; }
-                            i4 = i0 + 16;
-                            i6 = i2 + 16;
-                        } else {
-                            // words 2*sub and 2*sub+1 of the block (Q8_0: four codes per word)
-                            const int w0 = 2 * sub, w1 = 2 * sub + 1;
-                            if (blk & 1) { i0 = 4 * w0; i2 = 4 * w0 + 2; }
-                            else if (w0 == 0) { i0 = 0; i2 = 30; }
-                            else { i0 = 4 * w0 - 2; i2 = 4 * w0; }
-                            if (blk & 1) { i4 = 4 * w1; i6 = 4 * w1 + 2; }
-                            else { i4 = 4 * w1 - 2; i6 = 4 * w1; }
-                        }
-                        const uint32_t *xb = xt + blk * 16;     // 32 halves = 16 words per block
-                        a[b][0] = __ldg(xb + (i0 >> 1));
-                        a[b][1] = __ldg(xb + (i2 >> 1));
-                        a[b][2] = __ldg(xb + (i4 >> 1));
-                        a[b][3] = __ldg(xb + (i6 >> 1));
+            for (int b = 0; b < kStageItems; ++b) {
+                const int it = it0 + b * blockDim.x + threadIdx.x;
+                cidx[b] = -1;
+                tidx[b] = 0;
+                if (it < items) {
+                    const int tok = kOneToken ? 0 : it / chunks;
+                    const int c = it - tok * chunks;
+                    cidx[b] = c;
+                    tidx[b] = tok;
+                    const int blk = c >> 2, sub = c & 3;
+                    int i0, i2, i4, i6;    // first element of each loaded pair (in half units)
+                    if (FMT == kQ4_0) {
+                        // word `sub` of the block: bytes b0,b1 from (i0, i0+1), b2,b3 from (i2, i2+1);
+                        // low nibbles are elements i, high nibbles i + 16.
+                        if (blk & 1) { i0 = 4 * sub; i2 = 4 * sub + 2; }
+                        else if (sub == 0) { i0 = 0; i2 = 14; }
+                        else { i0 = 4 * sub - 2; i2 = 4 * sub; }
+                        i4 = i0 + 16;
+                        i6 = i2 + 16;
+                    } else {
+                        // words 2*sub and 2*sub+1 of the block (Q8_0: four codes per word)
+                        const int w0 = 2 * sub, w1 = 2 * sub + 1;
+                        if (blk & 1) { i0 = 4 * w0; i2 = 4 * w0 + 2; }
+                        else if (w0 == 0) { i0 = 0; i2 = 30; }
+                        else { i0 = 4 * w0 - 2; i2 = 4 * w0; }
+                        if (blk & 1) { i4 = 4 * w1; i6 = 4 * w1 + 2; }
+                        else { i4 = 4 * w1 - 2; i6 = 4 * w1; }
                     }
+                    const uint32_t *xb =
+                        reinterpret_cast<const uint32_t *>(p.x + (static_cast<int64_t>(prob_lo) * M + tok) * p.K) +
+                        blk * 16;     // 32 halves = 16 words per block
+                    a[b][0] = __ldg(xb + (i0 >> 1));
+                    a[b][1] = __ldg(xb + (i2 >> 1));
+                    a[b][2] = __ldg(xb + (i4 >> 1));
+                    a[b][3] = __ldg(xb + (i6 >> 1));
                 }
-                if (first) {
-                    first = false;
-                    for (int i = early; i < prefetch; ++i) issue_next();
-                }
+            }
+            if (first) {
+                first = false;
+                for (int i = early; i < prefetch; ++i) issue_next();
+            }
 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    if (cidx[b] >= 0) {
-                        const int c = cidx[b];
-                        const int blk = c >> 2, sub = c & 3;
-                        // pairs (first of each, first of each) and (second, second)
-                        const uint4 v = make_uint4(__byte_perm(a[b][0], a[b][1], 0x5410), __byte_perm(a[b][0], a[b][1], 0x7632),
-                                                   __byte_perm(a[b][2], a[b][3], 0x5410), __byte_perm(a[b][2], a[b][3], 0x7632));
-                        *reinterpret_cast<uint4 *>(xd + (blk >> 3) * kXUnitBytes + (blk & 7) * 64 + sub * 16) = v;
-                    }
+            for (int b = 0; b < kStageItems; ++b) {
+                if (cidx[b] >= 0) {
+                    const int c = cidx[b];
+                    const int blk = c >> 2, sub = c & 3;
+                    uint8_t *xd = xs + static_cast<size_t>(tidx[b]) * U * kXUnitBytes;
+                    // pairs (first of each, first of each) and (second, second)
+                    const uint4 v = make_uint4(__byte_perm(a[b][0], a[b][1], 0x5410), __byte_perm(a[b][0], a[b][1], 0x7632),
+                                               __byte_perm(a[b][2], a[b][3], 0x5410), __byte_perm(a[b][2], a[b][3], 0x7632));
+                    *reinterpret_cast<uint4 *>(xd + (blk >> 3) * kXUnitBytes + (blk & 7) * 64 + sub * 16) = v;
                 }
             }
         }
