@@ -403,8 +403,19 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
         const int ntok = (prob_hi - prob_lo + 1) * M;
         const int chunks = static_cast<int>(p.K / 8);          // 16-byte chunks per token (4 per block)
         const int items = ntok * chunks;
+        // Item slot b of this thread is item it0 + b * blockDim + threadIdx
+        // = (token tk[b], chunk ck[b]); both advance by a fixed step per round.
+        const int round = kStageItems * blockDim.x;
+        const int dq = kOneToken ? 0 : round / chunks, dr = kOneToken ? round : round - dq * chunks;
+        int tk[kStageItems], ck[kStageItems];
+#pragma unroll
+        for (int b = 0; b < kStageItems; ++b) {
+            const int it = b * blockDim.x + threadIdx.x;
+            tk[b] = kOneToken ? 0 : it / chunks;
+            ck[b] = it - tk[b] * chunks;
+        }
         bool first = true;
-        for (int it0 = 0; it0 < items || first; it0 += kStageItems * blockDim.x) {
+        for (int it0 = 0; it0 < items || first; it0 += round) {
             uint32_t a[kStageItems][4];
             int cidx[kStageItems], tidx[kStageItems];
 #pragma unroll
@@ -413,8 +424,8 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
                 cidx[b] = -1;
                 tidx[b] = 0;
                 if (it < items) {
-                    const int tok = kOneToken ? 0 : it / chunks;
-                    const int c = it - tok * chunks;
+                    const int tok = tk[b];
+                    const int c = ck[b];
                     cidx[b] = c;
                     tidx[b] = tok;
                     const int blk = c >> 2, sub = c & 3;
@@ -443,6 +454,15 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
                     a[b][1] = __ldg(xb + (i2 >> 1));
                     a[b][2] = __ldg(xb + (i4 >> 1));
                     a[b][3] = __ldg(xb + (i6 >> 1));
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < kStageItems; ++b) {
+                ck[b] += dr;
+                tk[b] += dq;
+                if (!kOneToken && ck[b] >= chunks) {
+                    ck[b] -= chunks;
+                    ++tk[b];
                 }
             }
             if (first) {
