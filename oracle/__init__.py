@@ -16,4 +16,5 @@ from .oracle import (  # noqa: F401
     moe,
     qmv,
     qmv_rows,
+    swiglu,
 )

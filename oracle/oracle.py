@@ -58,6 +58,9 @@ class Oracle:
         lib.oracle_moe.restype = ctypes.c_int
         lib.oracle_moe.argtypes = [ctypes.c_int, _ptr, _ptr, _i64, _ptr, _i64, _i64, _i64,
                                    _ptr, _ptr, ctypes.c_int]
+        lib.oracle_swiglu_rows.restype = ctypes.c_int
+        lib.oracle_swiglu_rows.argtypes = [ctypes.c_int, _ptr, _ptr, _ptr, _i64, _i64, _i64, _ptr, _i64,
+                                           _ptr, _ptr, _ptr, _ptr, _ptr, ctypes.c_int]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         self.lib = lib
@@ -139,6 +142,28 @@ class Oracle:
             raise ValueError(f"oracle_moe failed ({rc})")
         return y, S
 
+    def swiglu(self, fmt: int, Wg, Wu, x, N: int, K: int, rows=None, nthreads: int = 1):
+        """Gate + up + SwiGLU: dict of float64 [M][n] arrays y, g, u, Sg, Su
+        (n = N, or len(rows) for the listed rows)."""
+        Wgb, Wub = self._u8(Wg), self._u8(Wu)
+        xb = self._x_bits(x).reshape(-1, K)
+        M = xb.shape[0]
+        need = N * (K // 32) * self.block_bytes(fmt)
+        if Wgb.size < need or Wub.size < need:
+            raise ValueError("W buffer too small")
+        if rows is None:
+            rp, nr = None, N
+        else:
+            rows = np.ascontiguousarray(rows, dtype=np.int64)
+            rp, nr = rows.ctypes.data, rows.size
+        out = {k: np.empty((M, nr), dtype=np.float64) for k in ("y", "g", "u", "Sg", "Su")}
+        rc = self.lib.oracle_swiglu_rows(fmt, Wgb.ctypes.data, Wub.ctypes.data, xb.ctypes.data, N, K, M, rp, nr,
+                                         out["y"].ctypes.data, out["g"].ctypes.data, out["u"].ctypes.data,
+                                         out["Sg"].ctypes.data, out["Su"].ctypes.data, nthreads)
+        if rc != 0:
+            raise ValueError(f"oracle_swiglu_rows failed ({rc})")
+        return out
+
     def max_threads(self) -> int:
         return int(self.lib.oracle_max_threads())
 
@@ -168,6 +193,10 @@ def dequant_row(fmt, W, n, K):
 
 def qmv(fmt, W, x, N, K, nthreads=1):
     return default().qmv(fmt, W, x, N, K, nthreads)
+
+
+def swiglu(fmt, Wg, Wu, x, N, K, rows=None, nthreads=1):
+    return default().swiglu(fmt, Wg, Wu, x, N, K, rows, nthreads)
 
 
 def qmv_rows(fmt, W, x, N, K, rows, nthreads=1):

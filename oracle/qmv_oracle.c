@@ -183,6 +183,35 @@ int oracle_moe(int fmt, const uint8_t *W_pool, const int32_t *idx, int64_t n_exp
     return rc;
 }
 
+/* The MLP's gate + up + SwiGLU at decode, as one product over two tables that
+ * share the activations ("ours stacks gate and up into one table and converts
+ * once" -- volta-kernel-bakeoff, "A few tokens at once"; "fused W1 + W3 +
+ * SwiGLU into a single kernel -- X is read once" -- SovereignKernel diary,
+ * phase 6).  SwiGLU with its usual swish: the gate product goes through
+ * silu(g) = g / (1 + e^-g) and multiplies the up product:
+ *
+ *     g[m][n] = sum_k x[m][k] * wg[n][k]        u[m][n] = sum_k x[m][k] * wu[n][k]
+ *     y[m][n] = silu(g[m][n]) * u[m][n]
+ *
+ * For the listed rows (all rows when rows is NULL, then nrows = N); every
+ * output is [M][nrows] row-major and fp64: y, g, u and the S sums of the two
+ * products (the tolerance of a fused result is derived from them). */
+int oracle_swiglu_rows(int fmt, const uint8_t *Wg, const uint8_t *Wu, const uint16_t *x,
+                       int64_t N, int64_t K, int64_t M, const int64_t *rows, int64_t nrows,
+                       double *y, double *g, double *u, double *Sg, double *Su, int nthreads)
+{
+    int rc = oracle_qmv_rows(fmt, Wg, x, N, K, M, rows, nrows, g, Sg, nthreads);
+    if (rc != 0) return rc;
+    rc = oracle_qmv_rows(fmt, Wu, x, N, K, M, rows, nrows, u, Su, nthreads);
+    if (rc != 0) return rc;
+    if (rows == NULL) nrows = N;
+    for (int64_t i = 0; i < M * nrows; ++i) {
+        const double gate = g[i];
+        y[i] = gate / (1.0 + exp(-gate)) * u[i];
+    }
+    return 0;
+}
+
 int oracle_max_threads(void)
 {
 #ifdef _OPENMP

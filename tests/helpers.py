@@ -23,6 +23,27 @@ def normalised_error(y, y_ref, S):
     return float(err.max())
 
 
+SILU_SLOPE_MAX = 1.1   # sup |d silu / dz| = 1.0998 (at z = 2.40)
+
+
+def swiglu_normalised_error(y, ref):
+    """Fused gate + up + SwiGLU against the oracle (dict with y, g, u, Sg, Su).
+
+    Each of the two products carries the GEMV bound |dg| <= TOL * Sg,
+    |du| <= TOL * Su; through y = silu(g) * u (mean value theorem on silu):
+        |dy| <= TOL * (1.1 * Sg * (|u| + TOL * Su) + |silu(g)| * Su).
+    Returns max |y - y_ref| / (that bound / TOL + 1e-6), to compare with TOL."""
+    y = np.asarray(y, dtype=np.float64)
+    g, u = ref["g"], ref["u"]
+    if y.size == 0:
+        return 0.0
+    silu = g / (1.0 + np.exp(-g))
+    scale = SILU_SLOPE_MAX * ref["Sg"] * (np.abs(u) + TOL * ref["Su"]) + np.abs(silu) * ref["Su"]
+    err = np.abs(y - ref["y"]) / (scale + 1e-6)
+    err = np.where(np.isnan(err), np.inf, err)
+    return float(err.max())
+
+
 def _x_spec(spec, K):
     kind = spec[0]
     j = np.arange(K, dtype=np.float64)

@@ -5,6 +5,8 @@ forms (tests/golden), an exhaustive comparison of its fp16 decoder with numpy,
 integer special cases that reduce to a plain numpy matmul, exact invariants,
 and the sabotage check of volta-kernel-bakeoff ("Making it fair").
 """
+import math
+
 import numpy as np
 import pytest
 
@@ -219,3 +221,79 @@ def test_tolerance_helper():
     assert H.normalised_error([1.0], [1.0], [1.0]) == 0.0
     assert H.normalised_error([1.003], [1.0], [1.0]) > H.TOL
     assert H.normalised_error([np.nan], [1.0], [1.0]) == np.inf
+
+
+# -- gate + up + SwiGLU (closed forms) --------------------------------------------------
+
+def _uniform_table(code, d_bits, N=1, K=32):
+    return H.encode_q4_0(np.full((N, K), code, dtype=np.int64), np.full((N, K // 32), d_bits, dtype=np.uint16))
+
+
+def _silu(z):
+    return z / (1.0 + math.exp(-z))
+
+
+@pytest.mark.parametrize("gate_code,up_code,g,u", [
+    (9, 10, 1.0, 2.0),      # w = 1/32 and 2/32 against 32 ones
+    (7, 10, -1.0, 2.0),     # negative gate
+    (6, 9, -2.0, 1.0),
+    (12, 5, 4.0, -3.0),     # negative up
+])
+def test_swiglu_closed_form(orc, gate_code, up_code, g, u):
+    Wg = _uniform_table(gate_code, 0x2800)      # d = 2^-5
+    Wu = _uniform_table(up_code, 0x2800)
+    x = np.ones((1, 32), dtype=np.float16)
+    r = orc.swiglu(0, Wg, Wu, x, 1, 32)
+    assert r["g"][0, 0] == g and r["u"][0, 0] == u
+    assert r["Sg"][0, 0] == abs(g) and r["Su"][0, 0] == abs(u)
+    assert r["y"][0, 0] == pytest.approx(_silu(g) * u, rel=1e-15)
+
+
+def test_swiglu_zero_gate_or_up_gives_zero(orc):
+    x = np.ones((1, 32), dtype=np.float16)
+    assert orc.swiglu(0, _uniform_table(8, 0x3C00), _uniform_table(13, 0x3C00), x, 1, 32)["y"][0, 0] == 0.0
+    assert orc.swiglu(0, _uniform_table(13, 0x3C00), _uniform_table(8, 0x3C00), x, 1, 32)["y"][0, 0] == 0.0
+
+
+def test_swiglu_large_gate_is_linear(orc):
+    # g = 7 * 32 = 224 (d = 1): silu(g) = g to double precision; u = 32
+    x = np.ones((1, 32), dtype=np.float16)
+    r = orc.swiglu(0, _uniform_table(15, 0x3C00), _uniform_table(9, 0x3C00), x, 1, 32)
+    assert r["y"][0, 0] == 224.0 * 32.0
+
+
+def test_swiglu_rows_tokens_and_subset(orc):
+    # row 0: gate w = 1/32, up w = 2/32; row 1: gate w = -2/32, up w = 1/32;
+    # token 0: x = 1, token 1: x = 0.5
+    gc = np.array([[9] * 32, [6] * 32]); uc = np.array([[10] * 32, [9] * 32])
+    d = np.full((2, 1), 0x2800, dtype=np.uint16)
+    Wg, Wu = H.encode_q4_0(gc, d), H.encode_q4_0(uc, d)
+    x = np.stack([np.ones(32), np.full(32, 0.5)]).astype(np.float16)
+    r = orc.swiglu(0, Wg, Wu, x, 2, 32)
+    want = np.array([[_silu(1.0) * 2.0, _silu(-2.0) * 1.0], [_silu(0.5) * 1.0, _silu(-1.0) * 0.5]])
+    np.testing.assert_allclose(r["y"], want, rtol=1e-15, atol=0)
+    sub = orc.swiglu(0, Wg, Wu, x, 2, 32, rows=[1])
+    np.testing.assert_allclose(sub["y"][:, 0], want[:, 1], rtol=1e-15, atol=0)
+
+
+def test_silu_slope_bound():
+    # the constant of the fused tolerance: sup of silu'(z) = s(z) (1 + z (1 - s(z)))
+    z = np.linspace(-40, 40, 400001)
+    s = 1.0 / (1.0 + np.exp(-z))
+    slope = s * (1.0 + z * (1.0 - s))
+    assert np.abs(slope).max() < H.SILU_SLOPE_MAX
+    assert np.abs(slope).max() > 1.09
+
+
+def test_swiglu_tolerance_helper(orc):
+    x = np.ones((1, 32), dtype=np.float16)
+    ref = orc.swiglu(0, _uniform_table(9, 0x2800), _uniform_table(10, 0x2800), x, 1, 32)
+    assert H.swiglu_normalised_error(ref["y"], ref) == 0.0
+    # a gate product off by its whole allowance (TOL * Sg) stays inside
+    g2 = ref["g"] + H.TOL * ref["Sg"]
+    y2 = g2 / (1 + np.exp(-g2)) * ref["u"]
+    assert H.swiglu_normalised_error(y2, ref) <= H.TOL
+    # ten times that does not
+    g3 = ref["g"] + 10 * H.TOL * ref["Sg"]
+    y3 = g3 / (1 + np.exp(-g3)) * ref["u"]
+    assert H.swiglu_normalised_error(y3, ref) > H.TOL

@@ -54,6 +54,12 @@ MUTANTS = [
     ("moe_expert_stride", "int64_t expert_bytes = N * (K / 32) * bb;",
      "int64_t expert_bytes = (N - 1) * (K / 32) * bb;", 0),
     ("moe_output_offset", "y + s * N, S + s * N", "y, S", 0),
+    ("silu_sign", "gate / (1.0 + exp(-gate)) * u[i]", "gate / (1.0 + exp(gate)) * u[i]", 0),
+    ("silu_dropped", "y[i] = gate / (1.0 + exp(-gate)) * u[i];", "y[i] = gate * u[i];", 0),
+    ("sigmoid_without_gate", "y[i] = gate / (1.0 + exp(-gate)) * u[i];", "y[i] = 1.0 / (1.0 + exp(-gate)) * u[i];", 0),
+    ("gate_and_up_swapped", "const double gate = g[i];\n        y[i] = gate / (1.0 + exp(-gate)) * u[i];",
+     "const double gate = u[i];\n        y[i] = gate / (1.0 + exp(-gate)) * g[i];", 0),
+    ("up_table_is_gate", "rc = oracle_qmv_rows(fmt, Wu, x,", "rc = oracle_qmv_rows(fmt, Wg, x,", 0),
 ]
 
 
