@@ -40,6 +40,8 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "qmv_common.cuh"
@@ -350,9 +352,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                // The operands arrive through the async proxy (TMA writes, and
-                // dequantised writes published with fence.proxy.async before the
-                // arrive): the barrier wait is enough, no tcgen05 fence per slice.
+                // Order the MMAs after the barrier waits (the tcgen05 ops are
+                // asynchronous to this thread).
+                tc_fence_after();
                 if (NH == 1) {
                     mma_f16_slice(tmem_base, a_desc, b_desc, idesc, j == 0);
                     if (KSUB == 2)
@@ -405,6 +407,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 w[4 * i + 2] = v.z;
                 w[4 * i + 3] = v.w;
             }
+            // Hand the slot back only once this thread's reads of it are done:
+            // the words are consumed into a register, and fence.proxy.async
+            // orders the reads (generic proxy) before the producer's next
+            // copy into the slot (async proxy).  Without both, the next tile
+            // could land under a load still in flight.
+            {
+                uint32_t all = 0;
+#pragma unroll
+                for (int i = 0; i < 36; ++i) all ^= w[i];
+                asm volatile("" ::"r"(all) : "memory");
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) mbar_arrive(&wempty[slot]);
             if (++slot == NW) {
@@ -510,6 +524,24 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
+// Ring depths forced for tests and sweeps: QMV_PREFILL_RING="NW,NS" (packed-
+// weight slots, operand slots; values below 2 keep the rule).
+int ring_override(int which)
+{
+    static int nw = 0, ns = 0;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        const char *e = std::getenv("QMV_PREFILL_RING");
+        if (!e) return;
+        nw = std::atoi(e);
+        const char *c = std::strchr(e, ',');
+        if (c) ns = std::atoi(c + 1);
+    });
+    return which == 0 ? nw : ns;
+}
+int ring_override_nw() { return ring_override(0); }
+int ring_override_ns() { return ring_override(1); }
+
 int pick_tn(int64_t M)
 {
     // Multiples of 64 so that each of the two epilogue warps per lane quarter
@@ -595,6 +627,8 @@ cudaError_t launch_prefill(const void *W, const void *x, float *y, int64_t N, in
     const size_t fixed = 1024 + 512;
     auto total = [&] { return fixed + static_cast<size_t>(NW) * kPackedTileBytes +
                               static_cast<size_t>(NS) * (a_tile + b_tile); };
+    if (ring_override_nw() >= 2) NW = ring_override_nw();
+    if (ring_override_ns() >= 2) NS = ring_override_ns();
     while (total() > 225 * 1024 && NS > 2) --NS;
     while (total() > 225 * 1024 && NW > 2) --NW;
     p.NW = NW;
