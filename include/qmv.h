@@ -125,6 +125,28 @@ QMV_API qmv_status qmv_moe(const void *W_pool, const int32_t *expert_idx, int64_
                    qmv_stream_t stream);
 
 /*
+ * The MLP's gate + up + SwiGLU in one call (decode, 1..8 tokens): two Q4_0
+ * tables that share the activations, read together, with the activation
+ * function applied before anything is written --
+ *     y[m][n] = silu(g) * u,  g = sum_k x[m][k] wg[n][k],  u = sum_k x[m][k] wu[n][k],
+ *     silu(g) = g / (1 + e^-g)
+ * ("ours stacks gate and up into one table and converts once" --
+ * volta-kernel-bakeoff, "A few tokens at once"; "fused W1 + W3 + SwiGLU into a
+ * single kernel -- X is read once, ... only the final result written" --
+ * SovereignKernel diary, phase 6).  The two tables stay separate arrays; the
+ * kernel interleaves their rows as it streams them.
+ *   W_gate, W_up : Q4_0 bytes [N][K/32*18] each, 16-byte aligned (W_up may
+ *                  be NULL only when K == 0).
+ *   x : fp16 [M][K].  y : fp32 [M][N] (overwritten).  M <= 8.
+ * Accuracy: g and u each carry the product's bound above; through silu,
+ * |y - y_exact| <= 2e-3 * (1.1 * Sg * (|u| + 2e-3 * Su) + |silu(g)| * Su)
+ * with Sg, Su the two products' sums of |x w| (1.1 bounds |silu'|).
+ * Errors and asynchrony as for qmv_q4_0.
+ */
+QMV_API qmv_status qmv_q4_0_swiglu(const void *W_gate, const void *W_up, const void *x, float *y,
+                           int64_t N, int64_t K, int64_t M, qmv_stream_t stream);
+
+/*
  * Q4_0 prefill GEMM for many tokens (M >= 1, intended for M >= 64): "tensor
  * cores for prompts: unpack a tile to shared memory" (tc_q4 --
  * volta-kernel-bakeoff, "What's in the race"; "unpack quantized weights inside

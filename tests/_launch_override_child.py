@@ -20,7 +20,21 @@ def main():
     for case in sys.argv[2:]:
         kind, fmt, n, k, m = case.split(":")
         N, K, M = int(n), int(k), int(m)
-        if kind == "gemv":
+        if kind == "pfrep":   # the same prefill call repeated: outputs must be bit-identical
+            W = dev(synth.q4_0_weights(N, K, synth.seed_for(f"ovr_pf_{N}x{K}")))
+            x = dev(synth.activations(M, K, synth.seed_for(f"ovr_pf_x_{K}_{M}")))
+            ys = [q.qmm_q4_0_prefill(W, x) for _ in range(4)]
+            torch.cuda.synchronize()
+            res[case] = ys[0].cpu().numpy()
+            res[case + ":identical"] = np.array([all(torch.equal(ys[0], v) for v in ys[1:])])
+        elif kind == "swiglu":
+            Wg = synth.q4_0_weights(N, K, synth.seed_for(f"ovr_sg_{N}x{K}"))
+            Wu = synth.q4_0_weights(N, K, synth.seed_for(f"ovr_su_{N}x{K}"))
+            x = synth.activations(M, K, synth.seed_for(f"ovr_x_{K}_{M}"))
+            y = q.qmv_q4_0_swiglu(dev(Wg), dev(Wu), dev(x))
+            torch.cuda.synchronize()
+            res[case] = y.cpu().numpy()
+        elif kind == "gemv":
             W = synth.weights(fmt, N, K, synth.seed_for(f"ovr_{fmt}_{N}x{K}"))
             x = synth.activations(M, K, synth.seed_for(f"ovr_x_{K}_{M}"))
             fn = q.qmv_q4_0 if fmt == "q4_0" else q.qmv_q8_0

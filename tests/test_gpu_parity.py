@@ -204,6 +204,86 @@ def test_full_size_q8_0(orc, N, K, M):
     check("q8_0", W, x, N, K, orc, rows=_sample_rows(N))
 
 
+# -- fused gate + up + SwiGLU -----------------------------------------------------------
+
+def swiglu_check(Wg, Wu, x, N, K, orc, rows=None):
+    import weight_quantized_decode_gb300 as q
+    y = q.qmv_q4_0_swiglu(dev(Wg), dev(Wu), dev(x))
+    torch.cuda.synchronize()
+    yn = y.cpu().numpy().astype(np.float64)
+    ref = orc.swiglu(0, Wg, Wu, x, N, K, rows=rows, nthreads=8)
+    err = H.swiglu_normalised_error(yn if rows is None else yn[:, rows], ref)
+    assert err <= H.TOL, (N, K, x.shape[0], err)
+    return yn
+
+
+def _swiglu_tables(N, K, seed):
+    return synth.q4_0_weights(N, K, seed), synth.q4_0_weights(N, K, seed + 7919)
+
+
+@pytest.mark.parametrize("N,K", [(1, 256), (7, 512), (33, 768), (1000, 2048), (333, 4096), (64, 14336),
+                                 (130, 2560), (4133, 1024)])
+def test_swiglu_m1(orc, N, K):
+    Wg, Wu = _swiglu_tables(N, K, 300 + N + K)
+    swiglu_check(Wg, Wu, synth.activations(1, K, 301 + K), N, K, orc)
+
+
+@pytest.mark.parametrize("M", [2, 3, 5, 8])
+def test_swiglu_tokens(orc, M):
+    N, K = 515, 2560
+    Wg, Wu = _swiglu_tables(N, K, 310 + M)
+    swiglu_check(Wg, Wu, synth.activations(M, K, 311 + M), N, K, orc)
+
+
+@pytest.mark.parametrize("plant", ["large", "tiny"])
+@pytest.mark.parametrize("M", [1, 8])
+def test_swiglu_planted(orc, plant, M):
+    N, K = 300, 4096
+    Wg, Wu = _swiglu_tables(N, K, 320)
+    y = swiglu_check(Wg, Wu, synth.activations(M, K, 321, plant=plant), N, K, orc)
+    assert np.all(np.isfinite(y))
+
+
+@pytest.mark.parametrize("K", [96, 640])
+def test_swiglu_generic_kernel(orc, K):
+    N = 45
+    Wg, Wu = _swiglu_tables(N, K, 330 + K)
+    swiglu_check(Wg, Wu, synth.activations(3, K, 331), N, K, orc)
+
+
+@pytest.mark.parametrize("N,K", [(14336, 4096), (6144, 2048)])
+@pytest.mark.parametrize("M", [1, 8])
+def test_swiglu_full_size_sampled(orc, N, K, M):
+    Wg, Wu = _swiglu_tables(N, K, synth.seed_for(f"swiglu_{N}x{K}"))
+    x = synth.activations(M, K, synth.seed_for(f"swiglu_x_{K}_{M}"))
+    swiglu_check(Wg, Wu, x, N, K, orc, rows=_sample_rows(N))
+
+
+def test_swiglu_empty_and_sabotage(cuda_lib, orc):
+    q = cuda_lib
+    # K = 0: silu(0) * 0 = 0 everywhere
+    y = torch.full((2, 5), 7.0, device="cuda")
+    q.qmv_q4_0_swiglu_ptr(0, 0, torch.empty(0, dtype=torch.float16, device="cuda").data_ptr(), y.data_ptr(), 5, 0, 2, 0)
+    torch.cuda.synchronize()
+    assert torch.all(y == 0)
+    # N = 0 and M = 0: nothing to do
+    q.qmv_q4_0_swiglu_ptr(0, 0, 0, 0, 0, 256, 1, 0)
+    q.qmv_q4_0_swiglu_ptr(0, 0, 0, 0, 4, 256, 0, 0)
+    # corrupted tables: most outputs fail (outputs whose gate is near zero or
+    # far negative are small either way and may pass)
+    N, K = 256, 2048
+    Wg, Wu = _swiglu_tables(N, K, 340)
+    x = synth.activations(1, K, 341)
+    y = q.qmv_q4_0_swiglu(dev(H.sabotage(Wg, "q4_0")), dev(H.sabotage(Wu, "q4_0")), dev(x))
+    torch.cuda.synchronize()
+    ref = orc.swiglu(0, Wg, Wu, x, N, K, nthreads=8)
+    yn = y.cpu().numpy().astype(np.float64)
+    silu = ref["g"] / (1 + np.exp(-ref["g"]))
+    scale = H.SILU_SLOPE_MAX * ref["Sg"] * (np.abs(ref["u"]) + H.TOL * ref["Su"]) + np.abs(silu) * ref["Su"]
+    err = np.abs(yn - ref["y"]) / (scale + 1e-6)
+    assert (err > H.TOL).mean() > 0.75 and err.max() > 20 * H.TOL, ((err > H.TOL).mean(), err.max())
+
+
 # -- multi-expert decode --------------------------------------------------------------
 
 @pytest.mark.parametrize("E,slots,N,K", [(128, 10, 640, 2560), (128, 8, 512, 2048), (5, 5, 64, 512),
@@ -268,7 +348,9 @@ OVERRIDES = {
     # lanes per row that do not divide 32 (idle lanes, lane-order reduction)
     "G=10": ["gemv:q4_0:130:2560:1", "gemv:q8_0:77:2560:2", "moe:q4_0:64:2560:5"],
     "G=3,SP=3": ["gemv:q4_0:41:2304:1", "gemv:q8_0:50:1536:4", "moe:q4_0:20:2304:3"],
-    "G=12,warps=16": ["gemv:q4_0:90:3072:2", "gemv:q8_0:33:6144:1"],
+    "G=12,warps=16": ["gemv:q4_0:90:3072:2", "gemv:q8_0:33:6144:1", "swiglu:q4_0:90:3072:2"],
+    # the fused SwiGLU keeps an even number of rows per group (G clamped to <= 16)
+    "G=32": ["swiglu:q4_0:77:4096:1", "swiglu:q4_0:40:2048:8"],
 }
 
 
@@ -289,6 +371,14 @@ def test_launch_overrides(orc, tmp_path, tune):
         kind, fmt, n, k, m = case.split(":")
         N, K, M = int(n), int(k), int(m)
         y = res[case].astype(np.float64)
+        if kind == "swiglu":
+            Wg = synth.q4_0_weights(N, K, synth.seed_for(f"ovr_sg_{N}x{K}"))
+            Wu = synth.q4_0_weights(N, K, synth.seed_for(f"ovr_su_{N}x{K}"))
+            x = synth.activations(M, K, synth.seed_for(f"ovr_x_{K}_{M}"))
+            ref = orc.swiglu(0, Wg, Wu, x, N, K, nthreads=8)
+            err = H.swiglu_normalised_error(y, ref)
+            assert err <= H.TOL, (tune, case, err)
+            continue
         if kind == "gemv":
             W = synth.weights(fmt, N, K, synth.seed_for(f"ovr_{fmt}_{N}x{K}"))
             x = synth.activations(M, K, synth.seed_for(f"ovr_x_{K}_{M}"))
@@ -301,6 +391,49 @@ def test_launch_overrides(orc, tmp_path, tune):
             assert np.array_equal(res[case], res[case + ":single"]), (tune, case, "not bit-identical")
         err = H.normalised_error(y, y_ref, S)
         assert err <= H.TOL, (tune, case, err)
+
+
+@pytest.mark.parametrize("N,K,M", [(12288, 2560, 512), (8192, 2048, 512), (12288, 2560, 64), (9856, 256, 300)])
+def test_prefill_repeats_are_bit_identical(cuda_lib, orc, N, K, M):
+    """Every slot of every ring is reused many times at these sizes; a copy that
+    overtakes a read still in flight shows up as a changed output row."""
+    q = cuda_lib
+    W = dev(synth.q4_0_weights(N, K, synth.seed_for(f"prefill_{N}x{K}")))
+    x = dev(synth.activations(M, K, synth.seed_for(f"prefill_x_{M}")))
+    ys = [q.qmm_q4_0_prefill(W, x) for _ in range(5)]
+    torch.cuda.synchronize()
+    for y in ys[1:]:
+        assert torch.equal(y, ys[0])
+
+
+PREFILL_RINGS = {
+    # the shallowest rings (two packed-weight slots, two operand slots)
+    "2,2": ["pfrep:q4_0:12288:2560:512", "pfrep:q4_0:4096:2560:256", "pfrep:q4_0:2048:2560:64"],
+}
+
+
+@pytest.mark.parametrize("ring", list(PREFILL_RINGS))
+def test_prefill_shallow_rings(orc, tmp_path, ring):
+    import os
+    import subprocess
+    import sys
+    out = tmp_path / "y.npz"
+    env = dict(os.environ, QMV_PREFILL_RING=ring)
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-m", "tests._launch_override_child", str(out)] + PREFILL_RINGS[ring],
+                       env=env, cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    res = np.load(out)
+    assert int(res["status"][0]) == 0
+    for case in PREFILL_RINGS[ring]:
+        _, fmt, n, k, m = case.split(":")
+        N, K, M = int(n), int(k), int(m)
+        assert bool(res[case + ":identical"][0]), (ring, case, "repeats differ")
+        W = synth.q4_0_weights(N, K, synth.seed_for(f"ovr_pf_{N}x{K}"))
+        x = synth.activations(M, K, synth.seed_for(f"ovr_pf_x_{K}_{M}"))
+        rows = _sample_rows(N, k=32)
+        y_ref, S = orc.qmv_rows(0, W, x, N, K, rows, nthreads=8)
+        assert H.normalised_error(res[case].astype(np.float64)[:, rows], y_ref, S) <= H.TOL, (ring, case)
 
 
 def test_prefill_in_graph_on_a_new_stream(cuda_lib, orc):

@@ -57,6 +57,8 @@ def lib():
             f.argtypes = [vp, vp, vp, i64, i64, i64, vp]
         L.qmv_moe.restype = ctypes.c_int
         L.qmv_moe.argtypes = [vp, vp, i64, vp, vp, i64, i64, i64, vp]
+        L.qmv_q4_0_swiglu.restype = ctypes.c_int
+        L.qmv_q4_0_swiglu.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
         L.qmv_device_status.restype = ctypes.c_int
         L.qmv_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
         L.qmv_set_pdl.restype = None
@@ -86,6 +88,11 @@ def qmv_set_pdl(enable: bool) -> None:
 def _check(fn, code):
     if code != QMV_OK:
         raise QmvError(fn, code)
+
+
+def qmv_q4_0_swiglu_ptr(W_gate: int, W_up: int, x: int, y: int, N: int, K: int, M: int,
+                        stream: int = 0) -> None:
+    _check("qmv_q4_0_swiglu", lib().qmv_q4_0_swiglu(W_gate, W_up, x, y, N, K, M, stream))
 
 
 def qmv_q4_0_ptr(W: int, x: int, y: int, N: int, K: int, M: int, stream: int = 0) -> None:
@@ -152,6 +159,19 @@ def qmv_q4_0(W, x, y=None, stream=None):
     """y[M, N] = x[M, K] @ dequant(W)^T for Q4_0 weights ``W`` (uint8, N rows)."""
     W, x, y, N, K, M = _prep(W, x, y, Q4_0_BLOCK_BYTES, "qmv_q4_0")
     qmv_q4_0_ptr(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, _stream_handle(stream))
+    return y
+
+
+def qmv_q4_0_swiglu(W_gate, W_up, x, y=None, stream=None):
+    """y[M, N] = silu(x @ dequant(W_gate)^T) * (x @ dequant(W_up)^T) for two
+    Q4_0 tables of N rows each (the MLP's gate + up + SwiGLU in one call)."""
+    W_gate, x, y, N, K, M = _prep(W_gate, x, y, Q4_0_BLOCK_BYTES, "qmv_q4_0_swiglu")
+    torch = _torch()
+    if not (W_up.is_cuda and W_up.dtype == torch.uint8 and W_up.is_contiguous()
+            and W_up.numel() == W_gate.numel()):
+        raise ValueError("qmv_q4_0_swiglu: W_up must be a contiguous CUDA uint8 table shaped like W_gate")
+    qmv_q4_0_swiglu_ptr(W_gate.data_ptr(), W_up.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M,
+                        _stream_handle(stream))
     return y
 
 

@@ -145,10 +145,14 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
     p.U = static_cast<int>(U);
     const int unit_bytes = fmt == kQ4_0 ? 144 : 272;
     const Tune &tu = tune_overrides();
-    const TuneEntry *te = tune_lookup(fmt, p.N, p.K, M);
+    // One problem (a plain call, or the fused SwiGLU's gate and up tables
+    // stacked row by row) is planned as one table of rows_total rows; the
+    // multi-expert call by its per-expert shape.
+    const int64_t Nplan = p.n_problems == 1 ? p.rows_total : p.N;
+    const TuneEntry *te = tune_lookup(fmt, Nplan, p.K, M);
 
     // defaults by rule
-    const int64_t wbytes_per_sm = p.N * (p.K / 256) * unit_bytes / (sms > 0 ? sms : 1);
+    const int64_t wbytes_per_sm = Nplan * (p.K / 256) * unit_bytes / (sms > 0 ? sms : 1);
     const bool big = wbytes_per_sm > 128 * 1024 && M <= 2;
     int G = lanes_per_row(p.U, M);
     int warps = big ? 12 : 8;
@@ -181,6 +185,13 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
     if (tu.share >= 1) share = tu.share;
     const int ctas_per_sm = (tu.ctas >= 1 && tu.ctas <= 4) ? tu.ctas : 1;
 
+    if (p.W2) {
+        // fused SwiGLU: a gate row and its up row share a row group, so the
+        // group holds an even number of rows: G a power of two, at most 16.
+        int g2 = 1;
+        while (g2 * 2 <= G && g2 * 2 <= 16) g2 *= 2;
+        G = g2;
+    }
     p.G = G;
     // Passes per stage: odd for G < 8 keeps the lanes of a quarter warp in
     // distinct banks; any value works for G >= 8.
@@ -222,7 +233,7 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
 }
 
 qmv_status run_gemv(int fmt, const void *W, const int32_t *idx, int64_t n_experts, const void *x, float *y,
-                    int64_t N, int64_t K, int64_t M, int n_problems, cudaStream_t stream)
+                    int64_t N, int64_t K, int64_t M, int n_problems, cudaStream_t stream, const void *W2 = nullptr)
 {
     int dev = 0;
     if (current_device(&dev) != cudaSuccess) return QMV_ERR_CUDA;
@@ -242,6 +253,8 @@ qmv_status run_gemv(int fmt, const void *W, const int32_t *idx, int64_t n_expert
     p.n_problems = n_problems;
     p.max_local_problems = n_problems;
     p.rows_total = N * n_problems;
+    p.W2 = static_cast<const uint8_t *>(W2);
+    if (W2) p.rows_total = 2 * N;     // gate and up rows interleaved
     p.status = status;
     const int Mk = static_cast<int>(M);
     const bool pdl = g_pdl.load(std::memory_order_relaxed) != 0;
@@ -252,7 +265,7 @@ qmv_status run_gemv(int fmt, const void *W, const int32_t *idx, int64_t n_expert
         e = (fmt == kQ4_0) ? launch_gemv_stream_q4_0(Mk, p, pl.grid, pl.warps, pl.smem, stream, pdl)
                            : launch_gemv_stream_q8_0(Mk, p, pl.grid, pl.warps, pl.smem, stream, pdl);
     } else {
-        const int64_t warps_needed = p.rows_total;
+        const int64_t warps_needed = W2 ? N : p.rows_total;
         int64_t grid = (warps_needed + 7) / 8;
         if (grid > 32LL * sms) grid = 32LL * sms;
         if (grid < 1) grid = 1;
@@ -333,6 +346,18 @@ qmv_status qmv_q8_0(const void *W, const void *x, float *y, int64_t N, int64_t K
     qmv_status st = check_common(W, x, y, N, K, M, 8);
     if (st != QMV_OK || N == 0 || M == 0) return st;
     return run_gemv(kQ8_0, W, nullptr, 1, x, y, N, K, M, 1, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qmv_status qmv_q4_0_swiglu(const void *W_gate, const void *W_up, const void *x, float *y, int64_t N, int64_t K,
+                           int64_t M, qmv_stream_t stream)
+{
+    qmv_status st = check_common(W_gate, x, y, N, K, M, 8);
+    if (st != QMV_OK || N == 0 || M == 0) return st;
+    if (K > 0 && !W_up) return QMV_ERR_NULL;
+    if (W_up && !aligned(W_up, 16)) return QMV_ERR_ALIGN;
+    if (N > (int64_t(1) << 39)) return QMV_ERR_SHAPE;     // 2N interleaved rows
+    // K == 0 (W_up may then be null): y = silu(0) * 0 = 0, as the plain call gives.
+    return run_gemv(kQ4_0, W_gate, nullptr, 1, x, y, N, K, M, 1, reinterpret_cast<cudaStream_t>(stream), W_up);
 }
 
 qmv_status qmv_moe(const void *W_pool, const int32_t *expert_idx, int64_t n_experts, const void *x, float *y,

@@ -62,7 +62,8 @@ constexpr int kUnitWeights = 256;
 constexpr int kXUnitBytes = 528;   // 512 bytes of permuted activations + 16 bytes pad
 
 struct GemvParams {
-    const uint8_t *W;            // weights; for the multi-expert call, the expert pool
+    const uint8_t *W;            // weights; for the multi-expert call, the expert pool; fused SwiGLU: gate
+    const uint8_t *W2;           // fused SwiGLU: the up table (else nullptr)
     const __half *x;             // [n_problems * M][K]
     float *y;                    // [n_problems * M][N]
     const int32_t *expert_idx;   // multi-expert call only (else nullptr)
@@ -286,8 +287,13 @@ __device__ __forceinline__ bool stage_wait(uint64_t *bar, uint32_t parity, int *
 
 // MOE = the one-launch multi-expert form: problem p is expert slot p with its
 // own token, weights from expert_idx[p] of the pool.  Otherwise one problem
-// of M tokens.
-template <int FMT, int M, int MAXT, bool MOE>
+// of M tokens.  SWIGLU = the MLP's gate + up + SwiGLU in one pass: rows
+// 2n / 2n+1 are row n of the gate / up table (the two tables stacked row by
+// row, "ours stacks gate and up into one table" -- volta-kernel-bakeoff, "A
+// few tokens at once"), a CTA owns whole pairs, and y[m][n] = silu(g) * u is
+// formed in the epilogue ("SwiGLU applied immediately, only the final result
+// written" -- SovereignKernel diary, phase 6).
+template <int FMT, int M, int MAXT, bool MOE, bool SWIGLU = false>
 __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p)
 {
     using T = FmtTraits<FMT>;
@@ -312,8 +318,11 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
 
     // This CTA's contiguous range of (problem, row) pairs.
     const uint32_t R = static_cast<uint32_t>(p.rows_total);
-    const uint32_t row0 = static_cast<uint32_t>((static_cast<uint64_t>(R) * blockIdx.x) / gridDim.x);
-    const uint32_t row1 = static_cast<uint32_t>((static_cast<uint64_t>(R) * (blockIdx.x + 1)) / gridDim.x);
+    // (SwiGLU: whole gate/up pairs, so row0 is even and nrows even.)
+    const uint32_t row0 = SWIGLU ? 2u * static_cast<uint32_t>((static_cast<uint64_t>(R / 2) * blockIdx.x) / gridDim.x)
+                                 : static_cast<uint32_t>((static_cast<uint64_t>(R) * blockIdx.x) / gridDim.x);
+    const uint32_t row1 = SWIGLU ? 2u * static_cast<uint32_t>((static_cast<uint64_t>(R / 2) * (blockIdx.x + 1)) / gridDim.x)
+                                 : static_cast<uint32_t>((static_cast<uint64_t>(R) * (blockIdx.x + 1)) / gridDim.x);
     const int nrows = static_cast<int>(row1 - row0);
     // Problems (expert slots) this CTA touches; always 0..0 for the plain GEMV.
     const int prob_lo = (MOE && nrows > 0) ? static_cast<int>(row0 / N) : 0;
@@ -351,6 +360,9 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
                     const uint32_t n = row - prob * N;
                     const int64_t e = sidx[prob - prob_lo];
                     if (e >= 0 && e < p.n_experts) is_row = p.W + (e * p.N + n) * p.row_bytes;
+                } else if (SWIGLU) {
+                    const uint32_t row = row0 + lr;
+                    is_row = ((row & 1u) ? p.W2 : p.W) + static_cast<int64_t>(row >> 1) * p.row_bytes;
                 } else {
                     is_row = cta_rows + static_cast<int64_t>(lr) * p.row_bytes;
                 }
@@ -566,7 +578,18 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
                     acc[m] = sum;
                 }
             }
-            if (q == 0 && lane_on && lr < nrows) {
+            if (SWIGLU) {
+                // The up row (lr + 1) sits G lanes further on in the same group.
+#pragma unroll
+                for (int m = 0; m < M; ++m) {
+                    const float up = __shfl_down_sync(0xffffffffu, acc[m], G);
+                    if (q == 0 && lane_on && lr < nrows && (lr & 1) == 0) {
+                        const float gate = acc[m] * T::kPrescale;
+                        p.y[static_cast<int64_t>(m) * p.N + ((row0 + lr) >> 1)] =
+                            gate / (1.0f + __expf(-gate)) * (up * T::kPrescale);
+                    }
+                }
+            } else if (q == 0 && lane_on && lr < nrows) {
                 const uint32_t row = row0 + lr;
                 if (MOE) {
                     const uint32_t n = row - prob * N;
@@ -606,7 +629,10 @@ __global__ void __launch_bounds__(256) gemv_generic_kernel(const GemvParams p, i
     const int bb = FmtTraits<FMT>::kBlockBytes;
     const int64_t nblk = p.K / 32;
     pdl_wait_prior_grid();
-    for (int64_t row = gw; row < p.rows_total; row += nw) {
+    // Fused SwiGLU (W2 set): one warp per output row n, both products.
+    const bool swiglu = p.W2 != nullptr;
+    const int64_t nout = swiglu ? p.N : p.rows_total;
+    for (int64_t row = gw; row < nout; row += nw) {
         const int64_t prob = row / p.N;
         const int64_t n = row - prob * p.N;
         int64_t e = 0;
@@ -616,35 +642,47 @@ __global__ void __launch_bounds__(256) gemv_generic_kernel(const GemvParams p, i
             ok = (e >= 0 && e < p.n_experts);
         }
         for (int m0 = 0; m0 < M; m0 += 8) {
-            float acc[8];
+            float acc[8], gacc[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-            if (ok) {
-                const uint8_t *wr = p.W + (e * p.N + n) * p.row_bytes;
-                for (int64_t b = lane; b < nblk; b += 32) {
-                    const uint8_t *blk = wr + b * bb;
-                    const float d = __half2float(__ushort_as_half(
-                        static_cast<unsigned short>(blk[0] | (blk[1] << 8))));
-                    for (int j = 0; j < 32; ++j) {
-                        int c;
-                        if (FMT == kQ4_0) c = (j < 16 ? (blk[2 + j] & 0xF) : (blk[2 + j - 16] >> 4)) - 8;
-                        else c = static_cast<int8_t>(blk[2 + j]);
-                        const float wv = static_cast<float>(c) * d;
+            for (int j = 0; j < 8; ++j) acc[j] = gacc[j] = 0.0f;
+            for (int t = 0; t < (swiglu ? 2 : 1); ++t) {
+                if (t == 1) {
 #pragma unroll
-                        for (int mm = 0; mm < 8; ++mm) {
-                            if (m0 + mm < M)
-                                acc[mm] = fmaf(wv, __half2float(p.x[(prob * M + m0 + mm) * p.K + b * 32 + j]), acc[mm]);
+                    for (int j = 0; j < 8; ++j) {
+                        gacc[j] = acc[j];
+                        acc[j] = 0.0f;
+                    }
+                }
+                if (ok) {
+                    const uint8_t *wr = (t == 1 ? p.W2 : p.W) + (e * p.N + n) * p.row_bytes;
+                    for (int64_t b = lane; b < nblk; b += 32) {
+                        const uint8_t *blk = wr + b * bb;
+                        const float d = __half2float(__ushort_as_half(
+                            static_cast<unsigned short>(blk[0] | (blk[1] << 8))));
+                        for (int j = 0; j < 32; ++j) {
+                            int c;
+                            if (FMT == kQ4_0) c = (j < 16 ? (blk[2 + j] & 0xF) : (blk[2 + j - 16] >> 4)) - 8;
+                            else c = static_cast<int8_t>(blk[2 + j]);
+                            const float wv = static_cast<float>(c) * d;
+#pragma unroll
+                            for (int mm = 0; mm < 8; ++mm) {
+                                if (m0 + mm < M)
+                                    acc[mm] = fmaf(wv, __half2float(p.x[(prob * M + m0 + mm) * p.K + b * 32 + j]), acc[mm]);
+                            }
                         }
                     }
                 }
-            }
 #pragma unroll
-            for (int mm = 0; mm < 8; ++mm)
-                for (int off = 16; off > 0; off >>= 1) acc[mm] += __shfl_xor_sync(0xffffffffu, acc[mm], off);
+                for (int mm = 0; mm < 8; ++mm)
+                    for (int off = 16; off > 0; off >>= 1) acc[mm] += __shfl_xor_sync(0xffffffffu, acc[mm], off);
+            }
             if (lane == 0) {
                 if (!ok) atomicOr(p.status, kDevBadExpert);
-                for (int mm = 0; mm < 8 && m0 + mm < M; ++mm)
-                    p.y[(prob * M + m0 + mm) * p.N + n] = ok ? acc[mm] : __int_as_float(0x7fc00000);
+                for (int mm = 0; mm < 8 && m0 + mm < M; ++mm) {
+                    float v = acc[mm];
+                    if (swiglu) v = gacc[mm] / (1.0f + __expf(-gacc[mm])) * acc[mm];
+                    p.y[(prob * M + m0 + mm) * p.N + n] = ok ? v : __int_as_float(0x7fc00000);
+                }
             }
         }
     }

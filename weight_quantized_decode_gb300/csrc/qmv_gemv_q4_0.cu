@@ -4,10 +4,10 @@
 
 namespace qmv {
 
-template <int M, int MAXT, bool MOE>
+template <int M, int MAXT, bool MOE, bool SWIGLU = false>
 static cudaError_t launch_t(const GemvParams &p, int grid, int warps, size_t smem, cudaStream_t s, bool pdl)
 {
-    auto kernel = gemv_stream_kernel<kQ4_0, M, MAXT, MOE>;
+    auto kernel = gemv_stream_kernel<kQ4_0, M, MAXT, MOE, SWIGLU>;
     cudaError_t e = ensure_smem_optin(reinterpret_cast<const void *>(kernel), smem);
     if (e != cudaSuccess) return e;
     return launch_ex(kernel, dim3(grid), dim3(warps * 32), smem, s, pdl, p);
@@ -22,6 +22,13 @@ static cudaError_t launch_one(const GemvParams &p, int grid, int warps, size_t s
         if constexpr (M == 1) {
             if (warps <= 8) return launch_t<1, 256, true>(p, grid, warps, smem, s, pdl);
             if (warps <= 16) return launch_t<1, 512, true>(p, grid, warps, smem, s, pdl);
+        }
+        return cudaErrorInvalidConfiguration;
+    }
+    if (p.W2) {   // fused gate + up + SwiGLU
+        if (warps <= 8) return launch_t<M, 256, false, true>(p, grid, warps, smem, s, pdl);
+        if constexpr (M <= 2) {
+            if (warps <= 16) return launch_t<M, 512, false, true>(p, grid, warps, smem, s, pdl);
         }
         return cudaErrorInvalidConfiguration;
     }
