@@ -550,6 +550,9 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
                 }
             }
         }
+        // This lane's reads of the stage (generic proxy) are ordered before
+        // the bulk copy that refills the slot (async proxy).
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (issued < total) issue_next();
 
