@@ -56,6 +56,10 @@ WORKLOADS = {
              "shapes": [(12288, 2560), (2560, 6144), (8192, 2048)]},
     # Experts in one launch: (pool size, slots, N, K).
     "moe": {"kind": "moe", "fmt": "q4_0", "configs": [(128, 10, 640, 2560), (128, 8, 512, 2048)]},
+    # The MLP's gate + up + SwiGLU in one call: Llama-3-8B (gate and up 14336x4096
+    # each) and Qwen3-1.7B (6144x2048 each; volta-kernel-bakeoff, "A few tokens at
+    # once": "Qwen3-1.7B's gate + up + SwiGLU"), one token and eight.
+    "q4_0_swiglu": {"kind": "swiglu", "fmt": "q4_0", "M": [1, 8], "shapes": [(14336, 4096), (6144, 2048)]},
     # Prompt (prefill) on the tensor cores.
     "prefill": {"kind": "prefill", "fmt": "q4_0", "M": [64, 512], "shapes": [(12288, 2560), (8192, 2048)]},
 }
@@ -67,6 +71,8 @@ def metric_name(workload):
         return "Q4_0 prefill GEMM TFLOP/s (fp16 tensor cores; us/call per table in 'sweep')"
     if wl["kind"] == "moe":
         return "Q4_0 multi-expert GEMV (one launch) HBM GB/s (algorithmic bytes; us/call per config in 'sweep')"
+    if wl["kind"] == "swiglu":
+        return "Q4_0 fused gate+up+SwiGLU HBM GB/s (algorithmic bytes of both tables; us/call per table in 'sweep')"
     return f"{wl['fmt'].upper()} GEMV HBM GB/s (algorithmic bytes; us/call per table in 'sweep')"
 
 
@@ -84,6 +90,11 @@ def peaks():
 def algo_bytes(fmt, N, K, M):
     bb = 18 if fmt == "q4_0" else 34
     return N * (K // 32) * bb + 2 * M * K + 4 * M * N
+
+
+def algo_bytes_swiglu(N, K, M):
+    """Both Q4_0 tables once, the activations once, y once."""
+    return 2 * N * (K // 32) * 18 + 2 * M * K + 4 * M * N
 
 
 class ClockSampler:
@@ -239,6 +250,24 @@ def run_ours(args, dist, rank, local, world):
                 def call(s, c=c):
                     W = c["W"][s % c["copies"]]
                     fn_ptr(W.data_ptr(), c["x"].data_ptr(), c["y"].data_ptr(), c["N"], c["K"], c["M"], sh)
+                c["call"] = call
+                calls.append(c)
+    elif kind == "swiglu":
+        for (N, K) in wl["shapes"]:
+            # gate rows 0..N-1 and up rows N..2N-1 of one rotated allocation
+            Wd, copies = rotated_copies(2 * N, K, f"swiglu_{N}x{K}")
+            for M in wl["M"]:
+                x = synth.activations(M, K, synth.seed_for(f"x_{K}_{M}"))
+                c = {"name": f"{N}x{K}/M{M}", "N": N, "K": K, "M": M, "W": Wd, "copies": copies,
+                     "x": torch.from_numpy(x).to(dev), "y": torch.empty((M, N), dtype=torch.float32, device=dev),
+                     "x_host": torch.from_numpy(x).pin_memory(),
+                     "y_host": torch.empty((M, N), dtype=torch.float32).pin_memory(),
+                     "bytes": algo_bytes_swiglu(N, K, M), "flops": 4 * M * N * K}
+
+                def call(s, c=c):
+                    W = c["W"][s % c["copies"]]
+                    q.qmv_q4_0_swiglu_ptr(W[:c["N"]].data_ptr(), W[c["N"]:].data_ptr(), c["x"].data_ptr(),
+                                          c["y"].data_ptr(), c["N"], c["K"], c["M"], sh)
                 c["call"] = call
                 calls.append(c)
     else:  # moe: a pool of experts, distinct indices drawn per step
@@ -460,6 +489,23 @@ def oracle_tasks(workload):
     fid = 0 if fmt == "q4_0" else 1
     bb = 18 if fmt == "q4_0" else 34
     jobs = []
+    if wl["kind"] == "swiglu":
+        sjobs = []
+        for (N, K) in wl["shapes"]:
+            W2 = synth.weights(fmt, 2 * N, K, synth.seed_for(f"swiglu_{N}x{K}"))
+            for M in wl["M"]:
+                x = synth.activations(M, K, synth.seed_for(f"x_{K}_{M}"))
+                sjobs.append((W2[:N], W2[N:], x, N, K, M))
+
+        def run_swiglu(frac):
+            b = f = 0
+            for (Wg, Wu, x, N, K, M) in sjobs:
+                rows = np.linspace(0, N - 1, max(1, int(N * frac))).astype(np.int64)
+                orc.swiglu(fid, Wg, Wu, x, N, K, rows=rows, nthreads=threads)
+                b += 2 * rows.size * (K // 32) * bb + 2 * M * K + 4 * M * rows.size
+                f += 4 * M * rows.size * K
+            return b, f
+        return run_swiglu, threads, wl["kind"]
     if wl["kind"] in ("gemv", "prefill"):
         for (N, K) in wl["shapes"]:
             W = synth.weights(fmt, N, K, synth.seed_for(f"{fmt}_{N}x{K}"))
@@ -554,7 +600,8 @@ def run_reference(args, rank, world):
 def ncu_case(spec):
     """A handful of eager calls of one table over rotated copies larger than L2
     (a small, bounded program for an Nsight Compute capture).
-    spec: q4_0:NxK:M | q8_0:NxK:M | prefill:NxK:M | moe:NxK:SLOTS (pool of 128)."""
+    spec: q4_0:NxK:M | q8_0:NxK:M | prefill:NxK:M | moe:NxK:SLOTS (pool of 128) |
+    swiglu:NxK:M (gate and up tables of N rows each)."""
     import torch
     import weight_quantized_decode_gb300 as q
     kind, shape, M = spec.split(":")
@@ -563,7 +610,7 @@ def ncu_case(spec):
     dev = torch.device("cuda", 0)
     fmt = "q8_0" if kind == "q8_0" else "q4_0"
     bb = 18 if fmt == "q4_0" else 34
-    rows = 128 * N if kind == "moe" else N
+    rows = 128 * N if kind == "moe" else (2 * N if kind == "swiglu" else N)
     wbytes = rows * (K // 32) * bb
     copies = max(2, math.ceil(2.5 * 128e6 / wbytes))
     base = torch.from_numpy(synth.weights(fmt, rows, K, synth.seed_for(f"{fmt}_{rows}x{K}"))).to(dev)
@@ -576,6 +623,9 @@ def ncu_case(spec):
         Wi = W[i % copies].data_ptr()
         if kind == "moe":
             q.qmv_moe_ptr(Wi, idx[i].data_ptr(), 128, x.data_ptr(), y.data_ptr(), N, K, M, s)
+        elif kind == "swiglu":
+            Wc = W[i % copies]
+            q.qmv_q4_0_swiglu_ptr(Wc[:N].data_ptr(), Wc[N:].data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, s)
         else:
             fn = {"q4_0": q.qmv_q4_0_ptr, "q8_0": q.qmv_q8_0_ptr, "prefill": q.qmm_q4_0_prefill_ptr}[kind]
             fn(Wi, x.data_ptr(), y.data_ptr(), N, K, M, s)
