@@ -5,10 +5,10 @@ Default workload (one "step" = one call on every shape, each on its next
 rotated weight copy):  Q4_0 GEMV, M = 1 token, Llama-3-8B-style tables
 4096x4096, 6144x4096, 4096x14336, 14336x4096, 28672x4096, 128256x4096 (the
 shapes of sm8x-bench's summary table), codes uniform 0..15, per-32 fp16 scale
-uniform in [0.005, 0.02], fp16 N(0,1) activations, seeded.  Every shape cycles
-through enough copies of its weights to exceed 4x the L2 so each call streams
-from HBM ("cycles through enough copies of its weights" -- volta-kernel-bakeoff,
-"Making it fair").
+uniform in [0.005, 0.02], fp16 N(0,1) activations, seeded.  Every shape rotates
+over enough copies of its weights to exceed 4x the L2 so each call streams
+from HBM (the bakeoff rotates weight copies for the same reason --
+volta-kernel-bakeoff, "Making it fair").
 
 Metric: HBM GB/s of algorithmic bytes (weights + activations + outputs) over
 the timed steps, plus per-shape us/call, GB/s and the fraction of the measured
@@ -57,8 +57,8 @@ WORKLOADS = {
     # Experts in one launch: (pool size, slots, N, K).
     "moe": {"kind": "moe", "fmt": "q4_0", "configs": [(128, 10, 640, 2560), (128, 8, 512, 2048)]},
     # The MLP's gate + up + SwiGLU in one call: Llama-3-8B (gate and up 14336x4096
-    # each) and Qwen3-1.7B (6144x2048 each; volta-kernel-bakeoff, "A few tokens at
-    # once": "Qwen3-1.7B's gate + up + SwiGLU"), one token and eight.
+    # each) and Qwen3-1.7B (6144x2048 each, the fused MLP table the bakeoff times
+    # -- volta-kernel-bakeoff, "A few tokens at once"), one token and eight.
     "q4_0_swiglu": {"kind": "swiglu", "fmt": "q4_0", "M": [1, 8], "shapes": [(14336, 4096), (6144, 2048)]},
     # Prompt (prefill) on the tensor cores.
     "prefill": {"kind": "prefill", "fmt": "q4_0", "M": [64, 512], "shapes": [(12288, 2560), (8192, 2048)]},

@@ -2,9 +2,9 @@
  * qmv.h -- C ABI of the block-quantised weight x activation product used by
  * single-stream LLM decode, for one NVIDIA GB300 (sm_103a).
  *
- * The operation, for every call below (the "stack of GEMVs, one activation row
- * x each weight matrix" of H100-KERNEL-5X-ROADMAP, "Why the decode gap is
- * bandwidth, not arithmetic"):
+ * The operation, for every call below (one token's decode step multiplies its
+ * activation row by each weight matrix in turn -- H100-KERNEL-5X-ROADMAP,
+ * "Why the decode gap is bandwidth, not arithmetic"):
  *
  *     y[m][n] = sum_k x[m][k] * w[n][k],   0 <= m < M, 0 <= n < N, 0 <= k < K
  *
@@ -80,11 +80,11 @@ typedef enum {
 #define QMV_DEV_TIMEOUT     0x2   /* a bounded wait in a kernel gave up          */
 
 /*
- * Q4_0 decode GEMV.  "fused_q4 ...: one warp per output row, unpacks in
- * registers, fp32 sums; v2 = fp16 bit trick (0x6400 | n is the half 1024 + n)"
- * (volta-kernel-bakeoff, "What's in the race"); "multiple output rows per warp
- * for memory-level parallelism + a per-shape launch config" (sm8x-bench,
- * summary).
+ * Q4_0 decode GEMV.  Prior art: the bakeoff's fused_q4 kernels (a warp per
+ * row, codes unpacked in registers, fp32 sums; v2 builds halves from codes by
+ * OR-ing them into the 0x6400 pattern -- volta-kernel-bakeoff, "What's in the
+ * race") and the sm8x kernel (several rows per warp to keep more loads in
+ * flight, launch shape chosen per table -- sm8x-bench, summary).
  *   W : Q4_0 bytes [N][K/32*18], 16-byte aligned.
  *   x : fp16 [M][K], 2-byte aligned.        y : fp32 [M][N], 4-byte aligned.
  *   N >= 0, K >= 0 with K % 32 == 0, 0 <= M <= 8.
@@ -104,10 +104,10 @@ QMV_API qmv_status qmv_q8_0(const void *W, const void *x, float *y,
                     int64_t N, int64_t K, int64_t M, qmv_stream_t stream);
 
 /*
- * Several experts, one token each, in ONE launch ("moe_*: the MoE case: 8-10
- * experts, one token each, in one launch" -- volta-kernel-bakeoff, "What's in
- * the race"; "each expert with its own weights and token, so a wrong expert
- * index fails too" -- "Making it fair").
+ * Several experts, each with its own token, in ONE launch (the bakeoff's moe_*
+ * contenders run 8 to 10 experts this way -- volta-kernel-bakeoff, "What's in
+ * the race"; every expert gets distinct weights and its own token, so that a
+ * wrong index shows up as a wrong result -- "Making it fair").
  *   W_pool     : n_experts Q4_0 experts of N x K each, back to back
  *                (expert e starts at byte e * N * (K/32) * 18), 16-byte aligned.
  *   expert_idx : DEVICE int32 [M]; slot s uses expert expert_idx[s].
@@ -130,11 +130,12 @@ QMV_API qmv_status qmv_moe(const void *W_pool, const int32_t *expert_idx, int64_
  * function applied before anything is written --
  *     y[m][n] = silu(g) * u,  g = sum_k x[m][k] wg[n][k],  u = sum_k x[m][k] wu[n][k],
  *     silu(g) = g / (1 + e^-g)
- * ("ours stacks gate and up into one table and converts once" --
- * volta-kernel-bakeoff, "A few tokens at once"; "fused W1 + W3 + SwiGLU into a
- * single kernel -- X is read once, ... only the final result written" --
- * SovereignKernel diary, phase 6).  The two tables stay separate arrays; the
- * kernel interleaves their rows as it streams them.
+ * (the bakeoff treats gate and up as one stacked table with a single pass
+ * over the activations -- volta-kernel-bakeoff, "A few tokens at once"; the
+ * diary's phase-6 kernel fuses W1, W3 and SwiGLU so that the activations are
+ * read once and only the activated output is stored -- SovereignKernel diary,
+ * phase 6).  The two tables stay separate arrays; the kernel interleaves their
+ * rows as it streams them.
  *   W_gate, W_up : Q4_0 bytes [N][K/32*18] each, 16-byte aligned (W_up may
  *                  be NULL only when K == 0).
  *   x : fp16 [M][K].  y : fp32 [M][N] (overwritten).  M <= 8.
@@ -147,10 +148,11 @@ QMV_API qmv_status qmv_q4_0_swiglu(const void *W_gate, const void *W_up, const v
                            int64_t N, int64_t K, int64_t M, qmv_stream_t stream);
 
 /*
- * Q4_0 prefill GEMM for many tokens (M >= 1, intended for M >= 64): "tensor
- * cores for prompts: unpack a tile to shared memory" (tc_q4 --
- * volta-kernel-bakeoff, "What's in the race"; "unpack quantized weights inside
- * a tensor-core multiply" -- "What we'd do next", item 3).  On sm_103a: packed
+ * Q4_0 prefill GEMM for many tokens (M >= 1, intended for M >= 64).  Prior
+ * art: the bakeoff's tc_q4, which dequantises a tile into shared memory for the
+ * tensor cores (volta-kernel-bakeoff, "What's in the race"), and the plan to
+ * dequantise inside the tensor-core multiply ("What we'd do next", item 3).
+ * On sm_103a: packed
  * W tiles staged by bulk copies, dequantised to 16-bit in shared memory, fed to
  * tcgen05.mma with fp32 accumulators in tensor memory.
  *   W : Q4_0 bytes [N][K/32*18], 16-byte aligned.  The tensor-core kernel

@@ -186,16 +186,16 @@ __device__ __forceinline__ float half_hi_to_float(uint32_t u)
 // ---- fp16 magic-number unpack -----------------------------------------------------
 //
 // The half with bit pattern 0x6400 | n is exactly 1024 + n for 0 <= n < 1024
-// ("v2 = fp16 bit trick (0x6400 | n is the half 1024 + n)" -- volta-kernel-
-// bakeoff, "What's in the race").  One LOP3 places two nibbles (or, after a
+// (the unpack of the bakeoff's v2 kernel -- volta-kernel-bakeoff, "What's in
+// the race").  One LOP3 places two nibbles (or, after a
 // PRMT, two bytes) into the mantissas of a half2; one HFMA2 then removes the
 // 1024 offset and the code bias and applies a power-of-two pre-scale, exactly.
 //
 // The weights come out pre-scaled (Q4_0: (c - 8) / 32, Q8_0: q / 512) so that
-// fp16 partial sums of large activations cannot overflow ("weights are
-// unpacked as (code - 8) / 32 ... so no fp16 activation can overflow a partial
-// sum" -- volta-kernel-bakeoff, "A few tokens at once").  The fp32 block sums
-// are multiplied back by 32 (or 512) at the end.
+// fp16 partial sums of large activations stay finite (the bakeoff divides the
+// centred code by 32 for the same reason -- volta-kernel-bakeoff, "A few
+// tokens at once").  The fp32 block sums are multiplied back by 32 (or 512)
+// at the end.
 constexpr float kQ4Prescale = 32.0f;
 constexpr float kQ8Prescale = 512.0f;
 

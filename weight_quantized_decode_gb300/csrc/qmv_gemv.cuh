@@ -12,21 +12,23 @@
 //     of row r from the stage with 128-bit shared loads (a 144-/272-byte lane
 //     stride is bank-conflict-free), unpacks nibbles/bytes with the fp16
 //     0x6400|n trick, and accumulates half2 products per block, scaled to fp32
-//     per block ("v2 = fp16 bit trick", "v2w = a whole 32-value group per lane
-//     step" -- volta-kernel-bakeoff, "What's in the race").
-//   * G lanes per row, RG = 32/G rows per warp ("multiple output rows per warp
-//     for memory-level parallelism + a per-shape launch config" -- sm8x-bench,
-//     summary); the G partial sums of a row are combined with warp shuffles
-//     ("one warp (32 threads) per output row, __shfl_down_sync" --
-//     SovereignKernel diary, Phase 3): xor butterflies when G is a power of
+//     per block (the bakeoff's v2 unpack and its v2w variant, which takes a
+//     full 32-weight block per lane step -- volta-kernel-bakeoff, "What's in
+//     the race").
+//   * G lanes per row, RG = 32/G rows per warp (several rows per warp keep
+//     more loads in flight, and the launch shape is chosen per table --
+//     sm8x-bench, summary); the G partial sums of a row are combined with warp
+//     shuffles (the diary's kernel gives a whole warp to each row and reduces
+//     it with shuffles -- SovereignKernel diary, Phase 3): xor butterflies when G is a power of
 //     two; a G that does not divide 32 (a tuning choice, e.g. G = 10 for rows
 //     of 10 units) leaves lanes RG*G.. idle and sums the G partials in lane
 //     order.
 //   * Activations live in shared memory for the whole call, permuted once per
 //     CTA into the pair order the unpack produces and padded so that the G
 //     distinct units a warp reads at once fall in distinct banks.  For M > 1
-//     one unpacked weight register serves all M tokens ("lets one activation
-//     load serve several rows" -- volta-kernel-bakeoff, "A few tokens").
+//     one unpacked weight register serves all M tokens (the bakeoff's
+//     few-token kernel reuses each load across rows and tokens --
+//     volta-kernel-bakeoff, "A few tokens at once").
 //   * Rows are split across CTAs in balanced contiguous ranges; within a CTA
 //     the row groups are dealt to warps round-robin.
 //   * Programmatic dependent launch: the first S stages of W are requested
@@ -288,11 +290,10 @@ __device__ __forceinline__ bool stage_wait(uint64_t *bar, uint32_t parity, int *
 // MOE = the one-launch multi-expert form: problem p is expert slot p with its
 // own token, weights from expert_idx[p] of the pool.  Otherwise one problem
 // of M tokens.  SWIGLU = the MLP's gate + up + SwiGLU in one pass: rows
-// 2n / 2n+1 are row n of the gate / up table (the two tables stacked row by
-// row, "ours stacks gate and up into one table" -- volta-kernel-bakeoff, "A
-// few tokens at once"), a CTA owns whole pairs, and y[m][n] = silu(g) * u is
-// formed in the epilogue ("SwiGLU applied immediately, only the final result
-// written" -- SovereignKernel diary, phase 6).
+// 2n / 2n+1 are row n of the gate / up table (the two tables handled as one
+// stacked table -- volta-kernel-bakeoff, "A few tokens at once"), a CTA owns
+// whole pairs, and y[m][n] = silu(g) * u is formed in the epilogue, so only
+// the activated result reaches memory (SovereignKernel diary, phase 6).
 template <int FMT, int M, int MAXT, bool MOE, bool SWIGLU = false>
 __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p)
 {

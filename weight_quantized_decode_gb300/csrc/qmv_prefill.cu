@@ -3,10 +3,11 @@
 //
 //   y[m][n] = sum_k x[m][k] * w[n][k]     (many tokens m; W in GGUF Q4_0)
 //
-// Prior art on the pages: "tc_q4: ours, tensor cores for prompts: unpack a tile
-// to shared memory, WMMA 16x16x16" (volta-kernel-bakeoff, "What's in the
-// race"), and the Marlin-style plan of "What we'd do next" item 3 ("unpack
-// quantized weights inside a tensor-core multiply").  The GB300 form:
+// Prior art on the pages: the bakeoff's tc_q4 contender, which dequantises a
+// weight tile into shared memory and multiplies it with 16x16x16 WMMA
+// fragments (volta-kernel-bakeoff, "What's in the race"), and the Marlin-style
+// plan of "What we'd do next" item 3 (dequantise inside the tensor-core
+// multiply itself).  The GB300 form:
 //
 //   * One CTA computes a 128-row (weights) x TN-column (tokens) tile of y^T in
 //     tensor memory: weights are the MMA's M side (128 lanes), tokens its N
