@@ -61,6 +61,10 @@ class Oracle:
         lib.oracle_swiglu_rows.restype = ctypes.c_int
         lib.oracle_swiglu_rows.argtypes = [ctypes.c_int, _ptr, _ptr, _ptr, _i64, _i64, _i64, _ptr, _i64,
                                            _ptr, _ptr, _ptr, _ptr, _ptr, ctypes.c_int]
+        lib.oracle_qmv_rows_f32.restype = ctypes.c_int
+        lib.oracle_qmv_rows_f32.argtypes = lib.oracle_qmv_rows.argtypes
+        lib.oracle_swiglu_rows_f32.restype = ctypes.c_int
+        lib.oracle_swiglu_rows_f32.argtypes = lib.oracle_swiglu_rows.argtypes
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         self.lib = lib
@@ -81,6 +85,15 @@ class Oracle:
             raise TypeError("x must be float16 (or its uint16 bit patterns)")
         return x
 
+    @classmethod
+    def _x_arg(cls, x):
+        """(activations as passed to C, True for fp32): float32 arrays go to the
+        fp32 entry points, float16 / uint16 ones to the fp16 entry points."""
+        x = np.ascontiguousarray(x)
+        if x.dtype == np.float32:
+            return x, True
+        return cls._x_bits(x), False
+
     def half_to_double(self, bits: int) -> float:
         return self.lib.oracle_half_to_double(int(bits) & 0xFFFF)
 
@@ -96,17 +109,22 @@ class Oracle:
         return w
 
     def qmv(self, fmt: int, W, x, N: int, K: int, nthreads: int = 1):
-        """Return (y, S), both float64 [M][N]."""
+        """Return (y, S), both float64 [M][N].  x is float16 (or its uint16 bit
+        patterns) or float32; either way its values enter the fp64 sums exactly."""
         Wb = self._u8(W)
-        xb = self._x_bits(x)
+        xb, f32 = self._x_arg(x)
         xb = xb.reshape(xb.shape[0], K) if xb.ndim == 2 else xb.reshape(-1, K)
         M = xb.shape[0]
         if Wb.size < N * (K // 32) * self.block_bytes(fmt):
             raise ValueError("W buffer too small")
         y = np.empty((M, N), dtype=np.float64)
         S = np.empty((M, N), dtype=np.float64)
-        rc = self.lib.oracle_qmv(fmt, Wb.ctypes.data, xb.ctypes.data, N, K, M,
-                                 y.ctypes.data, S.ctypes.data, nthreads)
+        if f32:
+            rc = self.lib.oracle_qmv_rows_f32(fmt, Wb.ctypes.data, xb.ctypes.data, N, K, M, None, N,
+                                              y.ctypes.data, S.ctypes.data, nthreads)
+        else:
+            rc = self.lib.oracle_qmv(fmt, Wb.ctypes.data, xb.ctypes.data, N, K, M,
+                                     y.ctypes.data, S.ctypes.data, nthreads)
         if rc != 0:
             raise ValueError(f"oracle_qmv failed ({rc})")
         return y, S
@@ -114,14 +132,15 @@ class Oracle:
     def qmv_rows(self, fmt: int, W, x, N: int, K: int, rows, nthreads: int = 1):
         """(y, S) for the listed rows only: float64 [M][len(rows)]."""
         Wb = self._u8(W)
-        xb = self._x_bits(x).reshape(-1, K)
+        xb, f32 = self._x_arg(x)
+        xb = xb.reshape(-1, K)
         M = xb.shape[0]
         rows = np.ascontiguousarray(rows, dtype=np.int64)
         y = np.empty((M, rows.size), dtype=np.float64)
         S = np.empty((M, rows.size), dtype=np.float64)
-        rc = self.lib.oracle_qmv_rows(fmt, Wb.ctypes.data, xb.ctypes.data, N, K, M,
-                                      rows.ctypes.data, rows.size, y.ctypes.data,
-                                      S.ctypes.data, nthreads)
+        fn = self.lib.oracle_qmv_rows_f32 if f32 else self.lib.oracle_qmv_rows
+        rc = fn(fmt, Wb.ctypes.data, xb.ctypes.data, N, K, M,
+                rows.ctypes.data, rows.size, y.ctypes.data, S.ctypes.data, nthreads)
         if rc != 0:
             raise ValueError(f"oracle_qmv_rows failed ({rc})")
         return y, S
@@ -146,7 +165,8 @@ class Oracle:
         """Gate + up + SwiGLU: dict of float64 [M][n] arrays y, g, u, Sg, Su
         (n = N, or len(rows) for the listed rows)."""
         Wgb, Wub = self._u8(Wg), self._u8(Wu)
-        xb = self._x_bits(x).reshape(-1, K)
+        xb, f32 = self._x_arg(x)
+        xb = xb.reshape(-1, K)
         M = xb.shape[0]
         need = N * (K // 32) * self.block_bytes(fmt)
         if Wgb.size < need or Wub.size < need:
@@ -157,7 +177,8 @@ class Oracle:
             rows = np.ascontiguousarray(rows, dtype=np.int64)
             rp, nr = rows.ctypes.data, rows.size
         out = {k: np.empty((M, nr), dtype=np.float64) for k in ("y", "g", "u", "Sg", "Su")}
-        rc = self.lib.oracle_swiglu_rows(fmt, Wgb.ctypes.data, Wub.ctypes.data, xb.ctypes.data, N, K, M, rp, nr,
+        fn = self.lib.oracle_swiglu_rows_f32 if f32 else self.lib.oracle_swiglu_rows
+        rc = fn(fmt, Wgb.ctypes.data, Wub.ctypes.data, xb.ctypes.data, N, K, M, rp, nr,
                                          out["y"].ctypes.data, out["g"].ctypes.data, out["u"].ctypes.data,
                                          out["Sg"].ctypes.data, out["Su"].ctypes.data, nthreads)
         if rc != 0:

@@ -12,10 +12,11 @@
  *     y[m][n] = sum_k  x[m][k] * w[n][k]             (fp64)
  *     S[m][n] = sum_k |x[m][k] * w[n][k]|            (fp64, for the tolerance)
  *
- * "a CPU double-precision reference of the same quantized weights"
- *   -- volta-kernel-bakeoff, "Making it fair" (correct before fast).
- * "Single-stream decode is a stack of GEMVs (one activation row x each weight
- *  matrix)" -- H100-KERNEL-5X-ROADMAP, "Why the decode gap is bandwidth".
+ * Every kernel is checked against an fp64 CPU product over the same quantised
+ * weights before it is timed (volta-kernel-bakeoff, "Making it fair").  A
+ * decode step of one token is a sequence of such matrix-vector products, one
+ * per weight matrix (H100-KERNEL-5X-ROADMAP, "Why the decode gap is
+ * bandwidth, not arithmetic").
  *
  * Weight formats (GGUF; "Q4_0", "group_size 32" -- sm8x-bench, Q4_0 summary
  * and "Our kernel does what llama.cpp does"; Q8_0 -- H100-KERNEL-5X-ROADMAP,
@@ -26,7 +27,13 @@
  *   Q8_0 block, 34 bytes, 32 weights:  bytes 0..1 = fp16 d, bytes 2..33 =
  *     int8 codes q[0..31]; w = q * d.
  *   A row of W holds K/32 consecutive blocks; rows are dense (no padding).
- *   x is fp16 (IEEE binary16 bit patterns), row-major [M][K].
+ *   x is fp16 (IEEE binary16 bit patterns), row-major [M][K]; the _f32 entry
+ *   points take fp32 activations instead (the bakeoff's fused_q4_v3_fp32in
+ *   accepts fp32 and includes the narrowing in its time -- volta-kernel-
+ *   bakeoff, "Results (one token, microseconds, lower is better)"), whose
+ *   values enter the sums exactly: the product is defined on the activations
+ *   the caller passes, and any narrowing a kernel does on the way is part of
+ *   its rounding error, not of the definition.
  *
  * Parity pins: see tests/test_oracle.py (hand-computed fixtures under
  * tests/golden/, closed forms, invariants, exhaustive fp16 decode against
@@ -111,18 +118,29 @@ int oracle_dequant_row(int fmt, const uint8_t *W, int64_t n, int64_t K, double *
     return 0;
 }
 
-/* y and S for the rows listed in rows[0..nrows-1] (all rows when rows is NULL,
- * then nrows = N).  Outputs are [M][nrows] row-major. */
-int oracle_qmv_rows(int fmt, const uint8_t *W, const uint16_t *x,
-                    int64_t N, int64_t K, int64_t M,
-                    const int64_t *rows, int64_t nrows,
-                    double *y, double *S, int nthreads)
+/* Activations widened to fp64 (exact for both fp16 and fp32). */
+static double *widen_half(const uint16_t *x, int64_t n)
 {
-    if (oracle_block_bytes(fmt) < 0 || K % 32 != 0 || N < 0 || M < 0) return -1;
-    if (rows == NULL) nrows = N;
-    double *xd = (double *)malloc(sizeof(double) * (size_t)(M * K > 0 ? M * K : 1));
-    if (!xd) return -2;
-    for (int64_t i = 0; i < M * K; ++i) xd[i] = oracle_half_to_double(x[i]);
+    double *xd = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    if (xd)
+        for (int64_t i = 0; i < n; ++i) xd[i] = oracle_half_to_double(x[i]);
+    return xd;
+}
+
+static double *widen_float(const float *x, int64_t n)
+{
+    double *xd = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    if (xd)
+        for (int64_t i = 0; i < n; ++i) xd[i] = (double)x[i];
+    return xd;
+}
+
+/* y and S for the listed rows, from fp64 activations xd[M][K]. */
+static int qmv_rows_xd(int fmt, const uint8_t *W, const double *xd,
+                       int64_t N, int64_t K, int64_t M,
+                       const int64_t *rows, int64_t nrows,
+                       double *y, double *S, int nthreads)
+{
     int failed = 0;
 #ifdef _OPENMP
     if (nthreads < 1) nthreads = 1;
@@ -145,9 +163,39 @@ int oracle_qmv_rows(int fmt, const uint8_t *W, const uint16_t *x,
         }
         free(w);
     }
-    free(xd);
     (void)nthreads;
     return failed ? -3 : 0;
+}
+
+/* y and S for the rows listed in rows[0..nrows-1] (all rows when rows is NULL,
+ * then nrows = N).  Outputs are [M][nrows] row-major. */
+int oracle_qmv_rows(int fmt, const uint8_t *W, const uint16_t *x,
+                    int64_t N, int64_t K, int64_t M,
+                    const int64_t *rows, int64_t nrows,
+                    double *y, double *S, int nthreads)
+{
+    if (oracle_block_bytes(fmt) < 0 || K % 32 != 0 || N < 0 || M < 0) return -1;
+    if (rows == NULL) nrows = N;
+    double *xd = widen_half(x, M * K);
+    if (!xd) return -2;
+    int rc = qmv_rows_xd(fmt, W, xd, N, K, M, rows, nrows, y, S, nthreads);
+    free(xd);
+    return rc;
+}
+
+/* oracle_qmv_rows with fp32 activations x[M][K]. */
+int oracle_qmv_rows_f32(int fmt, const uint8_t *W, const float *x,
+                        int64_t N, int64_t K, int64_t M,
+                        const int64_t *rows, int64_t nrows,
+                        double *y, double *S, int nthreads)
+{
+    if (oracle_block_bytes(fmt) < 0 || K % 32 != 0 || N < 0 || M < 0) return -1;
+    if (rows == NULL) nrows = N;
+    double *xd = widen_float(x, M * K);
+    if (!xd) return -2;
+    int rc = qmv_rows_xd(fmt, W, xd, N, K, M, rows, nrows, y, S, nthreads);
+    free(xd);
+    return rc;
 }
 
 /* Full product: y[M][N], S[M][N]. */
@@ -157,10 +205,10 @@ int oracle_qmv(int fmt, const uint8_t *W, const uint16_t *x,
     return oracle_qmv_rows(fmt, W, x, N, K, M, NULL, N, y, S, nthreads);
 }
 
-/* Several experts, one token each, in one call ("moe_*: the MoE case: 8-10
- * experts, one token each, in one launch" -- volta-kernel-bakeoff, "What's in
- * the race"; "each expert with its own weights and token, so a wrong expert
- * index fails too" -- "Making it fair").
+/* Several experts, one token each, in one call (the bakeoff's moe_*
+ * contenders run 8 to 10 experts in a single launch -- volta-kernel-bakeoff,
+ * "What's in the race"; each expert has distinct weights and its own token, so
+ * a wrong index changes the result -- "Making it fair").
  * Slot s uses expert e = idx[s] of a pool of n_experts experts stored back to
  * back (expert e starts e * N * (K/32) blocks in), token x[s][0..K-1], and
  * writes y[s][0..N-1], S[s][0..N-1].  An index outside [0, n_experts) is an
@@ -184,10 +232,10 @@ int oracle_moe(int fmt, const uint8_t *W_pool, const int32_t *idx, int64_t n_exp
 }
 
 /* The MLP's gate + up + SwiGLU at decode, as one product over two tables that
- * share the activations ("ours stacks gate and up into one table and converts
- * once" -- volta-kernel-bakeoff, "A few tokens at once"; "fused W1 + W3 +
- * SwiGLU into a single kernel -- X is read once" -- SovereignKernel diary,
- * phase 6).  SwiGLU with its usual swish: the gate product goes through
+ * share the activations (gate and up handled as one stacked table --
+ * volta-kernel-bakeoff, "A few tokens at once"; W1, W3 and SwiGLU fused so the
+ * activations are read once -- SovereignKernel diary, phase 6).  SwiGLU with
+ * its usual swish: the gate product goes through
  * silu(g) = g / (1 + e^-g) and multiplies the up product:
  *
  *     g[m][n] = sum_k x[m][k] * wg[n][k]        u[m][n] = sum_k x[m][k] * wu[n][k]
@@ -196,20 +244,46 @@ int oracle_moe(int fmt, const uint8_t *W_pool, const int32_t *idx, int64_t n_exp
  * For the listed rows (all rows when rows is NULL, then nrows = N); every
  * output is [M][nrows] row-major and fp64: y, g, u and the S sums of the two
  * products (the tolerance of a fused result is derived from them). */
-int oracle_swiglu_rows(int fmt, const uint8_t *Wg, const uint8_t *Wu, const uint16_t *x,
-                       int64_t N, int64_t K, int64_t M, const int64_t *rows, int64_t nrows,
-                       double *y, double *g, double *u, double *Sg, double *Su, int nthreads)
+static int swiglu_rows_xd(int fmt, const uint8_t *Wg, const uint8_t *Wu, const double *xd,
+                          int64_t N, int64_t K, int64_t M, const int64_t *rows, int64_t nrows,
+                          double *y, double *g, double *u, double *Sg, double *Su, int nthreads)
 {
-    int rc = oracle_qmv_rows(fmt, Wg, x, N, K, M, rows, nrows, g, Sg, nthreads);
+    int rc = qmv_rows_xd(fmt, Wg, xd, N, K, M, rows, nrows, g, Sg, nthreads);
     if (rc != 0) return rc;
-    rc = oracle_qmv_rows(fmt, Wu, x, N, K, M, rows, nrows, u, Su, nthreads);
+    rc = qmv_rows_xd(fmt, Wu, xd, N, K, M, rows, nrows, u, Su, nthreads);
     if (rc != 0) return rc;
-    if (rows == NULL) nrows = N;
     for (int64_t i = 0; i < M * nrows; ++i) {
         const double gate = g[i];
         y[i] = gate / (1.0 + exp(-gate)) * u[i];
     }
     return 0;
+}
+
+int oracle_swiglu_rows(int fmt, const uint8_t *Wg, const uint8_t *Wu, const uint16_t *x,
+                       int64_t N, int64_t K, int64_t M, const int64_t *rows, int64_t nrows,
+                       double *y, double *g, double *u, double *Sg, double *Su, int nthreads)
+{
+    if (oracle_block_bytes(fmt) < 0 || K % 32 != 0 || N < 0 || M < 0) return -1;
+    if (rows == NULL) nrows = N;
+    double *xd = widen_half(x, M * K);
+    if (!xd) return -2;
+    int rc = swiglu_rows_xd(fmt, Wg, Wu, xd, N, K, M, rows, nrows, y, g, u, Sg, Su, nthreads);
+    free(xd);
+    return rc;
+}
+
+/* oracle_swiglu_rows with fp32 activations x[M][K]. */
+int oracle_swiglu_rows_f32(int fmt, const uint8_t *Wg, const uint8_t *Wu, const float *x,
+                           int64_t N, int64_t K, int64_t M, const int64_t *rows, int64_t nrows,
+                           double *y, double *g, double *u, double *Sg, double *Su, int nthreads)
+{
+    if (oracle_block_bytes(fmt) < 0 || K % 32 != 0 || N < 0 || M < 0) return -1;
+    if (rows == NULL) nrows = N;
+    double *xd = widen_float(x, M * K);
+    if (!xd) return -2;
+    int rc = swiglu_rows_xd(fmt, Wg, Wu, xd, N, K, M, rows, nrows, y, g, u, Sg, Su, nthreads);
+    free(xd);
+    return rc;
 }
 
 int oracle_max_threads(void)

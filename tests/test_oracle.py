@@ -297,3 +297,47 @@ def test_swiglu_tolerance_helper(orc):
     g3 = ref["g"] + 10 * H.TOL * ref["Sg"]
     y3 = g3 / (1 + np.exp(-g3)) * ref["u"]
     assert H.swiglu_normalised_error(y3, ref) > H.TOL
+
+
+# -- fp32 activations (values enter exactly; no narrowing to fp16) ---------------------
+
+def test_f32_equals_f16_on_half_values(orc):
+    # every fp16 value is an fp32 value: both entry points must give the same doubles
+    for fmt, name in ((0, "q4_0"), (1, "q8_0")):
+        W, x = _rand(name, 9, 768, 3, 11 + fmt)
+        y16, S16 = orc.qmv(fmt, W, x, 9, 768)
+        y32, S32 = orc.qmv(fmt, W, x.astype(np.float32), 9, 768)
+        assert np.array_equal(y16, y32) and np.array_equal(S16, S32)
+        r16, S16r = orc.qmv_rows(fmt, W, x, 9, 768, [8, 0, 3])
+        r32, S32r = orc.qmv_rows(fmt, W, x.astype(np.float32), 9, 768, [8, 0, 3])
+        assert np.array_equal(r16, r32) and np.array_equal(S16r, S32r)
+    Wg, x = _rand("q4_0", 5, 512, 2, 21)
+    Wu = synth.q4_0_weights(5, 512, 22)
+    a, b = orc.swiglu(0, Wg, Wu, x, 5, 512), orc.swiglu(0, Wg, Wu, x.astype(np.float32), 5, 512)
+    assert all(np.array_equal(a[k], b[k]) for k in a)
+
+
+@pytest.mark.parametrize("xv,scale", [
+    (1.0 + 2.0 ** -20, 1.0),            # fp32-exact, rounds to 1.0 in fp16
+    (11184811 / 2.0 ** 25, 1.0),        # the fp32 nearest to 1/3 (fp16's is 0.333251953125)
+    (1.0e6, 2.0 ** -10),                # far outside fp16's range
+    (2.0 ** -130, 1.0),                 # an fp32 subnormal (zero in fp16)
+])
+def test_f32_activations_enter_exactly(orc, xv, scale):
+    # Q8_0 row of K weights all equal to q * d = 3 * scale: y = 3 * scale * K * xv exactly
+    K = 64
+    d_bits = np.float16(scale).view(np.uint16)
+    W = H.encode_q8_0(np.full((1, K), 3, dtype=np.int64), np.full((1, K // 32), d_bits, dtype=np.uint16))
+    x = np.full((1, K), xv, dtype=np.float32)
+    assert float(x[0, 0]) == xv
+    y, S = orc.qmv(1, W, x, 1, K)
+    assert y[0, 0] == 3.0 * scale * K * xv and S[0, 0] == abs(y[0, 0])
+
+
+def test_f32_swiglu_closed_form(orc):
+    # gate w = 1/32 and up w = 2/32 against 32 activations of 1 + 2^-20 (fp32-exact)
+    e = 1.0 + 2.0 ** -20
+    x = np.full((1, 32), e, dtype=np.float32)
+    r = orc.swiglu(0, _uniform_table(9, 0x2800), _uniform_table(10, 0x2800), x, 1, 32)
+    assert r["g"][0, 0] == e and r["u"][0, 0] == 2.0 * e
+    assert r["y"][0, 0] == pytest.approx(_silu(e) * 2.0 * e, rel=1e-15)

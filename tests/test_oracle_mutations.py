@@ -59,7 +59,12 @@ MUTANTS = [
     ("sigmoid_without_gate", "y[i] = gate / (1.0 + exp(-gate)) * u[i];", "y[i] = 1.0 / (1.0 + exp(-gate)) * u[i];", 0),
     ("gate_and_up_swapped", "const double gate = g[i];\n        y[i] = gate / (1.0 + exp(-gate)) * u[i];",
      "const double gate = u[i];\n        y[i] = gate / (1.0 + exp(-gate)) * g[i];", 0),
-    ("up_table_is_gate", "rc = oracle_qmv_rows(fmt, Wu, x,", "rc = oracle_qmv_rows(fmt, Wg, x,", 0),
+    ("up_table_is_gate", "rc = qmv_rows_xd(fmt, Wu, xd,", "rc = qmv_rows_xd(fmt, Wg, xd,", 0),
+    ("f32_narrowed_to_half", "xd[i] = (double)x[i];", "xd[i] = (double)(_Float16)x[i];", 0),
+    ("f32_read_as_half", "double *xd = widen_float(x, M * K);",
+     "double *xd = widen_half((const uint16_t *)x, M * K);", 0),
+    ("f32_swiglu_read_as_half", "double *xd = widen_float(x, M * K);",
+     "double *xd = widen_half((const uint16_t *)x, M * K);", 1),
 ]
 
 
