@@ -60,6 +60,13 @@ WORKLOADS = {
     # each) and Qwen3-1.7B (6144x2048 each, the fused MLP table the bakeoff times
     # -- volta-kernel-bakeoff, "A few tokens at once"), one token and eight.
     "q4_0_swiglu": {"kind": "swiglu", "fmt": "q4_0", "M": [1, 8], "shapes": [(14336, 4096), (6144, 2048)]},
+    # fp32 activations in, narrowed to fp16 inside the kernel (the bakeoff's
+    # like-for-like fp32in comparison: its six one-token tables -- volta-kernel-
+    # bakeoff, "Results (one token, microseconds, lower is better)" -- at one
+    # token and eight; and Qwen3-1.7B's fused gate + up + SwiGLU).
+    "q4_0_f32in": {"kind": "gemv", "fmt": "q4_0", "x": "f32", "M": [1, 8],
+                   "shapes": [(12288, 2560), (8192, 2048), (6144, 2048), (640, 2560), (512, 2048), (2048, 512)]},
+    "q4_0_swiglu_f32in": {"kind": "swiglu", "fmt": "q4_0", "x": "f32", "M": [1, 8], "shapes": [(6144, 2048)]},
     # Prompt (prefill) on the tensor cores.
     "prefill": {"kind": "prefill", "fmt": "q4_0", "M": [64, 512], "shapes": [(12288, 2560), (8192, 2048)]},
 }
@@ -71,9 +78,11 @@ def metric_name(workload):
         return "Q4_0 prefill GEMM TFLOP/s (fp16 tensor cores; us/call per table in 'sweep')"
     if wl["kind"] == "moe":
         return "Q4_0 multi-expert GEMV (one launch) HBM GB/s (algorithmic bytes; us/call per config in 'sweep')"
+    xin = " (fp32 activations in)" if wl.get("x") == "f32" else ""
     if wl["kind"] == "swiglu":
-        return "Q4_0 fused gate+up+SwiGLU HBM GB/s (algorithmic bytes of both tables; us/call per table in 'sweep')"
-    return f"{wl['fmt'].upper()} GEMV HBM GB/s (algorithmic bytes; us/call per table in 'sweep')"
+        return (f"Q4_0 fused gate+up+SwiGLU{xin} HBM GB/s (algorithmic bytes of both tables; "
+                "us/call per table in 'sweep')")
+    return f"{wl['fmt'].upper()} GEMV{xin} HBM GB/s (algorithmic bytes; us/call per table in 'sweep')"
 
 
 # ---------------------------------------------------------------------------------
@@ -87,14 +96,20 @@ def peaks():
             "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-def algo_bytes(fmt, N, K, M):
+def algo_bytes(fmt, N, K, M, x_bytes=2):
+    """The table once, the activations once (x_bytes each), y once."""
     bb = 18 if fmt == "q4_0" else 34
-    return N * (K // 32) * bb + 2 * M * K + 4 * M * N
+    return N * (K // 32) * bb + x_bytes * M * K + 4 * M * N
 
 
-def algo_bytes_swiglu(N, K, M):
+def algo_bytes_swiglu(N, K, M, x_bytes=2):
     """Both Q4_0 tables once, the activations once, y once."""
-    return 2 * N * (K // 32) * 18 + 2 * M * K + 4 * M * N
+    return 2 * N * (K // 32) * 18 + x_bytes * M * K + 4 * M * N
+
+
+def x_dtype(wl):
+    """(numpy dtype, bytes) of a workload's activations."""
+    return (np.float32, 4) if wl.get("x") == "f32" else (np.float16, 2)
 
 
 class ClockSampler:
@@ -234,18 +249,21 @@ def run_ours(args, dist, rank, local, world):
     calls = []
     stream = torch.cuda.Stream(dev)
     sh = int(stream.cuda_stream)
+    xdt, xb = x_dtype(wl)
     if kind in ("gemv", "prefill"):
         fn_ptr = {"gemv": q.qmv_q4_0_ptr if fmt == "q4_0" else q.qmv_q8_0_ptr,
                   "prefill": q.qmm_q4_0_prefill_ptr}[kind]
+        if xb == 4:
+            fn_ptr = q.qmv_q4_0_f32_ptr
         for (N, K) in wl["shapes"]:
             Wd, copies = rotated_copies(N, K, f"{fmt}_{N}x{K}")
             for M in wl["M"]:
-                x = synth.activations(M, K, synth.seed_for(f"x_{K}_{M}"))
+                x = synth.activations(M, K, synth.seed_for(f"x_{K}_{M}"), dtype=xdt)
                 c = {"name": f"{N}x{K}/M{M}", "N": N, "K": K, "M": M, "W": Wd, "copies": copies,
                      "x": torch.from_numpy(x).to(dev), "y": torch.empty((M, N), dtype=torch.float32, device=dev),
                      "x_host": torch.from_numpy(x).pin_memory(),
                      "y_host": torch.empty((M, N), dtype=torch.float32).pin_memory(),
-                     "bytes": algo_bytes(fmt, N, K, M), "flops": 2 * M * N * K}
+                     "bytes": algo_bytes(fmt, N, K, M, xb), "flops": 2 * M * N * K}
 
                 def call(s, c=c):
                     W = c["W"][s % c["copies"]]
@@ -256,18 +274,19 @@ def run_ours(args, dist, rank, local, world):
         for (N, K) in wl["shapes"]:
             # gate rows 0..N-1 and up rows N..2N-1 of one rotated allocation
             Wd, copies = rotated_copies(2 * N, K, f"swiglu_{N}x{K}")
+            sw_ptr = q.qmv_q4_0_swiglu_f32_ptr if xb == 4 else q.qmv_q4_0_swiglu_ptr
             for M in wl["M"]:
-                x = synth.activations(M, K, synth.seed_for(f"x_{K}_{M}"))
+                x = synth.activations(M, K, synth.seed_for(f"x_{K}_{M}"), dtype=xdt)
                 c = {"name": f"{N}x{K}/M{M}", "N": N, "K": K, "M": M, "W": Wd, "copies": copies,
                      "x": torch.from_numpy(x).to(dev), "y": torch.empty((M, N), dtype=torch.float32, device=dev),
                      "x_host": torch.from_numpy(x).pin_memory(),
                      "y_host": torch.empty((M, N), dtype=torch.float32).pin_memory(),
-                     "bytes": algo_bytes_swiglu(N, K, M), "flops": 4 * M * N * K}
+                     "bytes": algo_bytes_swiglu(N, K, M, xb), "flops": 4 * M * N * K}
 
-                def call(s, c=c):
+                def call(s, c=c, sw_ptr=sw_ptr):
                     W = c["W"][s % c["copies"]]
-                    q.qmv_q4_0_swiglu_ptr(W[:c["N"]].data_ptr(), W[c["N"]:].data_ptr(), c["x"].data_ptr(),
-                                          c["y"].data_ptr(), c["N"], c["K"], c["M"], sh)
+                    sw_ptr(W[:c["N"]].data_ptr(), W[c["N"]:].data_ptr(), c["x"].data_ptr(),
+                           c["y"].data_ptr(), c["N"], c["K"], c["M"], sh)
                 c["call"] = call
                 calls.append(c)
     else:  # moe: a pool of experts, distinct indices drawn per step
@@ -421,7 +440,7 @@ def run_ours(args, dist, rank, local, world):
             stream.synchronize()
             wall = time.perf_counter() - t0
         e2e_ms = cross_rank_max_ms(dist, max(a.elapsed_time(b), wall * 1e3), dev)
-        h2d = sum(c["x_host"].numel() * 2 for c in calls)
+        h2d = sum(c["x_host"].numel() * c["x_host"].element_size() for c in calls)
         d2h = sum(c["y_host"].numel() * 4 for c in calls)
         e2e_val = whole_job_rate(step_flops / 1e12 if kind == "prefill" else step_bytes / 1e9, args.steps, world, e2e_ms)
         e2e = {"value": round(e2e_val, 3), "unit": "TFLOP/s" if kind == "prefill" else "GB/s",
@@ -488,13 +507,14 @@ def oracle_tasks(workload):
     fmt = wl["fmt"]
     fid = 0 if fmt == "q4_0" else 1
     bb = 18 if fmt == "q4_0" else 34
+    xdt, xb = x_dtype(wl)
     jobs = []
     if wl["kind"] == "swiglu":
         sjobs = []
         for (N, K) in wl["shapes"]:
             W2 = synth.weights(fmt, 2 * N, K, synth.seed_for(f"swiglu_{N}x{K}"))
             for M in wl["M"]:
-                x = synth.activations(M, K, synth.seed_for(f"x_{K}_{M}"))
+                x = synth.activations(M, K, synth.seed_for(f"x_{K}_{M}"), dtype=xdt)
                 sjobs.append((W2[:N], W2[N:], x, N, K, M))
 
         def run_swiglu(frac):
@@ -502,7 +522,7 @@ def oracle_tasks(workload):
             for (Wg, Wu, x, N, K, M) in sjobs:
                 rows = np.linspace(0, N - 1, max(1, int(N * frac))).astype(np.int64)
                 orc.swiglu(fid, Wg, Wu, x, N, K, rows=rows, nthreads=threads)
-                b += 2 * rows.size * (K // 32) * bb + 2 * M * K + 4 * M * rows.size
+                b += 2 * rows.size * (K // 32) * bb + xb * M * K + 4 * M * rows.size
                 f += 4 * M * rows.size * K
             return b, f
         return run_swiglu, threads, wl["kind"]
@@ -510,7 +530,7 @@ def oracle_tasks(workload):
         for (N, K) in wl["shapes"]:
             W = synth.weights(fmt, N, K, synth.seed_for(f"{fmt}_{N}x{K}"))
             for M in wl["M"]:
-                x = synth.activations(M, K, synth.seed_for(f"x_{K}_{M}"))
+                x = synth.activations(M, K, synth.seed_for(f"x_{K}_{M}"), dtype=xdt)
                 jobs.append((W, x, N, K, M))
     else:
         for (E, slots, N, K) in wl["configs"]:
@@ -526,7 +546,7 @@ def oracle_tasks(workload):
         for (W, x, N, K, M) in jobs:
             rows = np.linspace(0, N - 1, max(1, int(N * frac))).astype(np.int64)
             orc.qmv_rows(fid, W, x, N, K, rows, nthreads=threads)
-            b += rows.size * (K // 32) * bb + 2 * M * K + 4 * M * rows.size
+            b += rows.size * (K // 32) * bb + xb * M * K + 4 * M * rows.size
             f += 2 * M * rows.size * K
         return b, f
     return run, threads, wl["kind"]
@@ -601,10 +621,13 @@ def ncu_case(spec):
     """A handful of eager calls of one table over rotated copies larger than L2
     (a small, bounded program for an Nsight Compute capture).
     spec: q4_0:NxK:M | q8_0:NxK:M | prefill:NxK:M | moe:NxK:SLOTS (pool of 128) |
-    swiglu:NxK:M (gate and up tables of N rows each)."""
+    swiglu:NxK:M (gate and up tables of N rows each) | q4_0_f32:NxK:M | swiglu_f32:NxK:M
+    (fp32 activations)."""
     import torch
     import weight_quantized_decode_gb300 as q
     kind, shape, M = spec.split(":")
+    f32 = kind.endswith("_f32")
+    kind = kind[:-4] if f32 else kind
     N, K = (int(v) for v in shape.split("x"))
     M = int(M)
     dev = torch.device("cuda", 0)
@@ -615,7 +638,7 @@ def ncu_case(spec):
     copies = max(2, math.ceil(2.5 * 128e6 / wbytes))
     base = torch.from_numpy(synth.weights(fmt, rows, K, synth.seed_for(f"{fmt}_{rows}x{K}"))).to(dev)
     W = base.unsqueeze(0).repeat(copies, 1, 1)
-    x = torch.from_numpy(synth.activations(M, K, 1)).to(dev)
+    x = torch.from_numpy(synth.activations(M, K, 1, dtype=np.float32 if f32 else np.float16)).to(dev)
     y = torch.empty((M, N), dtype=torch.float32, device=dev)
     s = torch.cuda.current_stream().cuda_stream
     idx = torch.from_numpy(synth.expert_indices(8, M, 128, 3)).to(dev) if kind == "moe" else None
@@ -625,9 +648,11 @@ def ncu_case(spec):
             q.qmv_moe_ptr(Wi, idx[i].data_ptr(), 128, x.data_ptr(), y.data_ptr(), N, K, M, s)
         elif kind == "swiglu":
             Wc = W[i % copies]
-            q.qmv_q4_0_swiglu_ptr(Wc[:N].data_ptr(), Wc[N:].data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, s)
+            fn = q.qmv_q4_0_swiglu_f32_ptr if f32 else q.qmv_q4_0_swiglu_ptr
+            fn(Wc[:N].data_ptr(), Wc[N:].data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, s)
         else:
-            fn = {"q4_0": q.qmv_q4_0_ptr, "q8_0": q.qmv_q8_0_ptr, "prefill": q.qmm_q4_0_prefill_ptr}[kind]
+            fn = {"q4_0": q.qmv_q4_0_f32_ptr if f32 else q.qmv_q4_0_ptr, "q8_0": q.qmv_q8_0_ptr,
+                  "prefill": q.qmm_q4_0_prefill_ptr}[kind]
             fn(Wi, x.data_ptr(), y.data_ptr(), N, K, M, s)
     torch.cuda.synchronize()
     print(f"ncu case {spec}: {copies} copies, 8 calls, ok")

@@ -95,9 +95,9 @@ QMV_API qmv_status qmv_q4_0(const void *W, const void *x, float *y,
                     int64_t N, int64_t K, int64_t M, qmv_stream_t stream);
 
 /*
- * Q8_0 decode GEMV, same contract as qmv_q4_0 with 34-byte Q8_0 blocks
- * ("fused_q8: ours, int8 weights" -- volta-kernel-bakeoff, "What's in the
- * race"; k_q8_gemm -- H100-KERNEL-5X-ROADMAP, "Lever 1").
+ * Q8_0 decode GEMV, same contract as qmv_q4_0 with 34-byte Q8_0 blocks (the
+ * bakeoff's fused_q8 contender streams 8-bit weights -- volta-kernel-bakeoff,
+ * "What's in the race"; k_q8_gemm -- H100-KERNEL-5X-ROADMAP, "Lever 1").
  *   W : Q8_0 bytes [N][K/32*34], 16-byte aligned.  0 <= M <= 8.
  */
 QMV_API qmv_status qmv_q8_0(const void *W, const void *x, float *y,
@@ -146,6 +146,28 @@ QMV_API qmv_status qmv_moe(const void *W_pool, const int32_t *expert_idx, int64_
  */
 QMV_API qmv_status qmv_q4_0_swiglu(const void *W_gate, const void *W_up, const void *x, float *y,
                            int64_t N, int64_t K, int64_t M, qmv_stream_t stream);
+
+/*
+ * qmv_q4_0 and qmv_q4_0_swiglu with fp32 activations (the bakeoff's
+ * fused_q4_v3_fp32in takes fp32 in and counts the narrowing to fp16 in its
+ * time -- volta-kernel-bakeoff, "Results (one token, microseconds, lower is
+ * better)" and "A few tokens at once").  The narrowing happens inside the
+ * kernel, while each CTA stages the activations into shared memory, at every
+ * token count: no separate conversion launch and no fp16 copy in memory.
+ *   x : fp32 [M][K], 4-byte aligned (16-byte aligned with K % 256 == 0 for the
+ *       streaming kernel; otherwise the generic kernel runs).  Every value is
+ *       rounded to fp16 (nearest even) before the product, so the results
+ *       equal those of qmv_q4_0 / qmv_q4_0_swiglu on x rounded to fp16
+ *       (bit-identical: the same kernel runs after staging).  Values must lie
+ *       within fp16's range (|x| < 65520): larger ones round to +-inf.
+ *   W, W_gate, W_up, y, N, K, M, errors and asynchrony as for the fp16 calls.
+ * Accuracy against the exact product on the fp32 values: the bounds above,
+ * which also cover the rounding of x (at most 2^-11 of each |x w|).
+ */
+QMV_API qmv_status qmv_q4_0_f32(const void *W, const float *x, float *y,
+                        int64_t N, int64_t K, int64_t M, qmv_stream_t stream);
+QMV_API qmv_status qmv_q4_0_swiglu_f32(const void *W_gate, const void *W_up, const float *x, float *y,
+                               int64_t N, int64_t K, int64_t M, qmv_stream_t stream);
 
 /*
  * Q4_0 prefill GEMM for many tokens (M >= 1, intended for M >= 64).  Prior

@@ -31,7 +31,8 @@ def lib():
 
 def test_header_declares_the_boundary():
     names = set(_declared())
-    for n in ("qmv_q4_0", "qmv_q8_0", "qmv_moe", "qmm_q4_0_prefill", "qmv_device_status"):
+    for n in ("qmv_q4_0", "qmv_q8_0", "qmv_moe", "qmm_q4_0_prefill", "qmv_device_status", "qmv_q4_0_swiglu",
+              "qmv_q4_0_f32", "qmv_q4_0_swiglu_f32"):
         assert n in names
 
 
@@ -50,7 +51,7 @@ def test_version_and_status_strings(lib):
 FAKE = 1 << 20      # a 16-byte-aligned non-null address; never dereferenced here
 
 
-@pytest.mark.parametrize("fn", ["qmv_q4_0", "qmv_q8_0", "qmm_q4_0_prefill"])
+@pytest.mark.parametrize("fn", ["qmv_q4_0", "qmv_q8_0", "qmm_q4_0_prefill", "qmv_q4_0_f32"])
 def test_host_validation(lib, fn):
     f = getattr(lib, fn)
     assert f(None, FAKE, FAKE, 8, 256, 1, None) == 1          # NULL W
@@ -67,6 +68,26 @@ def test_host_validation(lib, fn):
     assert f(None, None, None, 8, 256, 0, None) == 0
     if fn != "qmm_q4_0_prefill":
         assert f(FAKE, FAKE, FAKE, 8, 256, 9, None) == 3      # decode takes M <= 8
+    if fn == "qmv_q4_0_f32":
+        assert f(FAKE, FAKE + 2, FAKE, 8, 256, 1, None) == 2  # fp32 x not 4-byte aligned
+
+
+@pytest.mark.parametrize("fn", ["qmv_q4_0_swiglu", "qmv_q4_0_swiglu_f32"])
+def test_host_validation_swiglu(lib, fn):
+    f = getattr(lib, fn)
+    assert f(None, FAKE, FAKE, FAKE, 8, 256, 1, None) == 1    # NULL gate table
+    assert f(FAKE, None, FAKE, FAKE, 8, 256, 1, None) == 1    # NULL up table
+    assert f(FAKE, FAKE, None, FAKE, 8, 256, 1, None) == 1    # NULL x
+    assert f(FAKE, FAKE, FAKE, None, 8, 256, 1, None) == 1    # NULL y
+    assert f(FAKE, FAKE + 8, FAKE, FAKE, 8, 256, 1, None) == 2  # up table misaligned
+    assert f(FAKE, FAKE, FAKE + 1, FAKE, 8, 256, 1, None) == 2  # x misaligned
+    assert f(FAKE, FAKE, FAKE, FAKE, 8, 256, 9, None) == 3    # M <= 8
+    assert f(FAKE, FAKE, FAKE, FAKE, 8, 250, 1, None) == 3    # K % 32
+    assert f(FAKE, FAKE, FAKE, FAKE, 1 << 40, 256, 1, None) == 3   # 2N rows overflow the row index range
+    assert f(None, None, None, None, 0, 256, 1, None) == 0    # empty
+    assert f(None, None, None, None, 8, 256, 0, None) == 0
+    if fn.endswith("_f32"):
+        assert f(FAKE, FAKE, FAKE + 2, FAKE, 8, 256, 1, None) == 2   # fp32 x not 4-byte aligned
 
 
 def test_host_validation_moe(lib):

@@ -80,6 +80,21 @@ def test_decode_tokens(orc, fmt, M):
     check(fmt, W, x, N, K, orc)
 
 
+# Shapes whose built-in launch rule takes a lane count that is not a power of
+# two (rows of 9..15 units at one or two tokens: one unit per lane) or more
+# lanes than the row has units (short tables at several tokens).
+RULE_SHAPES = [(37, 2304, 1), (300, 2816, 2), (200, 3072, 1), (64, 3328, 2), (129, 3584, 1), (41, 3840, 1),
+               (640, 2560, 8), (512, 2048, 8), (2048, 512, 8), (100, 2560, 5), (1000, 3584, 8), (96, 768, 3)]
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("N,K,M", RULE_SHAPES)
+def test_decode_rule_lane_counts(orc, fmt, N, K, M):
+    W = synth.weights(fmt, N, K, seed=N * 3 + K + M)
+    x = synth.activations(M, K, seed=N + 2 * K + M)
+    check(fmt, W, x, N, K, orc)
+
+
 @pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
 @pytest.mark.parametrize("plant", ["large", "tiny"])
 @pytest.mark.parametrize("M", [1, 8])

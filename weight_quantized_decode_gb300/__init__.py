@@ -9,6 +9,8 @@ raise if the library is missing or a tensor is not on a CUDA device.
 Functions (same names as the C ABI):
     qmv_q4_0(W, x, y=None, stream=None)          -> y fp32 [M, N]
     qmv_q8_0(W, x, y=None, stream=None)          -> y fp32 [M, N]
+    qmv_q4_0_swiglu(W_gate, W_up, x, y=None, stream=None) -> silu(gate) * up, fp32 [M, N]
+    qmv_q4_0_f32, qmv_q4_0_swiglu_f32            -> the same two with fp32 x
     qmv_moe(W_pool, expert_idx, n_experts, x, N, y=None, stream=None)
     qmm_q4_0_prefill(W, x, y=None, stream=None)  -> y fp32 [M, N]
     qmv_device_status(stream=None)               -> int (QMV_DEV_* bits, cleared)
@@ -51,7 +53,7 @@ def lib():
                                "(there is no CPU fallback)")
         L = ctypes.CDLL(LIB_PATH)
         vp, i64 = ctypes.c_void_p, ctypes.c_int64
-        for name in ("qmv_q4_0", "qmv_q8_0", "qmm_q4_0_prefill"):
+        for name in ("qmv_q4_0", "qmv_q8_0", "qmm_q4_0_prefill", "qmv_q4_0_f32"):
             f = getattr(L, name)
             f.restype = ctypes.c_int
             f.argtypes = [vp, vp, vp, i64, i64, i64, vp]
@@ -59,6 +61,8 @@ def lib():
         L.qmv_moe.argtypes = [vp, vp, i64, vp, vp, i64, i64, i64, vp]
         L.qmv_q4_0_swiglu.restype = ctypes.c_int
         L.qmv_q4_0_swiglu.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
+        L.qmv_q4_0_swiglu_f32.restype = ctypes.c_int
+        L.qmv_q4_0_swiglu_f32.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
         L.qmv_device_status.restype = ctypes.c_int
         L.qmv_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
         L.qmv_set_pdl.restype = None
@@ -99,6 +103,15 @@ def qmv_q4_0_ptr(W: int, x: int, y: int, N: int, K: int, M: int, stream: int = 0
     _check("qmv_q4_0", lib().qmv_q4_0(W, x, y, N, K, M, stream))
 
 
+def qmv_q4_0_f32_ptr(W: int, x: int, y: int, N: int, K: int, M: int, stream: int = 0) -> None:
+    _check("qmv_q4_0_f32", lib().qmv_q4_0_f32(W, x, y, N, K, M, stream))
+
+
+def qmv_q4_0_swiglu_f32_ptr(W_gate: int, W_up: int, x: int, y: int, N: int, K: int, M: int,
+                            stream: int = 0) -> None:
+    _check("qmv_q4_0_swiglu_f32", lib().qmv_q4_0_swiglu_f32(W_gate, W_up, x, y, N, K, M, stream))
+
+
 def qmv_q8_0_ptr(W: int, x: int, y: int, N: int, K: int, M: int, stream: int = 0) -> None:
     _check("qmv_q8_0", lib().qmv_q8_0(W, x, y, N, K, M, stream))
 
@@ -126,14 +139,15 @@ def _stream_handle(stream):
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def _prep(W, x, y, block_bytes, fn):
+def _prep(W, x, y, block_bytes, fn, x_dtype=None):
     torch = _torch()
+    x_dtype = torch.float16 if x_dtype is None else x_dtype
     if not (W.is_cuda and x.is_cuda):
         raise TypeError(f"{fn}: W and x must be CUDA tensors (no CPU path)")
     if W.dtype != torch.uint8:
         raise TypeError(f"{fn}: W must be uint8 GGUF bytes")
-    if x.dtype != torch.float16:
-        raise TypeError(f"{fn}: x must be float16")
+    if x.dtype != x_dtype:
+        raise TypeError(f"{fn}: x must be {str(x_dtype).replace('torch.', '')}")
     if x.dim() == 1:
         x = x.unsqueeze(0)
     if not (W.is_contiguous() and x.is_contiguous()):
@@ -162,16 +176,36 @@ def qmv_q4_0(W, x, y=None, stream=None):
     return y
 
 
+def qmv_q4_0_f32(W, x, y=None, stream=None):
+    """qmv_q4_0 with float32 activations, rounded to fp16 inside the kernel."""
+    W, x, y, N, K, M = _prep(W, x, y, Q4_0_BLOCK_BYTES, "qmv_q4_0_f32", _torch().float32)
+    qmv_q4_0_f32_ptr(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, _stream_handle(stream))
+    return y
+
+
+def _check_up(W_gate, W_up, fn):
+    torch = _torch()
+    if not (W_up.is_cuda and W_up.dtype == torch.uint8 and W_up.is_contiguous()
+            and W_up.numel() == W_gate.numel()):
+        raise ValueError(f"{fn}: W_up must be a contiguous CUDA uint8 table shaped like W_gate")
+
+
 def qmv_q4_0_swiglu(W_gate, W_up, x, y=None, stream=None):
     """y[M, N] = silu(x @ dequant(W_gate)^T) * (x @ dequant(W_up)^T) for two
     Q4_0 tables of N rows each (the MLP's gate + up + SwiGLU in one call)."""
     W_gate, x, y, N, K, M = _prep(W_gate, x, y, Q4_0_BLOCK_BYTES, "qmv_q4_0_swiglu")
-    torch = _torch()
-    if not (W_up.is_cuda and W_up.dtype == torch.uint8 and W_up.is_contiguous()
-            and W_up.numel() == W_gate.numel()):
-        raise ValueError("qmv_q4_0_swiglu: W_up must be a contiguous CUDA uint8 table shaped like W_gate")
+    _check_up(W_gate, W_up, "qmv_q4_0_swiglu")
     qmv_q4_0_swiglu_ptr(W_gate.data_ptr(), W_up.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M,
                         _stream_handle(stream))
+    return y
+
+
+def qmv_q4_0_swiglu_f32(W_gate, W_up, x, y=None, stream=None):
+    """qmv_q4_0_swiglu with float32 activations, rounded to fp16 inside the kernel."""
+    W_gate, x, y, N, K, M = _prep(W_gate, x, y, Q4_0_BLOCK_BYTES, "qmv_q4_0_swiglu_f32", _torch().float32)
+    _check_up(W_gate, W_up, "qmv_q4_0_swiglu_f32")
+    qmv_q4_0_swiglu_f32_ptr(W_gate.data_ptr(), W_up.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M,
+                            _stream_handle(stream))
     return y
 
 

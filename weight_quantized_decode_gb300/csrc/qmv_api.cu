@@ -60,22 +60,31 @@ cudaError_t device_info(int dev, int **status, int *sms, int *smem_optin)
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-int lanes_per_row(int U, int M)
+int lanes_per_row(int U, int M, int64_t N, int sms)
 {
-    // G lanes share a row, each taking every G-th 256-weight unit.  Prefer a G
-    // that divides the row (no idle lanes); for rows of 8 or more units that no
-    // power of two of at least 8 divides (e.g. K = 2560: 10 units) take 8 and
-    // accept a partly idle last stage -- short rows otherwise leave most warps
-    // without work.  Capped for several tokens so the G distinct activation
-    // units a warp reads at once stay cheap.
-    const int cap = (M <= 2) ? 16 : 8;
+    // G lanes share a row, each taking every G-th 256-weight unit.
+    if (M <= 2) {
+        // One or two tokens: bound by the weight stream.  Rows of 9..15 units
+        // get one unit per lane (e.g. K = 2560: G = 10, three rows per warp).
+        if (U > 8 && U <= 16 && U % 8 != 0) return U;
+        // Otherwise the largest power of two up to 16 that divides the row, at
+        // least 8 for rows of 8 or more units (short rows otherwise leave most
+        // warps without work), never more lanes than units.
+        int G = 1;
+        while (G * 2 <= 16 && U % (G * 2) == 0) G *= 2;
+        if (G < 8 && U >= 8) G = 8;
+        while (G > 1 && G > U) G >>= 1;
+        return G;
+    }
+    // Several tokens: bound by arithmetic per row, so rows are spread over as
+    // few lanes as still give every SM about four row groups (measured on
+    // Q4_0 tables of 512..28672 rows at 8 tokens), at most 16 lanes and no more
+    // than the smallest power of two that covers the row.
     int G = 1;
-    while (G * 2 <= cap && U % (G * 2) == 0) G *= 2;
-    // For several tokens the kernel is bound by arithmetic, and idle lanes cost
-    // more than the lost parallelism.
-    if (G < 8 && U >= 8 && M <= 2) G = 8;
-    while (G > 1 && G > U) G >>= 1;
-    return G;
+    while (G < 16 && N * G < int64_t(4) * 32 * (sms > 0 ? sms : 1)) G *= 2;
+    int cover = 1;
+    while (cover < U) cover *= 2;
+    return G < cover ? G : cover;
 }
 
 struct Plan {
@@ -138,7 +147,9 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
 {
     Plan pl{false, 0, 8, 0};
     if (p.K % 256 != 0 || p.K == 0) return pl;
-    if (reinterpret_cast<uintptr_t>(p.x) % 16 != 0) return pl;   // staged with 4-byte loads of 16-byte-aligned rows
+    // staged with 4-byte (fp16 pairs) or 8-byte (fp32 pairs) loads of 16-byte-aligned rows
+    const uintptr_t xaddr = p.xf ? reinterpret_cast<uintptr_t>(p.xf) : reinterpret_cast<uintptr_t>(p.x);
+    if (xaddr % 16 != 0) return pl;
     if (p.rows_total >= (int64_t(1) << 31)) return pl;             // 32-bit row indices
     const int64_t U = p.K / 256;
     if (U > (1 << 20)) return pl;
@@ -154,7 +165,7 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
     // defaults by rule
     const int64_t wbytes_per_sm = Nplan * (p.K / 256) * unit_bytes / (sms > 0 ? sms : 1);
     const bool big = wbytes_per_sm > 128 * 1024 && M <= 2;
-    int G = lanes_per_row(p.U, M);
+    int G = lanes_per_row(p.U, M, Nplan, sms);
     int warps = big ? 12 : 8;
     int stages = 2;
     int SP = 1;
@@ -233,8 +244,10 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
 }
 
 qmv_status run_gemv(int fmt, const void *W, const int32_t *idx, int64_t n_experts, const void *x, float *y,
-                    int64_t N, int64_t K, int64_t M, int n_problems, cudaStream_t stream, const void *W2 = nullptr)
+                    int64_t N, int64_t K, int64_t M, int n_problems, cudaStream_t stream, const void *W2 = nullptr,
+                    const float *xf = nullptr)
 {
+    if (xf && fmt != kQ4_0) return QMV_ERR_SHAPE;   // fp32 activations: Q4_0 kernels only
     int dev = 0;
     if (current_device(&dev) != cudaSuccess) return QMV_ERR_CUDA;
     int *status = nullptr;
@@ -244,6 +257,7 @@ qmv_status run_gemv(int fmt, const void *W, const int32_t *idx, int64_t n_expert
     GemvParams p = {};
     p.W = static_cast<const uint8_t *>(W);
     p.x = static_cast<const __half *>(x);
+    p.xf = xf;
     p.y = y;
     p.expert_idx = idx;
     p.N = N;
@@ -262,8 +276,11 @@ qmv_status run_gemv(int fmt, const void *W, const int32_t *idx, int64_t n_expert
     cudaError_t e;
     Plan pl = plan_gemv(fmt, p, Mk, sms, optin);
     if (pl.streaming) {
-        e = (fmt == kQ4_0) ? launch_gemv_stream_q4_0(Mk, p, pl.grid, pl.warps, pl.smem, stream, pdl)
-                           : launch_gemv_stream_q8_0(Mk, p, pl.grid, pl.warps, pl.smem, stream, pdl);
+        if (fmt == kQ4_0)
+            e = xf ? launch_gemv_stream_q4_0_f32(Mk, p, pl.grid, pl.warps, pl.smem, stream, pdl)
+                   : launch_gemv_stream_q4_0(Mk, p, pl.grid, pl.warps, pl.smem, stream, pdl);
+        else
+            e = launch_gemv_stream_q8_0(Mk, p, pl.grid, pl.warps, pl.smem, stream, pdl);
     } else {
         const int64_t warps_needed = W2 ? N : p.rows_total;
         int64_t grid = (warps_needed + 7) / 8;
@@ -358,6 +375,29 @@ qmv_status qmv_q4_0_swiglu(const void *W_gate, const void *W_up, const void *x, 
     if (N > (int64_t(1) << 39)) return QMV_ERR_SHAPE;     // 2N interleaved rows
     // K == 0 (W_up may then be null): y = silu(0) * 0 = 0, as the plain call gives.
     return run_gemv(kQ4_0, W_gate, nullptr, 1, x, y, N, K, M, 1, reinterpret_cast<cudaStream_t>(stream), W_up);
+}
+
+qmv_status qmv_q4_0_f32(const void *W, const float *x, float *y, int64_t N, int64_t K, int64_t M,
+                        qmv_stream_t stream)
+{
+    qmv_status st = check_common(W, x, y, N, K, M, 8);
+    if (st != QMV_OK || N == 0 || M == 0) return st;
+    if (x && !aligned(x, 4)) return QMV_ERR_ALIGN;
+    return run_gemv(kQ4_0, W, nullptr, 1, nullptr, y, N, K, M, 1, reinterpret_cast<cudaStream_t>(stream), nullptr,
+                    x);
+}
+
+qmv_status qmv_q4_0_swiglu_f32(const void *W_gate, const void *W_up, const float *x, float *y, int64_t N,
+                               int64_t K, int64_t M, qmv_stream_t stream)
+{
+    qmv_status st = check_common(W_gate, x, y, N, K, M, 8);
+    if (st != QMV_OK || N == 0 || M == 0) return st;
+    if (x && !aligned(x, 4)) return QMV_ERR_ALIGN;
+    if (K > 0 && !W_up) return QMV_ERR_NULL;
+    if (W_up && !aligned(W_up, 16)) return QMV_ERR_ALIGN;
+    if (N > (int64_t(1) << 39)) return QMV_ERR_SHAPE;     // 2N interleaved rows
+    return run_gemv(kQ4_0, W_gate, nullptr, 1, nullptr, y, N, K, M, 1, reinterpret_cast<cudaStream_t>(stream),
+                    W_up, x);
 }
 
 qmv_status qmv_moe(const void *W_pool, const int32_t *expert_idx, int64_t n_experts, const void *x, float *y,

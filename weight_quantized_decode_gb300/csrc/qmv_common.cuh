@@ -173,6 +173,14 @@ __device__ __forceinline__ __half2 as_h2(uint32_t u)
     return *reinterpret_cast<__half2 *>(&u);
 }
 
+// Two fp32 values rounded to fp16 (nearest even) as one half2 word: .x in
+// the low half, as two consecutive fp16 activations sit in memory.
+__device__ __forceinline__ uint32_t float2_to_half2_bits(float2 v)
+{
+    const __half2 h = __float22half2_rn(v);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
 __device__ __forceinline__ float half_lo_to_float(uint32_t u)
 {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(u & 0xffffu)));

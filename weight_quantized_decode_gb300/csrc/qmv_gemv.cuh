@@ -66,7 +66,8 @@ constexpr int kXUnitBytes = 528;   // 512 bytes of permuted activations + 16 byt
 struct GemvParams {
     const uint8_t *W;            // weights; for the multi-expert call, the expert pool; fused SwiGLU: gate
     const uint8_t *W2;           // fused SwiGLU: the up table (else nullptr)
-    const __half *x;             // [n_problems * M][K]
+    const __half *x;             // [n_problems * M][K] fp16 activations
+    const float *xf;             // fp32 activations of the same shape (XF32 kernels; x is then unused)
     float *y;                    // [n_problems * M][N]
     const int32_t *expert_idx;   // multi-expert call only (else nullptr)
     int64_t N;                   // rows per problem
@@ -294,7 +295,12 @@ __device__ __forceinline__ bool stage_wait(uint64_t *bar, uint32_t parity, int *
 // stacked table -- volta-kernel-bakeoff, "A few tokens at once"), a CTA owns
 // whole pairs, and y[m][n] = silu(g) * u is formed in the epilogue, so only
 // the activated result reaches memory (SovereignKernel diary, phase 6).
-template <int FMT, int M, int MAXT, bool MOE, bool SWIGLU = false>
+// XF32 = the activations arrive as fp32 (p.xf) and are rounded to fp16 while
+// they are staged, so the product that follows is the fp16 one (the bakeoff's
+// fp32in kernels convert inside the kernel for the same reason: a separate
+// conversion pass costs a launch -- volta-kernel-bakeoff, "Results (one token,
+// microseconds, lower is better)").
+template <int FMT, int M, int MAXT, bool MOE, bool SWIGLU = false, bool XF32 = false>
 __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p)
 {
     using T = FmtTraits<FMT>;
@@ -430,6 +436,7 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
         bool first = true;
         for (int it0 = 0; it0 < items || first; it0 += round) {
             uint32_t a[kStageItems][4];
+            float2 af[XF32 ? kStageItems : 1][4];    // fp32 pairs, rounded when stored
             int cidx[kStageItems], tidx[kStageItems];
 #pragma unroll
             for (int b = 0; b < kStageItems; ++b) {
@@ -460,13 +467,23 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
                         if (blk & 1) { i4 = 4 * w1; i6 = 4 * w1 + 2; }
                         else { i4 = 4 * w1 - 2; i6 = 4 * w1; }
                     }
-                    const uint32_t *xb =
-                        reinterpret_cast<const uint32_t *>(p.x + (static_cast<int64_t>(prob_lo) * M + tok) * p.K) +
-                        blk * 16;     // 32 halves = 16 words per block
-                    a[b][0] = __ldg(xb + (i0 >> 1));
-                    a[b][1] = __ldg(xb + (i2 >> 1));
-                    a[b][2] = __ldg(xb + (i4 >> 1));
-                    a[b][3] = __ldg(xb + (i6 >> 1));
+                    const int64_t xoff = (static_cast<int64_t>(prob_lo) * M + tok) * p.K;
+                    if constexpr (XF32) {
+                        // one 8-byte load per pair; all loads of the round are
+                        // issued before any of them is rounded to a half2 word
+                        const float2 *xb = reinterpret_cast<const float2 *>(p.xf + xoff) + blk * 16;
+                        af[b][0] = __ldg(xb + (i0 >> 1));
+                        af[b][1] = __ldg(xb + (i2 >> 1));
+                        af[b][2] = __ldg(xb + (i4 >> 1));
+                        af[b][3] = __ldg(xb + (i6 >> 1));
+                    } else {
+                        const uint32_t *xb = reinterpret_cast<const uint32_t *>(p.x + xoff) +
+                                             blk * 16;     // 32 halves = 16 words per block
+                        a[b][0] = __ldg(xb + (i0 >> 1));
+                        a[b][1] = __ldg(xb + (i2 >> 1));
+                        a[b][2] = __ldg(xb + (i4 >> 1));
+                        a[b][3] = __ldg(xb + (i6 >> 1));
+                    }
                 }
             }
 #pragma unroll
@@ -488,6 +505,10 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
                     const int c = cidx[b];
                     const int blk = c >> 2, sub = c & 3;
                     uint8_t *xd = xs + static_cast<size_t>(tidx[b]) * U * kXUnitBytes;
+                    if constexpr (XF32) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) a[b][k] = float2_to_half2_bits(af[b][k]);
+                    }
                     // pairs (first of each, first of each) and (second, second)
                     const uint4 v = make_uint4(__byte_perm(a[b][0], a[b][1], 0x5410), __byte_perm(a[b][0], a[b][1], 0x7632),
                                                __byte_perm(a[b][2], a[b][3], 0x5410), __byte_perm(a[b][2], a[b][3], 0x7632));
@@ -624,6 +645,13 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
 
 // ---- the generic kernel (any K % 32 == 0, any M, activations from global) ----------
 
+// Activation i as the product sees it: fp16, or fp32 rounded to fp16 (nearest
+// even) exactly as the streaming kernel stages it.
+__device__ __forceinline__ float load_x(const GemvParams &p, int64_t i)
+{
+    return p.xf ? __half2float(__float2half_rn(p.xf[i])) : __half2float(p.x[i]);
+}
+
 template <int FMT>
 __global__ void __launch_bounds__(256) gemv_generic_kernel(const GemvParams p, int M)
 {
@@ -671,7 +699,7 @@ __global__ void __launch_bounds__(256) gemv_generic_kernel(const GemvParams p, i
 #pragma unroll
                             for (int mm = 0; mm < 8; ++mm) {
                                 if (m0 + mm < M)
-                                    acc[mm] = fmaf(wv, __half2float(p.x[(prob * M + m0 + mm) * p.K + b * 32 + j]), acc[mm]);
+                                    acc[mm] = fmaf(wv, load_x(p, (prob * M + m0 + mm) * p.K + b * 32 + j), acc[mm]);
                             }
                         }
                     }

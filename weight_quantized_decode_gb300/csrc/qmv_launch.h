@@ -12,6 +12,9 @@ struct GemvParams;
 // Streaming decode kernel for one format and token count M (1..8).
 cudaError_t launch_gemv_stream_q4_0(int M, const GemvParams &p, int grid, int warps, size_t smem,
                                     cudaStream_t s, bool pdl);
+// Q4_0 with fp32 activations (plain and fused SwiGLU forms; p.xf set).
+cudaError_t launch_gemv_stream_q4_0_f32(int M, const GemvParams &p, int grid, int warps, size_t smem,
+                                        cudaStream_t s, bool pdl);
 cudaError_t launch_gemv_stream_q8_0(int M, const GemvParams &p, int grid, int warps, size_t smem,
                                     cudaStream_t s, bool pdl);
 // Generic kernel (any K % 32 == 0, activations read from global memory).

@@ -8,7 +8,7 @@ Value distributions (the configurations the library is measured on):
   * Q4_0: codes uniform in 0..15 (every qs byte uniform in 0..255), per-32
     fp16 scale d uniform in [0.005, 0.02];
   * Q8_0: int8 codes uniform in -127..127, per-32 fp16 scale in [0.001, 0.01];
-  * activations: fp16 N(0, 1); optional plants of large values
+  * activations: fp16 (or fp32) N(0, 1); optional plants of large values
     (+-20000..60000 in ~1 % of entries, like real down_proj inputs) or of tiny
     ones (~1e-4), as in volta-kernel-bakeoff, "A few tokens at once".
 """
@@ -70,8 +70,9 @@ def weights(fmt: str, N: int, K: int, seed: int) -> np.ndarray:
     raise ValueError(fmt)
 
 
-def activations(M: int, K: int, seed: int, plant: str | None = None) -> np.ndarray:
-    """fp16 activations [M, K], N(0,1), with optional 'large' or 'tiny' plants."""
+def activations(M: int, K: int, seed: int, plant: str | None = None, dtype=np.float16) -> np.ndarray:
+    """Activations [M, K], N(0,1), with optional 'large' or 'tiny' plants; fp16
+    by default, or the same draws rounded to fp32 (dtype=np.float32)."""
     rng = np.random.Generator(np.random.PCG64(seed ^ 0x5A5A5A5A))
     x = rng.standard_normal((M, K))
     if plant == "large":
@@ -83,7 +84,7 @@ def activations(M: int, K: int, seed: int, plant: str | None = None) -> np.ndarr
         x = x * 1e-4
     elif plant is not None:
         raise ValueError(plant)
-    return x.astype(np.float16)
+    return x.astype(dtype)
 
 
 def expert_indices(n_calls: int, n_slots: int, n_experts: int, seed: int) -> np.ndarray:
