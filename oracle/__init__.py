@@ -8,6 +8,7 @@ and its citations.
 from .oracle import (  # noqa: F401
     FMT_Q4_0,
     FMT_Q8_0,
+    FMT_Q2W,
     block_bytes,
     build,
     dequant_row,

@@ -15,6 +15,7 @@ import numpy as np
 
 FMT_Q4_0 = 0
 FMT_Q8_0 = 1
+FMT_Q2W = 2
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "qmv_oracle.c")

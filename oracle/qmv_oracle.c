@@ -26,6 +26,14 @@
  *     qs[j], element j>=16 is the high nibble of qs[j-16]; w = (c - 8) * d.
  *   Q8_0 block, 34 bytes, 32 weights:  bytes 0..1 = fp16 d, bytes 2..33 =
  *     int8 codes q[0..31]; w = q * d.
+ *   Plain 2-bit ("q2w": codes -2..1, one fp16 scale per 32 weights, 2.5 bits
+ *     per weight -- volta-kernel-bakeoff, "What's in the race", q2w_alu_v3),
+ *     10 bytes, 32 weights: bytes 0..1 = fp16 d, bytes 2..9 = qs[0..7].  The
+ *     pages fix the codes and the scale but not the bit order; it is read the
+ *     way Q4_0 splits a byte (elements j and j+16), one step further: element
+ *     j is bits 2*(j/8)..2*(j/8)+1 of qs[j % 8], an unsigned c in 0..3, so
+ *     byte i holds elements i, i+8, i+16, i+24 from its low bits up; and
+ *     w = (c - 2) * d.
  *   A row of W holds K/32 consecutive blocks; rows are dense (no padding).
  *   x is fp16 (IEEE binary16 bit patterns), row-major [M][K]; the _f32 entry
  *   points take fp32 activations instead (the bakeoff's fused_q4_v3_fp32in
@@ -50,6 +58,7 @@
 
 #define ORACLE_FMT_Q4_0 0
 #define ORACLE_FMT_Q8_0 1
+#define ORACLE_FMT_Q2W 2
 
 /* IEEE 754 binary16 -> double, written out from the format's definition:
  * 1 sign bit, 5 exponent bits (bias 15), 10 mantissa bits; exponent 0 is
@@ -74,6 +83,7 @@ int64_t oracle_block_bytes(int fmt)
 {
     if (fmt == ORACLE_FMT_Q4_0) return 18;
     if (fmt == ORACLE_FMT_Q8_0) return 34;
+    if (fmt == ORACLE_FMT_Q2W) return 10;
     return -1;
 }
 
@@ -88,6 +98,18 @@ static void dequant_block_q4_0(const uint8_t *blk, double *w)
         int hi = qs[j] >> 4;
         w[j] = (double)(lo - 8) * d;
         w[j + 16] = (double)(hi - 8) * d;
+    }
+}
+
+/* Dequantise one plain 2-bit block of 32 weights into w[0..31]. */
+static void dequant_block_q2w(const uint8_t *blk, double *w)
+{
+    uint16_t dbits = (uint16_t)(blk[0] | (blk[1] << 8));
+    double d = oracle_half_to_double(dbits);
+    const uint8_t *qs = blk + 2;
+    for (int j = 0; j < 32; ++j) {
+        int c = (qs[j % 8] >> (2 * (j / 8))) & 3;
+        w[j] = (double)(c - 2) * d;
     }
 }
 
@@ -112,8 +134,10 @@ int oracle_dequant_row(int fmt, const uint8_t *W, int64_t n, int64_t K, double *
     for (int64_t b = 0; b < nblk; ++b) {
         if (fmt == ORACLE_FMT_Q4_0)
             dequant_block_q4_0(row + b * bb, w + 32 * b);
-        else
+        else if (fmt == ORACLE_FMT_Q8_0)
             dequant_block_q8_0(row + b * bb, w + 32 * b);
+        else
+            dequant_block_q2w(row + b * bb, w + 32 * b);
     }
     return 0;
 }

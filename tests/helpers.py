@@ -7,8 +7,8 @@ import os
 import numpy as np
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
-FMT = {"q4_0": 0, "q8_0": 1}
-BLOCK_BYTES = {"q4_0": 18, "q8_0": 34}
+FMT = {"q4_0": 0, "q8_0": 1, "q2w": 2}
+BLOCK_BYTES = {"q4_0": 18, "q8_0": 34, "q2w": 10}
 TOL = 2e-3  # max |y - y_ref| / (S + 1e-6) per output
 
 
@@ -144,12 +144,26 @@ def encode_q8_0(codes, d_bits):
     return out.reshape(N, nb * 34)
 
 
+def encode_q2w(codes, d_bits):
+    """codes: int array [N, K] in 0..3 (w = (c - 2) d); d_bits: uint16 [N, K/32]
+    -> bytes (element j in bits 2*(j//8) of byte j % 8 of its block)."""
+    N, K = codes.shape
+    nb = K // 32
+    c = codes.reshape(N, nb, 4, 8).astype(np.uint8)      # [.., plane, byte]
+    out = np.empty((N, nb, 10), dtype=np.uint8)
+    out[:, :, 0] = d_bits & 0xFF
+    out[:, :, 1] = d_bits >> 8
+    out[:, :, 2:10] = c[:, :, 0] | (c[:, :, 1] << 2) | (c[:, :, 2] << 4) | (c[:, :, 3] << 6)
+    return out.reshape(N, nb * 10)
+
+
 def sabotage(W, fmt):
-    """XOR 0x88 into every code byte (scales untouched): each Q4_0 code moves by
-    8 in its top bit, i.e. every weight moves by +-8d (after volta-kernel-bakeoff,
-    'Making it fair': BAKEOFF_SABOTAGE breaks the packed weights)."""
+    """Flip code bits in every code byte (scales untouched), after
+    volta-kernel-bakeoff, 'Making it fair' (its sabotage switch breaks the
+    packed weights): XOR 0x88 moves each Q4_0 code by 8 in its top bit (every
+    weight by +-8d); for the 2-bit format XOR 0xAA moves every code by 2."""
     bb = BLOCK_BYTES[fmt]
     W = np.array(W, dtype=np.uint8, copy=True)
     v = W.reshape(W.shape[0], -1, bb)
-    v[:, :, 2:] ^= 0x88
+    v[:, :, 2:] ^= 0xAA if fmt == "q2w" else 0x88
     return W

@@ -28,7 +28,8 @@ def test_half_decode_exhaustive(orc):
 
 # -- hand-computed cases -----------------------------------------------------
 
-@pytest.mark.parametrize("case", H.load_cases("oracle_cases.txt"), ids=lambda c: c["name"])
+@pytest.mark.parametrize("case", H.load_cases("oracle_cases.txt") + H.load_cases("q2w_cases.txt"),
+                         ids=lambda c: c["name"])
 def test_golden_cases(orc, case):
     y, S = orc.qmv(H.FMT[case["fmt"]], case["W"], case["xarr"], case["N"], case["K"])
     for (m, n), v in case["y"].items():
@@ -137,6 +138,43 @@ def test_linear_in_x(orc):
     assert np.max(np.abs(y12 - (y1 + y2)) / (S + 1e-30)) < 1e-12
 
 
+def test_q2w_integer_case_matches_numpy(orc):
+    rng = np.random.default_rng(71)
+    N, K, M = 6, 256, 3
+    codes = rng.integers(0, 4, size=(N, K))
+    d_bits = np.full((N, K // 32), 0x3C00, dtype=np.uint16)          # d = 1
+    W = H.encode_q2w(codes, d_bits)
+    x = rng.integers(-50, 51, size=(M, K)).astype(np.float16)
+    y, S = orc.qmv(2, W, x, N, K)
+    Wi = (codes - 2).astype(np.float64)
+    xf = x.astype(np.float64)
+    assert np.array_equal(y, xf @ Wi.T)
+    assert np.array_equal(S, np.abs(xf) @ np.abs(Wi).T)
+
+
+def test_q2w_to_q4_reencoding_identical(orc):
+    # a 2-bit code c2 is the Q4_0 code c2 + 6: same weight (c2 - 2) d, same scale
+    N, K = 5, 512
+    W2 = synth.q2w_weights(N, K, 72)
+    x = synth.activations(3, K, 73)
+    v = W2.reshape(N, K // 32, 10)
+    planes = [(v[:, :, 2:10] >> (2 * p)) & 3 for p in range(4)]          # [N, nb, 8] each
+    codes = np.concatenate(planes, axis=2).reshape(N, K).astype(np.int64)  # element j = plane j//8, byte j%8
+    d_bits = v[:, :, 0:2].copy().view(np.uint16).reshape(N, K // 32)
+    W4 = H.encode_q4_0(codes + 6, d_bits)
+    y2, S2 = orc.qmv(2, W2, x, N, K)
+    y4, S4 = orc.qmv(0, W4, x, N, K)
+    assert np.array_equal(y2, y4) and np.array_equal(S2, S4)
+    assert np.array_equal(H.encode_q2w(codes, d_bits), W2)         # the encoder is the format's inverse
+
+
+def test_q2w_all_code2_gives_zero(orc):
+    N, K = 4, 256
+    W = H.encode_q2w(np.full((N, K), 2), np.full((N, K // 32), 0x3C00, dtype=np.uint16))
+    y, S = orc.qmv(2, W, synth.activations(2, K, 74), N, K)
+    assert np.all(y == 0) and np.all(S == 0)
+
+
 def test_q4_to_q8_reencoding_identical(orc):
     N, K = 5, 256
     W4, x = _rand("q4_0", N, K, 2, 4)
@@ -195,7 +233,7 @@ def test_empty_shapes(orc):
 
 # -- sabotage: corrupting the packed bytes must fail every check ----------------
 
-@pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0", "q2w"])
 def test_sabotage_fails_the_check(orc, fmt):
     """A check is the max error over a product's outputs.  Sabotage moves each
     weight by +-8d (Q4_0) or more (Q8_0): the expected normalised error is

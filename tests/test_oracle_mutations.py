@@ -60,6 +60,14 @@ MUTANTS = [
     ("gate_and_up_swapped", "const double gate = g[i];\n        y[i] = gate / (1.0 + exp(-gate)) * u[i];",
      "const double gate = u[i];\n        y[i] = gate / (1.0 + exp(-gate)) * g[i];", 0),
     ("up_table_is_gate", "rc = qmv_rows_xd(fmt, Wu, xd,", "rc = qmv_rows_xd(fmt, Wg, xd,", 0),
+    ("q2w_sequential_order", "int c = (qs[j % 8] >> (2 * (j / 8))) & 3;",
+     "int c = (qs[j / 4] >> (2 * (j % 4))) & 3;", 0),
+    ("q2w_planes_reversed", "int c = (qs[j % 8] >> (2 * (j / 8))) & 3;",
+     "int c = (qs[j % 8] >> (6 - 2 * (j / 8))) & 3;", 0),
+    ("q2w_bias_dropped", "w[j] = (double)(c - 2) * d;", "w[j] = (double)(c) * d;", 0),
+    ("q2w_bias_off_by_one", "w[j] = (double)(c - 2) * d;", "w[j] = (double)(c - 1) * d;", 0),
+    ("q2w_scale_dropped", "w[j] = (double)(c - 2) * d;", "w[j] = (double)(c - 2);", 0),
+    ("q2w_block_bytes", "if (fmt == ORACLE_FMT_Q2W) return 10;", "if (fmt == ORACLE_FMT_Q2W) return 8;", 0),
     ("f32_narrowed_to_half", "xd[i] = (double)x[i];", "xd[i] = (double)(_Float16)x[i];", 0),
     ("f32_read_as_half", "double *xd = widen_float(x, M * K);",
      "double *xd = widen_half((const uint16_t *)x, M * K);", 0),

@@ -8,6 +8,8 @@ Value distributions (the configurations the library is measured on):
   * Q4_0: codes uniform in 0..15 (every qs byte uniform in 0..255), per-32
     fp16 scale d uniform in [0.005, 0.02];
   * Q8_0: int8 codes uniform in -127..127, per-32 fp16 scale in [0.001, 0.01];
+  * plain 2-bit: codes uniform in 0..3 (every code byte uniform), per-32 fp16
+    scale in [0.01, 0.04];
   * activations: fp16 (or fp32) N(0, 1); optional plants of large values
     (+-20000..60000 in ~1 % of entries, like real down_proj inputs) or of tiny
     ones (~1e-4), as in volta-kernel-bakeoff, "A few tokens at once".
@@ -20,8 +22,9 @@ import numpy as np
 
 Q4_0 = "q4_0"
 Q8_0 = "q8_0"
+Q2W = "q2w"
 BLOCK = 32
-BLOCK_BYTES = {Q4_0: 18, Q8_0: 34}
+BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q2W: 10}
 
 
 def seed_for(name: str, copy: int = 0) -> int:
@@ -62,11 +65,26 @@ def q8_0_weights(N: int, K: int, seed: int, d_lo: float = 0.001, d_hi: float = 0
     return blocks.reshape(N, nb * 34)
 
 
+def q2w_weights(N: int, K: int, seed: int, d_lo: float = 0.01, d_hi: float = 0.04) -> np.ndarray:
+    """Plain 2-bit bytes (fp16 d, then 8 code bytes per 32 weights) for an N x K
+    matrix: uint8 array [N, K/32*10]."""
+    assert K % BLOCK == 0
+    rng = np.random.Generator(np.random.PCG64(seed))
+    nb = K // BLOCK
+    blocks = np.empty((N, nb, 10), dtype=np.uint8)
+    d = _scales(rng, (N, nb), d_lo, d_hi)
+    blocks[:, :, 0:2] = d.view(np.uint8).reshape(N, nb, 2)
+    blocks[:, :, 2:10] = rng.integers(0, 256, size=(N, nb, 8), dtype=np.uint8)
+    return blocks.reshape(N, nb * 10)
+
+
 def weights(fmt: str, N: int, K: int, seed: int) -> np.ndarray:
     if fmt == Q4_0:
         return q4_0_weights(N, K, seed)
     if fmt == Q8_0:
         return q8_0_weights(N, K, seed)
+    if fmt == Q2W:
+        return q2w_weights(N, K, seed)
     raise ValueError(fmt)
 
 
