@@ -39,6 +39,8 @@ sys.path.insert(0, ROOT)
 
 from weight_quantized_decode_gb300 import synth  # noqa: E402
 
+BLOCK_BYTES = {"q4_0": 18, "q8_0": 34, "q2w": 10}
+FMT_ID = {"q4_0": 0, "q8_0": 1, "q2w": 2}
 SPEC_HBM_GBS = 8000.0        # nominal HBM3e figure the target is quoted against
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -67,6 +69,11 @@ WORKLOADS = {
     "q4_0_f32in": {"kind": "gemv", "fmt": "q4_0", "x": "f32", "M": [1, 8],
                    "shapes": [(12288, 2560), (8192, 2048), (6144, 2048), (640, 2560), (512, 2048), (2048, 512)]},
     "q4_0_swiglu_f32in": {"kind": "swiglu", "fmt": "q4_0", "x": "f32", "M": [1, 8], "shapes": [(6144, 2048)]},
+    # Plain 2-bit (codes -2..1, fp16 scale per 32): the bakeoff's six one-token
+    # tables (volta-kernel-bakeoff, "Results (one token, microseconds, lower is
+    # better)", its 2-bit column).
+    "q2w": {"kind": "gemv", "fmt": "q2w", "M": [1],
+            "shapes": [(12288, 2560), (8192, 2048), (6144, 2048), (640, 2560), (512, 2048), (2048, 512)]},
     # Prompt (prefill) on the tensor cores.
     "prefill": {"kind": "prefill", "fmt": "q4_0", "M": [64, 512], "shapes": [(12288, 2560), (8192, 2048)]},
 }
@@ -98,7 +105,7 @@ def peaks():
 
 def algo_bytes(fmt, N, K, M, x_bytes=2):
     """The table once, the activations once (x_bytes each), y once."""
-    bb = 18 if fmt == "q4_0" else 34
+    bb = BLOCK_BYTES[fmt]
     return N * (K // 32) * bb + x_bytes * M * K + 4 * M * N
 
 
@@ -227,7 +234,7 @@ def run_ours(args, dist, rank, local, world):
     kind, fmt = wl["kind"], wl["fmt"]
     prop = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(prop, "L2_cache_size", 128 * 1024 * 1024) or 128 * 1024 * 1024)
-    bb = 18 if fmt == "q4_0" else 34
+    bb = BLOCK_BYTES[fmt]
 
     def rotated_copies(rows, K, seed_name):
         """A power of two of weight copies, >= 4x L2 in total, each with distinct
@@ -251,7 +258,7 @@ def run_ours(args, dist, rank, local, world):
     sh = int(stream.cuda_stream)
     xdt, xb = x_dtype(wl)
     if kind in ("gemv", "prefill"):
-        fn_ptr = {"gemv": q.qmv_q4_0_ptr if fmt == "q4_0" else q.qmv_q8_0_ptr,
+        fn_ptr = {"gemv": {"q4_0": q.qmv_q4_0_ptr, "q8_0": q.qmv_q8_0_ptr, "q2w": q.qmv_q2w_ptr}[fmt],
                   "prefill": q.qmm_q4_0_prefill_ptr}[kind]
         if xb == 4:
             fn_ptr = q.qmv_q4_0_f32_ptr
@@ -505,8 +512,8 @@ def oracle_tasks(workload):
     threads = os.cpu_count() or 1
     wl = WORKLOADS[workload]
     fmt = wl["fmt"]
-    fid = 0 if fmt == "q4_0" else 1
-    bb = 18 if fmt == "q4_0" else 34
+    fid = FMT_ID[fmt]
+    bb = BLOCK_BYTES[fmt]
     xdt, xb = x_dtype(wl)
     jobs = []
     if wl["kind"] == "swiglu":
@@ -622,7 +629,7 @@ def ncu_case(spec):
     (a small, bounded program for an Nsight Compute capture).
     spec: q4_0:NxK:M | q8_0:NxK:M | prefill:NxK:M | moe:NxK:SLOTS (pool of 128) |
     swiglu:NxK:M (gate and up tables of N rows each) | q4_0_f32:NxK:M | swiglu_f32:NxK:M
-    (fp32 activations)."""
+    (fp32 activations) | q2w:NxK:M (plain 2-bit)."""
     import torch
     import weight_quantized_decode_gb300 as q
     kind, shape, M = spec.split(":")
@@ -631,8 +638,8 @@ def ncu_case(spec):
     N, K = (int(v) for v in shape.split("x"))
     M = int(M)
     dev = torch.device("cuda", 0)
-    fmt = "q8_0" if kind == "q8_0" else "q4_0"
-    bb = 18 if fmt == "q4_0" else 34
+    fmt = kind if kind in ("q8_0", "q2w") else "q4_0"
+    bb = BLOCK_BYTES[fmt]
     rows = 128 * N if kind == "moe" else (2 * N if kind == "swiglu" else N)
     wbytes = rows * (K // 32) * bb
     copies = max(2, math.ceil(2.5 * 128e6 / wbytes))
@@ -652,7 +659,7 @@ def ncu_case(spec):
             fn(Wc[:N].data_ptr(), Wc[N:].data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, s)
         else:
             fn = {"q4_0": q.qmv_q4_0_f32_ptr if f32 else q.qmv_q4_0_ptr, "q8_0": q.qmv_q8_0_ptr,
-                  "prefill": q.qmm_q4_0_prefill_ptr}[kind]
+                  "q2w": q.qmv_q2w_ptr, "prefill": q.qmm_q4_0_prefill_ptr}[kind]
             fn(Wi, x.data_ptr(), y.data_ptr(), N, K, M, s)
     torch.cuda.synchronize()
     print(f"ncu case {spec}: {copies} copies, 8 calls, ok")

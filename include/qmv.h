@@ -104,6 +104,22 @@ QMV_API qmv_status qmv_q8_0(const void *W, const void *x, float *y,
                     int64_t N, int64_t K, int64_t M, qmv_stream_t stream);
 
 /*
+ * Plain 2-bit decode GEMV (the bakeoff's q2w format: codes -2..1 with one fp16
+ * scale per 32 weights, 2.5 bits per weight -- volta-kernel-bakeoff, "What's
+ * in the race" and the Results table's 2-bit column), same contract as
+ * qmv_q4_0 with 10-byte blocks:
+ *   W : [N][K/32*10] bytes, 16-byte aligned; a block is fp16 d (little
+ *       endian) then qs[0..7]; element j of the block is bits 2*(j/8) and
+ *       2*(j/8)+1 of qs[j % 8], an unsigned c in 0..3, and w = (c - 2) * d.
+ *       (The pages leave the bit order open; this is Q4_0's split of a byte
+ *       into elements j and j+16 carried one step further.)
+ *   0 <= M <= 8; K % 256 == 0 takes the streaming kernel, other K the
+ *   generic one.
+ */
+QMV_API qmv_status qmv_q2w(const void *W, const void *x, float *y,
+                   int64_t N, int64_t K, int64_t M, qmv_stream_t stream);
+
+/*
  * Several experts, each with its own token, in ONE launch (the bakeoff's moe_*
  * contenders run 8 to 10 experts this way -- volta-kernel-bakeoff, "What's in
  * the race"; every expert gets distinct weights and its own token, so that a

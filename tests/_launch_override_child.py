@@ -37,7 +37,7 @@ def main():
         elif kind == "gemv":
             W = synth.weights(fmt, N, K, synth.seed_for(f"ovr_{fmt}_{N}x{K}"))
             x = synth.activations(M, K, synth.seed_for(f"ovr_x_{K}_{M}"))
-            fn = q.qmv_q4_0 if fmt == "q4_0" else q.qmv_q8_0
+            fn = {"q4_0": q.qmv_q4_0, "q8_0": q.qmv_q8_0, "q2w": q.qmv_q2w}[fmt]
             y = fn(dev(W), dev(x))
             torch.cuda.synchronize()
             res[case] = y.cpu().numpy()

@@ -32,7 +32,7 @@ def lib():
 def test_header_declares_the_boundary():
     names = set(_declared())
     for n in ("qmv_q4_0", "qmv_q8_0", "qmv_moe", "qmm_q4_0_prefill", "qmv_device_status", "qmv_q4_0_swiglu",
-              "qmv_q4_0_f32", "qmv_q4_0_swiglu_f32"):
+              "qmv_q4_0_f32", "qmv_q4_0_swiglu_f32", "qmv_q2w"):
         assert n in names
 
 
@@ -51,7 +51,7 @@ def test_version_and_status_strings(lib):
 FAKE = 1 << 20      # a 16-byte-aligned non-null address; never dereferenced here
 
 
-@pytest.mark.parametrize("fn", ["qmv_q4_0", "qmv_q8_0", "qmm_q4_0_prefill", "qmv_q4_0_f32"])
+@pytest.mark.parametrize("fn", ["qmv_q4_0", "qmv_q8_0", "qmm_q4_0_prefill", "qmv_q4_0_f32", "qmv_q2w"])
 def test_host_validation(lib, fn):
     f = getattr(lib, fn)
     assert f(None, FAKE, FAKE, 8, 256, 1, None) == 1          # NULL W

@@ -39,7 +39,7 @@ def dev(a):
 
 def gpu_call(fmt, W, x):
     import weight_quantized_decode_gb300 as q
-    fn = q.qmv_q4_0 if fmt == "q4_0" else q.qmv_q8_0
+    fn = {"q4_0": q.qmv_q4_0, "q8_0": q.qmv_q8_0, "q2w": q.qmv_q2w}[fmt]
     y = fn(dev(W), dev(x))
     torch.cuda.synchronize()
     return y.cpu().numpy().astype(np.float64)
@@ -63,7 +63,7 @@ SHAPES = [(1, 256), (7, 512), (33, 768), (1000, 2048), (333, 4096), (4133, 1024)
           (77, 6144)]
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0", "q2w"])
 @pytest.mark.parametrize("N,K", SHAPES)
 def test_decode_m1(orc, fmt, N, K):
     W = synth.weights(fmt, N, K, seed=N * 7 + K)
@@ -71,7 +71,7 @@ def test_decode_m1(orc, fmt, N, K):
     check(fmt, W, x, N, K, orc)
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0", "q2w"])
 @pytest.mark.parametrize("M", [2, 3, 4, 5, 6, 7, 8])
 def test_decode_tokens(orc, fmt, M):
     N, K = 515, 2560
@@ -87,7 +87,7 @@ RULE_SHAPES = [(37, 2304, 1), (300, 2816, 2), (200, 3072, 1), (64, 3328, 2), (12
                (640, 2560, 8), (512, 2048, 8), (2048, 512, 8), (100, 2560, 5), (1000, 3584, 8), (96, 768, 3)]
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0", "q2w"])
 @pytest.mark.parametrize("N,K,M", RULE_SHAPES)
 def test_decode_rule_lane_counts(orc, fmt, N, K, M):
     W = synth.weights(fmt, N, K, seed=N * 3 + K + M)
@@ -95,7 +95,7 @@ def test_decode_rule_lane_counts(orc, fmt, N, K, M):
     check(fmt, W, x, N, K, orc)
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0", "q2w"])
 @pytest.mark.parametrize("plant", ["large", "tiny"])
 @pytest.mark.parametrize("M", [1, 8])
 def test_planted_activations(orc, fmt, plant, M):
@@ -106,7 +106,7 @@ def test_planted_activations(orc, fmt, plant, M):
     assert np.all(np.isfinite(y))
 
 
-@pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0", "q2w"])
 @pytest.mark.parametrize("K", [32, 96, 640, 1056])
 def test_generic_kernel_k_not_multiple_of_256(orc, fmt, K):
     N, M = 45, 3
@@ -217,6 +217,17 @@ def test_full_size_q8_0(orc, N, K, M):
     W = synth.q8_0_weights(N, K, synth.seed_for(f"q8_0_{N}x{K}"))
     x = synth.activations(M, K, synth.seed_for(f"x_{K}_{M}"))
     check("q8_0", W, x, N, K, orc, rows=_sample_rows(N))
+
+
+# The bakeoff's six one-token tables in the plain 2-bit format, plus a large
+# one, at one and eight tokens (sampled rows).
+@pytest.mark.parametrize("N,K", [(12288, 2560), (8192, 2048), (6144, 2048), (640, 2560), (512, 2048), (2048, 512),
+                                 (128256, 4096)])
+@pytest.mark.parametrize("M", [1, 8])
+def test_full_size_q2w(orc, N, K, M):
+    W = synth.q2w_weights(N, K, synth.seed_for(f"q2w_{N}x{K}"))
+    x = synth.activations(M, K, synth.seed_for(f"x_{K}_{M}"))
+    check("q2w", W, x, N, K, orc, rows=_sample_rows(N))
 
 
 # -- fused gate + up + SwiGLU -----------------------------------------------------------
@@ -355,13 +366,13 @@ OVERRIDES = {
     # from 1 to 32 (also ones that do not divide 32), odd passes per stage, deep
     # rings, two CTAs per SM; the multi-expert form must still equal the single
     # calls bit for bit.
-    "G=4,SP=3": ["gemv:q4_0:77:6144:1", "gemv:q8_0:130:2560:2", "moe:q4_0:64:2560:5"],
+    "G=4,SP=3": ["gemv:q4_0:77:6144:1", "gemv:q8_0:130:2560:2", "moe:q4_0:64:2560:5", "gemv:q2w:77:6144:3"],
     "G=32,warps=4": ["gemv:q4_0:40:8192:1", "gemv:q8_0:130:2560:4", "moe:q4_0:96:4096:6"],
-    "G=1,SP=5,stages=3": ["gemv:q4_0:16:14336:1", "gemv:q4_0:33:2048:3", "moe:q4_0:20:2048:3"],
-    "warps=16,stages=4,G=2": ["gemv:q4_0:100:4096:2", "gemv:q8_0:9:3072:1"],
+    "G=1,SP=5,stages=3": ["gemv:q4_0:16:14336:1", "gemv:q4_0:33:2048:3", "moe:q4_0:20:2048:3", "gemv:q2w:16:14336:1"],
+    "warps=16,stages=4,G=2": ["gemv:q4_0:100:4096:2", "gemv:q8_0:9:3072:1", "gemv:q2w:100:4096:1"],
     "ctas=2,share=2": ["gemv:q4_0:1000:4096:1", "gemv:q8_0:600:2048:1", "moe:q4_0:33:1024:7"],
     # lanes per row that do not divide 32 (idle lanes, lane-order reduction)
-    "G=10": ["gemv:q4_0:130:2560:1", "gemv:q8_0:77:2560:2", "moe:q4_0:64:2560:5"],
+    "G=10": ["gemv:q4_0:130:2560:1", "gemv:q8_0:77:2560:2", "moe:q4_0:64:2560:5", "gemv:q2w:130:2560:2"],
     "G=3,SP=3": ["gemv:q4_0:41:2304:1", "gemv:q8_0:50:1536:4", "moe:q4_0:20:2304:3"],
     "G=12,warps=16": ["gemv:q4_0:90:3072:2", "gemv:q8_0:33:6144:1", "swiglu:q4_0:90:3072:2"],
     # the fused SwiGLU keeps an even number of rows per group (G clamped to <= 16)
@@ -475,7 +486,7 @@ def test_prefill_in_graph_on_a_new_stream(cuda_lib, orc):
 
 # -- sabotage: corrupted packed bytes must fail every check ----------------------------
 
-@pytest.mark.parametrize("fmt", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0", "q2w"])
 def test_sabotage_fails(orc, fmt):
     N, K = 512, 2048
     W = synth.weights(fmt, N, K, 60)

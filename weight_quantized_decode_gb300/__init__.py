@@ -11,6 +11,7 @@ Functions (same names as the C ABI):
     qmv_q8_0(W, x, y=None, stream=None)          -> y fp32 [M, N]
     qmv_q4_0_swiglu(W_gate, W_up, x, y=None, stream=None) -> silu(gate) * up, fp32 [M, N]
     qmv_q4_0_f32, qmv_q4_0_swiglu_f32            -> the same two with fp32 x
+    qmv_q2w(W, x, y=None, stream=None)           -> plain 2-bit weights, y fp32 [M, N]
     qmv_moe(W_pool, expert_idx, n_experts, x, N, y=None, stream=None)
     qmm_q4_0_prefill(W, x, y=None, stream=None)  -> y fp32 [M, N]
     qmv_device_status(stream=None)               -> int (QMV_DEV_* bits, cleared)
@@ -31,6 +32,7 @@ QMV_DEV_BAD_EXPERT = 0x1
 QMV_DEV_TIMEOUT = 0x2
 Q4_0_BLOCK_BYTES = 18
 Q8_0_BLOCK_BYTES = 34
+Q2W_BLOCK_BYTES = 10
 
 _lock = threading.Lock()
 _lib = None
@@ -53,7 +55,7 @@ def lib():
                                "(there is no CPU fallback)")
         L = ctypes.CDLL(LIB_PATH)
         vp, i64 = ctypes.c_void_p, ctypes.c_int64
-        for name in ("qmv_q4_0", "qmv_q8_0", "qmm_q4_0_prefill", "qmv_q4_0_f32"):
+        for name in ("qmv_q4_0", "qmv_q8_0", "qmm_q4_0_prefill", "qmv_q4_0_f32", "qmv_q2w"):
             f = getattr(L, name)
             f.restype = ctypes.c_int
             f.argtypes = [vp, vp, vp, i64, i64, i64, vp]
@@ -114,6 +116,10 @@ def qmv_q4_0_swiglu_f32_ptr(W_gate: int, W_up: int, x: int, y: int, N: int, K: i
 
 def qmv_q8_0_ptr(W: int, x: int, y: int, N: int, K: int, M: int, stream: int = 0) -> None:
     _check("qmv_q8_0", lib().qmv_q8_0(W, x, y, N, K, M, stream))
+
+
+def qmv_q2w_ptr(W: int, x: int, y: int, N: int, K: int, M: int, stream: int = 0) -> None:
+    _check("qmv_q2w", lib().qmv_q2w(W, x, y, N, K, M, stream))
 
 
 def qmv_moe_ptr(W_pool: int, idx: int, n_experts: int, x: int, y: int, N: int, K: int, M: int,
@@ -213,6 +219,13 @@ def qmv_q8_0(W, x, y=None, stream=None):
     """y[M, N] = x[M, K] @ dequant(W)^T for Q8_0 weights."""
     W, x, y, N, K, M = _prep(W, x, y, Q8_0_BLOCK_BYTES, "qmv_q8_0")
     qmv_q8_0_ptr(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, _stream_handle(stream))
+    return y
+
+
+def qmv_q2w(W, x, y=None, stream=None):
+    """y[M, N] = x[M, K] @ dequant(W)^T for plain 2-bit weights (10-byte blocks)."""
+    W, x, y, N, K, M = _prep(W, x, y, Q2W_BLOCK_BYTES, "qmv_q2w")
+    qmv_q2w_ptr(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, _stream_handle(stream))
     return y
 
 

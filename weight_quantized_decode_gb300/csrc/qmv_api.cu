@@ -154,7 +154,7 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
     const int64_t U = p.K / 256;
     if (U > (1 << 20)) return pl;
     p.U = static_cast<int>(U);
-    const int unit_bytes = fmt == kQ4_0 ? 144 : 272;
+    const int unit_bytes = fmt == kQ4_0 ? 144 : (fmt == kQ2W ? 80 : 272);
     const Tune &tu = tune_overrides();
     // One problem (a plain call, or the fused SwiGLU's gate and up tables
     // stacked row by row) is planned as one table of rows_total rows; the
@@ -263,7 +263,7 @@ qmv_status run_gemv(int fmt, const void *W, const int32_t *idx, int64_t n_expert
     p.N = N;
     p.K = K;
     p.n_experts = n_experts;
-    p.row_bytes = (K / 32) * (fmt == kQ4_0 ? 18 : 34);
+    p.row_bytes = (K / 32) * (fmt == kQ4_0 ? 18 : (fmt == kQ2W ? 10 : 34));
     p.n_problems = n_problems;
     p.max_local_problems = n_problems;
     p.rows_total = N * n_problems;
@@ -279,6 +279,8 @@ qmv_status run_gemv(int fmt, const void *W, const int32_t *idx, int64_t n_expert
         if (fmt == kQ4_0)
             e = xf ? launch_gemv_stream_q4_0_f32(Mk, p, pl.grid, pl.warps, pl.smem, stream, pdl)
                    : launch_gemv_stream_q4_0(Mk, p, pl.grid, pl.warps, pl.smem, stream, pdl);
+        else if (fmt == kQ2W)
+            e = launch_gemv_stream_q2w(Mk, p, pl.grid, pl.warps, pl.smem, stream, pdl);
         else
             e = launch_gemv_stream_q8_0(Mk, p, pl.grid, pl.warps, pl.smem, stream, pdl);
     } else {
@@ -342,6 +344,7 @@ cudaError_t ensure_smem_optin(const void *func, size_t smem)
 cudaError_t launch_gemv_generic(int fmt, const GemvParams &p, int M, int grid, cudaStream_t s, bool pdl)
 {
     if (fmt == kQ4_0) return launch_ex(gemv_generic_kernel<kQ4_0>, dim3(grid), dim3(256), 0, s, pdl, p, M);
+    if (fmt == kQ2W) return launch_ex(gemv_generic_kernel<kQ2W>, dim3(grid), dim3(256), 0, s, pdl, p, M);
     return launch_ex(gemv_generic_kernel<kQ8_0>, dim3(grid), dim3(256), 0, s, pdl, p, M);
 }
 
@@ -363,6 +366,13 @@ qmv_status qmv_q8_0(const void *W, const void *x, float *y, int64_t N, int64_t K
     qmv_status st = check_common(W, x, y, N, K, M, 8);
     if (st != QMV_OK || N == 0 || M == 0) return st;
     return run_gemv(kQ8_0, W, nullptr, 1, x, y, N, K, M, 1, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qmv_status qmv_q2w(const void *W, const void *x, float *y, int64_t N, int64_t K, int64_t M, qmv_stream_t stream)
+{
+    qmv_status st = check_common(W, x, y, N, K, M, 8);
+    if (st != QMV_OK || N == 0 || M == 0) return st;
+    return run_gemv(kQ2W, W, nullptr, 1, x, y, N, K, M, 1, reinterpret_cast<cudaStream_t>(stream));
 }
 
 qmv_status qmv_q4_0_swiglu(const void *W_gate, const void *W_up, const void *x, float *y, int64_t N, int64_t K,

@@ -206,6 +206,7 @@ __device__ __forceinline__ float half_hi_to_float(uint32_t u)
 // at the end.
 constexpr float kQ4Prescale = 32.0f;
 constexpr float kQ8Prescale = 512.0f;
+constexpr float kQ2Prescale = 32.0f;
 
 // Q4_0: one 32-bit word of qs holding bytes (b0, b1, b2, b3) -> four half2
 // weights:  w[0] = (lo b0, lo b2)   w[1] = (lo b1, lo b3)
@@ -244,6 +245,29 @@ __device__ __forceinline__ void unpack_q8_word(uint32_t v, __half2 (&w)[2])
     const __half2 b = __halves2half2(__ushort_as_half(0xC080), __ushort_as_half(0xC080));  // -2.25
     w[0] = __hfma2(as_h2(h02), s, b);
     w[1] = __hfma2(as_h2(h13), s, b);
+}
+
+// Plain 2-bit: one 32-bit word of code bytes (b0, b1, b2, b3), each holding
+// four codes c in 0..3 at bits 0-1, 2-3, 4-5, 6-7 (planes 0..3) -> eight half2
+// weights (c - 2) / 32:
+//   w[2p] = (plane p of b0, plane p of b2)   w[2p+1] = (plane p of b1, plane p of b3)
+// Plane p lands in the mantissa as c * 4^p: 0x6400 | (c << 2p) is the half
+// 1024 + c * 4^p, and (1024 + c * 4^p) * 2^-(2p+5) - (2^(5-2p) + 1/16) =
+// (c - 2) / 32, a value fp16 holds exactly, so one HFMA2 per pair is exact.
+__device__ __forceinline__ void unpack_q2_word(uint32_t v, __half2 (&w)[8])
+{
+    const uint32_t magic = 0x64006400u;
+    const uint32_t v8 = v >> 8;
+    constexpr unsigned short kScale[4] = {0x2800, 0x2000, 0x1800, 0x1000};   // 2^-5, 2^-7, 2^-9, 2^-11
+    constexpr unsigned short kBias[4] = {0xD002, 0xC808, 0xC020, 0xB880};    // -32.0625, -8.0625, -2.0625, -0.5625
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const uint32_t mask = 0x00030003u << (2 * p);
+        const __half2 s = __halves2half2(__ushort_as_half(kScale[p]), __ushort_as_half(kScale[p]));
+        const __half2 b = __halves2half2(__ushort_as_half(kBias[p]), __ushort_as_half(kBias[p]));
+        w[2 * p] = __hfma2(as_h2(and_or(v, mask, magic)), s, b);
+        w[2 * p + 1] = __hfma2(as_h2(and_or(v8, mask, magic)), s, b);
+    }
 }
 
 }  // namespace qmv

@@ -39,7 +39,7 @@
 
 namespace qmv {
 
-enum Fmt : int { kQ4_0 = 0, kQ8_0 = 1 };
+enum Fmt : int { kQ4_0 = 0, kQ8_0 = 1, kQ2W = 2 };
 
 template <int FMT>
 struct FmtTraits;
@@ -58,6 +58,15 @@ struct FmtTraits<kQ8_0> {
     static constexpr int kUnitBytes = 272;
     static constexpr int kUnitWords = 68;
     static constexpr float kPrescale = kQ8Prescale;
+};
+
+// Plain 2-bit: fp16 d then 8 code bytes per 32 weights (2.5 bits per weight).
+template <>
+struct FmtTraits<kQ2W> {
+    static constexpr int kBlockBytes = 10;
+    static constexpr int kUnitBytes = 80;
+    static constexpr int kUnitWords = 20;
+    static constexpr float kPrescale = kQ2Prescale;
 };
 
 constexpr int kUnitWeights = 256;
@@ -87,7 +96,7 @@ struct GemvParams {
 // Shared-memory bytes the kernel needs for a configuration.
 __host__ __device__ inline size_t gemv_smem_bytes(int fmt, int M, int n_problems, int U, int warps, int S, int SP)
 {
-    const size_t unit_bytes = fmt == kQ4_0 ? 144 : 272;
+    const size_t unit_bytes = fmt == kQ4_0 ? 144 : (fmt == kQ2W ? 80 : 272);
     const size_t xbytes = static_cast<size_t>(n_problems) * M * U * kXUnitBytes;
     const size_t ring = static_cast<size_t>(warps) * S * 32 * SP * unit_bytes;
     const size_t bars = static_cast<size_t>(warps) * S * 8;
@@ -100,7 +109,8 @@ __host__ __device__ inline size_t gemv_smem_bytes(int fmt, int M, int n_problems
 // 16-byte group of slots lines up with the half2 pairs one unpacked 32-bit word
 // of codes produces.  Even blocks of a unit start 2 bytes into a 32-bit word,
 // so their first word is re-formed with a PRMT as qs bytes (0, 1, 14, 15)
-// [Q4_0] or (0, 1, 30, 31) [Q8_0]; the other words are aligned.
+// [Q4_0], (0, 1, 30, 31) [Q8_0] or (0, 1, 6, 7) [2-bit, whose second word is
+// then bytes (2..5)]; the other words are aligned.
 template <int FMT>
 __host__ __device__ __forceinline__ int x_perm_slot(int block_parity, int e)
 {
@@ -117,6 +127,16 @@ __host__ __device__ __forceinline__ int x_perm_slot(int block_parity, int e)
         const int pair = (bp & 1) + 2 * hi;
         const int second = bp >> 1;
         return word * 8 + pair * 2 + second;
+    } else if (FMT == kQ2W) {
+        const int plane = e >> 3, qi = e & 7;     // code byte qi, bits 2*plane
+        int word, bp;
+        if (block_parity) { word = qi >> 2; bp = qi & 3; }
+        else if (qi < 2 || qi >= 6) { word = 0; bp = qi < 2 ? qi : qi - 4; }
+        else { word = 1; bp = qi - 2; }
+        // unpack_q2_word pairs: 2p = (plane p of b0, of b2), 2p+1 = (of b1, of b3)
+        const int pair = 2 * plane + (bp & 1);
+        const int second = bp >> 1;
+        return word * 16 + pair * 2 + second;
     } else {
         const int qi = e;
         int word, bp;
@@ -269,6 +289,72 @@ __device__ __forceinline__ void dot_unit_q8_0(const uint8_t *wsrc, const uint8_t
                 h = __hfma2(wa[1], as_h2(xv.y), h);
                 h = __hfma2(wb[0], as_h2(xv.z), h);
                 h = __hfma2(wb[1], as_h2(xv.w), h);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < M; ++m) acc_block(part[b & 1][m], dsrc, ha[m], hb[m]);
+    }
+#pragma unroll
+    for (int m = 0; m < M; ++m) acc[m] += part[0][m] + part[1][m];
+}
+
+// Plain 2-bit: a unit is 80 bytes = 20 words; blocks 2h, 2h+1 share words
+// 5h..5h+4 as (d, c0, c1) (c2..c5) (c6, c7, d') (c'0..c'3) (c'4..c'7).
+template <int M>
+__device__ __forceinline__ void dot_unit_q2w(const uint8_t *wsrc, const uint8_t *xsrc, int xstride,
+                                             float (&acc)[M])
+{
+    uint32_t w[20];
+#pragma unroll
+    for (int c = 0; c < 5; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(wsrc + 16 * c);
+        w[4 * c + 0] = v.x;
+        w[4 * c + 1] = v.y;
+        w[4 * c + 2] = v.z;
+        w[4 * c + 3] = v.w;
+    }
+    float part[2][M];
+#pragma unroll
+    for (int m = 0; m < M; ++m) part[0][m] = part[1][m] = 0.0f;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+        const int h = b >> 1;
+        uint32_t q[2];
+        uint32_t dsrc;
+        if ((b & 1) == 0) {
+            dsrc = w[5 * h] & 0xffffu;
+            q[0] = __byte_perm(w[5 * h], w[5 * h + 2], 0x5432);   // code bytes 0, 1, 6, 7
+            q[1] = w[5 * h + 1];                                  // code bytes 2..5
+        } else {
+            dsrc = w[5 * h + 2] >> 16;
+            q[0] = w[5 * h + 3];
+            q[1] = w[5 * h + 4];
+        }
+        // One half2 chain per word and token (8 products per half), joined in fp32.
+        __half2 ha[M], hb[M];
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            ha[m] = __float2half2_rn(0.0f);
+            hb[m] = __float2half2_rn(0.0f);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            __half2 wv[8];
+            unpack_q2_word(q[j], wv);
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                const uint8_t *xp = xsrc + m * xstride + b * 64 + j * 32;
+                const uint4 x0 = *reinterpret_cast<const uint4 *>(xp);
+                const uint4 x1 = *reinterpret_cast<const uint4 *>(xp + 16);
+                __half2 &hh = (j == 0) ? ha[m] : hb[m];
+                hh = __hfma2(wv[0], as_h2(x0.x), hh);
+                hh = __hfma2(wv[1], as_h2(x0.y), hh);
+                hh = __hfma2(wv[2], as_h2(x0.z), hh);
+                hh = __hfma2(wv[3], as_h2(x0.w), hh);
+                hh = __hfma2(wv[4], as_h2(x1.x), hh);
+                hh = __hfma2(wv[5], as_h2(x1.y), hh);
+                hh = __hfma2(wv[6], as_h2(x1.z), hh);
+                hh = __hfma2(wv[7], as_h2(x1.w), hh);
             }
         }
 #pragma unroll
@@ -458,6 +544,19 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
                         else { i0 = 4 * sub - 2; i2 = 4 * sub; }
                         i4 = i0 + 16;
                         i6 = i2 + 16;
+                    } else if (FMT == kQ2W) {
+                        // planes 2*(sub & 1) and 2*(sub & 1) + 1 of word sub >> 1: bytes
+                        // b0,b1 from (i0, i0+1), b2,b3 from (i2, i2+1); byte i holds
+                        // elements i + 8 * plane.  Even blocks: words (0,1,6,7), (2..5).
+                        const int wd = sub >> 1, p0 = 2 * (sub & 1);
+                        int b0, b2;
+                        if (blk & 1) { b0 = 4 * wd; b2 = 4 * wd + 2; }
+                        else if (wd == 0) { b0 = 0; b2 = 6; }
+                        else { b0 = 2; b2 = 4; }
+                        i0 = b0 + 8 * p0;
+                        i2 = b2 + 8 * p0;
+                        i4 = i0 + 8;
+                        i6 = i2 + 8;
                     } else {
                         // words 2*sub and 2*sub+1 of the block (Q8_0: four codes per word)
                         const int w0 = 2 * sub, w1 = 2 * sub + 1;
@@ -567,6 +666,8 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
                 if (u < U) {
                     if (FMT == kQ4_0)
                         dot_unit_q4_0<M>(stage + (pass * G + q) * T::kUnitBytes, xrow + u * kXUnitBytes, xstride, acc);
+                    else if (FMT == kQ2W)
+                        dot_unit_q2w<M>(stage + (pass * G + q) * T::kUnitBytes, xrow + u * kXUnitBytes, xstride, acc);
                     else
                         dot_unit_q8_0<M>(stage + (pass * G + q) * T::kUnitBytes, xrow + u * kXUnitBytes, xstride, acc);
                 }
@@ -694,6 +795,7 @@ __global__ void __launch_bounds__(256) gemv_generic_kernel(const GemvParams p, i
                         for (int j = 0; j < 32; ++j) {
                             int c;
                             if (FMT == kQ4_0) c = (j < 16 ? (blk[2 + j] & 0xF) : (blk[2 + j - 16] >> 4)) - 8;
+                            else if (FMT == kQ2W) c = ((blk[2 + (j & 7)] >> (2 * (j >> 3))) & 3) - 2;
                             else c = static_cast<int8_t>(blk[2 + j]);
                             const float wv = static_cast<float>(c) * d;
 #pragma unroll

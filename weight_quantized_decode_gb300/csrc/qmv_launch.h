@@ -15,6 +15,9 @@ cudaError_t launch_gemv_stream_q4_0(int M, const GemvParams &p, int grid, int wa
 // Q4_0 with fp32 activations (plain and fused SwiGLU forms; p.xf set).
 cudaError_t launch_gemv_stream_q4_0_f32(int M, const GemvParams &p, int grid, int warps, size_t smem,
                                         cudaStream_t s, bool pdl);
+// Plain 2-bit (plain form only).
+cudaError_t launch_gemv_stream_q2w(int M, const GemvParams &p, int grid, int warps, size_t smem, cudaStream_t s,
+                                   bool pdl);
 cudaError_t launch_gemv_stream_q8_0(int M, const GemvParams &p, int grid, int warps, size_t smem,
                                     cudaStream_t s, bool pdl);
 // Generic kernel (any K % 32 == 0, activations read from global memory).
