@@ -66,6 +66,13 @@ class Oracle:
         lib.oracle_qmv_rows_f32.argtypes = lib.oracle_qmv_rows.argtypes
         lib.oracle_swiglu_rows_f32.restype = ctypes.c_int
         lib.oracle_swiglu_rows_f32.argtypes = lib.oracle_swiglu_rows.argtypes
+        lib.oracle_float_to_half.restype = ctypes.c_uint16
+        lib.oracle_float_to_half.argtypes = [ctypes.c_float]
+        lib.oracle_quantize_q8_1.restype = ctypes.c_int
+        lib.oracle_quantize_q8_1.argtypes = [_ptr, _i64, _i64, _ptr, _ptr, _ptr]
+        lib.oracle_qmv_q8_1_rows.restype = ctypes.c_int
+        lib.oracle_qmv_q8_1_rows.argtypes = [ctypes.c_int, _ptr, _ptr, _ptr, _i64, _i64, _i64, _ptr, _i64,
+                                             _ptr, _ptr, ctypes.c_int]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         self.lib = lib
@@ -185,6 +192,42 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"oracle_swiglu_rows failed ({rc})")
         return out
+
+    def float_to_half(self, f: float) -> int:
+        return int(self.lib.oracle_float_to_half(float(f)))
+
+    def quantize_q8_1(self, x):
+        """Q8_1 blocks of fp16 activations [M][K]: (q int8 [M][K], d_bits uint16
+        [M][K/32] (the fp16 scales), sumq int32 [M][K/32])."""
+        xb = self._x_bits(x)
+        xb = xb.reshape(xb.shape[0], -1) if xb.ndim == 2 else xb.reshape(1, -1)
+        M, K = xb.shape
+        q = np.empty((M, K), dtype=np.int8)
+        d = np.empty((M, K // 32), dtype=np.uint16)
+        s = np.empty((M, K // 32), dtype=np.int32)
+        rc = self.lib.oracle_quantize_q8_1(xb.ctypes.data, M, K, q.ctypes.data, d.ctypes.data, s.ctypes.data)
+        if rc != 0:
+            raise ValueError(f"oracle_quantize_q8_1 failed ({rc})")
+        return q, d, s
+
+    def qmv_q8_1(self, fmt: int, W, q, d_bits, N: int, K: int, rows=None, nthreads: int = 1):
+        """(y, S) of the weights against Q8_1 activations (q, d_bits): float64 [M][n]."""
+        Wb = self._u8(W)
+        q = np.ascontiguousarray(q, dtype=np.int8).reshape(-1, K)
+        d_bits = np.ascontiguousarray(d_bits, dtype=np.uint16).reshape(q.shape[0], K // 32)
+        M = q.shape[0]
+        if rows is None:
+            rp, nr = None, N
+        else:
+            rows = np.ascontiguousarray(rows, dtype=np.int64)
+            rp, nr = rows.ctypes.data, rows.size
+        y = np.empty((M, nr), dtype=np.float64)
+        S = np.empty((M, nr), dtype=np.float64)
+        rc = self.lib.oracle_qmv_q8_1_rows(fmt, Wb.ctypes.data, q.ctypes.data, d_bits.ctypes.data, N, K, M,
+                                           rp, nr, y.ctypes.data, S.ctypes.data, nthreads)
+        if rc != 0:
+            raise ValueError(f"oracle_qmv_q8_1_rows failed ({rc})")
+        return y, S
 
     def max_threads(self) -> int:
         return int(self.lib.oracle_max_threads())

@@ -79,6 +79,32 @@ double oracle_half_to_double(uint16_t h)
     return sign ? -v : v;
 }
 
+/* float -> IEEE binary16, round to nearest with ties to even, written out from
+ * the format's definition: |v| >= 65520 (the midpoint above 65504) is inf,
+ * |v| < 2^-14 is a subnormal multiple of 2^-24, otherwise 10 mantissa bits
+ * after the leading one.  The arithmetic is exact in double; rint rounds to
+ * nearest even in the default rounding mode. */
+uint16_t oracle_float_to_half(float f)
+{
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    const uint16_t sign = (uint16_t)((bits >> 16) & 0x8000u);
+    if (isnan(f)) return (uint16_t)(sign | 0x7e00u);
+    const double v = fabs((double)f);
+    if (v >= 65520.0) return (uint16_t)(sign | 0x7c00u);
+    if (v < ldexp(1.0, -14)) {
+        const double n = rint(v * ldexp(1.0, 24));       /* 0..1024; 1024 is the smallest normal */
+        return (uint16_t)(sign | (uint16_t)n);
+    }
+    int e2;
+    const double m = frexp(v, &e2);                       /* v = m * 2^e2, m in [0.5, 1) */
+    int e = e2 - 1;                                       /* v = (2m) * 2^e, 2m in [1, 2) */
+    double mant = rint((2.0 * m - 1.0) * 1024.0);
+    if (mant >= 1024.0) { mant = 0.0; e += 1; }
+    if (e > 15) return (uint16_t)(sign | 0x7c00u);
+    return (uint16_t)(sign | (uint16_t)((e + 15) << 10) | (uint16_t)mant);
+}
+
 int64_t oracle_block_bytes(int fmt)
 {
     if (fmt == ORACLE_FMT_Q4_0) return 18;
@@ -306,6 +332,64 @@ int oracle_swiglu_rows_f32(int fmt, const uint8_t *Wg, const uint8_t *Wu, const 
     double *xd = widen_float(x, M * K);
     if (!xd) return -2;
     int rc = swiglu_rows_xd(fmt, Wg, Wu, xd, N, K, M, rows, nrows, y, g, u, Sg, Su, nthreads);
+    free(xd);
+    return rc;
+}
+
+/* Activations quantised to 8 bits per block of 32 (Q8_1: llama.cpp and the
+ * sm8x kernel convert the activations to this form once per call and then
+ * take an int8 dot -- sm8x-bench, "Our kernel does what llama.cpp does").  For each
+ * block of each token, in fp32 with round-to-nearest (the same precision the
+ * kernel decides the codes in):
+ *     amax = max |x_i|,  d = amax / 127,  id = 1 / d (0 when d = 0),
+ *     q_i = round(x_i * id)   (ties away from zero),
+ * and the block keeps d as fp16 (its stored scale) and sum_i q_i.
+ * Outputs: q int8 [M][K], d_bits uint16 [M][K/32], sumq int32 [M][K/32]. */
+int oracle_quantize_q8_1(const uint16_t *x, int64_t M, int64_t K, int8_t *q, uint16_t *d_bits, int32_t *sumq)
+{
+    if (K % 32 != 0 || M < 0) return -1;
+    const int64_t nb = K / 32;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t b = 0; b < nb; ++b) {
+            const uint16_t *xb = x + m * K + b * 32;
+            float xf[32];
+            float amax = 0.0f;
+            for (int i = 0; i < 32; ++i) {
+                xf[i] = (float)oracle_half_to_double(xb[i]);
+                const float a = fabsf(xf[i]);
+                if (a > amax) amax = a;
+            }
+            const float d = amax / 127.0f;
+            const float id = d != 0.0f ? 1.0f / d : 0.0f;
+            int32_t s = 0;
+            for (int i = 0; i < 32; ++i) {
+                const float t = xf[i] * id;
+                const int c = (int)roundf(t);
+                q[m * K + b * 32 + i] = (int8_t)c;
+                s += c;
+            }
+            d_bits[m * nb + b] = oracle_float_to_half(d);
+            sumq[m * nb + b] = s;
+        }
+    }
+    return 0;
+}
+
+/* The product with Q8_1 activations: y[m][n] = sum_k w[n][k] * q[m][k] * d[m][k/32]
+ * with d the block's stored fp16 scale (the plain product on the activations
+ * the quantised form stands for); S likewise with absolute values. */
+int oracle_qmv_q8_1_rows(int fmt, const uint8_t *W, const int8_t *q, const uint16_t *d_bits,
+                         int64_t N, int64_t K, int64_t M, const int64_t *rows, int64_t nrows,
+                         double *y, double *S, int nthreads)
+{
+    if (oracle_block_bytes(fmt) < 0 || K % 32 != 0 || N < 0 || M < 0) return -1;
+    if (rows == NULL) nrows = N;
+    double *xd = (double *)malloc(sizeof(double) * (size_t)(M * K > 0 ? M * K : 1));
+    if (!xd) return -2;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k)
+            xd[m * K + k] = (double)q[m * K + k] * oracle_half_to_double(d_bits[m * (K / 32) + k / 32]);
+    int rc = qmv_rows_xd(fmt, W, xd, N, K, M, rows, nrows, y, S, nthreads);
     free(xd);
     return rc;
 }

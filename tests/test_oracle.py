@@ -379,3 +379,104 @@ def test_f32_swiglu_closed_form(orc):
     r = orc.swiglu(0, _uniform_table(9, 0x2800), _uniform_table(10, 0x2800), x, 1, 32)
     assert r["g"][0, 0] == e and r["u"][0, 0] == 2.0 * e
     assert r["y"][0, 0] == pytest.approx(_silu(e) * 2.0 * e, rel=1e-15)
+
+
+# -- fp16 encoder and Q8_1 activations ---------------------------------------------------
+
+def test_float_to_half_matches_numpy(orc):
+    """Round to nearest even, against numpy's float32 -> float16 cast: every finite
+    half, every midpoint between neighbours (the ties), a hair either side of
+    each midpoint, and log-uniform random values of both signs."""
+    bits = np.arange(0x0000, 0x7c00, dtype=np.uint16)           # finite non-negative halves
+    h = bits.view(np.float16).astype(np.float32)
+    mids = ((h[:-1].astype(np.float64) + h[1:].astype(np.float64)) / 2).astype(np.float32)
+    hair = np.float32(1 + 2.0 ** -20)
+    rng = np.random.default_rng(5)
+    rnd = (2.0 ** rng.uniform(-30, 17, 20000)).astype(np.float32)
+    vals = np.concatenate([h, mids, mids * hair, mids / hair, rnd, [65504, 65519.99, 65520, 65536, 1e9]]).astype(np.float32)
+    vals = np.concatenate([vals, -vals])
+    got = np.array([orc.float_to_half(v) for v in vals], dtype=np.uint16)
+    with np.errstate(over="ignore"):                          # the values above 65520 are meant to overflow
+        want = vals.astype(np.float16).view(np.uint16)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, [(float(vals[i]), hex(got[i]), hex(want[i])) for i in bad[:5]]
+
+
+def _q81(orc, x):
+    return orc.quantize_q8_1(np.asarray(x, dtype=np.float16).reshape(1, -1))
+
+
+def test_q8_1_closed_forms(orc):
+    # amax = 127: d = 1, q = x exactly
+    x = np.array(list(range(-127, 128, 8))[:31] + [127], dtype=np.float64)
+    q, d, s = _q81(orc, x)
+    assert np.array_equal(q[0], x.astype(np.int8)) and d[0, 0] == 0x3C00 and s[0, 0] == int(x.sum())
+    # all zeros: d = 0, q = 0
+    q, d, s = _q81(orc, np.zeros(32))
+    assert not q.any() and d[0, 0] == 0 and s[0, 0] == 0
+    # amax = 254: d = 2, id = 0.5; ties go away from zero (2.5 -> 3, -1.5 -> -2, 0.5 -> 1)
+    x = np.zeros(32); x[:8] = [254, 5, -3, 1, -1, 2, 7, -254]
+    q, d, s = _q81(orc, x)
+    assert list(q[0, :8]) == [127, 3, -2, 1, -1, 1, 4, -127] and d[0, 0] == 0x4000
+    assert s[0, 0] == 127 + 3 - 2 + 1 - 1 + 1 + 4 - 127
+    # amax = 1: d = 1/127 stored as the nearest fp16 (0x2008: 0.0078735...)
+    x = np.zeros(32); x[0] = 1.0; x[1] = -0.5
+    q, d, s = _q81(orc, x)
+    assert q[0, 0] == 127 and q[0, 1] == -64 and d[0, 0] == 0x2008   # -63.5 rounds away to -64
+
+
+def test_q8_1_blocks_tokens_and_symmetry(orc):
+    x = synth.activations(3, 256, 81)
+    q, d, s = orc.quantize_q8_1(x)
+    for m in range(3):
+        for b in range(8):
+            qb, db, sb = _q81(orc, x[m, 32 * b:32 * b + 32])
+            assert np.array_equal(qb[0], q[m, 32 * b:32 * b + 32]) and db[0, 0] == d[m, b] and sb[0, 0] == s[m, b]
+    qn, dn, sn = orc.quantize_q8_1(-x)
+    assert np.array_equal(qn, -q) and np.array_equal(dn, d) and np.array_equal(sn, -s)
+    assert np.array_equal(s, q.reshape(3, 8, 32).astype(np.int32).sum(axis=2))
+    # every code within half a step of x (d in fp32 before its fp16 rounding)
+    xf = x.astype(np.float64).reshape(3, 8, 32)
+    dd = np.abs(xf).max(axis=2, keepdims=True) / 127
+    assert np.all(np.abs(xf - q.reshape(3, 8, 32) * dd) <= dd * (0.5 + 1e-6))
+    assert np.abs(q).max() == 127
+
+
+def test_q8_1_product_integer_case_matches_numpy(orc):
+    # Q4_0 with d = 1 against activations whose every block has max |x| = 127:
+    # d_x = 1 and q = x, so y is the integer matmul
+    rng = np.random.default_rng(82)
+    N, K, M = 6, 256, 2
+    codes = rng.integers(0, 16, size=(N, K))
+    W = H.encode_q4_0(codes, np.full((N, K // 32), 0x3C00, dtype=np.uint16))
+    x = rng.integers(-127, 128, size=(M, K))
+    x.reshape(M, K // 32, 32)[:, :, 0] = 127
+    q, d, s = orc.quantize_q8_1(x.astype(np.float16))
+    assert np.array_equal(q, x) and np.all(d == 0x3C00)
+    y, S = orc.qmv_q8_1(0, W, q, d, N, K)
+    Wi = (codes - 8).astype(np.float64)
+    assert np.array_equal(y, x.astype(np.float64) @ Wi.T)
+    assert np.array_equal(S, np.abs(x).astype(np.float64) @ np.abs(Wi).T)
+
+
+def test_q8_1_product_is_the_product_on_dequantised_x(orc):
+    N, K, M = 9, 768, 3
+    W, x = _rand("q4_0", N, K, M, 83)
+    q, d, _ = orc.quantize_q8_1(x)
+    xhat = (q.reshape(M, K // 32, 32).astype(np.float32)
+            * d.view(np.float16).astype(np.float32)[:, :, None]).reshape(M, K)   # exact in fp32
+    y1, S1 = orc.qmv_q8_1(0, W, q, d, N, K)
+    y2, S2 = orc.qmv(0, W, xhat, N, K)
+    assert np.array_equal(y1, y2) and np.array_equal(S1, S2)
+    yr, Sr = orc.qmv_q8_1(0, W, q, d, N, K, rows=[8, 0, 4])
+    assert np.array_equal(yr, y1[:, [8, 0, 4]]) and np.array_equal(Sr, S1[:, [8, 0, 4]])
+    # against the exact product: the quantisation error stays within its bound
+    # sum |w| * (d_fp32 / 2 + |q| * |fp16(d) - d|) per output (w from the oracle's dequantisation)
+    ye, _ = orc.qmv(0, W, x, N, K)
+    wabs = np.abs(np.stack([orc.dequant_row(0, W, n, K) for n in range(N)]))
+    xf = x.astype(np.float64).reshape(M, K // 32, 32)
+    dd = np.abs(xf).max(axis=2) / 127
+    dq = d.view(np.float16).astype(np.float64)
+    per_x = (dd[:, :, None] / 2 + np.abs(q.reshape(M, K // 32, 32)) * np.abs(dq - dd)[:, :, None]).reshape(M, K)
+    bound = per_x @ wabs.T
+    assert np.all(np.abs(y1 - ye) <= bound * (1 + 1e-9))

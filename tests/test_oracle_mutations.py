@@ -68,6 +68,18 @@ MUTANTS = [
     ("q2w_bias_off_by_one", "w[j] = (double)(c - 2) * d;", "w[j] = (double)(c - 1) * d;", 0),
     ("q2w_scale_dropped", "w[j] = (double)(c - 2) * d;", "w[j] = (double)(c - 2);", 0),
     ("q2w_block_bytes", "if (fmt == ORACLE_FMT_Q2W) return 10;", "if (fmt == ORACLE_FMT_Q2W) return 8;", 0),
+    ("f2h_ties_away", "double mant = rint((2.0 * m - 1.0) * 1024.0);",
+     "double mant = round((2.0 * m - 1.0) * 1024.0);", 0),
+    ("f2h_truncates", "double mant = rint((2.0 * m - 1.0) * 1024.0);",
+     "double mant = floor((2.0 * m - 1.0) * 1024.0);", 0),
+    ("f2h_overflow_at_max", "if (v >= 65520.0) return", "if (v > 65504.0) return", 0),
+    ("f2h_subnormal_scale", "rint(v * ldexp(1.0, 24))", "rint(v * ldexp(1.0, 23))", 0),
+    ("q8_1_ties_to_even", "const int c = (int)roundf(t);", "const int c = (int)rintf(t);", 0),
+    ("q8_1_scale_128", "const float d = amax / 127.0f;", "const float d = amax / 128.0f;", 0),
+    ("q8_1_amax_signed", "const float a = fabsf(xf[i]);", "const float a = xf[i];", 0),
+    ("q8_1_sum_first_only", "s += c;", "s = c;", 0),
+    ("q8_1_scale_per_token", "xd[m * K + k] = (double)q[m * K + k] * oracle_half_to_double(d_bits[m * (K / 32) + k / 32]);",
+     "xd[m * K + k] = (double)q[m * K + k] * oracle_half_to_double(d_bits[m * (K / 32)]);", 0),
     ("f32_narrowed_to_half", "xd[i] = (double)x[i];", "xd[i] = (double)(_Float16)x[i];", 0),
     ("f32_read_as_half", "double *xd = widen_float(x, M * K);",
      "double *xd = widen_half((const uint16_t *)x, M * K);", 0),
