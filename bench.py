@@ -69,6 +69,12 @@ WORKLOADS = {
     "q4_0_f32in": {"kind": "gemv", "fmt": "q4_0", "x": "f32", "M": [1, 8],
                    "shapes": [(12288, 2560), (8192, 2048), (6144, 2048), (640, 2560), (512, 2048), (2048, 512)]},
     "q4_0_swiglu_f32in": {"kind": "swiglu", "fmt": "q4_0", "x": "f32", "M": [1, 8], "shapes": [(6144, 2048)]},
+    # Q4_0 against activations quantised to Q8_1 in the kernel, integer dots
+    # (sm8x-bench, "Our kernel does what llama.cpp does"): the Llama-3-8B
+    # tables at one token and eight.
+    "q4_0_q8_1": {"kind": "gemv", "fmt": "q4_0", "x": "q8_1", "M": [1, 8], "dtype": "i8",
+                  "shapes": [(4096, 4096), (6144, 4096), (4096, 14336), (14336, 4096), (28672, 4096),
+                             (128256, 4096)]},
     # Plain 2-bit (codes -2..1, fp16 scale per 32): the bakeoff's six one-token
     # tables (volta-kernel-bakeoff, "Results (one token, microseconds, lower is
     # better)", its 2-bit column).
@@ -85,7 +91,8 @@ def metric_name(workload):
         return "Q4_0 prefill GEMM TFLOP/s (fp16 tensor cores; us/call per table in 'sweep')"
     if wl["kind"] == "moe":
         return "Q4_0 multi-expert GEMV (one launch) HBM GB/s (algorithmic bytes; us/call per config in 'sweep')"
-    xin = " (fp32 activations in)" if wl.get("x") == "f32" else ""
+    xin = {"f32": " (fp32 activations in)", "q8_1": " (activations quantised to Q8_1 in the kernel, int8 dots)"}.get(
+        wl.get("x"), "")
     if wl["kind"] == "swiglu":
         return (f"Q4_0 fused gate+up+SwiGLU{xin} HBM GB/s (algorithmic bytes of both tables; "
                 "us/call per table in 'sweep')")
@@ -262,6 +269,8 @@ def run_ours(args, dist, rank, local, world):
                   "prefill": q.qmm_q4_0_prefill_ptr}[kind]
         if xb == 4:
             fn_ptr = q.qmv_q4_0_f32_ptr
+        if wl.get("x") == "q8_1":
+            fn_ptr = q.qmv_q4_0_q8_1_ptr
         for (N, K) in wl["shapes"]:
             Wd, copies = rotated_copies(N, K, f"{fmt}_{N}x{K}")
             for M in wl["M"]:
@@ -491,7 +500,7 @@ def run_ours(args, dist, rank, local, world):
         out = {
             "metric": metric_name(args.workload), "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": wl.get("dtype", "f16"), "data": "synthetic",
             "config": cfg,
             "sweep": sweep,
             "roofline": roof,
@@ -548,10 +557,18 @@ def oracle_tasks(workload):
                 e = int(idx[sl])
                 jobs.append((pool[e * N:(e + 1) * N], x[sl:sl + 1], N, K, 1))
 
+    q81 = wl.get("x") == "q8_1"
+
     def run(frac):
         b = f = 0
         for (W, x, N, K, M) in jobs:
             rows = np.linspace(0, N - 1, max(1, int(N * frac))).astype(np.int64)
+            if q81:   # the activations to Q8_1, then the product on them
+                qx, dx, _ = orc.quantize_q8_1(x)
+                orc.qmv_q8_1(fid, W, qx, dx, N, K, rows=rows, nthreads=threads)
+                b += rows.size * (K // 32) * bb + xb * M * K + 4 * M * rows.size
+                f += 2 * M * rows.size * K
+                continue
             orc.qmv_rows(fid, W, x, N, K, rows, nthreads=threads)
             b += rows.size * (K // 32) * bb + xb * M * K + 4 * M * rows.size
             f += 2 * M * rows.size * K
@@ -629,12 +646,14 @@ def ncu_case(spec):
     (a small, bounded program for an Nsight Compute capture).
     spec: q4_0:NxK:M | q8_0:NxK:M | prefill:NxK:M | moe:NxK:SLOTS (pool of 128) |
     swiglu:NxK:M (gate and up tables of N rows each) | q4_0_f32:NxK:M | swiglu_f32:NxK:M
-    (fp32 activations) | q2w:NxK:M (plain 2-bit)."""
+    (fp32 activations) | q2w:NxK:M (plain 2-bit) | q4_0_q81:NxK:M (Q8_1 activations)."""
     import torch
     import weight_quantized_decode_gb300 as q
     kind, shape, M = spec.split(":")
     f32 = kind.endswith("_f32")
     kind = kind[:-4] if f32 else kind
+    q81 = kind == "q4_0_q81"
+    kind = "q4_0" if q81 else kind
     N, K = (int(v) for v in shape.split("x"))
     M = int(M)
     dev = torch.device("cuda", 0)
@@ -658,7 +677,8 @@ def ncu_case(spec):
             fn = q.qmv_q4_0_swiglu_f32_ptr if f32 else q.qmv_q4_0_swiglu_ptr
             fn(Wc[:N].data_ptr(), Wc[N:].data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, s)
         else:
-            fn = {"q4_0": q.qmv_q4_0_f32_ptr if f32 else q.qmv_q4_0_ptr, "q8_0": q.qmv_q8_0_ptr,
+            fn = {"q4_0": q.qmv_q4_0_q8_1_ptr if q81 else (q.qmv_q4_0_f32_ptr if f32 else q.qmv_q4_0_ptr),
+                  "q8_0": q.qmv_q8_0_ptr,
                   "q2w": q.qmv_q2w_ptr, "prefill": q.qmm_q4_0_prefill_ptr}[kind]
             fn(Wi, x.data_ptr(), y.data_ptr(), N, K, M, s)
     torch.cuda.synchronize()

@@ -104,6 +104,39 @@ QMV_API qmv_status qmv_q8_0(const void *W, const void *x, float *y,
                     int64_t N, int64_t K, int64_t M, qmv_stream_t stream);
 
 /*
+ * Q4_0 decode GEMV against activations quantised to Q8_1, with integer dots
+ * (the sm8x kernel and llama.cpp convert the activations to 8-bit blocks once
+ * and take the Q4_0 dot with dp4a on nibbles masked by 0x0F0F0F0F --
+ * sm8x-bench, "Our kernel does what llama.cpp does").  Here each CTA quantises
+ * the activations while it stages them: no separate quantisation launch.
+ *   W, y, N, K, M (<= 8), errors and asynchrony as for qmv_q4_0; x fp16 [M][K].
+ * The activations are replaced by Q8_1 blocks (see qmv_quantize_q8_1), so the
+ * result is the product on the quantised activations:
+ *     y[m][n] = sum over blocks b of d_w * d_x[m][b] * sum_i (c_i - 8) * q[m][i],
+ * which differs from the exact product by up to sum_k |w| * (d/2 + |q| * |fp16(d) - d|)
+ * per output (d the block's fp32 scale).  Against that quantised product the
+ * kernel's only rounding is the fp32 accumulation of the per-block terms.
+ */
+QMV_API qmv_status qmv_q4_0_q8_1(const void *W, const void *x, float *y,
+                         int64_t N, int64_t K, int64_t M, qmv_stream_t stream);
+
+/*
+ * Q8_1 quantisation of fp16 activations, exactly as qmv_q4_0_q8_1 performs it
+ * inside its kernel: per block of 32 values of a row, in fp32 with
+ * round-to-nearest, amax = max |x|, d = amax / 127, id = 1 / d (0 for an
+ * all-zero block) and q = round(x * id) with ties away from zero; the block's
+ * scale is d rounded to fp16.  Values must be finite.
+ *   x      : DEVICE fp16 [M][K], 16-byte aligned; K % 32 == 0.
+ *   q      : DEVICE int8 [M][K] (8-byte aligned), the codes.
+ *   d_bits : DEVICE uint16 [M][K/32] (2-byte aligned), the fp16 scales' bits.
+ *   sumq   : DEVICE int32 [M][K/32] (4-byte aligned), each block's code sum.
+ * (llama.cpp's Q8_1 block stores d and d * sum(q) beside its 32 codes; these
+ * are the same quantities in three plain arrays.)
+ */
+QMV_API qmv_status qmv_quantize_q8_1(const void *x, int8_t *q, uint16_t *d_bits, int32_t *sumq,
+                             int64_t M, int64_t K, qmv_stream_t stream);
+
+/*
  * Plain 2-bit decode GEMV (the bakeoff's q2w format: codes -2..1 with one fp16
  * scale per 32 weights, 2.5 bits per weight -- volta-kernel-bakeoff, "What's
  * in the race" and the Results table's 2-bit column), same contract as

@@ -34,6 +34,12 @@ def main():
             y = q.qmv_q4_0_swiglu(dev(Wg), dev(Wu), dev(x))
             torch.cuda.synchronize()
             res[case] = y.cpu().numpy()
+        elif kind == "q81":
+            W = synth.q4_0_weights(N, K, synth.seed_for(f"ovr_q81_{N}x{K}"))
+            x = synth.activations(M, K, synth.seed_for(f"ovr_x_{K}_{M}"))
+            y = q.qmv_q4_0_q8_1(dev(W), dev(x))
+            torch.cuda.synchronize()
+            res[case] = y.cpu().numpy()
         elif kind == "gemv":
             W = synth.weights(fmt, N, K, synth.seed_for(f"ovr_{fmt}_{N}x{K}"))
             x = synth.activations(M, K, synth.seed_for(f"ovr_x_{K}_{M}"))

@@ -32,7 +32,7 @@ def lib():
 def test_header_declares_the_boundary():
     names = set(_declared())
     for n in ("qmv_q4_0", "qmv_q8_0", "qmv_moe", "qmm_q4_0_prefill", "qmv_device_status", "qmv_q4_0_swiglu",
-              "qmv_q4_0_f32", "qmv_q4_0_swiglu_f32", "qmv_q2w"):
+              "qmv_q4_0_f32", "qmv_q4_0_swiglu_f32", "qmv_q2w", "qmv_q4_0_q8_1", "qmv_quantize_q8_1"):
         assert n in names
 
 
@@ -51,7 +51,8 @@ def test_version_and_status_strings(lib):
 FAKE = 1 << 20      # a 16-byte-aligned non-null address; never dereferenced here
 
 
-@pytest.mark.parametrize("fn", ["qmv_q4_0", "qmv_q8_0", "qmm_q4_0_prefill", "qmv_q4_0_f32", "qmv_q2w"])
+@pytest.mark.parametrize("fn", ["qmv_q4_0", "qmv_q8_0", "qmm_q4_0_prefill", "qmv_q4_0_f32", "qmv_q2w",
+                                "qmv_q4_0_q8_1"])
 def test_host_validation(lib, fn):
     f = getattr(lib, fn)
     assert f(None, FAKE, FAKE, 8, 256, 1, None) == 1          # NULL W
@@ -88,6 +89,22 @@ def test_host_validation_swiglu(lib, fn):
     assert f(None, None, None, None, 8, 256, 0, None) == 0
     if fn.endswith("_f32"):
         assert f(FAKE, FAKE, FAKE + 2, FAKE, 8, 256, 1, None) == 2   # fp32 x not 4-byte aligned
+
+
+def test_host_validation_quantize_q8_1(lib):
+    f = lib.qmv_quantize_q8_1
+    assert f(None, FAKE, FAKE, FAKE, 2, 256, None) == 1           # NULL x
+    assert f(FAKE, None, FAKE, FAKE, 2, 256, None) == 1           # NULL codes
+    assert f(FAKE, FAKE, None, FAKE, 2, 256, None) == 1           # NULL scales
+    assert f(FAKE, FAKE, FAKE, None, 2, 256, None) == 1           # NULL sums
+    assert f(FAKE + 8, FAKE, FAKE, FAKE, 2, 256, None) == 2       # x not 16-byte aligned
+    assert f(FAKE, FAKE + 4, FAKE, FAKE, 2, 256, None) == 2       # codes not 8-byte aligned
+    assert f(FAKE, FAKE, FAKE + 1, FAKE, 2, 256, None) == 2       # scales not 2-byte aligned
+    assert f(FAKE, FAKE, FAKE, FAKE + 2, 2, 256, None) == 2       # sums not 4-byte aligned
+    assert f(FAKE, FAKE, FAKE, FAKE, 2, 48, None) == 3            # K % 32
+    assert f(FAKE, FAKE, FAKE, FAKE, -1, 256, None) == 3
+    assert f(None, None, None, None, 0, 256, None) == 0           # empty
+    assert f(None, None, None, None, 2, 0, None) == 0
 
 
 def test_host_validation_moe(lib):

@@ -366,13 +366,17 @@ OVERRIDES = {
     # from 1 to 32 (also ones that do not divide 32), odd passes per stage, deep
     # rings, two CTAs per SM; the multi-expert form must still equal the single
     # calls bit for bit.
-    "G=4,SP=3": ["gemv:q4_0:77:6144:1", "gemv:q8_0:130:2560:2", "moe:q4_0:64:2560:5", "gemv:q2w:77:6144:3"],
+    "G=4,SP=3": ["gemv:q4_0:77:6144:1", "gemv:q8_0:130:2560:2", "moe:q4_0:64:2560:5", "gemv:q2w:77:6144:3",
+                 "q81:q4_0:77:6144:3"],
     "G=32,warps=4": ["gemv:q4_0:40:8192:1", "gemv:q8_0:130:2560:4", "moe:q4_0:96:4096:6"],
     "G=1,SP=5,stages=3": ["gemv:q4_0:16:14336:1", "gemv:q4_0:33:2048:3", "moe:q4_0:20:2048:3", "gemv:q2w:16:14336:1"],
-    "warps=16,stages=4,G=2": ["gemv:q4_0:100:4096:2", "gemv:q8_0:9:3072:1", "gemv:q2w:100:4096:1"],
-    "ctas=2,share=2": ["gemv:q4_0:1000:4096:1", "gemv:q8_0:600:2048:1", "moe:q4_0:33:1024:7"],
+    "warps=16,stages=4,G=2": ["gemv:q4_0:100:4096:2", "gemv:q8_0:9:3072:1", "gemv:q2w:100:4096:1",
+                              "q81:q4_0:100:4096:2"],
+    "ctas=2,share=2": ["gemv:q4_0:1000:4096:1", "gemv:q8_0:600:2048:1", "moe:q4_0:33:1024:7",
+                       "q81:q4_0:1000:4096:8"],
     # lanes per row that do not divide 32 (idle lanes, lane-order reduction)
-    "G=10": ["gemv:q4_0:130:2560:1", "gemv:q8_0:77:2560:2", "moe:q4_0:64:2560:5", "gemv:q2w:130:2560:2"],
+    "G=10": ["gemv:q4_0:130:2560:1", "gemv:q8_0:77:2560:2", "moe:q4_0:64:2560:5", "gemv:q2w:130:2560:2",
+             "q81:q4_0:130:2560:1"],
     "G=3,SP=3": ["gemv:q4_0:41:2304:1", "gemv:q8_0:50:1536:4", "moe:q4_0:20:2304:3"],
     "G=12,warps=16": ["gemv:q4_0:90:3072:2", "gemv:q8_0:33:6144:1", "swiglu:q4_0:90:3072:2"],
     # the fused SwiGLU keeps an even number of rows per group (G clamped to <= 16)
@@ -404,6 +408,14 @@ def test_launch_overrides(orc, tmp_path, tune):
             ref = orc.swiglu(0, Wg, Wu, x, N, K, nthreads=8)
             err = H.swiglu_normalised_error(y, ref)
             assert err <= H.TOL, (tune, case, err)
+            continue
+        if kind == "q81":
+            W = synth.q4_0_weights(N, K, synth.seed_for(f"ovr_q81_{N}x{K}"))
+            x = synth.activations(M, K, synth.seed_for(f"ovr_x_{K}_{M}"))
+            qo, do, _ = orc.quantize_q8_1(x)
+            y_ref, S = orc.qmv_q8_1(0, W, qo, do, N, K, nthreads=8)
+            err = H.normalised_error(y, y_ref, S)
+            assert err <= 5e-5, (tune, case, err)
             continue
         if kind == "gemv":
             W = synth.weights(fmt, N, K, synth.seed_for(f"ovr_{fmt}_{N}x{K}"))

@@ -12,6 +12,8 @@ Functions (same names as the C ABI):
     qmv_q4_0_swiglu(W_gate, W_up, x, y=None, stream=None) -> silu(gate) * up, fp32 [M, N]
     qmv_q4_0_f32, qmv_q4_0_swiglu_f32            -> the same two with fp32 x
     qmv_q2w(W, x, y=None, stream=None)           -> plain 2-bit weights, y fp32 [M, N]
+    qmv_q4_0_q8_1(W, x, y=None, stream=None)     -> Q4_0 against Q8_1-quantised x (integer dots)
+    qmv_quantize_q8_1(x, stream=None)            -> (q, d_bits, sumq) of the Q8_1 activations
     qmv_moe(W_pool, expert_idx, n_experts, x, N, y=None, stream=None)
     qmm_q4_0_prefill(W, x, y=None, stream=None)  -> y fp32 [M, N]
     qmv_device_status(stream=None)               -> int (QMV_DEV_* bits, cleared)
@@ -55,7 +57,7 @@ def lib():
                                "(there is no CPU fallback)")
         L = ctypes.CDLL(LIB_PATH)
         vp, i64 = ctypes.c_void_p, ctypes.c_int64
-        for name in ("qmv_q4_0", "qmv_q8_0", "qmm_q4_0_prefill", "qmv_q4_0_f32", "qmv_q2w"):
+        for name in ("qmv_q4_0", "qmv_q8_0", "qmm_q4_0_prefill", "qmv_q4_0_f32", "qmv_q2w", "qmv_q4_0_q8_1"):
             f = getattr(L, name)
             f.restype = ctypes.c_int
             f.argtypes = [vp, vp, vp, i64, i64, i64, vp]
@@ -63,6 +65,8 @@ def lib():
         L.qmv_moe.argtypes = [vp, vp, i64, vp, vp, i64, i64, i64, vp]
         L.qmv_q4_0_swiglu.restype = ctypes.c_int
         L.qmv_q4_0_swiglu.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
+        L.qmv_quantize_q8_1.restype = ctypes.c_int
+        L.qmv_quantize_q8_1.argtypes = [vp, vp, vp, vp, i64, i64, vp]
         L.qmv_q4_0_swiglu_f32.restype = ctypes.c_int
         L.qmv_q4_0_swiglu_f32.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
         L.qmv_device_status.restype = ctypes.c_int
@@ -116,6 +120,14 @@ def qmv_q4_0_swiglu_f32_ptr(W_gate: int, W_up: int, x: int, y: int, N: int, K: i
 
 def qmv_q8_0_ptr(W: int, x: int, y: int, N: int, K: int, M: int, stream: int = 0) -> None:
     _check("qmv_q8_0", lib().qmv_q8_0(W, x, y, N, K, M, stream))
+
+
+def qmv_q4_0_q8_1_ptr(W: int, x: int, y: int, N: int, K: int, M: int, stream: int = 0) -> None:
+    _check("qmv_q4_0_q8_1", lib().qmv_q4_0_q8_1(W, x, y, N, K, M, stream))
+
+
+def qmv_quantize_q8_1_ptr(x: int, q: int, d_bits: int, sumq: int, M: int, K: int, stream: int = 0) -> None:
+    _check("qmv_quantize_q8_1", lib().qmv_quantize_q8_1(x, q, d_bits, sumq, M, K, stream))
 
 
 def qmv_q2w_ptr(W: int, x: int, y: int, N: int, K: int, M: int, stream: int = 0) -> None:
@@ -220,6 +232,30 @@ def qmv_q8_0(W, x, y=None, stream=None):
     W, x, y, N, K, M = _prep(W, x, y, Q8_0_BLOCK_BYTES, "qmv_q8_0")
     qmv_q8_0_ptr(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, _stream_handle(stream))
     return y
+
+
+def qmv_q4_0_q8_1(W, x, y=None, stream=None):
+    """qmv_q4_0 with the activations quantised to Q8_1 in the kernel (integer dots)."""
+    W, x, y, N, K, M = _prep(W, x, y, Q4_0_BLOCK_BYTES, "qmv_q4_0_q8_1")
+    qmv_q4_0_q8_1_ptr(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, _stream_handle(stream))
+    return y
+
+
+def qmv_quantize_q8_1(x, stream=None):
+    """Q8_1 blocks of fp16 activations [M, K] on the GPU: (q int8 [M, K],
+    d_bits int16 [M, K/32] holding the fp16 scales' bits, sumq int32 [M, K/32])."""
+    torch = _torch()
+    if not x.is_cuda or x.dtype != torch.float16:
+        raise TypeError("qmv_quantize_q8_1: x must be a float16 CUDA tensor (no CPU path)")
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    x = x.contiguous()
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    d = torch.empty((M, K // 32), dtype=torch.int16, device=x.device)
+    s = torch.empty((M, K // 32), dtype=torch.int32, device=x.device)
+    qmv_quantize_q8_1_ptr(x.data_ptr(), q.data_ptr(), d.data_ptr(), s.data_ptr(), M, K, _stream_handle(stream))
+    return q, d, s
 
 
 def qmv_q2w(W, x, y=None, stream=None):

@@ -220,7 +220,7 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
     int64_t pmax = (rows_per_cta + p.N - 1) / p.N + 1;
     if (pmax > p.n_problems) pmax = p.n_problems;
     p.max_local_problems = static_cast<int>(pmax);
-    const size_t xbytes = static_cast<size_t>(pmax) * M * p.U * kXUnitBytes;
+    const size_t xbytes = static_cast<size_t>(pmax) * M * p.U * (p.xq8 ? kXQ8UnitBytes : kXUnitBytes);
     const size_t budget = static_cast<size_t>(smem_optin) / (ctas_per_sm > share ? ctas_per_sm : share) - 1024;
     if (xbytes + 8 * 1024 > budget) return pl;
     // Fit the ring: fewer stages, then fewer passes, then fewer warps.
@@ -233,7 +233,7 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
             pl.streaming = true;
             pl.grid = grid;
             pl.warps = warps;
-            pl.smem = gemv_smem_bytes(fmt, M, static_cast<int>(pmax), p.U, warps, S, p.SP);
+            pl.smem = gemv_smem_bytes(fmt, M, static_cast<int>(pmax), p.U, warps, S, p.SP, p.xq8 != 0);
             return pl;
         }
         if (p.SP > 1) p.SP = 1;
@@ -245,7 +245,7 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
 
 qmv_status run_gemv(int fmt, const void *W, const int32_t *idx, int64_t n_experts, const void *x, float *y,
                     int64_t N, int64_t K, int64_t M, int n_problems, cudaStream_t stream, const void *W2 = nullptr,
-                    const float *xf = nullptr)
+                    const float *xf = nullptr, bool xq8 = false)
 {
     if (xf && fmt != kQ4_0) return QMV_ERR_SHAPE;   // fp32 activations: Q4_0 kernels only
     int dev = 0;
@@ -258,6 +258,7 @@ qmv_status run_gemv(int fmt, const void *W, const int32_t *idx, int64_t n_expert
     p.W = static_cast<const uint8_t *>(W);
     p.x = static_cast<const __half *>(x);
     p.xf = xf;
+    p.xq8 = xq8 ? 1 : 0;
     p.y = y;
     p.expert_idx = idx;
     p.N = N;
@@ -276,7 +277,9 @@ qmv_status run_gemv(int fmt, const void *W, const int32_t *idx, int64_t n_expert
     cudaError_t e;
     Plan pl = plan_gemv(fmt, p, Mk, sms, optin);
     if (pl.streaming) {
-        if (fmt == kQ4_0)
+        if (fmt == kQ4_0 && xq8)
+            e = launch_gemv_stream_q4_0_q8_1(Mk, p, pl.grid, pl.warps, pl.smem, stream, pdl);
+        else if (fmt == kQ4_0)
             e = xf ? launch_gemv_stream_q4_0_f32(Mk, p, pl.grid, pl.warps, pl.smem, stream, pdl)
                    : launch_gemv_stream_q4_0(Mk, p, pl.grid, pl.warps, pl.smem, stream, pdl);
         else if (fmt == kQ2W)
@@ -366,6 +369,31 @@ qmv_status qmv_q8_0(const void *W, const void *x, float *y, int64_t N, int64_t K
     qmv_status st = check_common(W, x, y, N, K, M, 8);
     if (st != QMV_OK || N == 0 || M == 0) return st;
     return run_gemv(kQ8_0, W, nullptr, 1, x, y, N, K, M, 1, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qmv_status qmv_q4_0_q8_1(const void *W, const void *x, float *y, int64_t N, int64_t K, int64_t M,
+                         qmv_stream_t stream)
+{
+    qmv_status st = check_common(W, x, y, N, K, M, 8);
+    if (st != QMV_OK || N == 0 || M == 0) return st;
+    return run_gemv(kQ4_0, W, nullptr, 1, x, y, N, K, M, 1, reinterpret_cast<cudaStream_t>(stream), nullptr,
+                    nullptr, true);
+}
+
+qmv_status qmv_quantize_q8_1(const void *x, int8_t *q, uint16_t *d_bits, int32_t *sumq, int64_t M, int64_t K,
+                             qmv_stream_t stream)
+{
+    if (M < 0 || K < 0 || K % 32 != 0 || K > (int64_t(1) << 31) || M > (int64_t(1) << 31)) return QMV_ERR_SHAPE;
+    if (M == 0 || K == 0) return QMV_OK;
+    if (!x || !q || !d_bits || !sumq) return QMV_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(q, 8) || !aligned(d_bits, 2) || !aligned(sumq, 4)) return QMV_ERR_ALIGN;
+    int dev = 0;
+    if (current_device(&dev) != cudaSuccess) return QMV_ERR_CUDA;
+    if (launch_quantize_q8_1(x, q, d_bits, sumq, M, K, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return QMV_ERR_LAUNCH;
+    }
+    return QMV_OK;
 }
 
 qmv_status qmv_q2w(const void *W, const void *x, float *y, int64_t N, int64_t K, int64_t M, qmv_stream_t stream)

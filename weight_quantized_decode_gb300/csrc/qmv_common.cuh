@@ -270,4 +270,58 @@ __device__ __forceinline__ void unpack_q2_word(uint32_t v, __half2 (&w)[8])
     }
 }
 
+// ---- Q8_1 activations (8-bit codes per block of 32) ---------------------------------
+//
+// Per block of 32 activations, decided in fp32 with round-to-nearest: amax =
+// max |x|, d = amax / 127, id = 1 / d (0 for an all-zero block), code =
+// round(x * id) with ties away from zero.  The block keeps d rounded to fp16
+// (its stored scale) and the sum of its codes (for the -8 * sum(q) term of a
+// Q4_0 dot).  Quantising the activations this way before an int8 dot is what
+// llama.cpp and the sm8x kernel do (sm8x-bench, "Our kernel does what
+// llama.cpp does").
+
+// One 8-activation chunk (16 bytes of fp16) of a 32-block whose four chunks are
+// held by lanes 4l..4l+3 of the warp.  Every lane of the warp calls this (lanes
+// without a chunk pass zeros).  Returns the chunk's eight codes in memory
+// order; dq and sumq receive the block's fp16-rounded scale and code sum.
+__device__ __forceinline__ uint2 q8_1_chunk(uint4 xv, float &dq, int &sumq)
+{
+    float f[8];
+    const uint32_t wv[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 t = __half22float2(as_h2(wv[k]));
+        f[2 * k] = t.x;
+        f[2 * k + 1] = t.y;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float id = d != 0.0f ? __frcp_rn(d) : 0.0f;
+    int s = 0;
+    uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int code = static_cast<int>(roundf(__fmul_rn(f[i], id)));
+        s += code;
+        packed[i >> 2] |= (static_cast<uint32_t>(code) & 0xffu) << (8 * (i & 3));
+    }
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    sumq = s;
+    dq = __half2float(__float2half_rn(d));
+    return make_uint2(packed[0], packed[1]);
+}
+
+// d = sum over four bytes of a (unsigned) times b (signed), plus c.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c)
+{
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
 }  // namespace qmv

@@ -71,6 +71,10 @@ struct FmtTraits<kQ2W> {
 
 constexpr int kUnitWeights = 256;
 constexpr int kXUnitBytes = 528;   // 512 bytes of permuted activations + 16 bytes pad
+// Q8_1 activations: per unit the 256 codes of its 8 blocks in element order,
+// then per block (fp32 scale, 8 * code sum), then 16 bytes pad (336 = 5 * 16
+// mod 128: the G units a warp reads at once fall in distinct banks).
+constexpr int kXQ8UnitBytes = 336;
 
 struct GemvParams {
     const uint8_t *W;            // weights; for the multi-expert call, the expert pool; fused SwiGLU: gate
@@ -90,14 +94,16 @@ struct GemvParams {
     int G;                       // lanes per row (1..32; RG = 32 / G rows per warp)
     int SP;                      // passes per stage (odd)
     int S;                       // stages in each warp's ring
+    int xq8;                     // Q4_0 against Q8_1-quantised activations (integer dots)
     int *status;                 // device status word
 };
 
 // Shared-memory bytes the kernel needs for a configuration.
-__host__ __device__ inline size_t gemv_smem_bytes(int fmt, int M, int n_problems, int U, int warps, int S, int SP)
+__host__ __device__ inline size_t gemv_smem_bytes(int fmt, int M, int n_problems, int U, int warps, int S, int SP,
+                                                   bool xq8 = false)
 {
     const size_t unit_bytes = fmt == kQ4_0 ? 144 : (fmt == kQ2W ? 80 : 272);
-    const size_t xbytes = static_cast<size_t>(n_problems) * M * U * kXUnitBytes;
+    const size_t xbytes = static_cast<size_t>(n_problems) * M * U * (xq8 ? kXQ8UnitBytes : kXUnitBytes);
     const size_t ring = static_cast<size_t>(warps) * S * 32 * SP * unit_bytes;
     const size_t bars = static_cast<size_t>(warps) * S * 8;
     const size_t idx = (static_cast<size_t>(n_problems) * 4 + 15) / 16 * 16;   // expert indices (multi-expert call)
@@ -364,6 +370,64 @@ __device__ __forceinline__ void dot_unit_q2w(const uint8_t *wsrc, const uint8_t 
     for (int m = 0; m < M; ++m) acc[m] += part[0][m] + part[1][m];
 }
 
+// Q4_0 weights against Q8_1 activations: per block, integer dots of the codes
+// (low nibbles against codes 0..15, high nibbles -- left in place, so 16 times
+// their value -- against codes 16..31), minus 8 * sum(q), scaled by d_w * d_x.
+template <int M>
+__device__ __forceinline__ void dot_unit_q4_0_q81(const uint8_t *wsrc, const uint8_t *xsrc, int xstride,
+                                                  float (&acc)[M])
+{
+    uint32_t w[36];
+#pragma unroll
+    for (int c = 0; c < 9; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(wsrc + 16 * c);
+        w[4 * c + 0] = v.x;
+        w[4 * c + 1] = v.y;
+        w[4 * c + 2] = v.z;
+        w[4 * c + 3] = v.w;
+    }
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+        const int h = b >> 1;
+        uint32_t qw[4];
+        uint32_t dsrc;
+        if ((b & 1) == 0) {
+            // qs starts 2 bytes into word 9h: realign to qs bytes 4k..4k+3
+            dsrc = w[9 * h] & 0xffffu;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) qw[k] = __byte_perm(w[9 * h + k], w[9 * h + k + 1], 0x5432);
+        } else {
+            dsrc = w[9 * h + 4] >> 16;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) qw[k] = w[9 * h + 5 + k];
+        }
+        uint32_t lo[4], hi[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            lo[k] = qw[k] & 0x0F0F0F0Fu;
+            hi[k] = qw[k] & 0xF0F0F0F0u;
+        }
+        const float dw = half_lo_to_float(dsrc);
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            const uint8_t *xp = xsrc + m * xstride;
+            const uint4 x0 = *reinterpret_cast<const uint4 *>(xp + b * 32);
+            const uint4 x1 = *reinterpret_cast<const uint4 *>(xp + b * 32 + 16);
+            const float2 meta = *reinterpret_cast<const float2 *>(xp + 256 + b * 8);   // (d_x, 8 * sum q)
+            int sl = dp4a_us(lo[0], x0.x, 0);
+            sl = dp4a_us(lo[1], x0.y, sl);
+            sl = dp4a_us(lo[2], x0.z, sl);
+            sl = dp4a_us(lo[3], x0.w, sl);
+            int sh = dp4a_us(hi[0], x1.x, 0);
+            sh = dp4a_us(hi[1], x1.y, sh);
+            sh = dp4a_us(hi[2], x1.z, sh);
+            sh = dp4a_us(hi[3], x1.w, sh);
+            const int sumi = sl + (sh >> 4) - __float_as_int(meta.y);
+            acc[m] = fmaf(static_cast<float>(sumi), dw * meta.x, acc[m]);
+        }
+    }
+}
+
 // ---- the streaming kernel ----------------------------------------------------------
 
 // Warp-collective wait for phase `parity` of `bar`: one vote when the stage
@@ -386,10 +450,15 @@ __device__ __forceinline__ bool stage_wait(uint64_t *bar, uint32_t parity, int *
 // fp32in kernels convert inside the kernel for the same reason: a separate
 // conversion pass costs a launch -- volta-kernel-bakeoff, "Results (one token,
 // microseconds, lower is better)").
-template <int FMT, int M, int MAXT, bool MOE, bool SWIGLU = false, bool XF32 = false>
+// XQ8 = the activations are quantised to Q8_1 while they are staged and the
+// Q4_0 products are integer dots (plain Q4_0 calls only).
+template <int FMT, int M, int MAXT, bool MOE, bool SWIGLU = false, bool XF32 = false, bool XQ8 = false>
 __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p)
 {
     using T = FmtTraits<FMT>;
+    static_assert(!XQ8 || (FMT == kQ4_0 && !MOE && !SWIGLU && !XF32), "Q8_1 activations: plain Q4_0 calls only");
+    constexpr int XUB = XQ8 ? kXQ8UnitBytes : kXUnitBytes;   // activation bytes per unit and token
+    constexpr float kPre = XQ8 ? 1.0f : T::kPrescale;           // the integer dot carries no pre-scale
     extern __shared__ __align__(128) uint8_t smem[];
 
     const int lane = threadIdx.x & 31;
@@ -401,7 +470,7 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
     const uint32_t N = static_cast<uint32_t>(p.N);
 
     // Shared-memory carve-up: activations, then per-warp rings, then barriers.
-    const size_t xbytes = static_cast<size_t>(p.max_local_problems) * M * U * kXUnitBytes;
+    const size_t xbytes = static_cast<size_t>(p.max_local_problems) * M * U * XUB;
     const int slot_bytes = 32 * SP * T::kUnitBytes;
     uint8_t *xs = smem;
     uint8_t *ring = smem + xbytes + static_cast<size_t>(warp) * S * slot_bytes;
@@ -502,7 +571,67 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
     // to kStageItems per thread per round with all their loads in flight, so
     // several tokens cost few L2 round trips (one token of a plain call keeps
     // two items per round: fewer registers live ahead of the main loop).
-    {
+    if constexpr (XQ8) {
+        // Q8_1: each item is a 16-byte chunk of 8 activations, read with one
+        // load; the four chunks of a 32-block sit in four adjacent lanes of one
+        // round (chunks per token and the round are multiples of 4), which
+        // share the block's max and code sum with shuffles.
+        constexpr int kQItems = (M == 1) ? 2 : 4;
+        const int ntok = M;
+        const int chunks = static_cast<int>(p.K / 8);
+        const int items = ntok * chunks;
+        const int round = kQItems * blockDim.x;
+        const int dq = round / chunks, dr = round - dq * chunks;
+        int tk[kQItems], ck[kQItems];
+#pragma unroll
+        for (int b = 0; b < kQItems; ++b) {
+            const int it = b * blockDim.x + threadIdx.x;
+            tk[b] = it / chunks;
+            ck[b] = it - tk[b] * chunks;
+        }
+        bool first = true;
+        for (int it0 = 0; it0 < items || first; it0 += round) {
+            uint4 xv[kQItems];
+            bool ok[kQItems];
+            int cidx[kQItems], tidx[kQItems];
+#pragma unroll
+            for (int b = 0; b < kQItems; ++b) {
+                ok[b] = it0 + b * static_cast<int>(blockDim.x) + static_cast<int>(threadIdx.x) < items;
+                cidx[b] = ck[b];
+                tidx[b] = tk[b];
+                xv[b] = make_uint4(0u, 0u, 0u, 0u);
+                if (ok[b])
+                    xv[b] = __ldg(reinterpret_cast<const uint4 *>(p.x + static_cast<int64_t>(tk[b]) * p.K) + ck[b]);
+            }
+#pragma unroll
+            for (int b = 0; b < kQItems; ++b) {
+                ck[b] += dr;
+                tk[b] += dq;
+                if (ck[b] >= chunks) {
+                    ck[b] -= chunks;
+                    ++tk[b];
+                }
+            }
+            if (first) {
+                first = false;
+                for (int i = early; i < prefetch; ++i) issue_next();
+            }
+#pragma unroll
+            for (int b = 0; b < kQItems; ++b) {
+                float dxq;
+                int sq;
+                const uint2 codes = q8_1_chunk(xv[b], dxq, sq);    // all lanes: it shuffles
+                if (ok[b]) {
+                    const int c = cidx[b];
+                    const int blk = c >> 2, sub = c & 3;
+                    uint8_t *xu = xs + static_cast<size_t>(tidx[b]) * U * XUB + (blk >> 3) * XUB;
+                    *reinterpret_cast<uint2 *>(xu + (blk & 7) * 32 + sub * 8) = codes;
+                    if (sub == 0)
+                        *reinterpret_cast<float2 *>(xu + 256 + (blk & 7) * 8) = make_float2(dxq, __int_as_float(8 * sq));
+                }
+            }
+        }
+    } else {
         constexpr bool kOneToken = (M == 1 && !MOE);
         constexpr int kStageItems = kOneToken ? 2 : 4;
         const int ntok = (prob_hi - prob_lo + 1) * M;
@@ -623,7 +752,7 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
     const int q = lane - r * G;
     const bool lane_on = r < RG;             // G that does not divide 32 leaves lanes RG*G.. idle
     const bool g_pow2 = (G & (G - 1)) == 0;
-    const int xstride = U * kXUnitBytes;     // bytes between tokens of a problem
+    const int xstride = U * XUB;             // bytes between tokens of a problem
     float acc[M];
 #pragma unroll
     for (int m = 0; m < M; ++m) acc[m] = 0.0f;
@@ -664,7 +793,9 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
             for (int pass = 0; pass < SP; ++pass) {
                 const int u = u0 + pass * G;
                 if (u < U) {
-                    if (FMT == kQ4_0)
+                    if constexpr (XQ8)
+                        dot_unit_q4_0_q81<M>(stage + (pass * G + q) * T::kUnitBytes, xrow + u * XUB, xstride, acc);
+                    else if (FMT == kQ4_0)
                         dot_unit_q4_0<M>(stage + (pass * G + q) * T::kUnitBytes, xrow + u * kXUnitBytes, xstride, acc);
                     else if (FMT == kQ2W)
                         dot_unit_q2w<M>(stage + (pass * G + q) * T::kUnitBytes, xrow + u * kXUnitBytes, xstride, acc);
@@ -710,9 +841,9 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
                 for (int m = 0; m < M; ++m) {
                     const float up = __shfl_down_sync(0xffffffffu, acc[m], G);
                     if (q == 0 && lane_on && lr < nrows && (lr & 1) == 0) {
-                        const float gate = acc[m] * T::kPrescale;
+                        const float gate = acc[m] * kPre;
                         p.y[static_cast<int64_t>(m) * p.N + ((row0 + lr) >> 1)] =
-                            gate / (1.0f + __expf(-gate)) * (up * T::kPrescale);
+                            gate / (1.0f + __expf(-gate)) * (up * kPre);
                     }
                 }
             } else if (q == 0 && lane_on && lr < nrows) {
@@ -721,10 +852,10 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
                     const uint32_t n = row - prob * N;
                     if (!row_ok) atomicOr(p.status, kDevBadExpert);
                     p.y[static_cast<int64_t>(prob) * p.N + n] =
-                        row_ok ? acc[0] * T::kPrescale : __int_as_float(0x7fc00000);
+                        row_ok ? acc[0] * kPre : __int_as_float(0x7fc00000);
                 } else {
 #pragma unroll
-                    for (int m = 0; m < M; ++m) p.y[static_cast<int64_t>(m) * p.N + row] = acc[m] * T::kPrescale;
+                    for (int m = 0; m < M; ++m) p.y[static_cast<int64_t>(m) * p.N + row] = acc[m] * kPre;
                 }
             }
 #pragma unroll
@@ -786,7 +917,32 @@ __global__ void __launch_bounds__(256) gemv_generic_kernel(const GemvParams p, i
                         acc[j] = 0.0f;
                     }
                 }
-                if (ok) {
+                if (ok && p.xq8) {
+                    // Q8_1 activations: each block's codes decided as the streaming
+                    // kernel decides them, then an integer dot per block.
+                    const uint8_t *wr = p.W + (e * p.N + n) * p.row_bytes;
+                    for (int64_t b = lane; b < nblk; b += 32) {
+                        const uint8_t *blk = wr + b * bb;
+                        const float dw = __half2float(__ushort_as_half(
+                            static_cast<unsigned short>(blk[0] | (blk[1] << 8))));
+#pragma unroll
+                        for (int mm = 0; mm < 8; ++mm) {
+                            if (m0 + mm >= M) continue;
+                            const __half *xb = p.x + (prob * M + m0 + mm) * p.K + b * 32;
+                            float amax = 0.0f;
+                            for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(__half2float(xb[j])));
+                            const float d = __fdiv_rn(amax, 127.0f);
+                            const float id = d != 0.0f ? __frcp_rn(d) : 0.0f;
+                            int s = 0;
+                            for (int j = 0; j < 32; ++j) {
+                                const int code = static_cast<int>(roundf(__fmul_rn(__half2float(xb[j]), id)));
+                                const int c = (j < 16 ? (blk[2 + j] & 0xF) : (blk[2 + j - 16] >> 4)) - 8;
+                                s += c * code;
+                            }
+                            acc[mm] = fmaf(static_cast<float>(s), dw * __half2float(__float2half_rn(d)), acc[mm]);
+                        }
+                    }
+                } else if (ok) {
                     const uint8_t *wr = (t == 1 ? p.W2 : p.W) + (e * p.N + n) * p.row_bytes;
                     for (int64_t b = lane; b < nblk; b += 32) {
                         const uint8_t *blk = wr + b * bb;

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstddef>
+#include <cstdint>
 #include <cuda_runtime.h>
 
 namespace qmv {
@@ -15,6 +16,12 @@ cudaError_t launch_gemv_stream_q4_0(int M, const GemvParams &p, int grid, int wa
 // Q4_0 with fp32 activations (plain and fused SwiGLU forms; p.xf set).
 cudaError_t launch_gemv_stream_q4_0_f32(int M, const GemvParams &p, int grid, int warps, size_t smem,
                                         cudaStream_t s, bool pdl);
+// Q4_0 against Q8_1-quantised activations (plain form only; p.xq8 set).
+cudaError_t launch_gemv_stream_q4_0_q8_1(int M, const GemvParams &p, int grid, int warps, size_t smem,
+                                         cudaStream_t s, bool pdl);
+// Q8_1 quantisation of fp16 activations [M][K] (K % 32 == 0, x 16-byte aligned).
+cudaError_t launch_quantize_q8_1(const void *x, int8_t *q, uint16_t *d_bits, int32_t *sumq, int64_t M, int64_t K,
+                                 cudaStream_t s);
 // Plain 2-bit (plain form only).
 cudaError_t launch_gemv_stream_q2w(int M, const GemvParams &p, int grid, int warps, size_t smem, cudaStream_t s,
                                    bool pdl);
