@@ -95,6 +95,30 @@ def test_decode_rule_lane_counts(orc, fmt, N, K, M):
     check(fmt, W, x, N, K, orc)
 
 
+# Eight tokens of K = 14336 in fp16 (235 KB) do not fit in shared memory beside
+# a weight ring: the call is split into launches over token subsets.
+@pytest.mark.parametrize("fmt", ["q4_0", "q8_0", "q2w"])
+@pytest.mark.parametrize("N,M", [(100, 8), (1029, 7), (37, 8)])
+def test_decode_token_split(orc, fmt, N, M):
+    K = 14336
+    W = synth.weights(fmt, N, K, seed=N + M)
+    x = synth.activations(M, K, seed=2 * N + M)
+    check(fmt, W, x, N, K, orc)
+
+
+def test_token_split_swiglu_and_fp32(cuda_lib, orc):
+    q = cuda_lib
+    N, K, M = 90, 14336, 8
+    Wg, Wu = _swiglu_tables(N, K, 360)
+    x = synth.activations(M, K, 361)
+    swiglu_check(Wg, Wu, x, N, K, orc)
+    xf = synth.activations(M, K, 362, dtype=np.float32)
+    y = q.qmv_q4_0_f32(dev(Wg), dev(xf))
+    torch.cuda.synchronize()
+    y_ref, S = orc.qmv(0, Wg, xf, N, K, nthreads=8)
+    assert H.normalised_error(y.cpu().numpy().astype(np.float64), y_ref, S) <= H.TOL
+
+
 @pytest.mark.parametrize("fmt", ["q4_0", "q8_0", "q2w"])
 @pytest.mark.parametrize("plant", ["large", "tiny"])
 @pytest.mark.parametrize("M", [1, 8])

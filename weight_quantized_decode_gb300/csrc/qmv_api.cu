@@ -160,7 +160,9 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
     // stacked row by row) is planned as one table of rows_total rows; the
     // multi-expert call by its per-expert shape.
     const int64_t Nplan = p.n_problems == 1 ? p.rows_total : p.N;
-    const TuneEntry *te = tune_lookup(fmt, Nplan, p.K, M);
+    // Q4_0 against Q8_1 activations has its own entries (table format 3): its
+    // per-unit arithmetic differs from the fp16 path's.
+    const TuneEntry *te = tune_lookup(p.xq8 ? 3 : fmt, Nplan, p.K, M);
 
     // defaults by rule
     const int64_t wbytes_per_sm = Nplan * (p.K / 256) * unit_bytes / (sms > 0 ? sms : 1);
@@ -243,6 +245,16 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
     return pl;
 }
 
+cudaError_t launch_streaming(int fmt, const GemvParams &p, int M, const Plan &pl, cudaStream_t stream, bool pdl)
+{
+    if (fmt == kQ4_0 && p.xq8) return launch_gemv_stream_q4_0_q8_1(M, p, pl.grid, pl.warps, pl.smem, stream, pdl);
+    if (fmt == kQ4_0)
+        return p.xf ? launch_gemv_stream_q4_0_f32(M, p, pl.grid, pl.warps, pl.smem, stream, pdl)
+                    : launch_gemv_stream_q4_0(M, p, pl.grid, pl.warps, pl.smem, stream, pdl);
+    if (fmt == kQ2W) return launch_gemv_stream_q2w(M, p, pl.grid, pl.warps, pl.smem, stream, pdl);
+    return launch_gemv_stream_q8_0(M, p, pl.grid, pl.warps, pl.smem, stream, pdl);
+}
+
 qmv_status run_gemv(int fmt, const void *W, const int32_t *idx, int64_t n_experts, const void *x, float *y,
                     int64_t N, int64_t K, int64_t M, int n_problems, cudaStream_t stream, const void *W2 = nullptr,
                     const float *xf = nullptr, bool xq8 = false)
@@ -275,17 +287,41 @@ qmv_status run_gemv(int fmt, const void *W, const int32_t *idx, int64_t n_expert
     const bool pdl = g_pdl.load(std::memory_order_relaxed) != 0;
 
     cudaError_t e;
+    GemvParams p0 = p;
     Plan pl = plan_gemv(fmt, p, Mk, sms, optin);
+    if (!pl.streaming && Mk > 1 && n_problems == 1) {
+        // The activations of all the tokens do not fit in shared memory beside
+        // a weight ring (e.g. 8 tokens of K = 14336 in fp16): split the tokens
+        // into the fewest launches whose activations fit.  Each launch streams
+        // the weights again, which is far cheaper than the generic kernel.
+        for (int parts = 2; parts <= Mk; ++parts) {
+            const int mc = (Mk + parts - 1) / parts;
+            GemvParams probe = p0;
+            if (!plan_gemv(fmt, probe, mc, sms, optin).streaming) continue;
+            for (int m0 = 0; m0 < Mk; m0 += mc) {
+                const int mm = Mk - m0 < mc ? Mk - m0 : mc;
+                GemvParams ps = p0;
+                if (ps.x) ps.x += static_cast<int64_t>(m0) * K;
+                if (ps.xf) ps.xf += static_cast<int64_t>(m0) * K;
+                ps.y += static_cast<int64_t>(m0) * N;
+                Plan pp = plan_gemv(fmt, ps, mm, sms, optin);
+                if (pp.streaming) {
+                    e = launch_streaming(fmt, ps, mm, pp, stream, pdl);
+                } else {   // not expected (fewer tokens than a part that fits), but correct
+                    int64_t grid = ((W2 ? N : ps.rows_total) + 7) / 8;
+                    if (grid > 32LL * sms) grid = 32LL * sms;
+                    e = launch_gemv_generic(fmt, ps, mm, static_cast<int>(grid < 1 ? 1 : grid), stream, pdl);
+                }
+                if (e != cudaSuccess) {
+                    (void)cudaGetLastError();
+                    return QMV_ERR_LAUNCH;
+                }
+            }
+            return QMV_OK;
+        }
+    }
     if (pl.streaming) {
-        if (fmt == kQ4_0 && xq8)
-            e = launch_gemv_stream_q4_0_q8_1(Mk, p, pl.grid, pl.warps, pl.smem, stream, pdl);
-        else if (fmt == kQ4_0)
-            e = xf ? launch_gemv_stream_q4_0_f32(Mk, p, pl.grid, pl.warps, pl.smem, stream, pdl)
-                   : launch_gemv_stream_q4_0(Mk, p, pl.grid, pl.warps, pl.smem, stream, pdl);
-        else if (fmt == kQ2W)
-            e = launch_gemv_stream_q2w(Mk, p, pl.grid, pl.warps, pl.smem, stream, pdl);
-        else
-            e = launch_gemv_stream_q8_0(Mk, p, pl.grid, pl.warps, pl.smem, stream, pdl);
+        e = launch_streaming(fmt, p, Mk, pl, stream, pdl);
     } else {
         const int64_t warps_needed = W2 ? N : p.rows_total;
         int64_t grid = (warps_needed + 7) / 8;
