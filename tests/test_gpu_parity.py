@@ -403,6 +403,11 @@ OVERRIDES = {
              "q81:q4_0:130:2560:1"],
     "G=3,SP=3": ["gemv:q4_0:41:2304:1", "gemv:q8_0:50:1536:4", "moe:q4_0:20:2304:3"],
     "G=12,warps=16": ["gemv:q4_0:90:3072:2", "gemv:q8_0:33:6144:1", "swiglu:q4_0:90:3072:2"],
+    # twelve warps per CTA at three or more tokens (384-thread instantiations)
+    "warps=12,G=4,SP=3": ["gemv:q4_0:300:4096:8", "gemv:q8_0:200:2048:5", "gemv:q2w:150:4096:6",
+                          "q81:q4_0:300:4096:8", "swiglu:q4_0:90:4096:8"],
+    "warps=12,stages=3,G=2": ["gemv:q4_0:1000:2048:3", "gemv:q8_0:77:6144:4", "gemv:q2w:640:2560:8",
+                              "q81:q4_0:515:2560:7", "swiglu:q4_0:300:2048:5"],
     # the fused SwiGLU keeps an even number of rows per group (G clamped to <= 16)
     "G=32": ["swiglu:q4_0:77:4096:1", "swiglu:q4_0:40:2048:8"],
 }

@@ -210,7 +210,7 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
     // distinct banks; any value works for G >= 8.
     p.SP = (SP >= 1 && SP <= 8 && ((SP & 1) || p.G >= 8)) ? SP : 1;
     if (share < 1 || share > 4) share = 1;
-    const int max_warps = (M <= 2) ? 16 : 8;
+    const int max_warps = (M <= 2) ? 16 : 12;
     if (warps < 1 || warps > max_warps) warps = 8;
 
     const int RG = 32 / p.G;
@@ -248,6 +248,7 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
 cudaError_t launch_streaming(int fmt, const GemvParams &p, int M, const Plan &pl, cudaStream_t stream, bool pdl)
 {
     if (fmt == kQ4_0 && p.xq8) return launch_gemv_stream_q4_0_q8_1(M, p, pl.grid, pl.warps, pl.smem, stream, pdl);
+    if (fmt == kQ4_0 && p.W2) return launch_gemv_stream_q4_0_swiglu(M, p, pl.grid, pl.warps, pl.smem, stream, pdl);
     if (fmt == kQ4_0)
         return p.xf ? launch_gemv_stream_q4_0_f32(M, p, pl.grid, pl.warps, pl.smem, stream, pdl)
                     : launch_gemv_stream_q4_0(M, p, pl.grid, pl.warps, pl.smem, stream, pdl);

@@ -22,6 +22,8 @@ static cudaError_t launch_q2w_one(const GemvParams &p, int grid, int warps, size
     if (warps <= 8) return launch_q2w_t<M, 256>(p, grid, warps, smem, s, pdl);
     if constexpr (M <= 2) {
         if (warps <= 16) return launch_q2w_t<M, 512>(p, grid, warps, smem, s, pdl);
+    } else {
+        if (warps <= 12) return launch_q2w_t<M, 384>(p, grid, warps, smem, s, pdl);
     }
     return cudaErrorInvalidConfiguration;
 }

@@ -18,44 +18,46 @@ static cudaError_t launch_q4_t(const GemvParams &p, int grid, int warps, size_t 
 }
 
 // Up to 8 warps per CTA for every token count; up to 16 (at most 128
-// registers a thread) for one or two tokens.
-template <int M, bool XF32>
+// registers a thread) for one or two tokens, up to 12 (at most 168) for three
+// or more: with eight tokens the staged activations leave room for one CTA per
+// SM, and its warps are all the latency hiding there is.
+// SW selects the instantiations of one translation unit: the fused SwiGLU
+// form, or the plain and multi-expert forms.
+template <int M, bool XF32, bool SW>
 static cudaError_t launch_q4_one(const GemvParams &p, int grid, int warps, size_t smem, cudaStream_t s, bool pdl)
 {
-    if (p.expert_idx) {
-        if constexpr (M == 1 && !XF32) {
-            if (warps <= 8) return launch_q4_t<1, 256, true, false, false>(p, grid, warps, smem, s, pdl);
-            if (warps <= 16) return launch_q4_t<1, 512, true, false, false>(p, grid, warps, smem, s, pdl);
+    if ((p.W2 != nullptr) != SW) return cudaErrorInvalidValue;
+    if constexpr (!SW) {
+        if (p.expert_idx) {
+            if constexpr (M == 1 && !XF32) {
+                if (warps <= 8) return launch_q4_t<1, 256, true, false, false>(p, grid, warps, smem, s, pdl);
+                if (warps <= 16) return launch_q4_t<1, 512, true, false, false>(p, grid, warps, smem, s, pdl);
+            }
+            return cudaErrorInvalidConfiguration;
         }
-        return cudaErrorInvalidConfiguration;
     }
-    if (p.W2) {   // fused gate + up + SwiGLU
-        if (warps <= 8) return launch_q4_t<M, 256, false, true, XF32>(p, grid, warps, smem, s, pdl);
-        if constexpr (M <= 2) {
-            if (warps <= 16) return launch_q4_t<M, 512, false, true, XF32>(p, grid, warps, smem, s, pdl);
-        }
-        return cudaErrorInvalidConfiguration;
-    }
-    if (warps <= 8) return launch_q4_t<M, 256, false, false, XF32>(p, grid, warps, smem, s, pdl);
+    if (warps <= 8) return launch_q4_t<M, 256, false, SW, XF32>(p, grid, warps, smem, s, pdl);
     if constexpr (M <= 2) {
-        if (warps <= 16) return launch_q4_t<M, 512, false, false, XF32>(p, grid, warps, smem, s, pdl);
+        if (warps <= 16) return launch_q4_t<M, 512, false, SW, XF32>(p, grid, warps, smem, s, pdl);
+    } else {
+        if (warps <= 12) return launch_q4_t<M, 384, false, SW, XF32>(p, grid, warps, smem, s, pdl);
     }
     return cudaErrorInvalidConfiguration;
 }
 
-template <bool XF32>
+template <bool XF32, bool SW>
 static cudaError_t launch_q4_by_m(int M, const GemvParams &p, int grid, int warps, size_t smem, cudaStream_t s,
                                   bool pdl)
 {
     switch (M) {
-    case 1: return launch_q4_one<1, XF32>(p, grid, warps, smem, s, pdl);
-    case 2: return launch_q4_one<2, XF32>(p, grid, warps, smem, s, pdl);
-    case 3: return launch_q4_one<3, XF32>(p, grid, warps, smem, s, pdl);
-    case 4: return launch_q4_one<4, XF32>(p, grid, warps, smem, s, pdl);
-    case 5: return launch_q4_one<5, XF32>(p, grid, warps, smem, s, pdl);
-    case 6: return launch_q4_one<6, XF32>(p, grid, warps, smem, s, pdl);
-    case 7: return launch_q4_one<7, XF32>(p, grid, warps, smem, s, pdl);
-    case 8: return launch_q4_one<8, XF32>(p, grid, warps, smem, s, pdl);
+    case 1: return launch_q4_one<1, XF32, SW>(p, grid, warps, smem, s, pdl);
+    case 2: return launch_q4_one<2, XF32, SW>(p, grid, warps, smem, s, pdl);
+    case 3: return launch_q4_one<3, XF32, SW>(p, grid, warps, smem, s, pdl);
+    case 4: return launch_q4_one<4, XF32, SW>(p, grid, warps, smem, s, pdl);
+    case 5: return launch_q4_one<5, XF32, SW>(p, grid, warps, smem, s, pdl);
+    case 6: return launch_q4_one<6, XF32, SW>(p, grid, warps, smem, s, pdl);
+    case 7: return launch_q4_one<7, XF32, SW>(p, grid, warps, smem, s, pdl);
+    case 8: return launch_q4_one<8, XF32, SW>(p, grid, warps, smem, s, pdl);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -28,6 +28,8 @@ static cudaError_t launch_one(const GemvParams &p, int grid, int warps, size_t s
     if (warps <= 8) return launch_t<M, 256, false>(p, grid, warps, smem, s, pdl);
     if constexpr (M <= 2) {
         if (warps <= 16) return launch_t<M, 512, false>(p, grid, warps, smem, s, pdl);
+    } else {
+        if (warps <= 12) return launch_t<M, 384, false>(p, grid, warps, smem, s, pdl);
     }
     return cudaErrorInvalidConfiguration;
 }

@@ -13,7 +13,12 @@ struct GemvParams;
 // Streaming decode kernel for one format and token count M (1..8).
 cudaError_t launch_gemv_stream_q4_0(int M, const GemvParams &p, int grid, int warps, size_t smem,
                                     cudaStream_t s, bool pdl);
-// Q4_0 with fp32 activations (plain and fused SwiGLU forms; p.xf set).
+// Q4_0 fused gate + up + SwiGLU (p.W2 set; fp16, or fp32 activations with p.xf).
+cudaError_t launch_gemv_stream_q4_0_swiglu(int M, const GemvParams &p, int grid, int warps, size_t smem,
+                                           cudaStream_t s, bool pdl);
+cudaError_t launch_gemv_stream_q4_0_swiglu_f32(int M, const GemvParams &p, int grid, int warps, size_t smem,
+                                               cudaStream_t s, bool pdl);
+// Q4_0 with fp32 activations (plain form; p.xf set).
 cudaError_t launch_gemv_stream_q4_0_f32(int M, const GemvParams &p, int grid, int warps, size_t smem,
                                         cudaStream_t s, bool pdl);
 // Q4_0 against Q8_1-quantised activations (plain form only; p.xq8 set).
