@@ -168,7 +168,10 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
     const int64_t wbytes_per_sm = Nplan * (p.K / 256) * unit_bytes / (sms > 0 ? sms : 1);
     const bool big = wbytes_per_sm > 128 * 1024 && M <= 2;
     int G = lanes_per_row(p.U, M, Nplan, sms);
-    int warps = big ? 12 : 8;
+    // 12 warps for large tables at one or two tokens, and for three or more
+    // tokens (one CTA per SM: its warps are the latency hiding; measured on the
+    // Llama-3-8B and Q8_0 tables at 4 and 8 tokens)
+    int warps = (big || M > 2) ? 12 : 8;
     int stages = 2;
     int SP = 1;
     int share = 1;
