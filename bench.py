@@ -75,6 +75,11 @@ WORKLOADS = {
     "q4_0_q8_1": {"kind": "gemv", "fmt": "q4_0", "x": "q8_1", "M": [1, 8], "dtype": "i8",
                   "shapes": [(4096, 4096), (6144, 4096), (4096, 14336), (14336, 4096), (28672, 4096),
                              (128256, 4096)]},
+    # The same tables in the two steps of the sm8x kernel and llama.cpp: the
+    # activations to Q8_1 (one launch), then the int8 product on them (another).
+    "q4_0_q8_1_pre": {"kind": "gemv", "fmt": "q4_0", "x": "q8_1_pre", "M": [1, 8], "dtype": "i8",
+                      "shapes": [(4096, 4096), (6144, 4096), (4096, 14336), (14336, 4096), (28672, 4096),
+                                 (128256, 4096)]},
     # Plain 2-bit (codes -2..1, fp16 scale per 32): the bakeoff's six one-token
     # tables (volta-kernel-bakeoff, "Results (one token, microseconds, lower is
     # better)", its 2-bit column).
@@ -91,8 +96,8 @@ def metric_name(workload):
         return "Q4_0 prefill GEMM TFLOP/s (fp16 tensor cores; us/call per table in 'sweep')"
     if wl["kind"] == "moe":
         return "Q4_0 multi-expert GEMV (one launch) HBM GB/s (algorithmic bytes; us/call per config in 'sweep')"
-    xin = {"f32": " (fp32 activations in)", "q8_1": " (activations quantised to Q8_1 in the kernel, int8 dots)"}.get(
-        wl.get("x"), "")
+    xin = {"f32": " (fp32 activations in)", "q8_1": " (activations quantised to Q8_1 in the kernel, int8 dots)",
+           "q8_1_pre": " (activations quantised to Q8_1 by a launch of their own, then int8 dots)"}.get(wl.get("x"), "")
     if wl["kind"] == "swiglu":
         return (f"Q4_0 fused gate+up+SwiGLU{xin} HBM GB/s (algorithmic bytes of both tables; "
                 "us/call per table in 'sweep')")
@@ -271,6 +276,7 @@ def run_ours(args, dist, rank, local, world):
             fn_ptr = q.qmv_q4_0_f32_ptr
         if wl.get("x") == "q8_1":
             fn_ptr = q.qmv_q4_0_q8_1_ptr
+        pre = wl.get("x") == "q8_1_pre"
         for (N, K) in wl["shapes"]:
             Wd, copies = rotated_copies(N, K, f"{fmt}_{N}x{K}")
             for M in wl["M"]:
@@ -281,9 +287,22 @@ def run_ours(args, dist, rank, local, world):
                      "y_host": torch.empty((M, N), dtype=torch.float32).pin_memory(),
                      "bytes": algo_bytes(fmt, N, K, M, xb), "flops": 2 * M * N * K}
 
-                def call(s, c=c):
-                    W = c["W"][s % c["copies"]]
-                    fn_ptr(W.data_ptr(), c["x"].data_ptr(), c["y"].data_ptr(), c["N"], c["K"], c["M"], sh)
+                if pre:   # Q8_1 buffers for the activations, written by the quantisation launch
+                    c["xq"] = torch.empty((M, K), dtype=torch.int8, device=dev)
+                    c["xq_d"] = torch.empty((M, K // 32), dtype=torch.int16, device=dev)
+                    c["xq_s"] = torch.empty((M, K // 32), dtype=torch.int32, device=dev)
+                    c["launches"] = 2
+
+                    def call(s, c=c):
+                        W = c["W"][s % c["copies"]]
+                        q.qmv_quantize_q8_1_ptr(c["x"].data_ptr(), c["xq"].data_ptr(), c["xq_d"].data_ptr(),
+                                                c["xq_s"].data_ptr(), c["M"], c["K"], sh)
+                        q.qmv_q4_0_q8_1_pre_ptr(W.data_ptr(), c["xq"].data_ptr(), c["xq_d"].data_ptr(),
+                                                c["xq_s"].data_ptr(), c["y"].data_ptr(), c["N"], c["K"], c["M"], sh)
+                else:
+                    def call(s, c=c):
+                        W = c["W"][s % c["copies"]]
+                        fn_ptr(W.data_ptr(), c["x"].data_ptr(), c["y"].data_ptr(), c["N"], c["K"], c["M"], sh)
                 c["call"] = call
                 calls.append(c)
     elif kind == "swiglu":
@@ -356,7 +375,7 @@ def run_ours(args, dist, rank, local, world):
 
     step_bytes = sum(c["bytes"] for c in calls)
     step_flops = sum(c["flops"] for c in calls)
-    launches_per_step = len(calls)
+    launches_per_step = sum(c.get("launches", 1) for c in calls)
 
     # one eager pass (module loading, shared-memory opt-in) before any capture
     with torch.cuda.stream(stream):
@@ -582,7 +601,7 @@ def oracle_tasks(workload):
                 e = int(idx[sl])
                 jobs.append((pool[e * N:(e + 1) * N], x[sl:sl + 1], N, K, 1))
 
-    q81 = wl.get("x") == "q8_1"
+    q81 = wl.get("x") in ("q8_1", "q8_1_pre")
 
     def run(frac):
         b = f = 0

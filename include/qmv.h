@@ -137,6 +137,21 @@ QMV_API qmv_status qmv_quantize_q8_1(const void *x, int8_t *q, uint16_t *d_bits,
                              int64_t M, int64_t K, qmv_stream_t stream);
 
 /*
+ * qmv_q4_0_q8_1 with the activations already in Q8_1 (as qmv_quantize_q8_1
+ * writes them): the two steps of the sm8x kernel and llama.cpp, quantise once
+ * and then take the int8 dot against several tables that share the
+ * activations.  The result equals qmv_q4_0_q8_1 on the fp16 activations those
+ * blocks came from, bit for bit.
+ *   q      : DEVICE int8 [M][K], 16-byte aligned (K % 256 == 0 for the
+ *            streaming kernel; other K run the generic kernel).
+ *   d_bits : DEVICE uint16 [M][K/32] (fp16 scales), 2-byte aligned.
+ *   sumq   : DEVICE int32 [M][K/32] (code sums), 4-byte aligned.
+ *   W, y, N, K, M (<= 8), errors and asynchrony as for qmv_q4_0.
+ */
+QMV_API qmv_status qmv_q4_0_q8_1_pre(const void *W, const int8_t *q, const uint16_t *d_bits, const int32_t *sumq,
+                             float *y, int64_t N, int64_t K, int64_t M, qmv_stream_t stream);
+
+/*
  * Plain 2-bit decode GEMV (the bakeoff's q2w format: codes -2..1 with one fp16
  * scale per 32 weights, 2.5 bits per weight -- volta-kernel-bakeoff, "What's
  * in the race" and the Results table's 2-bit column), same contract as

@@ -32,7 +32,8 @@ def lib():
 def test_header_declares_the_boundary():
     names = set(_declared())
     for n in ("qmv_q4_0", "qmv_q8_0", "qmv_moe", "qmm_q4_0_prefill", "qmv_device_status", "qmv_q4_0_swiglu",
-              "qmv_q4_0_f32", "qmv_q4_0_swiglu_f32", "qmv_q2w", "qmv_q4_0_q8_1", "qmv_quantize_q8_1"):
+              "qmv_q4_0_f32", "qmv_q4_0_swiglu_f32", "qmv_q2w", "qmv_q4_0_q8_1", "qmv_quantize_q8_1",
+              "qmv_q4_0_q8_1_pre"):
         assert n in names
 
 
@@ -105,6 +106,20 @@ def test_host_validation_quantize_q8_1(lib):
     assert f(FAKE, FAKE, FAKE, FAKE, -1, 256, None) == 3
     assert f(None, None, None, None, 0, 256, None) == 0           # empty
     assert f(None, None, None, None, 2, 0, None) == 0
+
+
+def test_host_validation_q8_1_pre(lib):
+    f = lib.qmv_q4_0_q8_1_pre
+    assert f(None, FAKE, FAKE, FAKE, FAKE, 8, 256, 1, None) == 1     # NULL W
+    assert f(FAKE, None, FAKE, FAKE, FAKE, 8, 256, 1, None) == 1     # NULL codes
+    assert f(FAKE, FAKE, None, FAKE, FAKE, 8, 256, 1, None) == 1     # NULL scales
+    assert f(FAKE, FAKE, FAKE, None, FAKE, 8, 256, 1, None) == 1     # NULL sums
+    assert f(FAKE, FAKE, FAKE, FAKE, None, 8, 256, 1, None) == 1     # NULL y
+    assert f(FAKE, FAKE, FAKE + 1, FAKE, FAKE, 8, 256, 1, None) == 2  # scales misaligned
+    assert f(FAKE, FAKE, FAKE, FAKE + 2, FAKE, 8, 256, 1, None) == 2  # sums misaligned
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 250, 1, None) == 3     # K % 32
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 256, 9, None) == 3     # M <= 8
+    assert f(None, None, None, None, None, 0, 256, 1, None) == 0     # empty
 
 
 def test_host_validation_moe(lib):

@@ -196,3 +196,33 @@ def test_q8_1_unaligned_x_empty_and_sabotage(cuda_lib, orc):
     qo, do, _ = orc.quantize_q8_1(x)
     yr, S = orc.qmv_q8_1(0, W, qo, do, N, K, nthreads=8)
     assert H.normalised_error(yb, yr, S) > 20 * H.TOL
+
+
+# -- activations quantised once, then the product (qmv_q4_0_q8_1_pre) ---------------------
+
+@pytest.mark.parametrize("N,K,M", [(1000, 2048, 1), (515, 2560, 5), (4096, 4096, 8), (45, 640, 3), (300, 14336, 8),
+                                   (77, 96, 2)])
+def test_prequantised_equals_fused(cuda_lib, orc, N, K, M):
+    q = cuda_lib
+    W = dev(synth.q4_0_weights(N, K, 760 + K))
+    x = dev(special_activations(M, K, 761 + N))
+    qc, qd, qs = q.qmv_quantize_q8_1(x)
+    y_pre = q.qmv_q4_0_q8_1_pre(W, qc, qd, qs)
+    y_fused = q.qmv_q4_0_q8_1(W, x)
+    torch.cuda.synchronize()
+    assert torch.equal(y_pre, y_fused)
+
+
+def test_prequantised_two_tables_share_one_quantisation(cuda_lib, orc):
+    q = cuda_lib
+    K, M = 4096, 4
+    x = synth.activations(M, K, 770)
+    qc, qd, qs = q.qmv_quantize_q8_1(dev(x))
+    qo, do, _ = orc.quantize_q8_1(x)
+    for N, seed in ((6144, 771), (1024, 772)):
+        W = synth.q4_0_weights(N, K, seed)
+        y = q.qmv_q4_0_q8_1_pre(dev(W), qc, qd, qs)
+        torch.cuda.synchronize()
+        rows = sample_rows(N)
+        yr, S = orc.qmv_q8_1(0, W, qo, do, N, K, rows=rows, nthreads=8)
+        assert H.normalised_error(y.cpu().numpy().astype(np.float64)[:, rows], yr, S) <= TIGHT

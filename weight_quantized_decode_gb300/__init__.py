@@ -14,6 +14,7 @@ Functions (same names as the C ABI):
     qmv_q2w(W, x, y=None, stream=None)           -> plain 2-bit weights, y fp32 [M, N]
     qmv_q4_0_q8_1(W, x, y=None, stream=None)     -> Q4_0 against Q8_1-quantised x (integer dots)
     qmv_quantize_q8_1(x, stream=None)            -> (q, d_bits, sumq) of the Q8_1 activations
+    qmv_q4_0_q8_1_pre(W, q, d_bits, sumq, ...)   -> the Q8_1 product on activations already quantised
     qmv_moe(W_pool, expert_idx, n_experts, x, N, y=None, stream=None)
     qmm_q4_0_prefill(W, x, y=None, stream=None)  -> y fp32 [M, N]
     qmv_device_status(stream=None)               -> int (QMV_DEV_* bits, cleared)
@@ -65,6 +66,8 @@ def lib():
         L.qmv_moe.argtypes = [vp, vp, i64, vp, vp, i64, i64, i64, vp]
         L.qmv_q4_0_swiglu.restype = ctypes.c_int
         L.qmv_q4_0_swiglu.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
+        L.qmv_q4_0_q8_1_pre.restype = ctypes.c_int
+        L.qmv_q4_0_q8_1_pre.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, vp]
         L.qmv_quantize_q8_1.restype = ctypes.c_int
         L.qmv_quantize_q8_1.argtypes = [vp, vp, vp, vp, i64, i64, vp]
         L.qmv_q4_0_swiglu_f32.restype = ctypes.c_int
@@ -124,6 +127,11 @@ def qmv_q8_0_ptr(W: int, x: int, y: int, N: int, K: int, M: int, stream: int = 0
 
 def qmv_q4_0_q8_1_ptr(W: int, x: int, y: int, N: int, K: int, M: int, stream: int = 0) -> None:
     _check("qmv_q4_0_q8_1", lib().qmv_q4_0_q8_1(W, x, y, N, K, M, stream))
+
+
+def qmv_q4_0_q8_1_pre_ptr(W: int, q: int, d_bits: int, sumq: int, y: int, N: int, K: int, M: int,
+                          stream: int = 0) -> None:
+    _check("qmv_q4_0_q8_1_pre", lib().qmv_q4_0_q8_1_pre(W, q, d_bits, sumq, y, N, K, M, stream))
 
 
 def qmv_quantize_q8_1_ptr(x: int, q: int, d_bits: int, sumq: int, M: int, K: int, stream: int = 0) -> None:
@@ -238,6 +246,30 @@ def qmv_q4_0_q8_1(W, x, y=None, stream=None):
     """qmv_q4_0 with the activations quantised to Q8_1 in the kernel (integer dots)."""
     W, x, y, N, K, M = _prep(W, x, y, Q4_0_BLOCK_BYTES, "qmv_q4_0_q8_1")
     qmv_q4_0_q8_1_ptr(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, _stream_handle(stream))
+    return y
+
+
+def qmv_q4_0_q8_1_pre(W, q, d_bits, sumq, y=None, stream=None):
+    """qmv_q4_0_q8_1 on activations already in Q8_1 (q int8 [M, K], d_bits int16
+    [M, K/32], sumq int32 [M, K/32], as qmv_quantize_q8_1 returns them)."""
+    torch = _torch()
+    if not (W.is_cuda and q.is_cuda and d_bits.is_cuda and sumq.is_cuda):
+        raise TypeError("qmv_q4_0_q8_1_pre: all tensors must be on a CUDA device (no CPU path)")
+    if W.dtype != torch.uint8 or q.dtype != torch.int8 or d_bits.dtype != torch.int16 or sumq.dtype != torch.int32:
+        raise TypeError("qmv_q4_0_q8_1_pre: W uint8, q int8, d_bits int16, sumq int32")
+    if q.dim() == 1:
+        q = q.unsqueeze(0)
+    M, K = q.shape
+    if K % 32 or d_bits.numel() != M * (K // 32) or sumq.numel() != M * (K // 32):
+        raise ValueError("qmv_q4_0_q8_1_pre: q [M, K] with K % 32 == 0, d_bits and sumq [M, K/32]")
+    if not (W.is_contiguous() and q.is_contiguous() and d_bits.is_contiguous() and sumq.is_contiguous()):
+        raise ValueError("qmv_q4_0_q8_1_pre: tensors must be contiguous")
+    row_bytes = (K // 32) * Q4_0_BLOCK_BYTES
+    N = W.numel() // row_bytes if row_bytes else 0
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=q.device)
+    qmv_q4_0_q8_1_pre_ptr(W.data_ptr(), q.data_ptr(), d_bits.data_ptr(), sumq.data_ptr(), y.data_ptr(), N, K, M,
+                          _stream_handle(stream))
     return y
 
 

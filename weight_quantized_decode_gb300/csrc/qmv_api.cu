@@ -147,8 +147,9 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
 {
     Plan pl{false, 0, 8, 0};
     if (p.K % 256 != 0 || p.K == 0) return pl;
-    // staged with 4-byte (fp16 pairs) or 8-byte (fp32 pairs) loads of 16-byte-aligned rows
-    const uintptr_t xaddr = p.xf ? reinterpret_cast<uintptr_t>(p.xf) : reinterpret_cast<uintptr_t>(p.x);
+    // staged with 4-byte (fp16 pairs), 8-byte (fp32 pairs) or 16-byte (codes) loads of 16-byte-aligned rows
+    const uintptr_t xaddr = p.xq ? reinterpret_cast<uintptr_t>(p.xq)
+                                 : (p.xf ? reinterpret_cast<uintptr_t>(p.xf) : reinterpret_cast<uintptr_t>(p.x));
     if (xaddr % 16 != 0) return pl;
     if (p.rows_total >= (int64_t(1) << 31)) return pl;             // 32-bit row indices
     const int64_t U = p.K / 256;
@@ -261,7 +262,8 @@ cudaError_t launch_streaming(int fmt, const GemvParams &p, int M, const Plan &pl
 
 qmv_status run_gemv(int fmt, const void *W, const int32_t *idx, int64_t n_experts, const void *x, float *y,
                     int64_t N, int64_t K, int64_t M, int n_problems, cudaStream_t stream, const void *W2 = nullptr,
-                    const float *xf = nullptr, bool xq8 = false)
+                    const float *xf = nullptr, bool xq8 = false, const int8_t *xq = nullptr,
+                    const uint16_t *xq_d = nullptr, const int32_t *xq_s = nullptr)
 {
     if (xf && fmt != kQ4_0) return QMV_ERR_SHAPE;   // fp32 activations: Q4_0 kernels only
     int dev = 0;
@@ -275,6 +277,9 @@ qmv_status run_gemv(int fmt, const void *W, const int32_t *idx, int64_t n_expert
     p.x = static_cast<const __half *>(x);
     p.xf = xf;
     p.xq8 = xq8 ? 1 : 0;
+    p.xq = xq;
+    p.xq_d = xq_d;
+    p.xq_s = xq_s;
     p.y = y;
     p.expert_idx = idx;
     p.N = N;
@@ -307,6 +312,11 @@ qmv_status run_gemv(int fmt, const void *W, const int32_t *idx, int64_t n_expert
                 GemvParams ps = p0;
                 if (ps.x) ps.x += static_cast<int64_t>(m0) * K;
                 if (ps.xf) ps.xf += static_cast<int64_t>(m0) * K;
+                if (ps.xq) {
+                    ps.xq += static_cast<int64_t>(m0) * K;
+                    ps.xq_d += static_cast<int64_t>(m0) * (K / 32);
+                    ps.xq_s += static_cast<int64_t>(m0) * (K / 32);
+                }
                 ps.y += static_cast<int64_t>(m0) * N;
                 Plan pp = plan_gemv(fmt, ps, mm, sms, optin);
                 if (pp.streaming) {
@@ -418,6 +428,17 @@ qmv_status qmv_q4_0_q8_1(const void *W, const void *x, float *y, int64_t N, int6
     if (st != QMV_OK || N == 0 || M == 0) return st;
     return run_gemv(kQ4_0, W, nullptr, 1, x, y, N, K, M, 1, reinterpret_cast<cudaStream_t>(stream), nullptr,
                     nullptr, true);
+}
+
+qmv_status qmv_q4_0_q8_1_pre(const void *W, const int8_t *q, const uint16_t *d_bits, const int32_t *sumq, float *y,
+                             int64_t N, int64_t K, int64_t M, qmv_stream_t stream)
+{
+    qmv_status st = check_common(W, q, y, N, K, M, 8);
+    if (st != QMV_OK || N == 0 || M == 0) return st;
+    if (K > 0 && (!d_bits || !sumq)) return QMV_ERR_NULL;
+    if ((d_bits && !aligned(d_bits, 2)) || (sumq && !aligned(sumq, 4))) return QMV_ERR_ALIGN;
+    return run_gemv(kQ4_0, W, nullptr, 1, nullptr, y, N, K, M, 1, reinterpret_cast<cudaStream_t>(stream), nullptr,
+                    nullptr, true, q, d_bits, sumq);
 }
 
 qmv_status qmv_quantize_q8_1(const void *x, int8_t *q, uint16_t *d_bits, int32_t *sumq, int64_t M, int64_t K,

@@ -95,6 +95,9 @@ struct GemvParams {
     int SP;                      // passes per stage (odd)
     int S;                       // stages in each warp's ring
     int xq8;                     // Q4_0 against Q8_1-quantised activations (integer dots)
+    const int8_t *xq;            // activations already in Q8_1 (codes [M][K]); else quantised in the kernel
+    const uint16_t *xq_d;        //   their fp16 scales' bits [M][K/32]
+    const int32_t *xq_s;         //   and code sums [M][K/32]
     int *status;                 // device status word
 };
 
@@ -571,7 +574,27 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
     // to kStageItems per thread per round with all their loads in flight, so
     // several tokens cost few L2 round trips (one token of a plain call keeps
     // two items per round: fewer registers live ahead of the main loop).
-    if constexpr (XQ8) {
+    if (XQ8 && p.xq) {
+        // Activations already in Q8_1: copy the codes (16 per load) and the
+        // blocks' (scale, 8 * code sum) into the staged layout.
+        const int chunks = static_cast<int>(p.K / 16);
+        for (int it = threadIdx.x; it < M * chunks; it += blockDim.x) {
+            const int tok = it / chunks, c = it - tok * chunks;
+            const int blk = c >> 1;
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.xq + static_cast<int64_t>(tok) * p.K) + c);
+            *reinterpret_cast<uint4 *>(xs + static_cast<size_t>(tok) * U * XUB + (blk >> 3) * XUB + (blk & 7) * 32 +
+                                       (c & 1) * 16) = v;
+        }
+        const int nb = static_cast<int>(p.K / 32);
+        for (int it = threadIdx.x; it < M * nb; it += blockDim.x) {
+            const int tok = it / nb, blk = it - tok * nb;
+            const int64_t j = static_cast<int64_t>(tok) * nb + blk;
+            const float dxq = __half2float(__ushort_as_half(__ldg(p.xq_d + j)));
+            *reinterpret_cast<float2 *>(xs + static_cast<size_t>(tok) * U * XUB + (blk >> 3) * XUB + 256 +
+                                        (blk & 7) * 8) = make_float2(dxq, __int_as_float(8 * __ldg(p.xq_s + j)));
+        }
+        for (int i = early; i < prefetch; ++i) issue_next();
+    } else if constexpr (XQ8) {
         // Q8_1: each item is a 16-byte chunk of 8 activations, read with one
         // load; the four chunks of a 32-block sit in four adjacent lanes of one
         // round (chunks per token and the round are multiples of 4), which
@@ -928,18 +951,30 @@ __global__ void __launch_bounds__(256) gemv_generic_kernel(const GemvParams p, i
 #pragma unroll
                         for (int mm = 0; mm < 8; ++mm) {
                             if (m0 + mm >= M) continue;
-                            const __half *xb = p.x + (prob * M + m0 + mm) * p.K + b * 32;
-                            float amax = 0.0f;
-                            for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(__half2float(xb[j])));
-                            const float d = __fdiv_rn(amax, 127.0f);
-                            const float id = d != 0.0f ? __frcp_rn(d) : 0.0f;
+                            const int64_t tok = prob * M + m0 + mm;
                             int s = 0;
-                            for (int j = 0; j < 32; ++j) {
-                                const int code = static_cast<int>(roundf(__fmul_rn(__half2float(xb[j]), id)));
-                                const int c = (j < 16 ? (blk[2 + j] & 0xF) : (blk[2 + j - 16] >> 4)) - 8;
-                                s += c * code;
+                            float dxq;
+                            if (p.xq) {   // activations already in Q8_1
+                                const int8_t *qb = p.xq + tok * p.K + b * 32;
+                                for (int j = 0; j < 32; ++j) {
+                                    const int c = (j < 16 ? (blk[2 + j] & 0xF) : (blk[2 + j - 16] >> 4)) - 8;
+                                    s += c * qb[j];
+                                }
+                                dxq = __half2float(__ushort_as_half(p.xq_d[tok * (p.K / 32) + b]));
+                            } else {
+                                const __half *xb = p.x + tok * p.K + b * 32;
+                                float amax = 0.0f;
+                                for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(__half2float(xb[j])));
+                                const float d = __fdiv_rn(amax, 127.0f);
+                                const float id = d != 0.0f ? __frcp_rn(d) : 0.0f;
+                                for (int j = 0; j < 32; ++j) {
+                                    const int code = static_cast<int>(roundf(__fmul_rn(__half2float(xb[j]), id)));
+                                    const int c = (j < 16 ? (blk[2 + j] & 0xF) : (blk[2 + j - 16] >> 4)) - 8;
+                                    s += c * code;
+                                }
+                                dxq = __half2float(__float2half_rn(d));
                             }
-                            acc[mm] = fmaf(static_cast<float>(s), dw * __half2float(__float2half_rn(d)), acc[mm]);
+                            acc[mm] = fmaf(static_cast<float>(s), dw * dxq, acc[mm]);
                         }
                     }
                 } else if (ok) {
