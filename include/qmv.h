@@ -132,6 +132,9 @@ QMV_API qmv_status qmv_q4_0_q8_1(const void *W, const void *x, float *y,
  *   sumq   : DEVICE int32 [M][K/32] (4-byte aligned), each block's code sum.
  * (llama.cpp's Q8_1 block stores d and d * sum(q) beside its 32 codes; these
  * are the same quantities in three plain arrays.)
+ * Asynchronous on `stream`; with programmatic dependent launch on, the next
+ * call of this library may start streaming its weights while this one runs and
+ * reads the codes only after it has completed.
  */
 QMV_API qmv_status qmv_quantize_q8_1(const void *x, int8_t *q, uint16_t *d_bits, int32_t *sumq,
                              int64_t M, int64_t K, qmv_stream_t stream);
@@ -256,8 +259,9 @@ QMV_API qmv_status qmm_q4_0_prefill(const void *W, const void *x, float *y,
  */
 QMV_API qmv_status qmv_device_status(qmv_stream_t stream, int32_t *out);
 
-/* Programmatic dependent launch for the decode and prefill kernels: 1 = on
- * (default), 0 = off (plain stream order).  Process-wide; affects later calls. */
+/* Programmatic dependent launch for the decode, prefill and Q8_1 quantisation
+ * kernels: 1 = on (default), 0 = off (plain stream order).  Process-wide;
+ * affects later calls. */
 QMV_API void qmv_set_pdl(int enable);
 
 /* Static description of a status code. */

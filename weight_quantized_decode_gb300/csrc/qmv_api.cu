@@ -450,7 +450,8 @@ qmv_status qmv_quantize_q8_1(const void *x, int8_t *q, uint16_t *d_bits, int32_t
     if (!aligned(x, 16) || !aligned(q, 8) || !aligned(d_bits, 2) || !aligned(sumq, 4)) return QMV_ERR_ALIGN;
     int dev = 0;
     if (current_device(&dev) != cudaSuccess) return QMV_ERR_CUDA;
-    if (launch_quantize_q8_1(x, q, d_bits, sumq, M, K, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    if (launch_quantize_q8_1(x, q, d_bits, sumq, M, K, reinterpret_cast<cudaStream_t>(stream),
+                             g_pdl.load(std::memory_order_relaxed) != 0) != cudaSuccess) {
         (void)cudaGetLastError();
         return QMV_ERR_LAUNCH;
     }

@@ -48,9 +48,14 @@ cudaError_t launch_gemv_stream_q4_0_q8_1(int M, const GemvParams &p, int grid, i
 // One thread per 16-byte chunk of 8 activations; the four chunks of a block
 // are adjacent lanes (the chunk count is a multiple of 4 and so is every
 // warp's first chunk).  Lanes past the end take part in the shuffles only.
+// Programmatic dependent launch: the next kernel (a product on these codes)
+// may start streaming its weights at once, and waits for this grid before it
+// reads the codes; this grid waits for the previous one before it reads x.
 __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const uint4 *x, int8_t *q, uint16_t *d_bits,
                                                            int32_t *sumq, int64_t nchunks)
 {
+    pdl_allow_next_grid();
+    pdl_wait_prior_grid();
     const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const bool ok = c < nchunks;
     const uint4 v = ok ? __ldg(x + c) : make_uint4(0u, 0u, 0u, 0u);
@@ -67,14 +72,13 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const uint4 *x, int8
 }
 
 cudaError_t launch_quantize_q8_1(const void *x, int8_t *q, uint16_t *d_bits, int32_t *sumq, int64_t M, int64_t K,
-                                 cudaStream_t s)
+                                 cudaStream_t s, bool pdl)
 {
     const int64_t nchunks = M * (K / 8);
     const int64_t grid = (nchunks + 255) / 256;
     if (grid > (int64_t(1) << 31) - 1) return cudaErrorInvalidValue;
-    quantize_q8_1_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(static_cast<const uint4 *>(x), q, d_bits, sumq,
-                                                                    nchunks);
-    return cudaGetLastError();
+    return launch_ex(quantize_q8_1_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, pdl,
+                     static_cast<const uint4 *>(x), q, d_bits, sumq, nchunks);
 }
 
 }  // namespace qmv
