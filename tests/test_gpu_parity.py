@@ -566,3 +566,52 @@ def test_prefill_full_size_sampled(cuda_lib, orc, N, K, M):
     rows = _sample_rows(N, k=48)
     y_ref, S = orc.qmv_rows(0, W, x, N, K, rows, nthreads=8)
     assert H.normalised_error(y[:, rows], y_ref, S) <= H.TOL
+
+
+# -- concurrent use from several host threads, each on its own stream ------------------
+
+def test_concurrent_host_threads_and_streams(cuda_lib, orc):
+    """The library's process-wide state (device information, shared-memory
+    opt-in, the launch-shape table, the PDL switch) is shared by threads that
+    call it at once, each on its own stream; every result must still match."""
+    import threading
+    q = cuda_lib
+    cases = [("q4_0", 700, 2048, 1), ("q8_0", 300, 4096, 3), ("q2w", 515, 2560, 8), ("q4_0", 4096, 14336, 8),
+             ("q8_0", 33, 768, 2), ("q4_0", 1000, 640, 4)]
+    inputs = []
+    for i, (fmt, N, K, M) in enumerate(cases):
+        W = synth.weights(fmt, N, K, 900 + i)
+        x = synth.activations(M, K, 950 + i)
+        inputs.append((fmt, N, K, M, W, x, dev(W), dev(x)))
+    results, errors = {}, []
+
+    def worker(t):
+        try:
+            s = torch.cuda.Stream()
+            fns = {"q4_0": q.qmv_q4_0, "q8_0": q.qmv_q8_0, "q2w": q.qmv_q2w}
+            with torch.cuda.stream(s):
+                for rep in range(3):
+                    for j, (fmt, N, K, M, _, _, Wd, xd) in enumerate(inputs):
+                        if (j + t) % 2 == 0:
+                            y = fns[fmt](Wd, xd, stream=s)
+                            results[(t, rep, j)] = y
+            s.synchronize()
+        except Exception as e:    # surfaced below
+            errors.append(repr(e))
+
+    torch.cuda.synchronize()           # the inputs are on the device before any side stream reads them
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(4)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    refs = {}
+    for (t, rep, j), y in results.items():
+        fmt, N, K, M, W, x, _, _ = inputs[j]
+        if j not in refs:
+            refs[j] = orc.qmv(H.FMT[fmt], W, x, N, K, nthreads=8)
+        err = H.normalised_error(y.cpu().numpy().astype(np.float64), *refs[j])
+        assert err <= H.TOL, (t, rep, j, err)
+    assert q.qmv_device_status() == 0
