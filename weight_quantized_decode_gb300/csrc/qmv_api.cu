@@ -97,9 +97,14 @@ struct Plan {
 // G=8,SP=1,ctas=2,share=2" (any subset; 0 or absent = the built-in rule).
 // ctas = CTAs per SM in the grid; share = the fraction 1/share of an SM's
 // shared memory one CTA may use (share=2 leaves room for the next call's CTA
-// to become resident early under programmatic dependent launch).
+// to become resident early under programmatic dependent launch).  N=, K= and
+// M= restrict the override to one table shape (N the planned rows: 2N for the
+// fused SwiGLU, the expert's rows for the multi-expert call).
 struct Tune {
     int warps = 0, stages = 0, G = 0, SP = 0, ctas = 0, share = 0;
+    // optional: apply only to the table shape N x K at M tokens (0 = every shape)
+    long long N = 0, K = 0;
+    int M = 0;
 };
 
 const Tune &tune_overrides()
@@ -116,10 +121,14 @@ const Tune &tune_overrides()
             while (*c && *c != '=' && k < 15) key[k++] = *c++;
             if (*c != '=') break;
             ++c;
-            const int v = std::atoi(c);
+            const long long vl = std::atoll(c);
+            const int v = static_cast<int>(vl);
             while (*c && *c != ',') ++c;
             if (*c == ',') ++c;
-            if (!std::strcmp(key, "warps")) t.warps = v;
+            if (!std::strcmp(key, "N")) t.N = vl;
+            else if (!std::strcmp(key, "K")) t.K = vl;
+            else if (!std::strcmp(key, "M")) t.M = v;
+            else if (!std::strcmp(key, "warps")) t.warps = v;
             else if (!std::strcmp(key, "stages")) t.stages = v;
             else if (!std::strcmp(key, "G")) t.G = v;
             else if (!std::strcmp(key, "SP")) t.SP = v;
@@ -156,7 +165,7 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
     if (U > (1 << 20)) return pl;
     p.U = static_cast<int>(U);
     const int unit_bytes = fmt == kQ4_0 ? 144 : (fmt == kQ2W ? 80 : 272);
-    const Tune &tu = tune_overrides();
+    const Tune &tu_all = tune_overrides();
     // One problem (a plain call, or the fused SwiGLU's gate and up tables
     // stacked row by row) is planned as one table of rows_total rows; the
     // multi-expert call by its per-expert shape.
@@ -164,6 +173,10 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
     // Q4_0 against Q8_1 activations has its own entries (table format 3): its
     // per-unit arithmetic differs from the fp16 path's.
     const TuneEntry *te = tune_lookup(p.xq8 ? 3 : fmt, Nplan, p.K, M);
+    const Tune none{};
+    const bool tu_applies = (tu_all.N == 0 || tu_all.N == Nplan) && (tu_all.K == 0 || tu_all.K == p.K) &&
+                            (tu_all.M == 0 || tu_all.M == M);
+    const Tune &tu = tu_applies ? tu_all : none;
 
     // defaults by rule
     const int64_t wbytes_per_sm = Nplan * (p.K / 256) * unit_bytes / (sms > 0 ? sms : 1);
