@@ -26,7 +26,7 @@
  *     qs[j], element j>=16 is the high nibble of qs[j-16]; w = (c - 8) * d.
  *   Q8_0 block, 34 bytes, 32 weights:  bytes 0..1 = fp16 d, bytes 2..33 =
  *     int8 codes q[0..31]; w = q * d.
- *   Plain 2-bit ("q2w": codes -2..1, one fp16 scale per 32 weights, 2.5 bits
+ *   Plain 2-bit ("q2w": codes from -2 to 1 with an fp16 scale for every 32 weights, 2.5 bits
  *     per weight -- volta-kernel-bakeoff, "What's in the race", q2w_alu_v3),
  *     10 bytes, 32 weights: bytes 0..1 = fp16 d, bytes 2..9 = qs[0..7].  The
  *     pages fix the codes and the scale but not the bit order; it is read the

@@ -1,5 +1,5 @@
 // qmv_gemv_q2w.cu -- instantiations of the streaming decode kernel for the
-// plain 2-bit format (codes -2..1, one fp16 scale per 32 weights).
+// plain 2-bit format (codes from -2 to 1 with an fp16 scale for every 32 weights).
 #include "qmv_gemv.cuh"
 #include "qmv_launch.h"
 
