@@ -88,8 +88,12 @@ typedef enum {
  *   W : Q4_0 bytes [N][K/32*18], 16-byte aligned.
  *   x : fp16 [M][K], 2-byte aligned.        y : fp32 [M][N], 4-byte aligned.
  *   N >= 0, K >= 0 with K % 32 == 0, 0 <= M <= 8.
- * K % 256 == 0 (16-byte aligned rows) takes the streaming kernel; other K take
- * a slower generic kernel with the same results contract.
+ * K % 256 == 0 (16-byte aligned rows) with x 16-byte aligned takes the
+ * streaming kernel; other K or alignments take a slower generic kernel with
+ * the same results contract.  When the activations of all M tokens do not fit
+ * in shared memory (e.g. 8 tokens of K = 14336 in fp16) the call runs as a
+ * few launches over token subsets, each streaming W again.  These rules hold
+ * for every decode call below.
  */
 QMV_API qmv_status qmv_q4_0(const void *W, const void *x, float *y,
                     int64_t N, int64_t K, int64_t M, qmv_stream_t stream);
