@@ -1,0 +1,214 @@
+// plan_check.cu -- host-only check of the decode kernels' index arithmetic for
+// every launch plan the library's planner produces over a grid of table
+// shapes, token counts, formats and call forms.  No GPU is needed and no kernel
+// runs: for each plan the program replays, per CTA, warp, stage and lane, the
+// kernel's row ranges, bulk-copy sizes and shared-memory destinations, the
+// units each lane consumes, the activation offsets it reads and the staging
+// writes, and checks every one against the buffer it addresses.  It also
+// checks that a call whose activations do not fit in shared memory can be
+// split into token subsets that do.
+//
+// Built and run by tests/test_plan_bounds.py: the planner's translation unit
+// is compiled into this program, with stubs for the launch functions.
+#include "../../weight_quantized_decode_gb300/csrc/qmv_api.cu"
+
+#include <algorithm>
+#include <cstdio>
+
+using namespace qmv;
+
+namespace {
+
+long g_bad = 0;
+long g_checked = 0;
+
+#define CHECK(cond, ...)                                   \
+    do {                                                   \
+        if (!(cond)) {                                     \
+            if (g_bad < 20) {                              \
+                std::printf("FAIL %s: ", #cond);           \
+                std::printf(__VA_ARGS__);                  \
+                std::printf("\n");                         \
+            }                                              \
+            ++g_bad;                                       \
+        }                                                  \
+    } while (0)
+
+constexpr int kSms = 152;          // GB300
+constexpr int kOptin = 232448;     // shared memory a CTA may opt into (227 KB)
+
+int unit_bytes_of(int fmt) { return fmt == kQ4_0 ? 144 : (fmt == kQ2W ? 80 : 272); }
+int block_bytes_of(int fmt) { return fmt == kQ4_0 ? 18 : (fmt == kQ2W ? 10 : 34); }
+
+GemvParams params(int fmt, int64_t N, int64_t K, int n_problems, bool xq8, bool swiglu)
+{
+    GemvParams p = {};
+    p.N = N;
+    p.K = K;
+    p.n_experts = 2 * n_problems;
+    p.row_bytes = (K / 32) * block_bytes_of(fmt);
+    p.n_problems = n_problems;
+    p.max_local_problems = n_problems;
+    p.rows_total = swiglu ? 2 * N : N * n_problems;
+    p.x = reinterpret_cast<const __half *>(0x1000);     // 16-byte aligned, never dereferenced
+    p.W2 = swiglu ? reinterpret_cast<const uint8_t *>(0x2000) : nullptr;
+    p.xq8 = xq8 ? 1 : 0;
+    return p;
+}
+
+// The plain, multi-expert and Q8_1 forms: copies, consumption, activations.
+void check_plan(int fmt, int64_t N, int64_t K, int M, int n_problems, bool xq8)
+{
+    GemvParams p = params(fmt, N, K, n_problems, xq8, false);
+    const Plan pl = plan_gemv(fmt, p, M, kSms, kOptin);
+    if (!pl.streaming) {
+        // A plain call that does not fit must split into token subsets that do.
+        if (M > 1 && n_problems == 1 && K % 256 == 0) {
+            bool split = false;
+            for (int parts = 2; parts <= M && !split; ++parts) {
+                const int mc = (M + parts - 1) / parts;
+                GemvParams probe = params(fmt, N, K, 1, xq8, false);
+                if (!plan_gemv(fmt, probe, mc, kSms, kOptin).streaming) continue;
+                split = true;
+                for (int mm = 1; mm <= mc; ++mm) {
+                    GemvParams part = params(fmt, N, K, 1, xq8, false);
+                    CHECK(plan_gemv(fmt, part, mm, kSms, kOptin).streaming, "part of %d tokens of %lldx%lld", mm,
+                          (long long)N, (long long)K);
+                }
+            }
+            CHECK(split || K > 65536, "no token split for fmt %d %lldx%lld M=%d", fmt, (long long)N, (long long)K, M);
+        }
+        return;
+    }
+    ++g_checked;
+    const int XUB = xq8 ? kXQ8UnitBytes : kXUnitBytes;
+    const int unit = unit_bytes_of(fmt);
+    CHECK(pl.smem <= static_cast<size_t>(kOptin), "smem %zu", pl.smem);
+    CHECK(pl.warps >= 1 && pl.warps <= (M <= 2 ? 16 : 12), "warps %d", pl.warps);
+    const int U = p.U, G = p.G, SP = p.SP, RG = 32 / G, warps = pl.warps;
+    CHECK(G >= 1 && G <= 32 && p.S >= 2, "G %d S %d", G, p.S);
+    const size_t xbytes = static_cast<size_t>(p.max_local_problems) * M * U * XUB;
+    const int slot_bytes = 32 * SP * unit;
+    const int ups = SP * G;                              // units per stage and row
+    const uint32_t lane_chunk = static_cast<uint32_t>(ups * unit);
+    const int T_stages = (U + ups - 1) / ups;
+    const uint32_t R = static_cast<uint32_t>(p.rows_total);
+    for (int b = 0; b < pl.grid; ++b) {
+        const uint32_t row0 = static_cast<uint32_t>(static_cast<uint64_t>(R) * b / pl.grid);
+        const uint32_t row1 = static_cast<uint32_t>(static_cast<uint64_t>(R) * (b + 1) / pl.grid);
+        const int nrows = static_cast<int>(row1 - row0);
+        const int prob_lo = (n_problems > 1 && nrows > 0) ? static_cast<int>(row0 / N) : 0;
+        const int prob_hi = n_problems > 1 ? (nrows > 0 ? static_cast<int>((row1 - 1) / N) : -1) : 0;
+        CHECK(prob_hi - prob_lo + 1 <= p.max_local_problems, "problems %d > %d", prob_hi - prob_lo + 1,
+              p.max_local_problems);
+        // staging writes of this CTA (token tok, 16-byte chunk c of a 32-block)
+        const int ntok = (prob_hi - prob_lo + 1) * M;
+        for (int tok = 0; tok < ntok; tok += std::max(1, ntok - 1)) {
+            for (int64_t blk = 0; blk < K / 32; blk += std::max<int64_t>(1, K / 32 - 1)) {
+                const size_t base = static_cast<size_t>(tok) * U * XUB + static_cast<size_t>(blk >> 3) * XUB;
+                if (xq8) {
+                    CHECK(base + (blk & 7) * 32 + 3 * 8 + 8 <= xbytes, "q8_1 codes");
+                    CHECK(base + 256 + (blk & 7) * 8 + 8 <= xbytes && 256 + 8 * 8 <= XUB, "q8_1 block data");
+                } else {
+                    CHECK(base + (blk & 7) * 64 + 3 * 16 + 16 <= xbytes, "fp16 chunk");
+                }
+            }
+        }
+        const int ngroups = (nrows + RG - 1) / RG;
+        for (int w = 0; w < warps; ++w) {
+            // row groups are dealt to the CTA's warps round-robin; each takes T_stages stages
+            for (int grp = w; grp < ngroups; grp += warps) {
+                for (int t = 0; t < T_stages; ++t) {
+                    const int u0 = t * ups, u1 = std::min(U, u0 + ups);
+                    for (int lane = 0; lane < 32; ++lane) {      // copy issue: lane = row of the group
+                        const int lr = grp * RG + lane;
+                        if (lane >= RG || lr >= nrows || u1 <= u0) continue;
+                        const uint32_t bytes = static_cast<uint32_t>(u1 - u0) * unit;
+                        CHECK(bytes % 16 == 0 && bytes <= lane_chunk, "copy bytes %u", bytes);
+                        CHECK(lane * lane_chunk + bytes <= static_cast<uint32_t>(slot_bytes), "copy destination");
+                        CHECK(u1 <= U, "source units %d..%d of %d", u0, u1, U);
+                    }
+                    for (int lane = 0; lane < 32; ++lane) {      // consumption: lane (r, q)
+                        const int r = lane / G, q = lane - r * G;
+                        if (r >= RG) continue;                  // idle lanes when G does not divide 32
+                        const int lr = grp * RG + r;
+                        if (lr >= nrows) continue;
+                        CHECK(r * G + G - 1 < 32, "reduction lanes");
+                        for (int pass = 0; pass < SP; ++pass) {
+                            const int u = u0 + q + pass * G;
+                            if (u >= U) continue;
+                            const int off = pass * G + q;       // unit within the lane's chunk
+                            CHECK(u < u1, "unit %d read but not copied (%d..%d)", u, u0, u1);
+                            CHECK(static_cast<size_t>(r) * lane_chunk + static_cast<size_t>(off + 1) * unit <=
+                                      static_cast<size_t>(slot_bytes),
+                                  "shared read");
+                            const uint32_t row = row0 + lr;
+                            const int prob = n_problems > 1 ? static_cast<int>(row / N) : 0;
+                            const size_t xo = static_cast<size_t>(prob - prob_lo) * M * U * XUB +
+                                              static_cast<size_t>(M - 1) * U * XUB + static_cast<size_t>(u + 1) * XUB;
+                            CHECK(xo <= xbytes, "activations %zu > %zu", xo, xbytes);
+                        }
+                    }
+                }
+            }
+        }
+    }
+}
+
+// The fused SwiGLU: CTAs own whole gate/up pairs, a row group holds whole pairs
+// and the up partner sits G lanes above its gate lane.
+void check_swiglu(int64_t N, int64_t K, int M)
+{
+    GemvParams p = params(kQ4_0, N, K, 1, false, true);
+    const Plan pl = plan_gemv(kQ4_0, p, M, kSms, kOptin);
+    if (!pl.streaming) return;
+    ++g_checked;
+    const int G = p.G, RG = 32 / G;
+    CHECK((G & (G - 1)) == 0 && G <= 16 && RG % 2 == 0, "G %d", G);
+    CHECK(pl.smem <= static_cast<size_t>(kOptin), "smem");
+    const uint32_t R = static_cast<uint32_t>(p.rows_total);
+    for (int b = 0; b < pl.grid; ++b) {
+        const uint32_t row0 = 2u * static_cast<uint32_t>((static_cast<uint64_t>(R / 2) * b) / pl.grid);
+        const uint32_t row1 = 2u * static_cast<uint32_t>((static_cast<uint64_t>(R / 2) * (b + 1)) / pl.grid);
+        const int nrows = static_cast<int>(row1 - row0);
+        CHECK(row0 % 2 == 0 && nrows % 2 == 0 && row1 <= R, "pairs");
+        const int ngroups = (nrows + RG - 1) / RG;
+        for (int gi = 0; gi < ngroups; ++gi) {
+            for (int lane = 0; lane < 32; ++lane) {
+                const int r = lane / G, q = lane - r * G;
+                if (r >= RG) continue;
+                const int lr = gi * RG + r;
+                if (lr >= nrows) continue;
+                const uint32_t row = row0 + lr;
+                CHECK((row >> 1) < static_cast<uint32_t>(N), "table row");
+                if ((lr & 1) == 0 && q == 0) CHECK(lane + G < 32 && r + 1 < RG && lr + 1 < nrows, "partner lane");
+            }
+        }
+    }
+}
+
+}  // namespace
+
+int main()
+{
+    const int64_t Ns[] = {1,   2,   7,    9,    16,   20,   33,   40,   64,    77,    96,    100,   130,   300,
+                          333, 515, 600,  640,  1000, 2560, 4096, 4133, 6144,  8192,  12288, 14336, 28672, 128256};
+    const int64_t Ks[] = {256,  512,  768,  1024, 2048, 2304, 2560,  2816,
+                          3072, 3328, 3584, 3840, 4096, 6144, 8192, 14336};
+    for (int fmt : {kQ4_0, kQ8_0, kQ2W})
+        for (int64_t N : Ns)
+            for (int64_t K : Ks)
+                for (int M = 1; M <= 8; ++M) check_plan(fmt, N, K, M, 1, false);
+    for (int64_t N : Ns)
+        for (int64_t K : Ks)
+            for (int slots : {2, 3, 5, 8, 10, 64})
+                if (N * slots < 200000) check_plan(kQ4_0, N, K, 1, slots, false);
+    for (int64_t N : Ns)
+        for (int64_t K : Ks)
+            for (int M = 1; M <= 8; ++M) {
+                check_swiglu(N, K, M);
+                check_plan(kQ4_0, N, K, M, 1, true);
+            }
+    std::printf("checked %ld plans, %ld failures\n", g_checked, g_bad);
+    return g_bad ? 1 : 0;
+}
