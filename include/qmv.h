@@ -251,7 +251,10 @@ QMV_API qmv_status qmv_q4_0_swiglu_f32(const void *W_gate, const void *W_up, con
  *   W : Q4_0 bytes [N][K/32*18], 16-byte aligned.  The tensor-core kernel
  *       takes K % 256 == 0 (any N: a ragged last 128-row tile is masked);
  *       other K take the generic kernel.
- *   x : fp16 [M][K], 16-byte aligned.  y : fp32 [M][N].  M >= 0.
+ *   x : fp16 [M][K], 16-byte aligned.  y : fp32 [M][N].
+ *   0 <= M <= 2^24 (QMV_ERR_SHAPE above).  Above 65535 * 256 tokens the
+ *   token tiles would exceed the grid's y limit, and the generic kernel takes
+ *   the call.
  */
 QMV_API qmv_status qmm_q4_0_prefill(const void *W, const void *x, float *y,
                             int64_t N, int64_t K, int64_t M, qmv_stream_t stream);

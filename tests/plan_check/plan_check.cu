@@ -6,7 +6,9 @@
 // units each lane consumes, the activation offsets it reads and the staging
 // writes, and checks every one against the buffer it addresses.  It also
 // checks that a call whose activations do not fit in shared memory can be
-// split into token subsets that do.
+// split into token subsets that do.  The tensor-core prefill kernel's plans
+// are replayed the same way (tensor-copy coordinates, shared-memory layout,
+// tensor-memory columns, epilogue coverage).
 //
 // Built and run by tests/test_plan_bounds.py: the planner's translation unit
 // is compiled into this program, with stubs for the launch functions.
@@ -187,6 +189,115 @@ void check_swiglu(int64_t N, int64_t K, int M)
     }
 }
 
+// The tensor-core prefill kernel: tile and ring choices, the shared-memory
+// layout and its alignment, tensor-copy boxes and coordinates, tensor-memory
+// columns, the dequantising threads' reads and writes, and the epilogue's
+// coverage of every (lane quarter, column chunk) of the accumulator.
+void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int ns_force)
+{
+    const PrefillPlan pl = plan_prefill(N, K, M, sms, nw_force, ns_force);
+    const bool shape_ok = K % kKChunk == 0 && K > 0 && N > 0 && M > 0 && N < (int64_t(1) << 31) &&
+                          M < (int64_t(1) << 31) && K < (int64_t(1) << 30);
+    if (!pl.ok) {
+        // a shape of the kernel's form is refused only where the grid would exceed gridDim.y
+        CHECK(!shape_ok || pl.grid_y > kMaxGridY, "prefill refused %lldx%lld M=%lld", (long long)N, (long long)K,
+              (long long)M);
+        return;
+    }
+    ++g_checked;
+    CHECK(shape_ok, "prefill took %lldx%lld M=%lld", (long long)N, (long long)K, (long long)M);
+    const int TN = pl.TN, NH = pl.NH, KSUB = pl.KSUB, NW = pl.NW, NS = pl.NS;
+    const int TNH = TN / NH;
+    CHECK(TN % 64 == 0 && TN <= 512 && TN % NH == 0 && (NH == 1 || NH == 2), "TN %d NH %d", TN, NH);
+    CHECK(TNH % 16 == 0 && TNH >= 16 && TNH <= 256, "MMA N %d", TNH);   // kind::f16 with M = 128
+    CHECK((KSUB == 1 || KSUB == 2) && (NH == 1 || KSUB == 1), "KSUB %d NH %d", KSUB, NH);
+    CHECK(NW >= 2 && NS >= 2, "rings %d %d", NW, NS);
+    CHECK(pl.smem <= static_cast<size_t>(kOptin), "prefill smem %zu", pl.smem);
+    const uint32_t cols = pl.tmem_cols;
+    CHECK(cols >= 32 && cols <= 512 && (cols & (cols - 1)) == 0 && static_cast<uint32_t>(TN) <= cols, "TMEM %u",
+          cols);
+    CHECK(pl.grid_x >= 1 && pl.grid_x <= INT32_MAX && pl.grid_y >= 1 && pl.grid_y <= kMaxGridY, "grid");
+    CHECK(pl.grid_x * kBM >= N && (pl.grid_x - 1) * kBM < N, "row tiles");
+    CHECK(pl.grid_y * TN >= M && (pl.grid_y - 1) * TN < M, "token tiles");
+    const int64_t nK = K / (kKB * KSUB), nC = K / kKChunk;
+    CHECK(nK * KSUB * kKB == K && nC * 4 == nK * KSUB && nK < INT32_MAX, "K loop");
+
+    // shared memory, as offsets from the 1024-byte-aligned base
+    const size_t a_slot = static_cast<size_t>(KSUB) * kATileBytes;
+    const size_t b_atom = static_cast<size_t>(TN) * kKB * 2, b_half = static_cast<size_t>(TNH) * kKB * 2;
+    const size_t b_slot = KSUB * b_atom;
+    const size_t b_off = NS * a_slot, w_off = b_off + NS * b_slot;
+    const size_t bar_off = w_off + static_cast<size_t>(NW) * kPackedTileBytes;
+    const size_t bar_end = bar_off + static_cast<size_t>(2 * NW + 3 * NS + 1) * 8 + 4 + 4;
+    CHECK(1023 + bar_end <= pl.smem, "layout %zu + slack > %zu", bar_end, pl.smem);
+    CHECK((bar_off + 1024) >> 4 < (size_t(1) << 14), "descriptor address field");
+    for (int s = 0; s < NS; ++s)
+        for (int a = 0; a < KSUB; ++a) {
+            CHECK((s * a_slot + a * kATileBytes) % 1024 == 0, "A tile alignment");
+            for (int h = 0; h < NH; ++h)
+                CHECK((b_off + s * b_slot + a * b_atom + h * b_half) % 1024 == 0, "B tile alignment");
+        }
+    for (int w = 0; w < NW; ++w) CHECK((w_off + static_cast<size_t>(w) * kPackedTileBytes) % 128 == 0, "W slot");
+
+    // tensor-copy boxes: within the box limits; bytes landed = the barrier's expected count
+    CHECK(kPackedRowBytes <= 256 && kBM <= 256 && TNH <= 256 && kKB * 2 <= 128, "boxes");
+    CHECK(static_cast<size_t>(kPackedRowBytes) * kBM == static_cast<size_t>(kPackedTileBytes), "W box bytes");
+    CHECK(static_cast<size_t>(KSUB) * NH * kKB * TNH * 2 == b_slot, "x box bytes");
+    // coordinates: innermost x times the element size on 16 bytes and inside the row
+    const int64_t row_bytes = (K / 32) * 18;
+    for (int64_t c = 0; c < nC; c += (c < 4 || c + 4 >= nC) ? 1 : std::max<int64_t>(1, nC / 64)) {
+        const int64_t x = c * kPackedRowBytes;
+        CHECK(x % 16 == 0 && x + kPackedRowBytes <= row_bytes && x < INT32_MAX, "W x %lld", (long long)x);
+    }
+    for (int64_t j = 0; j < nK; j += (j < 4 || j + 4 >= nK) ? 1 : std::max<int64_t>(1, nK / 64))
+        for (int a = 0; a < KSUB; ++a) {
+            const int64_t x = (j * KSUB + a) * kKB;
+            CHECK((x * 2) % 16 == 0 && x + kKB <= K, "x x %lld", (long long)x);
+        }
+    for (int64_t by = 0; by < pl.grid_y; ++by)
+        for (int h = 0; h < NH; ++h) {
+            const int64_t yc = by * TN + static_cast<int64_t>(h) * TNH;   // rows past M read the fill value
+            CHECK(yc >= 0 && yc + TNH <= INT32_MAX, "x y %lld", (long long)yc);
+        }
+    CHECK((pl.grid_x - 1) * kBM < N && (pl.grid_x - 1) * kBM <= INT32_MAX, "W y");
+
+    // dequantising threads: reads of the packed slot, writes of the A tile
+    static unsigned char cover[kATileBytes / 16];
+    for (int s = 0; s < NS; ++s)
+        for (int a = 0; a < KSUB; ++a) {
+            std::fill(cover, cover + kATileBytes / 16, 0);
+            for (int dt = 0; dt < 256; ++dt) {
+                const int r = dt & (kBM - 1), hsel = dt >> 7;
+                CHECK(static_cast<size_t>(NW - 1) * kPackedTileBytes + r * kPackedRowBytes + 16 * 8 + 16 <=
+                          static_cast<size_t>(NW) * kPackedTileBytes,
+                      "packed read");
+                for (int ch = 0; ch < 4; ++ch) {
+                    const int cc = 4 * hsel + ch;
+                    const size_t off = (r >> 3) * 1024 + (r & 7) * 128 + ((cc ^ (r & 7)) << 4);
+                    CHECK(s * a_slot + a * kATileBytes + off + 16 <= NS * a_slot, "A write");
+                    ++cover[off / 16];
+                }
+            }
+            for (int i = 0; i < kATileBytes / 16; ++i) CHECK(cover[i] == 1, "A chunk %d written %d times", i, cover[i]);
+        }
+    for (int sub = 0; sub < 4; ++sub) CHECK(4 * (9 * sub + 8) + 4 <= kPackedRowBytes, "block words");
+
+    // epilogue: each (lane quarter, 32-column chunk) read by exactly one warp, inside the allocation
+    static unsigned char ecover[4][16];
+    std::fill(&ecover[0][0], &ecover[0][0] + 64, 0);
+    const int warps = kPrefillThreads / 32;
+    for (int w = 0; w < warps; ++w) {
+        const int quarter = w & 3, nq = (warps - quarter + 3) / 4, rank = w >> 2;
+        for (int c0 = 32 * rank; c0 < TN; c0 += 32 * nq) {
+            CHECK(c0 + 32 <= TN && static_cast<uint32_t>(c0 + 32) <= cols, "epilogue columns");
+            ++ecover[quarter][c0 / 32];
+        }
+    }
+    for (int q = 0; q < 4; ++q)
+        for (int c = 0; c < TN / 32; ++c) CHECK(ecover[q][c] == 1, "epilogue chunk %d,%d read %d times", q, c, ecover[q][c]);
+    for (int h = 0; h < NH; ++h) CHECK(static_cast<uint32_t>((h + 1) * TNH) <= cols, "accumulator %d", h);
+}
+
 }  // namespace
 
 int main()
@@ -209,6 +320,17 @@ int main()
                 check_swiglu(N, K, M);
                 check_plan(kQ4_0, N, K, M, 1, true);
             }
+    const int64_t pN[] = {1, 127, 128, 129, 640, 4096, 14336, 128256, (int64_t(1) << 31) - 1};
+    const int64_t pK[] = {32, 256, 512, 2560, 4096, 14336, (int64_t(1) << 30) - 256, int64_t(1) << 30};
+    const int64_t pM[] = {1,   2,   63,   64,    65,    127,    128,           129,               192,
+                          255, 256, 257,  511,   512,   513,    1024,          4096,              16384,
+                          65535LL * 256,  65535LL * 256 + 1,    int64_t(1) << 24, (int64_t(1) << 31) - 1};
+    for (int64_t N : pN)
+        for (int64_t K : pK)
+            for (int64_t M : pM)
+                for (int sms : {152, 148, 132, 1})
+                    for (int nw : {0, 2, 3, 5, 8})
+                        for (int ns : {0, 2, 3, 4, 6}) check_prefill(N, K, M, sms, nw, ns);
     std::printf("checked %ld plans, %ld failures\n", g_checked, g_bad);
     return g_bad ? 1 : 0;
 }

@@ -22,10 +22,10 @@ cudaError_t launch_quantize_q8_1(const void *, int8_t *, uint16_t *, int32_t *, 
     return cudaSuccess;
 }
 
-bool prefill_supported(int64_t, int64_t, int64_t) { return false; }
+PrefillPlan prefill_plan(int64_t, int64_t, int64_t, int) { return PrefillPlan{}; }
 
-cudaError_t launch_prefill(const void *, const void *, float *, int64_t, int64_t, int64_t, int, int *, cudaStream_t,
-                           bool)
+cudaError_t launch_prefill(const PrefillPlan &, const void *, const void *, float *, int64_t, int64_t, int64_t, int *,
+                           cudaStream_t, bool)
 {
     return cudaSuccess;
 }

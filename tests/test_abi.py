@@ -70,6 +70,9 @@ def test_host_validation(lib, fn):
     assert f(None, None, None, 8, 256, 0, None) == 0
     if fn != "qmm_q4_0_prefill":
         assert f(FAKE, FAKE, FAKE, 8, 256, 9, None) == 3      # decode takes M <= 8
+    else:
+        assert f(FAKE, FAKE, FAKE, 8, 256, (1 << 24) + 1, None) == 3   # prefill takes M <= 2^24
+        assert f(FAKE, FAKE + 2, FAKE, 8, 256, 64, None) == 2          # tensor-copy x: 16-byte aligned
     if fn == "qmv_q4_0_f32":
         assert f(FAKE, FAKE + 2, FAKE, 8, 256, 1, None) == 2  # fp32 x not 4-byte aligned
 

@@ -540,8 +540,9 @@ qmv_status qmm_q4_0_prefill(const void *W, const void *x, float *y, int64_t N, i
     int *status = nullptr;
     int sms = 0, optin = 0;
     if (device_info(dev, &status, &sms, &optin) != cudaSuccess) return QMV_ERR_CUDA;
-    if (prefill_supported(N, K, M)) {
-        cudaError_t e = launch_prefill(W, x, y, N, K, M, sms, status, s, g_pdl.load(std::memory_order_relaxed) != 0);
+    const PrefillPlan pl = prefill_plan(N, K, M, sms);
+    if (pl.ok) {
+        cudaError_t e = launch_prefill(pl, W, x, y, N, K, M, status, s, g_pdl.load(std::memory_order_relaxed) != 0);
         if (e != cudaSuccess) {
             (void)cudaGetLastError();
             return QMV_ERR_LAUNCH;

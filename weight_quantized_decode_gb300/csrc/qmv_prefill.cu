@@ -48,18 +48,13 @@
 #include "qmv_common.cuh"
 #include "qmv_launch.h"
 #include "qmv_prefill.h"
+#include "qmv_prefill_plan.h"
 
 namespace qmv {
 
 namespace {
 
-constexpr int kBM = 128;                 // weight rows per tile (MMA M)
-constexpr int kKB = 64;                  // K per MMA slice (one 128-byte swizzle atom of fp16)
-constexpr int kKChunk = 256;             // K per packed weight tile (8 Q4_0 blocks = 144 bytes per row)
-constexpr int kPackedRowBytes = 144;
-constexpr int kPackedTileBytes = kBM * kPackedRowBytes;    // 18432
-constexpr int kATileBytes = kBM * kKB * 2;                 // 16384
-constexpr int kThreads = 352;            // 11 warps: 8 dequantising, MMA issue, 2 copy producers
+constexpr int kThreads = kPrefillThreads;   // 11 warps: 8 dequantising, MMA issue, 2 copy producers
 constexpr int kMmaWarp = 1, kWProducerWarp = 5, kXProducerWarp = 9;
 constexpr int kDeqThreads = 256;
 
@@ -543,28 +538,20 @@ int ring_override(int which)
 int ring_override_nw() { return ring_override(0); }
 int ring_override_ns() { return ring_override(1); }
 
-int pick_tn(int64_t M)
-{
-    // Multiples of 64 so that each of the two epilogue warps per lane quarter
-    // reads whole 32-column chunks.
-    if (M >= 256) return 256;
-    int tn = static_cast<int>((M + 63) / 64) * 64;
-    return tn < 64 ? 64 : tn;
-}
-
 }  // namespace
 
-bool prefill_supported(int64_t N, int64_t K, int64_t M)
+PrefillPlan prefill_plan(int64_t N, int64_t K, int64_t M, int sms)
 {
-    return K % kKChunk == 0 && K > 0 && N > 0 && M > 0 && N < (int64_t(1) << 31) && M < (int64_t(1) << 31) &&
-           K < (int64_t(1) << 30) && encode_fn() != nullptr;
+    PrefillPlan pl = plan_prefill(N, K, M, sms, ring_override_nw(), ring_override_ns());
+    if (encode_fn() == nullptr) pl.ok = false;
+    return pl;
 }
 
-cudaError_t launch_prefill(const void *W, const void *x, float *y, int64_t N, int64_t K, int64_t M, int sms,
-                           int *status, cudaStream_t s, bool pdl)
+cudaError_t launch_prefill(const PrefillPlan &pl, const void *W, const void *x, float *y, int64_t N, int64_t K,
+                           int64_t M, int *status, cudaStream_t s, bool pdl)
 {
     EncodeTiledFn enc = encode_fn();
-    if (!enc) return cudaErrorNotSupported;
+    if (!enc || !pl.ok) return cudaErrorNotSupported;
     const int64_t row_bytes = (K / 32) * 18;
     CUtensorMap wmap, xmap;
     {
@@ -577,20 +564,10 @@ cudaError_t launch_prefill(const void *W, const void *x, float *y, int64_t N, in
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    int TN = pick_tn(M);
-    int NH = 1;
-    // When 256-token tiles would need a second wave of CTAs, one CTA takes
-    // 512 tokens in two accumulators (512 TMEM columns): one wave, and each
-    // weight tile is dequantised once for all of them.
-    const int64_t row_tiles = (N + kBM - 1) / kBM;
-    if (TN == 256 && row_tiles * ((M + 255) / 256) > sms && row_tiles * ((M + 511) / 512) <= sms) {
-        TN = 512;
-        NH = 2;
-    }
     {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K * 2)};
-        const cuuint32_t box[2] = {kKB, static_cast<cuuint32_t>(TN / NH)};
+        const cuuint32_t box[2] = {kKB, static_cast<cuuint32_t>(pl.TN / pl.NH)};
         const cuuint32_t estr[2] = {1, 1};
         if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(x), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -603,46 +580,16 @@ cudaError_t launch_prefill(const void *W, const void *x, float *y, int64_t N, in
     p.N = N;
     p.K = K;
     p.M = M;
-    p.TN = TN;
-    p.NH = NH;
-    // Up to 128 token columns a slot holds two 64-K atoms: eight MMAs per
-    // barrier round and per commit (the issuing thread's fixed cost per round
-    // is then paid half as often); a 256-column slot would not fit twice.
-    const int KSUB = TN <= 128 ? 2 : 1;
-    const int b_tile = KSUB * TN * kKB * 2;
-    const int a_tile = KSUB * kATileBytes;
-    // Ring depths: the packed-weight ring must cover DRAM latency, the
-    // activation ring L2 latency, at the MMA rate of this tile width.
-    int NW = 4, NS = 3;
-    if (TN > 256) {
-        NW = 3;
-        NS = 2;
-    } else if (TN <= 64) {
-        NW = 4;
-        NS = 3;
-    } else if (TN <= 128) {
-        NW = 4;
-        NS = 2;
-    }
-    // alignment slack + barriers (2*NW + 3*NS + 1 of 8 bytes) + TMEM slot + flag
-    const size_t fixed = 1024 + 512;
-    auto total = [&] { return fixed + static_cast<size_t>(NW) * kPackedTileBytes +
-                              static_cast<size_t>(NS) * (a_tile + b_tile); };
-    if (ring_override_nw() >= 2) NW = ring_override_nw();
-    if (ring_override_ns() >= 2) NS = ring_override_ns();
-    while (total() > 225 * 1024 && NS > 2) --NS;
-    while (total() > 225 * 1024 && NW > 2) --NW;
-    p.NW = NW;
-    p.NS = NS;
-    p.KSUB = KSUB;
-    uint32_t cols = 32;
-    while (cols < static_cast<uint32_t>(TN)) cols <<= 1;
-    p.tmem_cols = cols;
-    const size_t smem = total();
-    cudaError_t e = ensure_smem_optin(reinterpret_cast<const void *>(prefill_kernel), smem);
+    p.TN = pl.TN;
+    p.NH = pl.NH;
+    p.NW = pl.NW;
+    p.NS = pl.NS;
+    p.KSUB = pl.KSUB;
+    p.tmem_cols = pl.tmem_cols;
+    cudaError_t e = ensure_smem_optin(reinterpret_cast<const void *>(prefill_kernel), pl.smem);
     if (e != cudaSuccess) return e;
-    const dim3 grid(static_cast<unsigned>((N + kBM - 1) / kBM), static_cast<unsigned>((M + TN - 1) / TN));
-    return launch_ex(prefill_kernel, grid, dim3(kThreads), smem, s, pdl, wmap, xmap, p);
+    const dim3 grid(static_cast<unsigned>(pl.grid_x), static_cast<unsigned>(pl.grid_y));
+    return launch_ex(prefill_kernel, grid, dim3(kThreads), pl.smem, s, pdl, wmap, xmap, p);
 }
 
 }  // namespace qmv

@@ -4,12 +4,16 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "qmv_prefill_plan.h"
+
 namespace qmv {
 
-// True when the tensor-core kernel handles this shape.
-bool prefill_supported(int64_t N, int64_t K, int64_t M);
+// The tensor-core kernel's plan for this call on a device of `sms` SMs, with
+// the ring depths forced through QMV_PREFILL_RING applied; ok is false when
+// that kernel does not take the shape (or the tensor-map encoder is missing).
+PrefillPlan prefill_plan(int64_t N, int64_t K, int64_t M, int sms);
 
-cudaError_t launch_prefill(const void *W, const void *x, float *y, int64_t N, int64_t K, int64_t M, int sms,
-                           int *status, cudaStream_t s, bool pdl);
+cudaError_t launch_prefill(const PrefillPlan &pl, const void *W, const void *x, float *y, int64_t N, int64_t K,
+                           int64_t M, int *status, cudaStream_t s, bool pdl);
 
 }  // namespace qmv
