@@ -141,3 +141,13 @@ def test_no_cpu_path():
     x = torch.zeros((1, 256), dtype=torch.float16)
     with pytest.raises(TypeError):
         q.qmv_q4_0(W, x)
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    # Without the built library every call raises; nothing falls back to a CPU path.
+    monkeypatch.setattr(q, "_lib", None)
+    monkeypatch.setattr(q, "LIB_PATH", str(tmp_path / "libqmv.so"))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        q.qmv_version()
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        q.qmv_q4_0_ptr(FAKE, FAKE, FAKE, 8, 256, 1)
