@@ -476,6 +476,8 @@ def test_prefill_repeats_are_bit_identical(cuda_lib, orc, N, K, M):
 PREFILL_RINGS = {
     # the shallowest rings (two packed-weight slots, two operand slots)
     "2,2": ["pfrep:q4_0:12288:2560:512", "pfrep:q4_0:4096:2560:256", "pfrep:q4_0:2048:2560:64"],
+    # one packed-weight slot, the deepest operand ring that then fits
+    "1,4": ["pfrep:q4_0:12288:2560:512", "pfrep:q4_0:4096:2560:256", "pfrep:q4_0:2048:2560:64"],
 }
 
 

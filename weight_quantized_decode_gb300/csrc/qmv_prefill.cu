@@ -521,7 +521,7 @@ EncodeTiledFn encode_fn()
 }
 
 // Ring depths forced for tests and sweeps: QMV_PREFILL_RING="NW,NS" (packed-
-// weight slots, operand slots; values below 2 keep the rule).
+// weight slots, operand slots; NW below 1 or NS below 2 keeps the rule).
 int ring_override(int which)
 {
     static int nw = 0, ns = 0;

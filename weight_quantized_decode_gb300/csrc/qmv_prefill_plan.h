@@ -44,8 +44,12 @@ inline int prefill_pick_tn(int64_t M)
     return tn < 64 ? 64 : tn;
 }
 
-// nw_force / ns_force: ring depths forced for tests and sweeps (values below 2
-// keep the rule; shared memory still caps them).
+// nw_force / ns_force: ring depths forced for tests and sweeps (a packed-weight
+// depth below 1 or an operand depth below 2 keeps the rule; shared memory still
+// caps them).  One packed-weight slot is correct (each dequantising thread
+// copies its 144-byte row into registers before releasing the slot) but slow
+// for narrow token tiles: the four 64-K atoms held in registers do not cover
+// the next tile's DRAM latency.
 inline PrefillPlan plan_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int ns_force)
 {
     PrefillPlan pl = {};
@@ -85,7 +89,7 @@ inline PrefillPlan plan_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw
         return kPrefillFixedSmem + static_cast<size_t>(NW) * kPackedTileBytes +
                static_cast<size_t>(NS) * static_cast<size_t>(a_tile + b_tile);
     };
-    if (nw_force >= 2) NW = nw_force;
+    if (nw_force >= 1) NW = nw_force;
     if (ns_force >= 2) NS = ns_force;
     while (total() > kPrefillSmemCap && NS > 2) --NS;
     while (total() > kPrefillSmemCap && NW > 2) --NW;
