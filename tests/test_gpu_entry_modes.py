@@ -89,3 +89,32 @@ def test_eager_pdl_off_and_graph_agree(cuda_lib, name):
     assert torch.equal(y_eager, y_plain)
     assert torch.equal(y_eager, y1) and torch.equal(y_eager, y2)
     assert q.qmv_device_status() == 0
+
+
+def test_binding_refuses_bad_arguments(cuda_lib):
+    """The Python binding refuses, before any launch, arguments the kernels
+    would read with the wrong layout or size."""
+    q = cuda_lib
+    N, K = 64, 512
+    W = dev(synth.q4_0_weights(N, K, 11))
+    x = dev(synth.activations(2, K, 12))
+    pool = dev(synth.q4_0_weights(4 * N, K, 13))
+    idx = torch.tensor([1, 3], dtype=torch.int32, device="cuda")
+    qc, qd, qs = q.qmv_quantize_q8_1(x)
+    wide = dev(synth.activations(2, 2 * K, 14))
+    with pytest.raises(ValueError):          # strided activations
+        q.qmv_moe(pool, idx, 4, wide[:, ::2], N)
+    with pytest.raises(ValueError):          # output of the wrong size
+        q.qmv_moe(pool, idx, 4, x, N, y=torch.empty((2, N + 1), dtype=torch.float32, device="cuda"))
+    with pytest.raises(ValueError):          # W not a whole number of rows
+        q.qmv_q4_0_q8_1_pre(W.view(-1)[:-18 * 3], qc, qd, qs)
+    with pytest.raises(ValueError):
+        q.qmv_q4_0_q8_1_pre(W, qc, qd, qs, y=torch.empty((2, N), dtype=torch.float16, device="cuda"))
+    with pytest.raises(ValueError):
+        q.qmv_q4_0(W, x, y=torch.empty((3, N), dtype=torch.float32, device="cuda"))
+    # the accepted forms still agree with each other
+    y_pre = q.qmv_q4_0_q8_1_pre(W, qc, qd, qs)
+    y_one = q.qmv_q4_0_q8_1(W, x)
+    torch.cuda.synchronize()
+    assert torch.equal(y_pre, y_one)
+    assert q.qmv_device_status() == 0

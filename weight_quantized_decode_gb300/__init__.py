@@ -165,6 +165,24 @@ def _stream_handle(stream):
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def _on_device(fn, *tensors):
+    """All tensors on one CUDA device; returns a context that makes it current.
+    The library launches on the current device and takes its status word and
+    SM count from it, so a call on another device's tensors must switch first."""
+    torch = _torch()
+    dev = tensors[0].device
+    for t in tensors[1:]:
+        if t.device != dev:
+            raise ValueError(f"{fn}: all tensors must be on one device ({dev} and {t.device})")
+    return torch.cuda.device(dev)
+
+
+def _check_y(y, M, N, fn):
+    torch = _torch()
+    if not (y.is_cuda and y.dtype == torch.float32 and y.is_contiguous() and y.numel() == M * N):
+        raise ValueError(f"{fn}: y must be a contiguous CUDA float32 tensor of {M}x{N}")
+
+
 def _prep(W, x, y, block_bytes, fn, x_dtype=None):
     torch = _torch()
     x_dtype = torch.float16 if x_dtype is None else x_dtype
@@ -190,22 +208,24 @@ def _prep(W, x, y, block_bytes, fn, x_dtype=None):
         N = W.numel() // row_bytes
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=x.device)
-    elif not (y.is_cuda and y.dtype == torch.float32 and y.is_contiguous() and y.numel() == M * N):
-        raise ValueError(f"{fn}: y must be a contiguous CUDA float32 tensor of {M}x{N}")
+    else:
+        _check_y(y, M, N, fn)
     return W, x, y, N, K, M
 
 
 def qmv_q4_0(W, x, y=None, stream=None):
     """y[M, N] = x[M, K] @ dequant(W)^T for Q4_0 weights ``W`` (uint8, N rows)."""
     W, x, y, N, K, M = _prep(W, x, y, Q4_0_BLOCK_BYTES, "qmv_q4_0")
-    qmv_q4_0_ptr(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, _stream_handle(stream))
+    with _on_device("qmv_q4_0", W, x, y):
+        qmv_q4_0_ptr(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, _stream_handle(stream))
     return y
 
 
 def qmv_q4_0_f32(W, x, y=None, stream=None):
     """qmv_q4_0 with float32 activations, rounded to fp16 inside the kernel."""
     W, x, y, N, K, M = _prep(W, x, y, Q4_0_BLOCK_BYTES, "qmv_q4_0_f32", _torch().float32)
-    qmv_q4_0_f32_ptr(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, _stream_handle(stream))
+    with _on_device("qmv_q4_0_f32", W, x, y):
+        qmv_q4_0_f32_ptr(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, _stream_handle(stream))
     return y
 
 
@@ -221,8 +241,9 @@ def qmv_q4_0_swiglu(W_gate, W_up, x, y=None, stream=None):
     Q4_0 tables of N rows each (the MLP's gate + up + SwiGLU in one call)."""
     W_gate, x, y, N, K, M = _prep(W_gate, x, y, Q4_0_BLOCK_BYTES, "qmv_q4_0_swiglu")
     _check_up(W_gate, W_up, "qmv_q4_0_swiglu")
-    qmv_q4_0_swiglu_ptr(W_gate.data_ptr(), W_up.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M,
-                        _stream_handle(stream))
+    with _on_device("qmv_q4_0_swiglu", W_gate, W_up, x, y):
+        qmv_q4_0_swiglu_ptr(W_gate.data_ptr(), W_up.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M,
+                            _stream_handle(stream))
     return y
 
 
@@ -230,22 +251,25 @@ def qmv_q4_0_swiglu_f32(W_gate, W_up, x, y=None, stream=None):
     """qmv_q4_0_swiglu with float32 activations, rounded to fp16 inside the kernel."""
     W_gate, x, y, N, K, M = _prep(W_gate, x, y, Q4_0_BLOCK_BYTES, "qmv_q4_0_swiglu_f32", _torch().float32)
     _check_up(W_gate, W_up, "qmv_q4_0_swiglu_f32")
-    qmv_q4_0_swiglu_f32_ptr(W_gate.data_ptr(), W_up.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M,
-                            _stream_handle(stream))
+    with _on_device("qmv_q4_0_swiglu_f32", W_gate, W_up, x, y):
+        qmv_q4_0_swiglu_f32_ptr(W_gate.data_ptr(), W_up.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M,
+                                _stream_handle(stream))
     return y
 
 
 def qmv_q8_0(W, x, y=None, stream=None):
     """y[M, N] = x[M, K] @ dequant(W)^T for Q8_0 weights."""
     W, x, y, N, K, M = _prep(W, x, y, Q8_0_BLOCK_BYTES, "qmv_q8_0")
-    qmv_q8_0_ptr(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, _stream_handle(stream))
+    with _on_device("qmv_q8_0", W, x, y):
+        qmv_q8_0_ptr(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, _stream_handle(stream))
     return y
 
 
 def qmv_q4_0_q8_1(W, x, y=None, stream=None):
     """qmv_q4_0 with the activations quantised to Q8_1 in the kernel (integer dots)."""
     W, x, y, N, K, M = _prep(W, x, y, Q4_0_BLOCK_BYTES, "qmv_q4_0_q8_1")
-    qmv_q4_0_q8_1_ptr(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, _stream_handle(stream))
+    with _on_device("qmv_q4_0_q8_1", W, x, y):
+        qmv_q4_0_q8_1_ptr(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, _stream_handle(stream))
     return y
 
 
@@ -265,11 +289,16 @@ def qmv_q4_0_q8_1_pre(W, q, d_bits, sumq, y=None, stream=None):
     if not (W.is_contiguous() and q.is_contiguous() and d_bits.is_contiguous() and sumq.is_contiguous()):
         raise ValueError("qmv_q4_0_q8_1_pre: tensors must be contiguous")
     row_bytes = (K // 32) * Q4_0_BLOCK_BYTES
-    N = W.numel() // row_bytes if row_bytes else 0
+    if row_bytes and W.numel() % row_bytes:
+        raise ValueError(f"qmv_q4_0_q8_1_pre: W size {W.numel()} is not a whole number of rows of {row_bytes} bytes")
+    N = W.numel() // row_bytes if row_bytes else (W.shape[0] if W.dim() >= 1 else 0)
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=q.device)
-    qmv_q4_0_q8_1_pre_ptr(W.data_ptr(), q.data_ptr(), d_bits.data_ptr(), sumq.data_ptr(), y.data_ptr(), N, K, M,
-                          _stream_handle(stream))
+    else:
+        _check_y(y, M, N, "qmv_q4_0_q8_1_pre")
+    with _on_device("qmv_q4_0_q8_1_pre", W, q, d_bits, sumq, y):
+        qmv_q4_0_q8_1_pre_ptr(W.data_ptr(), q.data_ptr(), d_bits.data_ptr(), sumq.data_ptr(), y.data_ptr(), N, K,
+                              M, _stream_handle(stream))
     return y
 
 
@@ -286,21 +315,24 @@ def qmv_quantize_q8_1(x, stream=None):
     q = torch.empty((M, K), dtype=torch.int8, device=x.device)
     d = torch.empty((M, K // 32), dtype=torch.int16, device=x.device)
     s = torch.empty((M, K // 32), dtype=torch.int32, device=x.device)
-    qmv_quantize_q8_1_ptr(x.data_ptr(), q.data_ptr(), d.data_ptr(), s.data_ptr(), M, K, _stream_handle(stream))
+    with _on_device("qmv_quantize_q8_1", x):
+        qmv_quantize_q8_1_ptr(x.data_ptr(), q.data_ptr(), d.data_ptr(), s.data_ptr(), M, K, _stream_handle(stream))
     return q, d, s
 
 
 def qmv_q2w(W, x, y=None, stream=None):
     """y[M, N] = x[M, K] @ dequant(W)^T for plain 2-bit weights (10-byte blocks)."""
     W, x, y, N, K, M = _prep(W, x, y, Q2W_BLOCK_BYTES, "qmv_q2w")
-    qmv_q2w_ptr(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, _stream_handle(stream))
+    with _on_device("qmv_q2w", W, x, y):
+        qmv_q2w_ptr(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, _stream_handle(stream))
     return y
 
 
 def qmm_q4_0_prefill(W, x, y=None, stream=None):
     """Many-token (prefill) form of qmv_q4_0 on the tensor cores."""
     W, x, y, N, K, M = _prep(W, x, y, Q4_0_BLOCK_BYTES, "qmm_q4_0_prefill")
-    qmm_q4_0_prefill_ptr(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, _stream_handle(stream))
+    with _on_device("qmm_q4_0_prefill", W, x, y):
+        qmm_q4_0_prefill_ptr(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, _stream_handle(stream))
     return y
 
 
@@ -315,6 +347,8 @@ def qmv_moe(W_pool, expert_idx, n_experts, x, N, y=None, stream=None):
         raise TypeError("qmv_moe: W_pool must be uint8, x float16")
     if x.dim() == 1:
         x = x.unsqueeze(0)
+    if not (W_pool.is_contiguous() and x.is_contiguous()):
+        raise ValueError("qmv_moe: W_pool and x must be contiguous")
     M, K = x.shape
     if expert_idx.numel() != M:
         raise ValueError("qmv_moe: one expert index per token")
@@ -323,8 +357,11 @@ def qmv_moe(W_pool, expert_idx, n_experts, x, N, y=None, stream=None):
         raise ValueError(f"qmv_moe: W_pool holds {W_pool.numel()} bytes, needs {need}")
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=x.device)
-    qmv_moe_ptr(W_pool.data_ptr(), expert_idx.data_ptr(), int(n_experts), x.data_ptr(), y.data_ptr(),
-                int(N), int(K), int(M), _stream_handle(stream))
+    else:
+        _check_y(y, M, N, "qmv_moe")
+    with _on_device("qmv_moe", W_pool, expert_idx, x, y):
+        qmv_moe_ptr(W_pool.data_ptr(), expert_idx.data_ptr(), int(n_experts), x.data_ptr(), y.data_ptr(),
+                    int(N), int(K), int(M), _stream_handle(stream))
     return y
 
 
