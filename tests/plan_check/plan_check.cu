@@ -320,6 +320,16 @@ int main()
                 check_swiglu(N, K, M);
                 check_plan(kQ4_0, N, K, M, 1, true);
             }
+    // every shape of the measured launch table, in each call form that can look it up
+    for (const TuneEntry &e : kTuneTable) {
+        const int f = e.fmt == 3 ? kQ4_0 : e.fmt;
+        check_plan(f, e.N, e.K, e.M, 1, e.fmt == 3);
+        if (e.fmt == kQ4_0) {
+            for (int slots : {8, 10}) check_plan(kQ4_0, e.N, e.K, 1, slots, false);
+            check_swiglu(e.N, e.K, e.M);
+            if (e.N % 2 == 0) check_swiglu(e.N / 2, e.K, e.M);
+        }
+    }
     const int64_t pN[] = {1, 127, 128, 129, 640, 4096, 14336, 128256, (int64_t(1) << 31) - 1};
     const int64_t pK[] = {32, 256, 512, 2560, 4096, 14336, (int64_t(1) << 30) - 256, int64_t(1) << 30};
     const int64_t pM[] = {1,   2,   63,   64,    65,    127,    128,           129,               192,
