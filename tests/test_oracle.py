@@ -459,6 +459,23 @@ def test_q8_1_product_integer_case_matches_numpy(orc):
     assert np.array_equal(S, np.abs(x).astype(np.float64) @ np.abs(Wi).T)
 
 
+def test_q8_1_product_integer_case_q8_0(orc):
+    # Q8_0 with d = 1 and codes over the whole signed range, against activations
+    # whose every block has max |x| = 127: y is the integer matmul of the codes
+    rng = np.random.default_rng(84)
+    N, K, M = 5, 512, 3
+    codes = rng.integers(-128, 128, size=(N, K))
+    W = H.encode_q8_0(codes, np.full((N, K // 32), 0x3C00, dtype=np.uint16))
+    x = rng.integers(-127, 128, size=(M, K))
+    x.reshape(M, K // 32, 32)[:, :, 31] = -127
+    q, d, s = orc.quantize_q8_1(x.astype(np.float16))
+    assert np.array_equal(q, x) and np.all(d == 0x3C00)
+    y, S = orc.qmv_q8_1(1, W, q, d, N, K)
+    Wi = codes.astype(np.float64)
+    assert np.array_equal(y, x.astype(np.float64) @ Wi.T)
+    assert np.array_equal(S, np.abs(x).astype(np.float64) @ np.abs(Wi).T)
+
+
 def test_q8_1_product_is_the_product_on_dequantised_x(orc):
     N, K, M = 9, 768, 3
     W, x = _rand("q4_0", N, K, M, 83)
