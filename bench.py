@@ -80,6 +80,12 @@ WORKLOADS = {
     "q4_0_q8_1_pre": {"kind": "gemv", "fmt": "q4_0", "x": "q8_1_pre", "M": [1, 8], "dtype": "i8",
                       "shapes": [(4096, 4096), (6144, 4096), (4096, 14336), (14336, 4096), (28672, 4096),
                                  (128256, 4096)]},
+    # The Q8_0 tables against activations quantised to Q8_1, signed int8 dots
+    # (the Q8_1 form carried from Q4_0 to Q8_0): fused, and in two launches.
+    "q8_0_q8_1": {"kind": "gemv", "fmt": "q8_0", "x": "q8_1", "M": [1, 2, 4, 8], "dtype": "i8",
+                  "shapes": [(12288, 2560), (2560, 6144), (8192, 2048)]},
+    "q8_0_q8_1_pre": {"kind": "gemv", "fmt": "q8_0", "x": "q8_1_pre", "M": [1, 2, 4, 8], "dtype": "i8",
+                      "shapes": [(12288, 2560), (2560, 6144), (8192, 2048)]},
     # Plain 2-bit (codes -2..1, fp16 scale per 32): the bakeoff's six one-token
     # tables (volta-kernel-bakeoff, "Results (one token, microseconds, lower is
     # better)", its 2-bit column).
@@ -275,7 +281,7 @@ def run_ours(args, dist, rank, local, world):
         if xb == 4:
             fn_ptr = q.qmv_q4_0_f32_ptr
         if wl.get("x") == "q8_1":
-            fn_ptr = q.qmv_q4_0_q8_1_ptr
+            fn_ptr = {"q4_0": q.qmv_q4_0_q8_1_ptr, "q8_0": q.qmv_q8_0_q8_1_ptr}[fmt]
         pre = wl.get("x") == "q8_1_pre"
         for (N, K) in wl["shapes"]:
             Wd, copies = rotated_copies(N, K, f"{fmt}_{N}x{K}")
@@ -297,8 +303,13 @@ def run_ours(args, dist, rank, local, world):
                         W = c["W"][s % c["copies"]]
                         q.qmv_quantize_q8_1_ptr(c["x"].data_ptr(), c["xq"].data_ptr(), c["xq_d"].data_ptr(),
                                                 c["xq_s"].data_ptr(), c["M"], c["K"], sh)
-                        q.qmv_q4_0_q8_1_pre_ptr(W.data_ptr(), c["xq"].data_ptr(), c["xq_d"].data_ptr(),
-                                                c["xq_s"].data_ptr(), c["y"].data_ptr(), c["N"], c["K"], c["M"], sh)
+                        if fmt == "q8_0":   # Q8_0 codes carry no offset: no code sums
+                            q.qmv_q8_0_q8_1_pre_ptr(W.data_ptr(), c["xq"].data_ptr(), c["xq_d"].data_ptr(),
+                                                    c["y"].data_ptr(), c["N"], c["K"], c["M"], sh)
+                        else:
+                            q.qmv_q4_0_q8_1_pre_ptr(W.data_ptr(), c["xq"].data_ptr(), c["xq_d"].data_ptr(),
+                                                    c["xq_s"].data_ptr(), c["y"].data_ptr(), c["N"], c["K"], c["M"],
+                                                    sh)
                 else:
                     def call(s, c=c):
                         W = c["W"][s % c["copies"]]

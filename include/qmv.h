@@ -159,6 +159,33 @@ QMV_API qmv_status qmv_q4_0_q8_1_pre(const void *W, const int8_t *q, const uint1
                              float *y, int64_t N, int64_t K, int64_t M, qmv_stream_t stream);
 
 /*
+ * Q8_0 decode GEMV against activations quantised to Q8_1, with signed integer
+ * dots.  The pages give the Q8_1 integer dot for Q4_0 weights only
+ * (sm8x-bench, "Our kernel does what llama.cpp does"); this call carries it to
+ * Q8_0, whose codes are already signed bytes, so a block's dot is a plain
+ * int8 x int8 sum with no nibble split and no code-sum correction:
+ *     y[m][n] = sum over blocks b of d_w * d_x[m][b] * sum_i c_i * q[m][i].
+ * Quantisation of the activations, error bound against the exact product and
+ * the kernel's rounding as for qmv_q4_0_q8_1.
+ *   W : Q8_0 bytes [N][K/32*34], 16-byte aligned; x fp16 [M][K].
+ *   y, N, K, M (<= 8), errors and asynchrony as for qmv_q8_0.
+ */
+QMV_API qmv_status qmv_q8_0_q8_1(const void *W, const void *x, float *y,
+                         int64_t N, int64_t K, int64_t M, qmv_stream_t stream);
+
+/*
+ * qmv_q8_0_q8_1 with the activations already in Q8_1 (as qmv_quantize_q8_1
+ * writes them; the code sums are not needed).  Equal to qmv_q8_0_q8_1 on the
+ * fp16 activations those blocks came from, bit for bit.
+ *   q      : DEVICE int8 [M][K], 16-byte aligned (K % 256 == 0 for the
+ *            streaming kernel; other K run the generic kernel).
+ *   d_bits : DEVICE uint16 [M][K/32] (fp16 scales), 2-byte aligned.
+ *   W, y, N, K, M (<= 8), errors and asynchrony as for qmv_q8_0.
+ */
+QMV_API qmv_status qmv_q8_0_q8_1_pre(const void *W, const int8_t *q, const uint16_t *d_bits,
+                             float *y, int64_t N, int64_t K, int64_t M, qmv_stream_t stream);
+
+/*
  * Plain 2-bit decode GEMV (the bakeoff's q2w format: codes -2..1 with one fp16
  * scale per 32 weights, 2.5 bits per weight -- volta-kernel-bakeoff, "What's
  * in the race" and the Results table's 2-bit column), same contract as

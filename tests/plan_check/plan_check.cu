@@ -319,11 +319,12 @@ int main()
             for (int M = 1; M <= 8; ++M) {
                 check_swiglu(N, K, M);
                 check_plan(kQ4_0, N, K, M, 1, true);
+                check_plan(kQ8_0, N, K, M, 1, true);
             }
     // every shape of the measured launch table, in each call form that can look it up
     for (const TuneEntry &e : kTuneTable) {
-        const int f = e.fmt == 3 ? kQ4_0 : e.fmt;
-        check_plan(f, e.N, e.K, e.M, 1, e.fmt == 3);
+        const int f = e.fmt == 3 ? kQ4_0 : (e.fmt == 4 ? kQ8_0 : e.fmt);
+        check_plan(f, e.N, e.K, e.M, 1, e.fmt >= 3);
         if (e.fmt == kQ4_0) {
             for (int slots : {8, 10}) check_plan(kQ4_0, e.N, e.K, 1, slots, false);
             check_swiglu(e.N, e.K, e.M);

@@ -15,6 +15,7 @@ QMV_STUB_GEMV(launch_gemv_stream_q2w)
 QMV_STUB_GEMV(launch_gemv_stream_q4_0_swiglu)
 QMV_STUB_GEMV(launch_gemv_stream_q4_0_swiglu_f32)
 QMV_STUB_GEMV(launch_gemv_stream_q4_0_q8_1)
+QMV_STUB_GEMV(launch_gemv_stream_q8_0_q8_1)
 #undef QMV_STUB_GEMV
 
 cudaError_t launch_quantize_q8_1(const void *, int8_t *, uint16_t *, int32_t *, int64_t, int64_t, cudaStream_t, bool)

@@ -53,7 +53,7 @@ FAKE = 1 << 20      # a 16-byte-aligned non-null address; never dereferenced her
 
 
 @pytest.mark.parametrize("fn", ["qmv_q4_0", "qmv_q8_0", "qmm_q4_0_prefill", "qmv_q4_0_f32", "qmv_q2w",
-                                "qmv_q4_0_q8_1"])
+                                "qmv_q4_0_q8_1", "qmv_q8_0_q8_1"])
 def test_host_validation(lib, fn):
     f = getattr(lib, fn)
     assert f(None, FAKE, FAKE, 8, 256, 1, None) == 1          # NULL W
@@ -93,6 +93,20 @@ def test_host_validation_swiglu(lib, fn):
     assert f(None, None, None, None, 8, 256, 0, None) == 0
     if fn.endswith("_f32"):
         assert f(FAKE, FAKE, FAKE + 2, FAKE, 8, 256, 1, None) == 2   # fp32 x not 4-byte aligned
+
+
+def test_host_validation_q8_0_q8_1_pre(lib):
+    f = lib.qmv_q8_0_q8_1_pre
+    assert f(None, FAKE, FAKE, FAKE, 8, 256, 1, None) == 1        # NULL W
+    assert f(FAKE, None, FAKE, FAKE, 8, 256, 1, None) == 1        # NULL codes
+    assert f(FAKE, FAKE, None, FAKE, 8, 256, 1, None) == 1        # NULL scales
+    assert f(FAKE, FAKE, FAKE, None, 8, 256, 1, None) == 1        # NULL y
+    assert f(FAKE + 8, FAKE, FAKE, FAKE, 8, 256, 1, None) == 2    # W not 16-byte aligned
+    assert f(FAKE, FAKE, FAKE + 1, FAKE, 8, 256, 1, None) == 2    # scales not 2-byte aligned
+    assert f(FAKE, FAKE, FAKE, FAKE, 8, 250, 1, None) == 3        # K % 32
+    assert f(FAKE, FAKE, FAKE, FAKE, 8, 256, 9, None) == 3        # M <= 8
+    assert f(None, None, None, None, 0, 256, 1, None) == 0        # empty
+    assert f(None, None, None, None, 8, 256, 0, None) == 0
 
 
 def test_host_validation_quantize_q8_1(lib):

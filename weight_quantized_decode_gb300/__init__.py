@@ -58,7 +58,8 @@ def lib():
                                "(there is no CPU fallback)")
         L = ctypes.CDLL(LIB_PATH)
         vp, i64 = ctypes.c_void_p, ctypes.c_int64
-        for name in ("qmv_q4_0", "qmv_q8_0", "qmm_q4_0_prefill", "qmv_q4_0_f32", "qmv_q2w", "qmv_q4_0_q8_1"):
+        for name in ("qmv_q4_0", "qmv_q8_0", "qmm_q4_0_prefill", "qmv_q4_0_f32", "qmv_q2w", "qmv_q4_0_q8_1",
+                     "qmv_q8_0_q8_1"):
             f = getattr(L, name)
             f.restype = ctypes.c_int
             f.argtypes = [vp, vp, vp, i64, i64, i64, vp]
@@ -68,6 +69,8 @@ def lib():
         L.qmv_q4_0_swiglu.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
         L.qmv_q4_0_q8_1_pre.restype = ctypes.c_int
         L.qmv_q4_0_q8_1_pre.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, vp]
+        L.qmv_q8_0_q8_1_pre.restype = ctypes.c_int
+        L.qmv_q8_0_q8_1_pre.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
         L.qmv_quantize_q8_1.restype = ctypes.c_int
         L.qmv_quantize_q8_1.argtypes = [vp, vp, vp, vp, i64, i64, vp]
         L.qmv_q4_0_swiglu_f32.restype = ctypes.c_int
@@ -132,6 +135,14 @@ def qmv_q4_0_q8_1_ptr(W: int, x: int, y: int, N: int, K: int, M: int, stream: in
 def qmv_q4_0_q8_1_pre_ptr(W: int, q: int, d_bits: int, sumq: int, y: int, N: int, K: int, M: int,
                           stream: int = 0) -> None:
     _check("qmv_q4_0_q8_1_pre", lib().qmv_q4_0_q8_1_pre(W, q, d_bits, sumq, y, N, K, M, stream))
+
+
+def qmv_q8_0_q8_1_ptr(W: int, x: int, y: int, N: int, K: int, M: int, stream: int = 0) -> None:
+    _check("qmv_q8_0_q8_1", lib().qmv_q8_0_q8_1(W, x, y, N, K, M, stream))
+
+
+def qmv_q8_0_q8_1_pre_ptr(W: int, q: int, d_bits: int, y: int, N: int, K: int, M: int, stream: int = 0) -> None:
+    _check("qmv_q8_0_q8_1_pre", lib().qmv_q8_0_q8_1_pre(W, q, d_bits, y, N, K, M, stream))
 
 
 def qmv_quantize_q8_1_ptr(x: int, q: int, d_bits: int, sumq: int, M: int, K: int, stream: int = 0) -> None:
@@ -273,32 +284,59 @@ def qmv_q4_0_q8_1(W, x, y=None, stream=None):
     return y
 
 
-def qmv_q4_0_q8_1_pre(W, q, d_bits, sumq, y=None, stream=None):
-    """qmv_q4_0_q8_1 on activations already in Q8_1 (q int8 [M, K], d_bits int16
-    [M, K/32], sumq int32 [M, K/32], as qmv_quantize_q8_1 returns them)."""
+def _prep_pre(W, q, d_bits, sumq, y, block_bytes, fn):
+    """Checks shared by the calls on activations already in Q8_1 (sumq may be None)."""
     torch = _torch()
-    if not (W.is_cuda and q.is_cuda and d_bits.is_cuda and sumq.is_cuda):
-        raise TypeError("qmv_q4_0_q8_1_pre: all tensors must be on a CUDA device (no CPU path)")
-    if W.dtype != torch.uint8 or q.dtype != torch.int8 or d_bits.dtype != torch.int16 or sumq.dtype != torch.int32:
-        raise TypeError("qmv_q4_0_q8_1_pre: W uint8, q int8, d_bits int16, sumq int32")
+    tensors = [W, q, d_bits] + ([sumq] if sumq is not None else [])
+    if not all(t.is_cuda for t in tensors):
+        raise TypeError(f"{fn}: all tensors must be on a CUDA device (no CPU path)")
+    if W.dtype != torch.uint8 or q.dtype != torch.int8 or d_bits.dtype != torch.int16 or \
+            (sumq is not None and sumq.dtype != torch.int32):
+        raise TypeError(f"{fn}: W uint8, q int8, d_bits int16" + (", sumq int32" if sumq is not None else ""))
     if q.dim() == 1:
         q = q.unsqueeze(0)
     M, K = q.shape
-    if K % 32 or d_bits.numel() != M * (K // 32) or sumq.numel() != M * (K // 32):
-        raise ValueError("qmv_q4_0_q8_1_pre: q [M, K] with K % 32 == 0, d_bits and sumq [M, K/32]")
-    if not (W.is_contiguous() and q.is_contiguous() and d_bits.is_contiguous() and sumq.is_contiguous()):
-        raise ValueError("qmv_q4_0_q8_1_pre: tensors must be contiguous")
-    row_bytes = (K // 32) * Q4_0_BLOCK_BYTES
+    if K % 32 or d_bits.numel() != M * (K // 32) or (sumq is not None and sumq.numel() != M * (K // 32)):
+        raise ValueError(f"{fn}: q [M, K] with K % 32 == 0, d_bits" + (" and sumq" if sumq is not None else "")
+                         + " [M, K/32]")
+    if not all(t.is_contiguous() for t in tensors):
+        raise ValueError(f"{fn}: tensors must be contiguous")
+    row_bytes = (K // 32) * block_bytes
     if row_bytes and W.numel() % row_bytes:
-        raise ValueError(f"qmv_q4_0_q8_1_pre: W size {W.numel()} is not a whole number of rows of {row_bytes} bytes")
+        raise ValueError(f"{fn}: W size {W.numel()} is not a whole number of rows of {row_bytes} bytes")
     N = W.numel() // row_bytes if row_bytes else (W.shape[0] if W.dim() >= 1 else 0)
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=q.device)
     else:
-        _check_y(y, M, N, "qmv_q4_0_q8_1_pre")
+        _check_y(y, M, N, fn)
+    return q, y, N, K, M
+
+
+def qmv_q4_0_q8_1_pre(W, q, d_bits, sumq, y=None, stream=None):
+    """qmv_q4_0_q8_1 on activations already in Q8_1 (q int8 [M, K], d_bits int16
+    [M, K/32], sumq int32 [M, K/32], as qmv_quantize_q8_1 returns them)."""
+    q, y, N, K, M = _prep_pre(W, q, d_bits, sumq, y, Q4_0_BLOCK_BYTES, "qmv_q4_0_q8_1_pre")
     with _on_device("qmv_q4_0_q8_1_pre", W, q, d_bits, sumq, y):
         qmv_q4_0_q8_1_pre_ptr(W.data_ptr(), q.data_ptr(), d_bits.data_ptr(), sumq.data_ptr(), y.data_ptr(), N, K,
                               M, _stream_handle(stream))
+    return y
+
+
+def qmv_q8_0_q8_1(W, x, y=None, stream=None):
+    """qmv_q8_0 with the activations quantised to Q8_1 in the kernel (signed integer dots)."""
+    W, x, y, N, K, M = _prep(W, x, y, Q8_0_BLOCK_BYTES, "qmv_q8_0_q8_1")
+    with _on_device("qmv_q8_0_q8_1", W, x, y):
+        qmv_q8_0_q8_1_ptr(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, _stream_handle(stream))
+    return y
+
+
+def qmv_q8_0_q8_1_pre(W, q, d_bits, y=None, stream=None):
+    """qmv_q8_0_q8_1 on activations already in Q8_1 (q int8 [M, K], d_bits int16
+    [M, K/32]; the code sums qmv_quantize_q8_1 also returns are not needed)."""
+    q, y, N, K, M = _prep_pre(W, q, d_bits, None, y, Q8_0_BLOCK_BYTES, "qmv_q8_0_q8_1_pre")
+    with _on_device("qmv_q8_0_q8_1_pre", W, q, d_bits, y):
+        qmv_q8_0_q8_1_pre_ptr(W.data_ptr(), q.data_ptr(), d_bits.data_ptr(), y.data_ptr(), N, K, M,
+                              _stream_handle(stream))
     return y
 
 

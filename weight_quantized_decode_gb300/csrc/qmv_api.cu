@@ -170,9 +170,9 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
     // stacked row by row) is planned as one table of rows_total rows; the
     // multi-expert call by its per-expert shape.
     const int64_t Nplan = p.n_problems == 1 ? p.rows_total : p.N;
-    // Q4_0 against Q8_1 activations has its own entries (table format 3): its
-    // per-unit arithmetic differs from the fp16 path's.
-    const TuneEntry *te = tune_lookup(p.xq8 ? 3 : fmt, Nplan, p.K, M);
+    // Q4_0 and Q8_0 against Q8_1 activations have their own entries (table
+    // formats 3 and 4): their per-unit arithmetic differs from the fp16 path's.
+    const TuneEntry *te = tune_lookup(p.xq8 ? (fmt == kQ8_0 ? 4 : 3) : fmt, Nplan, p.K, M);
     const Tune none{};
     const bool tu_applies = (tu_all.N == 0 || tu_all.N == Nplan) && (tu_all.K == 0 || tu_all.K == p.K) &&
                             (tu_all.M == 0 || tu_all.M == M);
@@ -265,6 +265,7 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
 cudaError_t launch_streaming(int fmt, const GemvParams &p, int M, const Plan &pl, cudaStream_t stream, bool pdl)
 {
     if (fmt == kQ4_0 && p.xq8) return launch_gemv_stream_q4_0_q8_1(M, p, pl.grid, pl.warps, pl.smem, stream, pdl);
+    if (fmt == kQ8_0 && p.xq8) return launch_gemv_stream_q8_0_q8_1(M, p, pl.grid, pl.warps, pl.smem, stream, pdl);
     if (fmt == kQ4_0 && p.W2) return launch_gemv_stream_q4_0_swiglu(M, p, pl.grid, pl.warps, pl.smem, stream, pdl);
     if (fmt == kQ4_0)
         return p.xf ? launch_gemv_stream_q4_0_f32(M, p, pl.grid, pl.warps, pl.smem, stream, pdl)
@@ -452,6 +453,26 @@ qmv_status qmv_q4_0_q8_1_pre(const void *W, const int8_t *q, const uint16_t *d_b
     if ((d_bits && !aligned(d_bits, 2)) || (sumq && !aligned(sumq, 4))) return QMV_ERR_ALIGN;
     return run_gemv(kQ4_0, W, nullptr, 1, nullptr, y, N, K, M, 1, reinterpret_cast<cudaStream_t>(stream), nullptr,
                     nullptr, true, q, d_bits, sumq);
+}
+
+qmv_status qmv_q8_0_q8_1(const void *W, const void *x, float *y, int64_t N, int64_t K, int64_t M,
+                         qmv_stream_t stream)
+{
+    qmv_status st = check_common(W, x, y, N, K, M, 8);
+    if (st != QMV_OK || N == 0 || M == 0) return st;
+    return run_gemv(kQ8_0, W, nullptr, 1, x, y, N, K, M, 1, reinterpret_cast<cudaStream_t>(stream), nullptr,
+                    nullptr, true);
+}
+
+qmv_status qmv_q8_0_q8_1_pre(const void *W, const int8_t *q, const uint16_t *d_bits, float *y, int64_t N,
+                             int64_t K, int64_t M, qmv_stream_t stream)
+{
+    qmv_status st = check_common(W, q, y, N, K, M, 8);
+    if (st != QMV_OK || N == 0 || M == 0) return st;
+    if (K > 0 && !d_bits) return QMV_ERR_NULL;
+    if (d_bits && !aligned(d_bits, 2)) return QMV_ERR_ALIGN;
+    return run_gemv(kQ8_0, W, nullptr, 1, nullptr, y, N, K, M, 1, reinterpret_cast<cudaStream_t>(stream), nullptr,
+                    nullptr, true, q, d_bits, nullptr);
 }
 
 qmv_status qmv_quantize_q8_1(const void *x, int8_t *q, uint16_t *d_bits, int32_t *sumq, int64_t M, int64_t K,

@@ -94,7 +94,7 @@ struct GemvParams {
     int G;                       // lanes per row (1..32; RG = 32 / G rows per warp)
     int SP;                      // passes per stage (odd)
     int S;                       // stages in each warp's ring
-    int xq8;                     // Q4_0 against Q8_1-quantised activations (integer dots)
+    int xq8;                     // Q4_0 or Q8_0 against Q8_1-quantised activations (integer dots)
     const int8_t *xq;            // activations already in Q8_1 (codes [M][K]); else quantised in the kernel
     const uint16_t *xq_d;        //   their fp16 scales' bits [M][K/32]
     const int32_t *xq_s;         //   and code sums [M][K/32]
@@ -431,6 +431,59 @@ __device__ __forceinline__ void dot_unit_q4_0_q81(const uint8_t *wsrc, const uin
     }
 }
 
+// Q8_0 against Q8_1 activations: both operands are signed bytes, so a block's
+// dot is eight signed dp4a and its contribution d_w * d_x * sum(c_w * c_x); the
+// codes carry no offset, so the activations' code sums are not needed.  An
+// even block's codes start 2 bytes into a 4-byte word: each of its code words
+// is re-formed from two adjacent words with one PRMT (the activations are
+// staged in natural order).
+template <int M>
+__device__ __forceinline__ void dot_unit_q8_0_q81(const uint8_t *wsrc, const uint8_t *xsrc, int xstride,
+                                                  float (&acc)[M])
+{
+    uint32_t w[68];
+#pragma unroll
+    for (int c = 0; c < 17; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(wsrc + 16 * c);
+        w[4 * c + 0] = v.x;
+        w[4 * c + 1] = v.y;
+        w[4 * c + 2] = v.z;
+        w[4 * c + 3] = v.w;
+    }
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+        const int h = b >> 1;
+        uint32_t qw[8];
+        uint32_t dsrc;
+        if ((b & 1) == 0) {
+            dsrc = w[17 * h] & 0xffffu;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) qw[k] = __byte_perm(w[17 * h + k], w[17 * h + k + 1], 0x5432);
+        } else {
+            dsrc = w[17 * h + 8] >> 16;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) qw[k] = w[17 * h + 9 + k];
+        }
+        const float dw = half_lo_to_float(dsrc);
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            const uint8_t *xp = xsrc + m * xstride;
+            const uint4 x0 = *reinterpret_cast<const uint4 *>(xp + b * 32);
+            const uint4 x1 = *reinterpret_cast<const uint4 *>(xp + b * 32 + 16);
+            const float dx = *reinterpret_cast<const float *>(xp + 256 + b * 8);
+            int s = __dp4a(static_cast<int>(qw[0]), static_cast<int>(x0.x), 0);
+            s = __dp4a(static_cast<int>(qw[1]), static_cast<int>(x0.y), s);
+            s = __dp4a(static_cast<int>(qw[2]), static_cast<int>(x0.z), s);
+            s = __dp4a(static_cast<int>(qw[3]), static_cast<int>(x0.w), s);
+            s = __dp4a(static_cast<int>(qw[4]), static_cast<int>(x1.x), s);
+            s = __dp4a(static_cast<int>(qw[5]), static_cast<int>(x1.y), s);
+            s = __dp4a(static_cast<int>(qw[6]), static_cast<int>(x1.z), s);
+            s = __dp4a(static_cast<int>(qw[7]), static_cast<int>(x1.w), s);
+            acc[m] = fmaf(static_cast<float>(s), dw * dx, acc[m]);
+        }
+    }
+}
+
 // ---- the streaming kernel ----------------------------------------------------------
 
 // Warp-collective wait for phase `parity` of `bar`: one vote when the stage
@@ -459,7 +512,8 @@ template <int FMT, int M, int MAXT, bool MOE, bool SWIGLU = false, bool XF32 = f
 __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p)
 {
     using T = FmtTraits<FMT>;
-    static_assert(!XQ8 || (FMT == kQ4_0 && !MOE && !SWIGLU && !XF32), "Q8_1 activations: plain Q4_0 calls only");
+    static_assert(!XQ8 || ((FMT == kQ4_0 || FMT == kQ8_0) && !MOE && !SWIGLU && !XF32),
+                  "Q8_1 activations: plain Q4_0 and Q8_0 calls only");
     constexpr int XUB = XQ8 ? kXQ8UnitBytes : kXUnitBytes;   // activation bytes per unit and token
     constexpr float kPre = XQ8 ? 1.0f : T::kPrescale;           // the integer dot carries no pre-scale
     extern __shared__ __align__(128) uint8_t smem[];
@@ -590,8 +644,10 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
             const int tok = it / nb, blk = it - tok * nb;
             const int64_t j = static_cast<int64_t>(tok) * nb + blk;
             const float dxq = __half2float(__ushort_as_half(__ldg(p.xq_d + j)));
+            int sum8 = 0;   // Q8_0 codes carry no offset: the code sums are not read
+            if constexpr (FMT == kQ4_0) sum8 = 8 * __ldg(p.xq_s + j);
             *reinterpret_cast<float2 *>(xs + static_cast<size_t>(tok) * U * XUB + (blk >> 3) * XUB + 256 +
-                                        (blk & 7) * 8) = make_float2(dxq, __int_as_float(8 * __ldg(p.xq_s + j)));
+                                        (blk & 7) * 8) = make_float2(dxq, __int_as_float(sum8));
         }
         for (int i = early; i < prefetch; ++i) issue_next();
     } else if constexpr (XQ8) {
@@ -816,7 +872,9 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
             for (int pass = 0; pass < SP; ++pass) {
                 const int u = u0 + pass * G;
                 if (u < U) {
-                    if constexpr (XQ8)
+                    if constexpr (XQ8 && FMT == kQ8_0)
+                        dot_unit_q8_0_q81<M>(stage + (pass * G + q) * T::kUnitBytes, xrow + u * XUB, xstride, acc);
+                    else if constexpr (XQ8)
                         dot_unit_q4_0_q81<M>(stage + (pass * G + q) * T::kUnitBytes, xrow + u * XUB, xstride, acc);
                     else if (FMT == kQ4_0)
                         dot_unit_q4_0<M>(stage + (pass * G + q) * T::kUnitBytes, xrow + u * kXUnitBytes, xstride, acc);
@@ -907,6 +965,15 @@ __device__ __forceinline__ float load_x(const GemvParams &p, int64_t i)
     return p.xf ? __half2float(__float2half_rn(p.xf[i])) : __half2float(p.x[i]);
 }
 
+// Signed code of weight j of a block (before its scale), for the generic kernel.
+template <int FMT>
+__device__ __forceinline__ int weight_code(const uint8_t *blk, int j)
+{
+    if (FMT == kQ4_0) return (j < 16 ? (blk[2 + j] & 0xF) : (blk[2 + j - 16] >> 4)) - 8;
+    if (FMT == kQ2W) return ((blk[2 + (j & 7)] >> (2 * (j >> 3))) & 3) - 2;
+    return static_cast<int8_t>(blk[2 + j]);
+}
+
 template <int FMT>
 __global__ void __launch_bounds__(256) gemv_generic_kernel(const GemvParams p, int M)
 {
@@ -956,10 +1023,7 @@ __global__ void __launch_bounds__(256) gemv_generic_kernel(const GemvParams p, i
                             float dxq;
                             if (p.xq) {   // activations already in Q8_1
                                 const int8_t *qb = p.xq + tok * p.K + b * 32;
-                                for (int j = 0; j < 32; ++j) {
-                                    const int c = (j < 16 ? (blk[2 + j] & 0xF) : (blk[2 + j - 16] >> 4)) - 8;
-                                    s += c * qb[j];
-                                }
+                                for (int j = 0; j < 32; ++j) s += weight_code<FMT>(blk, j) * qb[j];
                                 dxq = __half2float(__ushort_as_half(p.xq_d[tok * (p.K / 32) + b]));
                             } else {
                                 const __half *xb = p.x + tok * p.K + b * 32;
@@ -969,8 +1033,7 @@ __global__ void __launch_bounds__(256) gemv_generic_kernel(const GemvParams p, i
                                 const float id = d != 0.0f ? __frcp_rn(d) : 0.0f;
                                 for (int j = 0; j < 32; ++j) {
                                     const int code = static_cast<int>(roundf(__fmul_rn(__half2float(xb[j]), id)));
-                                    const int c = (j < 16 ? (blk[2 + j] & 0xF) : (blk[2 + j - 16] >> 4)) - 8;
-                                    s += c * code;
+                                    s += weight_code<FMT>(blk, j) * code;
                                 }
                                 dxq = __half2float(__float2half_rn(d));
                             }
@@ -984,11 +1047,7 @@ __global__ void __launch_bounds__(256) gemv_generic_kernel(const GemvParams p, i
                         const float d = __half2float(__ushort_as_half(
                             static_cast<unsigned short>(blk[0] | (blk[1] << 8))));
                         for (int j = 0; j < 32; ++j) {
-                            int c;
-                            if (FMT == kQ4_0) c = (j < 16 ? (blk[2 + j] & 0xF) : (blk[2 + j - 16] >> 4)) - 8;
-                            else if (FMT == kQ2W) c = ((blk[2 + (j & 7)] >> (2 * (j >> 3))) & 3) - 2;
-                            else c = static_cast<int8_t>(blk[2 + j]);
-                            const float wv = static_cast<float>(c) * d;
+                            const float wv = static_cast<float>(weight_code<FMT>(blk, j)) * d;
 #pragma unroll
                             for (int mm = 0; mm < 8; ++mm) {
                                 if (m0 + mm < M)

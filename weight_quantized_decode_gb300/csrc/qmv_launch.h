@@ -24,6 +24,9 @@ cudaError_t launch_gemv_stream_q4_0_f32(int M, const GemvParams &p, int grid, in
 // Q4_0 against Q8_1-quantised activations (plain form only; p.xq8 set).
 cudaError_t launch_gemv_stream_q4_0_q8_1(int M, const GemvParams &p, int grid, int warps, size_t smem,
                                          cudaStream_t s, bool pdl);
+// Q8_0 against Q8_1-quantised activations (plain form only; p.xq8 set).
+cudaError_t launch_gemv_stream_q8_0_q8_1(int M, const GemvParams &p, int grid, int warps, size_t smem,
+                                         cudaStream_t s, bool pdl);
 // Q8_1 quantisation of fp16 activations [M][K] (K % 32 == 0, x 16-byte aligned).
 cudaError_t launch_quantize_q8_1(const void *x, int8_t *q, uint16_t *d_bits, int32_t *sumq, int64_t M, int64_t K,
                                  cudaStream_t s, bool pdl);
