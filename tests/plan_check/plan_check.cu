@@ -304,8 +304,8 @@ int main()
 {
     const int64_t Ns[] = {1,   2,   7,    9,    16,   20,   33,   40,   64,    77,    96,    100,   130,   300,
                           333, 515, 600,  640,  1000, 2560, 4096, 4133, 6144,  8192,  12288, 14336, 28672, 128256};
-    const int64_t Ks[] = {256,  512,  768,  1024, 2048, 2304, 2560,  2816,
-                          3072, 3328, 3584, 3840, 4096, 6144, 8192, 14336};
+    const int64_t Ks[] = {256,  512,  768,  1024, 2048, 2304, 2560, 2816, 3072,
+                          3328, 3584, 3840, 4096, 5632, 6144, 6912, 8192, 14336};
     for (int fmt : {kQ4_0, kQ8_0, kQ2W})
         for (int64_t N : Ns)
             for (int64_t K : Ks)

@@ -52,12 +52,15 @@ def _calls(q):
         "swiglu_f32": lambda s: q.qmv_q4_0_swiglu_f32(W4, Wu, xf, stream=s),
         "q8_1": lambda s: q.qmv_q4_0_q8_1(W4, x, stream=s),
         "q8_1_pre": lambda s: q.qmv_q4_0_q8_1_pre(W4, qc, qd, qs, stream=s),
+        "q8_0_q8_1": lambda s: q.qmv_q8_0_q8_1(W8, x, stream=s),
+        "q8_0_q8_1_pre": lambda s: q.qmv_q8_0_q8_1_pre(W8, qc, qd, stream=s),
         "moe": lambda s: q.qmv_moe(pool, idx, 16, xe, 128, stream=s),
         "prefill": lambda s: q.qmm_q4_0_prefill(Wp, xp, stream=s),
     }
 
 
-NAMES = ["q4_0", "q8_0", "q2w", "q4_0_f32", "swiglu", "swiglu_f32", "q8_1", "q8_1_pre", "moe", "prefill"]
+NAMES = ["q4_0", "q8_0", "q2w", "q4_0_f32", "swiglu", "swiglu_f32", "q8_1", "q8_1_pre", "q8_0_q8_1", "q8_0_q8_1_pre",
+         "moe", "prefill"]
 
 
 @pytest.mark.parametrize("name", NAMES)
