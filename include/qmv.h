@@ -125,8 +125,8 @@ QMV_API qmv_status qmv_q4_0_q8_1(const void *W, const void *x, float *y,
                          int64_t N, int64_t K, int64_t M, qmv_stream_t stream);
 
 /*
- * Q8_1 quantisation of fp16 activations, exactly as qmv_q4_0_q8_1 performs it
- * inside its kernel: per block of 32 values of a row, in fp32 with
+ * Q8_1 quantisation of fp16 activations, exactly as qmv_q4_0_q8_1 and
+ * qmv_q8_0_q8_1 perform it inside their kernel: per block of 32 values of a row, in fp32 with
  * round-to-nearest, amax = max |x|, d = amax / 127, id = 1 / d (0 for an
  * all-zero block) and q = round(x * id) with ties away from zero; the block's
  * scale is d rounded to fp16.  Values must be finite.

@@ -506,8 +506,9 @@ __device__ __forceinline__ bool stage_wait(uint64_t *bar, uint32_t parity, int *
 // fp32in kernels convert inside the kernel for the same reason: a separate
 // conversion pass costs a launch -- volta-kernel-bakeoff, "Results (one token,
 // microseconds, lower is better)").
-// XQ8 = the activations are quantised to Q8_1 while they are staged and the
-// Q4_0 products are integer dots (plain Q4_0 calls only).
+// XQ8 = the activations are quantised to Q8_1 while they are staged (or copied
+// in, already quantised) and the block products are integer dots (plain Q4_0
+// and Q8_0 calls only).
 template <int FMT, int M, int MAXT, bool MOE, bool SWIGLU = false, bool XF32 = false, bool XQ8 = false>
 __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p)
 {
