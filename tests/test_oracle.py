@@ -476,6 +476,23 @@ def test_q8_1_product_integer_case_q8_0(orc):
     assert np.array_equal(S, np.abs(x).astype(np.float64) @ np.abs(Wi).T)
 
 
+def test_q8_1_product_integer_case_q2w(orc):
+    # plain 2-bit with d = 1 (codes 0..3, weights c - 2) against activations
+    # whose every block has max |x| = 127: y is the integer matmul
+    rng = np.random.default_rng(85)
+    N, K, M = 4, 768, 2
+    codes = rng.integers(0, 4, size=(N, K))
+    W = H.encode_q2w(codes, np.full((N, K // 32), 0x3C00, dtype=np.uint16))
+    x = rng.integers(-127, 128, size=(M, K))
+    x.reshape(M, K // 32, 32)[:, :, 13] = 127
+    q, d, s = orc.quantize_q8_1(x.astype(np.float16))
+    assert np.array_equal(q, x) and np.all(d == 0x3C00)
+    y, S = orc.qmv_q8_1(2, W, q, d, N, K)
+    Wi = (codes - 2).astype(np.float64)
+    assert np.array_equal(y, x.astype(np.float64) @ Wi.T)
+    assert np.array_equal(S, np.abs(x).astype(np.float64) @ np.abs(Wi).T)
+
+
 def test_q8_1_product_is_the_product_on_dequantised_x(orc):
     N, K, M = 9, 768, 3
     W, x = _rand("q4_0", N, K, M, 83)
