@@ -119,17 +119,6 @@ __host__ __device__ __forceinline__ uint32_t f16_idesc(int tn)
            | (static_cast<uint32_t>(kBM >> 4) << 24);  // M / 16
 }
 
-__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                        bool accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate ? 1 : 0)
-        : "memory");
-}
-
 // Four K=16 steps over one 64-K slice: descriptors advance by 32 bytes (2 in
 // the 16-byte address field) per step.  `first` clears the accumulator.
 __device__ __forceinline__ void mma_f16_slice(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
