@@ -26,7 +26,10 @@
  * with y_exact the fp64 dequantise-then-dot (volta-kernel-bakeoff, "Making it
  * fair": CPU double-precision reference; "A few tokens at once": checked like
  * cuBLAS fp16, 2e-3, large and tiny activations planted).  Activations must be
- * finite fp16.
+ * finite fp16.  Exceptions, each stated at its declaration: the *_f32 calls
+ * take fp32 activations (rounded to fp16 in the kernel), and the *_q8_1 calls
+ * compute the product on the activations quantised to Q8_1, with their own
+ * accuracy statement.
  *
  * Conventions common to every entry point:
  *   - All array pointers are DEVICE pointers on the current CUDA device, owned
