@@ -37,6 +37,39 @@ def test_header_declares_the_boundary():
         assert n in names
 
 
+_CTYPE = {"const void *": ctypes.c_void_p, "void *": ctypes.c_void_p, "float *": ctypes.c_void_p,
+          "const float *": ctypes.c_void_p, "const int8_t *": ctypes.c_void_p, "int8_t *": ctypes.c_void_p,
+          "const uint16_t *": ctypes.c_void_p, "uint16_t *": ctypes.c_void_p, "const int32_t *": ctypes.c_void_p,
+          "int32_t *": ctypes.c_void_p, "uint32_t *": ctypes.c_void_p, "qmv_stream_t": ctypes.c_void_p,
+          "int64_t": ctypes.c_int64, "int": ctypes.c_int, "qmv_status": ctypes.c_int}
+
+
+def _signatures():
+    """name -> list of parameter types as written in include/*.h."""
+    sigs = {}
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        txt = open(h).read()
+        for name, params in re.findall(r"^QMV_API\s+[\w\s\*]+?\b(\w+)\s*\(([^)]*)\)", txt, flags=re.M):
+            plist = [] if params.strip() in ("", "void") else [p.strip() for p in params.split(",")]
+            # drop the parameter name: the type is everything before the last identifier
+            sigs[name] = [re.sub(r"\s*\b\w+$", "", " ".join(p.split())).replace(" *", " *") for p in plist]
+    return sigs
+
+
+def test_binding_signatures_match_the_header(lib):
+    # every entry point's ctypes argument list has the header's length and kinds
+    # (pointers as void pointers, sizes as int64, flags as int)
+    for name, types in _signatures().items():
+        f = getattr(lib, name)
+        assert f.argtypes is not None, name
+        want = [_CTYPE[t] for t in types]
+        got = list(f.argtypes)
+        assert len(got) == len(want), (name, types, got)
+        for t, w, g in zip(types, want, got):
+            ok = g == w or (w is ctypes.c_void_p and getattr(g, "_type_", None) is not None)
+            assert ok, (name, t, g)
+
+
 def test_every_declared_symbol_is_exported(lib):
     raw = ctypes.CDLL(q.LIB_PATH)
     missing = [n for n in _declared() if not hasattr(raw, n)]
