@@ -25,11 +25,24 @@
  * Accuracy contract: per output, |y - y_exact| <= 2e-3 * (sum_k |x w| + 1e-6),
  * with y_exact the fp64 dequantise-then-dot (volta-kernel-bakeoff, "Making it
  * fair": CPU double-precision reference; "A few tokens at once": checked like
- * cuBLAS fp16, 2e-3, large and tiny activations planted).  Activations must be
- * finite fp16.  Exceptions, each stated at its declaration: the *_f32 calls
- * take fp32 activations (rounded to fp16 in the kernel), and the *_q8_1 calls
- * compute the product on the activations quantised to Q8_1, with their own
- * accuracy statement.
+ * cuBLAS fp16, 2e-3, large and tiny activations planted).  This bound is the
+ * acceptance bar on activations like the pages' (N(0,1), their large plant of
+ * +-20000..60000 and tiny plant of x 1e-4) and on whole blocks of +-65504.
+ * What holds for every input follows from the arithmetic of the decode
+ * kernels, which sum eight products per fp16 partial sum with weights
+ * pre-scaled to |w'| <= 1/8 (Q4_0: (c - 8)/64, Q8_0: q/1024; 2-bit: 1/16):
+ *   - for finite fp16 activations and finite scales every output is finite:
+ *     no fp16 partial sum can overflow (after eight products of at most
+ *     65504/8 each, round-to-nearest stays at or below 65504);
+ *   - |y - y_exact| <= about 2^-8 * sum_k |x w| + 2^-25 * P * K * max |d|,
+ *     P the pre-scale (64, 1024, 32): eight fp16 roundings of at most 2^-11
+ *     of a partial sum each, plus at most half a subnormal step (2^-25) per
+ *     rounding when products fall below fp16's normal range.
+ * Activations must be finite fp16.  Exceptions, each stated at its
+ * declaration: the *_f32 calls take fp32 activations (rounded to fp16 in the
+ * kernel), the *_q8_1 calls compute the product on the activations quantised
+ * to Q8_1 (their own accuracy statement), and the prefill call rounds each
+ * dequantised weight (c - 8) * d to fp16 (so |d| <= 8188 keeps it finite).
  *
  * Conventions common to every entry point:
  *   - All array pointers are DEVICE pointers on the current CUDA device, owned
@@ -47,8 +60,10 @@
  *     use programmatic dependent launch: a call may begin streaming (and, for
  *     prefill, dequantising) W while the previous kernel on `stream` is still
  *     finishing, and reads x / writes y only after that kernel has completed.
- *     If the kernel that runs right before a call on the same stream WRITES W,
- *     call qmv_set_pdl(0) first.
+ *     So W must not be written by the kernel that runs immediately before a
+ *     call on the same stream; if it is (in-place re-quantisation, a weight
+ *     loader), call qmv_set_pdl(0) first.  Every declaration below that takes
+ *     W is subject to this condition.
  */
 #ifndef QMV_H
 #define QMV_H
@@ -97,6 +112,8 @@ typedef enum {
  * in shared memory (e.g. 8 tokens of K = 14336 in fp16) the call runs as a
  * few launches over token subsets, each streaming W again.  These rules hold
  * for every decode call below.
+ * W must not be written by the kernel right before this call on `stream`
+ * while programmatic dependent launch is on (see the preamble).
  */
 QMV_API qmv_status qmv_q4_0(const void *W, const void *x, float *y,
                     int64_t N, int64_t K, int64_t M, qmv_stream_t stream);
@@ -291,10 +308,30 @@ QMV_API qmv_status qmm_q4_0_prefill(const void *W, const void *x, float *y,
 
 /*
  * Reads and clears the device status word (QMV_DEV_* bits) of the current
- * device.  Synchronises `stream` first.  *out receives the bits.
- * Returns QMV_ERR_NULL for out == NULL, QMV_ERR_CUDA on a runtime error.
+ * device, in one atomic step enqueued on `stream` (so it follows every kernel
+ * enqueued before it on `stream`; a bit that a kernel on another stream sets
+ * meanwhile is kept for the next read, never lost).  Synchronises `stream`.
+ * *out receives the bits.  Returns QMV_ERR_NULL for out == NULL, QMV_ERR_CUDA
+ * or QMV_ERR_LAUNCH on a runtime error.
  */
 QMV_API qmv_status qmv_device_status(qmv_stream_t stream, int32_t *out);
+
+/*
+ * Read-only bandwidth probe (a measurement utility, not part of the product):
+ * streams `bytes` of device memory through per-warp shared-memory rings filled
+ * by bulk (TMA) copies, the way the decode kernels stream their weights, with
+ * no arithmetic on the bytes.  Timing it over a buffer several times the L2
+ * gives the read roofline the decode kernels are compared with, beside the
+ * copy bandwidth (sm8x-bench reports its kernels against a measured bandwidth
+ * probe as well as the spec figure -- sm8x-bench, methodology bullets).
+ *   buf   : DEVICE, 16-byte aligned, `bytes` long; bytes % 256 == 0.
+ *   out   : DEVICE uint32, 4-byte aligned: receives the XOR, over every
+ *           256-byte-aligned offset o < bytes, of the four 32-bit little-endian
+ *           words at buf + o .. o + 15 (proof that the bytes were consumed).
+ * Asynchronous on `stream`; bytes == 0 writes 0.  QMV_ERR_SHAPE for a
+ * negative or unaligned size, QMV_ERR_NULL / QMV_ERR_ALIGN as usual.
+ */
+QMV_API qmv_status qmv_read_probe(const void *buf, int64_t bytes, uint32_t *out, qmv_stream_t stream);
 
 /* Programmatic dependent launch for the decode, prefill and Q8_1 quantisation
  * kernels: 1 = on (default), 0 = off (plain stream order).  Process-wide;

@@ -19,6 +19,13 @@ namespace qmv {
 // One status word per device; kernels receive its address.
 __device__ int g_device_status;
 
+// Where qmv_device_status leaves the word it fetched and cleared: one slot per
+// concurrent reader (a host-side ticket picks the slot).
+constexpr int kFetchSlots = 64;
+__device__ int g_status_fetched[kFetchSlots];
+
+__global__ void status_fetch_clear_kernel(int *status, int *slot) { *slot = atomicExch(status, 0); }
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -26,6 +33,35 @@ std::atomic<int *> g_status_ptr[kMaxDevices];
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_smem_optin[kMaxDevices];
 std::atomic<int> g_pdl{1};
+std::atomic<unsigned> g_fetch_ticket{0};
+
+// Failure detection is tested without a GPU fault: QMV_TEST_SKIP_COPY=
+// "decode:N" or "prefill:N" makes the N-th launch (counted from 1) of the
+// streaming decode kernel or of the prefill kernel in this process skip one
+// bulk copy whose bytes a barrier still expects.  The wait on that barrier
+// then runs out, the kernel records QMV_DEV_TIMEOUT, waits (bounded) for its
+// other copies and returns; nothing else of the call changes.  Unset in every
+// normal run.
+constexpr int kArmDecode = 0, kArmPrefill = 1;
+std::atomic<long long> g_launches_seen[2];
+
+bool test_skip_this_launch(int kind)
+{
+    static int armed_kind = -1;
+    static long long armed_n = 0;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        const char *e = std::getenv("QMV_TEST_SKIP_COPY");
+        if (!e) return;
+        const char *c = std::strchr(e, ':');
+        if (!c) return;
+        if (!std::strncmp(e, "decode", static_cast<size_t>(c - e))) armed_kind = kArmDecode;
+        else if (!std::strncmp(e, "prefill", static_cast<size_t>(c - e))) armed_kind = kArmPrefill;
+        armed_n = std::atoll(c + 1);
+    });
+    if (armed_kind != kind) return false;
+    return g_launches_seen[kind].fetch_add(1) + 1 == armed_n;
+}
 
 cudaError_t current_device(int *dev)
 {
@@ -262,8 +298,10 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
     return pl;
 }
 
-cudaError_t launch_streaming(int fmt, const GemvParams &p, int M, const Plan &pl, cudaStream_t stream, bool pdl)
+cudaError_t launch_streaming(int fmt, const GemvParams &p0, int M, const Plan &pl, cudaStream_t stream, bool pdl)
 {
+    GemvParams p = p0;
+    p.test_skip_copy = test_skip_this_launch(kArmDecode) ? 1 : 0;
     if (fmt == kQ4_0 && p.xq8) return launch_gemv_stream_q4_0_q8_1(M, p, pl.grid, pl.warps, pl.smem, stream, pdl);
     if (fmt == kQ8_0 && p.xq8) return launch_gemv_stream_q8_0_q8_1(M, p, pl.grid, pl.warps, pl.smem, stream, pdl);
     if (fmt == kQ4_0 && p.W2) return launch_gemv_stream_q4_0_swiglu(M, p, pl.grid, pl.warps, pl.smem, stream, pdl);
@@ -410,9 +448,9 @@ cudaError_t ensure_smem_optin(const void *func, size_t smem)
 
 cudaError_t launch_gemv_generic(int fmt, const GemvParams &p, int M, int grid, cudaStream_t s, bool pdl)
 {
-    if (fmt == kQ4_0) return launch_ex(gemv_generic_kernel<kQ4_0>, dim3(grid), dim3(256), 0, s, pdl, p, M);
-    if (fmt == kQ2W) return launch_ex(gemv_generic_kernel<kQ2W>, dim3(grid), dim3(256), 0, s, pdl, p, M);
-    return launch_ex(gemv_generic_kernel<kQ8_0>, dim3(grid), dim3(256), 0, s, pdl, p, M);
+    if (fmt == kQ4_0) return launch_ex(qmv_generic_kernel<kQ4_0>, dim3(grid), dim3(256), 0, s, pdl, p, M);
+    if (fmt == kQ2W) return launch_ex(qmv_generic_kernel<kQ2W>, dim3(grid), dim3(256), 0, s, pdl, p, M);
+    return launch_ex(qmv_generic_kernel<kQ8_0>, dim3(grid), dim3(256), 0, s, pdl, p, M);
 }
 
 }  // namespace qmv
@@ -563,7 +601,8 @@ qmv_status qmm_q4_0_prefill(const void *W, const void *x, float *y, int64_t N, i
     if (device_info(dev, &status, &sms, &optin) != cudaSuccess) return QMV_ERR_CUDA;
     const PrefillPlan pl = prefill_plan(N, K, M, sms);
     if (pl.ok) {
-        cudaError_t e = launch_prefill(pl, W, x, y, N, K, M, status, s, g_pdl.load(std::memory_order_relaxed) != 0);
+        cudaError_t e = launch_prefill(pl, W, x, y, N, K, M, status, s, g_pdl.load(std::memory_order_relaxed) != 0,
+                                       test_skip_this_launch(kArmPrefill));
         if (e != cudaSuccess) {
             (void)cudaGetLastError();
             return QMV_ERR_LAUNCH;
@@ -598,12 +637,43 @@ qmv_status qmm_q4_0_prefill(const void *W, const void *x, float *y, int64_t N, i
 qmv_status qmv_device_status(qmv_stream_t stream, int32_t *out)
 {
     if (!out) return QMV_ERR_NULL;
-    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return QMV_ERR_CUDA;
+    int dev = 0;
+    if (current_device(&dev) != cudaSuccess) return QMV_ERR_CUDA;
+    int *status = nullptr;
+    int sms = 0, optin = 0;
+    if (device_info(dev, &status, &sms, &optin) != cudaSuccess) return QMV_ERR_CUDA;
+    // Fetch and clear in one atomic step, in `stream` order: a kernel on
+    // another stream that sets a bit in between is never lost (it stays for
+    // the next read).  Concurrent readers take different result slots.
+    void *slots = nullptr;
+    if (cudaGetSymbolAddress(&slots, g_status_fetched) != cudaSuccess) return QMV_ERR_CUDA;
+    int *slot = static_cast<int *>(slots) + (g_fetch_ticket.fetch_add(1) % kFetchSlots);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    status_fetch_clear_kernel<<<1, 1, 0, s>>>(status, slot);
+    if (cudaGetLastError() != cudaSuccess) return QMV_ERR_LAUNCH;
     int v = 0;
-    if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return QMV_ERR_CUDA;
-    const int zero = 0;
-    if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return QMV_ERR_CUDA;
+    if (cudaMemcpyAsync(&v, slot, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return QMV_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return QMV_ERR_CUDA;
     *out = v;
+    return QMV_OK;
+}
+
+qmv_status qmv_read_probe(const void *buf, int64_t bytes, uint32_t *out, qmv_stream_t stream)
+{
+    if (bytes < 0 || bytes % 256 != 0 || bytes > (int64_t(1) << 46)) return QMV_ERR_SHAPE;
+    if (!out || (bytes > 0 && !buf)) return QMV_ERR_NULL;
+    if (!aligned(buf, 16) || !aligned(out, 4)) return QMV_ERR_ALIGN;
+    int dev = 0;
+    if (current_device(&dev) != cudaSuccess) return QMV_ERR_CUDA;
+    int *status = nullptr;
+    int sms = 0, optin = 0;
+    if (device_info(dev, &status, &sms, &optin) != cudaSuccess) return QMV_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (bytes == 0) return cudaMemsetAsync(out, 0, sizeof(uint32_t), s) == cudaSuccess ? QMV_OK : QMV_ERR_CUDA;
+    if (launch_read_probe(buf, bytes, out, status, sms, s) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return QMV_ERR_LAUNCH;
+    }
     return QMV_OK;
 }
 

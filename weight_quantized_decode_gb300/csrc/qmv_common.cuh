@@ -199,17 +199,25 @@ __device__ __forceinline__ float half_hi_to_float(uint32_t u)
 // PRMT, two bytes) into the mantissas of a half2; one HFMA2 then removes the
 // 1024 offset and the code bias and applies a power-of-two pre-scale, exactly.
 //
-// The weights come out pre-scaled (Q4_0: (c - 8) / 32, Q8_0: q / 512) so that
-// fp16 partial sums of large activations stay finite (the bakeoff divides the
-// centred code by 32 for the same reason -- volta-kernel-bakeoff, "A few
-// tokens at once").  The fp32 block sums are multiplied back by 32 (or 512)
-// at the end.
-constexpr float kQ4Prescale = 32.0f;
-constexpr float kQ8Prescale = 512.0f;
+// The weights come out pre-scaled so that no fp16 partial sum can overflow,
+// whatever the (finite) fp16 activations: a lane sums two code words, i.e.
+// eight products, in each half of a half2 chain before the chain goes to fp32,
+// and the page's rule for that case is to divide the centred code by 64
+// instead of 32 (volta-kernel-bakeoff, "A few tokens at once").  Q4_0 weights
+// enter as (c - 8) / 64 and Q8_0 weights as q / 1024, so |w'| <= 1/8 and one
+// product is at most 65504 / 8 = 8188 in magnitude.  Round-to-nearest is
+// monotone, so after i products a partial sum is at most B_i with B_1 = 8188
+// and B_i = fp16(B_{i-1} + 8188): 8188, 16376, 24560, 32752, 40928, 49120,
+// 57312, 65504 -- finite after all eight (a CPU test replays this sequence
+// against the constants below).  The plain 2-bit weights enter as (c - 2) / 32
+// (|w'| <= 1/16: at most 32752 after eight products).  The fp32 block sums are
+// multiplied back by the pre-scale at the end (exact: a power of two).
+constexpr float kQ4Prescale = 64.0f;
+constexpr float kQ8Prescale = 1024.0f;
 constexpr float kQ2Prescale = 32.0f;
 
 // Q4_0: one 32-bit word of qs holding bytes (b0, b1, b2, b3) -> four half2
-// weights:  w[0] = (lo b0, lo b2)   w[1] = (lo b1, lo b3)
+// weights (c - 8) / 64:  w[0] = (lo b0, lo b2)   w[1] = (lo b1, lo b3)
 //           w[2] = (hi b0, hi b2)   w[3] = (hi b1, hi b3)
 // Low nibbles of qs[i] are element i of the block, high nibbles element i+16.
 __device__ __forceinline__ void unpack_q4_word(uint32_t v, __half2 (&w)[4])
@@ -220,12 +228,12 @@ __device__ __forceinline__ void unpack_q4_word(uint32_t v, __half2 (&w)[4])
     const uint32_t l13 = and_or(v8, 0x000F000Fu, magic);
     const uint32_t h02 = and_or(v, 0x00F000F0u, magic);   // 1024 + 16 n
     const uint32_t h13 = and_or(v8, 0x00F000F0u, magic);
-    // (1024 + n) / 32 - 1032 / 32 = (n - 8) / 32
-    const __half2 s_lo = __halves2half2(__ushort_as_half(0x2800), __ushort_as_half(0x2800));  // 2^-5
-    const __half2 b_lo = __halves2half2(__ushort_as_half(0xD008), __ushort_as_half(0xD008));  // -32.25
-    // (1024 + 16 n) / 512 - 2.25 = (n - 8) / 32
-    const __half2 s_hi = __halves2half2(__ushort_as_half(0x1800), __ushort_as_half(0x1800));  // 2^-9
-    const __half2 b_hi = __halves2half2(__ushort_as_half(0xC080), __ushort_as_half(0xC080));  // -2.25
+    // (1024 + n) / 64 - 1032 / 64 = (n - 8) / 64
+    const __half2 s_lo = __halves2half2(__ushort_as_half(0x2400), __ushort_as_half(0x2400));  // 2^-6
+    const __half2 b_lo = __halves2half2(__ushort_as_half(0xCC08), __ushort_as_half(0xCC08));  // -16.125
+    // (1024 + 16 n) / 1024 - 1.125 = (n - 8) / 64
+    const __half2 s_hi = __halves2half2(__ushort_as_half(0x1400), __ushort_as_half(0x1400));  // 2^-10
+    const __half2 b_hi = __halves2half2(__ushort_as_half(0xBC80), __ushort_as_half(0xBC80));  // -1.125
     w[0] = __hfma2(as_h2(l02), s_lo, b_lo);
     w[1] = __hfma2(as_h2(l13), s_lo, b_lo);
     w[2] = __hfma2(as_h2(h02), s_hi, b_hi);
@@ -233,16 +241,16 @@ __device__ __forceinline__ void unpack_q4_word(uint32_t v, __half2 (&w)[4])
 }
 
 // Q8_0: one 32-bit word holding int8 codes (q0, q1, q2, q3) -> two half2
-// weights w[0] = (q0, q2) / 512, w[1] = (q1, q3) / 512.  Biasing each byte by
+// weights w[0] = (q0, q2) / 1024, w[1] = (q1, q3) / 1024.  Biasing each byte by
 // +128 (XOR 0x80) makes it an unsigned mantissa: 0x6400 | (q + 128) = 1152 + q.
 __device__ __forceinline__ void unpack_q8_word(uint32_t v, __half2 (&w)[2])
 {
     const uint32_t u = v ^ 0x80808080u;
     const uint32_t h02 = __byte_perm(u, 0x64646464u, 0x4240);   // (0x64|b0, 0x64|b2)
     const uint32_t h13 = __byte_perm(u, 0x64646464u, 0x4341);   // (0x64|b1, 0x64|b3)
-    // (1152 + q) / 512 - 2.25 = q / 512
-    const __half2 s = __halves2half2(__ushort_as_half(0x1800), __ushort_as_half(0x1800));  // 2^-9
-    const __half2 b = __halves2half2(__ushort_as_half(0xC080), __ushort_as_half(0xC080));  // -2.25
+    // (1152 + q) / 1024 - 1.125 = q / 1024
+    const __half2 s = __halves2half2(__ushort_as_half(0x1400), __ushort_as_half(0x1400));  // 2^-10
+    const __half2 b = __halves2half2(__ushort_as_half(0xBC80), __ushort_as_half(0xBC80));  // -1.125
     w[0] = __hfma2(as_h2(h02), s, b);
     w[1] = __hfma2(as_h2(h13), s, b);
 }

@@ -99,6 +99,8 @@ struct GemvParams {
     const uint16_t *xq_d;        //   their fp16 scales' bits [M][K/32]
     const int32_t *xq_s;         //   and code sums [M][K/32]
     int *status;                 // device status word
+    int test_skip_copy;          // failure-detection test only: CTA 0's warp 0 never requests its first
+                                 // stage, so its bounded wait runs out (0 in every normal call)
 };
 
 // Shared-memory bytes the kernel needs for a configuration.
@@ -510,7 +512,7 @@ __device__ __forceinline__ bool stage_wait(uint64_t *bar, uint32_t parity, int *
 // in, already quantised) and the block products are integer dots (plain Q4_0
 // and Q8_0 calls only).
 template <int FMT, int M, int MAXT, bool MOE, bool SWIGLU = false, bool XF32 = false, bool XQ8 = false>
-__global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p)
+__global__ void __launch_bounds__(MAXT, 1) qmv_stream_kernel(const GemvParams p)
 {
     using T = FmtTraits<FMT>;
     static_assert(!XQ8 || ((FMT == kQ4_0 || FMT == kQ8_0) && !MOE && !SWIGLU && !XF32),
@@ -594,7 +596,10 @@ __global__ void __launch_bounds__(MAXT, 1) gemv_stream_kernel(const GemvParams p
         const uint32_t total_bytes = __reduce_add_sync(0xffffffffu, my_bytes);
         if (lane == 0) mbar_arrive_expect_tx(&bars[is_slot], total_bytes);
         __syncwarp();
-        if (my_bytes)
+        // (test only) the first stage of CTA 0's warp 0 is expected but never
+        // requested: nothing is in flight into that slot when its wait gives up
+        const bool skip = p.test_skip_copy && blockIdx.x == 0 && warp == 0 && issued == 0;
+        if (my_bytes && !skip)
             bulk_g2s_hint(ring + static_cast<size_t>(is_slot) * slot_bytes + lane * lane_chunk_bytes,
                           is_row + static_cast<size_t>(u0) * T::kUnitBytes, my_bytes, &bars[is_slot], l2_policy);
         ++issued;
@@ -976,7 +981,7 @@ __device__ __forceinline__ int weight_code(const uint8_t *blk, int j)
 }
 
 template <int FMT>
-__global__ void __launch_bounds__(256) gemv_generic_kernel(const GemvParams p, int M)
+__global__ void __launch_bounds__(256) qmv_generic_kernel(const GemvParams p, int M)
 {
     const int lane = threadIdx.x & 31;
     const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;

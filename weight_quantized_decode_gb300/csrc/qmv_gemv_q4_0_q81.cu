@@ -9,7 +9,7 @@ namespace qmv {
 template <int M, int MAXT>
 static cudaError_t launch_q81_t(const GemvParams &p, int grid, int warps, size_t smem, cudaStream_t s, bool pdl)
 {
-    auto kernel = gemv_stream_kernel<kQ4_0, M, MAXT, false, false, false, true>;
+    auto kernel = qmv_stream_kernel<kQ4_0, M, MAXT, false, false, false, true>;
     cudaError_t e = ensure_smem_optin(reinterpret_cast<const void *>(kernel), smem);
     if (e != cudaSuccess) return e;
     return launch_ex(kernel, dim3(grid), dim3(warps * 32), smem, s, pdl, p);

@@ -68,6 +68,7 @@ struct PrefillParams {
     int NS;            // slot ring depth: each slot holds KSUB dequantised-weight and activation atoms
     int KSUB;          // 64-K atoms per slot (1 or 2): MMAs per barrier round = 4 * KSUB
     uint32_t tmem_cols;
+    int test_skip_copy;   // failure-detection test only: CTA (0, 0) never requests its first packed tile
 };
 
 // ---- tcgen05 / TMA wrappers -------------------------------------------------------
@@ -280,8 +281,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 mbar_arrive_expect_tx(&wfull[slot], kPackedTileBytes);
-                tma_load_2d(w_tiles + slot * kPackedTileBytes, &wmap, c * kPackedRowBytes, static_cast<int>(n0),
-                            &wfull[slot]);
+                // (test only) the first tile of CTA (0, 0) is expected but never
+                // requested, so the waits on it run out and the CTA aborts
+                if (!(p.test_skip_copy && c == 0 && blockIdx.x == 0 && blockIdx.y == 0))
+                    tma_load_2d(w_tiles + slot * kPackedTileBytes, &wmap, c * kPackedRowBytes,
+                                static_cast<int>(n0), &wfull[slot]);
                 ++issued;
                 if (++slot == NW) {
                     slot = 0;
@@ -537,7 +541,7 @@ PrefillPlan prefill_plan(int64_t N, int64_t K, int64_t M, int sms)
 }
 
 cudaError_t launch_prefill(const PrefillPlan &pl, const void *W, const void *x, float *y, int64_t N, int64_t K,
-                           int64_t M, int *status, cudaStream_t s, bool pdl)
+                           int64_t M, int *status, cudaStream_t s, bool pdl, bool test_skip_copy)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc || !pl.ok) return cudaErrorNotSupported;
@@ -575,6 +579,7 @@ cudaError_t launch_prefill(const PrefillPlan &pl, const void *W, const void *x, 
     p.NS = pl.NS;
     p.KSUB = pl.KSUB;
     p.tmem_cols = pl.tmem_cols;
+    p.test_skip_copy = test_skip_copy ? 1 : 0;
     cudaError_t e = ensure_smem_optin(reinterpret_cast<const void *>(prefill_kernel), pl.smem);
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>(pl.grid_x), static_cast<unsigned>(pl.grid_y));

@@ -13,7 +13,9 @@ namespace qmv {
 // that kernel does not take the shape (or the tensor-map encoder is missing).
 PrefillPlan prefill_plan(int64_t N, int64_t K, int64_t M, int sms);
 
+// test_skip_copy: failure-detection tests only (one tile of CTA (0, 0) is never
+// requested, so its bounded waits run out); false in every normal call.
 cudaError_t launch_prefill(const PrefillPlan &pl, const void *W, const void *x, float *y, int64_t N, int64_t K,
-                           int64_t M, int *status, cudaStream_t s, bool pdl);
+                           int64_t M, int *status, cudaStream_t s, bool pdl, bool test_skip_copy);
 
 }  // namespace qmv
