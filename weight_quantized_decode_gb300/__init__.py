@@ -18,6 +18,7 @@ Functions (same names as the C ABI):
     qmv_moe(W_pool, expert_idx, n_experts, x, N, y=None, stream=None)
     qmm_q4_0_prefill(W, x, y=None, stream=None)  -> y fp32 [M, N]
     qmv_device_status(stream=None)               -> int (QMV_DEV_* bits, cleared)
+    qmv_read_probe(buf, out=None, stream=None)   -> checksum tensor (read-only bandwidth probe)
     qmv_set_pdl(enable), qmv_status_str(code), qmv_version()
 Raw-pointer forms (``*_ptr``) take integers and are what the benchmark times.
 """
@@ -77,6 +78,8 @@ def lib():
         L.qmv_q4_0_swiglu_f32.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
         L.qmv_device_status.restype = ctypes.c_int
         L.qmv_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
+        L.qmv_read_probe.restype = ctypes.c_int
+        L.qmv_read_probe.argtypes = [vp, i64, vp, vp]
         L.qmv_set_pdl.restype = None
         L.qmv_set_pdl.argtypes = [ctypes.c_int]
         L.qmv_status_str.restype = ctypes.c_char_p
@@ -160,6 +163,10 @@ def qmv_moe_ptr(W_pool: int, idx: int, n_experts: int, x: int, y: int, N: int, K
 
 def qmm_q4_0_prefill_ptr(W: int, x: int, y: int, N: int, K: int, M: int, stream: int = 0) -> None:
     _check("qmm_q4_0_prefill", lib().qmm_q4_0_prefill(W, x, y, N, K, M, stream))
+
+
+def qmv_read_probe_ptr(buf: int, nbytes: int, out: int, stream: int = 0) -> None:
+    _check("qmv_read_probe", lib().qmv_read_probe(buf, nbytes, out, stream))
 
 
 # -- torch-tensor entry points ---------------------------------------------------------
@@ -401,6 +408,20 @@ def qmv_moe(W_pool, expert_idx, n_experts, x, N, y=None, stream=None):
         qmv_moe_ptr(W_pool.data_ptr(), expert_idx.data_ptr(), int(n_experts), x.data_ptr(), y.data_ptr(),
                     int(N), int(K), int(M), _stream_handle(stream))
     return y
+
+
+def qmv_read_probe(buf, out=None, stream=None):
+    """Stream the bytes of the CUDA tensor ``buf`` (a multiple of 256 bytes) through
+    the read-only bandwidth probe; returns the device uint32 checksum tensor ``out``
+    (an int32 view: the XOR of the 16 bytes at every 256-byte offset, as 32-bit words)."""
+    torch = _torch()
+    if not (buf.is_cuda and buf.is_contiguous()):
+        raise ValueError("qmv_read_probe: buf must be a contiguous CUDA tensor (no CPU path)")
+    if out is None:
+        out = torch.empty(1, dtype=torch.int32, device=buf.device)
+    with _on_device("qmv_read_probe", buf, out):
+        qmv_read_probe_ptr(buf.data_ptr(), buf.numel() * buf.element_size(), out.data_ptr(), _stream_handle(stream))
+    return out
 
 
 def qmv_device_status(stream=None) -> int:

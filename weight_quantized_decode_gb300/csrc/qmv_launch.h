@@ -35,6 +35,9 @@ cudaError_t launch_gemv_stream_q2w(int M, const GemvParams &p, int grid, int war
                                    bool pdl);
 cudaError_t launch_gemv_stream_q8_0(int M, const GemvParams &p, int grid, int warps, size_t smem,
                                     cudaStream_t s, bool pdl);
+// Read-only bandwidth probe over `bytes` (a multiple of 256) of device memory;
+// *out (device) receives an XOR checksum of the bytes it consumed.
+cudaError_t launch_read_probe(const void *buf, int64_t bytes, uint32_t *out, int *status, int sms, cudaStream_t s);
 // Generic kernel (any K % 32 == 0, activations read from global memory).
 cudaError_t launch_gemv_generic(int fmt, const GemvParams &p, int M, int grid, cudaStream_t s, bool pdl);
 
