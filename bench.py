@@ -241,17 +241,11 @@ def whole_job_rate(units_per_step, steps, world, ms):
     return units_per_step * steps * world / (ms * 1e-3)
 
 
-def run_ours(args, dist, rank, local, world):
-    import torch
-    import weight_quantized_decode_gb300 as q
-
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    q.lib()
-    wl = WORKLOADS[args.workload]
+def build_calls(workload, q, torch, dev, l2, sh):
+    """The calls one step of `workload` makes, each on its own rotated weight
+    copies, and the rotation period (steps after which the sequence repeats)."""
+    wl = WORKLOADS[workload]
     kind, fmt = wl["kind"], wl["fmt"]
-    prop = torch.cuda.get_device_properties(dev)
-    l2 = int(getattr(prop, "L2_cache_size", 128 * 1024 * 1024) or 128 * 1024 * 1024)
     bb = BLOCK_BYTES[fmt]
 
     def rotated_copies(rows, K, seed_name):
@@ -267,13 +261,10 @@ def run_ours(args, dist, rank, local, world):
             Wd[c].view(rows, K // 32, bb)[:, :, 2:].bitwise_xor_(c & 0xFF)
         return Wd, copies
 
-    # ---- inputs: one entry per call made once per step ----------------------------
     # Copies per table are powers of two, so every table's rotation divides the
     # longest one and a single CUDA graph of `period` steps replays the exact
     # call sequence.
     calls = []
-    stream = torch.cuda.Stream(dev)
-    sh = int(stream.cuda_stream)
     xdt, xb = x_dtype(wl)
     if kind in ("gemv", "prefill"):
         fn_ptr = {"gemv": {"q4_0": q.qmv_q4_0_ptr, "q8_0": q.qmv_q8_0_ptr, "q2w": q.qmv_q2w_ptr}[fmt],
@@ -356,6 +347,153 @@ def run_ours(args, dist, rank, local, world):
             c["call"] = call
             calls.append(c)
     period = max(max(c["copies"] for c in calls), max(c.get("idx_period", 1) for c in calls))
+    return calls, period
+
+
+class StepRunner:
+    """CUDA graphs that replay the exact call sequence of any number of steps."""
+
+    def __init__(self, torch, stream, calls, period):
+        self.torch, self.stream, self.calls, self.period = torch, stream, calls, period
+        self.rem = {}
+        self.g_period = self.capture(period)
+
+    def enqueue(self, s):
+        for c in self.calls:
+            c["call"](s)
+
+    def capture(self, count):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(self.stream):
+            with torch.cuda.graph(g, stream=self.stream):
+                for s in range(count):
+                    self.enqueue(s)
+        return g
+
+    def prepare(self, n):
+        """Capture the remainder graph for n steps (outside any timed region)."""
+        r = n % self.period
+        if r and r not in self.rem:
+            self.rem[r] = self.capture(r)
+
+    def run(self, n):
+        for _ in range(n // self.period):
+            self.g_period.replay()
+        r = n % self.period
+        if r:
+            self.prepare(n)
+            self.rem[r].replay()
+
+    def time_ms(self, n):
+        torch = self.torch
+        self.prepare(n)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            e0.record(self.stream)
+            self.run(n)
+            e1.record(self.stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+
+def per_call_sweep(torch, stream, calls, kind, pk):
+    """Per call: us/call over a graph of R back-to-back calls cycling copies
+    (best of 5) and one call alone in its own graph (median of 20)."""
+    def event_time_us(g, reps=1):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for _ in range(reps):
+                g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3
+
+    sweep = []
+    for c in calls:
+        R = max(64, 2 * c["copies"])
+
+        def cap(count, c=c):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                with torch.cuda.graph(g, stream=stream):
+                    for s_ in range(count):
+                        c["call"](s_)
+            return g
+
+        g = cap(R)
+        g1 = cap(1)
+        event_time_us(g)
+        best = min(event_time_us(g) / R for _ in range(5))
+        # one call on its own (graph launch + ramp + drain), median of 20
+        iso = statistics.median(event_time_us(g1) for _ in range(20))
+        gbs = c["bytes"] / (best * 1e-6) / 1e9
+        row = {"call": c["name"], "copies": c["copies"], "us_per_call": round(best, 3),
+               "us_isolated_call": round(iso, 3), "GBps": round(gbs, 1),
+               "frac_of_measured_hbm": round(gbs / pk["hbm_gbs"], 4),
+               "frac_of_8TBps_spec": round(gbs / SPEC_HBM_GBS, 4)}
+        if pk.get("read_probe_gbs"):
+            row["frac_of_read_probe"] = round(gbs / pk["read_probe_gbs"], 4)
+        if kind == "prefill":
+            tf = c["flops"] / (best * 1e-6) / 1e12
+            row["TFLOPs"] = round(tf, 1)
+            row["frac_of_measured_tensor"] = round(tf / pk["bf16_tflops"], 4)
+        sweep.append(row)
+    return sweep
+
+
+def read_probe_gbs(q, torch, dev, stream, l2):
+    """The read-only bandwidth probe (the decode kernels' bulk-copy streaming
+    with no arithmetic) over 16x L2: best of 5 runs of 10 back-to-back launches."""
+    nbytes = (16 * l2 + 255) // 256 * 256
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    buf.random_(0, 256)
+    out = torch.empty(1, dtype=torch.int32, device=dev)
+    sh = int(stream.cuda_stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            q.qmv_read_probe_ptr(buf.data_ptr(), nbytes, out.data_ptr(), sh)
+        torch.cuda.synchronize()
+        best = None
+        for _ in range(5):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(10):
+                q.qmv_read_probe_ptr(buf.data_ptr(), nbytes, out.data_ptr(), sh)
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b)
+            best = ms if best is None else min(best, ms)
+    del buf
+    return 10 * nbytes / (best * 1e-3) / 1e9, nbytes
+
+
+# Other configurations of the metric, timed by the default run after the
+# headline workload: Q8_0 at 1..8 tokens, the multi-expert call, prefill.
+EXTRA_SWEEPS = {"sweep_q8_0": "q8_0", "sweep_moe": "moe", "sweep_prefill": "prefill"}
+
+
+def run_ours(args, dist, rank, local, world):
+    import torch
+    import weight_quantized_decode_gb300 as q
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    q.lib()
+    wl = WORKLOADS[args.workload]
+    kind, fmt = wl["kind"], wl["fmt"]
+    prop = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(prop, "L2_cache_size", 128 * 1024 * 1024) or 128 * 1024 * 1024)
+    stream = torch.cuda.Stream(dev)
+    sh = int(stream.cuda_stream)
+    pk = peaks()
+
+    calls, period = build_calls(args.workload, q, torch, dev, l2, sh)
 
     def one_buffer(key_dev, key_host):
         """Lay the calls' device tensors `key_dev` out in one device buffer (pieces
@@ -380,47 +518,23 @@ def run_ours(args, dist, rank, local, world):
     x_dev_all, x_host_all = one_buffer("x", "x_host")
     y_dev_all, y_host_all = one_buffer("y", "y_host")
 
-    def enqueue_step(s):
-        for c in calls:
-            c["call"](s)
-
     step_bytes = sum(c["bytes"] for c in calls)
     step_flops = sum(c["flops"] for c in calls)
     launches_per_step = sum(c.get("launches", 1) for c in calls)
 
     # one eager pass (module loading, shared-memory opt-in) before any capture
     with torch.cuda.stream(stream):
-        enqueue_step(0)
+        for c in calls:
+            c["call"](0)
     torch.cuda.synchronize()
 
     # ---- CUDA graphs covering the exact step sequence ---------------------------
-    def capture(count):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(g, stream=stream):
-                for s in range(count):
-                    enqueue_step(s)
-        return g
-
-    g_period = capture(period)
-    rem_graphs = {}
-
-    def run_steps(n):
-        for _ in range(n // period):
-            g_period.replay()
-        r = n % period
-        if r:
-            if r not in rem_graphs:
-                rem_graphs[r] = capture(r)
-            rem_graphs[r].replay()
-
-    # capture the remainder graphs outside the timed region
-    for n in (args.warmup, args.steps):
-        if n % period and (n % period) not in rem_graphs:
-            rem_graphs[n % period] = capture(n % period)
+    runner = StepRunner(torch, stream, calls, period)
+    runner.prepare(args.warmup)
+    runner.prepare(args.steps)
     torch.cuda.synchronize()
 
-    run_steps(args.warmup)
+    runner.run(args.warmup)
     torch.cuda.synchronize()
 
     clocks = ClockSampler(local)
@@ -428,59 +542,48 @@ def run_ours(args, dist, rank, local, world):
     time.sleep(0.3)
     if dist:
         dist.barrier()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        run_steps(args.steps)
-        e1.record(stream)
-    torch.cuda.synchronize()
+    ms = runner.time_ms(args.steps)
     if dist:
         dist.barrier()
-    ms = e0.elapsed_time(e1)
 
-    # ---- per-shape us/call (graph of R back-to-back calls cycling copies) -------
-    sweep = []
-    pk = peaks()
-    def event_time_us(g, reps=1):
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            a.record(stream)
-            for _ in range(reps):
-                g.replay()
-            b.record(stream)
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) * 1e3
+    # ---- the read roofline, then per-shape us/call ------------------------------
+    probe_gbs, probe_bytes = read_probe_gbs(q, torch, dev, stream, l2)
+    pk["read_probe_gbs"] = probe_gbs
+    sweep = per_call_sweep(torch, stream, calls, kind, pk)
 
-    for c in calls:
-        R = max(64, 2 * c["copies"])
-
-        def cap(count, c=c):
-            g = torch.cuda.CUDAGraph()
+    # ---- the rest of the metric's configurations (default run only) -------------
+    extras = {}
+    if args.workload == "q4_0_m1_sweep" and not args.no_extra:
+        for key, ewl in EXTRA_SWEEPS.items():
+            ecalls, eperiod = build_calls(ewl, q, torch, dev, l2, sh)
             with torch.cuda.stream(stream):
-                with torch.cuda.graph(g, stream=stream):
-                    for s_ in range(count):
-                        c["call"](s_)
-            return g
-
-        g = cap(R)
-        g1 = cap(1)
-        event_time_us(g)
-        best = min(event_time_us(g) / R for _ in range(5))
-        # one call on its own (graph launch + ramp + drain), median of 20
-        iso = statistics.median(event_time_us(g1) for _ in range(20))
-        gbs = c["bytes"] / (best * 1e-6) / 1e9
-        row = {"call": c["name"], "copies": c["copies"], "us_per_call": round(best, 3),
-               "us_isolated_call": round(iso, 3), "GBps": round(gbs, 1),
-               "frac_of_measured_hbm": round(gbs / pk["hbm_gbs"], 4),
-               "frac_of_8TBps_spec": round(gbs / SPEC_HBM_GBS, 4)}
-        if kind == "prefill":
-            tf = c["flops"] / (best * 1e-6) / 1e12
-            row["TFLOPs"] = round(tf, 1)
-            row["frac_of_measured_tensor"] = round(tf / pk["bf16_tflops"], 4)
-        sweep.append(row)
+                for c in ecalls:
+                    c["call"](0)
+            torch.cuda.synchronize()
+            er = StepRunner(torch, stream, ecalls, eperiod)
+            n_steps = max(3 * eperiod, 96)
+            er.run(max(eperiod, 8))
+            e_ms = er.time_ms(n_steps)
+            ekind = WORKLOADS[ewl]["kind"]
+            eb = sum(c["bytes"] for c in ecalls) * n_steps
+            ef = sum(c["flops"] for c in ecalls) * n_steps
+            entry = {"workload": ewl, "steps": n_steps, "ms_per_step": round(e_ms / n_steps, 4),
+                     "calls_per_step": [c["name"] for c in ecalls],
+                     "launches_per_step": sum(c.get("launches", 1) for c in ecalls)}
+            if ekind == "prefill":
+                tf = ef / (e_ms * 1e-3) / 1e12
+                entry.update({"value": round(tf, 1), "unit": "TFLOP/s",
+                              "frac_of_measured_tensor": round(tf / pk["bf16_tflops"], 4)})
+            else:
+                gb = eb / (e_ms * 1e-3) / 1e9
+                entry.update({"value": round(gb, 1), "unit": "GB/s",
+                              "frac_of_measured_hbm": round(gb / pk["hbm_gbs"], 4),
+                              "frac_of_read_probe": round(gb / probe_gbs, 4)})
+            entry["sweep"] = per_call_sweep(torch, stream, ecalls, ekind, pk)
+            extras[key] = entry
+            del er, ecalls
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
 
     clock_info = clocks.stop()
 
@@ -538,7 +641,11 @@ def run_ours(args, dist, rank, local, world):
             roof = {"bound": "hbm", "achieved": round(gbs_total / world, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                     "frac": round(gbs_total / world / pk["hbm_gbs"], 4),
                     "peak_source": f"{pk['source']} (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)",
-                    "kernel": "gemv_stream_kernel"}
+                    "kernel": "qmv_stream_kernel"}
+        roof["peak_read_probe"] = round(probe_gbs, 1)
+        roof["frac_of_read_probe"] = None if kind == "prefill" else round(gbs_total / world / probe_gbs, 4)
+        roof["read_probe"] = (f"qmv_read_probe: {probe_bytes / 2**30:.2f} GiB (16x L2) streamed by bulk copies "
+                              f"into per-warp rings, no arithmetic; best of 5 x 10 launches on this GPU")
         tr = traffic_record(args.workload)
         roof["traffic"] = (tr or {}).get("bytes_per_launch")
         if tr:
@@ -564,6 +671,7 @@ def run_ours(args, dist, rank, local, world):
             "e2e": e2e,
             "impl": "ours",
         }
+        out.update(extras)
     return out, step_bytes, calls
 
 
@@ -702,6 +810,91 @@ def run_reference(args, rank, world):
 
 
 # ---------------------------------------------------------------------------------
+def phase_timeline(workload, out_json=None):
+    """Per-phase timeline of one workload's calls replayed back to back from
+    CUDA graphs, read from global-timer stamps that a build with
+    -DQMV_PHASE_STAMPS records per CTA (a separate library variant; the product
+    build has no stamps).  Run under QMV_LIB pointing at that variant.
+
+    Decode calls (per CTA: entry, griddepcontrol.wait returned, activations
+    staged, first and last warp done) and prefill calls (entry, set-up done,
+    first MMA, last commit, accumulator ready, exit, SM cycles of the MMA span)
+    are summarised per call as medians over the CTAs of each launch and then
+    over steps (ns)."""
+    import ctypes
+    import torch
+    import weight_quantized_decode_gb300 as q
+    L = q.lib()
+    prefill = WORKLOADS[workload]["kind"] == "prefill"
+    words = 8 if prefill else 7
+    fn = L.qmv_prefill_phase_stamps if prefill else L.qmv_phase_stamps
+    fn.restype = ctypes.c_int64
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_int64]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    l2 = int(torch.cuda.get_device_properties(dev).L2_cache_size)
+    stream = torch.cuda.Stream(dev)
+    calls, period = build_calls(workload, q, torch, dev, l2, int(stream.cuda_stream))
+    with torch.cuda.stream(stream):
+        for c in calls:
+            c["call"](0)
+    torch.cuda.synchronize()
+    runner = StepRunner(torch, stream, calls, period)
+    runner.run(2 * period)
+    cap = 1 << 18
+    buf = (ctypes.c_ulonglong * (cap * words))()
+    fn(buf, cap)                      # discard the warm-up records
+    ms = runner.time_ms(period)       # one replay of the period graph: every launch once
+    n = fn(buf, cap)
+    a = np.frombuffer(buf, dtype=np.uint64, count=n * words).reshape(n, words).astype(np.int64)
+    # launches in replay order; a call split into token subsets has several
+    seqs = sorted(set((a[:, 0] >> 32).tolist()))
+    launches = [a[(a[:, 0] >> 32) == s] for s in seqs]
+    per_step = len(launches) // period
+    names = []
+    for c in calls:
+        names.append(c["name"])
+    if per_step != len(names):     # token-split calls: label the extra launches
+        names = [f"launch{i}" for i in range(per_step)]
+    rows = {}
+    for i, r in enumerate(launches):
+        nm = names[i % per_step]
+        d = rows.setdefault(nm, {})
+        def put(k, v):
+            d.setdefault(k, []).append(float(v))
+        put("grid", len(r))
+        prev_end = launches[i - 1][:, 6 if prefill else 5].max() if i else None
+        if prefill:
+            e, su, f, lc, acc, ex, clk = (r[:, j] for j in range(1, 8))
+            put("setup", np.median(su - e))
+            put("to_first_mma", np.median(f - su))
+            put("mma_span", np.median(lc - f))
+            put("sm_mhz", np.median(clk / np.maximum(lc - f, 1) * 1e3))
+            put("acc_ready_after_last_commit", np.median(acc - lc))
+            put("epilogue", np.median(ex - acc))
+            if prev_end is not None:
+                put("call_period", ex.max() - prev_end)
+                put("entry_after_prev_end", np.median(e) - prev_end)
+        else:
+            e, w, st, first, last = (r[:, j] for j in range(1, 6))
+            put("wait_minus_entry", np.median(w - e))
+            put("stage_activations", np.median(st - w))
+            put("main_loop", np.median(last - st))
+            put("tail", last.max() - np.median(last))
+            if prev_end is not None:
+                put("call_period", last.max() - prev_end)
+                put("wait_after_prev_end", np.median(w) - prev_end)
+    summary = {nm: {k: round(statistics.median(v), 1) for k, v in d.items()} for nm, d in rows.items()}
+    out = {"workload": workload, "us_per_step": round(ms / period * 1e3, 2), "steps": period,
+           "unit": "ns (medians over the CTAs of a launch, then over steps)", "calls": summary}
+    print(json.dumps(out, indent=1))
+    if out_json:
+        with open(out_json, "w") as f:
+            json.dump(out, f, indent=1)
+    return out
+
+
+# ---------------------------------------------------------------------------------
 def ncu_case(spec):
     """A handful of eager calls of one table over rotated copies larger than L2
     (a small, bounded program for an Nsight Compute capture).
@@ -754,11 +947,24 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="q4_0_m1_sweep")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="default workload only: skip the Q8_0, multi-expert and prefill sweeps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--phase-timeline", default=None, metavar="WORKLOAD",
+                    help="build the phase-stamp variant of the library and print the per-phase timeline of "
+                         "WORKLOAD's calls back to back (no bench line)")
     ap.add_argument("--ncu-case", default=None,
                     help="FMT:NxK:M -- only run a few eager calls of one shape (for Nsight Compute captures)")
     args = ap.parse_args()
+    if args.phase_timeline:
+        if not os.environ.get("QMV_LIB"):
+            from weight_quantized_decode_gb300 import build as _b
+            lib = _b.build(extra=["-DQMV_PHASE_STAMPS"], variant="phase")
+            env = dict(os.environ, QMV_LIB=lib)
+            sys.exit(subprocess.run([sys.executable] + sys.argv, env=env).returncode)
+        phase_timeline(args.phase_timeline)
+        return
     if args.ncu_case:
         ncu_case(args.ncu_case)
         return

@@ -29,7 +29,9 @@ import os
 import threading
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libqmv.so")
+# QMV_LIB selects another build of the same library (the phase-timeline
+# variant of phase_timeline.py); there is no CPU path either way.
+LIB_PATH = os.environ.get("QMV_LIB") or os.path.join(_HERE, "libqmv.so")
 
 QMV_OK = 0
 QMV_DEV_BAD_EXPERT = 0x1

@@ -35,8 +35,13 @@ def _stale(obj: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, extra: list[str] | None = None) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, extra: list[str] | None = None, variant: str | None = None) -> str:
+    """Compile and link the library.  `extra` adds nvcc flags; `variant` builds
+    into _build_<variant>/ and libqmv_<variant>.so instead of the product
+    library (e.g. the phase-timeline build with -DQMV_PHASE_STAMPS)."""
+    build_dir = BUILD if variant is None else os.path.join(HERE, f"_build_{variant}")
+    lib_path = LIB if variant is None else os.path.join(HERE, f"libqmv_{variant}.so")
+    os.makedirs(build_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     headers = glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + \
         [os.path.join(HERE, "..", "include", "qmv.h")]
@@ -44,8 +49,8 @@ def build(verbose: bool = False, extra: list[str] | None = None) -> str:
     extra = list(extra or [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-        if _stale(obj, [src] + headers) or extra:
+        obj = os.path.join(build_dir, os.path.basename(src) + ".o")
+        if _stale(obj, [src] + headers) or (extra and variant is None):
             cmd = [cc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
             if verbose:
                 print(" ".join(cmd), flush=True)
@@ -58,14 +63,14 @@ def build(verbose: bool = False, extra: list[str] | None = None) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    if _stale(LIB, objs) or extra:
-        tmp = LIB + f".tmp{os.getpid()}"
+    if _stale(lib_path, objs) or (extra and variant is None):
+        tmp = lib_path + f".tmp{os.getpid()}"
         cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -26,6 +26,12 @@ __device__ int g_status_fetched[kFetchSlots];
 
 __global__ void status_fetch_clear_kernel(int *status, int *slot) { *slot = atomicExch(status, 0); }
 
+#ifdef QMV_PHASE_STAMPS
+// Phase-timeline builds only: [record count, records of kPhaseWords words].
+__device__ unsigned long long g_phase_buf[1 + static_cast<size_t>(kPhaseWords) * kPhaseCap];
+std::atomic<unsigned> g_phase_seq{0};
+#endif
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -130,14 +136,15 @@ struct Plan {
 };
 
 // Launch-shape overrides for tuning sweeps: QMV_GEMV_TUNE="warps=16,stages=3,
-// G=8,SP=1,ctas=2,share=2" (any subset; 0 or absent = the built-in rule).
+// G=8,SP=1,ctas=2,share=2,early=1" (any subset; 0 or absent = the built-in
+// rule; early = stages requested before the previous grid completes).
 // ctas = CTAs per SM in the grid; share = the fraction 1/share of an SM's
 // shared memory one CTA may use (share=2 leaves room for the next call's CTA
 // to become resident early under programmatic dependent launch).  N=, K= and
 // M= restrict the override to one table shape (N the planned rows: 2N for the
 // fused SwiGLU, the expert's rows for the multi-expert call).
 struct Tune {
-    int warps = 0, stages = 0, G = 0, SP = 0, ctas = 0, share = 0;
+    int warps = 0, stages = 0, G = 0, SP = 0, ctas = 0, share = 0, early = -1;
     // optional: apply only to the table shape N x K at M tokens (0 = every shape)
     long long N = 0, K = 0;
     int M = 0;
@@ -170,6 +177,7 @@ const Tune &tune_overrides()
             else if (!std::strcmp(key, "SP")) t.SP = v;
             else if (!std::strcmp(key, "ctas")) t.ctas = v;
             else if (!std::strcmp(key, "share")) t.share = v;
+            else if (!std::strcmp(key, "early")) t.early = v;
         }
     });
     return t;
@@ -285,6 +293,7 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
         if (S > stages) S = stages;
         if (S >= 2) {
             p.S = S;
+            p.early = tu.early >= 0 ? tu.early : 1;
             pl.streaming = true;
             pl.grid = grid;
             pl.warps = warps;
@@ -302,6 +311,11 @@ cudaError_t launch_streaming(int fmt, const GemvParams &p0, int M, const Plan &p
 {
     GemvParams p = p0;
     p.test_skip_copy = test_skip_this_launch(kArmDecode) ? 1 : 0;
+#ifdef QMV_PHASE_STAMPS
+    void *ph = nullptr;
+    if (cudaGetSymbolAddress(&ph, g_phase_buf) == cudaSuccess) p.phase = static_cast<unsigned long long *>(ph);
+    p.phase_seq = g_phase_seq.fetch_add(1);
+#endif
     if (fmt == kQ4_0 && p.xq8) return launch_gemv_stream_q4_0_q8_1(M, p, pl.grid, pl.warps, pl.smem, stream, pdl);
     if (fmt == kQ8_0 && p.xq8) return launch_gemv_stream_q8_0_q8_1(M, p, pl.grid, pl.warps, pl.smem, stream, pdl);
     if (fmt == kQ4_0 && p.W2) return launch_gemv_stream_q4_0_swiglu(M, p, pl.grid, pl.warps, pl.smem, stream, pdl);
@@ -436,7 +450,12 @@ cudaError_t ensure_smem_optin(const void *func, size_t smem)
     int optin = 0;
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    // The opt-in limit covers static and dynamic shared memory together.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, func);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             optin - static_cast<int>(fa.sharedSizeBytes));
     if (e != cudaSuccess) return e;
     if (nseen < 256) {
         seen_func[nseen] = func;
@@ -694,5 +713,27 @@ const char *qmv_status_str(qmv_status s)
 }
 
 const char *qmv_version(void) { return "qmv 0.1.0 sm_103a"; }
+
+#ifdef QMV_PHASE_STAMPS
+// Phase-timeline builds only (not declared in include/qmv.h): copies up to
+// max_records records of the streaming decode kernel's phase stamps to host
+// memory, then resets the record count and the launch sequence.  Returns the
+// number of records copied, or -1 on a CUDA error.
+QMV_API int64_t qmv_phase_stamps(unsigned long long *host, int64_t max_records)
+{
+    if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+    unsigned long long n = 0;
+    if (cudaMemcpyFromSymbol(&n, g_phase_buf, sizeof(n)) != cudaSuccess) return -1;
+    if (n > static_cast<unsigned long long>(kPhaseCap)) n = kPhaseCap;
+    if (static_cast<int64_t>(n) > max_records) n = static_cast<unsigned long long>(max_records);
+    if (n && cudaMemcpyFromSymbol(host, g_phase_buf, n * kPhaseWords * sizeof(unsigned long long),
+                                  sizeof(unsigned long long)) != cudaSuccess)
+        return -1;
+    const unsigned long long zero = 0;
+    if (cudaMemcpyToSymbol(g_phase_buf, &zero, sizeof(zero)) != cudaSuccess) return -1;
+    g_phase_seq.store(0);
+    return static_cast<int64_t>(n);
+}
+#endif
 
 }  // extern "C"

@@ -94,6 +94,8 @@ struct GemvParams {
     int G;                       // lanes per row (1..32; RG = 32 / G rows per warp)
     int SP;                      // passes per stage (odd)
     int S;                       // stages in each warp's ring
+    int early;                   // stages requested before griddepcontrol.wait (the rest after the
+                                 // activation loads); the multi-expert call requests none early
     int xq8;                     // Q4_0 or Q8_0 against Q8_1-quantised activations (integer dots)
     const int8_t *xq;            // activations already in Q8_1 (codes [M][K]); else quantised in the kernel
     const uint16_t *xq_d;        //   their fp16 scales' bits [M][K/32]
@@ -101,7 +103,16 @@ struct GemvParams {
     int *status;                 // device status word
     int test_skip_copy;          // failure-detection test only: CTA 0's warp 0 never requests its first
                                  // stage, so its bounded wait runs out (0 in every normal call)
+    unsigned long long *phase;   // phase-timeline builds only (QMV_PHASE_STAMPS): [count, records...]
+    unsigned int phase_seq;      //   this launch's sequence number
 };
+
+// Phase timeline: a build switch (QMV_PHASE_STAMPS), off by default, that
+// adds no work to the product build.  Each CTA records global-timer stamps at
+// entry, when griddepcontrol.wait returns (the previous grid has completed),
+// when the activations are staged, and when its first and last warps finish.
+constexpr int kPhaseWords = 7;   // seq << 32 | cta, t_entry, t_wait, t_staged, t_first_done, t_last_done, smid
+constexpr int kPhaseCap = 1 << 18;
 
 // Shared-memory bytes the kernel needs for a configuration.
 __host__ __device__ inline size_t gemv_smem_bytes(int fmt, int M, int n_problems, int U, int warps, int S, int SP,
@@ -525,6 +536,15 @@ __global__ void __launch_bounds__(MAXT, 1) qmv_stream_kernel(const GemvParams p)
     const int warp = threadIdx.x >> 5;
     const int warps = blockDim.x >> 5;
     const int U = p.U, G = p.G, SP = p.SP, S = p.S;
+#ifdef QMV_PHASE_STAMPS
+    __shared__ unsigned long long ph_t[4];   // entry, wait, staged, first warp done
+    __shared__ unsigned long long ph_last;
+    if (threadIdx.x == 0) {
+        ph_t[0] = global_timer_ns();
+        ph_t[3] = ~0ull;
+        ph_last = 0;
+    }
+#endif
     const int RG = 32 / G;
     // Row indices fit in 32 bits (checked on the host).
     const uint32_t N = static_cast<uint32_t>(p.N);
@@ -616,10 +636,13 @@ __global__ void __launch_bounds__(MAXT, 1) qmv_stream_kernel(const GemvParams p)
     // thread's activation loads: the activations are on the critical path and
     // must not queue behind megabytes of weight traffic.
     const int prefetch = total < S ? total : S;
-    const int early = MOE ? 0 : (prefetch < 1 ? prefetch : 1);
+    const int early = MOE ? 0 : (prefetch < p.early ? prefetch : p.early);
     for (int i = 0; i < early; ++i) issue_next();
 
     pdl_wait_prior_grid();
+#ifdef QMV_PHASE_STAMPS
+    if (threadIdx.x == 0) ph_t[1] = global_timer_ns();
+#endif
 
     if (MOE) {
         // The CTA's expert indices, once, before any copy needs them.
@@ -832,6 +855,9 @@ __global__ void __launch_bounds__(MAXT, 1) qmv_stream_kernel(const GemvParams p)
     }
     __syncthreads();
     pdl_allow_next_grid();
+#ifdef QMV_PHASE_STAMPS
+    if (threadIdx.x == 0) ph_t[2] = global_timer_ns();
+#endif
 
     const int r = lane / G;
     const int q = lane - r * G;
@@ -960,6 +986,29 @@ __global__ void __launch_bounds__(MAXT, 1) qmv_stream_kernel(const GemvParams p)
         }
         __syncwarp();
     }
+#ifdef QMV_PHASE_STAMPS
+    if (lane == 0) {
+        const unsigned long long t = global_timer_ns();
+        atomicMin(&ph_t[3], t);
+        atomicMax(&ph_last, t);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && p.phase) {
+        const unsigned long long i = atomicAdd(p.phase, 1ull);
+        if (i < kPhaseCap) {
+            unsigned smid;
+            asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+            unsigned long long *rec = p.phase + 1 + i * kPhaseWords;
+            rec[0] = (static_cast<unsigned long long>(p.phase_seq) << 32) | blockIdx.x;
+            rec[1] = ph_t[0];
+            rec[2] = ph_t[1];
+            rec[3] = ph_t[2];
+            rec[4] = ph_t[3];
+            rec[5] = ph_last;
+            rec[6] = smid;
+        }
+    }
+#endif
 }
 
 // ---- the generic kernel (any K % 32 == 0, any M, activations from global) ----------

@@ -40,11 +40,13 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
 
+#include "../../include/qmv.h"
 #include "qmv_common.cuh"
 #include "qmv_launch.h"
 #include "qmv_prefill.h"
@@ -69,7 +71,18 @@ struct PrefillParams {
     int KSUB;          // 64-K atoms per slot (1 or 2): MMAs per barrier round = 4 * KSUB
     uint32_t tmem_cols;
     int test_skip_copy;   // failure-detection test only: CTA (0, 0) never requests its first packed tile
+    unsigned long long *phase;   // phase-timeline builds only (QMV_PHASE_STAMPS): [count, records...]
+    unsigned int phase_seq;
 };
+
+#ifdef QMV_PHASE_STAMPS
+// Phase-timeline record (QMV_PHASE_STAMPS builds): seq << 32 | CTA, global-timer
+// stamps at entry, after set-up, at the first MMA, after the last commit, when
+// the accumulator is complete and at exit, and the SM clock cycles between the
+// first MMA and the last commit.
+constexpr int kPrefillPhaseWords = 8;
+constexpr int kPrefillPhaseCap = 1 << 16;
+#endif
 
 // ---- tcgen05 / TMA wrappers -------------------------------------------------------
 
@@ -235,6 +248,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+#ifdef QMV_PHASE_STAMPS
+    __shared__ unsigned long long phs[7];   // entry, setup, first MMA, last commit, acc ready, clk0, clk1
+    if (threadIdx.x == 0) phs[0] = global_timer_ns();
+#endif
     const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kBM;
     const int64_t m0 = static_cast<int64_t>(blockIdx.y) * TN;
     const int nK = static_cast<int>(p.K / (kKB * KSUB));   // slots of KSUB x 64 K
@@ -260,6 +277,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+#ifdef QMV_PHASE_STAMPS
+    if (threadIdx.x == 0) phs[1] = global_timer_ns();
+#endif
     // The next kernel of the stream may be scheduled now (its CTAs start on
     // free SMs and stream their own weights); it reads what this kernel
     // writes only after its own griddepcontrol.wait.
@@ -344,6 +364,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Order the MMAs after the barrier waits (the tcgen05 ops are
                 // asynchronous to this thread).
                 tc_fence_after();
+#ifdef QMV_PHASE_STAMPS
+                if (j == 0) {
+                    phs[2] = global_timer_ns();
+                    phs[5] = clock64();
+                }
+#endif
                 if (NH == 1) {
                     mma_f16_slice(tmem_base, a_desc, b_desc, idesc, j == 0);
                     if (KSUB == 2)
@@ -369,6 +395,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             mma_commit(accfull);
+#ifdef QMV_PHASE_STAMPS
+            phs[3] = global_timer_ns();
+            phs[6] = clock64();
+#endif
             if (!ok && committed > 0) mbar_wait_bounded(accfull, 0, nullptr);
         }
     } else {
@@ -467,6 +497,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (!mbar_try_wait_sleep(accfull, 0, kSuspendHintNs)) {
         }
         tc_fence_after();
+#ifdef QMV_PHASE_STAMPS
+        if (threadIdx.x == 0) phs[4] = global_timer_ns();
+#endif
         const int quarter = warp & 3;
         const int nq = (kThreads / 32 - quarter + 3) / 4;   // warps in this quarter
         const int rank = warp >> 2;
@@ -490,9 +523,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem_base, p.tmem_cols);
     }
+#ifdef QMV_PHASE_STAMPS
+    if (threadIdx.x == 0 && p.phase) {
+        const unsigned long long i = atomicAdd(p.phase, 1ull);
+        if (i < kPrefillPhaseCap) {
+            unsigned long long *rec = p.phase + 1 + i * kPrefillPhaseWords;
+            rec[0] = (static_cast<unsigned long long>(p.phase_seq) << 32) | (blockIdx.y * gridDim.x + blockIdx.x);
+            rec[1] = phs[0];
+            rec[2] = phs[1];
+            rec[3] = phs[2];
+            rec[4] = phs[3];
+            rec[5] = phs[4];
+            rec[6] = global_timer_ns();
+            rec[7] = phs[6] - phs[5];
+        }
+    }
+#endif
 }
 
 // ---- host side -------------------------------------------------------------------
+
+#ifdef QMV_PHASE_STAMPS
+__device__ unsigned long long g_prefill_phase[1 + static_cast<size_t>(kPrefillPhaseWords) * kPrefillPhaseCap];
+std::atomic<unsigned> g_prefill_phase_seq{0};
+#endif
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
@@ -580,6 +634,14 @@ cudaError_t launch_prefill(const PrefillPlan &pl, const void *W, const void *x, 
     p.KSUB = pl.KSUB;
     p.tmem_cols = pl.tmem_cols;
     p.test_skip_copy = test_skip_copy ? 1 : 0;
+#ifdef QMV_PHASE_STAMPS
+    {
+        void *ph = nullptr;
+        if (cudaGetSymbolAddress(&ph, g_prefill_phase) == cudaSuccess)
+            p.phase = static_cast<unsigned long long *>(ph);
+        p.phase_seq = g_prefill_phase_seq.fetch_add(1);
+    }
+#endif
     cudaError_t e = ensure_smem_optin(reinterpret_cast<const void *>(prefill_kernel), pl.smem);
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>(pl.grid_x), static_cast<unsigned>(pl.grid_y));
@@ -587,3 +649,25 @@ cudaError_t launch_prefill(const PrefillPlan &pl, const void *W, const void *x, 
 }
 
 }  // namespace qmv
+
+#ifdef QMV_PHASE_STAMPS
+// Phase-timeline builds only (not declared in include/qmv.h): copies up to
+// max_records prefill records to host memory and resets them; returns the
+// count or -1 on a CUDA error.
+extern "C" QMV_API int64_t qmv_prefill_phase_stamps(unsigned long long *host, int64_t max_records)
+{
+    using namespace qmv;
+    if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+    unsigned long long n = 0;
+    if (cudaMemcpyFromSymbol(&n, g_prefill_phase, sizeof(n)) != cudaSuccess) return -1;
+    if (n > static_cast<unsigned long long>(kPrefillPhaseCap)) n = kPrefillPhaseCap;
+    if (static_cast<int64_t>(n) > max_records) n = static_cast<unsigned long long>(max_records);
+    if (n && cudaMemcpyFromSymbol(host, g_prefill_phase, n * kPrefillPhaseWords * sizeof(unsigned long long),
+                                  sizeof(unsigned long long)) != cudaSuccess)
+        return -1;
+    const unsigned long long zero = 0;
+    if (cudaMemcpyToSymbol(g_prefill_phase, &zero, sizeof(zero)) != cudaSuccess) return -1;
+    g_prefill_phase_seq.store(0);
+    return static_cast<int64_t>(n);
+}
+#endif
