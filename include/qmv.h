@@ -293,8 +293,8 @@ QMV_API qmv_status qmv_q4_0_swiglu_f32(const void *W_gate, const void *W_up, con
  * tensor cores (volta-kernel-bakeoff, "What's in the race"), and the plan to
  * dequantise inside the tensor-core multiply ("What we'd do next", item 3).
  * On sm_103a: packed
- * W tiles staged by bulk copies, dequantised to 16-bit in shared memory, fed to
- * tcgen05.mma with fp32 accumulators in tensor memory.
+ * W tiles staged by bulk copies, dequantised to fp16 straight into tensor
+ * memory, where tcgen05.mma reads them beside its fp32 accumulators.
  *   W : Q4_0 bytes [N][K/32*18], 16-byte aligned.  The tensor-core kernel
  *       takes K % 256 == 0 (any N: a ragged last 128-row tile is masked);
  *       other K take the generic kernel.

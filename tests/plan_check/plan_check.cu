@@ -191,8 +191,11 @@ void check_swiglu(int64_t N, int64_t K, int M)
 
 // The tensor-core prefill kernel: tile and ring choices, the shared-memory
 // layout and its alignment, tensor-copy boxes and coordinates, tensor-memory
-// columns, the dequantising threads' reads and writes, and the epilogue's
-// coverage of every (lane quarter, column chunk) of the accumulator.
+// columns (accumulator and dequantised weight atoms), the dequantising
+// threads' reads of the packed slot and writes of tensor memory (each lane and
+// column of every weight atom written exactly once, by a warp whose lane
+// quarter holds it), the MMAs' operand addresses, and the epilogue's coverage
+// of every (lane quarter, column chunk) of the accumulator.
 void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int ns_force)
 {
     const PrefillPlan pl = plan_prefill(N, K, M, sms, nw_force, ns_force);
@@ -206,16 +209,15 @@ void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int n
     }
     ++g_checked;
     CHECK(shape_ok, "prefill took %lldx%lld M=%lld", (long long)N, (long long)K, (long long)M);
-    const int TN = pl.TN, NH = pl.NH, KSUB = pl.KSUB, NW = pl.NW, NS = pl.NS;
-    const int TNH = TN / NH;
-    CHECK(TN % 64 == 0 && TN <= 512 && TN % NH == 0 && (NH == 1 || NH == 2), "TN %d NH %d", TN, NH);
-    CHECK(TNH % 16 == 0 && TNH >= 16 && TNH <= 256, "MMA N %d", TNH);   // kind::f16 with M = 128
-    CHECK((KSUB == 1 || KSUB == 2) && (NH == 1 || KSUB == 1), "KSUB %d NH %d", KSUB, NH);
+    const int TN = pl.TN, KSUB = pl.KSUB, NW = pl.NW, NS = pl.NS;
+    CHECK(TN % 64 == 0 && TN >= 64 && TN <= 256, "TN %d", TN);                 // kind::f16, M = 128: N <= 256
+    CHECK(KSUB == 1 || KSUB == 2 || KSUB == 4, "KSUB %d", KSUB);              // a slot never straddles a W tile
     CHECK(NW >= 1 && NS >= 2, "rings %d %d", NW, NS);
     CHECK(pl.smem <= static_cast<size_t>(kOptin), "prefill smem %zu", pl.smem);
     const uint32_t cols = pl.tmem_cols;
-    CHECK(cols >= 32 && cols <= 512 && (cols & (cols - 1)) == 0 && static_cast<uint32_t>(TN) <= cols, "TMEM %u",
-          cols);
+    CHECK(cols == 512, "TMEM %u", cols);
+    const int64_t a_end = TN + static_cast<int64_t>(NS) * KSUB * kAtomCols;
+    CHECK(a_end <= cols, "TMEM columns %lld > %u", (long long)a_end, cols);
     CHECK(pl.grid_x >= 1 && pl.grid_x <= INT32_MAX && pl.grid_y >= 1 && pl.grid_y <= kMaxGridY, "grid");
     CHECK(pl.grid_x * kBM >= N && (pl.grid_x - 1) * kBM < N, "row tiles");
     CHECK(pl.grid_y * TN >= M && (pl.grid_y - 1) * TN < M, "token tiles");
@@ -223,26 +225,21 @@ void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int n
     CHECK(nK * KSUB * kKB == K && nC * 4 == nK * KSUB && nK < INT32_MAX, "K loop");
 
     // shared memory, as offsets from the 1024-byte-aligned base
-    const size_t a_slot = static_cast<size_t>(KSUB) * kATileBytes;
-    const size_t b_atom = static_cast<size_t>(TN) * kKB * 2, b_half = static_cast<size_t>(TNH) * kKB * 2;
+    const size_t b_atom = static_cast<size_t>(TN) * kKB * 2;
     const size_t b_slot = KSUB * b_atom;
-    const size_t b_off = NS * a_slot, w_off = b_off + NS * b_slot;
+    const size_t w_off = NS * b_slot;
     const size_t bar_off = w_off + static_cast<size_t>(NW) * kPackedTileBytes;
     const size_t bar_end = bar_off + static_cast<size_t>(2 * NW + 3 * NS + 1) * 8 + 4 + 4;
     CHECK(1023 + bar_end <= pl.smem, "layout %zu + slack > %zu", bar_end, pl.smem);
     CHECK((bar_off + 1024) >> 4 < (size_t(1) << 14), "descriptor address field");
     for (int s = 0; s < NS; ++s)
-        for (int a = 0; a < KSUB; ++a) {
-            CHECK((s * a_slot + a * kATileBytes) % 1024 == 0, "A tile alignment");
-            for (int h = 0; h < NH; ++h)
-                CHECK((b_off + s * b_slot + a * b_atom + h * b_half) % 1024 == 0, "B tile alignment");
-        }
+        for (int a = 0; a < KSUB; ++a) CHECK((s * b_slot + a * b_atom) % 1024 == 0, "B tile alignment");
     for (int w = 0; w < NW; ++w) CHECK((w_off + static_cast<size_t>(w) * kPackedTileBytes) % 128 == 0, "W slot");
 
     // tensor-copy boxes: within the box limits; bytes landed = the barrier's expected count
-    CHECK(kPackedRowBytes <= 256 && kBM <= 256 && TNH <= 256 && kKB * 2 <= 128, "boxes");
+    CHECK(kPackedRowBytes <= 256 && kBM <= 256 && TN <= 256 && kKB * 2 <= 128, "boxes");
     CHECK(static_cast<size_t>(kPackedRowBytes) * kBM == static_cast<size_t>(kPackedTileBytes), "W box bytes");
-    CHECK(static_cast<size_t>(KSUB) * NH * kKB * TNH * 2 == b_slot, "x box bytes");
+    CHECK(static_cast<size_t>(KSUB) * kKB * TN * 2 == b_slot, "x box bytes");
     // coordinates: innermost x times the element size on 16 bytes and inside the row
     const int64_t row_bytes = (K / 32) * 18;
     for (int64_t c = 0; c < nC; c += (c < 4 || c + 4 >= nC) ? 1 : std::max<int64_t>(1, nC / 64)) {
@@ -254,48 +251,52 @@ void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int n
             const int64_t x = (j * KSUB + a) * kKB;
             CHECK((x * 2) % 16 == 0 && x + kKB <= K, "x x %lld", (long long)x);
         }
-    for (int64_t by = 0; by < pl.grid_y; ++by)
-        for (int h = 0; h < NH; ++h) {
-            const int64_t yc = by * TN + static_cast<int64_t>(h) * TNH;   // rows past M read the fill value
-            CHECK(yc >= 0 && yc + TNH <= INT32_MAX, "x y %lld", (long long)yc);
-        }
+    for (int64_t by = 0; by < pl.grid_y; ++by) {
+        const int64_t yc = by * TN;   // rows past M read the fill value
+        CHECK(yc >= 0 && yc + TN <= INT32_MAX, "x y %lld", (long long)yc);
+    }
     CHECK((pl.grid_x - 1) * kBM < N && (pl.grid_x - 1) * kBM <= INT32_MAX, "W y");
 
-    // dequantising threads: reads of the packed slot, writes of the A tile
-    static unsigned char cover[kATileBytes / 16];
+    // dequantising warps 0..7: reads of the packed slot; tensor-memory writes
+    static unsigned char cover[kBM][kAtomCols];
     for (int s = 0; s < NS; ++s)
         for (int a = 0; a < KSUB; ++a) {
-            std::fill(cover, cover + kATileBytes / 16, 0);
-            for (int dt = 0; dt < 256; ++dt) {
-                const int r = dt & (kBM - 1), hsel = dt >> 7;
-                CHECK(static_cast<size_t>(NW - 1) * kPackedTileBytes + r * kPackedRowBytes + 16 * 8 + 16 <=
-                          static_cast<size_t>(NW) * kPackedTileBytes,
-                      "packed read");
-                for (int ch = 0; ch < 4; ++ch) {
-                    const int cc = 4 * hsel + ch;
-                    const size_t off = (r >> 3) * 1024 + (r & 7) * 128 + ((cc ^ (r & 7)) << 4);
-                    CHECK(s * a_slot + a * kATileBytes + off + 16 <= NS * a_slot, "A write");
-                    ++cover[off / 16];
+            std::fill(&cover[0][0], &cover[0][0] + kBM * kAtomCols, 0);
+            for (int w = 0; w < 8; ++w) {
+                const int quarter = w & 3, hsel = w >> 2;
+                CHECK(w != 8 && w != 9 && w != 10, "dequantiser role");
+                for (int lane = 0; lane < 32; ++lane) {
+                    const int r = 32 * quarter + lane;
+                    CHECK(r / 32 == (w & 3), "lane quarter of warp %d", w);
+                    CHECK(static_cast<size_t>(NW - 1) * kPackedTileBytes + r * kPackedRowBytes + 16 * 8 + 16 <=
+                              static_cast<size_t>(NW) * kPackedTileBytes,
+                          "packed read");
+                    const int64_t c0 = TN + static_cast<int64_t>(s * KSUB + a) * kAtomCols + 16 * hsel;
+                    CHECK(c0 >= TN && c0 + 16 <= a_end, "A columns");
+                    for (int j = 0; j < 16; ++j) ++cover[r][16 * hsel + j];
                 }
             }
-            for (int i = 0; i < kATileBytes / 16; ++i) CHECK(cover[i] == 1, "A chunk %d written %d times", i, cover[i]);
+            for (int r = 0; r < kBM; ++r)
+                for (int c = 0; c < kAtomCols; ++c) CHECK(cover[r][c] == 1, "A cell %d,%d written %d times", r, c, cover[r][c]);
+            // the MMAs of this atom read columns [base, base + 32) in four K = 16 steps of 8 columns
+            const int64_t base = TN + static_cast<int64_t>(s * KSUB + a) * kAtomCols;
+            for (int k = 0; k < 4; ++k) CHECK(base + 8 * k + 8 <= a_end, "MMA A columns");
         }
     for (int sub = 0; sub < 4; ++sub) CHECK(4 * (9 * sub + 8) + 4 <= kPackedRowBytes, "block words");
 
-    // epilogue: each (lane quarter, 32-column chunk) read by exactly one warp, inside the allocation
+    // epilogue: each (lane quarter, 32-column chunk) read by exactly one warp, inside the accumulator
     static unsigned char ecover[4][16];
     std::fill(&ecover[0][0], &ecover[0][0] + 64, 0);
     const int warps = kPrefillThreads / 32;
     for (int w = 0; w < warps; ++w) {
         const int quarter = w & 3, nq = (warps - quarter + 3) / 4, rank = w >> 2;
         for (int c0 = 32 * rank; c0 < TN; c0 += 32 * nq) {
-            CHECK(c0 + 32 <= TN && static_cast<uint32_t>(c0 + 32) <= cols, "epilogue columns");
+            CHECK(c0 + 32 <= TN, "epilogue columns");
             ++ecover[quarter][c0 / 32];
         }
     }
     for (int q = 0; q < 4; ++q)
         for (int c = 0; c < TN / 32; ++c) CHECK(ecover[q][c] == 1, "epilogue chunk %d,%d read %d times", q, c, ecover[q][c]);
-    for (int h = 0; h < NH; ++h) CHECK(static_cast<uint32_t>((h + 1) * TNH) <= cols, "accumulator %d", h);
 }
 
 }  // namespace

@@ -293,7 +293,10 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
         if (S > stages) S = stages;
         if (S >= 2) {
             p.S = S;
-            p.early = tu.early >= 0 ? tu.early : 1;
+            // stages requested before the activation loads: one for a plain
+            // call (before the previous grid completes), all for the
+            // multi-expert call (right after its indices are read)
+            p.early = tu.early >= 0 ? tu.early : (p.n_problems > 1 ? S : 1);
             pl.streaming = true;
             pl.grid = grid;
             pl.warps = warps;

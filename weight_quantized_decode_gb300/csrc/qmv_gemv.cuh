@@ -635,8 +635,12 @@ __global__ void __launch_bounds__(MAXT, 1) qmv_stream_kernel(const GemvParams p)
     // call waits first.  The remaining prefetch is requested after this
     // thread's activation loads: the activations are on the critical path and
     // must not queue behind megabytes of weight traffic.
+    // The multi-expert call requests its first p.early stages as soon as it
+    // has the indices, ahead of its activation loads (it has no weights in
+    // flight before then).
     const int prefetch = total < S ? total : S;
-    const int early = MOE ? 0 : (prefetch < p.early ? prefetch : p.early);
+    const int early_n = prefetch < p.early ? prefetch : p.early;
+    int early = MOE ? 0 : early_n;
     for (int i = 0; i < early; ++i) issue_next();
 
     pdl_wait_prior_grid();
@@ -648,6 +652,8 @@ __global__ void __launch_bounds__(MAXT, 1) qmv_stream_kernel(const GemvParams p)
         // The CTA's expert indices, once, before any copy needs them.
         for (int i = threadIdx.x; i <= prob_hi - prob_lo; i += blockDim.x) sidx[i] = p.expert_idx[prob_lo + i];
         __syncthreads();
+        for (int i = 0; i < early_n; ++i) issue_next();
+        early = early_n;
     }
 
     // Stage the activations: permuted pair order, 528-byte padded units.  Each

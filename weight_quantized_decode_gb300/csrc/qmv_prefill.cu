@@ -11,26 +11,29 @@
 //
 //   * One CTA computes a 128-row (weights) x TN-column (tokens) tile of y^T in
 //     tensor memory: weights are the MMA's M side (128 lanes), tokens its N
-//     side (TN <= 256 columns of fp32; when 256-token tiles would need a
-//     second wave of CTAs, TN = 512 in two 256-column accumulators).
-//   * Roles by warp: a warp runs on scheduler (warp id mod 4).  Scheduler 1
-//     hosts only the MMA-issuing warp and the two copy producers, which sleep
-//     in mbarrier waits, so the single MMA-issuing thread is not starved of
-//     issue slots by the dequantising warps on schedulers 0, 2 and 3.
-//   * Warp 5 streams packed 128-row x 256-K Q4_0 tiles (144 bytes per row)
-//     and warp 9 streams 64-K activation tiles, both with TMA tensor copies,
-//     into their own shared-memory rings (deep enough to cover DRAM / L2
-//     latency); the activation tiles land in the 128-byte-swizzled K-major
-//     layout the tensor core reads.
-//   * Warps 0, 2, 3, 4, 6, 7, 8, 10 (two threads per weight row, one block
-//     each) dequantise into fp16 with the 0x6400|n bit trick,
-//     w = (c - 8) * d, and write 64-K slices of the A operand in the same
-//     swizzled layout.
-//   * Warp 1 allocates tensor memory and one thread issues tcgen05.mma
-//     (kind::f16, 128 x TN x 16) four times per 64-K atom; a ring slot holds
-//     one atom (TN = 256) or two (TN <= 128: eight MMAs per barrier round);
-//     tcgen05.commit releases the slot's A and B buffers and finally signals
-//     the epilogue.
+//     side (TN <= 256 columns of fp32).
+//   * The dequantised weights never touch shared memory: the dequantising
+//     warps write them straight into tensor memory (tcgen05.st), and the MMA
+//     reads its A operand from there.  Shared memory then carries only the
+//     packed weights and the activation tiles, so the tensor core's operand
+//     reads and the copies into shared memory no longer compete with a
+//     round trip of the dequantised tile (which had made the kernel bound by
+//     shared-memory bandwidth rather than by the tensor pipe).
+//   * Roles by warp: warps 0..7 dequantise (warp w writes tensor-memory lane
+//     quarter w mod 4 -- the only lanes its sub-partition can reach -- and
+//     blocks of parity w / 4); warp 8 allocates tensor memory and one of its
+//     threads issues the MMAs; warp 9 streams packed 128-row x 256-K Q4_0
+//     tiles (144 bytes per row) and warp 10 streams 64-K activation tiles, both
+//     with TMA tensor copies, into their own shared-memory rings (deep enough
+//     to cover DRAM / L2 latency); the activation tiles land in the
+//     128-byte-swizzled K-major layout the tensor core reads.
+//   * Dequantisation uses the fp16 0x6400|n bit trick, w = (c - 8) * d, one
+//     32-weight block per thread and atom, stored as 16 columns of half2.
+//   * One thread issues tcgen05.mma (kind::f16, 128 x TN x 16, A from tensor
+//     memory) four times per 64-K atom; a ring slot holds KSUB atoms (4, 2 or
+//     1 for 64-, 128- and wider token tiles); tcgen05.commit releases the
+//     slot's activation tile and weight atoms, and finally signals the
+//     epilogue.
 //   * All warps read the accumulator with tcgen05.ld (32 lanes x 32 columns
 //     per instruction; warp w reads lane quarter w mod 4, the warps of a
 //     quarter split the columns) and store y with coalesced fp32 stores.
@@ -57,18 +60,17 @@ namespace qmv {
 namespace {
 
 constexpr int kThreads = kPrefillThreads;   // 11 warps: 8 dequantising, MMA issue, 2 copy producers
-constexpr int kMmaWarp = 1, kWProducerWarp = 5, kXProducerWarp = 9;
-constexpr int kDeqThreads = 256;
+constexpr int kDeqWarps = 8;                // warps 0..7
+constexpr int kMmaWarp = 8, kWProducerWarp = 9, kXProducerWarp = 10;
 
 struct PrefillParams {
     float *y;
     int *status;
     int64_t N, K, M;
-    int TN;            // token columns per tile (multiple of 64, <= 512)
-    int NH;            // accumulators per tile: TN / NH <= 256 columns each (the MMA's N)
+    int TN;            // token columns per tile = the MMA's N (multiple of 64, <= 256)
     int NW;            // packed-weight ring slots (256-K tiles)
     int NS;            // slot ring depth: each slot holds KSUB dequantised-weight and activation atoms
-    int KSUB;          // 64-K atoms per slot (1 or 2): MMAs per barrier round = 4 * KSUB
+    int KSUB;          // 64-K atoms per slot (1, 2 or 4): MMAs per barrier round = 4 * KSUB
     uint32_t tmem_cols;
     int test_skip_copy;   // failure-detection test only: CTA (0, 0) never requests its first packed tile
     unsigned long long *phase;   // phase-timeline builds only (QMV_PHASE_STAMPS): [count, records...]
@@ -133,25 +135,41 @@ __host__ __device__ __forceinline__ uint32_t f16_idesc(int tn)
            | (static_cast<uint32_t>(kBM >> 4) << 24);  // M / 16
 }
 
-// Four K=16 steps over one 64-K slice: descriptors advance by 32 bytes (2 in
-// the 16-byte address field) per step.  `first` clears the accumulator.
-__device__ __forceinline__ void mma_f16_slice(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                              bool first)
+// Four K=16 steps over one 64-K atom with A in tensor memory: A advances by
+// 8 columns (16 fp16) and the B descriptor by 32 bytes (2 in its 16-byte
+// address field) per step.  `first` clears the accumulator.
+__device__ __forceinline__ void mma_f16_atom_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                                bool first)
 {
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
-        ".reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
-        "setp.eq.b32 p, %4, 0;\n\t"
+        ".reg .b32 a1, a2, a3;\n\t"
+        ".reg .b64 b1, b2, b3;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
         "setp.eq.b32 q, 0, 0;\n\t"
-        "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"
+        "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
         "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, q;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, q;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, q;\n\t}"
-        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(first ? 1 : 0)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, q;\n\t}"
+        ::"r"(tmem_d), "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(first ? 0 : 1)
         : "memory");
 }
+
+// 16 consecutive 32-bit tensor-memory columns of this thread's lane (the warp
+// writes its lane quarter: taddr carries the quarter's first lane).
+__device__ __forceinline__ void tmem_st_16cols(uint32_t taddr, const uint32_t (&v)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+          "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void mma_commit(uint64_t *bar)
 {
@@ -224,24 +242,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const PrefillParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    // 1024-byte alignment of the operand tiles (required by the 128-byte swizzle).
+    // 1024-byte alignment of the activation tiles (required by the 128-byte swizzle).
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-    const int NW = p.NW, NS = p.NS, TN = p.TN, KSUB = p.KSUB, NH = p.NH;
-    const int TNH = TN / NH;                                // MMA N: token columns per accumulator
-    const int b_atom_bytes = TN * kKB * 2;                  // one 64-K activation atom (all NH halves)
-    const int b_half_bytes = TNH * kKB * 2;
-    const int a_slot_bytes = KSUB * kATileBytes;
+    const int NW = p.NW, NS = p.NS, TN = p.TN, KSUB = p.KSUB;
+    const int b_atom_bytes = TN * kKB * 2;                  // one 64-K activation atom
     const int b_slot_bytes = KSUB * b_atom_bytes;
-    uint8_t *a_tiles = smem;
-    uint8_t *b_tiles = a_tiles + NS * a_slot_bytes;
+    uint8_t *b_tiles = smem;
     uint8_t *w_tiles = b_tiles + NS * b_slot_bytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(w_tiles + NW * kPackedTileBytes);
     uint64_t *wfull = bars;             // [NW]
     uint64_t *wempty = wfull + NW;      // [NW]
-    uint64_t *afull = wempty + NW;      // [NS] dequantised slice written
-    uint64_t *bfull = afull + NS;       // [NS] activation slice landed
-    uint64_t *sempty = bfull + NS;      // [NS] the slice's MMAs are done: both tiles free
+    uint64_t *afull = wempty + NW;      // [NS] dequantised atoms written to tensor memory
+    uint64_t *bfull = afull + NS;       // [NS] activation atoms landed
+    uint64_t *sempty = bfull + NS;      // [NS] the slot's MMAs are done: both operands free
     uint64_t *accfull = sempty + NS;    // [1]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accfull + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -256,7 +270,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t m0 = static_cast<int64_t>(blockIdx.y) * TN;
     const int nK = static_cast<int>(p.K / (kKB * KSUB));   // slots of KSUB x 64 K
     const int nC = static_cast<int>(p.K / kKChunk);        // packed 256-K tiles
-    constexpr int kDeqWarps = kDeqThreads / 32;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NW; ++i) {
@@ -277,6 +290,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Columns [0, TN) hold the accumulator; the dequantised weight atoms of
+    // ring slot s follow at TN + (s * KSUB + atom) * 32.
+    const uint32_t tmem_a0 = tmem_base + static_cast<uint32_t>(TN);
 #ifdef QMV_PHASE_STAMPS
     if (threadIdx.x == 0) phs[1] = global_timer_ns();
 #endif
@@ -317,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_wait_bounded(&wfull[c % NW], (c / NW) & 1, nullptr);
         }
     } else if (warp == kXProducerWarp) {
-        // ---------------- activations: TMA tensor copies, one per slice slot ----------------
+        // ---------------- activations: TMA tensor copies, one per atom ----------------
         if (lane == 0) {
             pdl_wait_prior_grid();
             int issued = 0, s = 0;
@@ -329,9 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mbar_arrive_expect_tx(&bfull[s], b_slot_bytes);
                 for (int a = 0; a < KSUB; ++a)
-                    for (int h = 0; h < NH; ++h)
-                        tma_load_2d(b_tiles + s * b_slot_bytes + a * b_atom_bytes + h * b_half_bytes, &xmap,
-                                    (j * KSUB + a) * kKB, static_cast<int>(m0) + h * TNH, &bfull[s]);
+                    tma_load_2d(b_tiles + s * b_slot_bytes + a * b_atom_bytes, &xmap, (j * KSUB + a) * kKB,
+                                static_cast<int>(m0), &bfull[s]);
                 ++issued;
                 if (++s == NS) {
                     s = 0;
@@ -345,16 +360,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issue: one thread ----------------
         if (lane == 0) {
-            const uint32_t idesc = f16_idesc(TNH);
-            // Descriptors of slot 0; a slot (or a 16-wide K step: 32 bytes = 2
-            // in the 16-byte address field) is a plain addition.
-            const uint64_t a_desc0 = sw128_desc(smem_u32(a_tiles));
+            const uint32_t idesc = f16_idesc(TN);
+            // Descriptor of slot 0's first activation atom; a slot (or a 16-wide
+            // K step: 32 bytes = 2 in the 16-byte address field) is a plain addition.
             const uint64_t b_desc0 = sw128_desc(smem_u32(b_tiles));
-            const uint64_t a_step = static_cast<uint64_t>(a_slot_bytes) >> 4;
             const uint64_t b_step = static_cast<uint64_t>(b_slot_bytes) >> 4;
+            const uint64_t b_atom_step = static_cast<uint64_t>(b_atom_bytes) >> 4;
+            const uint32_t a_slot_cols = static_cast<uint32_t>(KSUB * kAtomCols);
             int committed = 0, s = 0;
             uint32_t ph = 0;
-            uint64_t a_desc = a_desc0, b_desc = b_desc0;
+            uint64_t b_desc = b_desc0;
+            uint32_t a_tmem = tmem_a0;
             for (int j = 0; j < nK; ++j) {
                 if (!wait_or_abort(&bfull[s], ph, abort_flag, p.status) ||
                     !wait_or_abort(&afull[s], ph, abort_flag, p.status)) {
@@ -362,7 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 // Order the MMAs after the barrier waits (the tcgen05 ops are
-                // asynchronous to this thread).
+                // asynchronous to this thread) and after the weight atoms'
+                // tensor-memory stores the barrier published.
                 tc_fence_after();
 #ifdef QMV_PHASE_STAMPS
                 if (j == 0) {
@@ -370,28 +387,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     phs[5] = clock64();
                 }
 #endif
-                if (NH == 1) {
-                    mma_f16_slice(tmem_base, a_desc, b_desc, idesc, j == 0);
-                    if (KSUB == 2)
-                        mma_f16_slice(tmem_base, a_desc + (kATileBytes >> 4),
-                                      b_desc + (static_cast<uint64_t>(b_atom_bytes) >> 4), idesc, false);
-                } else {
-                    // Accumulator h (TMEM columns h * TNH ..) takes token half h;
-                    // 512-token tiles hold one atom per slot.
-                    for (int h = 0; h < NH; ++h)
-                        mma_f16_slice(tmem_base + h * TNH, a_desc,
-                                      b_desc + (static_cast<uint64_t>(h * b_half_bytes) >> 4), idesc, j == 0);
-                }
+                for (int a = 0; a < KSUB; ++a)
+                    mma_f16_atom_ts(tmem_base, a_tmem + a * kAtomCols, b_desc + a * b_atom_step, idesc,
+                                    j == 0 && a == 0);
                 mma_commit(&sempty[s]);
                 ++committed;
                 if (++s == NS) {
                     s = 0;
                     ph ^= 1u;
-                    a_desc = a_desc0;
                     b_desc = b_desc0;
+                    a_tmem = tmem_a0;
                 } else {
-                    a_desc += a_step;
                     b_desc += b_step;
+                    a_tmem += a_slot_cols;
                 }
             }
             mma_commit(accfull);
@@ -402,13 +410,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok && committed > 0) mbar_wait_bounded(accfull, 0, nullptr);
         }
     } else {
-        // ---------------- dequantising warps ----------------
-        // warps 0, 2, 3, 4, 6, 7, 8, 10 -> dequantiser index 0..7
-        const int dw = warp - (warp >= 1) - (warp >= 5) - (warp >= 9);
-        const int dt = dw * 32 + lane;
-        const int r = dt & (kBM - 1);              // weight row within the tile
-        const int hsel = dt >> 7;                  // 0: even blocks of a slice, 1: odd blocks
-        int slot = 0, sa = 0;
+        // ---------------- dequantising warps 0..7 ----------------
+        // Warp w writes lanes 32 * (w mod 4) .. + 31 (weight rows) of tensor
+        // memory, the even (w < 4) or odd (w >= 4) block of each 64-K atom.
+        const int quarter = warp & 3;
+        const int hsel = warp >> 2;
+        const int r = 32 * quarter + lane;         // weight row within the tile
+        const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
+        int slot = 0, sa = 0, atom = 0;
         uint32_t wpar = 0, apar = 1;
         for (int c = 0; ok && c < nC; ++c) {
             if (lane == 0) ok = wait_or_abort(&wfull[slot], wpar, abort_flag, p.status);
@@ -429,8 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Hand the slot back only once this thread's reads of it are done:
             // the words are consumed into a register, and fence.proxy.async
             // orders the reads (generic proxy) before the producer's next
-            // copy into the slot (async proxy).  Without both, the next tile
-            // could land under a load still in flight.
+            // copy into the slot (async proxy).
             {
                 uint32_t all = 0;
 #pragma unroll
@@ -446,13 +454,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 #pragma unroll
             for (int sub = 0; sub < 4; ++sub) {
-                const int atom = sub & (KSUB - 1);      // atom within the slot
                 if (atom == 0) {
+                    // the slot's previous atoms have been read by their MMAs
                     if (lane == 0) ok = wait_or_abort(&sempty[sa], apar, abort_flag, p.status);
                     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                     if (!ok) break;
                     while (!mbar_try_wait_sleep(&sempty[sa], apar, kSuspendHintNs)) {
                     }
+                    tc_fence_after();
                 }
                 // block 2*sub + hsel: even blocks start 2 bytes into word 9*sub
                 const int h = 9 * sub;
@@ -467,15 +476,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dbits = w[h + 4] >> 16;
                 }
                 dequant_block_f16(dbits, q, f);
-                uint8_t *arow = a_tiles + sa * a_slot_bytes + atom * kATileBytes + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    const int cc = 4 * hsel + ch;    // 16-byte chunk within the 128-byte row
-                    *reinterpret_cast<uint4 *>(arow + ((cc ^ (r & 7)) << 4)) =
-                        make_uint4(f[4 * ch], f[4 * ch + 1], f[4 * ch + 2], f[4 * ch + 3]);
-                }
-                if (atom == KSUB - 1) {
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                // elements 2j, 2j+1 of the block -> column 16 * hsel + j of the atom
+                tmem_st_16cols(tmem_a0 + lane_base +
+                                   static_cast<uint32_t>((sa * KSUB + atom) * kAtomCols + 16 * hsel),
+                               f);
+                if (++atom == KSUB) {
+                    atom = 0;
+                    tmem_st_wait();
+                    tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&afull[sa]);
                     if (++sa == NS) {
@@ -614,7 +622,7 @@ cudaError_t launch_prefill(const PrefillPlan &pl, const void *W, const void *x, 
     {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K * 2)};
-        const cuuint32_t box[2] = {kKB, static_cast<cuuint32_t>(pl.TN / pl.NH)};
+        const cuuint32_t box[2] = {kKB, static_cast<cuuint32_t>(pl.TN)};
         const cuuint32_t estr[2] = {1, 1};
         if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(x), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -628,7 +636,6 @@ cudaError_t launch_prefill(const PrefillPlan &pl, const void *W, const void *x, 
     p.K = K;
     p.M = M;
     p.TN = pl.TN;
-    p.NH = pl.NH;
     p.NW = pl.NW;
     p.NS = pl.NS;
     p.KSUB = pl.KSUB;
