@@ -196,9 +196,9 @@ void check_swiglu(int64_t N, int64_t K, int M)
 // column of every weight atom written exactly once, by a warp whose lane
 // quarter holds it), the MMAs' operand addresses, and the epilogue's coverage
 // of every (lane quarter, column chunk) of the accumulator.
-void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int ns_force)
+void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int ns_force, int cl_force)
 {
-    const PrefillPlan pl = plan_prefill(N, K, M, sms, nw_force, ns_force);
+    const PrefillPlan pl = plan_prefill(N, K, M, sms, nw_force, ns_force, cl_force);
     const bool shape_ok = K % kKChunk == 0 && K > 0 && N > 0 && M > 0 && N < (int64_t(1) << 31) &&
                           M < (int64_t(1) << 31) && K < (int64_t(1) << 30);
     if (!pl.ok) {
@@ -219,7 +219,10 @@ void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int n
     const int64_t a_end = TN + static_cast<int64_t>(NS) * KSUB * kAtomCols;
     CHECK(a_end <= cols, "TMEM columns %lld > %u", (long long)a_end, cols);
     CHECK(pl.grid_x >= 1 && pl.grid_x <= INT32_MAX && pl.grid_y >= 1 && pl.grid_y <= kMaxGridY, "grid");
-    CHECK(pl.grid_x * kBM >= N && (pl.grid_x - 1) * kBM < N, "row tiles");
+    const int CL = pl.cluster;
+    CHECK(CL == 1 || CL == 2, "cluster %d", CL);
+    CHECK(pl.grid_x % CL == 0, "grid x %lld not a multiple of the cluster", (long long)pl.grid_x);
+    CHECK(pl.grid_x * kBM >= N && (pl.grid_x - CL) * kBM < N, "row tiles");
     CHECK(pl.grid_y * TN >= M && (pl.grid_y - 1) * TN < M, "token tiles");
     const int64_t nK = K / (kKB * KSUB), nC = K / kKChunk;
     CHECK(nK * KSUB * kKB == K && nC * 4 == nK * KSUB && nK < INT32_MAX, "K loop");
@@ -229,17 +232,24 @@ void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int n
     const size_t b_slot = KSUB * b_atom;
     const size_t w_off = NS * b_slot;
     const size_t bar_off = w_off + static_cast<size_t>(NW) * kPackedTileBytes;
-    const size_t bar_end = bar_off + static_cast<size_t>(2 * NW + 3 * NS + 1) * 8 + 4 + 4;
+    const size_t bar_end = bar_off + static_cast<size_t>(2 * NW + 4 * NS + 1) * 8 + 4 + 4;
     CHECK(1023 + bar_end <= pl.smem, "layout %zu + slack > %zu", bar_end, pl.smem);
     CHECK((bar_off + 1024) >> 4 < (size_t(1) << 14), "descriptor address field");
     for (int s = 0; s < NS; ++s)
-        for (int a = 0; a < KSUB; ++a) CHECK((s * b_slot + a * b_atom) % 1024 == 0, "B tile alignment");
+        for (int a = 0; a < KSUB; ++a)
+            for (int r = 0; r < CL; ++r) {
+                // each cluster CTA's share of the token rows lands at its own 1024-byte-aligned offset
+                const size_t off = s * b_slot + a * b_atom + static_cast<size_t>(r) * (TN / CL) * 128;
+                CHECK(off % 1024 == 0 && off + static_cast<size_t>(TN / CL) * 128 <= s * b_slot + (a + 1) * b_atom,
+                      "B tile share alignment");
+            }
     for (int w = 0; w < NW; ++w) CHECK((w_off + static_cast<size_t>(w) * kPackedTileBytes) % 128 == 0, "W slot");
 
     // tensor-copy boxes: within the box limits; bytes landed = the barrier's expected count
-    CHECK(kPackedRowBytes <= 256 && kBM <= 256 && TN <= 256 && kKB * 2 <= 128, "boxes");
+    CHECK(kPackedRowBytes <= 256 && kBM <= 256 && TN / CL <= 256 && TN % CL == 0 && kKB * 2 <= 128, "boxes");
     CHECK(static_cast<size_t>(kPackedRowBytes) * kBM == static_cast<size_t>(kPackedTileBytes), "W box bytes");
-    CHECK(static_cast<size_t>(KSUB) * kKB * TN * 2 == b_slot, "x box bytes");
+    // the slot's barrier expects the bytes of every CTA's multicast share
+    CHECK(static_cast<size_t>(KSUB) * CL * kKB * (TN / CL) * 2 == b_slot, "x box bytes");
     // coordinates: innermost x times the element size on 16 bytes and inside the row
     const int64_t row_bytes = (K / 32) * 18;
     for (int64_t c = 0; c < nC; c += (c < 4 || c + 4 >= nC) ? 1 : std::max<int64_t>(1, nC / 64)) {
@@ -251,11 +261,12 @@ void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int n
             const int64_t x = (j * KSUB + a) * kKB;
             CHECK((x * 2) % 16 == 0 && x + kKB <= K, "x x %lld", (long long)x);
         }
-    for (int64_t by = 0; by < pl.grid_y; ++by) {
-        const int64_t yc = by * TN;   // rows past M read the fill value
-        CHECK(yc >= 0 && yc + TN <= INT32_MAX, "x y %lld", (long long)yc);
-    }
-    CHECK((pl.grid_x - 1) * kBM < N && (pl.grid_x - 1) * kBM <= INT32_MAX, "W y");
+    for (int64_t by = 0; by < pl.grid_y; ++by)
+        for (int r = 0; r < CL; ++r) {
+            const int64_t yc = by * TN + static_cast<int64_t>(r) * (TN / CL);   // rows past M read the fill value
+            CHECK(yc >= 0 && yc + TN / CL <= INT32_MAX, "x y %lld", (long long)yc);
+        }
+    CHECK((pl.grid_x - 1) * kBM <= INT32_MAX, "W y");
 
     // dequantising warps 0..7: reads of the packed slot; tensor-memory writes
     static unsigned char cover[kBM][kAtomCols];
@@ -342,7 +353,8 @@ int main()
             for (int64_t M : pM)
                 for (int sms : {152, 148, 132, 1})
                     for (int nw : {0, 1, 2, 3, 5, 8})
-                        for (int ns : {0, 2, 3, 4, 6}) check_prefill(N, K, M, sms, nw, ns);
+                        for (int ns : {0, 2, 3, 4, 6})
+                            for (int cl : {0, 1, 2}) check_prefill(N, K, M, sms, nw, ns, cl);
     std::printf("checked %ld plans, %ld failures\n", g_checked, g_bad);
     return g_bad ? 1 : 0;
 }

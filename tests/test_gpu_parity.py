@@ -478,6 +478,12 @@ PREFILL_RINGS = {
     "2,2": ["pfrep:q4_0:12288:2560:512", "pfrep:q4_0:4096:2560:256", "pfrep:q4_0:2048:2560:64"],
     # one packed-weight slot, the deepest operand ring that then fits
     "1,4": ["pfrep:q4_0:12288:2560:512", "pfrep:q4_0:4096:2560:256", "pfrep:q4_0:2048:2560:64"],
+    # no cluster: each CTA loads whole activation tiles itself (the rule's choice)
+    "0,0,1": ["pfrep:q4_0:12288:2560:512", "pfrep:q4_0:4096:2560:256", "pfrep:q4_0:2048:2560:64",
+              "pfrep:q4_0:384:512:100"],
+    # CTA pairs sharing each activation tile by multicast, also with an odd tile
+    # count (one CTA of the last pair lies past N)
+    "0,0,2": ["pfrep:q4_0:384:512:100", "pfrep:q4_0:130:256:70", "pfrep:q4_0:8192:2048:64"],
 }
 
 

@@ -661,8 +661,7 @@ __global__ void __launch_bounds__(MAXT, 1) qmv_stream_kernel(const GemvParams p)
     // 4-byte loads (pairs of consecutive activations) and four PRMTs.  The
     // (token, chunk) items of all the CTA's tokens are dealt out together, up
     // to kStageItems per thread per round with all their loads in flight, so
-    // several tokens cost few L2 round trips (one token of a plain call keeps
-    // two items per round: fewer registers live ahead of the main loop).
+    // long rows and several tokens cost few L2 round trips.
     if (XQ8 && p.xq) {
         // Activations already in Q8_1: copy the codes (16 per load) and the
         // blocks' (scale, 8 * code sum) into the staged layout.
@@ -747,7 +746,7 @@ __global__ void __launch_bounds__(MAXT, 1) qmv_stream_kernel(const GemvParams p)
         }
     } else {
         constexpr bool kOneToken = (M == 1 && !MOE);
-        constexpr int kStageItems = kOneToken ? 2 : 4;
+        constexpr int kStageItems = 4;
         const int ntok = (prob_hi - prob_lo + 1) * M;
         const int chunks = static_cast<int>(p.K / 8);          // 16-byte chunks per token (4 per block)
         const int items = ntok * chunks;

@@ -63,4 +63,33 @@ cudaError_t launch_ex(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStr
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// launch_ex with thread-block clusters of `cluster` CTAs along x (1 = none).
+template <typename Kernel, typename... Args>
+cudaError_t launch_ex_cluster(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                              int cluster, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace qmv

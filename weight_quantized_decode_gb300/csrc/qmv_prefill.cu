@@ -71,6 +71,7 @@ struct PrefillParams {
     int NW;            // packed-weight ring slots (256-K tiles)
     int NS;            // slot ring depth: each slot holds KSUB dequantised-weight and activation atoms
     int KSUB;          // 64-K atoms per slot (1, 2 or 4): MMAs per barrier round = 4 * KSUB
+    int cluster;       // CTAs per cluster sharing each activation tile by multicast (1 or 2)
     uint32_t tmem_cols;
     int test_skip_copy;   // failure-detection test only: CTA (0, 0) never requests its first packed tile
     unsigned long long *phase;   // phase-timeline builds only (QMV_PHASE_STAMPS): [count, records...]
@@ -84,6 +85,17 @@ struct PrefillParams {
 // first MMA and the last commit.
 constexpr int kPrefillPhaseWords = 8;
 constexpr int kPrefillPhaseCap = 1 << 16;
+constexpr int kTraceSlotsDev = 128;
+__device__ unsigned long long g_prefill_trace_dev[kTraceSlotsDev * 6];
+#define QMV_TRACE(j, k)                                                                                     \
+    do {                                                                                                  \
+        if (blockIdx.x == 0 && blockIdx.y == 0 && (j) < kTraceSlotsDev)                                   \
+            g_prefill_trace_dev[(j) * 6 + (k)] = global_timer_ns();                                       \
+    } while (0)
+#else
+#define QMV_TRACE(j, k) \
+    do {                \
+    } while (0)
 #endif
 
 // ---- tcgen05 / TMA wrappers -------------------------------------------------------
@@ -94,6 +106,31 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
         ::"r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
+}
+
+// tma_load_2d delivered to every CTA of `mask` in the cluster, at the same
+// shared-memory offsets (destination and barrier) in each.
+__device__ __forceinline__ void tma_load_2d_mc(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar,
+                                               uint16_t mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols)
@@ -177,6 +214,16 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar)
                  : "memory");
 }
 
+// Arrive on the barrier at this offset in every CTA of `mask` once the MMAs
+// issued so far are complete.
+__device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+        ::"r"(smem_u32(bar)), "h"(mask)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&v)[32])
 {
     asm volatile(
@@ -246,6 +293,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
     const int NW = p.NW, NS = p.NS, TN = p.TN, KSUB = p.KSUB;
+    const int CL = p.cluster;
+    const uint32_t crank = CL > 1 ? cluster_rank() : 0u;
+    const uint16_t cmask = static_cast<uint16_t>((1u << CL) - 1u);
     const int b_atom_bytes = TN * kKB * 2;                  // one 64-K activation atom
     const int b_slot_bytes = KSUB * b_atom_bytes;
     uint8_t *b_tiles = smem;
@@ -255,8 +305,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *wempty = wfull + NW;      // [NW]
     uint64_t *afull = wempty + NW;      // [NS] dequantised atoms written to tensor memory
     uint64_t *bfull = afull + NS;       // [NS] activation atoms landed
-    uint64_t *sempty = bfull + NS;      // [NS] the slot's MMAs are done: both operands free
-    uint64_t *accfull = sempty + NS;    // [1]
+    uint64_t *sempty = bfull + NS;      // [NS] the slot's MMAs are done: its weight atoms are free
+    uint64_t *bempty = sempty + NS;     // [NS] every cluster CTA's MMAs of the slot are done: its
+                                        //      activation tile may be refilled in all of them
+    uint64_t *accfull = bempty + NS;    // [1]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accfull + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -280,6 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&afull[i], kDeqWarps);
             mbar_init(&bfull[i], 1);
             mbar_init(&sempty[i], 1);
+            mbar_init(&bempty[i], CL);
         }
         mbar_init(accfull, 1);
         *abort_flag = 0;
@@ -287,7 +340,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == kMmaWarp) tmem_alloc(tmem_slot, p.tmem_cols);
     tc_fence_before();
-    __syncthreads();
+    // The peer CTAs' barriers are initialised before any multicast copy or
+    // commit can reach them.
+    if (CL > 1)
+        cluster_sync();
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     // Columns [0, TN) hold the accumulator; the dequantised weight atoms of
@@ -334,19 +392,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kXProducerWarp) {
         // ---------------- activations: TMA tensor copies, one per atom ----------------
+        // With a cluster, this CTA loads rows [crank * TN / CL, ...) of every
+        // atom and multicasts them into the same offsets of all the cluster's
+        // CTAs; a slot is refilled once every CTA's MMAs have released it.
         if (lane == 0) {
             pdl_wait_prior_grid();
+            const int rows = TN / CL;
+            const int row_off_bytes = static_cast<int>(crank) * rows * 128;
             int issued = 0, s = 0;
             uint32_t phase = 1;
             for (int j = 0; j < nK; ++j) {
-                if (!wait_or_abort(&sempty[s], phase, abort_flag, p.status)) {
+                if (!wait_or_abort(&bempty[s], phase, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 mbar_arrive_expect_tx(&bfull[s], b_slot_bytes);
-                for (int a = 0; a < KSUB; ++a)
-                    tma_load_2d(b_tiles + s * b_slot_bytes + a * b_atom_bytes, &xmap, (j * KSUB + a) * kKB,
-                                static_cast<int>(m0), &bfull[s]);
+                for (int a = 0; a < KSUB; ++a) {
+                    uint8_t *dst = b_tiles + s * b_slot_bytes + a * b_atom_bytes + row_off_bytes;
+                    if (CL > 1)
+                        tma_load_2d_mc(dst, &xmap, (j * KSUB + a) * kKB, static_cast<int>(m0) + static_cast<int>(crank) * rows,
+                                       &bfull[s], cmask);
+                    else
+                        tma_load_2d(dst, &xmap, (j * KSUB + a) * kKB, static_cast<int>(m0), &bfull[s]);
+                }
+                QMV_TRACE(j, 0);
                 ++issued;
                 if (++s == NS) {
                     s = 0;
@@ -372,11 +441,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint64_t b_desc = b_desc0;
             uint32_t a_tmem = tmem_a0;
             for (int j = 0; j < nK; ++j) {
-                if (!wait_or_abort(&bfull[s], ph, abort_flag, p.status) ||
-                    !wait_or_abort(&afull[s], ph, abort_flag, p.status)) {
+                if (!wait_or_abort(&bfull[s], ph, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
+                QMV_TRACE(j, 1);
+                if (!wait_or_abort(&afull[s], ph, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                QMV_TRACE(j, 2);
                 // Order the MMAs after the barrier waits (the tcgen05 ops are
                 // asynchronous to this thread) and after the weight atoms'
                 // tensor-memory stores the barrier published.
@@ -391,6 +465,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_f16_atom_ts(tmem_base, a_tmem + a * kAtomCols, b_desc + a * b_atom_step, idesc,
                                     j == 0 && a == 0);
                 mma_commit(&sempty[s]);
+                if (CL > 1)
+                    mma_commit_mc(&bempty[s], cmask);
+                else
+                    mma_commit(&bempty[s]);
+                QMV_TRACE(j, 3);
                 ++committed;
                 if (++s == NS) {
                     s = 0;
@@ -419,6 +498,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
         int slot = 0, sa = 0, atom = 0;
         uint32_t wpar = 0, apar = 1;
+#ifdef QMV_PHASE_STAMPS
+        int jd = 0;   // ring rounds published (trace only)
+#endif
         for (int c = 0; ok && c < nC; ++c) {
             if (lane == 0) ok = wait_or_abort(&wfull[slot], wpar, abort_flag, p.status);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -462,6 +544,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     while (!mbar_try_wait_sleep(&sempty[sa], apar, kSuspendHintNs)) {
                     }
                     tc_fence_after();
+#ifdef QMV_PHASE_STAMPS
+                    if (warp == 0 && lane == 0) QMV_TRACE(jd, 4);
+#endif
                 }
                 // block 2*sub + hsel: even blocks start 2 bytes into word 9*sub
                 const int h = 9 * sub;
@@ -486,6 +571,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&afull[sa]);
+#ifdef QMV_PHASE_STAMPS
+                    if (warp == 0 && lane == 0) QMV_TRACE(jd, 5);
+                    ++jd;
+#endif
                     if (++sa == NS) {
                         sa = 0;
                         apar ^= 1u;
@@ -531,6 +620,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem_base, p.tmem_cols);
     }
+    // No CTA leaves while a peer may still multicast into its shared memory or
+    // arrive on its barriers.
+    if (CL > 1) cluster_sync();
 #ifdef QMV_PHASE_STAMPS
     if (threadIdx.x == 0 && p.phase) {
         const unsigned long long i = atomicAdd(p.phase, 1ull);
@@ -553,6 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 #ifdef QMV_PHASE_STAMPS
 __device__ unsigned long long g_prefill_phase[1 + static_cast<size_t>(kPrefillPhaseWords) * kPrefillPhaseCap];
+
 std::atomic<unsigned> g_prefill_phase_seq{0};
 #endif
 
@@ -575,29 +668,30 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// Ring depths forced for tests and sweeps: QMV_PREFILL_RING="NW,NS" (packed-
-// weight slots, operand slots; NW below 1 or NS below 2 keeps the rule).
+// Ring depths and cluster size forced for tests and sweeps:
+// QMV_PREFILL_RING="NW,NS[,CL]" (packed-weight slots, operand slots, CTAs per
+// cluster; NW below 1, NS below 2 or CL other than 1 or 2 keeps the rule).
 int ring_override(int which)
 {
-    static int nw = 0, ns = 0;
+    static int v[3] = {0, 0, 0};
     static std::once_flag once;
     std::call_once(once, [] {
         const char *e = std::getenv("QMV_PREFILL_RING");
         if (!e) return;
-        nw = std::atoi(e);
-        const char *c = std::strchr(e, ',');
-        if (c) ns = std::atoi(c + 1);
+        for (int i = 0; i < 3 && e; ++i) {
+            v[i] = std::atoi(e);
+            e = std::strchr(e, ',');
+            if (e) ++e;
+        }
     });
-    return which == 0 ? nw : ns;
+    return v[which];
 }
-int ring_override_nw() { return ring_override(0); }
-int ring_override_ns() { return ring_override(1); }
 
 }  // namespace
 
 PrefillPlan prefill_plan(int64_t N, int64_t K, int64_t M, int sms)
 {
-    PrefillPlan pl = plan_prefill(N, K, M, sms, ring_override_nw(), ring_override_ns());
+    PrefillPlan pl = plan_prefill(N, K, M, sms, ring_override(0), ring_override(1), ring_override(2));
     if (encode_fn() == nullptr) pl.ok = false;
     return pl;
 }
@@ -622,7 +716,7 @@ cudaError_t launch_prefill(const PrefillPlan &pl, const void *W, const void *x, 
     {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K * 2)};
-        const cuuint32_t box[2] = {kKB, static_cast<cuuint32_t>(pl.TN)};
+        const cuuint32_t box[2] = {kKB, static_cast<cuuint32_t>(pl.TN / pl.cluster)};
         const cuuint32_t estr[2] = {1, 1};
         if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(x), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -639,6 +733,7 @@ cudaError_t launch_prefill(const PrefillPlan &pl, const void *W, const void *x, 
     p.NW = pl.NW;
     p.NS = pl.NS;
     p.KSUB = pl.KSUB;
+    p.cluster = pl.cluster;
     p.tmem_cols = pl.tmem_cols;
     p.test_skip_copy = test_skip_copy ? 1 : 0;
 #ifdef QMV_PHASE_STAMPS
@@ -652,7 +747,7 @@ cudaError_t launch_prefill(const PrefillPlan &pl, const void *W, const void *x, 
     cudaError_t e = ensure_smem_optin(reinterpret_cast<const void *>(prefill_kernel), pl.smem);
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>(pl.grid_x), static_cast<unsigned>(pl.grid_y));
-    return launch_ex(prefill_kernel, grid, dim3(kThreads), pl.smem, s, pdl, wmap, xmap, p);
+    return launch_ex_cluster(prefill_kernel, grid, dim3(kThreads), pl.smem, s, pdl, pl.cluster, wmap, xmap, p);
 }
 
 }  // namespace qmv
@@ -661,6 +756,17 @@ cudaError_t launch_prefill(const PrefillPlan &pl, const void *W, const void *x, 
 // Phase-timeline builds only (not declared in include/qmv.h): copies up to
 // max_records prefill records to host memory and resets them; returns the
 // count or -1 on a CUDA error.
+// The slot-level trace of CTA (0, 0) of the last prefill launch: 128 rounds x 6 stamps.
+extern "C" QMV_API int qmv_prefill_trace(unsigned long long *host)
+{
+    using namespace qmv;
+    if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+    return cudaMemcpyFromSymbol(host, g_prefill_trace_dev, sizeof(unsigned long long) * kTraceSlotsDev * 6) ==
+                   cudaSuccess
+               ? 0
+               : -1;
+}
+
 extern "C" QMV_API int64_t qmv_prefill_phase_stamps(unsigned long long *host, int64_t max_records)
 {
     using namespace qmv;
