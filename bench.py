@@ -189,26 +189,39 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def traffic_record(kernel_name):
-    """ncu DRAM traffic per launch for a kernel, if recorded for the current source."""
+def traffic_record(workload):
+    """ncu DRAM traffic per launch for a workload, if recorded for the current
+    sources of the kernels it runs."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     try:
-        rec = json.load(open(p)).get(kernel_name)
+        rec = json.load(open(p)).get(workload)
     except (ValueError, OSError):
         return None
-    if not rec or rec.get("source_sha") != source_sha():
+    family = "prefill" if WORKLOADS.get(workload, {}).get("kind") == "prefill" else "decode"
+    if not rec or rec.get("source_sha") != source_sha(family):
         return None
     return rec
 
 
-def source_sha():
+PREFILL_SOURCES = ("qmv_prefill.cu", "qmv_prefill.h", "qmv_prefill_plan.h", "qmv_common.cuh", "qmv_launch.h")
+
+
+def source_sha(family="decode"):
+    """Hash of the kernel sources a traffic record depends on: the prefill
+    kernel's files, or (decode) every other source of the library."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "weight_quantized_decode_gb300", "csrc")
     for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, fn), "rb").read())
+        if not fn.endswith((".cu", ".cuh", ".h")):
+            continue
+        if family == "prefill":
+            if fn not in PREFILL_SOURCES:
+                continue
+        elif fn in ("qmv_prefill.cu", "qmv_prefill_plan.h", "qmv_probe.cu"):
+            continue
+        h.update(open(os.path.join(csrc, fn), "rb").read())
     return h.hexdigest()[:16]
 
 
