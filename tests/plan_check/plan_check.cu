@@ -191,38 +191,43 @@ void check_swiglu(int64_t N, int64_t K, int M)
 
 // The tensor-core prefill kernel: tile and ring choices, the shared-memory
 // layout and its alignment, tensor-copy boxes and coordinates, tensor-memory
-// columns (accumulator and dequantised weight atoms), the dequantising
-// threads' reads of the packed slot and writes of tensor memory (each lane and
-// column of every weight atom written exactly once, by a warp whose lane
-// quarter holds it), the MMAs' operand addresses, and the epilogue's coverage
-// of every (lane quarter, column chunk) of the accumulator.
-void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int ns_force, int cl_force)
+// columns (WT accumulators and the dequantised weight atoms), the
+// dequantising threads' reads of the packed slot and writes of tensor memory
+// (each lane and column of every weight atom written exactly once, by a warp
+// whose lane quarter holds it), the MMAs' operand addresses, and the
+// epilogue's coverage of every (lane quarter, column chunk) of the
+// accumulators.
+void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int ns_force, int cl_force,
+                   int tn_force, int wt_force)
 {
-    const PrefillPlan pl = plan_prefill(N, K, M, sms, nw_force, ns_force, cl_force);
+    const PrefillPlan pl = plan_prefill(N, K, M, sms, nw_force, ns_force, cl_force, tn_force, wt_force);
     const bool shape_ok = K % kKChunk == 0 && K > 0 && N > 0 && M > 0 && N < (int64_t(1) << 31) &&
                           M < (int64_t(1) << 31) && K < (int64_t(1) << 30);
     if (!pl.ok) {
-        // a shape of the kernel's form is refused only where the grid would exceed gridDim.y
-        CHECK(!shape_ok || pl.grid_y > kMaxGridY, "prefill refused %lldx%lld M=%lld", (long long)N, (long long)K,
-              (long long)M);
+        // a shape of the kernel's form is refused only where the grid would exceed gridDim.y, or where a
+        // forced tile is not available
+        CHECK(!shape_ok || pl.grid_y > kMaxGridY || tn_force || wt_force, "prefill refused %lldx%lld M=%lld",
+              (long long)N, (long long)K, (long long)M);
         return;
     }
     ++g_checked;
     CHECK(shape_ok, "prefill took %lldx%lld M=%lld", (long long)N, (long long)K, (long long)M);
-    const int TN = pl.TN, KSUB = pl.KSUB, NW = pl.NW, NS = pl.NS;
+    const int TN = pl.TN, WT = pl.WT, KSUB = pl.KSUB, NW = pl.NW, NSA = pl.NSA, NSB = pl.NSB;
     CHECK(TN % 64 == 0 && TN >= 64 && TN <= 256, "TN %d", TN);                 // kind::f16, M = 128: N <= 256
-    CHECK(KSUB == 1 || KSUB == 2 || KSUB == 4, "KSUB %d", KSUB);              // a slot never straddles a W tile
-    CHECK(NW >= 1 && NS >= 2, "rings %d %d", NW, NS);
+    CHECK(WT == 1 || WT == 2, "WT %d", WT);
+    CHECK(KSUB == 1 || KSUB == 2 || KSUB == 4, "KSUB %d", KSUB);              // a slot never straddles a W chunk
+    CHECK(NW >= 1 && NSA >= 2 && NSB >= 2, "rings %d %d %d", NW, NSA, NSB);
     CHECK(pl.smem <= static_cast<size_t>(kOptin), "prefill smem %zu", pl.smem);
     const uint32_t cols = pl.tmem_cols;
     CHECK(cols == 512, "TMEM %u", cols);
-    const int64_t a_end = TN + static_cast<int64_t>(NS) * KSUB * kAtomCols;
+    const int64_t a_end = static_cast<int64_t>(WT) * TN + static_cast<int64_t>(NSA) * KSUB * WT * kAtomCols;
     CHECK(a_end <= cols, "TMEM columns %lld > %u", (long long)a_end, cols);
-    CHECK(pl.grid_x >= 1 && pl.grid_x <= INT32_MAX && pl.grid_y >= 1 && pl.grid_y <= kMaxGridY, "grid");
     const int CL = pl.cluster;
     CHECK(CL == 1 || CL == 2, "cluster %d", CL);
+    CHECK(pl.grid_x >= 1 && pl.grid_x <= INT32_MAX && pl.grid_y >= 1 && pl.grid_y <= kMaxGridY, "grid");
     CHECK(pl.grid_x % CL == 0, "grid x %lld not a multiple of the cluster", (long long)pl.grid_x);
-    CHECK(pl.grid_x * kBM >= N && (pl.grid_x - CL) * kBM < N, "row tiles");
+    const int64_t rows_per_cta = static_cast<int64_t>(kBM) * WT;
+    CHECK(pl.grid_x * rows_per_cta >= N && (pl.grid_x - CL) * rows_per_cta < N, "row tiles");
     CHECK(pl.grid_y * TN >= M && (pl.grid_y - 1) * TN < M, "token tiles");
     const int64_t nK = K / (kKB * KSUB), nC = K / kKChunk;
     CHECK(nK * KSUB * kKB == K && nC * 4 == nK * KSUB && nK < INT32_MAX, "K loop");
@@ -230,12 +235,13 @@ void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int n
     // shared memory, as offsets from the 1024-byte-aligned base
     const size_t b_atom = static_cast<size_t>(TN) * kKB * 2;
     const size_t b_slot = KSUB * b_atom;
-    const size_t w_off = NS * b_slot;
-    const size_t bar_off = w_off + static_cast<size_t>(NW) * kPackedTileBytes;
-    const size_t bar_end = bar_off + static_cast<size_t>(2 * NW + 4 * NS + 1) * 8 + 4 + 4;
+    const size_t w_slot = static_cast<size_t>(WT) * kPackedTileBytes;
+    const size_t w_off = NSB * b_slot;
+    const size_t bar_off = w_off + static_cast<size_t>(NW) * w_slot;
+    const size_t bar_end = bar_off + static_cast<size_t>(2 * NW + 2 * NSA + 2 * NSB + 1) * 8 + 4 + 4;
     CHECK(1023 + bar_end <= pl.smem, "layout %zu + slack > %zu", bar_end, pl.smem);
     CHECK((bar_off + 1024) >> 4 < (size_t(1) << 14), "descriptor address field");
-    for (int s = 0; s < NS; ++s)
+    for (int s = 0; s < NSB; ++s)
         for (int a = 0; a < KSUB; ++a)
             for (int r = 0; r < CL; ++r) {
                 // each cluster CTA's share of the token rows lands at its own 1024-byte-aligned offset
@@ -243,11 +249,14 @@ void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int n
                 CHECK(off % 1024 == 0 && off + static_cast<size_t>(TN / CL) * 128 <= s * b_slot + (a + 1) * b_atom,
                       "B tile share alignment");
             }
-    for (int w = 0; w < NW; ++w) CHECK((w_off + static_cast<size_t>(w) * kPackedTileBytes) % 128 == 0, "W slot");
+    for (int w = 0; w < NW; ++w)
+        for (int t = 0; t < WT; ++t)
+            CHECK((w_off + static_cast<size_t>(w) * w_slot + static_cast<size_t>(t) * kPackedTileBytes) % 128 == 0,
+                  "W slot");
 
     // tensor-copy boxes: within the box limits; bytes landed = the barrier's expected count
     CHECK(kPackedRowBytes <= 256 && kBM <= 256 && TN / CL <= 256 && TN % CL == 0 && kKB * 2 <= 128, "boxes");
-    CHECK(static_cast<size_t>(kPackedRowBytes) * kBM == static_cast<size_t>(kPackedTileBytes), "W box bytes");
+    CHECK(static_cast<size_t>(kPackedRowBytes) * kBM * WT == w_slot, "W box bytes");
     // the slot's barrier expects the bytes of every CTA's multicast share
     CHECK(static_cast<size_t>(KSUB) * CL * kKB * (TN / CL) * 2 == b_slot, "x box bytes");
     // coordinates: innermost x times the element size on 16 bytes and inside the row
@@ -266,48 +275,53 @@ void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int n
             const int64_t yc = by * TN + static_cast<int64_t>(r) * (TN / CL);   // rows past M read the fill value
             CHECK(yc >= 0 && yc + TN / CL <= INT32_MAX, "x y %lld", (long long)yc);
         }
-    CHECK((pl.grid_x - 1) * kBM <= INT32_MAX, "W y");
+    // W rows of the last CTA's tiles (rows past N read zeros)
+    CHECK((pl.grid_x - 1) * rows_per_cta + (WT - 1) * kBM <= INT32_MAX, "W y");
 
     // dequantising warps 0..7: reads of the packed slot; tensor-memory writes
     static unsigned char cover[kBM][kAtomCols];
-    for (int s = 0; s < NS; ++s)
-        for (int a = 0; a < KSUB; ++a) {
-            std::fill(&cover[0][0], &cover[0][0] + kBM * kAtomCols, 0);
-            for (int w = 0; w < 8; ++w) {
-                const int quarter = w & 3, hsel = w >> 2;
-                CHECK(w != 8 && w != 9 && w != 10, "dequantiser role");
-                for (int lane = 0; lane < 32; ++lane) {
-                    const int r = 32 * quarter + lane;
-                    CHECK(r / 32 == (w & 3), "lane quarter of warp %d", w);
-                    CHECK(static_cast<size_t>(NW - 1) * kPackedTileBytes + r * kPackedRowBytes + 16 * 8 + 16 <=
-                              static_cast<size_t>(NW) * kPackedTileBytes,
-                          "packed read");
-                    const int64_t c0 = TN + static_cast<int64_t>(s * KSUB + a) * kAtomCols + 16 * hsel;
-                    CHECK(c0 >= TN && c0 + 16 <= a_end, "A columns");
-                    for (int j = 0; j < 16; ++j) ++cover[r][16 * hsel + j];
+    for (int s = 0; s < NSA; ++s)
+        for (int a = 0; a < KSUB; ++a)
+            for (int t = 0; t < WT; ++t) {
+                std::fill(&cover[0][0], &cover[0][0] + kBM * kAtomCols, 0);
+                const int64_t base = static_cast<int64_t>(WT) * TN + static_cast<int64_t>((s * KSUB + a) * WT + t) * kAtomCols;
+                for (int w = 0; w < 8; ++w) {
+                    const int quarter = w & 3, hsel = w >> 2;
+                    for (int lane = 0; lane < 32; ++lane) {
+                        const int r = 32 * quarter + lane;
+                        CHECK(r / 32 == (w & 3), "lane quarter of warp %d", w);
+                        CHECK(static_cast<size_t>(NW - 1) * w_slot + static_cast<size_t>(t) * kPackedTileBytes +
+                                      r * kPackedRowBytes + 16 * 8 + 16 <=
+                                  static_cast<size_t>(NW) * w_slot,
+                              "packed read");
+                        const int64_t c0 = base + 16 * hsel;
+                        CHECK(c0 >= static_cast<int64_t>(WT) * TN && c0 + 16 <= a_end, "A columns");
+                        for (int j = 0; j < 16; ++j) ++cover[r][16 * hsel + j];
+                    }
                 }
+                for (int r = 0; r < kBM; ++r)
+                    for (int c = 0; c < kAtomCols; ++c)
+                        CHECK(cover[r][c] == 1, "A cell %d,%d written %d times", r, c, cover[r][c]);
+                // the MMAs of this atom read columns [base, base + 32) in four K = 16 steps of 8 columns
+                for (int k = 0; k < 4; ++k) CHECK(base + 8 * k + 8 <= a_end, "MMA A columns");
             }
-            for (int r = 0; r < kBM; ++r)
-                for (int c = 0; c < kAtomCols; ++c) CHECK(cover[r][c] == 1, "A cell %d,%d written %d times", r, c, cover[r][c]);
-            // the MMAs of this atom read columns [base, base + 32) in four K = 16 steps of 8 columns
-            const int64_t base = TN + static_cast<int64_t>(s * KSUB + a) * kAtomCols;
-            for (int k = 0; k < 4; ++k) CHECK(base + 8 * k + 8 <= a_end, "MMA A columns");
-        }
+    for (int t = 0; t < WT; ++t) CHECK(static_cast<int64_t>(t + 1) * TN <= a_end - static_cast<int64_t>(NSA) * KSUB * WT * kAtomCols, "accumulator %d", t);
     for (int sub = 0; sub < 4; ++sub) CHECK(4 * (9 * sub + 8) + 4 <= kPackedRowBytes, "block words");
 
-    // epilogue: each (lane quarter, 32-column chunk) read by exactly one warp, inside the accumulator
+    // epilogue: each (lane quarter, 32-column chunk) read by exactly one warp, inside the accumulators
     static unsigned char ecover[4][16];
     std::fill(&ecover[0][0], &ecover[0][0] + 64, 0);
     const int warps = kPrefillThreads / 32;
     for (int w = 0; w < warps; ++w) {
         const int quarter = w & 3, nq = (warps - quarter + 3) / 4, rank = w >> 2;
-        for (int c0 = 32 * rank; c0 < TN; c0 += 32 * nq) {
-            CHECK(c0 + 32 <= TN, "epilogue columns");
+        for (int c0 = 32 * rank; c0 < WT * TN; c0 += 32 * nq) {
+            CHECK(c0 + 32 <= WT * TN && (c0 % TN) + 32 <= TN, "epilogue columns");
             ++ecover[quarter][c0 / 32];
         }
     }
     for (int q = 0; q < 4; ++q)
-        for (int c = 0; c < TN / 32; ++c) CHECK(ecover[q][c] == 1, "epilogue chunk %d,%d read %d times", q, c, ecover[q][c]);
+        for (int c = 0; c < WT * TN / 32; ++c)
+            CHECK(ecover[q][c] == 1, "epilogue chunk %d,%d read %d times", q, c, ecover[q][c]);
 }
 
 }  // namespace
@@ -354,7 +368,14 @@ int main()
                 for (int sms : {152, 148, 132, 1})
                     for (int nw : {0, 1, 2, 3, 5, 8})
                         for (int ns : {0, 2, 3, 4, 6})
-                            for (int cl : {0, 1, 2}) check_prefill(N, K, M, sms, nw, ns, cl);
+                            for (int cl : {0, 1, 2}) check_prefill(N, K, M, sms, nw, ns, cl, 0, 0);
+    // every token tile and weight-tile count forced, over the same shapes
+    for (int64_t N : pN)
+        for (int64_t K : pK)
+            for (int64_t M : pM)
+                for (int tn : {64, 128, 192, 256})
+                    for (int wt : {1, 2})
+                        for (int cl : {1, 2}) check_prefill(N, K, M, 152, 0, 0, cl, tn, wt);
     std::printf("checked %ld plans, %ld failures\n", g_checked, g_bad);
     return g_bad ? 1 : 0;
 }

@@ -68,9 +68,11 @@ struct PrefillParams {
     int *status;
     int64_t N, K, M;
     int TN;            // token columns per tile = the MMA's N (multiple of 64, <= 256)
-    int NW;            // packed-weight ring slots (256-K tiles)
-    int NS;            // slot ring depth: each slot holds KSUB dequantised-weight and activation atoms
-    int KSUB;          // 64-K atoms per slot (1, 2 or 4): MMAs per barrier round = 4 * KSUB
+    int WT;            // 128-row weight tiles per CTA (1 or 2)
+    int NW;            // packed-weight ring slots (256-K chunks of WT tiles)
+    int NSA;           // weight-atom ring slots (tensor memory)
+    int NSB;           // activation ring slots (shared memory)
+    int KSUB;          // 64-K atoms per slot (1, 2 or 4): MMAs per barrier round = 4 * KSUB * WT
     int cluster;       // CTAs per cluster sharing each activation tile by multicast (1 or 2)
     uint32_t tmem_cols;
     int test_skip_copy;   // failure-detection test only: CTA (0, 0) never requests its first packed tile
@@ -284,6 +286,7 @@ __device__ __forceinline__ void dequant_block_f16(uint32_t dbits, const uint32_t
     }
 }
 
+template <int WT, int CL>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                    const PrefillParams p)
@@ -292,23 +295,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 1024-byte alignment of the activation tiles (required by the 128-byte swizzle).
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-    const int NW = p.NW, NS = p.NS, TN = p.TN, KSUB = p.KSUB;
-    const int CL = p.cluster;
-    const uint32_t crank = CL > 1 ? cluster_rank() : 0u;
+    const int NW = p.NW, NSA = p.NSA, NSB = p.NSB, TN = p.TN, KSUB = p.KSUB;
+    // Equal ring depths without a cluster: one set of release barriers
+    // (aempty) serves both rings, and a slot is released with one commit.
+    const bool one_ring = NSA == NSB && CL == 1;
+    uint32_t crank = 0u;
+    if constexpr (CL > 1) crank = cluster_rank();
     const uint16_t cmask = static_cast<uint16_t>((1u << CL) - 1u);
     const int b_atom_bytes = TN * kKB * 2;                  // one 64-K activation atom
     const int b_slot_bytes = KSUB * b_atom_bytes;
+    const int w_slot_bytes = WT * kPackedTileBytes;         // one 256-K chunk of the CTA's WT weight tiles
     uint8_t *b_tiles = smem;
-    uint8_t *w_tiles = b_tiles + NS * b_slot_bytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(w_tiles + NW * kPackedTileBytes);
+    uint8_t *w_tiles = b_tiles + NSB * b_slot_bytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(w_tiles + NW * w_slot_bytes);
     uint64_t *wfull = bars;             // [NW]
     uint64_t *wempty = wfull + NW;      // [NW]
-    uint64_t *afull = wempty + NW;      // [NS] dequantised atoms written to tensor memory
-    uint64_t *bfull = afull + NS;       // [NS] activation atoms landed
-    uint64_t *sempty = bfull + NS;      // [NS] the slot's MMAs are done: its weight atoms are free
-    uint64_t *bempty = sempty + NS;     // [NS] every cluster CTA's MMAs of the slot are done: its
-                                        //      activation tile may be refilled in all of them
-    uint64_t *accfull = bempty + NS;    // [1]
+    uint64_t *afull = wempty + NW;      // [NSA] dequantised atoms written to tensor memory
+    uint64_t *aempty = afull + NSA;     // [NSA] the slot's MMAs are done: its weight atoms are free
+    uint64_t *bfull = aempty + NSA;     // [NSB] activation atoms landed
+    uint64_t *bempty = bfull + NSB;     // [NSB] every cluster CTA's MMAs of the slot are done: its
+                                        //       activation tile may be refilled in all of them
+    uint64_t *accfull = bempty + NSB;   // [1]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accfull + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -318,20 +325,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ unsigned long long phs[7];   // entry, setup, first MMA, last commit, acc ready, clk0, clk1
     if (threadIdx.x == 0) phs[0] = global_timer_ns();
 #endif
-    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kBM;
+    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kBM * WT;
     const int64_t m0 = static_cast<int64_t>(blockIdx.y) * TN;
     const int nK = static_cast<int>(p.K / (kKB * KSUB));   // slots of KSUB x 64 K
-    const int nC = static_cast<int>(p.K / kKChunk);        // packed 256-K tiles
+    const int nC = static_cast<int>(p.K / kKChunk);        // packed 256-K chunks
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NW; ++i) {
             mbar_init(&wfull[i], 1);
             mbar_init(&wempty[i], kDeqWarps);
         }
-        for (int i = 0; i < NS; ++i) {
+        for (int i = 0; i < NSA; ++i) {
             mbar_init(&afull[i], kDeqWarps);
+            mbar_init(&aempty[i], 1);
+        }
+        for (int i = 0; i < NSB; ++i) {
             mbar_init(&bfull[i], 1);
-            mbar_init(&sempty[i], 1);
             mbar_init(&bempty[i], CL);
         }
         mbar_init(accfull, 1);
@@ -342,15 +351,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     // The peer CTAs' barriers are initialised before any multicast copy or
     // commit can reach them.
-    if (CL > 1)
+    if constexpr (CL > 1)
         cluster_sync();
     else
         __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    // Columns [0, TN) hold the accumulator; the dequantised weight atoms of
-    // ring slot s follow at TN + (s * KSUB + atom) * 32.
-    const uint32_t tmem_a0 = tmem_base + static_cast<uint32_t>(TN);
+    // Columns [t * TN, (t + 1) * TN) hold weight tile t's accumulator; weight
+    // atom (slot s, atom a, tile t) follows at WT * TN + ((s * KSUB + a) * WT + t) * 32.
+    const uint32_t tmem_a0 = tmem_base + static_cast<uint32_t>(WT * TN);
 #ifdef QMV_PHASE_STAMPS
     if (threadIdx.x == 0) phs[1] = global_timer_ns();
 #endif
@@ -374,12 +383,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(&wfull[slot], kPackedTileBytes);
-                // (test only) the first tile of CTA (0, 0) is expected but never
+                mbar_arrive_expect_tx(&wfull[slot], static_cast<uint32_t>(w_slot_bytes));
+                // (test only) the first chunk of CTA (0, 0) is expected but never
                 // requested, so the waits on it run out and the CTA aborts
                 if (!(p.test_skip_copy && c == 0 && blockIdx.x == 0 && blockIdx.y == 0))
-                    tma_load_2d(w_tiles + slot * kPackedTileBytes, &wmap, c * kPackedRowBytes,
-                                static_cast<int>(n0), &wfull[slot]);
+                    for (int t = 0; t < WT; ++t)   // rows past N read zeros
+                        tma_load_2d(w_tiles + slot * w_slot_bytes + t * kPackedTileBytes, &wmap, c * kPackedRowBytes,
+                                    static_cast<int>(n0) + t * kBM, &wfull[slot]);
                 ++issued;
                 if (++slot == NW) {
                     slot = 0;
@@ -402,51 +412,51 @@ __global__ void __launch_bounds__(kThreads, 1)
             int issued = 0, s = 0;
             uint32_t phase = 1;
             for (int j = 0; j < nK; ++j) {
-                if (!wait_or_abort(&bempty[s], phase, abort_flag, p.status)) {
+                if (!wait_or_abort(one_ring ? &aempty[s] : &bempty[s], phase, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 mbar_arrive_expect_tx(&bfull[s], b_slot_bytes);
                 for (int a = 0; a < KSUB; ++a) {
                     uint8_t *dst = b_tiles + s * b_slot_bytes + a * b_atom_bytes + row_off_bytes;
-                    if (CL > 1)
-                        tma_load_2d_mc(dst, &xmap, (j * KSUB + a) * kKB, static_cast<int>(m0) + static_cast<int>(crank) * rows,
-                                       &bfull[s], cmask);
+                    if constexpr (CL > 1)
+                        tma_load_2d_mc(dst, &xmap, (j * KSUB + a) * kKB,
+                                       static_cast<int>(m0) + static_cast<int>(crank) * rows, &bfull[s], cmask);
                     else
                         tma_load_2d(dst, &xmap, (j * KSUB + a) * kKB, static_cast<int>(m0), &bfull[s]);
                 }
                 QMV_TRACE(j, 0);
                 ++issued;
-                if (++s == NS) {
+                if (++s == NSB) {
                     s = 0;
                     phase ^= 1u;
                 }
             }
             if (!ok)
-                for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j)
-                    mbar_wait_bounded(&bfull[j % NS], (j / NS) & 1, nullptr);
+                for (int j = (issued > NSB ? issued - NSB : 0); j < issued; ++j)
+                    mbar_wait_bounded(&bfull[j % NSB], (j / NSB) & 1, nullptr);
         }
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issue: one thread ----------------
         if (lane == 0) {
             const uint32_t idesc = f16_idesc(TN);
-            // Descriptor of slot 0's first activation atom; a slot (or a 16-wide
+            // Descriptor of activation slot 0's first atom; a slot (or a 16-wide
             // K step: 32 bytes = 2 in the 16-byte address field) is a plain addition.
             const uint64_t b_desc0 = sw128_desc(smem_u32(b_tiles));
             const uint64_t b_step = static_cast<uint64_t>(b_slot_bytes) >> 4;
             const uint64_t b_atom_step = static_cast<uint64_t>(b_atom_bytes) >> 4;
-            const uint32_t a_slot_cols = static_cast<uint32_t>(KSUB * kAtomCols);
-            int committed = 0, s = 0;
-            uint32_t ph = 0;
+            const uint32_t a_slot_cols = static_cast<uint32_t>(KSUB * WT * kAtomCols);
+            int committed = 0, sa = 0, sb = 0;
+            uint32_t pha = 0, phb = 0;
             uint64_t b_desc = b_desc0;
             uint32_t a_tmem = tmem_a0;
             for (int j = 0; j < nK; ++j) {
-                if (!wait_or_abort(&bfull[s], ph, abort_flag, p.status)) {
+                if (!wait_or_abort(&bfull[sb], phb, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 QMV_TRACE(j, 1);
-                if (!wait_or_abort(&afull[s], ph, abort_flag, p.status)) {
+                if (!wait_or_abort(&afull[sa], pha, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
@@ -462,23 +472,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
 #endif
                 for (int a = 0; a < KSUB; ++a)
-                    mma_f16_atom_ts(tmem_base, a_tmem + a * kAtomCols, b_desc + a * b_atom_step, idesc,
-                                    j == 0 && a == 0);
-                mma_commit(&sempty[s]);
-                if (CL > 1)
-                    mma_commit_mc(&bempty[s], cmask);
-                else
-                    mma_commit(&bempty[s]);
+                    for (int t = 0; t < WT; ++t)
+                        mma_f16_atom_ts(tmem_base + static_cast<uint32_t>(t * TN),
+                                        a_tmem + static_cast<uint32_t>((a * WT + t) * kAtomCols),
+                                        b_desc + a * b_atom_step, idesc, j == 0 && a == 0);
+                mma_commit(&aempty[sa]);
+                if constexpr (CL > 1)
+                    mma_commit_mc(&bempty[sb], cmask);
+                else if (!one_ring)
+                    mma_commit(&bempty[sb]);
                 QMV_TRACE(j, 3);
                 ++committed;
-                if (++s == NS) {
-                    s = 0;
-                    ph ^= 1u;
-                    b_desc = b_desc0;
+                if (++sa == NSA) {
+                    sa = 0;
+                    pha ^= 1u;
                     a_tmem = tmem_a0;
                 } else {
-                    b_desc += b_step;
                     a_tmem += a_slot_cols;
+                }
+                if (++sb == NSB) {
+                    sb = 0;
+                    phb ^= 1u;
+                    b_desc = b_desc0;
+                } else {
+                    b_desc += b_step;
                 }
             }
             mma_commit(accfull);
@@ -490,11 +507,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------- dequantising warps 0..7 ----------------
-        // Warp w writes lanes 32 * (w mod 4) .. + 31 (weight rows) of tensor
-        // memory, the even (w < 4) or odd (w >= 4) block of each 64-K atom.
+        // Warp w writes lanes 32 * (w mod 4) .. + 31 (weight rows r of each of
+        // the WT tiles) of tensor memory, the even (w < 4) or odd (w >= 4)
+        // block of each 64-K atom.
         const int quarter = warp & 3;
         const int hsel = warp >> 2;
-        const int r = 32 * quarter + lane;         // weight row within the tile
+        const int r = 32 * quarter + lane;         // weight row within each tile
         const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
         int slot = 0, sa = 0, atom = 0;
         uint32_t wpar = 0, apar = 1;
@@ -507,15 +525,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             while (!mbar_try_wait_sleep(&wfull[slot], wpar, kSuspendHintNs)) {
             }
-            uint32_t w[36];
-            const uint8_t *src = w_tiles + slot * kPackedTileBytes + r * kPackedRowBytes;
+            // this thread's row of each weight tile: 36 words (a 256-K chunk)
+            uint32_t w[WT][36];
 #pragma unroll
-            for (int i = 0; i < 9; ++i) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(src + 16 * i);
-                w[4 * i] = v.x;
-                w[4 * i + 1] = v.y;
-                w[4 * i + 2] = v.z;
-                w[4 * i + 3] = v.w;
+            for (int t = 0; t < WT; ++t) {
+                const uint8_t *src = w_tiles + slot * w_slot_bytes + t * kPackedTileBytes + r * kPackedRowBytes;
+#pragma unroll
+                for (int i = 0; i < 9; ++i) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(src + 16 * i);
+                    w[t][4 * i] = v.x;
+                    w[t][4 * i + 1] = v.y;
+                    w[t][4 * i + 2] = v.z;
+                    w[t][4 * i + 3] = v.w;
+                }
             }
             // Hand the slot back only once this thread's reads of it are done:
             // the words are consumed into a register, and fence.proxy.async
@@ -524,7 +546,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             {
                 uint32_t all = 0;
 #pragma unroll
-                for (int i = 0; i < 36; ++i) all ^= w[i];
+                for (int t = 0; t < WT; ++t)
+#pragma unroll
+                    for (int i = 0; i < 36; ++i) all ^= w[t][i];
                 asm volatile("" ::"r"(all) : "memory");
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -538,10 +562,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int sub = 0; sub < 4; ++sub) {
                 if (atom == 0) {
                     // the slot's previous atoms have been read by their MMAs
-                    if (lane == 0) ok = wait_or_abort(&sempty[sa], apar, abort_flag, p.status);
+                    if (lane == 0) ok = wait_or_abort(&aempty[sa], apar, abort_flag, p.status);
                     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                     if (!ok) break;
-                    while (!mbar_try_wait_sleep(&sempty[sa], apar, kSuspendHintNs)) {
+                    while (!mbar_try_wait_sleep(&aempty[sa], apar, kSuspendHintNs)) {
                     }
                     tc_fence_after();
 #ifdef QMV_PHASE_STAMPS
@@ -550,21 +574,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // block 2*sub + hsel: even blocks start 2 bytes into word 9*sub
                 const int h = 9 * sub;
-                uint32_t q[4], f[16], dbits;
-                if (hsel == 0) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) q[i] = __byte_perm(w[h + i], w[h + i + 1], 0x5432);
-                    dbits = w[h] & 0xffffu;
-                } else {
+                for (int t = 0; t < WT; ++t) {
+                    uint32_t q[4], f[16], dbits;
+                    if (hsel == 0) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) q[i] = w[h + 5 + i];
-                    dbits = w[h + 4] >> 16;
+                        for (int i = 0; i < 4; ++i) q[i] = __byte_perm(w[t][h + i], w[t][h + i + 1], 0x5432);
+                        dbits = w[t][h] & 0xffffu;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) q[i] = w[t][h + 5 + i];
+                        dbits = w[t][h + 4] >> 16;
+                    }
+                    dequant_block_f16(dbits, q, f);
+                    // elements 2j, 2j+1 of the block -> column 16 * hsel + j of the atom
+                    tmem_st_16cols(tmem_a0 + lane_base +
+                                       static_cast<uint32_t>(((sa * KSUB + atom) * WT + t) * kAtomCols + 16 * hsel),
+                                   f);
                 }
-                dequant_block_f16(dbits, q, f);
-                // elements 2j, 2j+1 of the block -> column 16 * hsel + j of the atom
-                tmem_st_16cols(tmem_a0 + lane_base +
-                                   static_cast<uint32_t>((sa * KSUB + atom) * kAtomCols + 16 * hsel),
-                               f);
                 if (++atom == KSUB) {
                     atom = 0;
                     tmem_st_wait();
@@ -575,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (warp == 0 && lane == 0) QMV_TRACE(jd, 5);
                     ++jd;
 #endif
-                    if (++sa == NS) {
+                    if (++sa == NSA) {
                         sa = 0;
                         apar ^= 1u;
                     }
@@ -585,8 +612,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---------------- epilogue: every warp ----------------
-    // Warp w reads TMEM lane quarter w mod 4; the warps of a quarter take its
-    // 32-column chunks round-robin.  A role that gave up skips it.
+    // Warp w reads TMEM lane quarter w mod 4; the warps of a quarter take the
+    // 32-column chunks of the WT accumulators round-robin.  A role that gave
+    // up skips it.
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     if (lane == 0) ok = ok && wait_or_abort(accfull, 0, abort_flag, p.status);
     ok = __shfl_sync(0xffffffffu, (ok && !*abort_flag) ? 1 : 0, 0) != 0;
@@ -600,15 +628,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;
         const int nq = (kThreads / 32 - quarter + 3) / 4;   // warps in this quarter
         const int rank = warp >> 2;
-        const int64_t row = n0 + 32 * quarter + lane;
-        for (int c0 = 32 * rank; c0 < TN; c0 += 32 * nq) {
-            uint32_t v[32];
-            tmem_ld_32cols(tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) + c0, v);
-            if (row < p.N) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int64_t m = m0 + c0 + i;
-                    if (m < p.M) p.y[m * p.N + row] = __uint_as_float(v[i]);
+        for (int t = 0; t < WT; ++t) {
+            const int64_t row = n0 + t * kBM + 32 * quarter + lane;
+            for (int c0 = 32 * rank; c0 < TN; c0 += 32 * nq) {
+                uint32_t v[32];
+                tmem_ld_32cols(tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) + t * TN + c0, v);
+                if (row < p.N) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int64_t m = m0 + c0 + i;
+                        if (m < p.M) p.y[m * p.N + row] = __uint_as_float(v[i]);
+                    }
                 }
             }
         }
@@ -622,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // No CTA leaves while a peer may still multicast into its shared memory or
     // arrive on its barriers.
-    if (CL > 1) cluster_sync();
+    if constexpr (CL > 1) cluster_sync();
 #ifdef QMV_PHASE_STAMPS
     if (threadIdx.x == 0 && p.phase) {
         const unsigned long long i = atomicAdd(p.phase, 1ull);
@@ -668,17 +699,18 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// Ring depths and cluster size forced for tests and sweeps:
-// QMV_PREFILL_RING="NW,NS[,CL]" (packed-weight slots, operand slots, CTAs per
-// cluster; NW below 1, NS below 2 or CL other than 1 or 2 keeps the rule).
+// Ring depths, cluster size and tile forced for tests and sweeps:
+// QMV_PREFILL_RING="NW,NS[,CL[,TN[,WT]]]" (packed-weight slots, activation
+// slots, CTAs per cluster, token tile, weight tiles per CTA; NW below 1, NS
+// below 2, CL other than 1 or 2, TN or WT of 0 keep the rule).
 int ring_override(int which)
 {
-    static int v[3] = {0, 0, 0};
+    static int v[5] = {0, 0, 0, 0, 0};
     static std::once_flag once;
     std::call_once(once, [] {
         const char *e = std::getenv("QMV_PREFILL_RING");
         if (!e) return;
-        for (int i = 0; i < 3 && e; ++i) {
+        for (int i = 0; i < 5 && e; ++i) {
             v[i] = std::atoi(e);
             e = std::strchr(e, ',');
             if (e) ++e;
@@ -691,7 +723,8 @@ int ring_override(int which)
 
 PrefillPlan prefill_plan(int64_t N, int64_t K, int64_t M, int sms)
 {
-    PrefillPlan pl = plan_prefill(N, K, M, sms, ring_override(0), ring_override(1), ring_override(2));
+    PrefillPlan pl = plan_prefill(N, K, M, sms, ring_override(0), ring_override(1), ring_override(2),
+                                  ring_override(3), ring_override(4));
     if (encode_fn() == nullptr) pl.ok = false;
     return pl;
 }
@@ -730,8 +763,10 @@ cudaError_t launch_prefill(const PrefillPlan &pl, const void *W, const void *x, 
     p.K = K;
     p.M = M;
     p.TN = pl.TN;
+    p.WT = pl.WT;
     p.NW = pl.NW;
-    p.NS = pl.NS;
+    p.NSA = pl.NSA;
+    p.NSB = pl.NSB;
     p.KSUB = pl.KSUB;
     p.cluster = pl.cluster;
     p.tmem_cols = pl.tmem_cols;
@@ -744,10 +779,12 @@ cudaError_t launch_prefill(const PrefillPlan &pl, const void *W, const void *x, 
         p.phase_seq = g_prefill_phase_seq.fetch_add(1);
     }
 #endif
-    cudaError_t e = ensure_smem_optin(reinterpret_cast<const void *>(prefill_kernel), pl.smem);
+    auto kernel = pl.WT == 2 ? (pl.cluster > 1 ? prefill_kernel<2, 2> : prefill_kernel<2, 1>)
+                             : (pl.cluster > 1 ? prefill_kernel<1, 2> : prefill_kernel<1, 1>);
+    cudaError_t e = ensure_smem_optin(reinterpret_cast<const void *>(kernel), pl.smem);
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>(pl.grid_x), static_cast<unsigned>(pl.grid_y));
-    return launch_ex_cluster(prefill_kernel, grid, dim3(kThreads), pl.smem, s, pdl, pl.cluster, wmap, xmap, p);
+    return launch_ex_cluster(kernel, grid, dim3(kThreads), pl.smem, s, pdl, pl.cluster, wmap, xmap, p);
 }
 
 }  // namespace qmv

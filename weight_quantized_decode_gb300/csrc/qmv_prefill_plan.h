@@ -18,8 +18,8 @@ constexpr int kAtomCols = kKB / 2;       // tensor-memory columns of one dequant
 constexpr int kTmemCols = 512;           // every CTA allocates all of tensor memory
 constexpr int kPrefillThreads = 352;     // 11 warps: 8 dequantising, MMA issue, 2 copy producers
 // Alignment slack for the 1024-byte-aligned activation tiles, then the
-// barriers (2*NW + 4*NS + 1 of 8 bytes), the tensor-memory address slot and
-// the abort flag.
+// barriers (2*NW + 2*NSA + 2*NSB + 1 of 8 bytes), the tensor-memory address
+// slot and the abort flag.
 constexpr size_t kPrefillFixedSmem = 1024 + 512;
 constexpr size_t kPrefillSmemCap = 225 * 1024;
 constexpr int64_t kMaxGridY = 65535;     // CUDA's limit on gridDim.y
@@ -27,66 +27,116 @@ constexpr int64_t kMaxGridY = 65535;     // CUDA's limit on gridDim.y
 struct PrefillPlan {
     bool ok;           // false: the tensor-core kernel does not take this shape
     int TN;            // token columns per tile = the MMA's N (multiple of 64, <= 256)
-    int KSUB;          // 64-K atoms per ring slot (1, 2 or 4): MMAs per barrier round = 4 * KSUB
-    int NW;            // packed-weight ring slots (256-K tiles)
-    int NS;            // operand ring slots (activation atoms in shared memory, weight atoms in tensor memory)
+    int WT;            // 128-row weight tiles per CTA (1 or 2): each activation atom feeds WT MMAs
+    int KSUB;          // 64-K atoms per ring slot (1, 2 or 4): MMAs per barrier round = 4 * KSUB * WT
+    int NW;            // packed-weight ring slots (256-K chunks of WT tiles)
+    int NSA;           // weight-atom ring slots in tensor memory
+    int NSB;           // activation ring slots in shared memory
     int cluster;       // CTAs per cluster along the weight tiles (1 or 2): each loads 1/cluster of every
                        // activation tile and multicasts it to the others
-    uint32_t tmem_cols;   // allocated: the accumulator [0, TN), then NS * KSUB atoms of A
+    uint32_t tmem_cols;   // allocated: WT accumulators [t * TN, (t + 1) * TN), then the weight atoms
     size_t smem;       // dynamic shared memory per CTA
-    int64_t grid_x;    // 128-row weight tiles
+    int64_t grid_x;    // CTAs along the weight rows (WT * 128 rows each)
     int64_t grid_y;    // token tiles
 };
 
-inline int prefill_pick_tn(int64_t M)
+// Atoms per ring slot: a barrier round carries at least 8 MMAs when it can.
+inline int prefill_ksub(int TN, int WT)
 {
-    // Multiples of 64 so that the epilogue warps read whole 32-column chunks.
-    if (M >= 256) return 256;
-    int tn = static_cast<int>((M + 63) / 64) * 64;
-    return tn < 64 ? 64 : tn;
+    const int k = TN <= 64 ? 4 : (TN <= 128 ? 2 : 1);
+    return k / WT > 0 ? k / WT : 1;
+}
+
+inline int64_t prefill_tmem_cols(int TN, int WT, int KSUB, int NSA)
+{
+    return static_cast<int64_t>(WT) * TN + static_cast<int64_t>(NSA) * KSUB * WT * kAtomCols;
+}
+
+// Estimated SM cycles of a call with token tiles of TN and WT weight tiles per
+// CTA, fitted to slot-level timelines on the GB300: a CTA sustains about 4000
+// flop per cycle in its main loop whatever the tile (7.7-7.9 TFLOP/s per SM
+// for 128 x 256 and 2 x 128 x 192 tiles), and no 64-K slice takes less than
+// ~130 cycles per MMA to issue (64-token tiles); plus ~6000 cycles of ramp and
+// epilogue per wave of CTAs.  Two weight tiles per CTA are only tried with
+// 192-token tiles, where they were measured to pay (a 2 x 128 x 128 tile ran
+// at 4.9 TFLOP/s per SM).
+inline int64_t prefill_cost(int64_t N, int64_t K, int64_t M, int sms, int TN, int WT)
+{
+    const int64_t grid = (N + 128 * WT - 1) / (128 * WT) * ((M + TN - 1) / TN);
+    const int64_t waves = (grid + sms - 1) / (sms > 0 ? sms : 1);
+    const int64_t flops = 2LL * 128 * WT * TN * kKB;
+    const int64_t tensor = flops / 4000;
+    const int64_t issue = 4LL * WT * 130;
+    return waves * ((K / kKB) * (tensor > issue ? tensor : issue) + 6000);
 }
 
 // nw_force / ns_force: ring depths forced for tests and sweeps (a packed-weight
-// depth below 1 or an operand depth below 2 keeps the rule; shared memory and
-// tensor memory still cap them).  One packed-weight slot is correct (each
-// dequantising thread copies its 144-byte row into registers before releasing
-// the slot) but slow: the four atoms held in registers do not cover the next
-// tile's DRAM latency.
-// cluster_force: 1 or 2 forces the cluster size (0 keeps the rule).
+// depth below 1 or an activation-ring depth below 2 keeps the rule; shared
+// memory and tensor memory still cap them).  One packed-weight slot is correct
+// (each dequantising thread copies its rows into registers before releasing
+// the slot) but slow.  cluster_force: 1 or 2 forces the cluster size;
+// tn_force (64..256, a multiple of 64) and wt_force (1 or 2) force the tile
+// (0 keeps the rule).
 inline PrefillPlan plan_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int ns_force,
-                                int cluster_force = 0)
+                                int cluster_force = 0, int tn_force = 0, int wt_force = 0)
 {
-    (void)sms;
     PrefillPlan pl = {};
     if (!(K % kKChunk == 0 && K > 0 && N > 0 && M > 0 && N < (int64_t(1) << 31) && M < (int64_t(1) << 31) &&
           K < (int64_t(1) << 30)))
         return pl;
-    const int TN = prefill_pick_tn(M);
-    // Narrow token tiles take several 64-K atoms per barrier round, so the
-    // MMA-issuing thread's fixed cost per round (two barrier waits and a
-    // commit) is paid once per 8 or 16 MMAs.
-    const int KSUB = TN <= 64 ? 4 : (TN <= 128 ? 2 : 1);
+    // Tile choice: the (token tile, weight tiles per CTA) of least estimated
+    // time among those tensor memory holds with two weight-atom slots; ties
+    // go to the larger grid.  Token tiles wider than the call are not tried.
+    const int64_t m_cover = (M + 63) / 64 * 64;
+    int TN = 0, WT = 0;
+    int64_t best = 0, best_grid = 0;
+    for (int tn = 64; tn <= 256; tn += 64) {
+        if (tn > m_cover && tn > 64) break;
+        if (tn_force && tn != tn_force) continue;
+        for (int wt = 1; wt <= 2; ++wt) {
+            if (wt_force && wt != wt_force) continue;
+            if (!wt_force && wt == 2 && tn != 192) continue;
+            if (prefill_tmem_cols(tn, wt, prefill_ksub(tn, wt), 2) > kTmemCols) continue;
+            const int64_t c = prefill_cost(N, K, M, sms, tn, wt);
+            const int64_t g = (N + 128 * wt - 1) / (128 * wt) * ((M + tn - 1) / tn);
+            if (TN == 0 || c < best || (c == best && g > best_grid)) {
+                TN = tn;
+                WT = wt;
+                best = c;
+                best_grid = g;
+            }
+        }
+    }
+    if (TN == 0) return pl;
+    const int KSUB = prefill_ksub(TN, WT);
     const size_t b_atom = static_cast<size_t>(TN) * kKB * 2;
-    // Activation tiles take 1.5-2 us to land (measured), so the operand ring
-    // is as deep as tensor memory (TN + NS * KSUB * 32 columns) and shared
-    // memory allow; three packed-weight slots cover DRAM latency at these rates.
-    int NW = 3, NS = TN <= 64 ? 3 : 5;
+    const size_t w_tile = static_cast<size_t>(WT) * kPackedTileBytes;
+    // Activation tiles take 1.5-2 us to land (measured), so their ring is as
+    // deep as shared memory allows; the weight atoms only wait for the
+    // dequantising warps, and take what tensor memory leaves.
+    int NW = 3, NSB = 5, NSA = 6;
     auto total = [&] {
-        return kPrefillFixedSmem + static_cast<size_t>(NW) * kPackedTileBytes +
-               static_cast<size_t>(NS) * KSUB * b_atom;
+        return kPrefillFixedSmem + static_cast<size_t>(NW) * w_tile + static_cast<size_t>(NSB) * KSUB * b_atom;
     };
-    auto tmem = [&] { return static_cast<int64_t>(TN) + static_cast<int64_t>(NS) * KSUB * kAtomCols; };
     if (nw_force >= 1) NW = nw_force;
-    if (ns_force >= 2) NS = ns_force;
-    while ((total() > kPrefillSmemCap || tmem() > kTmemCols) && NS > 2) --NS;
+    if (ns_force >= 2) NSB = ns_force;
+    while (prefill_tmem_cols(TN, WT, KSUB, NSA) > kTmemCols && NSA > 2) --NSA;
+    while (total() > kPrefillSmemCap && NSB > 2) --NSB;
     while (total() > kPrefillSmemCap && NW > 2) --NW;
+    // One ring for both operands when both can be at least three deep: the
+    // MMA thread then releases a slot with one commit instead of two (one
+    // 64-token slot of 16 MMAs: 1088 against 1440 ns; 128 x 256 tiles: 21.3
+    // against 25.5 us per call on 8192x2048 at 512 tokens).
+    if (NSA >= 3 && NSB >= 3 && ns_force < 2) NSA = NSB = (NSA < NSB ? NSA : NSB);
     pl.TN = TN;
+    pl.WT = WT;
     pl.KSUB = KSUB;
     pl.NW = NW;
-    pl.NS = NS;
+    pl.NSA = NSA;
+    pl.NSB = NSB;
     pl.tmem_cols = kTmemCols;
     pl.smem = total();
-    pl.grid_x = (N + kBM - 1) / kBM;
+    pl.grid_x = (N + 128 * WT - 1) / (128 * WT);
     // Pairs of CTAs on neighbouring weight tiles can share every activation
     // tile (cluster = 2): each brings in half of its token rows and multicasts
     // them to both.  It halves the L2 reads and each SM's tensor-copy requests
@@ -101,7 +151,8 @@ inline PrefillPlan plan_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw
     pl.grid_y = (M + TN - 1) / TN;
     // More token tiles than gridDim.y allows (M above 65535 * 256) take the
     // generic kernel rather than a launch the runtime would refuse.
-    pl.ok = pl.grid_y <= kMaxGridY && pl.smem <= kPrefillSmemCap && tmem() <= kTmemCols;
+    pl.ok = pl.grid_y <= kMaxGridY && pl.smem <= kPrefillSmemCap &&
+            prefill_tmem_cols(TN, WT, KSUB, NSA) <= kTmemCols;
     return pl;
 }
 
