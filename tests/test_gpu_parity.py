@@ -410,9 +410,6 @@ OVERRIDES = {
                               "q81:q4_0:515:2560:7", "swiglu:q4_0:300:2048:5"],
     # the fused SwiGLU keeps an even number of rows per group (G clamped to <= 16)
     "G=32": ["swiglu:q4_0:77:4096:1", "swiglu:q4_0:40:2048:8"],
-    # fp16 activations staged by bulk copies and permuted in shared memory (the rule gathers them)
-    "xbulk=1": ["gemv:q4_0:1000:4096:1", "gemv:q8_0:300:2560:8", "gemv:q2w:130:2560:3", "moe:q4_0:64:2560:5",
-                "swiglu:q4_0:90:4096:2", "gemv:q4_0:100:14336:8"],
 }
 
 

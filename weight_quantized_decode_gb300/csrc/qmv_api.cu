@@ -136,16 +136,15 @@ struct Plan {
 };
 
 // Launch-shape overrides for tuning sweeps: QMV_GEMV_TUNE="warps=16,stages=3,
-// G=8,SP=1,ctas=2,share=2,early=1,xbulk=1" (any subset; 0 or absent = the
-// built-in rule; early = stages requested before the previous grid completes,
-// xbulk = fp16 activations staged by bulk copies (1) or by loads (0)).
+// G=8,SP=1,ctas=2,share=2,early=1" (any subset; 0 or absent = the built-in
+// rule; early = stages requested before the previous grid completes).
 // ctas = CTAs per SM in the grid; share = the fraction 1/share of an SM's
 // shared memory one CTA may use (share=2 leaves room for the next call's CTA
 // to become resident early under programmatic dependent launch).  N=, K= and
 // M= restrict the override to one table shape (N the planned rows: 2N for the
 // fused SwiGLU, the expert's rows for the multi-expert call).
 struct Tune {
-    int warps = 0, stages = 0, G = 0, SP = 0, ctas = 0, share = 0, early = -1, xbulk = -1;
+    int warps = 0, stages = 0, G = 0, SP = 0, ctas = 0, share = 0, early = -1;
     // optional: apply only to the table shape N x K at M tokens (0 = every shape)
     long long N = 0, K = 0;
     int M = 0;
@@ -179,7 +178,6 @@ const Tune &tune_overrides()
             else if (!std::strcmp(key, "ctas")) t.ctas = v;
             else if (!std::strcmp(key, "share")) t.share = v;
             else if (!std::strcmp(key, "early")) t.early = v;
-            else if (!std::strcmp(key, "xbulk")) t.xbulk = v;
         }
     });
     return t;
@@ -301,12 +299,6 @@ Plan plan_gemv(int fmt, GemvParams &p, int M, int sms, int smem_optin)
             // loads (requesting them all right after the indices measured
             // 1467 against 1503 GB/s on its workload)
             p.early = tu.early >= 0 ? tu.early : (p.n_problems > 1 ? 0 : 1);
-            // fp16 activations gathered pair by pair with loads; xbulk=1 stages
-            // them by bulk copies of whole units and permutes them in shared
-            // memory instead, which measured slower (headline workload 4697
-            // against 4397 GB/s, Q8_0 workload 2037 against 1866 on the same
-            // GB300): the copies queue in the same engine as the weight stream
-            p.xbulk = tu.xbulk >= 0 ? (tu.xbulk ? 1 : 0) : 0;
             pl.streaming = true;
             pl.grid = grid;
             pl.warps = warps;

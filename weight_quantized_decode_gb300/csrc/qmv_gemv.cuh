@@ -94,8 +94,6 @@ struct GemvParams {
     int G;                       // lanes per row (1..32; RG = 32 / G rows per warp)
     int SP;                      // passes per stage (odd)
     int S;                       // stages in each warp's ring
-    int xbulk;                   // fp16 activations staged by bulk copies of whole units, then permuted in
-                                 // place (1), or gathered pair by pair with loads (0)
     int early;                   // stages requested before griddepcontrol.wait (the rest after the
                                  // activation loads); the multi-expert call requests none early
     int xq8;                     // Q4_0 or Q8_0 against Q8_1-quantised activations (integer dots)
@@ -123,7 +121,7 @@ __host__ __device__ inline size_t gemv_smem_bytes(int fmt, int M, int n_problems
     const size_t unit_bytes = fmt == kQ4_0 ? 144 : (fmt == kQ2W ? 80 : 272);
     const size_t xbytes = static_cast<size_t>(n_problems) * M * U * (xq8 ? kXQ8UnitBytes : kXUnitBytes);
     const size_t ring = static_cast<size_t>(warps) * S * 32 * SP * unit_bytes;
-    const size_t bars = (static_cast<size_t>(warps) * S + 1) * 8;   // the rings' and the activations' barriers
+    const size_t bars = static_cast<size_t>(warps) * S * 8;
     const size_t idx = (static_cast<size_t>(n_problems) * 4 + 15) / 16 * 16;   // expert indices (multi-expert call)
     return xbytes + ring + bars + idx;
 }
@@ -172,61 +170,6 @@ __host__ __device__ __forceinline__ int x_perm_slot(int block_parity, int e)
         const int pair = bp & 1;
         const int second = bp >> 1;
         return word * 4 + pair * 2 + second;
-    }
-}
-
-// The permuted chunk `sub` (0..3) of a 32-block is built from four pairs of
-// consecutive activations starting at halves i[0..3] of the block (natural
-// order): chunk = (lo(i0), lo(i2)), (hi(i0), hi(i2)), (lo(i4), lo(i6)),
-// (hi(i4), hi(i6)), the pair order x_perm_slot describes.
-template <int FMT>
-__host__ __device__ __forceinline__ void x_perm_sources(int parity, int sub, int (&i)[4])
-{
-    if (FMT == kQ4_0) {
-        // word `sub` of the block: bytes b0,b1 from (i0, i0+1), b2,b3 from (i2, i2+1);
-        // low nibbles are elements i, high nibbles i + 16.
-        if (parity) { i[0] = 4 * sub; i[1] = 4 * sub + 2; }
-        else if (sub == 0) { i[0] = 0; i[1] = 14; }
-        else { i[0] = 4 * sub - 2; i[1] = 4 * sub; }
-        i[2] = i[0] + 16;
-        i[3] = i[1] + 16;
-    } else if (FMT == kQ2W) {
-        // planes 2*(sub & 1) and 2*(sub & 1) + 1 of word sub >> 1: byte i holds
-        // elements i + 8 * plane.  Even blocks: words (0,1,6,7), (2..5).
-        const int wd = sub >> 1, p0 = 2 * (sub & 1);
-        int b0, b2;
-        if (parity) { b0 = 4 * wd; b2 = 4 * wd + 2; }
-        else if (wd == 0) { b0 = 0; b2 = 6; }
-        else { b0 = 2; b2 = 4; }
-        i[0] = b0 + 8 * p0;
-        i[1] = b2 + 8 * p0;
-        i[2] = i[0] + 8;
-        i[3] = i[1] + 8;
-    } else {
-        // words 2*sub and 2*sub+1 of the block (Q8_0: four codes per word)
-        const int w0 = 2 * sub, w1 = 2 * sub + 1;
-        if (parity) { i[0] = 4 * w0; i[1] = 4 * w0 + 2; i[2] = 4 * w1; i[3] = 4 * w1 + 2; }
-        else {
-            if (w0 == 0) { i[0] = 0; i[1] = 30; }
-            else { i[0] = 4 * w0 - 2; i[1] = 4 * w0; }
-            i[2] = 4 * w1 - 2;
-            i[3] = 4 * w1;
-        }
-    }
-}
-
-// One 32-block of fp16 activations, natural order in w[0..15] (pairs), into
-// the four permuted 16-byte chunks of its parity.
-template <int FMT, int PARITY>
-__device__ __forceinline__ void x_permute_block(const uint32_t (&w)[16], uint4 (&out)[4])
-{
-#pragma unroll
-    for (int sub = 0; sub < 4; ++sub) {
-        int i[4];
-        x_perm_sources<FMT>(PARITY, sub, i);
-        const uint32_t a0 = w[i[0] >> 1], a1 = w[i[1] >> 1], a2 = w[i[2] >> 1], a3 = w[i[3] >> 1];
-        out[sub] = make_uint4(__byte_perm(a0, a1, 0x5410), __byte_perm(a0, a1, 0x7632),
-                              __byte_perm(a2, a3, 0x5410), __byte_perm(a2, a3, 0x7632));
     }
 }
 
@@ -613,8 +556,7 @@ __global__ void __launch_bounds__(MAXT, 1) qmv_stream_kernel(const GemvParams p)
     uint8_t *ring = smem + xbytes + static_cast<size_t>(warp) * S * slot_bytes;
     uint64_t *bars_all = reinterpret_cast<uint64_t *>(smem + xbytes + static_cast<size_t>(warps) * S * slot_bytes);
     uint64_t *bars = bars_all + warp * S;
-    uint64_t *xbar = bars_all + warps * S;                                 // activations staged (fp16 path)
-    int32_t *sidx = reinterpret_cast<int32_t *>(bars_all + warps * S + 1);   // this CTA's expert indices
+    int32_t *sidx = reinterpret_cast<int32_t *>(bars_all + warps * S);   // this CTA's expert indices
 
     // This CTA's contiguous range of (problem, row) pairs.
     const uint32_t R = static_cast<uint32_t>(p.rows_total);
@@ -635,10 +577,8 @@ __global__ void __launch_bounds__(MAXT, 1) qmv_stream_kernel(const GemvParams p)
     const uint32_t lane_chunk_bytes = static_cast<uint32_t>(units_per_stage) * T::kUnitBytes;
     const uint8_t *cta_rows = p.W + static_cast<int64_t>(row0) * p.row_bytes;   // plain GEMV only
 
-    constexpr bool kBulkPath = !XF32 && !XQ8;     // fp16 activations may be staged by bulk copies
     if (lane == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
-        if (kBulkPath && threadIdx.x == 0) mbar_init(xbar, 1);
         mbar_init_fence();
     }
     __syncwarp();
@@ -703,8 +643,6 @@ __global__ void __launch_bounds__(MAXT, 1) qmv_stream_kernel(const GemvParams p)
     int early = MOE ? 0 : early_n;
     for (int i = 0; i < early; ++i) issue_next();
 
-    // every warp sees the activation barrier initialised before it can wait on it
-    if (kBulkPath && p.xbulk) __syncthreads();
     pdl_wait_prior_grid();
 #ifdef QMV_PHASE_STAMPS
     if (threadIdx.x == 0) ph_t[1] = global_timer_ns();
@@ -724,7 +662,6 @@ __global__ void __launch_bounds__(MAXT, 1) qmv_stream_kernel(const GemvParams p)
     // (token, chunk) items of all the CTA's tokens are dealt out together, up
     // to kStageItems per thread per round with all their loads in flight, so
     // long rows and several tokens cost few L2 round trips.
-    bool staged_ok = true;   // false: the activations' bounded wait gave up
     if (XQ8 && p.xq) {
         // Activations already in Q8_1: copy the codes (16 per load) and the
         // blocks' (scale, 8 * code sum) into the staged layout.
@@ -808,54 +745,6 @@ __global__ void __launch_bounds__(MAXT, 1) qmv_stream_kernel(const GemvParams p)
             }
         }
     } else {
-      bool bulk_done = false;
-      if constexpr (kBulkPath) {
-        if (p.xbulk) {
-            // fp16: one bulk copy per 512-byte unit of every token into its
-            // 528-byte slot (the copies need no registers and all fly at
-            // once), then each 32-block is permuted in place by one thread.
-            const int ntok = (prob_hi - prob_lo + 1) * M;
-            const int ncopies = ntok * U;
-            if (warp == 0) {
-                if (lane == 0) mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(ncopies) * 512u);
-                __syncwarp();
-                for (int i = lane; i < ncopies; i += 32) {
-                    const int tok = i / U, u = i - tok * U;
-                    const __half *src = p.x + (static_cast<int64_t>(prob_lo) * M + tok) * p.K + static_cast<int64_t>(u) * 256;
-                    bulk_g2s(xs + (static_cast<size_t>(tok) * U + u) * kXUnitBytes, src, 512u, xbar);
-                }
-            }
-            for (int i = early; i < prefetch; ++i) issue_next();
-            if (mbar_wait_warp(xbar, 0, p.status)) {
-                const int nblk = static_cast<int>(p.K / 32);
-                for (int bi = threadIdx.x; bi < ntok * nblk; bi += blockDim.x) {
-                    const int tok = bi / nblk, blk = bi - tok * nblk;
-                    uint4 *bp = reinterpret_cast<uint4 *>(xs + static_cast<size_t>(tok) * U * kXUnitBytes +
-                                                          (blk >> 3) * kXUnitBytes + (blk & 7) * 64);
-                    uint32_t w[16];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint4 v = bp[k];
-                        w[4 * k] = v.x;
-                        w[4 * k + 1] = v.y;
-                        w[4 * k + 2] = v.z;
-                        w[4 * k + 3] = v.w;
-                    }
-                    uint4 out[4];
-                    if (blk & 1)
-                        x_permute_block<FMT, 1>(w, out);
-                    else
-                        x_permute_block<FMT, 0>(w, out);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) bp[k] = out[k];
-                }
-            } else {
-                staged_ok = false;
-            }
-            bulk_done = true;
-        }
-      }
-      if (!bulk_done) {
         constexpr bool kOneToken = (M == 1 && !MOE);
         constexpr int kStageItems = 4;
         const int ntok = (prob_hi - prob_lo + 1) * M;
@@ -968,7 +857,6 @@ __global__ void __launch_bounds__(MAXT, 1) qmv_stream_kernel(const GemvParams p)
                 }
             }
         }
-      }
     }
     __syncthreads();
     pdl_allow_next_grid();
@@ -985,7 +873,7 @@ __global__ void __launch_bounds__(MAXT, 1) qmv_stream_kernel(const GemvParams p)
 #pragma unroll
     for (int m = 0; m < M; ++m) acc[m] = 0.0f;
 
-    bool alive = staged_ok;
+    bool alive = true;
     int consumed = 0;
     int slot = 0;
     uint32_t phase = 0;
@@ -997,7 +885,7 @@ __global__ void __launch_bounds__(MAXT, 1) qmv_stream_kernel(const GemvParams p)
     const uint8_t *xrow = xs;
     const uint8_t *lane_stage = ring + r * lane_chunk_bytes;
 
-    for (int i = 0; alive && i < total; ++i) {
+    for (int i = 0; i < total; ++i) {
         if (t == 0) {
             lr = g * RG + r;
             row_ok = lane_on && lr < nrows;
@@ -1100,8 +988,6 @@ __global__ void __launch_bounds__(MAXT, 1) qmv_stream_kernel(const GemvParams p)
         if (lane == 0) {
             for (int j = consumed; j < issued; ++j)
                 mbar_wait_bounded(&bars[j % S], static_cast<uint32_t>((j / S) & 1), nullptr);
-            // and the activation copies, if their wait gave up
-            if (kBulkPath && !staged_ok && warp == 0) mbar_wait_bounded(xbar, 0, nullptr);
         }
         __syncwarp();
     }
