@@ -256,6 +256,38 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
     }
 }
 
+// Warp-collective wait_or_abort: every lane calls it and gets the same answer.
+// The common case (phase already complete) stays converged; otherwise lane 0
+// waits and the others follow.
+__device__ __forceinline__ bool warp_wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                                   int *status)
+{
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = wait_or_abort(bar, parity, abort_flag, status);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (ok)   // the phase has completed: every lane observes it before going on
+        while (!mbar_try_wait(bar, parity)) {
+        }
+    return ok;
+}
+
+// One lane of a converged warp (the same lane on every call with all lanes
+// active).  The tensor-core and tensor-copy issue paths run inside such a
+// block of a warp that executes the loop as a whole: measured on the GB300,
+// a loop run by a lone lane issued 64-column MMAs at ~105 cycles each, the
+// same loop run by the converged warp with an elected issuer at ~50.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t e;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(e));
+    return e != 0;
+}
+
 // Dequantise one 32-weight Q4_0 block (scale bits `dbits`, codes in 4 aligned
 // words q[0..3] = qs[0..15]) into 32 fp16 weights in natural K order:
 // out[0..3] = elements 0..7, out[4..7] = 8..15, out[8..11] = 16..23,
@@ -371,18 +403,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     if (warp == kWProducerWarp) {
         // ---------------- packed weights: TMA tensor copies, NW deep ----------------
-        if (lane == 0) {
-            // W is never written by the kernel before this one (a documented
-            // condition of the call), so its copies do not wait for it.
-            // Loop state is kept incremental (no division): this thread's
-            // instruction latency is on the pipeline's critical path.
-            int issued = 0, slot = 0;
-            uint32_t phase = 1;            // an empty slot starts "released"
-            for (int c = 0; c < nC; ++c) {
-                if (!wait_or_abort(&wempty[slot], phase, abort_flag, p.status)) {
-                    ok = false;
-                    break;
-                }
+        // The whole warp runs the loop; one elected lane issues the copies.
+        // W is never written by the kernel before this one (a documented
+        // condition of the call), so its copies do not wait for it.
+        int issued = 0, slot = 0;
+        uint32_t phase = 1;            // an empty slot starts "released"
+        for (int c = 0; c < nC; ++c) {
+            if (!warp_wait_or_abort(&wempty[slot], phase, abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            if (elect_one()) {
                 mbar_arrive_expect_tx(&wfull[slot], static_cast<uint32_t>(w_slot_bytes));
                 // (test only) the first chunk of CTA (0, 0) is expected but never
                 // requested, so the waits on it run out and the CTA aborts
@@ -390,32 +421,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int t = 0; t < WT; ++t)   // rows past N read zeros
                         tma_load_2d(w_tiles + slot * w_slot_bytes + t * kPackedTileBytes, &wmap, c * kPackedRowBytes,
                                     static_cast<int>(n0) + t * kBM, &wfull[slot]);
-                ++issued;
-                if (++slot == NW) {
-                    slot = 0;
-                    phase ^= 1u;
-                }
             }
-            if (!ok)   // let the copies already requested land before the CTA exits
-                for (int c = (issued > NW ? issued - NW : 0); c < issued; ++c)
-                    mbar_wait_bounded(&wfull[c % NW], (c / NW) & 1, nullptr);
+            __syncwarp();
+            ++issued;
+            if (++slot == NW) {
+                slot = 0;
+                phase ^= 1u;
+            }
         }
+        if (!ok && lane == 0)   // let the copies already requested land before the CTA exits
+            for (int c = (issued > NW ? issued - NW : 0); c < issued; ++c)
+                mbar_wait_bounded(&wfull[c % NW], (c / NW) & 1, nullptr);
     } else if (warp == kXProducerWarp) {
         // ---------------- activations: TMA tensor copies, one per atom ----------------
         // With a cluster, this CTA loads rows [crank * TN / CL, ...) of every
         // atom and multicasts them into the same offsets of all the cluster's
         // CTAs; a slot is refilled once every CTA's MMAs have released it.
-        if (lane == 0) {
-            pdl_wait_prior_grid();
-            const int rows = TN / CL;
-            const int row_off_bytes = static_cast<int>(crank) * rows * 128;
-            int issued = 0, s = 0;
-            uint32_t phase = 1;
-            for (int j = 0; j < nK; ++j) {
-                if (!wait_or_abort(one_ring ? &aempty[s] : &bempty[s], phase, abort_flag, p.status)) {
-                    ok = false;
-                    break;
-                }
+        // The whole warp runs the loop; one elected lane issues the copies.
+        pdl_wait_prior_grid();
+        const int rows = TN / CL;
+        const int row_off_bytes = static_cast<int>(crank) * rows * 128;
+        int issued = 0, s = 0;
+        uint32_t phase = 1;
+        for (int j = 0; j < nK; ++j) {
+            if (!warp_wait_or_abort(one_ring ? &aempty[s] : &bempty[s], phase, abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            if (elect_one()) {
                 mbar_arrive_expect_tx(&bfull[s], b_slot_bytes);
                 for (int a = 0; a < KSUB; ++a) {
                     uint8_t *dst = b_tiles + s * b_slot_bytes + a * b_atom_bytes + row_off_bytes;
@@ -426,45 +459,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_2d(dst, &xmap, (j * KSUB + a) * kKB, static_cast<int>(m0), &bfull[s]);
                 }
                 QMV_TRACE(j, 0);
-                ++issued;
-                if (++s == NSB) {
-                    s = 0;
-                    phase ^= 1u;
-                }
             }
-            if (!ok)
-                for (int j = (issued > NSB ? issued - NSB : 0); j < issued; ++j)
-                    mbar_wait_bounded(&bfull[j % NSB], (j / NSB) & 1, nullptr);
+            __syncwarp();
+            ++issued;
+            if (++s == NSB) {
+                s = 0;
+                phase ^= 1u;
+            }
         }
+        if (!ok && lane == 0)
+            for (int j = (issued > NSB ? issued - NSB : 0); j < issued; ++j)
+                mbar_wait_bounded(&bfull[j % NSB], (j / NSB) & 1, nullptr);
     } else if (warp == kMmaWarp) {
-        // ---------------- MMA issue: one thread ----------------
-        if (lane == 0) {
-            const uint32_t idesc = f16_idesc(TN);
-            // Descriptor of activation slot 0's first atom; a slot (or a 16-wide
-            // K step: 32 bytes = 2 in the 16-byte address field) is a plain addition.
-            const uint64_t b_desc0 = sw128_desc(smem_u32(b_tiles));
-            const uint64_t b_step = static_cast<uint64_t>(b_slot_bytes) >> 4;
-            const uint64_t b_atom_step = static_cast<uint64_t>(b_atom_bytes) >> 4;
-            const uint32_t a_slot_cols = static_cast<uint32_t>(KSUB * WT * kAtomCols);
-            int committed = 0, sa = 0, sb = 0;
-            uint32_t pha = 0, phb = 0;
-            uint64_t b_desc = b_desc0;
-            uint32_t a_tmem = tmem_a0;
-            for (int j = 0; j < nK; ++j) {
-                if (!wait_or_abort(&bfull[sb], phb, abort_flag, p.status)) {
-                    ok = false;
-                    break;
-                }
-                QMV_TRACE(j, 1);
-                if (!wait_or_abort(&afull[sa], pha, abort_flag, p.status)) {
-                    ok = false;
-                    break;
-                }
+        // ---------------- MMA issue: the warp runs the loop, one elected lane issues ----------------
+        const uint32_t idesc = f16_idesc(TN);
+        // Descriptor of activation slot 0's first atom; a slot (or a 16-wide
+        // K step: 32 bytes = 2 in the 16-byte address field) is a plain addition.
+        const uint64_t b_desc0 = sw128_desc(smem_u32(b_tiles));
+        const uint64_t b_step = static_cast<uint64_t>(b_slot_bytes) >> 4;
+        const uint64_t b_atom_step = static_cast<uint64_t>(b_atom_bytes) >> 4;
+        const uint32_t a_slot_cols = static_cast<uint32_t>(KSUB * WT * kAtomCols);
+        int committed = 0, sa = 0, sb = 0;
+        uint32_t pha = 0, phb = 0;
+        uint64_t b_desc = b_desc0;
+        uint32_t a_tmem = tmem_a0;
+        for (int j = 0; j < nK; ++j) {
+            if (!warp_wait_or_abort(&bfull[sb], phb, abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) QMV_TRACE(j, 1);
+            if (!warp_wait_or_abort(&afull[sa], pha, abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            // Order the MMAs after the barrier waits (the tcgen05 ops are
+            // asynchronous to this thread) and after the weight atoms'
+            // tensor-memory stores the barrier published.
+            tc_fence_after();
+            // The same lane issues every MMA and every commit: a commit tracks
+            // the MMAs its own thread issued.
+            if (elect_one()) {
                 QMV_TRACE(j, 2);
-                // Order the MMAs after the barrier waits (the tcgen05 ops are
-                // asynchronous to this thread) and after the weight atoms'
-                // tensor-memory stores the barrier published.
-                tc_fence_after();
 #ifdef QMV_PHASE_STAMPS
                 if (j == 0) {
                     phs[2] = global_timer_ns();
@@ -482,29 +518,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else if (!one_ring)
                     mma_commit(&bempty[sb]);
                 QMV_TRACE(j, 3);
-                ++committed;
-                if (++sa == NSA) {
-                    sa = 0;
-                    pha ^= 1u;
-                    a_tmem = tmem_a0;
-                } else {
-                    a_tmem += a_slot_cols;
-                }
-                if (++sb == NSB) {
-                    sb = 0;
-                    phb ^= 1u;
-                    b_desc = b_desc0;
-                } else {
-                    b_desc += b_step;
-                }
             }
+            __syncwarp();
+            ++committed;
+            if (++sa == NSA) {
+                sa = 0;
+                pha ^= 1u;
+                a_tmem = tmem_a0;
+            } else {
+                a_tmem += a_slot_cols;
+            }
+            if (++sb == NSB) {
+                sb = 0;
+                phb ^= 1u;
+                b_desc = b_desc0;
+            } else {
+                b_desc += b_step;
+            }
+        }
+        if (elect_one()) {
             mma_commit(accfull);
 #ifdef QMV_PHASE_STAMPS
             phs[3] = global_timer_ns();
             phs[6] = clock64();
 #endif
-            if (!ok && committed > 0) mbar_wait_bounded(accfull, 0, nullptr);
         }
+        __syncwarp();
+        if (!ok && committed > 0 && lane == 0) mbar_wait_bounded(accfull, 0, nullptr);
     } else {
         // ---------------- dequantising warps 0..7 ----------------
         // Warp w writes lanes 32 * (w mod 4) .. + 31 (weight rows r of each of
