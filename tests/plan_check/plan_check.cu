@@ -198,9 +198,9 @@ void check_swiglu(int64_t N, int64_t K, int M)
 // epilogue's coverage of every (lane quarter, column chunk) of the
 // accumulators.
 void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int ns_force, int cl_force,
-                   int tn_force, int wt_force)
+                   int tn_force, int wt_force, int ksub_force = 0)
 {
-    const PrefillPlan pl = plan_prefill(N, K, M, sms, nw_force, ns_force, cl_force, tn_force, wt_force);
+    const PrefillPlan pl = plan_prefill(N, K, M, sms, nw_force, ns_force, cl_force, tn_force, wt_force, ksub_force);
     const bool shape_ok = K % kKChunk == 0 && K > 0 && N > 0 && M > 0 && N < (int64_t(1) << 31) &&
                           M < (int64_t(1) << 31) && K < (int64_t(1) << 30);
     if (!pl.ok) {
@@ -375,7 +375,8 @@ int main()
             for (int64_t M : pM)
                 for (int tn : {64, 128, 192, 256})
                     for (int wt : {1, 2})
-                        for (int cl : {1, 2}) check_prefill(N, K, M, 152, 0, 0, cl, tn, wt);
+                        for (int cl : {1, 2})
+                            for (int ks : {0, 1, 2, 4}) check_prefill(N, K, M, 152, 0, 0, cl, tn, wt, ks);
     std::printf("checked %ld plans, %ld failures\n", g_checked, g_bad);
     return g_bad ? 1 : 0;
 }

@@ -64,6 +64,7 @@ constexpr int kDeqWarps = 8;                // warps 0..7
 constexpr int kMmaWarp = 8, kWProducerWarp = 9, kXProducerWarp = 10;
 
 struct PrefillParams {
+    const uint8_t *x;  // the activations (fp16 [M][K]): only for the L2 prefetch, the tiles come by TMA
     float *y;
     int *status;
     int64_t N, K, M;
@@ -256,6 +257,14 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
     }
 }
 
+// Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, bytes a
+// multiple of 16).
+constexpr int64_t kPrefetchUnits = 2048;   // 32 KB per prefetch
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Warp-collective wait_or_abort: every lane calls it and gets the same answer.
 // The common case (phase already complete) stays converged; otherwise lane 0
 // waits and the others follow.
@@ -439,6 +448,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         // CTAs; a slot is refilled once every CTA's MMAs have released it.
         // The whole warp runs the loop; one elected lane issues the copies.
         pdl_wait_prior_grid();
+        // The token tile's activation rows are one contiguous range of X.  The
+        // CTAs along the weight tiles each prefetch a share of it into L2 at
+        // once, so that the tile copies of later slots hit L2 instead of
+        // waiting, all at the same moment, for their first touch of HBM.
+        if (elect_one()) {
+            const int64_t rows_here = p.M - m0 < TN ? p.M - m0 : TN;
+            const int64_t units = rows_here * p.K * 2 / 16;              // 16-byte units (K % 256 == 0)
+            const int64_t u0 = units * blockIdx.x / gridDim.x;
+            const int64_t u1 = units * (blockIdx.x + 1) / gridDim.x;
+            const uint8_t *base = p.x + m0 * p.K * 2;
+            for (int64_t u = u0; u < u1; u += kPrefetchUnits) {
+                const int64_t n = u1 - u < kPrefetchUnits ? u1 - u : kPrefetchUnits;
+                prefetch_l2(base + u * 16, static_cast<uint32_t>(n * 16));
+            }
+        }
+        __syncwarp();
         const int rows = TN / CL;
         const int row_off_bytes = static_cast<int>(crank) * rows * 128;
         int issued = 0, s = 0;
@@ -560,10 +585,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int jd = 0;   // ring rounds published (trace only)
 #endif
         for (int c = 0; ok && c < nC; ++c) {
-            if (lane == 0) ok = wait_or_abort(&wfull[slot], wpar, abort_flag, p.status);
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            if (!ok) break;
-            while (!mbar_try_wait_sleep(&wfull[slot], wpar, kSuspendHintNs)) {
+            if (!warp_wait_or_abort(&wfull[slot], wpar, abort_flag, p.status)) {
+                ok = false;
+                break;
             }
             // this thread's row of each weight tile: 36 words (a 256-K chunk)
             uint32_t w[WT][36];
@@ -600,23 +624,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 #pragma unroll
             for (int sub = 0; sub < 4; ++sub) {
-                if (atom == 0) {
-                    // the slot's previous atoms have been read by their MMAs
-                    if (lane == 0) ok = wait_or_abort(&aempty[sa], apar, abort_flag, p.status);
-                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                    if (!ok) break;
-                    while (!mbar_try_wait_sleep(&aempty[sa], apar, kSuspendHintNs)) {
-                    }
-                    tc_fence_after();
-#ifdef QMV_PHASE_STAMPS
-                    if (warp == 0 && lane == 0) QMV_TRACE(jd, 4);
-#endif
-                }
-                // block 2*sub + hsel: even blocks start 2 bytes into word 9*sub
+                // Dequantise block 2*sub + hsel of each weight tile into
+                // registers first (even blocks start 2 bytes into word 9*sub):
+                // the arithmetic overlaps the wait for the tensor-memory slot,
+                // and only the stores remain once the slot is free.
                 const int h = 9 * sub;
+                uint32_t f[WT][16];
 #pragma unroll
                 for (int t = 0; t < WT; ++t) {
-                    uint32_t q[4], f[16], dbits;
+                    uint32_t q[4], dbits;
                     if (hsel == 0) {
 #pragma unroll
                         for (int i = 0; i < 4; ++i) q[i] = __byte_perm(w[t][h + i], w[t][h + i + 1], 0x5432);
@@ -626,12 +642,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int i = 0; i < 4; ++i) q[i] = w[t][h + 5 + i];
                         dbits = w[t][h + 4] >> 16;
                     }
-                    dequant_block_f16(dbits, q, f);
-                    // elements 2j, 2j+1 of the block -> column 16 * hsel + j of the atom
+                    dequant_block_f16(dbits, q, f[t]);
+                }
+                if (atom == 0) {
+                    // the slot's previous atoms have been read by their MMAs
+                    if (!warp_wait_or_abort(&aempty[sa], apar, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#ifdef QMV_PHASE_STAMPS
+                    if (warp == 0 && lane == 0) QMV_TRACE(jd, 4);
+#endif
+                }
+                // elements 2j, 2j+1 of the block -> column 16 * hsel + j of the atom
+#pragma unroll
+                for (int t = 0; t < WT; ++t)
                     tmem_st_16cols(tmem_a0 + lane_base +
                                        static_cast<uint32_t>(((sa * KSUB + atom) * WT + t) * kAtomCols + 16 * hsel),
-                                   f);
-                }
+                                   f[t]);
                 if (++atom == KSUB) {
                     atom = 0;
                     tmem_st_wait();
@@ -740,17 +769,18 @@ EncodeTiledFn encode_fn()
 }
 
 // Ring depths, cluster size and tile forced for tests and sweeps:
-// QMV_PREFILL_RING="NW,NS[,CL[,TN[,WT]]]" (packed-weight slots, activation
-// slots, CTAs per cluster, token tile, weight tiles per CTA; NW below 1, NS
-// below 2, CL other than 1 or 2, TN or WT of 0 keep the rule).
+// QMV_PREFILL_RING="NW,NS[,CL[,TN[,WT[,KSUB]]]]" (packed-weight slots,
+// activation slots, CTAs per cluster, token tile, weight tiles per CTA, atoms
+// per slot; NW below 1, NS below 2, CL other than 1 or 2, TN, WT or KSUB of 0
+// keep the rule).
 int ring_override(int which)
 {
-    static int v[5] = {0, 0, 0, 0, 0};
+    static int v[6] = {0, 0, 0, 0, 0, 0};
     static std::once_flag once;
     std::call_once(once, [] {
         const char *e = std::getenv("QMV_PREFILL_RING");
         if (!e) return;
-        for (int i = 0; i < 5 && e; ++i) {
+        for (int i = 0; i < 6 && e; ++i) {
             v[i] = std::atoi(e);
             e = std::strchr(e, ',');
             if (e) ++e;
@@ -764,7 +794,7 @@ int ring_override(int which)
 PrefillPlan prefill_plan(int64_t N, int64_t K, int64_t M, int sms)
 {
     PrefillPlan pl = plan_prefill(N, K, M, sms, ring_override(0), ring_override(1), ring_override(2),
-                                  ring_override(3), ring_override(4));
+                                  ring_override(3), ring_override(4), ring_override(5));
     if (encode_fn() == nullptr) pl.ok = false;
     return pl;
 }
@@ -797,6 +827,7 @@ cudaError_t launch_prefill(const PrefillPlan &pl, const void *W, const void *x, 
             return cudaErrorInvalidValue;
     }
     PrefillParams p = {};
+    p.x = static_cast<const uint8_t *>(x);
     p.y = y;
     p.status = status;
     p.N = N;

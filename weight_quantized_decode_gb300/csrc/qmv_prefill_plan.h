@@ -75,10 +75,11 @@ inline int64_t prefill_cost(int64_t N, int64_t K, int64_t M, int sms, int TN, in
 // memory and tensor memory still cap them).  One packed-weight slot is correct
 // (each dequantising thread copies its rows into registers before releasing
 // the slot) but slow.  cluster_force: 1 or 2 forces the cluster size;
-// tn_force (64..256, a multiple of 64) and wt_force (1 or 2) force the tile
-// (0 keeps the rule).
+// tn_force (64..256, a multiple of 64) and wt_force (1 or 2) force the tile,
+// ksub_force (1, 2 or 4) the atoms per ring slot where tensor memory still
+// holds two weight-atom slots (0 keeps the rule).
 inline PrefillPlan plan_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int ns_force,
-                                int cluster_force = 0, int tn_force = 0, int wt_force = 0)
+                                int cluster_force = 0, int tn_force = 0, int wt_force = 0, int ksub_force = 0)
 {
     PrefillPlan pl = {};
     if (!(K % kKChunk == 0 && K > 0 && N > 0 && M > 0 && N < (int64_t(1) << 31) && M < (int64_t(1) << 31) &&
@@ -108,9 +109,14 @@ inline PrefillPlan plan_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw
         }
     }
     if (TN == 0) return pl;
-    const int KSUB = prefill_ksub(TN, WT);
     const size_t b_atom = static_cast<size_t>(TN) * kKB * 2;
     const size_t w_tile = static_cast<size_t>(WT) * kPackedTileBytes;
+    int KSUB = prefill_ksub(TN, WT);
+    if ((ksub_force == 1 || ksub_force == 2 || ksub_force == 4) &&
+        prefill_tmem_cols(TN, WT, ksub_force, 2) <= kTmemCols &&
+        kPrefillFixedSmem + static_cast<size_t>(nw_force >= 1 && nw_force < 2 ? nw_force : 2) * w_tile +
+                2 * static_cast<size_t>(ksub_force) * b_atom <= kPrefillSmemCap)
+        KSUB = ksub_force;
     // Activation tiles take 1.5-2 us to land (measured), so their ring is as
     // deep as shared memory allows; the weight atoms only wait for the
     // dequantising warps, and take what tensor memory leaves.
