@@ -115,6 +115,22 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, i
     return ok;
 }
 
+// One lane of a converged warp (the same lane on every call with all lanes
+// active).  The tensor-core and tensor-copy issue paths run inside such a
+// block of a warp that executes the loop as a whole: measured on the GB300,
+// a loop run by a lone lane issued 64-column MMAs at ~105 cycles each, the
+// same loop run by the converged warp with an elected issuer at ~50.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t e;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(e));
+    return e != 0;
+}
+
 // ---- bulk copies (TMA, non-tensor) --------------------------------------------
 
 // Global -> shared bulk copy that signals `bar` with complete_tx.  dst, src and

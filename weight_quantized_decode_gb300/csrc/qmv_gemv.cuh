@@ -588,40 +588,62 @@ __global__ void __launch_bounds__(MAXT, 1) qmv_stream_kernel(const GemvParams p)
     int is_slot = 0;         // slot of the next stage to request
     int is_t = 0;            // its stage index within the row group
     int is_g = warp;         // its row group (CTA-local)
-    const uint8_t *is_row = nullptr;   // row of lane r < RG in the current group (null: none)
+    const uint8_t *is_row = nullptr;   // multi-expert call: row of lane r < RG in the current group (null: none)
     const uint64_t l2_policy = l2_evict_first_policy();   // weights stream through L2 once
 
+    // One elected lane requests the row chunks of a stage in a loop (except in
+    // the multi-expert call): a copy whose operands differ per lane is issued
+    // one lane at a time anyway, at several times the cost (on the GB300, 32
+    // per-lane 256-byte copies took ~1760 cycles to issue, the same 32 from one
+    // lane ~420).
     auto issue_next = [&]() {
-        if (is_t == 0) {
-            is_row = nullptr;
-            const int lr = is_g * RG + lane;
-            if (lane < RG && lr < nrows) {
-                if (MOE) {
-                    const uint32_t row = row0 + lr;
+        const int u0 = is_t * units_per_stage;
+        const int u1 = min(U, u0 + units_per_stage);
+        const uint32_t bytes = static_cast<uint32_t>(u1 - u0) * T::kUnitBytes;
+        const size_t off = static_cast<size_t>(u0) * T::kUnitBytes;
+        const int lr0 = is_g * RG;
+        const int nr = min(RG, nrows - lr0);   // rows of the group (at least one while stages remain)
+        // (test only) the first stage of CTA 0's warp 0 is expected but never
+        // requested: nothing is in flight into that slot when its wait gives up
+        const bool skip = p.test_skip_copy && blockIdx.x == 0 && warp == 0 && issued == 0;
+        if constexpr (MOE) {
+            // Per-lane copies here (lane r requests group row r): each row's
+            // expert id comes from shared memory, and rows whose id is out of
+            // range request nothing (their dot products read zeros).  Measured
+            // ahead of an elected lane's loop for the multi-expert call.
+            if (is_t == 0) {
+                is_row = nullptr;
+                if (lane < nr) {
+                    const uint32_t row = row0 + static_cast<uint32_t>(lr0 + lane);
                     const uint32_t prob = row / N;
                     const uint32_t n = row - prob * N;
                     const int64_t e = sidx[prob - prob_lo];
                     if (e >= 0 && e < p.n_experts) is_row = p.W + (e * p.N + n) * p.row_bytes;
-                } else if (SWIGLU) {
-                    const uint32_t row = row0 + lr;
-                    is_row = ((row & 1u) ? p.W2 : p.W) + static_cast<int64_t>(row >> 1) * p.row_bytes;
-                } else {
-                    is_row = cta_rows + static_cast<int64_t>(lr) * p.row_bytes;
                 }
             }
+            const uint32_t my_bytes = is_row ? bytes : 0u;
+            const uint32_t total_bytes = __reduce_add_sync(0xffffffffu, my_bytes);
+            if (lane == 0) mbar_arrive_expect_tx(&bars[is_slot], total_bytes);
+            __syncwarp();
+            if (my_bytes && !skip)
+                bulk_g2s_hint(ring + static_cast<size_t>(is_slot) * slot_bytes + lane * lane_chunk_bytes, is_row + off,
+                              my_bytes, &bars[is_slot], l2_policy);
+        } else if (elect_one()) {
+            uint8_t *dst = ring + static_cast<size_t>(is_slot) * slot_bytes;
+            mbar_arrive_expect_tx(&bars[is_slot], static_cast<uint32_t>(nr) * bytes);
+            if (!skip)
+                for (int i = 0; i < nr; ++i) {
+                    const uint8_t *src;
+                    if (SWIGLU) {
+                        const uint32_t row = row0 + static_cast<uint32_t>(lr0 + i);
+                        src = ((row & 1u) ? p.W2 : p.W) + static_cast<int64_t>(row >> 1) * p.row_bytes;
+                    } else {
+                        src = cta_rows + static_cast<int64_t>(lr0 + i) * p.row_bytes;
+                    }
+                    bulk_g2s_hint(dst + i * lane_chunk_bytes, src + off, bytes, &bars[is_slot], l2_policy);
+                }
         }
-        const int u0 = is_t * units_per_stage;
-        const int u1 = min(U, u0 + units_per_stage);
-        const uint32_t my_bytes = is_row ? static_cast<uint32_t>(u1 - u0) * T::kUnitBytes : 0u;
-        const uint32_t total_bytes = __reduce_add_sync(0xffffffffu, my_bytes);
-        if (lane == 0) mbar_arrive_expect_tx(&bars[is_slot], total_bytes);
         __syncwarp();
-        // (test only) the first stage of CTA 0's warp 0 is expected but never
-        // requested: nothing is in flight into that slot when its wait gives up
-        const bool skip = p.test_skip_copy && blockIdx.x == 0 && warp == 0 && issued == 0;
-        if (my_bytes && !skip)
-            bulk_g2s_hint(ring + static_cast<size_t>(is_slot) * slot_bytes + lane * lane_chunk_bytes,
-                          is_row + static_cast<size_t>(u0) * T::kUnitBytes, my_bytes, &bars[is_slot], l2_policy);
         ++issued;
         if (++is_slot == S) is_slot = 0;
         if (++is_t == T_stages) {

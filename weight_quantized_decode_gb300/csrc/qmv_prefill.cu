@@ -281,22 +281,6 @@ __device__ __forceinline__ bool warp_wait_or_abort(uint64_t *bar, uint32_t parit
     return ok;
 }
 
-// One lane of a converged warp (the same lane on every call with all lanes
-// active).  The tensor-core and tensor-copy issue paths run inside such a
-// block of a warp that executes the loop as a whole: measured on the GB300,
-// a loop run by a lone lane issued 64-column MMAs at ~105 cycles each, the
-// same loop run by the converged warp with an elected issuer at ~50.
-__device__ __forceinline__ bool elect_one()
-{
-    uint32_t e;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "elect.sync _|p, 0xffffffff;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(e));
-    return e != 0;
-}
-
 // Dequantise one 32-weight Q4_0 block (scale bits `dbits`, codes in 4 aligned
 // words q[0..3] = qs[0..15]) into 32 fp16 weights in natural K order:
 // out[0..3] = elements 0..7, out[4..7] = 8..15, out[8..11] = 16..23,
