@@ -89,11 +89,12 @@ struct PrefillParams {
 constexpr int kPrefillPhaseWords = 8;
 constexpr int kPrefillPhaseCap = 1 << 16;
 constexpr int kTraceSlotsDev = 128;
-__device__ unsigned long long g_prefill_trace_dev[kTraceSlotsDev * 6];
+constexpr int kTraceCols = 8;
+__device__ unsigned long long g_prefill_trace_dev[kTraceSlotsDev * kTraceCols];
 #define QMV_TRACE(j, k)                                                                                     \
     do {                                                                                                  \
         if (blockIdx.x == 0 && blockIdx.y == 0 && (j) < kTraceSlotsDev)                                   \
-            g_prefill_trace_dev[(j) * 6 + (k)] = global_timer_ns();                                       \
+            g_prefill_trace_dev[(j) * kTraceCols + (k)] = global_timer_ns();                              \
     } while (0)
 #else
 #define QMV_TRACE(j, k) \
@@ -573,6 +574,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
             }
+#ifdef QMV_PHASE_STAMPS
+            if (warp == 0 && lane == 0) QMV_TRACE(jd, 6);
+#endif
             // this thread's row of each weight tile: 36 words (a 256-K chunk)
             uint32_t w[WT][36];
 #pragma unroll
@@ -588,24 +592,85 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             // Hand the slot back only once this thread's reads of it are done:
-            // the words are consumed into a register, and fence.proxy.async
-            // orders the reads (generic proxy) before the producer's next
-            // copy into the slot (async proxy).
-            {
-                uint32_t all = 0;
+            // the words are consumed (into a register, or by the dequantising
+            // arithmetic), and fence.proxy.async orders the reads (generic
+            // proxy) before the producer's next copy into the slot (async
+            // proxy).
+            int wslot = slot;
+            auto release_w = [&](bool consumed) {
+                if (!consumed) {
+                    uint32_t x4[4] = {0u, 0u, 0u, 0u};   // four short XOR chains
 #pragma unroll
-                for (int t = 0; t < WT; ++t)
+                    for (int t = 0; t < WT; ++t)
 #pragma unroll
-                    for (int i = 0; i < 36; ++i) all ^= w[t][i];
-                asm volatile("" ::"r"(all) : "memory");
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&wempty[slot]);
+                        for (int i = 0; i < 36; ++i) x4[i & 3] ^= w[t][i];
+                    asm volatile("" ::"r"(x4[0] ^ x4[1] ^ x4[2] ^ x4[3]) : "memory");
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&wempty[wslot]);
+            };
             if (++slot == NW) {
                 slot = 0;
                 wpar ^= 1u;
             }
+            if (WT == 1 && KSUB == 4) {
+                // One slot is the whole 256-K chunk (64-token tiles): all four
+                // blocks are dequantised before the slot wait, four independent
+                // chains the scheduler can interleave.
+                uint32_t f4[4][16];
+#pragma unroll
+                for (int sub = 0; sub < 4; ++sub) {
+                    const int h = 9 * sub;
+                    uint32_t q[4], dbits;
+                    if (hsel == 0) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) q[i] = __byte_perm(w[0][h + i], w[0][h + i + 1], 0x5432);
+                        dbits = w[0][h] & 0xffffu;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) q[i] = w[0][h + 5 + i];
+                        dbits = w[0][h + 4] >> 16;
+                    }
+                    dequant_block_f16(dbits, q, f4[sub]);
+                }
+                // Every word this thread loaded has fed the arithmetic above
+                // (values 0, 2, 4, 6 of a block depend on all its code words
+                // and its scale), so the loads are complete.
+#pragma unroll
+                for (int sub = 0; sub < 4; ++sub)
+                    asm volatile("" ::"r"(f4[sub][0]), "r"(f4[sub][2]), "r"(f4[sub][4]), "r"(f4[sub][6]) : "memory");
+                release_w(true);
+#ifdef QMV_PHASE_STAMPS
+                if (warp == 0 && lane == 0) QMV_TRACE(jd, 7);
+#endif
+                if (!warp_wait_or_abort(&aempty[sa], apar, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#ifdef QMV_PHASE_STAMPS
+                if (warp == 0 && lane == 0) QMV_TRACE(jd, 4);
+#endif
+#pragma unroll
+                for (int sub = 0; sub < 4; ++sub)
+                    tmem_st_16cols(tmem_a0 + lane_base + static_cast<uint32_t>((sa * 4 + sub) * kAtomCols + 16 * hsel),
+                                   f4[sub]);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&afull[sa]);
+#ifdef QMV_PHASE_STAMPS
+                if (warp == 0 && lane == 0) QMV_TRACE(jd, 5);
+                ++jd;
+#endif
+                if (++sa == NSA) {
+                    sa = 0;
+                    apar ^= 1u;
+                }
+                continue;
+            }
+            release_w(false);
 #pragma unroll
             for (int sub = 0; sub < 4; ++sub) {
                 // Dequantise block 2*sub + hsel of each weight tile into
@@ -848,12 +913,12 @@ cudaError_t launch_prefill(const PrefillPlan &pl, const void *W, const void *x, 
 // Phase-timeline builds only (not declared in include/qmv.h): copies up to
 // max_records prefill records to host memory and resets them; returns the
 // count or -1 on a CUDA error.
-// The slot-level trace of CTA (0, 0) of the last prefill launch: 128 rounds x 6 stamps.
+// The slot-level trace of CTA (0, 0) of the last prefill launch: 128 rounds x 8 stamps.
 extern "C" QMV_API int qmv_prefill_trace(unsigned long long *host)
 {
     using namespace qmv;
     if (cudaDeviceSynchronize() != cudaSuccess) return -1;
-    return cudaMemcpyFromSymbol(host, g_prefill_trace_dev, sizeof(unsigned long long) * kTraceSlotsDev * 6) ==
+    return cudaMemcpyFromSymbol(host, g_prefill_trace_dev, sizeof(unsigned long long) * kTraceSlotsDev * kTraceCols) ==
                    cudaSuccess
                ? 0
                : -1;
