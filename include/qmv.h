@@ -307,6 +307,18 @@ QMV_API qmv_status qmm_q4_0_prefill(const void *W, const void *x, float *y,
                             int64_t N, int64_t K, int64_t M, qmv_stream_t stream);
 
 /*
+ * The same many-token GEMM for Q8_0 weights (the roadmap's measured Q8_0
+ * baseline -- roadmap, "The measured baseline" -- taken to many tokens): each
+ * 34-byte block's int8 codes times its fp16 scale, rounded once to fp16, in
+ * tensor memory; fp32 accumulation.
+ *   W : Q8_0 bytes [N][K/32*34], 16-byte aligned.  The tensor-core kernel
+ *       takes K % 256 == 0; other K take the generic kernel.
+ *   x, y, M, errors and asynchrony as for qmm_q4_0_prefill.
+ */
+QMV_API qmv_status qmm_q8_0_prefill(const void *W, const void *x, float *y,
+                            int64_t N, int64_t K, int64_t M, qmv_stream_t stream);
+
+/*
  * Reads and clears the device status word (QMV_DEV_* bits) of the current
  * device, in one atomic step enqueued on `stream` (so it follows every kernel
  * enqueued before it on `stream`; a bit that a kernel on another stream sets

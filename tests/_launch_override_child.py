@@ -21,9 +21,10 @@ def main():
         kind, fmt, n, k, m = case.split(":")
         N, K, M = int(n), int(k), int(m)
         if kind == "pfrep":   # the same prefill call repeated: outputs must be bit-identical
-            W = dev(synth.q4_0_weights(N, K, synth.seed_for(f"ovr_pf_{N}x{K}")))
+            W = dev(synth.weights(fmt, N, K, synth.seed_for(f"ovr_pf_{N}x{K}")))
             x = dev(synth.activations(M, K, synth.seed_for(f"ovr_pf_x_{K}_{M}")))
-            ys = [q.qmm_q4_0_prefill(W, x) for _ in range(4)]
+            fn = {"q4_0": q.qmm_q4_0_prefill, "q8_0": q.qmm_q8_0_prefill}[fmt]
+            ys = [fn(W, x) for _ in range(4)]
             torch.cuda.synchronize()
             res[case] = ys[0].cpu().numpy()
             res[case + ":identical"] = np.array([all(torch.equal(ys[0], v) for v in ys[1:])])

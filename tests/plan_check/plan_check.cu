@@ -198,9 +198,10 @@ void check_swiglu(int64_t N, int64_t K, int M)
 // epilogue's coverage of every (lane quarter, column chunk) of the
 // accumulators.
 void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int ns_force, int cl_force,
-                   int tn_force, int wt_force, int ksub_force = 0)
+                   int tn_force, int wt_force, int ksub_force = 0, int fmt = kPfQ4_0, int splitk = 0)
 {
-    const PrefillPlan pl = plan_prefill(N, K, M, sms, nw_force, ns_force, cl_force, tn_force, wt_force, ksub_force);
+    const PrefillPlan pl =
+        plan_prefill(N, K, M, sms, nw_force, ns_force, cl_force, tn_force, wt_force, ksub_force, fmt, splitk);
     const bool shape_ok = K % kKChunk == 0 && K > 0 && N > 0 && M > 0 && N < (int64_t(1) << 31) &&
                           M < (int64_t(1) << 31) && K < (int64_t(1) << 30);
     if (!pl.ok) {
@@ -213,14 +214,23 @@ void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int n
     ++g_checked;
     CHECK(shape_ok, "prefill took %lldx%lld M=%lld", (long long)N, (long long)K, (long long)M);
     const int TN = pl.TN, WT = pl.WT, KSUB = pl.KSUB, NW = pl.NW, NSA = pl.NSA, NSB = pl.NSB;
-    CHECK(TN % 64 == 0 && TN >= 64 && TN <= 256, "TN %d", TN);                 // kind::f16, M = 128: N <= 256
+    // kind::f16, M = 128: N a multiple of 16 up to 256; 16-token tiles for calls of up to 16 tokens
+    CHECK((TN % 64 == 0 && TN >= 64 && TN <= 256) || (TN == 16 && M <= 16 && WT == 1), "TN %d", TN);
+    CHECK(pl.fmt == fmt, "format");
+    const int SK = pl.splitk;
+    const int64_t chunks_all = K / kKChunk;
+    CHECK(SK >= 1 && SK <= 8 && SK <= chunks_all, "split K %d", SK);
+    CHECK(SK == 1 || (TN == 16 && pl.cluster == 1), "split K needs 16-token tiles without multicast");
+    CHECK(splitk != 0 || SK == 1, "split K unasked");
+    if (splitk < 0 && SK > 1) CHECK(pl.grid_x * pl.grid_y * SK <= sms, "split K beyond one wave");
     CHECK(WT == 1 || WT == 2, "WT %d", WT);
     CHECK(KSUB == 1 || KSUB == 2 || KSUB == 4, "KSUB %d", KSUB);              // a slot never straddles a W chunk
     CHECK(NW >= 1 && NSA >= 2 && NSB >= 2, "rings %d %d %d", NW, NSA, NSB);
     CHECK(pl.smem <= static_cast<size_t>(kOptin), "prefill smem %zu", pl.smem);
     const uint32_t cols = pl.tmem_cols;
     CHECK(cols == 512, "TMEM %u", cols);
-    const int64_t a_end = static_cast<int64_t>(WT) * TN + static_cast<int64_t>(NSA) * KSUB * WT * kAtomCols;
+    const int64_t a0 = (static_cast<int64_t>(WT) * TN + 31) / 32 * 32;   // first weight-atom column
+    const int64_t a_end = a0 + static_cast<int64_t>(NSA) * KSUB * WT * kAtomCols;
     CHECK(a_end <= cols, "TMEM columns %lld > %u", (long long)a_end, cols);
     const int CL = pl.cluster;
     CHECK(CL == 1 || CL == 2, "cluster %d", CL);
@@ -229,13 +239,23 @@ void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int n
     const int64_t rows_per_cta = static_cast<int64_t>(kBM) * WT;
     CHECK(pl.grid_x * rows_per_cta >= N && (pl.grid_x - CL) * rows_per_cta < N, "row tiles");
     CHECK(pl.grid_y * TN >= M && (pl.grid_y - 1) * TN < M, "token tiles");
+    // each CTA along K: chunks [c_first, c_first + nC), nK slots
+    int64_t covered = 0;
+    for (int z = 0; z < SK; ++z) {
+        const int64_t c_first = chunks_all * z / SK, nCz = chunks_all * (z + 1) / SK - c_first;
+        CHECK(c_first == covered && nCz >= 1 && (nCz * 4) % KSUB == 0, "split K chunks %d", z);
+        covered += nCz;
+    }
+    CHECK(covered == chunks_all, "split K cover");
     const int64_t nK = K / (kKB * KSUB), nC = K / kKChunk;
     CHECK(nK * KSUB * kKB == K && nC * 4 == nK * KSUB && nK < INT32_MAX, "K loop");
+    const int row_b = prefill_row_bytes(fmt), esz = fmt == kPfQ8_0 ? 2 : 1;
+    CHECK(row_b % 16 == 0 && row_b / esz <= 256, "W box row");
 
     // shared memory, as offsets from the 1024-byte-aligned base
     const size_t b_atom = static_cast<size_t>(TN) * kKB * 2;
     const size_t b_slot = KSUB * b_atom;
-    const size_t w_slot = static_cast<size_t>(WT) * kPackedTileBytes;
+    const size_t w_slot = static_cast<size_t>(WT) * kBM * row_b;
     const size_t w_off = NSB * b_slot;
     const size_t bar_off = w_off + static_cast<size_t>(NW) * w_slot;
     const size_t bar_end = bar_off + static_cast<size_t>(2 * NW + 2 * NSA + 2 * NSB + 1) * 8 + 4 + 4;
@@ -251,20 +271,24 @@ void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int n
             }
     for (int w = 0; w < NW; ++w)
         for (int t = 0; t < WT; ++t)
-            CHECK((w_off + static_cast<size_t>(w) * w_slot + static_cast<size_t>(t) * kPackedTileBytes) % 128 == 0,
+            CHECK((w_off + static_cast<size_t>(w) * w_slot + static_cast<size_t>(t) * kBM * row_b) % 128 == 0,
                   "W slot");
 
     // tensor-copy boxes: within the box limits; bytes landed = the barrier's expected count
-    CHECK(kPackedRowBytes <= 256 && kBM <= 256 && TN / CL <= 256 && TN % CL == 0 && kKB * 2 <= 128, "boxes");
-    CHECK(static_cast<size_t>(kPackedRowBytes) * kBM * WT == w_slot, "W box bytes");
+    CHECK(kBM <= 256 && TN / CL <= 256 && TN % CL == 0 && kKB * 2 <= 128, "boxes");
+    CHECK(static_cast<size_t>(row_b) * kBM * WT == w_slot, "W box bytes");
     // the slot's barrier expects the bytes of every CTA's multicast share
     CHECK(static_cast<size_t>(KSUB) * CL * kKB * (TN / CL) * 2 == b_slot, "x box bytes");
     // coordinates: innermost x times the element size on 16 bytes and inside the row
-    const int64_t row_bytes = (K / 32) * 18;
+    const int64_t row_bytes = (K / 32) * (fmt == kPfQ8_0 ? 34 : 18);
+    CHECK(row_bytes % 16 == 0, "W row stride");
     for (int64_t c = 0; c < nC; c += (c < 4 || c + 4 >= nC) ? 1 : std::max<int64_t>(1, nC / 64)) {
-        const int64_t x = c * kPackedRowBytes;
-        CHECK(x % 16 == 0 && x + kPackedRowBytes <= row_bytes && x < INT32_MAX, "W x %lld", (long long)x);
+        const int64_t x = c * (row_b / esz);   // in the map's elements
+        CHECK((x * esz) % 16 == 0 && (x * esz) + row_b <= row_bytes && x < INT32_MAX, "W x %lld", (long long)x);
     }
+    if (fmt == kPfQ8_0)   // a thread's nine words of block 2 * sub + hsel lie inside its 272-byte row
+        for (int sub = 0; sub < 4; ++sub)
+            for (int hsel = 0; hsel < 2; ++hsel) CHECK(4 * (17 * sub + 8 * hsel + 9) <= row_b, "Q8_0 block words");
     for (int64_t j = 0; j < nK; j += (j < 4 || j + 4 >= nK) ? 1 : std::max<int64_t>(1, nK / 64))
         for (int a = 0; a < KSUB; ++a) {
             const int64_t x = (j * KSUB + a) * kKB;
@@ -284,7 +308,7 @@ void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int n
         for (int a = 0; a < KSUB; ++a)
             for (int t = 0; t < WT; ++t) {
                 std::fill(&cover[0][0], &cover[0][0] + kBM * kAtomCols, 0);
-                const int64_t base = static_cast<int64_t>(WT) * TN + static_cast<int64_t>((s * KSUB + a) * WT + t) * kAtomCols;
+                const int64_t base = a0 + static_cast<int64_t>((s * KSUB + a) * WT + t) * kAtomCols;
                 for (int w = 0; w < 8; ++w) {
                     const int quarter = w & 3, hsel = w >> 2;
                     for (int lane = 0; lane < 32; ++lane) {
@@ -295,7 +319,7 @@ void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int n
                                   static_cast<size_t>(NW) * w_slot,
                               "packed read");
                         const int64_t c0 = base + 16 * hsel;
-                        CHECK(c0 >= static_cast<int64_t>(WT) * TN && c0 + 16 <= a_end, "A columns");
+                        CHECK(c0 >= a0 && c0 % 16 == 0 && base % 32 == 0 && c0 + 16 <= a_end, "A columns");
                         for (int j = 0; j < 16; ++j) ++cover[r][16 * hsel + j];
                     }
                 }
@@ -305,23 +329,41 @@ void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int n
                 // the MMAs of this atom read columns [base, base + 32) in four K = 16 steps of 8 columns
                 for (int k = 0; k < 4; ++k) CHECK(base + 8 * k + 8 <= a_end, "MMA A columns");
             }
-    for (int t = 0; t < WT; ++t) CHECK(static_cast<int64_t>(t + 1) * TN <= a_end - static_cast<int64_t>(NSA) * KSUB * WT * kAtomCols, "accumulator %d", t);
-    for (int sub = 0; sub < 4; ++sub) CHECK(4 * (9 * sub + 8) + 4 <= kPackedRowBytes, "block words");
+    for (int t = 0; t < WT; ++t) CHECK(static_cast<int64_t>(t + 1) * TN <= a0, "accumulator %d", t);
+    if (fmt == kPfQ4_0)
+        for (int sub = 0; sub < 4; ++sub) CHECK(4 * (9 * sub + 8) + 4 <= kPackedRowBytes, "block words");
 
     // epilogue: each (lane quarter, 32-column chunk) read by exactly one warp, inside the accumulators
     static unsigned char ecover[4][16];
     std::fill(&ecover[0][0], &ecover[0][0] + 64, 0);
     const int warps = kPrefillThreads / 32;
-    for (int w = 0; w < warps; ++w) {
-        const int quarter = w & 3, nq = (warps - quarter + 3) / 4, rank = w >> 2;
-        for (int c0 = 32 * rank; c0 < WT * TN; c0 += 32 * nq) {
-            CHECK(c0 + 32 <= WT * TN && (c0 % TN) + 32 <= TN, "epilogue columns");
-            ++ecover[quarter][c0 / 32];
+    if (TN < 32) {
+        // 16-token tiles: the first warp of each lane quarter reads its 16 columns
+        for (int w = 0; w < warps; ++w)
+            if ((w >> 2) == 0) ++ecover[w & 3][0];
+        for (int q = 0; q < 4; ++q) CHECK(ecover[q][0] == 1, "epilogue quarter %d read %d times", q, ecover[q][0]);
+        // split K: the partial tile [128][TN] fp32 fits the idle rings, and the
+        // CTAs' row shares cover the 128 rows once
+        CHECK(SK == 1 || static_cast<size_t>(kBM) * TN * 4 <= bar_off, "split-K partial");
+        int rows = 0;
+        for (int z = 0; z < SK; ++z) {
+            const int r0 = kBM * z / SK, r1 = kBM * (z + 1) / SK;
+            CHECK(r0 == rows && r1 >= r0, "split-K rows %d", z);
+            rows = r1;
         }
+        CHECK(rows == kBM, "split-K row cover");
+    } else {
+        for (int w = 0; w < warps; ++w) {
+            const int quarter = w & 3, nq = (warps - quarter + 3) / 4, rank = w >> 2;
+            for (int c0 = 32 * rank; c0 < WT * TN; c0 += 32 * nq) {
+                CHECK(c0 + 32 <= WT * TN && (c0 % TN) + 32 <= TN, "epilogue columns");
+                ++ecover[quarter][c0 / 32];
+            }
+        }
+        for (int q = 0; q < 4; ++q)
+            for (int c = 0; c < WT * TN / 32; ++c)
+                CHECK(ecover[q][c] == 1, "epilogue chunk %d,%d read %d times", q, c, ecover[q][c]);
     }
-    for (int q = 0; q < 4; ++q)
-        for (int c = 0; c < WT * TN / 32; ++c)
-            CHECK(ecover[q][c] == 1, "epilogue chunk %d,%d read %d times", q, c, ecover[q][c]);
 }
 
 }  // namespace
@@ -377,6 +419,15 @@ int main()
                     for (int wt : {1, 2})
                         for (int cl : {1, 2})
                             for (int ks : {0, 1, 2, 4}) check_prefill(N, K, M, 152, 0, 0, cl, tn, wt, ks);
+    // Q8_0 weights, and split K over up to 8 CTAs (automatic and forced), over the same shapes
+    for (int64_t N : pN)
+        for (int64_t K : pK)
+            for (int64_t M : pM)
+                for (int sms : {152, 132, 1}) {
+                    for (int sk : {0, -1, 2, 3, 8}) check_prefill(N, K, M, sms, 0, 0, 0, 0, 0, 0, kPfQ8_0, sk);
+                    for (int sk : {-1, 2, 5, 8}) check_prefill(N, K, M, sms, 0, 0, 0, 0, 0, 0, kPfQ4_0, sk);
+                    check_prefill(N, K, M, sms, 1, 0, 2, 0, 0, 0, kPfQ8_0, 0);
+                }
     std::printf("checked %ld plans, %ld failures\n", g_checked, g_bad);
     return g_bad ? 1 : 0;
 }

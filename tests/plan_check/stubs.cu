@@ -25,7 +25,7 @@ cudaError_t launch_quantize_q8_1(const void *, int8_t *, uint16_t *, int32_t *, 
 
 cudaError_t launch_read_probe(const void *, int64_t, uint32_t *, int *, int, cudaStream_t) { return cudaSuccess; }
 
-PrefillPlan prefill_plan(int64_t, int64_t, int64_t, int) { return PrefillPlan{}; }
+PrefillPlan prefill_plan(int64_t, int64_t, int64_t, int, int, int) { return PrefillPlan{}; }
 
 cudaError_t launch_prefill(const PrefillPlan &, const void *, const void *, float *, int64_t, int64_t, int64_t, int *,
                            cudaStream_t, bool, bool)

@@ -475,7 +475,6 @@ def test_prefill_repeats_are_bit_identical(cuda_lib, orc, N, K, M):
 
 PREFILL_RINGS = {
     # the shallowest rings (two packed-weight slots, two operand slots)
-    "2,2": ["pfrep:q4_0:12288:2560:512", "pfrep:q4_0:4096:2560:256", "pfrep:q4_0:2048:2560:64"],
     # one packed-weight slot, the deepest operand ring that then fits
     "1,4": ["pfrep:q4_0:12288:2560:512", "pfrep:q4_0:4096:2560:256", "pfrep:q4_0:2048:2560:64"],
     # no cluster: each CTA loads whole activation tiles itself (the rule's choice)
@@ -484,6 +483,14 @@ PREFILL_RINGS = {
     # CTA pairs sharing each activation tile by multicast, also with an odd tile
     # count (one CTA of the last pair lies past N)
     "0,0,2": ["pfrep:q4_0:384:512:100", "pfrep:q4_0:130:256:70", "pfrep:q4_0:8192:2048:64"],
+    # 16-token tiles split along K over a cluster of 2, 3 or 8 CTAs (partials added
+    # through distributed shared memory), ragged rows and a ragged chunk share
+    "0,0,0,0,0,0,2": ["pfrep:q4_0:384:2560:8", "pfrep:q8_0:300:2048:16", "pfrep:q8_0:4096:6144:8"],
+    "0,0,0,0,0,0,3": ["pfrep:q4_0:200:2560:5", "pfrep:q8_0:129:1792:1"],
+    "0,0,0,0,0,0,8": ["pfrep:q4_0:256:2048:3", "pfrep:q8_0:130:4096:16", "pfrep:q8_0:2560:6144:8"],
+    # the shallowest rings (two packed-weight slots, two operand slots), Q4_0 and Q8_0
+    "2,2": ["pfrep:q4_0:12288:2560:512", "pfrep:q4_0:4096:2560:256", "pfrep:q4_0:2048:2560:64",
+            "pfrep:q8_0:12288:2560:512", "pfrep:q8_0:2048:2560:64"],
 }
 
 
@@ -504,10 +511,10 @@ def test_prefill_shallow_rings(orc, tmp_path, ring):
         _, fmt, n, k, m = case.split(":")
         N, K, M = int(n), int(k), int(m)
         assert bool(res[case + ":identical"][0]), (ring, case, "repeats differ")
-        W = synth.q4_0_weights(N, K, synth.seed_for(f"ovr_pf_{N}x{K}"))
+        W = synth.weights(fmt, N, K, synth.seed_for(f"ovr_pf_{N}x{K}"))
         x = synth.activations(M, K, synth.seed_for(f"ovr_pf_x_{K}_{M}"))
         rows = _sample_rows(N, k=32)
-        y_ref, S = orc.qmv_rows(0, W, x, N, K, rows, nthreads=8)
+        y_ref, S = orc.qmv_rows(H.FMT[fmt], W, x, N, K, rows, nthreads=8)
         assert H.normalised_error(res[case].astype(np.float64)[:, rows], y_ref, S) <= H.TOL, (ring, case)
 
 
@@ -563,6 +570,35 @@ def test_prefill(cuda_lib, orc, N, K, M):
     torch.cuda.synchronize()
     y_ref, S = orc.qmv(0, W, x, N, K, nthreads=8)
     assert H.normalised_error(y.cpu().numpy(), y_ref, S) <= H.TOL
+
+
+# Q8_0 weights: 16-token tiles (M <= 16), 64-token tiles, wide tiles with one and
+# two weight tiles per CTA, ragged rows and tokens.
+@pytest.mark.parametrize("N,K,M", [(256, 512, 64), (384, 1024, 100), (128, 256, 1), (1024, 2560, 512),
+                                   (200, 512, 70), (130, 2048, 16), (300, 4096, 9), (12000, 512, 512)])
+def test_prefill_q8_0(cuda_lib, orc, N, K, M):
+    q = cuda_lib
+    W = synth.q8_0_weights(N, K, N + K + M)
+    x = synth.activations(M, K, M)
+    y = q.qmm_q8_0_prefill(dev(W), dev(x))
+    torch.cuda.synchronize()
+    y_ref, S = orc.qmv(1, W, x, N, K, nthreads=8)
+    assert H.normalised_error(y.cpu().numpy(), y_ref, S) <= H.TOL
+
+
+@pytest.mark.parametrize("N,K,M", [(12288, 2560, 512), (12288, 2560, 8), (2560, 6144, 16)])
+def test_prefill_q8_0_repeats_are_bit_identical(cuda_lib, orc, N, K, M):
+    q = cuda_lib
+    W = dev(synth.q8_0_weights(N, K, synth.seed_for(f"prefill8_{N}x{K}")))
+    x = dev(synth.activations(M, K, synth.seed_for(f"prefill8_x_{M}")))
+    ys = [q.qmm_q8_0_prefill(W, x) for _ in range(5)]
+    torch.cuda.synchronize()
+    for y in ys[1:]:
+        assert torch.equal(y, ys[0])
+    rows = _sample_rows(N, k=32)
+    y_ref, S = orc.qmv_rows(1, synth.q8_0_weights(N, K, synth.seed_for(f"prefill8_{N}x{K}")),
+                            synth.activations(M, K, synth.seed_for(f"prefill8_x_{M}")), N, K, rows, nthreads=8)
+    assert H.normalised_error(ys[0].cpu().numpy()[:, rows], y_ref, S) <= H.TOL
 
 
 @pytest.mark.parametrize("N,K,M", [(12288, 2560, 64), (12288, 2560, 512), (8192, 2048, 64), (8192, 2048, 512)])

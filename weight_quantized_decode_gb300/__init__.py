@@ -17,6 +17,7 @@ Functions (same names as the C ABI):
     qmv_q4_0_q8_1_pre(W, q, d_bits, sumq, ...)   -> the Q8_1 product on activations already quantised
     qmv_moe(W_pool, expert_idx, n_experts, x, N, y=None, stream=None)
     qmm_q4_0_prefill(W, x, y=None, stream=None)  -> y fp32 [M, N]
+    qmm_q8_0_prefill(W, x, y=None, stream=None)  -> y fp32 [M, N]
     qmv_device_status(stream=None)               -> int (QMV_DEV_* bits, cleared)
     qmv_read_probe(buf, out=None, stream=None)   -> checksum tensor (read-only bandwidth probe)
     qmv_set_pdl(enable), qmv_status_str(code), qmv_version()
@@ -61,7 +62,7 @@ def lib():
                                "(there is no CPU fallback)")
         L = ctypes.CDLL(LIB_PATH)
         vp, i64 = ctypes.c_void_p, ctypes.c_int64
-        for name in ("qmv_q4_0", "qmv_q8_0", "qmm_q4_0_prefill", "qmv_q4_0_f32", "qmv_q2w", "qmv_q4_0_q8_1",
+        for name in ("qmv_q4_0", "qmv_q8_0", "qmm_q4_0_prefill", "qmm_q8_0_prefill", "qmv_q4_0_f32", "qmv_q2w", "qmv_q4_0_q8_1",
                      "qmv_q8_0_q8_1"):
             f = getattr(L, name)
             f.restype = ctypes.c_int
@@ -165,6 +166,10 @@ def qmv_moe_ptr(W_pool: int, idx: int, n_experts: int, x: int, y: int, N: int, K
 
 def qmm_q4_0_prefill_ptr(W: int, x: int, y: int, N: int, K: int, M: int, stream: int = 0) -> None:
     _check("qmm_q4_0_prefill", lib().qmm_q4_0_prefill(W, x, y, N, K, M, stream))
+
+
+def qmm_q8_0_prefill_ptr(W: int, x: int, y: int, N: int, K: int, M: int, stream: int = 0) -> None:
+    _check("qmm_q8_0_prefill", lib().qmm_q8_0_prefill(W, x, y, N, K, M, stream))
 
 
 def qmv_read_probe_ptr(buf: int, nbytes: int, out: int, stream: int = 0) -> None:
@@ -380,6 +385,14 @@ def qmm_q4_0_prefill(W, x, y=None, stream=None):
     W, x, y, N, K, M = _prep(W, x, y, Q4_0_BLOCK_BYTES, "qmm_q4_0_prefill")
     with _on_device("qmm_q4_0_prefill", W, x, y):
         qmm_q4_0_prefill_ptr(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, _stream_handle(stream))
+    return y
+
+
+def qmm_q8_0_prefill(W, x, y=None, stream=None):
+    """Many-token (prefill) form of qmv_q8_0 on the tensor cores."""
+    W, x, y, N, K, M = _prep(W, x, y, Q8_0_BLOCK_BYTES, "qmm_q8_0_prefill")
+    with _on_device("qmm_q8_0_prefill", W, x, y):
+        qmm_q8_0_prefill_ptr(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, M, _stream_handle(stream))
     return y
 
 

@@ -611,8 +611,13 @@ qmv_status qmv_moe(const void *W_pool, const int32_t *expert_idx, int64_t n_expe
                     reinterpret_cast<cudaStream_t>(stream));
 }
 
-qmv_status qmm_q4_0_prefill(const void *W, const void *x, float *y, int64_t N, int64_t K, int64_t M,
-                            qmv_stream_t stream)
+namespace {
+
+// The many-token GEMM on the tensor cores for Q4_0 (fmt kPfQ4_0) or Q8_0
+// weights; shapes the tensor-core kernel does not take run on the generic
+// kernel.
+qmv_status run_prefill(int fmt, const void *W, const void *x, float *y, int64_t N, int64_t K, int64_t M,
+                       qmv_stream_t stream)
 {
     qmv_status st = check_common(W, x, y, N, K, M, int64_t(1) << 24);
     if (st != QMV_OK || N == 0 || M == 0) return st;
@@ -623,7 +628,7 @@ qmv_status qmm_q4_0_prefill(const void *W, const void *x, float *y, int64_t N, i
     int *status = nullptr;
     int sms = 0, optin = 0;
     if (device_info(dev, &status, &sms, &optin) != cudaSuccess) return QMV_ERR_CUDA;
-    const PrefillPlan pl = prefill_plan(N, K, M, sms);
+    const PrefillPlan pl = prefill_plan(N, K, M, sms, fmt);
     if (pl.ok) {
         cudaError_t e = launch_prefill(pl, W, x, y, N, K, M, status, s, g_pdl.load(std::memory_order_relaxed) != 0,
                                        test_skip_this_launch(kArmPrefill));
@@ -641,7 +646,7 @@ qmv_status qmm_q4_0_prefill(const void *W, const void *x, float *y, int64_t N, i
     p.N = N;
     p.K = K;
     p.n_experts = 1;
-    p.row_bytes = (K / 32) * 18;
+    p.row_bytes = (K / 32) * (fmt == kPfQ8_0 ? 34 : 18);
     p.n_problems = 1;
     p.max_local_problems = 1;
     p.rows_total = N;
@@ -649,13 +654,27 @@ qmv_status qmm_q4_0_prefill(const void *W, const void *x, float *y, int64_t N, i
     int64_t grid = (N + 7) / 8;
     if (grid > 32LL * sms) grid = 32LL * sms;
     if (grid < 1) grid = 1;
-    cudaError_t e = launch_gemv_generic(kQ4_0, p, static_cast<int>(M), static_cast<int>(grid), s,
-                                        g_pdl.load() != 0);
+    cudaError_t e = launch_gemv_generic(fmt == kPfQ8_0 ? kQ8_0 : kQ4_0, p, static_cast<int>(M),
+                                        static_cast<int>(grid), s, g_pdl.load() != 0);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return QMV_ERR_LAUNCH;
     }
     return QMV_OK;
+}
+
+}  // namespace
+
+qmv_status qmm_q4_0_prefill(const void *W, const void *x, float *y, int64_t N, int64_t K, int64_t M,
+                            qmv_stream_t stream)
+{
+    return run_prefill(kPfQ4_0, W, x, y, N, K, M, stream);
+}
+
+qmv_status qmm_q8_0_prefill(const void *W, const void *x, float *y, int64_t N, int64_t K, int64_t M,
+                            qmv_stream_t stream)
+{
+    return run_prefill(kPfQ8_0, W, x, y, N, K, M, stream);
 }
 
 qmv_status qmv_device_status(qmv_stream_t stream, int32_t *out)

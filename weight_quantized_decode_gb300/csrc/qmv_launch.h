@@ -63,10 +63,11 @@ cudaError_t launch_ex(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStr
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-// launch_ex with thread-block clusters of `cluster` CTAs along x (1 = none).
+// launch_ex with thread-block clusters of cluster.x * cluster.y * cluster.z
+// CTAs (all ones = none).
 template <typename Kernel, typename... Args>
-cudaError_t launch_ex_cluster(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
-                              int cluster, Args... args)
+cudaError_t launch_ex_cluster_dims(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                                   dim3 cluster, Args... args)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -80,16 +81,25 @@ cudaError_t launch_ex_cluster(Kernel kernel, dim3 grid, dim3 block, size_t smem,
         attr[n].val.programmaticStreamSerializationAllowed = 1;
         ++n;
     }
-    if (cluster > 1) {
+    if (cluster.x * cluster.y * cluster.z > 1) {
         attr[n].id = cudaLaunchAttributeClusterDimension;
-        attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
-        attr[n].val.clusterDim.y = 1;
-        attr[n].val.clusterDim.z = 1;
+        attr[n].val.clusterDim.x = cluster.x;
+        attr[n].val.clusterDim.y = cluster.y;
+        attr[n].val.clusterDim.z = cluster.z;
         ++n;
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// launch_ex with thread-block clusters of `cluster` CTAs along x (1 = none).
+template <typename Kernel, typename... Args>
+cudaError_t launch_ex_cluster(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                              int cluster, Args... args)
+{
+    return launch_ex_cluster_dims(kernel, grid, block, smem, s, pdl, dim3(static_cast<unsigned>(cluster), 1, 1),
+                                  args...);
 }
 
 }  // namespace qmv

@@ -312,7 +312,58 @@ __device__ __forceinline__ void dequant_block_f16(uint32_t dbits, const uint32_t
     }
 }
 
-template <int WT, int CL>
+// Dequantise one 34-byte Q8_0 block (fp16 scale, then 32 int8 codes) from
+// the nine 32-bit words of a packed 256-K row chunk that hold it: EVEN blocks
+// start a word (scale in the low half of v[0], code pair j in v[(j + 1) / 2]),
+// odd blocks start half a word in (scale in the upper half of v[0], code
+// pair j in v[1 + j / 2]).  A code byte b becomes the fp16 1024 + (b ^ 0x80)
+// = 1152 + code (the sign flip makes it unsigned, 0x64 its exponent byte);
+// subtracting 1152 is exact, and the product with the scale is rounded once.
+// Output j is the half2 of elements (2j, 2j + 1).
+template <bool EVEN>
+__device__ __forceinline__ void dequant_block_q8_f16(const uint32_t *v, uint32_t (&out)[16])
+{
+    const uint32_t dbits = EVEN ? (v[0] & 0xffffu) : (v[0] >> 16);
+    const __half d = __ushort_as_half(static_cast<unsigned short>(dbits));
+    const __half2 d2 = __halves2half2(d, d);
+    const __half2 c1152 = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));   // 1152
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const uint32_t word = EVEN ? v[(j + 1) >> 1] : v[1 + (j >> 1)];
+        // EVEN: pair j sits in bytes 2, 3 (j even) or 0, 1 (j odd) of its word
+        const uint32_t sel = EVEN ? ((j & 1) ? 0x4140u : 0x4342u) : ((j & 1) ? 0x4342u : 0x4140u);
+        const uint32_t t = __byte_perm(word ^ 0x80808080u, 0x64646464u, sel);
+        const __half2 c = __hsub2(as_h2(t), c1152);   // the codes, exact
+        const __half2 w = __hmul2(c, d2);
+        out[j] = *reinterpret_cast<const uint32_t *>(&w);
+    }
+}
+
+// 16 consecutive 32-bit tensor-memory columns of this thread's lane into v.
+__device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, uint32_t (&v)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// A float at this shared-memory location of cluster CTA `rank`.
+__device__ __forceinline__ float ld_cluster_f32(const float *local, uint32_t rank)
+{
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+// SMALL: 16-token tiles (one weight tile, no multicast), which may be split
+// along K over a cluster; the other tiles compile without that code.
+template <int WT, int CL, int FMT, bool SMALL>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                    const PrefillParams p)
@@ -330,7 +381,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint16_t cmask = static_cast<uint16_t>((1u << CL) - 1u);
     const int b_atom_bytes = TN * kKB * 2;                  // one 64-K activation atom
     const int b_slot_bytes = KSUB * b_atom_bytes;
-    const int w_slot_bytes = WT * kPackedTileBytes;         // one 256-K chunk of the CTA's WT weight tiles
+    // One weight row's 256-K chunk (144 bytes Q4_0, 272 Q8_0) and the TMA
+    // coordinate step per chunk (bytes for Q4_0; the Q8_0 map counts 16-bit
+    // elements, its 272-byte box row being wider than a box's 256 elements).
+    constexpr int kRowB = prefill_row_bytes(FMT);
+    constexpr int kTileB = kBM * kRowB;
+    constexpr int kWCoord = FMT == kPfQ8_0 ? kRowB / 2 : kRowB;
+    const int w_slot_bytes = WT * kTileB;                   // one 256-K chunk of the CTA's WT weight tiles
     uint8_t *b_tiles = smem;
     uint8_t *w_tiles = b_tiles + NSB * b_slot_bytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(w_tiles + NW * w_slot_bytes);
@@ -353,8 +410,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #endif
     const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kBM * WT;
     const int64_t m0 = static_cast<int64_t>(blockIdx.y) * TN;
-    const int nK = static_cast<int>(p.K / (kKB * KSUB));   // slots of KSUB x 64 K
-    const int nC = static_cast<int>(p.K / kKChunk);        // packed 256-K chunks
+    // Split K (16-token tiles): CTA z of the cluster along z takes chunks
+    // [c_first, c_first + nC).
+    const int64_t chunks_all = p.K / kKChunk;
+    const int c_first = SMALL ? static_cast<int>(chunks_all * blockIdx.z / gridDim.z) : 0;
+    const int nC = SMALL ? static_cast<int>(chunks_all * (blockIdx.z + 1) / gridDim.z) - c_first
+                         : static_cast<int>(chunks_all);            // packed 256-K chunks
+    const int nK = SMALL ? nC * (kKChunk / kKB) / KSUB : static_cast<int>(p.K / (kKB * KSUB));   // slots
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NW; ++i) {
@@ -384,8 +446,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     // Columns [t * TN, (t + 1) * TN) hold weight tile t's accumulator; weight
-    // atom (slot s, atom a, tile t) follows at WT * TN + ((s * KSUB + a) * WT + t) * 32.
-    const uint32_t tmem_a0 = tmem_base + static_cast<uint32_t>(WT * TN);
+    // atom (slot s, atom a, tile t) follows at A0 + ((s * KSUB + a) * WT + t) * 32,
+    // A0 = WT * TN rounded up to 32 columns (16-token tiles: 32).
+    const uint32_t tmem_a0 = tmem_base + (SMALL ? 32u : static_cast<uint32_t>(WT * TN));
 #ifdef QMV_PHASE_STAMPS
     if (threadIdx.x == 0) phs[1] = global_timer_ns();
 #endif
@@ -413,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // requested, so the waits on it run out and the CTA aborts
                 if (!(p.test_skip_copy && c == 0 && blockIdx.x == 0 && blockIdx.y == 0))
                     for (int t = 0; t < WT; ++t)   // rows past N read zeros
-                        tma_load_2d(w_tiles + slot * w_slot_bytes + t * kPackedTileBytes, &wmap, c * kPackedRowBytes,
+                        tma_load_2d(w_tiles + slot * w_slot_bytes + t * kTileB, &wmap, (c_first + c) * kWCoord,
                                     static_cast<int>(n0) + t * kBM, &wfull[slot]);
             }
             __syncwarp();
@@ -462,11 +525,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(&bfull[s], b_slot_bytes);
                 for (int a = 0; a < KSUB; ++a) {
                     uint8_t *dst = b_tiles + s * b_slot_bytes + a * b_atom_bytes + row_off_bytes;
+                    const int xk = ((SMALL ? c_first * (kKChunk / kKB) : 0) + j * KSUB + a) * kKB;
                     if constexpr (CL > 1)
-                        tma_load_2d_mc(dst, &xmap, (j * KSUB + a) * kKB,
-                                       static_cast<int>(m0) + static_cast<int>(crank) * rows, &bfull[s], cmask);
+                        tma_load_2d_mc(dst, &xmap, xk, static_cast<int>(m0) + static_cast<int>(crank) * rows,
+                                       &bfull[s], cmask);
                     else
-                        tma_load_2d(dst, &xmap, (j * KSUB + a) * kKB, static_cast<int>(m0), &bfull[s]);
+                        tma_load_2d(dst, &xmap, xk, static_cast<int>(m0), &bfull[s]);
                 }
                 QMV_TRACE(j, 0);
             }
@@ -555,6 +619,86 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (!ok && committed > 0 && lane == 0) mbar_wait_bounded(accfull, 0, nullptr);
+    } else if constexpr (FMT == kPfQ8_0) {
+        // ---------------- dequantising warps 0..7, Q8_0 ----------------
+        // The same split as for Q4_0 (warp w: lane quarter w mod 4, block
+        // parity w / 4 of every 64-K atom); a thread loads the nine words of
+        // each of its four blocks of the chunk (words 17 * sub + 8 * hsel + i).
+        const int quarter = warp & 3;
+        const int hsel = warp >> 2;
+        const int r = 32 * quarter + lane;         // weight row within each tile
+        const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
+        int slot = 0, sa = 0, atom = 0;
+        uint32_t wpar = 0, apar = 1;
+        for (int c = 0; ok && c < nC; ++c) {
+            if (!warp_wait_or_abort(&wfull[slot], wpar, abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            uint32_t w[WT][36];
+#pragma unroll
+            for (int t = 0; t < WT; ++t) {
+                const uint32_t *row =
+                    reinterpret_cast<const uint32_t *>(w_tiles + slot * w_slot_bytes + t * kTileB + r * kRowB);
+#pragma unroll
+                for (int sub = 0; sub < 4; ++sub)
+#pragma unroll
+                    for (int i = 0; i < 9; ++i) w[t][9 * sub + i] = row[17 * sub + 8 * hsel + i];
+            }
+            // Hand the slot back once this thread's reads of it are done (the
+            // words consumed into a register; fence.proxy.async orders the
+            // generic-proxy reads before the producer's next copy).
+            {
+                uint32_t x4[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                for (int t = 0; t < WT; ++t)
+#pragma unroll
+                    for (int i = 0; i < 36; ++i) x4[i & 3] ^= w[t][i];
+                asm volatile("" ::"r"(x4[0] ^ x4[1] ^ x4[2] ^ x4[3]) : "memory");
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&wempty[slot]);
+            if (++slot == NW) {
+                slot = 0;
+                wpar ^= 1u;
+            }
+#pragma unroll
+            for (int sub = 0; sub < 4; ++sub) {
+                // dequantise first, then wait for the tensor-memory slot
+                uint32_t f[WT][16];
+#pragma unroll
+                for (int t = 0; t < WT; ++t) {
+                    if (hsel == 0)
+                        dequant_block_q8_f16<true>(&w[t][9 * sub], f[t]);
+                    else
+                        dequant_block_q8_f16<false>(&w[t][9 * sub], f[t]);
+                }
+                if (atom == 0) {
+                    if (!warp_wait_or_abort(&aempty[sa], apar, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+#pragma unroll
+                for (int t = 0; t < WT; ++t)
+                    tmem_st_16cols(tmem_a0 + lane_base +
+                                       static_cast<uint32_t>(((sa * KSUB + atom) * WT + t) * kAtomCols + 16 * hsel),
+                                   f[t]);
+                if (++atom == KSUB) {
+                    atom = 0;
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&afull[sa]);
+                    if (++sa == NSA) {
+                        sa = 0;
+                        apar ^= 1u;
+                    }
+                }
+            }
+        }
     } else {
         // ---------------- dequantising warps 0..7 ----------------
         // Warp w writes lanes 32 * (w mod 4) .. + 31 (weight rows r of each of
@@ -746,21 +890,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;
         const int nq = (kThreads / 32 - quarter + 3) / 4;   // warps in this quarter
         const int rank = warp >> 2;
+        if constexpr (SMALL) {
+            // 16-token tiles: the first warp of each lane quarter reads its 16
+            // columns; with split K the partial tile goes to this CTA's shared
+            // memory (the rings are idle now), row-major [128][TN].
+            if (rank == 0) {
+                uint32_t v[16];
+                tmem_ld_16cols(tmem_base + (static_cast<uint32_t>(32 * quarter) << 16), v);
+                const int rl = 32 * quarter + lane;
+                const int64_t row = n0 + rl;
+                if (gridDim.z > 1) {
+                    float *part = reinterpret_cast<float *>(smem) + rl * TN;
 #pragma unroll
-        for (int t = 0; t < WT; ++t) {
-            const int64_t row = n0 + t * kBM + 32 * quarter + lane;
-            for (int c0 = 32 * rank; c0 < TN; c0 += 32 * nq) {
-                uint32_t v[32];
-                tmem_ld_32cols(tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) + t * TN + c0, v);
-                if (row < p.N) {
+                    for (int i = 0; i < 16; ++i) part[i] = __uint_as_float(v[i]);
+                } else if (row < p.N) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int64_t m = m0 + c0 + i;
+                    for (int i = 0; i < 16; ++i) {
+                        const int64_t m = m0 + i;
                         if (m < p.M) p.y[m * p.N + row] = __uint_as_float(v[i]);
                     }
                 }
             }
+        } else {
+#pragma unroll
+            for (int t = 0; t < WT; ++t) {
+                const int64_t row = n0 + t * kBM + 32 * quarter + lane;
+                for (int c0 = 32 * rank; c0 < TN; c0 += 32 * nq) {
+                    uint32_t v[32];
+                    tmem_ld_32cols(tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) + t * TN + c0, v);
+                    if (row < p.N) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int64_t m = m0 + c0 + i;
+                            if (m < p.M) p.y[m * p.N + row] = __uint_as_float(v[i]);
+                        }
+                    }
+                }
+            }
         }
+    }
+    if (SMALL && gridDim.z > 1) {
+        // Split K (16-token tiles, one cluster along z): once every CTA's
+        // partial is in its shared memory, CTA z adds rows [128 z / SK,
+        // 128 (z + 1) / SK) of all of them in rank order (the same order on
+        // every call) and stores y; the second barrier keeps each CTA's shared
+        // memory alive until the others have read it.
+        cluster_sync();
+        const int sk = static_cast<int>(gridDim.z), z = static_cast<int>(blockIdx.z);
+        const int r0 = kBM * z / sk, nr = kBM * (z + 1) / sk - r0;
+        const float *part = reinterpret_cast<const float *>(smem);
+        for (int i = threadIdx.x; i < nr * TN; i += blockDim.x) {
+            const int col = i / nr, rl = r0 + (i - col * nr);
+            float acc = 0.0f;
+            for (int q = 0; q < sk; ++q) acc += ld_cluster_f32(part + rl * TN + col, static_cast<uint32_t>(q));
+            const int64_t row = n0 + rl, m = m0 + col;
+            if (ok && row < p.N && m < p.M) p.y[m * p.N + row] = acc;
+        }
+        cluster_sync();
     }
 
     tc_fence_before();
@@ -818,18 +1004,18 @@ EncodeTiledFn encode_fn()
 }
 
 // Ring depths, cluster size and tile forced for tests and sweeps:
-// QMV_PREFILL_RING="NW,NS[,CL[,TN[,WT[,KSUB]]]]" (packed-weight slots,
+// QMV_PREFILL_RING="NW,NS[,CL[,TN[,WT[,KSUB[,SK]]]]]" (packed-weight slots,
 // activation slots, CTAs per cluster, token tile, weight tiles per CTA, atoms
-// per slot; NW below 1, NS below 2, CL other than 1 or 2, TN, WT or KSUB of 0
-// keep the rule).
+// per slot, CTAs along K; NW below 1, NS below 2, CL other than 1 or 2, TN,
+// WT, KSUB or SK of 0 keep the rule).
 int ring_override(int which)
 {
-    static int v[6] = {0, 0, 0, 0, 0, 0};
+    static int v[7] = {0, 0, 0, 0, 0, 0, 0};
     static std::once_flag once;
     std::call_once(once, [] {
         const char *e = std::getenv("QMV_PREFILL_RING");
         if (!e) return;
-        for (int i = 0; i < 6 && e; ++i) {
+        for (int i = 0; i < 7 && e; ++i) {
             v[i] = std::atoi(e);
             e = std::strchr(e, ',');
             if (e) ++e;
@@ -840,10 +1026,12 @@ int ring_override(int which)
 
 }  // namespace
 
-PrefillPlan prefill_plan(int64_t N, int64_t K, int64_t M, int sms)
+PrefillPlan prefill_plan(int64_t N, int64_t K, int64_t M, int sms, int fmt, int splitk)
 {
+    const int sk_force = ring_override(6);
     PrefillPlan pl = plan_prefill(N, K, M, sms, ring_override(0), ring_override(1), ring_override(2),
-                                  ring_override(3), ring_override(4), ring_override(5));
+                                  ring_override(3), ring_override(4), ring_override(5), fmt,
+                                  sk_force > 0 ? sk_force : splitk);
     if (encode_fn() == nullptr) pl.ok = false;
     return pl;
 }
@@ -853,16 +1041,20 @@ cudaError_t launch_prefill(const PrefillPlan &pl, const void *W, const void *x, 
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc || !pl.ok) return cudaErrorNotSupported;
-    const int64_t row_bytes = (K / 32) * 18;
+    const bool q8 = pl.fmt == kPfQ8_0;
+    const int64_t row_bytes = (K / 32) * (q8 ? 34 : 18);
     CUtensorMap wmap, xmap;
     {
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(N)};
+        // Q8_0: 16-bit elements, so that one 272-byte chunk row fits a box
+        // (at most 256 elements per box dimension).
+        const int esz = q8 ? 2 : 1;
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes / esz), static_cast<cuuint64_t>(N)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
-        const cuuint32_t box[2] = {kPackedRowBytes, kBM};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(prefill_row_bytes(pl.fmt) / esz), kBM};
         const cuuint32_t estr[2] = {1, 1};
-        if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(W), dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        if (enc(&wmap, q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(W),
+                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
     {
@@ -899,12 +1091,21 @@ cudaError_t launch_prefill(const PrefillPlan &pl, const void *W, const void *x, 
         p.phase_seq = g_prefill_phase_seq.fetch_add(1);
     }
 #endif
-    auto kernel = pl.WT == 2 ? (pl.cluster > 1 ? prefill_kernel<2, 2> : prefill_kernel<2, 1>)
-                             : (pl.cluster > 1 ? prefill_kernel<1, 2> : prefill_kernel<1, 1>);
+    // Q8_0 takes no multicast pairs (the plan never sets them for it).
+    if (q8 && pl.cluster > 1) return cudaErrorInvalidValue;
+    if (pl.splitk > 1 && (pl.cluster > 1 || pl.TN != 16)) return cudaErrorInvalidValue;
+    if (pl.TN == 16 && (pl.WT != 1 || pl.cluster != 1)) return cudaErrorInvalidValue;
+    auto kernel =
+        pl.TN == 16 ? (q8 ? prefill_kernel<1, 1, kPfQ8_0, true> : prefill_kernel<1, 1, kPfQ4_0, true>)
+        : q8 ? (pl.WT == 2 ? prefill_kernel<2, 1, kPfQ8_0, false> : prefill_kernel<1, 1, kPfQ8_0, false>)
+        : pl.WT == 2 ? (pl.cluster > 1 ? prefill_kernel<2, 2, kPfQ4_0, false> : prefill_kernel<2, 1, kPfQ4_0, false>)
+                     : (pl.cluster > 1 ? prefill_kernel<1, 2, kPfQ4_0, false> : prefill_kernel<1, 1, kPfQ4_0, false>);
     cudaError_t e = ensure_smem_optin(reinterpret_cast<const void *>(kernel), pl.smem);
     if (e != cudaSuccess) return e;
-    const dim3 grid(static_cast<unsigned>(pl.grid_x), static_cast<unsigned>(pl.grid_y));
-    return launch_ex_cluster(kernel, grid, dim3(kThreads), pl.smem, s, pdl, pl.cluster, wmap, xmap, p);
+    const dim3 grid(static_cast<unsigned>(pl.grid_x), static_cast<unsigned>(pl.grid_y),
+                    static_cast<unsigned>(pl.splitk));
+    const dim3 cluster(static_cast<unsigned>(pl.cluster), 1, static_cast<unsigned>(pl.splitk));
+    return launch_ex_cluster_dims(kernel, grid, dim3(kThreads), pl.smem, s, pdl, cluster, wmap, xmap, p);
 }
 
 }  // namespace qmv

@@ -11,8 +11,12 @@ namespace qmv {
 
 constexpr int kBM = 128;                 // weight rows per tile (MMA M)
 constexpr int kKB = 64;                  // K per atom: one 128-byte swizzle row of fp16 activations
-constexpr int kKChunk = 256;             // K per packed weight tile (8 Q4_0 blocks = 144 bytes per row)
-constexpr int kPackedRowBytes = 144;
+constexpr int kKChunk = 256;             // K per packed weight tile (8 blocks of 32 weights per row)
+// Packed weight formats the kernel takes, and one row's 256-K chunk in bytes:
+// eight 18-byte Q4_0 blocks or eight 34-byte Q8_0 blocks.
+constexpr int kPfQ4_0 = 0, kPfQ8_0 = 1;
+constexpr int prefill_row_bytes(int fmt) { return fmt == kPfQ8_0 ? 272 : 144; }
+constexpr int kPackedRowBytes = 144;     // Q4_0
 constexpr int kPackedTileBytes = kBM * kPackedRowBytes;    // 18432
 constexpr int kAtomCols = kKB / 2;       // tensor-memory columns of one dequantised 64-K atom (2 fp16 per column)
 constexpr int kTmemCols = 512;           // every CTA allocates all of tensor memory
@@ -26,7 +30,8 @@ constexpr int64_t kMaxGridY = 65535;     // CUDA's limit on gridDim.y
 
 struct PrefillPlan {
     bool ok;           // false: the tensor-core kernel does not take this shape
-    int TN;            // token columns per tile = the MMA's N (multiple of 64, <= 256)
+    int fmt;           // kPfQ4_0 or kPfQ8_0
+    int TN;            // token columns per tile = the MMA's N (16, or a multiple of 64 up to 256)
     int WT;            // 128-row weight tiles per CTA (1 or 2): each activation atom feeds WT MMAs
     int KSUB;          // 64-K atoms per ring slot (1, 2 or 4): MMAs per barrier round = 4 * KSUB * WT
     int NW;            // packed-weight ring slots (256-K chunks of WT tiles)
@@ -38,6 +43,9 @@ struct PrefillPlan {
     size_t smem;       // dynamic shared memory per CTA
     int64_t grid_x;    // CTAs along the weight rows (WT * 128 rows each)
     int64_t grid_y;    // token tiles
+    int splitk;        // CTAs along K (gridDim.z, one cluster): each takes a contiguous share of the
+                       // 256-K chunks, and the cluster adds the partial tiles through distributed
+                       // shared memory in rank order
 };
 
 // Atoms per ring slot: a barrier round carries at least 8 MMAs when it can.
@@ -47,9 +55,10 @@ inline int prefill_ksub(int TN, int WT)
     return k / WT > 0 ? k / WT : 1;
 }
 
+// Accumulators (WT * TN columns, rounded up to 32), then NSA slots of weight atoms.
 inline int64_t prefill_tmem_cols(int TN, int WT, int KSUB, int NSA)
 {
-    return static_cast<int64_t>(WT) * TN + static_cast<int64_t>(NSA) * KSUB * WT * kAtomCols;
+    return (static_cast<int64_t>(WT) * TN + 31) / 32 * 32 + static_cast<int64_t>(NSA) * KSUB * WT * kAtomCols;
 }
 
 // Estimated SM cycles of a call with token tiles of TN and WT weight tiles per
@@ -78,12 +87,20 @@ inline int64_t prefill_cost(int64_t N, int64_t K, int64_t M, int sms, int TN, in
 // tn_force (64..256, a multiple of 64) and wt_force (1 or 2) force the tile,
 // ksub_force (1, 2 or 4) the atoms per ring slot where tensor memory still
 // holds two weight-atom slots (0 keeps the rule).
+//
+// fmt: the packed weight format.  splitk: 0 = one CTA per tile along K;
+// -1 = as many CTAs along K (at most 8, at most one per 256-K chunk) as keep
+// the grid within one wave of `sms`; n > 0 forces n (tests and sweeps; kept
+// within the same limits).  Split K is taken with 16-token tiles only.
 inline PrefillPlan plan_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int ns_force,
-                                int cluster_force = 0, int tn_force = 0, int wt_force = 0, int ksub_force = 0)
+                                int cluster_force = 0, int tn_force = 0, int wt_force = 0, int ksub_force = 0,
+                                int fmt = kPfQ4_0, int splitk = 0)
 {
     PrefillPlan pl = {};
+    pl.fmt = fmt;
+    pl.splitk = 1;
     if (!(K % kKChunk == 0 && K > 0 && N > 0 && M > 0 && N < (int64_t(1) << 31) && M < (int64_t(1) << 31) &&
-          K < (int64_t(1) << 30)))
+          K < (int64_t(1) << 30) && (fmt == kPfQ4_0 || fmt == kPfQ8_0)))
         return pl;
     // Tile choice: the (token tile, weight tiles per CTA) of least estimated
     // time among those tensor memory holds with two weight-atom slots; ties
@@ -91,7 +108,14 @@ inline PrefillPlan plan_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw
     const int64_t m_cover = (M + 63) / 64 * 64;
     int TN = 0, WT = 0;
     int64_t best = 0, best_grid = 0;
-    for (int tn = 64; tn <= 256; tn += 64) {
+    // Up to 16 tokens: 16-token tiles (the MMA's smallest N at M = 128), one
+    // weight tile per CTA.
+    const bool small = M <= 16 && (tn_force == 0 || tn_force == 16) && (wt_force == 0 || wt_force == 1);
+    if (small) {
+        TN = 16;
+        WT = 1;
+    }
+    for (int tn = 64; !small && tn <= 256; tn += 64) {
         if (tn > m_cover && tn > 64) break;
         if (tn_force && tn != tn_force) continue;
         for (int wt = 1; wt <= 2; ++wt) {
@@ -110,7 +134,7 @@ inline PrefillPlan plan_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw
     }
     if (TN == 0) return pl;
     const size_t b_atom = static_cast<size_t>(TN) * kKB * 2;
-    const size_t w_tile = static_cast<size_t>(WT) * kPackedTileBytes;
+    const size_t w_tile = static_cast<size_t>(WT) * kBM * prefill_row_bytes(fmt);
     int KSUB = prefill_ksub(TN, WT);
     if ((ksub_force == 1 || ksub_force == 2 || ksub_force == 4) &&
         prefill_tmem_cols(TN, WT, ksub_force, 2) <= kTmemCols &&
@@ -152,13 +176,27 @@ inline PrefillPlan plan_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw
     // then gets one extra CTA whose rows lie past N (it loads zeros for its
     // weights and stores nothing).
     pl.cluster = 1;
-    if (cluster_force == 1 || cluster_force == 2) pl.cluster = cluster_force;
+    if ((cluster_force == 1 || cluster_force == 2) && fmt == kPfQ4_0) pl.cluster = cluster_force;
     pl.grid_x = (pl.grid_x + pl.cluster - 1) / pl.cluster * pl.cluster;
     pl.grid_y = (M + TN - 1) / TN;
+    // Split K: the cluster's CTAs reduce their partial tiles (128 x TN fp32)
+    // out of their own shared memory, which the partial must fit.
+    const int64_t chunks = K / kKChunk;
+    if (splitk != 0 && TN == 16 && pl.cluster == 1) {
+        int64_t sk = splitk > 0 ? splitk : 8;
+        if (splitk < 0)
+            while (sk > 1 && pl.grid_x * pl.grid_y * sk > sms) --sk;
+        if (sk > 8) sk = 8;
+        if (sk > chunks) sk = chunks;
+        if (sk < 1) sk = 1;
+        pl.splitk = static_cast<int>(sk);
+    }
     // More token tiles than gridDim.y allows (M above 65535 * 256) take the
     // generic kernel rather than a launch the runtime would refuse.
     pl.ok = pl.grid_y <= kMaxGridY && pl.smem <= kPrefillSmemCap &&
-            prefill_tmem_cols(TN, WT, KSUB, NSA) <= kTmemCols;
+            prefill_tmem_cols(TN, WT, KSUB, NSA) <= kTmemCols &&
+            (pl.splitk == 1 || static_cast<size_t>(kBM) * TN * 4 <=
+                                   static_cast<size_t>(NSB) * KSUB * b_atom + static_cast<size_t>(NW) * w_tile);
     return pl;
 }
 
