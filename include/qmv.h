@@ -41,8 +41,11 @@
  * Activations must be finite fp16.  Exceptions, each stated at its
  * declaration: the *_f32 calls take fp32 activations (rounded to fp16 in the
  * kernel), the *_q8_1 calls compute the product on the activations quantised
- * to Q8_1 (their own accuracy statement), and the prefill call rounds each
- * dequantised weight (c - 8) * d to fp16 (so |d| <= 8188 keeps it finite).
+ * to Q8_1 (their own accuracy statement), and the prefill calls -- and the
+ * several-token Q4_0 / Q8_0 decode calls that run on the tensor cores (at
+ * qmv_q4_0) -- round each dequantised weight to fp16 and sum its products in
+ * fp32 (so |d| <= 8188 for Q4_0, |d| <= 511 for Q8_0 keeps every weight
+ * finite; within the 2e-3 bar above).
  *
  * Conventions common to every entry point:
  *   - All array pointers are DEVICE pointers on the current CUDA device, owned
@@ -112,6 +115,15 @@ typedef enum {
  * in shared memory (e.g. 8 tokens of K = 14336 in fp16) the call runs as a
  * few launches over token subsets, each streaming W again.  These rules hold
  * for every decode call below.
+ * Several tokens on the tensor cores (qmv_q4_0 and qmv_q8_0 only): with
+ * K % 256 == 0 and W, x 16-byte aligned, calls of 8 tokens, and of 4..7 tokens
+ * with K >= 2560, run on the prefill kernel's 16-token tiles (the weights
+ * dequantised into tensor memory, fp32 accumulation; split along K over a
+ * cluster of up to 8 CTAs where the 128-row tiles alone would leave SMs idle,
+ * the partial tiles added in a fixed order).  Measured on the GB300 they are
+ * faster there (e.g. Q8_0 12288x2560 at eight tokens 21.9 -> 13.0 us, Q4_0
+ * 4096x14336 43.4 -> 15.3 us); the weight rounding is that of the prefill
+ * call (the preamble).
  * W must not be written by the kernel right before this call on `stream`
  * while programmatic dependent launch is on (see the preamble).
  */
@@ -276,7 +288,10 @@ QMV_API qmv_status qmv_q4_0_swiglu(const void *W_gate, const void *W_up, const v
  *       streaming kernel; otherwise the generic kernel runs).  Every value is
  *       rounded to fp16 (nearest even) before the product, so the results
  *       equal those of qmv_q4_0 / qmv_q4_0_swiglu on x rounded to fp16
- *       (bit-identical: the same kernel runs after staging).  Values must lie
+ *       (bit-identical: the same kernel runs after staging), except where
+ *       qmv_q4_0 takes the tensor cores (several tokens, at qmv_q4_0): this
+ *       call always streams, and the two then agree within the accuracy
+ *       bound.  Values must lie
  *       within fp16's range (|x| < 65520): larger ones round to +-inf.
  *   W, W_gate, W_up, y, N, K, M, errors and asynchrony as for the fp16 calls.
  * Accuracy against the exact product on the fp32 values: the bounds above,

@@ -260,6 +260,12 @@ void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int n
     const size_t bar_off = w_off + static_cast<size_t>(NW) * w_slot;
     const size_t bar_end = bar_off + static_cast<size_t>(2 * NW + 2 * NSA + 2 * NSB + 1) * 8 + 4 + 4;
     CHECK(1023 + bar_end <= pl.smem, "layout %zu + slack > %zu", bar_end, pl.smem);
+    CHECK(bar_end <= bar_off + 512, "barriers within their 512 bytes");
+    if (pl.splitk > 1) {
+        // the split-K receive buffer after the barriers: [SK][ceil(128/SK)][16] fp32, 16-byte rows
+        const size_t red_end = bar_off + 512 + static_cast<size_t>(pl.splitk) * ((kBM + pl.splitk - 1) / pl.splitk) * 64;
+        CHECK(1023 + red_end <= pl.smem && (bar_off + 512) % 16 == 0, "split-K buffer %zu > %zu", red_end, pl.smem);
+    }
     CHECK((bar_off + 1024) >> 4 < (size_t(1) << 14), "descriptor address field");
     for (int s = 0; s < NSB; ++s)
         for (int a = 0; a < KSUB; ++a)
@@ -342,13 +348,14 @@ void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int n
         for (int w = 0; w < warps; ++w)
             if ((w >> 2) == 0) ++ecover[w & 3][0];
         for (int q = 0; q < 4; ++q) CHECK(ecover[q][0] == 1, "epilogue quarter %d read %d times", q, ecover[q][0]);
-        // split K: the partial tile [128][TN] fp32 fits the idle rings, and the
-        // CTAs' row shares cover the 128 rows once
-        CHECK(SK == 1 || static_cast<size_t>(kBM) * TN * 4 <= bar_off, "split-K partial");
+        // split K: the CTAs' row shares cover the 128 rows once, and every row's
+        // owner (as the kernel computes it) holds it
         int rows = 0;
+        const int rmax = (kBM + SK - 1) / SK;
         for (int z = 0; z < SK; ++z) {
             const int r0 = kBM * z / SK, r1 = kBM * (z + 1) / SK;
-            CHECK(r0 == rows && r1 >= r0, "split-K rows %d", z);
+            CHECK(r0 == rows && r1 >= r0 && r1 - r0 <= rmax, "split-K rows %d", z);
+            for (int rl = r0; rl < r1; ++rl) CHECK(((rl + 1) * SK - 1) / kBM == z, "split-K owner of row %d", rl);
             rows = r1;
         }
         CHECK(rows == kBM, "split-K row cover");

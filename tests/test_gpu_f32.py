@@ -127,17 +127,28 @@ def test_f32_swiglu_full_size_sampled(cuda_lib, orc, M):
 # -- bit-identity with the fp16 calls on x rounded to fp16 --------------------------------
 
 @pytest.mark.parametrize("N,K,M", [(1000, 2048, 1), (515, 2560, 3), (4096, 4096, 8), (45, 640, 2), (7, 96, 1)])
-def test_f32_equals_fp16_call_on_rounded_x(cuda_lib, N, K, M):
+def test_f32_equals_fp16_call_on_rounded_x(cuda_lib, orc, N, K, M):
     q = cuda_lib
-    W = dev(synth.q4_0_weights(N, K, 550 + K))
-    x = dev(x32(M, K, 551 + M, plant="large"))
+    W_host = synth.q4_0_weights(N, K, 550 + K)
+    x_host = x32(M, K, 551 + M, plant="large")
+    W = dev(W_host)
+    x = dev(x_host)
     y32 = q.qmv_q4_0_f32(W, x)
     y16 = q.qmv_q4_0(W, x.half())
     Wu = dev(synth.q4_0_weights(N, K, 552 + K))
     s32 = q.qmv_q4_0_swiglu_f32(W, Wu, x)
     s16 = q.qmv_q4_0_swiglu(W, Wu, x.half())
     torch.cuda.synchronize()
-    assert torch.equal(y32, y16) and torch.equal(s32, s16)
+    assert torch.equal(s32, s16)
+    if M >= 4 and K % 256 == 0:
+        # qmv_q4_0 may take the tensor cores at several tokens (the header's
+        # rule); the fp32 call always streams: both within the bound of the
+        # exact product on the rounded x
+        y_ref, S = orc.qmv(0, W_host, x_host.astype(np.float16), N, K, nthreads=8)
+        assert H.normalised_error(y32.cpu().numpy(), y_ref, S) <= H.TOL
+        assert H.normalised_error(y16.cpu().numpy(), y_ref, S) <= H.TOL
+    else:
+        assert torch.equal(y32, y16)
 
 
 # -- edges ----------------------------------------------------------------------------

@@ -410,6 +410,11 @@ OVERRIDES = {
                               "q81:q4_0:515:2560:7", "swiglu:q4_0:300:2048:5"],
     # the fused SwiGLU keeps an even number of rows per group (G clamped to <= 16)
     "G=32": ["swiglu:q4_0:77:4096:1", "swiglu:q4_0:40:2048:8"],
+    # the streaming kernel's own launch rule at the token counts the tensor cores
+    # otherwise take (these tests run with that path off), including the token
+    # split of eight tokens of K = 14336 into several launches
+    "early=1": ["gemv:q4_0:4096:4096:8", "gemv:q8_0:2560:6144:4", "gemv:q8_0:12288:2560:8",
+                "gemv:q4_0:4096:14336:8", "gemv:q4_0:515:2560:5"],
 }
 
 
@@ -419,7 +424,8 @@ def test_launch_overrides(orc, tmp_path, tune):
     import subprocess
     import sys
     out = tmp_path / "y.npz"
-    env = dict(os.environ, QMV_GEMV_TUNE=tune)
+    # the streaming kernel at every token count (no tensor-core path)
+    env = dict(os.environ, QMV_GEMV_TUNE=tune, QMV_TC_MIN_TOKENS="0")
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     r = subprocess.run([sys.executable, "-m", "tests._launch_override_child", str(out)] + OVERRIDES[tune],
                        env=env, cwd=root, capture_output=True, text=True, timeout=600)

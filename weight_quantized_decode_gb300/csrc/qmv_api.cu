@@ -331,6 +331,27 @@ cudaError_t launch_streaming(int fmt, const GemvParams &p0, int M, const Plan &p
     return launch_gemv_stream_q8_0(M, p, pl.grid, pl.warps, pl.smem, stream, pdl);
 }
 
+// Whether a plain Q4_0 / Q8_0 decode call of M tokens goes to the tensor
+// cores.  Measured on the GB300 (us per call back to back, streaming kernel
+// against tensor cores): eight tokens, the tensor cores win on every table
+// (Q8_0 12288x2560 21.9 -> 13.0, 2560x6144 24.0 -> 9.1, 8192x2048 12.6 -> 9.3;
+// Q4_0 4096x14336 43.4 -> 15.3, 128256x4096 193 -> 107); four tokens they win
+// from K = 2560 up (Q8_0 12288x2560 14.3 -> 13.0, 2560x6144 10.5 -> 9.1;
+// Q4_0 4096x14336 21.7 -> 15.3) and lose below (Q8_0 8192x2048 8.0 against
+// 9.3); two tokens the streaming kernel wins.  QMV_TC_MIN_TOKENS=n replaces
+// the rule by "n tokens or more" for sweeps (0 or above 8: never).
+bool tc_route(int64_t K, int M)
+{
+    static const int forced = [] {
+        const char *e = std::getenv("QMV_TC_MIN_TOKENS");
+        if (!e) return -1;
+        const int n = std::atoi(e);
+        return (n >= 1 && n <= 8) ? n : 1 << 20;
+    }();
+    if (forced >= 0) return M >= forced;
+    return M >= 8 || (M >= 4 && K >= 2560);
+}
+
 qmv_status run_gemv(int fmt, const void *W, const int32_t *idx, int64_t n_experts, const void *x, float *y,
                     int64_t N, int64_t K, int64_t M, int n_problems, cudaStream_t stream, const void *W2 = nullptr,
                     const float *xf = nullptr, bool xq8 = false, const int8_t *xq = nullptr,
@@ -367,6 +388,21 @@ qmv_status run_gemv(int fmt, const void *W, const int32_t *idx, int64_t n_expert
     const bool pdl = g_pdl.load(std::memory_order_relaxed) != 0;
 
     cudaError_t e;
+    // Several tokens of a plain Q4_0 / Q8_0 GEMV on the tensor cores (the
+    // prefill kernel's 16-token tiles, split along K over a cluster where the
+    // weight tiles alone leave SMs idle) where tc_route() says they win.
+    if (n_problems == 1 && !W2 && !xf && !xq8 && (fmt == kQ4_0 || fmt == kQ8_0) && tc_route(K, Mk) &&
+        K % 256 == 0 && aligned(W, 16) && aligned(x, 16)) {
+        const PrefillPlan pp = prefill_plan(N, K, M, sms, fmt == kQ8_0 ? kPfQ8_0 : kPfQ4_0, -1);
+        if (pp.ok && pp.TN == 16) {
+            e = launch_prefill(pp, W, x, y, N, K, M, status, stream, pdl, test_skip_this_launch(kArmDecode));
+            if (e != cudaSuccess) {
+                (void)cudaGetLastError();
+                return QMV_ERR_LAUNCH;
+            }
+            return QMV_OK;
+        }
+    }
     GemvParams p0 = p;
     Plan pl = plan_gemv(fmt, p, Mk, sms, optin);
     if (!pl.streaming && Mk > 1 && n_problems == 1) {

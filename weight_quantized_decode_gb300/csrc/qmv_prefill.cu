@@ -47,7 +47,9 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "../../include/qmv.h"
 #include "qmv_common.cuh"
@@ -351,14 +353,17 @@ __device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, uint32_t (&v)[16]
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// A float at this shared-memory location of cluster CTA `rank`.
-__device__ __forceinline__ float ld_cluster_f32(const float *local, uint32_t rank)
+// Sixteen floats (16-byte aligned) to this shared-memory location of cluster
+// CTA `rank`.
+__device__ __forceinline__ void st_cluster_f32x16(const float *local, uint32_t rank, const uint32_t (&v)[16])
 {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(remote + 16u * i), "r"(v[4 * i]),
+                     "r"(v[4 * i + 1]), "r"(v[4 * i + 2]), "r"(v[4 * i + 3])
+                     : "memory");
 }
 
 // SMALL: 16-token tiles (one weight tile, no multicast), which may be split
@@ -401,6 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *accfull = bempty + NSB;   // [1]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accfull + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    // split K: the receive buffer for other CTAs' partial rows (16-token tiles)
+    float *red_buf = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(bars) + 512);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -900,9 +907,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int rl = 32 * quarter + lane;
                 const int64_t row = n0 + rl;
                 if (gridDim.z > 1) {
-                    float *part = reinterpret_cast<float *>(smem) + rl * TN;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) part[i] = __uint_as_float(v[i]);
+                    // split K: store this partial row into its owner's receive
+                    // buffer, slot of this CTA's rank
+                    const int sk = static_cast<int>(gridDim.z);
+                    const int owner = ((rl + 1) * sk - 1) / kBM;
+                    const int rmax = (kBM + sk - 1) / sk;
+                    const float *dst = red_buf + (static_cast<int>(blockIdx.z) * rmax + (rl - kBM * owner / sk)) * 16;
+                    st_cluster_f32x16(dst, static_cast<uint32_t>(owner), v);
                 } else if (row < p.N) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
@@ -930,23 +941,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     if (SMALL && gridDim.z > 1) {
-        // Split K (16-token tiles, one cluster along z): once every CTA's
-        // partial is in its shared memory, CTA z adds rows [128 z / SK,
-        // 128 (z + 1) / SK) of all of them in rank order (the same order on
-        // every call) and stores y; the second barrier keeps each CTA's shared
-        // memory alive until the others have read it.
+        // Split K (16-token tiles, one cluster along z): every CTA has stored
+        // its partial rows into their owners' receive buffers (rows [128 z /
+        // SK, 128 (z + 1) / SK) belong to CTA z); after the cluster barrier
+        // CTA z adds its rows' partials in rank order (the same order on every
+        // call) from its own shared memory and stores y.  Nothing reads another
+        // CTA's shared memory after the barrier, so one barrier suffices.
         cluster_sync();
         const int sk = static_cast<int>(gridDim.z), z = static_cast<int>(blockIdx.z);
         const int r0 = kBM * z / sk, nr = kBM * (z + 1) / sk - r0;
-        const float *part = reinterpret_cast<const float *>(smem);
-        for (int i = threadIdx.x; i < nr * TN; i += blockDim.x) {
-            const int col = i / nr, rl = r0 + (i - col * nr);
+        const int rmax = (kBM + sk - 1) / sk;
+        for (int i = threadIdx.x; i < nr * 16; i += blockDim.x) {
+            const int col = i / nr, rr = i - col * nr;
             float acc = 0.0f;
-            for (int q = 0; q < sk; ++q) acc += ld_cluster_f32(part + rl * TN + col, static_cast<uint32_t>(q));
-            const int64_t row = n0 + rl, m = m0 + col;
+            for (int q = 0; q < sk; ++q) acc += red_buf[(q * rmax + rr) * 16 + col];
+            const int64_t row = n0 + r0 + rr, m = m0 + col;
             if (ok && row < p.N && m < p.M) p.y[m * p.N + row] = acc;
         }
-        cluster_sync();
     }
 
     tc_fence_before();
@@ -1026,12 +1037,61 @@ int ring_override(int which)
 
 }  // namespace
 
+namespace {
+
+// Clusters of `sk` CTAs along z (16-token tiles of format `fmt`, `smem` bytes
+// each) the device can hold at once: a cluster's CTAs must share one GPC, so
+// sizes that do not pack its SMs leave some idle (measured: 20 tiles split 7
+// ways, 140 CTAs, ran as two waves).  Cached per (format, size, bytes).
+int max_active_clusters(int fmt, int sk, size_t smem)
+{
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, size_t, int>, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const auto key = std::make_tuple(fmt, sk, smem, dev);
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    const void *k = fmt == kPfQ8_0 ? reinterpret_cast<const void *>(prefill_kernel<1, 1, kPfQ8_0, true>)
+                                   : reinterpret_cast<const void *>(prefill_kernel<1, 1, kPfQ4_0, true>);
+    int n = 0;
+    if (ensure_smem_optin(k, smem) == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1, 1, static_cast<unsigned>(sk));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = static_cast<unsigned>(sk);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) n = 0;
+    }
+    (void)cudaGetLastError();
+    std::lock_guard<std::mutex> lk(mu);
+    cache[key] = n;
+    return n;
+}
+
+}  // namespace
+
 PrefillPlan prefill_plan(int64_t N, int64_t K, int64_t M, int sms, int fmt, int splitk)
 {
     const int sk_force = ring_override(6);
-    PrefillPlan pl = plan_prefill(N, K, M, sms, ring_override(0), ring_override(1), ring_override(2),
-                                  ring_override(3), ring_override(4), ring_override(5), fmt,
-                                  sk_force > 0 ? sk_force : splitk);
+    auto plan = [&](int sk) {
+        return plan_prefill(N, K, M, sms, ring_override(0), ring_override(1), ring_override(2), ring_override(3),
+                            ring_override(4), ring_override(5), fmt, sk);
+    };
+    PrefillPlan pl = plan(sk_force > 0 ? sk_force : splitk);
+    // An automatic split keeps every cluster of the grid resident at once.
+    if (sk_force <= 0 && splitk < 0)
+        while (pl.ok && pl.splitk > 1 && pl.grid_x * pl.grid_y > max_active_clusters(fmt, pl.splitk, pl.smem))
+            pl = plan(pl.splitk - 1);
     if (encode_fn() == nullptr) pl.ok = false;
     return pl;
 }

@@ -25,6 +25,10 @@ constexpr int kPrefillThreads = 352;     // 11 warps: 8 dequantising, MMA issue,
 // barriers (2*NW + 2*NSA + 2*NSB + 1 of 8 bytes), the tensor-memory address
 // slot and the abort flag.
 constexpr size_t kPrefillFixedSmem = 1024 + 512;
+// Split K: each CTA receives the other CTAs' partial rows of its share in a
+// buffer after the barriers' 512 bytes, [SK][ceil(128 / SK)][16] fp32 (16-token
+// tiles): at most 135 rows of 64 bytes.
+constexpr size_t kPrefillSplitSmem = 135 * 64;
 constexpr size_t kPrefillSmemCap = 225 * 1024;
 constexpr int64_t kMaxGridY = 65535;     // CUDA's limit on gridDim.y
 
@@ -179,8 +183,8 @@ inline PrefillPlan plan_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw
     if ((cluster_force == 1 || cluster_force == 2) && fmt == kPfQ4_0) pl.cluster = cluster_force;
     pl.grid_x = (pl.grid_x + pl.cluster - 1) / pl.cluster * pl.cluster;
     pl.grid_y = (M + TN - 1) / TN;
-    // Split K: the cluster's CTAs reduce their partial tiles (128 x TN fp32)
-    // out of their own shared memory, which the partial must fit.
+    // Split K: CTA z of the cluster adds rows [128 z / SK, 128 (z + 1) / SK) of
+    // every CTA's partial tile, which the others store into its shared memory.
     const int64_t chunks = K / kKChunk;
     if (splitk != 0 && TN == 16 && pl.cluster == 1) {
         int64_t sk = splitk > 0 ? splitk : 8;
@@ -191,12 +195,11 @@ inline PrefillPlan plan_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw
         if (sk < 1) sk = 1;
         pl.splitk = static_cast<int>(sk);
     }
+    if (pl.splitk > 1) pl.smem += kPrefillSplitSmem;
     // More token tiles than gridDim.y allows (M above 65535 * 256) take the
     // generic kernel rather than a launch the runtime would refuse.
     pl.ok = pl.grid_y <= kMaxGridY && pl.smem <= kPrefillSmemCap &&
-            prefill_tmem_cols(TN, WT, KSUB, NSA) <= kTmemCols &&
-            (pl.splitk == 1 || static_cast<size_t>(kBM) * TN * 4 <=
-                                   static_cast<size_t>(NSB) * KSUB * b_atom + static_cast<size_t>(NW) * w_tile);
+            prefill_tmem_cols(TN, WT, KSUB, NSA) <= kTmemCols;
     return pl;
 }
 
