@@ -308,33 +308,54 @@ void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int n
     // W rows of the last CTA's tiles (rows past N read zeros)
     CHECK((pl.grid_x - 1) * rows_per_cta + (WT - 1) * kBM <= INT32_MAX, "W y");
 
-    // dequantising warps 0..7: reads of the packed slot; tensor-memory writes
-    static unsigned char cover[kBM][kAtomCols];
+    // dequantising warps: reads of the packed slot; tensor-memory writes.  With
+    // 8 warps (the rule's tiles), warp w writes block half w / 4 of every atom;
+    // with 16 (16-token tiles: one slot per 256-K chunk of one weight tile),
+    // warp w writes blocks w / 4 and w / 4 + 4 of the chunk (atom b / 2, half
+    // b mod 2), reading only those blocks' words.
+    const bool small = TN == 16;
+    CHECK(!small || (KSUB == 4 && WT == 1), "16-token tiles: one slot per chunk of one tile");
+    const int dq = small ? 16 : 8;
+    static unsigned char cover[4][kBM][kAtomCols];
     for (int s = 0; s < NSA; ++s)
-        for (int a = 0; a < KSUB; ++a)
-            for (int t = 0; t < WT; ++t) {
-                std::fill(&cover[0][0], &cover[0][0] + kBM * kAtomCols, 0);
+        for (int t = 0; t < WT; ++t) {
+            std::fill(&cover[0][0][0], &cover[0][0][0] + 4 * kBM * kAtomCols, 0);
+            auto mark = [&](int w, int a, int half) {
+                const int quarter = w & 3;
                 const int64_t base = a0 + static_cast<int64_t>((s * KSUB + a) * WT + t) * kAtomCols;
-                for (int w = 0; w < 8; ++w) {
-                    const int quarter = w & 3, hsel = w >> 2;
-                    for (int lane = 0; lane < 32; ++lane) {
-                        const int r = 32 * quarter + lane;
-                        CHECK(r / 32 == (w & 3), "lane quarter of warp %d", w);
-                        CHECK(static_cast<size_t>(NW - 1) * w_slot + static_cast<size_t>(t) * kPackedTileBytes +
-                                      r * kPackedRowBytes + 16 * 8 + 16 <=
-                                  static_cast<size_t>(NW) * w_slot,
-                              "packed read");
-                        const int64_t c0 = base + 16 * hsel;
-                        CHECK(c0 >= a0 && c0 % 16 == 0 && base % 32 == 0 && c0 + 16 <= a_end, "A columns");
-                        for (int j = 0; j < 16; ++j) ++cover[r][16 * hsel + j];
-                    }
+                for (int lane = 0; lane < 32; ++lane) {
+                    const int r = 32 * quarter + lane;
+                    CHECK(r / 32 == (w & 3), "lane quarter of warp %d", w);
+                    CHECK(static_cast<size_t>(NW - 1) * w_slot + static_cast<size_t>(t) * kBM * row_b +
+                                  static_cast<size_t>(r) * row_b + row_b <=
+                              static_cast<size_t>(NW) * w_slot,
+                          "packed read");
+                    const int64_t c0 = base + 16 * half;
+                    CHECK(c0 >= a0 && c0 % 16 == 0 && base % 32 == 0 && c0 + 16 <= a_end, "A columns");
+                    for (int j = 0; j < 16; ++j) ++cover[a][r][16 * half + j];
                 }
+            };
+            if (!small) {
+                for (int w = 0; w < dq; ++w)
+                    for (int a = 0; a < KSUB; ++a) mark(w, a, w >> 2);
+            } else {
+                for (int w = 0; w < dq; ++w)
+                    for (int k = 0; k < 2; ++k) {
+                        const int b = (w >> 2) + 4 * k;
+                        const int words = fmt == kPfQ8_0 ? 17 * (b >> 1) + 8 * (b & 1) + 9 : 9 * (b >> 1) + 4 * (b & 1) + 5;
+                        CHECK(4 * words <= row_b, "block %d words", b);
+                        mark(w, b >> 1, b & 1);
+                    }
+            }
+            for (int a = 0; a < KSUB; ++a) {
                 for (int r = 0; r < kBM; ++r)
                     for (int c = 0; c < kAtomCols; ++c)
-                        CHECK(cover[r][c] == 1, "A cell %d,%d written %d times", r, c, cover[r][c]);
+                        CHECK(cover[a][r][c] == 1, "A cell %d,%d written %d times", r, c, cover[a][r][c]);
                 // the MMAs of this atom read columns [base, base + 32) in four K = 16 steps of 8 columns
+                const int64_t base = a0 + static_cast<int64_t>((s * KSUB + a) * WT + t) * kAtomCols;
                 for (int k = 0; k < 4; ++k) CHECK(base + 8 * k + 8 <= a_end, "MMA A columns");
             }
+        }
     for (int t = 0; t < WT; ++t) CHECK(static_cast<int64_t>(t + 1) * TN <= a0, "accumulator %d", t);
     if (fmt == kPfQ4_0)
         for (int sub = 0; sub < 4; ++sub) CHECK(4 * (9 * sub + 8) + 4 <= kPackedRowBytes, "block words");
@@ -342,7 +363,7 @@ void check_prefill(int64_t N, int64_t K, int64_t M, int sms, int nw_force, int n
     // epilogue: each (lane quarter, 32-column chunk) read by exactly one warp, inside the accumulators
     static unsigned char ecover[4][16];
     std::fill(&ecover[0][0], &ecover[0][0] + 64, 0);
-    const int warps = kPrefillThreads / 32;
+    const int warps = prefill_threads(TN == 16) / 32;
     if (TN < 32) {
         // 16-token tiles: the first warp of each lane quarter reads its 16 columns
         for (int w = 0; w < warps; ++w)

@@ -61,9 +61,11 @@ namespace qmv {
 
 namespace {
 
-constexpr int kThreads = kPrefillThreads;   // 11 warps: 8 dequantising, MMA issue, 2 copy producers
-constexpr int kDeqWarps = 8;                // warps 0..7
-constexpr int kMmaWarp = 8, kWProducerWarp = 9, kXProducerWarp = 10;
+// Threads of a CTA: the dequantising warps (8; 16 in the 16-token tiles,
+// whose kernels need few registers and whose slots are whole 256-K chunks),
+// then the MMA warp and the two copy producers.
+constexpr int kThreads = kPrefillThreads;                          // 11 warps
+constexpr int kThreadsSmall = prefill_threads(true);               // 19 warps
 
 struct PrefillParams {
     const uint8_t *x;  // the activations (fp16 [M][K]): only for the L2 prefetch, the tiles come by TMA
@@ -369,7 +371,7 @@ __device__ __forceinline__ void st_cluster_f32x16(const float *local, uint32_t r
 // SMALL: 16-token tiles (one weight tile, no multicast), which may be split
 // along K over a cluster; the other tiles compile without that code.
 template <int WT, int CL, int FMT, bool SMALL>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(SMALL ? kThreadsSmall : kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                    const PrefillParams p)
 {
@@ -409,6 +411,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // split K: the receive buffer for other CTAs' partial rows (16-token tiles)
     float *red_buf = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(bars) + 512);
 
+    constexpr int kDeqWarps = SMALL ? 16 : 8;                  // warps 0 .. kDeqWarps-1
+    constexpr int kMmaWarp = kDeqWarps, kWProducerWarp = kDeqWarps + 1, kXProducerWarp = kDeqWarps + 2;
+    constexpr int kWarps = kDeqWarps + 3;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 #ifdef QMV_PHASE_STAMPS
@@ -626,6 +631,111 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (!ok && committed > 0 && lane == 0) mbar_wait_bounded(accfull, 0, nullptr);
+    } else if constexpr (SMALL) {
+        // ---------------- dequantising warps 0..15, 16-token tiles ----------------
+        // One weight tile and one ring slot per 256-K chunk.  Four warps per
+        // tensor-memory lane quarter (warp w writes lanes 32 * (w mod 4) .. +31):
+        // part p = w / 4 dequantises blocks p and p + 4 of the chunk (atoms
+        // p / 2 and p / 2 + 2, half p mod 2), loading only those blocks' words.
+        constexpr int kBW = FMT == kPfQ8_0 ? 9 : 5;   // 32-bit words holding one block
+        const int quarter = warp & 3;
+        const int part = warp >> 2;
+        const int r = 32 * quarter + lane;         // weight row within the tile
+        const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
+        int slot = 0, sa = 0;
+        uint32_t wpar = 0, apar = 1;
+#ifdef QMV_PHASE_STAMPS
+        int jd = 0;   // ring rounds published (trace only)
+#endif
+        for (int c = 0; ok && c < nC; ++c) {
+            if (!warp_wait_or_abort(&wfull[slot], wpar, abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+#ifdef QMV_PHASE_STAMPS
+            if (warp == 0 && lane == 0) QMV_TRACE(jd, 6);
+#endif
+            const uint32_t *row = reinterpret_cast<const uint32_t *>(w_tiles + slot * w_slot_bytes + r * kRowB);
+            uint32_t v[2][kBW];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int b = part + 4 * k;   // block of the chunk
+                // Q4_0: 18-byte blocks, block b from word 9 (b / 2) + 4 (b mod 2);
+                // Q8_0: 34-byte blocks, from word 17 (b / 2) + 8 (b mod 2)
+                const uint32_t *w = row + (FMT == kPfQ8_0 ? 17 * (b >> 1) + 8 * (b & 1) : 9 * (b >> 1) + 4 * (b & 1));
+#pragma unroll
+                for (int i = 0; i < kBW; ++i) v[k][i] = w[i];
+            }
+            // Hand the slot back once this thread's reads of it are done (the
+            // words consumed into a register; fence.proxy.async orders the
+            // generic-proxy reads before the producer's next copy).
+            {
+                uint32_t x = 0u;
+#pragma unroll
+                for (int k = 0; k < 2; ++k)
+#pragma unroll
+                    for (int i = 0; i < kBW; ++i) x ^= v[k][i];
+                asm volatile("" ::"r"(x) : "memory");
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&wempty[slot]);
+            if (++slot == NW) {
+                slot = 0;
+                wpar ^= 1u;
+            }
+            uint32_t f2[2][16];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                if constexpr (FMT == kPfQ8_0) {
+                    if ((part & 1) == 0)
+                        dequant_block_q8_f16<true>(v[k], f2[k]);
+                    else
+                        dequant_block_q8_f16<false>(v[k], f2[k]);
+                } else {
+                    uint32_t q[4], dbits;
+                    if ((part & 1) == 0) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) q[i] = __byte_perm(v[k][i], v[k][i + 1], 0x5432);
+                        dbits = v[k][0] & 0xffffu;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) q[i] = v[k][i + 1];
+                        dbits = v[k][0] >> 16;
+                    }
+                    dequant_block_f16(dbits, q, f2[k]);
+                }
+            }
+#ifdef QMV_PHASE_STAMPS
+            if (warp == 0 && lane == 0) QMV_TRACE(jd, 7);
+#endif
+            if (!warp_wait_or_abort(&aempty[sa], apar, abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+#ifdef QMV_PHASE_STAMPS
+            if (warp == 0 && lane == 0) QMV_TRACE(jd, 4);
+#endif
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int b = part + 4 * k;
+                tmem_st_16cols(tmem_a0 + lane_base + static_cast<uint32_t>((sa * 4 + (b >> 1)) * kAtomCols + 16 * (b & 1)),
+                               f2[k]);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&afull[sa]);
+#ifdef QMV_PHASE_STAMPS
+            if (warp == 0 && lane == 0) QMV_TRACE(jd, 5);
+            ++jd;
+#endif
+            if (++sa == NSA) {
+                sa = 0;
+                apar ^= 1u;
+            }
+        }
     } else if constexpr (FMT == kPfQ8_0) {
         // ---------------- dequantising warps 0..7, Q8_0 ----------------
         // The same split as for Q4_0 (warp w: lane quarter w mod 4, block
@@ -895,7 +1005,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (threadIdx.x == 0) phs[4] = global_timer_ns();
 #endif
         const int quarter = warp & 3;
-        const int nq = (kThreads / 32 - quarter + 3) / 4;   // warps in this quarter
+        const int nq = (kWarps - quarter + 3) / 4;   // warps in this quarter
         const int rank = warp >> 2;
         if constexpr (SMALL) {
             // 16-token tiles: the first warp of each lane quarter reads its 16
@@ -1061,7 +1171,7 @@ int max_active_clusters(int fmt, int sk, size_t smem)
     if (ensure_smem_optin(k, smem) == cudaSuccess) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(1, 1, static_cast<unsigned>(sk));
-        cfg.blockDim = dim3(kThreads);
+        cfg.blockDim = dim3(kThreadsSmall);
         cfg.dynamicSmemBytes = smem;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1165,7 +1275,8 @@ cudaError_t launch_prefill(const PrefillPlan &pl, const void *W, const void *x, 
     const dim3 grid(static_cast<unsigned>(pl.grid_x), static_cast<unsigned>(pl.grid_y),
                     static_cast<unsigned>(pl.splitk));
     const dim3 cluster(static_cast<unsigned>(pl.cluster), 1, static_cast<unsigned>(pl.splitk));
-    return launch_ex_cluster_dims(kernel, grid, dim3(kThreads), pl.smem, s, pdl, cluster, wmap, xmap, p);
+    return launch_ex_cluster_dims(kernel, grid, dim3(pl.TN == 16 ? kThreadsSmall : kThreads), pl.smem, s, pdl,
+                                  cluster, wmap, xmap, p);
 }
 
 }  // namespace qmv

@@ -20,7 +20,10 @@ constexpr int kPackedRowBytes = 144;     // Q4_0
 constexpr int kPackedTileBytes = kBM * kPackedRowBytes;    // 18432
 constexpr int kAtomCols = kKB / 2;       // tensor-memory columns of one dequantised 64-K atom (2 fp16 per column)
 constexpr int kTmemCols = 512;           // every CTA allocates all of tensor memory
-constexpr int kPrefillThreads = 352;     // 11 warps: 8 dequantising, MMA issue, 2 copy producers
+// Threads of a CTA: 8 dequantising warps (16 in 16-token tiles), the MMA warp
+// and the two copy producers.
+constexpr int prefill_threads(bool small) { return ((small ? 16 : 8) + 3) * 32; }
+constexpr int kPrefillThreads = prefill_threads(false);
 // Alignment slack for the 1024-byte-aligned activation tiles, then the
 // barriers (2*NW + 2*NSA + 2*NSB + 1 of 8 bytes), the tensor-memory address
 // slot and the abort flag.
