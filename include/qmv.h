@@ -317,6 +317,8 @@ QMV_API qmv_status qmv_q4_0_swiglu_f32(const void *W_gate, const void *W_up, con
  *   0 <= M <= 2^24 (QMV_ERR_SHAPE above).  Above 65535 * 256 tokens the
  *   token tiles would exceed the grid's y limit, and the generic kernel takes
  *   the call.
+ * W must not be written by the kernel right before this call on `stream`
+ * while programmatic dependent launch is on (see the preamble).
  */
 QMV_API qmv_status qmm_q4_0_prefill(const void *W, const void *x, float *y,
                             int64_t N, int64_t K, int64_t M, qmv_stream_t stream);
@@ -329,6 +331,8 @@ QMV_API qmv_status qmm_q4_0_prefill(const void *W, const void *x, float *y,
  *   W : Q8_0 bytes [N][K/32*34], 16-byte aligned.  The tensor-core kernel
  *       takes K % 256 == 0; other K take the generic kernel.
  *   x, y, M, errors and asynchrony as for qmm_q4_0_prefill.
+ * W must not be written by the kernel right before this call on `stream`
+ * while programmatic dependent launch is on (see the preamble).
  */
 QMV_API qmv_status qmm_q8_0_prefill(const void *W, const void *x, float *y,
                             int64_t N, int64_t K, int64_t M, qmv_stream_t stream);
