@@ -1,7 +1,8 @@
-// qmv_prefill.cu -- Q4_0 prefill GEMM on the 5th-generation tensor cores
-// (tcgen05.mma with fp32 accumulators in tensor memory), sm_103a.
+// qmv_prefill.cu -- Q4_0 / Q8_0 prefill GEMM on the 5th-generation tensor
+// cores (tcgen05.mma with fp32 accumulators in tensor memory), sm_103a; also
+// the several-token decode calls the launch rule sends here.
 //
-//   y[m][n] = sum_k x[m][k] * w[n][k]     (many tokens m; W in GGUF Q4_0)
+//   y[m][n] = sum_k x[m][k] * w[n][k]     (tokens m; W in GGUF Q4_0 or Q8_0)
 //
 // Prior art on the pages: the bakeoff's tc_q4 contender, which dequantises a
 // weight tile into shared memory and multiplies it with 16x16x16 WMMA
@@ -10,35 +11,37 @@
 // multiply itself).  The GB300 form:
 //
 //   * One CTA computes a 128-row (weights) x TN-column (tokens) tile of y^T in
-//     tensor memory: weights are the MMA's M side (128 lanes), tokens its N
-//     side (TN <= 256 columns of fp32).
+//     tensor memory (one or two such weight tiles): weights are the MMA's M
+//     side (128 lanes), tokens its N side (16, or 64..256 columns of fp32).
 //   * The dequantised weights never touch shared memory: the dequantising
 //     warps write them straight into tensor memory (tcgen05.st), and the MMA
 //     reads its A operand from there.  Shared memory then carries only the
-//     packed weights and the activation tiles, so the tensor core's operand
-//     reads and the copies into shared memory no longer compete with a
-//     round trip of the dequantised tile (which had made the kernel bound by
-//     shared-memory bandwidth rather than by the tensor pipe).
-//   * Roles by warp: warps 0..7 dequantise (warp w writes tensor-memory lane
-//     quarter w mod 4 -- the only lanes its sub-partition can reach -- and
-//     blocks of parity w / 4); warp 8 allocates tensor memory and one of its
-//     threads issues the MMAs; warp 9 streams packed 128-row x 256-K Q4_0
-//     tiles (144 bytes per row) and warp 10 streams 64-K activation tiles, both
-//     with TMA tensor copies, into their own shared-memory rings (deep enough
-//     to cover DRAM / L2 latency); the activation tiles land in the
-//     128-byte-swizzled K-major layout the tensor core reads.
-//   * Dequantisation uses the fp16 0x6400|n bit trick, w = (c - 8) * d, one
-//     32-weight block per thread and atom, stored as 16 columns of half2.
-//   * One thread issues tcgen05.mma (kind::f16, 128 x TN x 16, A from tensor
-//     memory) four times per 64-K atom; a ring slot holds KSUB atoms (4, 2 or
-//     1 for 64-, 128- and wider token tiles); tcgen05.commit releases the
-//     slot's activation tile and weight atoms, and finally signals the
-//     epilogue.
-//   * All warps read the accumulator with tcgen05.ld (32 lanes x 32 columns
-//     per instruction; warp w reads lane quarter w mod 4, the warps of a
-//     quarter split the columns) and store y with coalesced fp32 stores.
-// Operands are fp16: the activations arrive as fp16 and the dequantised
-// weight (c - 8) * d is rounded once to fp16.  Every wait is bounded.
+//     packed weights and the activation tiles.
+//   * Roles by warp: the dequantising warps (8; 16 in 16-token tiles) -- warp
+//     w writes tensor-memory lane quarter w mod 4, the only lanes its
+//     sub-partition can reach; then the MMA warp, which allocates tensor memory
+//     and issues the MMAs from one elected lane; then two copy producers, one
+//     streaming packed 128-row x 256-K weight tiles (144 bytes per row for
+//     Q4_0, 272 for Q8_0) and one 64-K activation tiles, with TMA tensor
+//     copies into their own shared-memory rings; the activation tiles land in
+//     the 128-byte-swizzled K-major layout the tensor core reads.  The MMA and
+//     copy loops run as whole warps (warp-collective waits, an elected issuer).
+//   * Dequantisation uses fp16 bit tricks (Q4_0: 0x6400|n, w = (c - 8) * d;
+//     Q8_0: 0x64 above the sign-flipped code, w = q * d), one 32-weight block
+//     per thread and atom, computed before the wait for its tensor-memory slot
+//     and stored as 16 columns of half2.
+//   * tcgen05.mma (kind::f16, 128 x TN x 16, A from tensor memory) four times
+//     per 64-K atom; a ring slot holds KSUB atoms (4, 2 or 1 for 16/64-, 128-
+//     and wider token tiles); tcgen05.commit releases the slot's activation
+//     tile and weight atoms, and finally signals the epilogue.
+//   * 16-token tiles may split K over a cluster of up to 8 CTAs along z; each
+//     CTA stores its partial rows into their owner's shared memory and the
+//     owner adds them in rank order after one cluster barrier.
+//   * The epilogue reads the accumulators with tcgen05.ld (warp w reads lane
+//     quarter w mod 4, the warps of a quarter split the columns) and stores y
+//     with coalesced fp32 stores.
+// Operands are fp16: the activations arrive as fp16 and each dequantised
+// weight is rounded once to fp16.  Every mbarrier wait is bounded.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
