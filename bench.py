@@ -199,10 +199,23 @@ def traffic_record(workload):
         rec = json.load(open(p)).get(workload)
     except (ValueError, OSError):
         return None
-    family = "prefill" if WORKLOADS.get(workload, {}).get("kind") == "prefill" else "decode"
-    if not rec or rec.get("source_sha") != source_sha(family):
+    if not rec or rec.get("source_sha") != source_sha(source_family(workload)):
         return None
     return rec
+
+
+def source_family(workload):
+    """Which kernel sources a workload's launches come from: the prefill
+    kernel alone, the decode kernels alone, or both (fp16-activation Q4_0 /
+    Q8_0 GEMVs with four tokens or more, whose calls may run on the prefill
+    kernel's 16-token tiles)."""
+    wl = WORKLOADS.get(workload, {})
+    if wl.get("kind") == "prefill":
+        return "prefill"
+    if (wl.get("kind") == "gemv" and wl.get("fmt") in ("q4_0", "q8_0") and "x" not in wl
+            and max(wl.get("M", [1])) >= 4):
+        return "all"
+    return "decode"
 
 
 PREFILL_SOURCES = ("qmv_prefill.cu", "qmv_prefill.h", "qmv_prefill_plan.h", "qmv_common.cuh", "qmv_launch.h")
@@ -210,7 +223,8 @@ PREFILL_SOURCES = ("qmv_prefill.cu", "qmv_prefill.h", "qmv_prefill_plan.h", "qmv
 
 def source_sha(family="decode"):
     """Hash of the kernel sources a traffic record depends on: the prefill
-    kernel's files, or (decode) every other source of the library."""
+    kernel's files, (decode) every other source of the library, or (all)
+    every source."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "weight_quantized_decode_gb300", "csrc")
     for fn in sorted(os.listdir(csrc)):
@@ -219,7 +233,7 @@ def source_sha(family="decode"):
         if family == "prefill":
             if fn not in PREFILL_SOURCES:
                 continue
-        elif fn in ("qmv_prefill.cu", "qmv_prefill_plan.h", "qmv_probe.cu"):
+        elif fn == "qmv_probe.cu" or (family == "decode" and fn in ("qmv_prefill.cu", "qmv_prefill_plan.h")):
             continue
         h.update(open(os.path.join(csrc, fn), "rb").read())
     return h.hexdigest()[:16]

@@ -71,7 +71,6 @@ constexpr int kThreads = kPrefillThreads;                          // 11 warps
 constexpr int kThreadsSmall = prefill_threads(true);               // 19 warps
 
 struct PrefillParams {
-    const uint8_t *x;  // the activations (fp16 [M][K]): only for the L2 prefetch, the tiles come by TMA
     float *y;
     int *status;
     int64_t N, K, M;
@@ -263,14 +262,6 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
             return false;
         }
     }
-}
-
-// Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, bytes a
-// multiple of 16).
-constexpr int64_t kPrefetchUnits = 2048;   // 32 KB per prefetch
-__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // Warp-collective wait_or_abort: every lane calls it and gets the same answer.
@@ -511,22 +502,6 @@ __global__ void __launch_bounds__(SMALL ? kThreadsSmall : kThreads, 1)
         // CTAs; a slot is refilled once every CTA's MMAs have released it.
         // The whole warp runs the loop; one elected lane issues the copies.
         pdl_wait_prior_grid();
-        // The token tile's activation rows are one contiguous range of X.  The
-        // CTAs along the weight tiles each prefetch a share of it into L2 at
-        // once, so that the tile copies of later slots hit L2 instead of
-        // waiting, all at the same moment, for their first touch of HBM.
-        if (elect_one()) {
-            const int64_t rows_here = p.M - m0 < TN ? p.M - m0 : TN;
-            const int64_t units = rows_here * p.K * 2 / 16;              // 16-byte units (K % 256 == 0)
-            const int64_t u0 = units * blockIdx.x / gridDim.x;
-            const int64_t u1 = units * (blockIdx.x + 1) / gridDim.x;
-            const uint8_t *base = p.x + m0 * p.K * 2;
-            for (int64_t u = u0; u < u1; u += kPrefetchUnits) {
-                const int64_t n = u1 - u < kPrefetchUnits ? u1 - u : kPrefetchUnits;
-                prefetch_l2(base + u * 16, static_cast<uint32_t>(n * 16));
-            }
-        }
-        __syncwarp();
         const int rows = TN / CL;
         const int row_off_bytes = static_cast<int>(crank) * rows * 128;
         int issued = 0, s = 0;
@@ -1241,7 +1216,6 @@ cudaError_t launch_prefill(const PrefillPlan &pl, const void *W, const void *x, 
             return cudaErrorInvalidValue;
     }
     PrefillParams p = {};
-    p.x = static_cast<const uint8_t *>(x);
     p.y = y;
     p.status = status;
     p.N = N;
