@@ -317,6 +317,9 @@ QMV_API qmv_status qmv_q4_0_swiglu_f32(const void *W_gate, const void *W_up, con
  *   0 <= M <= 2^24 (QMV_ERR_SHAPE above).  Above 65535 * 256 tokens the
  *   token tiles would exceed the grid's y limit, and the generic kernel takes
  *   the call.
+ * Calls of up to 16 tokens run on 16-token tiles, split along K over a
+ * cluster of up to 8 CTAs where the 128-row tiles alone would leave SMs idle
+ * (the same launch as the several-token decode calls above).
  * W must not be written by the kernel right before this call on `stream`
  * while programmatic dependent launch is on (see the preamble).
  */

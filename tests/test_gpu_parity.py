@@ -466,7 +466,8 @@ def test_launch_overrides(orc, tmp_path, tune):
         assert err <= H.TOL, (tune, case, err)
 
 
-@pytest.mark.parametrize("N,K,M", [(12288, 2560, 512), (8192, 2048, 512), (12288, 2560, 64), (9856, 256, 300)])
+@pytest.mark.parametrize("N,K,M", [(12288, 2560, 512), (8192, 2048, 512), (12288, 2560, 64), (9856, 256, 300),
+                                   (8192, 2048, 64)])
 def test_prefill_repeats_are_bit_identical(cuda_lib, orc, N, K, M):
     """Every slot of every ring is reused many times at these sizes; a copy that
     overtakes a read still in flight shows up as a changed output row."""

@@ -664,7 +664,7 @@ qmv_status run_prefill(int fmt, const void *W, const void *x, float *y, int64_t 
     int *status = nullptr;
     int sms = 0, optin = 0;
     if (device_info(dev, &status, &sms, &optin) != cudaSuccess) return QMV_ERR_CUDA;
-    const PrefillPlan pl = prefill_plan(N, K, M, sms, fmt);
+    const PrefillPlan pl = prefill_plan(N, K, M, sms, fmt, -1);
     if (pl.ok) {
         cudaError_t e = launch_prefill(pl, W, x, y, N, K, M, status, s, g_pdl.load(std::memory_order_relaxed) != 0,
                                        test_skip_this_launch(kArmPrefill));
