@@ -1059,6 +1059,9 @@ __global__ void __launch_bounds__(SMALL ? kThreadsSmall : kThreads, 1)
     if constexpr (CL > 1) cluster_sync();
 #ifdef QMV_PHASE_STAMPS
     if (threadIdx.x == 0 && p.phase) {
+        // the end stamp is taken before the record's slot is claimed: the
+        // atomic's round trip (every CTA on one counter) is not the kernel's
+        const unsigned long long t_end = global_timer_ns();
         const unsigned long long i = atomicAdd(p.phase, 1ull);
         if (i < kPrefillPhaseCap) {
             unsigned long long *rec = p.phase + 1 + i * kPrefillPhaseWords;
@@ -1068,7 +1071,7 @@ __global__ void __launch_bounds__(SMALL ? kThreadsSmall : kThreads, 1)
             rec[3] = phs[2];
             rec[4] = phs[3];
             rec[5] = phs[4];
-            rec[6] = global_timer_ns();
+            rec[6] = t_end;
             rec[7] = phs[6] - phs[5];
         }
     }
