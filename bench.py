@@ -96,6 +96,18 @@ WORKLOADS = {
 }
 
 
+def call_names(workload):
+    """The calls of one step of a workload, in order (as build_calls names them)."""
+    wl = WORKLOADS[workload]
+    if wl["kind"] == "moe":
+        return [f"{slots}x({N}x{K}) of {E}" for (E, slots, N, K) in wl["configs"]]
+    return [f"{N}x{K}/M{M}" for (N, K) in wl["shapes"] for M in wl["M"]]
+
+
+VALUES = ("Q4_0 codes uniform 0..15, d~U[0.005,0.02]; Q8_0 codes U[-127,127], d~U[0.001,0.01]; "
+          "x fp16 N(0,1); seeded")
+
+
 def metric_name(workload):
     wl = WORKLOADS[workload]
     if wl["kind"] == "prefill":
@@ -680,8 +692,7 @@ def run_ours(args, dist, rank, local, world):
         roof["achieved_basis"] = ("algorithmic work of all launches in the timed region / CUDA-event time on the "
                                   "launching stream (per-launch figures in 'sweep')")
         cfg = {"workload": args.workload, "format": fmt, "calls_per_step": [c["name"] for c in calls],
-               "values": "Q4_0 codes uniform 0..15, d~U[0.005,0.02]; Q8_0 codes U[-127,127], d~U[0.001,0.01]; "
-                         "x fp16 N(0,1); seeded",
+               "values": VALUES,
                "l2": "inputs larger than L2: each table cycles >= 4x L2 bytes of weight copies",
                "timing": "CUDA graphs of back-to-back calls (programmatic dependent launch for the decode "
                          "kernels), CUDA events on the launching stream",
@@ -828,7 +839,8 @@ def run_reference(args, rank, world):
         "metric": metric_name(args.workload), "value": round(value, 5), "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "format": wl["fmt"]},
+        "config": {"workload": args.workload, "format": wl["fmt"], "calls_per_step": call_names(args.workload),
+                   "values": VALUES, "parallelism": f"replica x{world} (independent problems per GPU)"},
         "impl": "reference",
         "cpu_baseline": {"value": round(value, 5), "unit": unit, "cores": threads, "kind": "oracle",
                          "sample": sample},

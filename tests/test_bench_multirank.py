@@ -66,3 +66,5 @@ def test_reference_arm_under_torchrun():
     assert out["cpu_baseline"]["kind"] == "oracle"
     assert out["e2e"]["h2d_bytes_per_step"] == 0 and out["e2e"]["d2h_bytes_per_step"] == 0
     assert out["value"] > 0
+    # the same workload description as the GPU arm's line
+    assert out["config"]["workload"] == "q4_0_mlp_up" and out["config"]["calls_per_step"] == ["6144x2048/M1"]
